@@ -1,0 +1,262 @@
+"""CPU oracle of the sparsely-gated Mixture-of-Experts FFN layer forward pass.
+
+TEST INFRASTRUCTURE ONLY.  This module is the plain, slow, obviously correct
+statement of what the layer computes.  Only the test-suite, the package smoke
+check and the benchmark's CPU-baseline leg may import it; the product path
+never does.  It shares no code with the CUDA path.
+
+Arithmetic is fp64 (numpy), on stored inputs widened exactly.  Each function
+cites the passage it follows.  Page titles used in citations:
+
+* [LECTURE]  "Mixture of Experts: Scaling Parameters Without Scaling Compute"
+* [DAY59]    "Mixture-of-Experts -- making a model wider without using all of
+             it for every token"
+* [RATISH]   "Mixture of Experts" (learn.ratishfolio.com)
+* [GLOSSARY] "Mixture of Experts (MoE)" (inferensys glossary)
+* [AIINBED]  "Mixture of experts: big models, small bills"
+
+Readings taken where the pages are silent or garbled (the display formulas of
+the combine and of the auxiliary loss did not survive extraction):
+
+* routing decisions are taken on the fp32 router logits (softmax is
+  monotone), ties going to the lower expert index;
+* k >= 2 weights are renormalised over the selected experts; with
+  ``renormalize=False`` (Switch top-1) the weight is the router probability;
+* the capacity cap keeps, per expert, the first ``capacity`` assignments in
+  (token, slot) ascending order; a dropped assignment contributes 0 (the
+  residual add is outside the layer) and surviving weights are not
+  renormalised again;
+* f_i of the auxiliary loss counts the top-1 choice only, before any drop.
+
+Parity: the routing, capacity, auxiliary-loss and combine functions are pinned
+by the pages' worked examples, closed forms and brute force (tests).  The
+full-layer numeric output is pinned by invariants and by special cases that
+reduce to library routines, not by any printed value: the pages print no layer
+output.
+"""
+from __future__ import annotations
+
+import math
+from dataclasses import dataclass
+
+import numpy as np
+from scipy.special import erf
+
+f64 = np.float64
+
+
+def router_logits(x, W_r, logit_bias=None) -> np.ndarray:
+    """g = W_r x (+ per-expert bias), computed in fp64 and rounded to fp32.
+
+    [LECTURE] "The MoE layer", step 1 (router logits, an ``nn.Linear`` with no
+    bias in its listing).  The optional additive per-expert bias is the fixed
+    logit offset of the Switch workload (the mechanism [LECTURE] "The central
+    problem: load balancing" names for bias-based balancing).
+    x: (T, d); W_r: (E, d); returns (T, E) fp32.
+    """
+    g = np.asarray(x, f64) @ np.asarray(W_r, f64).T
+    if logit_bias is not None:
+        g = g + np.asarray(logit_bias, f64)[None, :]
+    return g.astype(np.float32)
+
+
+def softmax(logits) -> np.ndarray:
+    """p = softmax(g) over experts, fp64, max-subtracted.
+
+    [LECTURE] "The MoE layer", step 1; [AIINBED] "Experts and the router".
+    """
+    g = np.asarray(logits, f64)
+    z = np.exp(g - g.max(axis=1, keepdims=True))
+    return z / z.sum(axis=1, keepdims=True)
+
+
+def top_k(logits, k: int) -> np.ndarray:
+    """Indices of the k largest logits per token, largest first.
+
+    [LECTURE] "The MoE layer", step 2; [DAY59] "Replace one MLP with many
+    experts" (top-2 example).  Equal logits: the lower expert index comes
+    first (a stable descending sort, as the router demo of [AIINBED] does).
+    Returns (T, k) int32.
+    """
+    g = np.asarray(logits)
+    order = np.argsort(-g, axis=1, kind="stable")
+    return order[:, :k].astype(np.int32)
+
+
+def gate_weights(probs, idx, renormalize: bool) -> np.ndarray:
+    """Weights of the selected experts: p_sel / sum(p_sel), or p_sel as is.
+
+    [LECTURE] "The MoE layer" ("selected probabilities (often renormalised)");
+    [DAY59] "Replace one MLP with many experts".  Returns (T, k) fp64.
+    """
+    sel = np.take_along_axis(np.asarray(probs, f64), np.asarray(idx, np.int64), axis=1)
+    if renormalize:
+        return sel / sel.sum(axis=1, keepdims=True)
+    return sel
+
+
+def expert_capacity(capacity_factor: float, T: int, E: int) -> int:
+    """C = ceil(capacity_factor * T / E).
+
+    [LECTURE] "The central problem: load balancing" (capacity factor x tokens
+    / experts); rounding up is the reading taken (the display formula of
+    [DAY59] "Experts also have capacity limits" is lost).
+    """
+    return int(math.ceil(capacity_factor * T / E))
+
+
+def capacity_keep(idx, E: int, capacity: int | None) -> np.ndarray:
+    """Which assignments survive the per-expert capacity cap.
+
+    [LECTURE] "The central problem: load balancing" (overflow tokens are
+    dropped); [GLOSSARY] expert capacity.  Assignments are visited in token
+    order, then slot order; each expert keeps its first ``capacity``.
+    ``capacity=None`` keeps everything.  Returns (T, k) bool.
+    """
+    idx = np.asarray(idx)
+    T, k = idx.shape
+    kept = np.ones((T, k), dtype=bool)
+    if capacity is None:
+        return kept
+    taken = [0] * E
+    for t in range(T):
+        for j in range(k):
+            e = int(idx[t, j])
+            if taken[e] < capacity:
+                taken[e] += 1
+            else:
+                kept[t, j] = False
+    return kept
+
+
+def gelu(u) -> np.ndarray:
+    """Exact GELU, 0.5 u (1 + erf(u / sqrt 2)) (``nn.GELU()`` default).
+
+    [LECTURE] "The MoE layer" (each expert is Linear, GELU, Linear).
+    """
+    u = np.asarray(u, f64)
+    return 0.5 * u * (1.0 + erf(u / math.sqrt(2.0)))
+
+
+def expert_ffn(X, W1e, b1e, W2e, b2e) -> np.ndarray:
+    """One expert: Linear(d, F) + bias, GELU, Linear(F, d) + bias, in fp64.
+
+    [LECTURE] "The MoE layer" (expert definition); [DAY59] "Replace one MLP
+    with many experts" (each expert is an ordinary feed-forward network).
+    X: (n, d); W1e: (F, d); b1e: (F,); W2e: (d, F); b2e: (d,).
+    """
+    U = np.asarray(X, f64) @ np.asarray(W1e, f64).T + np.asarray(b1e, f64)[None, :]
+    H = gelu(U)
+    return H @ np.asarray(W2e, f64).T + np.asarray(b2e, f64)[None, :]
+
+
+def aux_loss(probs, idx, E: int) -> float:
+    """Switch load-balancing loss E * sum_i f_i P_i.
+
+    [LECTURE] "The central problem: load balancing" (f_i = fraction of tokens
+    routed to expert i, P_i = mean router probability) and the loss lines of
+    its listing (f from the top-1 choice, P = mean of the softmax); [DAY59]
+    "Load-balancing losses encourage better routing".
+    """
+    idx = np.asarray(idx)
+    T = idx.shape[0]
+    f = np.bincount(idx[:, 0].astype(np.int64), minlength=E).astype(f64) / T
+    P = np.asarray(probs, f64).mean(axis=0)
+    return float(E * np.sum(f * P))
+
+
+def dispatch_layout(idx, kept, E: int):
+    """Expert-contiguous order of the kept assignments.
+
+    [LECTURE] "The MoE layer", the dispatch loop of its listing: for each
+    expert in turn, the rows (tokens) routed to it, in ascending token order.
+    Returns
+      counts     (E,)   assignments routed to each expert, before the cap
+      kept_count (E,)   assignments kept per expert
+      offsets    (E+1,) start of each expert's segment (exclusive prefix sum)
+      slot_of    (T, k) segment position of each assignment, -1 if dropped
+      perm_token (n_kept,) token of each segment position
+    """
+    idx = np.asarray(idx)
+    T, k = idx.shape
+    counts = np.zeros(E, np.int64)
+    kept_count = np.zeros(E, np.int64)
+    for e in range(E):
+        counts[e] = int(np.sum(idx == e))
+        kept_count[e] = int(np.sum((idx == e) & kept))
+    offsets = np.zeros(E + 1, np.int64)
+    offsets[1:] = np.cumsum(kept_count)
+    slot_of = np.full((T, k), -1, np.int64)
+    perm_token = np.zeros(int(offsets[E]), np.int64)
+    for e in range(E):
+        pos = int(offsets[e])
+        for t in np.nonzero(((idx == e) & kept).any(axis=1))[0]:
+            j = int(np.nonzero(idx[t] == e)[0][0])
+            slot_of[t, j] = pos
+            perm_token[pos] = t
+            pos += 1
+    return counts, kept_count, offsets, slot_of, perm_token
+
+
+@dataclass
+class OracleResult:
+    logits: np.ndarray      # (T, E) fp32 routing input
+    probs: np.ndarray       # (T, E) fp64
+    idx: np.ndarray         # (T, k) int32
+    w: np.ndarray           # (T, k) fp64
+    kept: np.ndarray        # (T, k) bool
+    counts: np.ndarray      # (E,)
+    kept_count: np.ndarray  # (E,)
+    offsets: np.ndarray     # (E+1,)
+    slot_of: np.ndarray     # (T, k)
+    perm_token: np.ndarray  # (n_kept,)
+    aux: float
+    y: np.ndarray           # (len(tokens), d) fp64
+    tokens: np.ndarray      # rows of the layer output held in y
+
+
+def moe_forward(x, W_r, W1, b1, W2, b2, k: int, renormalize: bool = True,
+                capacity: int | None = None, logit_bias=None, logits=None,
+                tokens=None, layout: bool = True) -> OracleResult:
+    """The MoE layer forward pass, looping over experts.
+
+    [LECTURE] "The MoE layer": router logits and softmax, top-k selection,
+    output = sum over the selected experts of weight x expert output; its
+    listing's loop dispatches each expert's tokens and accumulates the
+    weighted outputs; "The central problem: load balancing" gives the
+    capacity drop and the auxiliary loss.  [RATISH] "How does MoE work?"
+    (router, experts, combine).
+
+    ``logits`` (T, E fp32) replaces the router GEMM when given (routing from
+    identical logits).  ``tokens`` restricts the expert computation (not the
+    routing, cap or loss, which always cover the whole batch) to a subset of
+    token rows; ``y`` then holds those rows in that order.
+    """
+    x = np.asarray(x)
+    T, d = x.shape
+    E = np.asarray(W_r).shape[0]
+    if logits is None:
+        logits = router_logits(x, W_r, logit_bias)
+    logits = np.asarray(logits, np.float32)
+    probs = softmax(logits)
+    idx = top_k(logits, k)
+    w = gate_weights(probs, idx, renormalize)
+    kept = capacity_keep(idx, E, capacity)
+    if layout:
+        counts, kept_count, offsets, slot_of, perm_token = dispatch_layout(idx, kept, E)
+    else:
+        counts = kept_count = offsets = slot_of = perm_token = None
+    tokens = np.arange(T) if tokens is None else np.asarray(tokens, np.int64)
+    y = np.zeros((len(tokens), d), f64)
+    sub_idx, sub_kept, sub_w = idx[tokens], kept[tokens], w[tokens]
+    for e in range(E):
+        sel = (sub_idx == e) & sub_kept                 # (n, k)
+        rows = np.nonzero(sel.any(axis=1))[0]
+        if rows.size == 0:
+            continue
+        out = expert_ffn(x[tokens[rows]], W1[e], b1[e], W2[e], b2[e])
+        we = (sub_w * sel)[rows].sum(axis=1)
+        y[rows] += we[:, None] * out
+    aux = aux_loss(probs, idx, E)
+    return OracleResult(logits, probs, idx, w, kept, counts, kept_count, offsets, slot_of,
+                        perm_token, aux, y, tokens)

@@ -1,0 +1,404 @@
+"""Pins of the CPU oracle against what the pages and the mathematics fix.
+
+Each test names the passage or the closed form it checks.  None of them
+re-types an oracle formula: expected values come from the pages' worked
+examples, from exact special cases, from brute force with plain loops, or
+from library routines (torch on CPU, fp64).
+"""
+import math
+import random
+
+import numpy as np
+import pytest
+import torch
+import torch.nn.functional as TF
+
+from conftest import read_golden
+from oracle import moe_oracle as O
+from sparse_mixture_experts_71_b300.inputs import SWITCH
+
+rng = np.random.default_rng(1234)
+
+
+def _rand_layer(T, d, F, E, seed=0):
+    g = np.random.default_rng(seed)
+    return dict(
+        x=g.standard_normal((T, d)),
+        W_r=g.standard_normal((E, d)) * 0.5,
+        W1=g.standard_normal((E, F, d)) / math.sqrt(d),
+        b1=g.uniform(-0.3, 0.3, (E, F)),
+        W2=g.standard_normal((E, d, F)) / math.sqrt(F),
+        b2=g.uniform(-0.3, 0.3, (E, d)),
+    )
+
+
+# ---------------------------------------------------------------- routing pins
+
+def test_day59_worked_top2_example():
+    """day-59 "Replace one MLP with many experts": probabilities of Experts
+    1..8 -> the token goes to Experts 2 and 4."""
+    gold = read_golden("day59_top2_example.txt")
+    p = np.array([float(v) for v in gold["probs"]])
+    logits = np.log(p).astype(np.float32)[None, :]
+    idx = O.top_k(logits, 2)
+    assert [int(i) + 1 for i in idx[0]] == [int(v) for v in gold["top2_1based"]]
+    # softmax of ln p gives p back (the printed probabilities sum to 1)
+    probs = O.softmax(logits)
+    np.testing.assert_allclose(probs[0], p, rtol=1e-6)
+    # renormalised over the two chosen experts: 0.51/0.82 and 0.31/0.82
+    w = O.gate_weights(probs, idx, True)
+    np.testing.assert_allclose(w[0], [0.51 / 0.82, 0.31 / 0.82], rtol=1e-6)
+    # not renormalised: the router probabilities themselves
+    np.testing.assert_allclose(O.gate_weights(probs, idx, False)[0], [0.51, 0.31], rtol=1e-6)
+
+
+def test_ratish_router_table():
+    """ratishfolio "How does MoE work?" Part 1: scores A .10 B .75 C .15 ->
+    top-1 B; top-2 B and C."""
+    gold = read_golden("ratish_router_table.txt")
+    s = np.array([float(v) for v in gold["scores"]])
+    names = "ABC"
+    logits = np.log(s).astype(np.float32)[None, :]
+    assert [names[i] for i in O.top_k(logits, 1)[0]] == gold["top1"]
+    assert [names[i] for i in O.top_k(logits, 2)[0]] == gold["top2"]
+    w = O.gate_weights(O.softmax(logits), O.top_k(logits, 2), True)
+    np.testing.assert_allclose(w[0], [0.75 / 0.90, 0.15 / 0.90], rtol=1e-6)
+
+
+def test_aiinbed_router_demo():
+    """aiinbed "Experts and the router": Gaussian router scores (stdlib RNG,
+    seed 7, 8 experts, 4 tokens), softmax, top-2, shares renormalised over the
+    two.  The expected picks are computed here with plain Python floats by the
+    procedure the page states; the oracle routes the same scores as fp32
+    logits and must agree on picks and rounded percentages."""
+    random.seed(7)
+    E, k = 8, 2
+    for _ in range(4):
+        scores = [random.gauss(0, 1) for _ in range(E)]
+        ex = [math.exp(v) for v in scores]
+        tot = sum(ex)
+        probs = [v / tot for v in ex]
+        best = sorted(range(E), key=lambda i: probs[i], reverse=True)[:k]
+        share = sum(probs[i] for i in best)
+        want = [(i, round(100 * probs[i] / share)) for i in best]
+        logits = np.array(scores, np.float32)[None, :]
+        idx = O.top_k(logits, k)[0]
+        w = O.gate_weights(O.softmax(logits), idx[None, :], True)[0]
+        got = [(int(i), round(100 * float(v))) for i, v in zip(idx, w)]
+        assert got == want
+
+
+def test_top_k_ties_go_to_lower_index():
+    """Equal logits: lower expert index first (stable descending order)."""
+    g = np.array([[1.0, 3.0, 3.0, 0.0, 3.0]], np.float32)
+    assert O.top_k(g, 2)[0].tolist() == [1, 2]
+    assert O.top_k(g, 3)[0].tolist() == [1, 2, 4]
+    z = np.zeros((1, 6), np.float32)
+    assert O.top_k(z, 4)[0].tolist() == [0, 1, 2, 3]
+
+
+def test_top_k_brute_force():
+    """Top-k against an explicit selection loop on random fp32 logits."""
+    g = rng.standard_normal((50, 7)).astype(np.float32)
+    g[:, 3] = g[:, 5]  # force some ties
+    for k in (1, 2, 3, 7):
+        idx = O.top_k(g, k)
+        for t in range(g.shape[0]):
+            left = list(range(g.shape[1]))
+            want = []
+            for _ in range(k):
+                b = left[0]
+                for e in left:
+                    if g[t, e] > g[t, b]:
+                        b = e
+                want.append(b)
+                left.remove(b)
+            assert idx[t].tolist() == want
+
+
+def test_renormalised_weights_sum_to_one():
+    """Renormalised weights of every token sum to 1 (fp64 round-off)."""
+    g = (rng.standard_normal((200, 16)) * 3).astype(np.float32)
+    for k in (2, 4, 16):
+        w = O.gate_weights(O.softmax(g), O.top_k(g, k), True)
+        assert np.max(np.abs(w.sum(axis=1) - 1.0)) <= 4e-16
+        assert np.all(w > 0)
+
+
+def test_softmax_matches_torch():
+    g = (rng.standard_normal((40, 64)) * 5).astype(np.float32)
+    want = torch.softmax(torch.from_numpy(g).double(), dim=-1).numpy()
+    np.testing.assert_allclose(O.softmax(g), want, rtol=1e-13, atol=0)
+
+
+# ---------------------------------------------------------- auxiliary loss pins
+
+@pytest.mark.parametrize("E,k", [(1, 1), (4, 2), (8, 2), (64, 1), (8, 8)])
+def test_aux_loss_uniform_routing_is_one(E, k):
+    """All logits equal -> P_i = 1/E, so E * sum f_i / E = 1 exactly, whatever
+    the tie-break ("The central problem: load balancing")."""
+    g = np.zeros((96, E), np.float32)
+    p = O.softmax(g)
+    assert abs(O.aux_loss(p, O.top_k(g, k), E) - 1.0) <= 1e-14
+
+
+def test_aux_loss_balanced_top1_is_one():
+    """Top-1 counts exactly balanced (f_i = 1/E) -> aux = sum_i P_i = 1."""
+    E, T = 8, 256
+    g = rng.standard_normal((T, E)).astype(np.float32)
+    g[np.arange(T), np.arange(T) % E] += 20.0
+    p = O.softmax(g)
+    idx = O.top_k(g, 2)
+    assert np.all(np.bincount(idx[:, 0], minlength=E) == T // E)
+    assert abs(O.aux_loss(p, idx, E) - 1.0) <= 1e-13
+
+
+def test_aux_loss_day59_imbalance():
+    """day-59 "The router can create traffic jams": 8 experts, 8000 tokens,
+    loads 4700/800/.../200.  With one-hot routing probabilities P_i = f_i, so
+    aux = 8 * sum f_i^2 = 2.995 (derived from the printed loads)."""
+    gold = read_golden("day59_imbalance_loads.txt")
+    E, T = int(gold["experts"][0]), int(gold["tokens"][0])
+    loads = [int(v) for v in gold["loads"]]
+    assert sum(loads) == T
+    top1 = np.repeat(np.arange(E), loads)
+    np.random.default_rng(5).shuffle(top1)
+    g = np.zeros((T, E), np.float32)
+    g[np.arange(T), top1] = 80.0
+    p = O.softmax(g)
+    idx = O.top_k(g, 2)
+    assert np.array_equal(idx[:, 0], top1)
+    assert abs(O.aux_loss(p, idx, E) - 2.995) <= 1e-12
+
+
+def test_aux_loss_counts_top1_slot_only():
+    """f_i counts the first (highest) choice only: moving a token's second
+    choice does not change aux."""
+    E = 4
+    g = np.array([[4.0, 3.0, 0.0, 0.0], [4.0, 0.0, 3.0, 0.0]], np.float32)
+    p = O.softmax(g)
+    idx = O.top_k(g, 2)
+    # f = (1, 0, 0, 0): aux = E * P_0
+    assert abs(O.aux_loss(p, idx, E) - E * p[:, 0].mean()) <= 1e-15
+
+
+# ------------------------------------------------------------- capacity pins
+
+def test_switch_capacity_value():
+    """C = ceil(1.25 * T / E) for the Switch workload: 1.25 * 32768 / 64 = 640."""
+    assert O.expert_capacity(1.25, 32768, 64) == 640 == SWITCH.capacity
+    assert O.expert_capacity(1.0, 10, 3) == 4
+
+
+def test_capacity_day59_loads():
+    """day-59 loads 4700/800/.../200 with C = ceil(1.25 * 8000 / 8) = 1250:
+    expert 0 keeps its first 1250 tokens in token order, every other expert
+    keeps all of its tokens; the 3450 later tokens of expert 0 are dropped."""
+    gold = read_golden("day59_imbalance_loads.txt")
+    E, T = int(gold["experts"][0]), int(gold["tokens"][0])
+    loads = [int(v) for v in gold["loads"]]
+    C = O.expert_capacity(1.25, T, E)
+    assert C == 1250
+    top1 = np.repeat(np.arange(E), loads)
+    np.random.default_rng(9).shuffle(top1)
+    kept = O.capacity_keep(top1[:, None], E, C)[:, 0]
+    for e in range(E):
+        toks = np.nonzero(top1 == e)[0]
+        n = min(loads[e], C)
+        assert kept[toks[:n]].all() and not kept[toks[n:]].any()
+    assert int((~kept).sum()) == 3450
+
+
+def test_capacity_slot_order_for_k2():
+    """Cap 1: in (token, slot) order the first assignment to an expert wins."""
+    idx = np.array([[1, 0], [0, 1], [2, 1]])
+    kept = O.capacity_keep(idx, 3, 1)
+    assert kept.tolist() == [[True, True], [False, False], [True, False]]
+
+
+def test_dispatch_layout_brute_force():
+    """Segments are expert-major and token-ascending inside an expert; every
+    kept assignment has one slot, every dropped one has -1."""
+    T, k, E = 37, 2, 5
+    g = rng.standard_normal((T, E)).astype(np.float32)
+    idx = O.top_k(g, k)
+    kept = O.capacity_keep(idx, E, 9)
+    counts, kc, off, slot_of, perm = O.dispatch_layout(idx, kept, E)
+    want_perm = []
+    for e in range(E):
+        assert counts[e] == sum(int(idx[t, j] == e) for t in range(T) for j in range(k))
+        for t in range(T):
+            for j in range(k):
+                if idx[t, j] == e and kept[t, j]:
+                    assert slot_of[t, j] == off[0] + len(want_perm)
+                    want_perm.append(t)
+                elif not kept[t, j]:
+                    assert slot_of[t, j] == -1
+        assert off[e + 1] == len(want_perm)
+    assert perm.tolist() == want_perm
+
+
+# ------------------------------------------------------------------ GELU pins
+
+def test_gelu_values():
+    """GELU(0) = 0; GELU(+-1) = +-Phi(+-1); matches torch's exact GELU."""
+    assert O.gelu(np.array([0.0]))[0] == 0.0
+    assert abs(O.gelu(np.array([1.0]))[0] - 0.8413447460685429) <= 1e-15
+    assert abs(O.gelu(np.array([-1.0]))[0] + 0.15865525393145707) <= 1e-15
+    u = np.linspace(-8, 8, 1001)
+    want = TF.gelu(torch.from_numpy(u)).numpy()
+    np.testing.assert_allclose(O.gelu(u), want, rtol=1e-14, atol=1e-15)
+
+
+# ------------------------------------------------------- whole-layer pins
+
+def _brute_force_dense(L, k, renormalize, capacity):
+    """Run every expert on every token with plain loops, then mask by the
+    gate weights (0 off the top-k and for dropped assignments)."""
+    x, W_r, W1, b1, W2, b2 = (L[n] for n in ("x", "W_r", "W1", "b1", "W2", "b2"))
+    T, d = x.shape
+    E, F, _ = W1.shape
+    logits = np.zeros((T, E), np.float32)
+    for t in range(T):
+        for e in range(E):
+            logits[t, e] = np.float32(sum(float(W_r[e, j]) * float(x[t, j]) for j in range(d)))
+    y = np.zeros((T, d))
+    taken = [0] * E
+    for t in range(T):
+        m = max(logits[t])
+        ex = [math.exp(float(v) - float(m)) for v in logits[t]]
+        s = sum(ex)
+        p = [v / s for v in ex]
+        order = sorted(range(E), key=lambda e: (-float(logits[t, e]), e))[:k]
+        share = sum(p[e] for e in order) if renormalize else 1.0
+        gate = [0.0] * E
+        for e in order:
+            if capacity is None or taken[e] < capacity:
+                taken[e] += 1
+                gate[e] = p[e] / share
+        for e in range(E):
+            h = [0.0] * F
+            for f in range(F):
+                u = b1[e, f] + sum(W1[e, f, j] * x[t, j] for j in range(d))
+                h[f] = 0.5 * u * (1.0 + math.erf(u / math.sqrt(2.0)))
+            for i in range(d):
+                o = b2[e, i] + sum(W2[e, i, f] * h[f] for f in range(F))
+                y[t, i] += gate[e] * o
+    return logits, y
+
+
+@pytest.mark.parametrize("k,renorm,cap", [(1, False, None), (2, True, None), (2, True, 3),
+                                          (3, True, 2), (1, False, 0)])
+def test_forward_equals_dense_masked_brute_force(k, renorm, cap):
+    """Loop-over-experts forward == every expert on every token, masked."""
+    L = _rand_layer(T=9, d=5, F=6, E=4, seed=k * 10 + (cap or 0))
+    logits, want = _brute_force_dense(L, k, renorm, cap)
+    r = O.moe_forward(**L, k=k, renormalize=renorm, capacity=cap)
+    assert np.array_equal(r.logits, logits)
+    np.testing.assert_allclose(r.y, want, rtol=1e-12, atol=1e-12)
+
+
+def test_single_expert_is_dense_ffn():
+    """E = 1, k = 1, renormalised -> the plain Linear-GELU-Linear FFN
+    (torch.nn.functional on CPU, fp64)."""
+    L = _rand_layer(T=33, d=16, F=40, E=1, seed=3)
+    r = O.moe_forward(**L, k=1, renormalize=True)
+    t = {n: torch.from_numpy(v) for n, v in L.items()}
+    want = TF.linear(TF.gelu(TF.linear(t["x"], t["W1"][0], t["b1"][0])), t["W2"][0], t["b2"][0])
+    np.testing.assert_allclose(r.y, want.numpy(), rtol=1e-12, atol=1e-12)
+    assert abs(r.aux - 1.0) <= 1e-15
+
+
+def test_k_equals_E_is_soft_mixture():
+    """k = E, renormalised -> y = sum_e p_e f_e(x) (torch, fp64)."""
+    L = _rand_layer(T=21, d=12, F=20, E=5, seed=4)
+    r = O.moe_forward(**L, k=5, renormalize=True)
+    t = {n: torch.from_numpy(v) for n, v in L.items()}
+    logits = torch.from_numpy(r.logits).double()
+    p = torch.softmax(logits, -1)
+    want = torch.zeros_like(t["x"])
+    for e in range(5):
+        fe = TF.linear(TF.gelu(TF.linear(t["x"], t["W1"][e], t["b1"][e])), t["W2"][e], t["b2"][e])
+        want += p[:, e:e + 1] * fe
+    np.testing.assert_allclose(r.y, want.numpy(), rtol=1e-12, atol=1e-12)
+    # and the fp32 logits are the fp64 product rounded once
+    want_g = (t["x"] @ t["W_r"].T).float().numpy()
+    assert np.array_equal(r.logits, want_g)
+
+
+def test_capacity_extremes():
+    """C >= T -> same as no cap; C = 0 -> every assignment dropped, y = 0."""
+    L = _rand_layer(T=30, d=8, F=16, E=4, seed=5)
+    a = O.moe_forward(**L, k=2)
+    b = O.moe_forward(**L, k=2, capacity=30)
+    assert np.array_equal(a.y, b.y) and np.array_equal(a.slot_of, b.slot_of)
+    z = O.moe_forward(**L, k=2, capacity=0)
+    assert not z.y.any() and np.all(z.slot_of == -1) and z.offsets[-1] == 0
+    assert z.aux == a.aux  # the loss is taken before any drop
+
+
+def test_token_permutation():
+    """No cap: permuting tokens permutes y and keeps aux.  With a cap the
+    drop is in token order, so a permutation changes which token is dropped."""
+    L = _rand_layer(T=25, d=8, F=12, E=3, seed=6)
+    perm = np.random.default_rng(2).permutation(25)
+    a = O.moe_forward(**L, k=2)
+    Lp = dict(L, x=L["x"][perm])
+    b = O.moe_forward(**Lp, k=2)
+    np.testing.assert_allclose(b.y, a.y[perm], rtol=1e-12, atol=1e-13)
+    assert abs(a.aux - b.aux) <= 1e-13
+    ca = O.moe_forward(**L, k=1, capacity=4)
+    cb = O.moe_forward(**Lp, k=1, capacity=4)
+    assert not np.array_equal(ca.kept[perm], cb.kept)
+
+
+def test_token_subset_matches_full():
+    """Computing only some token rows gives those rows of the full output."""
+    L = _rand_layer(T=40, d=8, F=12, E=4, seed=7)
+    full = O.moe_forward(**L, k=2, capacity=12)
+    sub = np.array([39, 0, 17, 5])
+    part = O.moe_forward(**L, k=2, capacity=12, tokens=sub)
+    np.testing.assert_allclose(part.y, full.y[sub], rtol=1e-12, atol=1e-13)
+
+
+# ------------------------------------------- the pins catch planted mistakes
+
+def _planted(monkeypatch, name, fn):
+    monkeypatch.setattr(O, name, fn)
+
+
+def test_planted_mistakes_are_caught(monkeypatch):
+    """Plausible oracle mistakes, planted on the CPU, each fail a pin above."""
+    good_topk, good_gate, good_aux = O.top_k, O.gate_weights, O.aux_loss
+
+    # ties to the higher index
+    _planted(monkeypatch, "top_k", lambda g, k: np.argsort(-np.asarray(g)[:, ::-1], axis=1,
+                                                            kind="stable")[:, :k] * -1
+             + np.asarray(g).shape[1] - 1)
+    with pytest.raises(AssertionError):
+        test_top_k_ties_go_to_lower_index()
+    monkeypatch.setattr(O, "top_k", good_topk)
+
+    # weights not renormalised
+    _planted(monkeypatch, "gate_weights", lambda p, i, r: good_gate(p, i, False))
+    with pytest.raises(AssertionError):
+        test_day59_worked_top2_example()
+    monkeypatch.setattr(O, "gate_weights", good_gate)
+
+    # aux loss with f over all k slots instead of the top-1 choice
+    def aux_all_slots(p, idx, E):
+        idx = np.asarray(idx)
+        f = np.bincount(idx.ravel(), minlength=E) / idx.size
+        return float(E * np.sum(f * np.asarray(p).mean(0)))
+    _planted(monkeypatch, "aux_loss", aux_all_slots)
+    with pytest.raises(AssertionError):
+        test_aux_loss_counts_top1_slot_only()
+    monkeypatch.setattr(O, "aux_loss", good_aux)
+
+    # tanh GELU instead of the exact one
+    good_gelu = O.gelu
+    _planted(monkeypatch, "gelu", lambda u: 0.5 * np.asarray(u) * (1 + np.tanh(
+        math.sqrt(2 / math.pi) * (np.asarray(u) + 0.044715 * np.asarray(u) ** 3))))
+    with pytest.raises(AssertionError):
+        test_single_expert_is_dense_ffn()
+    monkeypatch.setattr(O, "gelu", good_gelu)
