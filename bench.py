@@ -1,0 +1,387 @@
+#!/usr/bin/env python3
+"""Throughput of the MoE-layer forward pass on B300 (libmoe, sm_103a).
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+                    [--workload NAME] [--no-cpu-baseline]
+
+A step is one forward pass of the layer (route, dispatch, expert FFN,
+combine) over one batch of seeded synthetic inputs of the named workload
+(default: bf16, T=4096 tokens, d=1024, d_ff=4096, E=8, top-2).  The inputs
+and the expert weights are resident in HBM when the timed region starts; L2
+is flushed (a 256 MiB write) before every timed step and the flush is not
+timed.  Rank 0 prints one JSON line.
+
+Under torchrun (N > 1) every rank runs an independent replica of the layer
+on its own GPU (the layer has no cross-GPU step); the line reports the tokens
+of all ranks over the slowest rank's time.
+
+--impl reference times the CPU oracle (fp64, numpy) on the host cores on a
+bounded token sample of the same workload per step.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import math
+import os
+import statistics
+import sys
+import threading
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+from sparse_mixture_experts_71_b300 import inputs as I  # noqa: E402
+
+DEFAULT_WORKLOAD = I.MEDIUM.name
+PEAKS_FALLBACK = {"hbm_gbs": 6400.0, "bf16_tflops": 1800.0, "bf16_tflops_sustained": 1400.0}
+METRIC = "MoE-layer fwd tokens/s and achieved TFLOP/s (or HBM GB/s) vs B300 roofline"
+
+
+def peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as f:
+            d = json.load(f)
+        return d, "measured"
+    return dict(PEAKS_FALLBACK), "fallback"
+
+
+def algorithmic_work(wl, kept_per_expert):
+    """FLOPs and minimum HBM bytes of one forward pass.
+
+    FLOPs: router 2*T*d*E plus 4*d*d_ff per kept assignment (two GEMMs).
+    Bytes: x, y, W_r, and the weights and biases of every expert that kept at
+    least one assignment.
+    """
+    es = 4 if wl.dtype == "f32" else 2
+    kept = int(sum(kept_per_expert))
+    used = int(sum(1 for c in kept_per_expert if c > 0))
+    flops_router = 2.0 * wl.T * wl.d * wl.E
+    flops_ffn = 4.0 * kept * wl.d * wl.F
+    w_bytes = used * (2 * wl.d * wl.F + wl.F + wl.d) * es
+    io_bytes = 2 * wl.T * wl.d * es + wl.E * wl.d * 4
+    return dict(flops=flops_router + flops_ffn, flops_ffn=flops_ffn, bytes=w_bytes + io_bytes,
+                ffn_bytes=w_bytes + kept * wl.d * (es + 4), kept=kept, experts_used=used)
+
+
+class ClockSampler:
+    """Samples SM clock and throttle reasons through NVML while running."""
+
+    REASONS = {  # NVML clocks-event-reason bits
+        0x1: "gpu_idle", 0x2: "applications_clocks_setting", 0x4: "sw_power_cap",
+        0x8: "hw_slowdown", 0x10: "sync_boost", 0x20: "sw_thermal_slowdown",
+        0x40: "hw_thermal_slowdown", 0x80: "hw_power_brake_slowdown",
+        0x100: "display_clock_setting"}
+
+    def __init__(self, index: int, period_s: float = 0.01):
+        self.index, self.period = index, period_s
+        self.samples, self.reasons = [], set()
+        self.max_mhz = None
+        self._stop = threading.Event()
+        self._t = None
+        self.ok = False
+        try:
+            import pynvml
+            pynvml.nvmlInit()
+            self._nv = pynvml
+            self._h = pynvml.nvmlDeviceGetHandleByIndex(index)
+            self.max_mhz = pynvml.nvmlDeviceGetMaxClockInfo(self._h, pynvml.NVML_CLOCK_SM)
+            self.ok = True
+        except Exception:
+            self.ok = False
+
+    def _run(self):
+        nv = self._nv
+        while not self._stop.is_set():
+            try:
+                self.samples.append(nv.nvmlDeviceGetClockInfo(self._h, nv.NVML_CLOCK_SM))
+                r = nv.nvmlDeviceGetCurrentClocksEventReasons(self._h)
+                for bit, name in self.REASONS.items():
+                    if r & bit:
+                        self.reasons.add(name)
+            except Exception:
+                pass
+            time.sleep(self.period)
+
+    def __enter__(self):
+        if self.ok:
+            self._t = threading.Thread(target=self._run, daemon=True)
+            self._t.start()
+        return self
+
+    def __exit__(self, *a):
+        self._stop.set()
+        if self._t is not None:
+            self._t.join()
+
+    def summary(self):
+        if not self.samples:
+            return {"sm_mhz": None, "sm_max_mhz": self.max_mhz, "reasons": sorted(self.reasons),
+                    "samples": 0}
+        return {"sm_mhz": statistics.median(self.samples), "sm_max_mhz": self.max_mhz,
+                "reasons": sorted(self.reasons - {"gpu_idle"}), "samples": len(self.samples)}
+
+
+def dist_setup():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return world, rank, local
+
+
+def cpu_oracle_rate(wl, inp, budget_s: float, min_tokens: int = 64):
+    """Tokens/s of the oracle on a token sample sized to the time budget.
+
+    The sample is the first n tokens of the batch taken as a batch of its own
+    (routing, experts, combine and loss all run on it)."""
+    from oracle import moe_oracle as O
+    from threadpoolctl import threadpool_info
+    x = inp.as_f32("x")
+    W1, b1, W2, b2 = (inp.as_f32(n) for n in ("W1", "b1", "W2", "b2"))
+
+    def run(n):
+        t0 = time.perf_counter()
+        O.moe_forward(x[:n], inp.W_r, W1, b1, W2, b2, k=wl.k, renormalize=wl.renormalize,
+                      capacity=wl.capacity, logit_bias=inp.logit_bias, layout=False)
+        return time.perf_counter() - t0
+
+    n0 = min(wl.T, 256)
+    t0 = run(n0)
+    n = int(min(wl.T, max(min_tokens, n0 * budget_s / max(t0, 1e-6))))
+    t = run(n) if n != n0 else t0
+    threads = max([p.get("num_threads", 1) for p in threadpool_info()] + [1])
+    return n / t, n, t, threads
+
+
+def bench_reference(args, wl):
+    world, rank, _ = dist_setup()
+    if rank != 0:
+        return 0
+    inp = I.make_inputs(wl, seed=0)
+    per_step = max(0.5, 150.0 / max(1, args.steps + args.warmup))
+    from oracle import moe_oracle as O
+    from threadpoolctl import threadpool_info
+    x = inp.as_f32("x")
+    W1, b1, W2, b2 = (inp.as_f32(n) for n in ("W1", "b1", "W2", "b2"))
+    # size the per-step sample from one probe step
+    rate, n, _, threads = cpu_oracle_rate(wl, inp, per_step)
+    n = max(1, min(wl.T, int(rate * per_step)))
+
+    def step():
+        O.moe_forward(x[:n], inp.W_r, W1, b1, W2, b2, k=wl.k, renormalize=wl.renormalize,
+                      capacity=wl.capacity, logit_bias=inp.logit_bias, layout=False)
+
+    for _ in range(args.warmup):
+        step()
+    times = []
+    for _ in range(args.steps):
+        t0 = time.perf_counter()
+        step()
+        times.append(time.perf_counter() - t0)
+    threads = max([p.get("num_threads", 1) for p in threadpool_info()] + [threads])
+    total = sum(times)
+    value = n * args.steps / total
+    sample = f"first {n} of {wl.T} tokens as a batch of their own, per step"
+    line = {"metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * total / args.steps,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+            "data": "synthetic", "impl": "reference",
+            "config": {"workload": wl.name, "T": wl.T, "d": wl.d, "d_ff": wl.F, "E": wl.E,
+                       "k": wl.k, "capacity": wl.capacity},
+            "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": threads,
+                             "kind": "oracle", "sample": sample},
+            "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0,
+                    "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+def bench_ours(args, wl):
+    import torch
+    import torch.distributed as dist
+    from sparse_mixture_experts_71_b300 import binding as B
+    from sparse_mixture_experts_71_b300.layer import MoELayer, device_inputs
+
+    world, rank, local = dist_setup()
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    if world > 1:
+        dist.init_process_group("nccl", device_id=dev)
+
+    inp = I.make_inputs(wl, seed=0)
+    D = device_inputs(inp, dev)
+    layer = MoELayer(D["W_r"], D["W1"], D["b1"], D["W2"], D["b2"], k=wl.k, capacity=wl.capacity,
+                     renormalize=wl.renormalize, logit_bias=D["logit_bias"])
+    cfg = layer.config(wl.T)
+    ws = layer.workspace(wl.T)
+    stream = torch.cuda.current_stream(dev)
+    T, k, E, d = wl.T, wl.k, wl.E, wl.d
+    n = T * k
+    i32, f32 = torch.int32, torch.float32
+    dt = D["x"].dtype
+    buf = dict(idx=torch.empty((T, k), dtype=i32, device=dev),
+               w=torch.empty((T, k), dtype=f32, device=dev),
+               counts=torch.empty(E, dtype=i32, device=dev),
+               aux=torch.empty(1, dtype=f32, device=dev),
+               offsets=torch.empty(E + 1, dtype=i32, device=dev),
+               slot_of=torch.empty((T, k), dtype=i32, device=dev),
+               perm_token=torch.empty(n, dtype=i32, device=dev),
+               perm_w=torch.empty(n, dtype=f32, device=dev),
+               x_perm=torch.empty((n, d), dtype=dt, device=dev),
+               y_perm=torch.empty((n, d), dtype=f32, device=dev),
+               y=torch.empty((T, d), dtype=dt, device=dev))
+    flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
+
+    def staged_step(ev=None):
+        b = buf
+        if ev is not None:
+            ev[0].record(stream)
+        B.route(cfg, D["x"], D["W_r"], b["idx"], b["w"], ws, logit_bias=D["logit_bias"],
+                expert_counts=b["counts"], aux_out=b["aux"], stream=stream)
+        B.dispatch(cfg, D["x"], b["idx"], b["offsets"], b["slot_of"], b["perm_token"],
+                   b["x_perm"], ws, topk_w=b["w"], perm_w=b["perm_w"], stream=stream)
+        if ev is not None:
+            ev[1].record(stream)
+        B.expert_ffn(cfg, b["x_perm"], b["offsets"], D["W1"], D["b1"], D["W2"], D["b2"],
+                     b["y_perm"], ws, perm_w=b["perm_w"], stream=stream)
+        if ev is not None:
+            ev[2].record(stream)
+        B.combine(cfg, b["y_perm"], b["slot_of"], b["y"], stream=stream)
+        if ev is not None:
+            ev[3].record(stream)
+
+    for _ in range(max(args.warmup, 3)):
+        flush.fill_(1)
+        staged_step()
+    torch.cuda.synchronize(dev)
+    kept = [int(v) for v in torch.diff(buf["offsets"]).cpu().tolist()]
+    work = algorithmic_work(wl, kept)
+
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(args.steps)]
+    launches0 = B.launch_count()
+    sampler = ClockSampler(local)
+    if world > 1:
+        dist.barrier()
+    torch.cuda.synchronize(dev)
+    with sampler:
+        for s in range(args.steps):
+            flush.fill_(s & 0xFF)
+            staged_step(evs[s])
+        torch.cuda.synchronize(dev)
+    if world > 1:
+        dist.barrier()
+    launches = B.launch_count() - launches0
+    step_ms = [e[0].elapsed_time(e[3]) for e in evs]
+    ffn_ms = [e[1].elapsed_time(e[2]) for e in evs]
+    route_ms = [e[0].elapsed_time(e[1]) for e in evs]
+    comb_ms = [e[2].elapsed_time(e[3]) for e in evs]
+    total_ms = sum(step_ms)
+    if world > 1:
+        t = torch.tensor([total_ms], dtype=torch.float64, device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        total_ms = float(t.item())
+    ms_per_step = total_ms / args.steps
+    value = world * T * args.steps / (total_ms * 1e-3)
+
+    # end to end through the public layer API with host buffers
+    x_host = torch.from_numpy(inp.x.view(np.int16) if inp.x.dtype == np.uint16 else inp.x)
+    x_host = (x_host.view(torch.bfloat16) if inp.x.dtype == np.uint16 else x_host).pin_memory()
+    y_host = torch.empty((T, d), dtype=dt).pin_memory()
+    aux_host = torch.empty(1, dtype=f32).pin_memory()
+    x_dev = torch.empty_like(D["x"])
+    y_dev = torch.empty_like(D["x"])
+    aux_dev = torch.empty(1, dtype=f32, device=dev)
+
+    def e2e_step():
+        x_dev.copy_(x_host, non_blocking=True)
+        layer.forward(x_dev, y=y_dev, aux=aux_dev, stream=stream)
+        y_host.copy_(y_dev, non_blocking=True)
+        aux_host.copy_(aux_dev, non_blocking=True)
+
+    for _ in range(3):
+        e2e_step()
+    torch.cuda.synchronize(dev)
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e2e_ms = 0.0
+    for s in range(args.steps):
+        flush.fill_(s & 0xFF)
+        e0.record(stream)
+        e2e_step()
+        e1.record(stream)
+        e1.synchronize()
+        e2e_ms += e0.elapsed_time(e1)
+    if world > 1:
+        t = torch.tensor([e2e_ms], dtype=torch.float64, device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        e2e_ms = float(t.item())
+    e2e_value = world * T * args.steps / (e2e_ms * 1e-3)
+    es = 2 if dt == torch.bfloat16 else 4
+
+    pk, pk_kind = peaks()
+    ffn_s = statistics.mean(ffn_ms) * 1e-3
+    if wl.dtype == "bf16":
+        achieved = work["flops_ffn"] / ffn_s / 1e12
+        peak = pk["bf16_tflops"]
+        roof = {"bound": "tensor", "unit": "TFLOP/s"}
+    else:
+        achieved = work["ffn_bytes"] / ffn_s / 1e9
+        peak = pk["hbm_gbs"]
+        roof = {"bound": "hbm", "unit": "GB/s"}
+    roof.update({"kernel": "expert FFN (grouped GEMM1 + GEMM2)", "achieved": achieved,
+                 "peak": peak, "peak_source": pk_kind, "frac": achieved / peak,
+                 "traffic": args.traffic})
+
+    line = {"metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_per_step,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+            "dtype": "bf16" if wl.dtype == "bf16" else "f32", "data": "synthetic",
+            "config": {"workload": wl.name, "T": T, "d": d, "d_ff": wl.F, "E": E, "k": k,
+                       "capacity": wl.capacity, "parallelism": f"replicas{world}",
+                       "l2": "flushed before every timed step (256 MiB write, untimed)"},
+            "tflops": work["flops"] / (ms_per_step * 1e-3) / 1e12 * world,
+            "hbm_gbs_algorithmic": work["bytes"] / (ms_per_step * 1e-3) / 1e9 * world,
+            "stages_ms": {"route+dispatch": statistics.mean(route_ms),
+                          "expert_ffn": statistics.mean(ffn_ms),
+                          "combine": statistics.mean(comb_ms)},
+            "kept_assignments": work["kept"],
+            "roofline": roof,
+            "e2e": {"value": e2e_value, "unit": "tokens/s",
+                    "h2d_bytes_per_step": T * d * es, "d2h_bytes_per_step": T * d * es + 4},
+            "gpu_launches": launches,
+            "clocks": sampler.summary()}
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        rate, n_tok, t, threads = cpu_oracle_rate(wl, inp, budget_s=12.0)
+        line["cpu_baseline"] = {"value": rate, "unit": "tokens/s", "cores": threads,
+                                "kind": "oracle",
+                                "sample": f"first {n_tok} of {T} tokens as a batch of their "
+                                          f"own, {t:.1f} s"}
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        dist.destroy_process_group()
+    return 0
+
+
+def main():
+    ap = argparse.ArgumentParser(description=__doc__.split("\n")[0])
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=50)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=("ours", "reference"), default="ours")
+    ap.add_argument("--workload", default=DEFAULT_WORKLOAD, choices=list(I.WORKLOADS))
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--traffic", type=float, default=None,
+                    help="DRAM bytes per expert-FFN launch pair from an ncu capture")
+    args = ap.parse_args()
+    wl = I.WORKLOADS[args.workload]
+    if args.impl == "reference":
+        return bench_reference(args, wl)
+    return bench_ours(args, wl)
+
+
+if __name__ == "__main__":
+    sys.exit(main())

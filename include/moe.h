@@ -1,0 +1,181 @@
+/*
+ * moe.h -- C ABI of the B300 (sm_103a) sparsely-gated Mixture-of-Experts FFN
+ * layer forward pass.
+ *
+ * The operation is the MoE layer of "Mixture of Experts: Scaling Parameters
+ * Without Scaling Compute", section "The MoE layer": router logits
+ * g = W_r x, probabilities p = softmax(g), the top-k experts per token, and
+ * the output y = sum over the selected experts i of w_i * f_i(x), where each
+ * expert f_i is Linear(d, d_ff) + bias, exact GELU, Linear(d_ff, d) + bias and
+ * w_i is the selected probability, renormalised over the k choices or not.
+ * Section "The central problem: load balancing" of the same page adds the
+ * expert capacity (overflow assignments are dropped) and the Switch-style
+ * auxiliary loss E * sum_i f_i P_i.
+ *
+ * Conventions shared by every call
+ * --------------------------------
+ *  - Every pointer argument is a DEVICE pointer owned by the caller, except
+ *    `cfg` (host).  The library allocates no memory.
+ *  - Every call is asynchronous on `stream` (a cudaStream_t; NULL means the
+ *    legacy default stream) and returns after enqueueing its kernels; none
+ *    synchronises, except moe_get_device_error.
+ *  - Layouts are row-major.  Weights use the nn.Linear (out, in) layout:
+ *      W_r [E][d] fp32, W1 [E][d_ff][d], b1 [E][d_ff], W2 [E][d][d_ff],
+ *      b2 [E][d].
+ *    x, W1, b1, W2, b2 and y have the element type cfg->dtype (fp32 or bf16).
+ *  - Alignment: x, W1, W2, x_perm, y_perm and y must be 16-byte aligned; d
+ *    and d_ff must be multiples of 8.
+ *  - Routing: experts are ranked by their fp32 router logit, larger first;
+ *    equal logits rank the lower expert index first (softmax is monotone, so
+ *    this is the top-k of p).
+ *  - Capacity: when cfg->capacity >= 0 each expert keeps at most that many
+ *    assignments, the first ones in (token, slot) order; the others are
+ *    dropped and contribute zero to y.  cfg->capacity < 0 means no cap.
+ *  - Dispatch order: the kept assignments of expert e occupy rows
+ *    offsets[e] .. offsets[e+1]-1 of the permuted buffers, in ascending token
+ *    order (the per-expert row lists of the page's dispatch loop).
+ *  - Errors: arguments are validated on the host before any launch; an
+ *    invalid call returns a status and enqueues nothing.  A problem found on
+ *    the device (an expert index outside [0, E) handed to moe_dispatch, a
+ *    pipeline wait that gave up) is recorded in the workspace and reported by
+ *    moe_get_device_error; the offending element is skipped, never written
+ *    out of bounds.
+ *  - Workspace: `ws` is scratch device memory of at least
+ *    moe_workspace_size(cfg) bytes, 256-byte aligned.  Calls that run
+ *    concurrently must not share a workspace.
+ */
+#ifndef MOE_H
+#define MOE_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum moe_status {
+    MOE_OK = 0,
+    MOE_ERR_INVALID_ARG = 1,  /* null pointer, bad size or shape */
+    MOE_ERR_ALIGNMENT = 2,    /* a pointer or a row length breaks the alignment rule */
+    MOE_ERR_WORKSPACE = 3,    /* ws_bytes < moe_workspace_size(cfg) or ws misaligned */
+    MOE_ERR_UNSUPPORTED = 4,  /* shape outside what the kernels implement (E > 256 ...) */
+    MOE_ERR_CUDA = 5,         /* a CUDA runtime call failed (launch, memset ...) */
+    MOE_ERR_DEVICE = 6        /* the device recorded an error (see moe_get_device_error) */
+} moe_status;
+
+typedef enum moe_dtype { MOE_F32 = 0, MOE_BF16 = 1 } moe_dtype;
+
+/* Shape and options of one layer call. */
+typedef struct moe_config {
+    int32_t T;           /* tokens in the batch (>= 0) */
+    int32_t d;           /* model width (multiple of 8) */
+    int32_t d_ff;        /* expert hidden width (multiple of 8) */
+    int32_t E;           /* experts, 1 .. 256 */
+    int32_t k;           /* experts per token, 1 .. min(E, 8) */
+    int32_t dtype;       /* moe_dtype of x, W1, b1, W2, b2, y */
+    int32_t capacity;    /* < 0: no cap; >= 0: kept assignments per expert at most */
+    int32_t renormalize; /* 1: w = p_sel / sum(p_sel); 0: w = p_sel */
+} moe_config;
+
+/* Bytes of workspace any call below needs for this configuration. */
+size_t moe_workspace_size(const moe_config* cfg);
+
+/* Static text for a status code. */
+const char* moe_status_string(moe_status s);
+
+/*
+ * Router: logits, softmax, top-k and gate weights, per-expert counts and the
+ * auxiliary loss ("The MoE layer", steps 1-2; "The central problem: load
+ * balancing", auxiliary loss).
+ *   x           [T][d] dtype          token batch
+ *   W_r         [E][d] fp32           router weight
+ *   logit_bias  [E] fp32 or NULL      added to every token's logits
+ *   logits_in   [T][E] fp32 or NULL   if given, used as the logits (x, W_r
+ *                                     and logit_bias are then not read)
+ *   logits_out  [T][E] fp32 or NULL   receives the logits used for routing
+ *   topk_idx    [T][k] int32          selected experts, best first
+ *   topk_w      [T][k] fp32           gate weights of the selected experts
+ *   expert_counts [E] int32 or NULL   assignments per expert, all k slots,
+ *                                     before any capacity drop
+ *   aux_out     [1] fp32 or NULL      E * sum_i f_i P_i, f_i from the first
+ *                                     slot; 0 when T == 0
+ */
+moe_status moe_route(const moe_config* cfg, const void* x, const float* W_r,
+                     const float* logit_bias, const float* logits_in, float* logits_out,
+                     int32_t* topk_idx, float* topk_w, int32_t* expert_counts, float* aux_out,
+                     void* ws, size_t ws_bytes, void* stream);
+
+/*
+ * Dispatch: expert offsets, the capacity drop and the gather of token rows
+ * into expert-contiguous order ("The MoE layer", dispatch of each expert's
+ * tokens; "The central problem: load balancing", capacity).
+ *   x           [T][d] dtype
+ *   topk_idx    [T][k] int32          from moe_route (values outside [0, E)
+ *                                     are skipped and flagged)
+ *   topk_w      [T][k] fp32 or NULL   gate weights; if given, copied to perm_w
+ *   offsets     [E+1] int32           segment starts; offsets[E] = kept total
+ *   slot_of     [T][k] int32          row of each assignment, -1 if dropped
+ *   perm_token  [T*k] int32           token of each kept row (first
+ *                                     offsets[E] entries are written)
+ *   perm_w      [T*k] fp32 or NULL    gate weight of each kept row
+ *   x_perm      [T*k][d] dtype        gathered rows (first offsets[E] rows)
+ */
+moe_status moe_dispatch(const moe_config* cfg, const void* x, const int32_t* topk_idx,
+                        const float* topk_w, int32_t* offsets, int32_t* slot_of,
+                        int32_t* perm_token, float* perm_w, void* x_perm,
+                        void* ws, size_t ws_bytes, void* stream);
+
+/*
+ * Experts: for every expert segment, y_perm = w * (GELU(x_perm W1^T + b1)
+ * W2^T + b2) ("The MoE layer", expert = Linear, GELU, Linear).
+ *   x_perm      [T*k][d] dtype        rows grouped by expert (moe_dispatch)
+ *   offsets     [E+1] int32           segment starts (device; not read on the host)
+ *   W1, b1, W2, b2                    expert bank, dtype
+ *   perm_w      [T*k] fp32 or NULL    per-row weight; NULL means 1
+ *   y_perm      [T*k][d] fp32         expert outputs (first offsets[E] rows)
+ * The hidden activations live in the workspace (bf16 for bf16 layers).
+ */
+moe_status moe_expert_ffn(const moe_config* cfg, const void* x_perm, const int32_t* offsets,
+                          const void* W1, const void* b1, const void* W2, const void* b2,
+                          const float* perm_w, float* y_perm,
+                          void* ws, size_t ws_bytes, void* stream);
+
+/*
+ * Combine: y[t] = sum over j = 0..k-1 with slot_of[t][j] >= 0 of
+ * y_perm[slot_of[t][j]], summed in slot order in fp32, stored as dtype; a
+ * token with every assignment dropped gets 0 ("The MoE layer", weighted
+ * combination; the weights were applied by moe_expert_ffn).
+ *   y_perm [T*k][d] fp32, slot_of [T][k] int32, y [T][d] dtype.
+ */
+moe_status moe_combine(const moe_config* cfg, const float* y_perm, const int32_t* slot_of,
+                       void* y, void* stream);
+
+/*
+ * The whole layer: route, dispatch, experts, combine.  Intermediates live in
+ * the workspace.  aux_out, expert_counts and logits_out may be NULL.
+ */
+moe_status moe_forward(const moe_config* cfg, const void* x, const float* W_r,
+                       const float* logit_bias, const void* W1, const void* b1,
+                       const void* W2, const void* b2, void* y, float* aux_out,
+                       int32_t* expert_counts, float* logits_out,
+                       void* ws, size_t ws_bytes, void* stream);
+
+/*
+ * Synchronises `stream`, then reads and clears the device error record of
+ * workspace `ws`.  Returns MOE_OK, or MOE_ERR_DEVICE with *code (if not
+ * NULL) set to the first recorded error code (1: expert index out of range;
+ * 2: pipeline wait timed out) and *info to a detail value.
+ */
+moe_status moe_get_device_error(void* ws, void* stream, int32_t* code, int32_t* info);
+
+/*
+ * Diagnostics: number of CUDA kernels libmoe has enqueued in this process
+ * since it was loaded (memsets excluded).  No counterpart on the pages.
+ */
+uint64_t moe_launch_count(void);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* MOE_H */

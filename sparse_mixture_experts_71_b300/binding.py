@@ -1,0 +1,154 @@
+"""Thin ctypes binding of libmoe (the C ABI declared in include/moe.h).
+
+Argument marshalling only: every step of the layer runs in libmoe's CUDA
+kernels.  PyTorch supplies device memory and the current CUDA stream.  The
+functions keep the C names without the ``moe_`` prefix.
+
+The library must have been built (``python -m sparse_mixture_experts_71_b300.build``);
+importing this module without it raises, it never falls back to anything else.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+
+import torch
+
+_LIB_PATH = os.path.join(os.path.dirname(os.path.abspath(__file__)), "libmoe.so")
+
+MOE_F32, MOE_BF16 = 0, 1
+STATUS = {0: "ok", 1: "invalid argument", 2: "misaligned pointer or row length",
+          3: "workspace missing, misaligned or too small", 4: "unsupported shape",
+          5: "CUDA runtime error", 6: "device-side error recorded"}
+
+EXPORTED = ("moe_workspace_size", "moe_status_string", "moe_route", "moe_dispatch",
+            "moe_expert_ffn", "moe_combine", "moe_forward", "moe_get_device_error",
+            "moe_launch_count")
+
+
+class MoeConfig(ctypes.Structure):
+    _fields_ = [("T", ctypes.c_int32), ("d", ctypes.c_int32), ("d_ff", ctypes.c_int32),
+                ("E", ctypes.c_int32), ("k", ctypes.c_int32), ("dtype", ctypes.c_int32),
+                ("capacity", ctypes.c_int32), ("renormalize", ctypes.c_int32)]
+
+
+class MoeError(RuntimeError):
+    def __init__(self, fn: str, status: int):
+        super().__init__(f"{fn}: {STATUS.get(status, 'unknown status')} (status {status})")
+        self.status = status
+
+
+_P = ctypes.c_void_p
+_lib = None
+
+
+def load() -> ctypes.CDLL:
+    """Load libmoe.so once; raise if it has not been built."""
+    global _lib
+    if _lib is None:
+        if not os.path.exists(_LIB_PATH):
+            raise ImportError(f"libmoe.so is not built ({_LIB_PATH}); run "
+                              "python -m sparse_mixture_experts_71_b300.build")
+        lib = ctypes.CDLL(_LIB_PATH)
+        lib.moe_workspace_size.restype = ctypes.c_size_t
+        lib.moe_workspace_size.argtypes = [ctypes.POINTER(MoeConfig)]
+        lib.moe_status_string.restype = ctypes.c_char_p
+        lib.moe_status_string.argtypes = [ctypes.c_int]
+        cfgp = ctypes.POINTER(MoeConfig)
+        sz = ctypes.c_size_t
+        lib.moe_route.argtypes = [cfgp] + [_P] * 9 + [_P, sz, _P]
+        lib.moe_dispatch.argtypes = [cfgp] + [_P] * 8 + [_P, sz, _P]
+        lib.moe_expert_ffn.argtypes = [cfgp] + [_P] * 8 + [_P, sz, _P]
+        lib.moe_combine.argtypes = [cfgp, _P, _P, _P, _P]
+        lib.moe_forward.argtypes = [cfgp] + [_P] * 11 + [_P, sz, _P]
+        lib.moe_get_device_error.argtypes = [_P, _P, ctypes.POINTER(ctypes.c_int32),
+                                             ctypes.POINTER(ctypes.c_int32)]
+        for name in EXPORTED[2:-1]:
+            getattr(lib, name).restype = ctypes.c_int
+        lib.moe_launch_count.restype = ctypes.c_uint64
+        lib.moe_launch_count.argtypes = []
+        _lib = lib
+    return _lib
+
+
+def config(T, d, d_ff, E, k, dtype="bf16", capacity=None, renormalize=True) -> MoeConfig:
+    return MoeConfig(T, d, d_ff, E, k, MOE_BF16 if dtype == "bf16" else MOE_F32,
+                     -1 if capacity is None else int(capacity), 1 if renormalize else 0)
+
+
+def _ptr(t):
+    if t is None:
+        return None
+    if isinstance(t, int):
+        return t
+    return t.data_ptr()
+
+
+def _stream(stream):
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return stream.cuda_stream if hasattr(stream, "cuda_stream") else stream
+
+
+def _check(fn, st):
+    if st != 0:
+        raise MoeError(fn, st)
+
+
+def workspace_size(cfg: MoeConfig) -> int:
+    return int(load().moe_workspace_size(ctypes.byref(cfg)))
+
+
+def workspace(cfg: MoeConfig, device="cuda") -> torch.Tensor:
+    """A zero-filled workspace (the device error record must start at zero)."""
+    n = workspace_size(cfg)
+    if n == 0:
+        raise MoeError("moe_workspace_size", 1)
+    return torch.zeros(n, dtype=torch.uint8, device=device)
+
+
+def route(cfg, x, W_r, topk_idx, topk_w, ws, logit_bias=None, logits_in=None, logits_out=None,
+          expert_counts=None, aux_out=None, stream=None):
+    _check("moe_route", load().moe_route(
+        ctypes.byref(cfg), _ptr(x), _ptr(W_r), _ptr(logit_bias), _ptr(logits_in), _ptr(logits_out),
+        _ptr(topk_idx), _ptr(topk_w), _ptr(expert_counts), _ptr(aux_out), _ptr(ws),
+        ws.numel(), _stream(stream)))
+
+
+def dispatch(cfg, x, topk_idx, offsets, slot_of, perm_token, x_perm, ws, topk_w=None,
+             perm_w=None, stream=None):
+    _check("moe_dispatch", load().moe_dispatch(
+        ctypes.byref(cfg), _ptr(x), _ptr(topk_idx), _ptr(topk_w), _ptr(offsets), _ptr(slot_of),
+        _ptr(perm_token), _ptr(perm_w), _ptr(x_perm), _ptr(ws), ws.numel(), _stream(stream)))
+
+
+def expert_ffn(cfg, x_perm, offsets, W1, b1, W2, b2, y_perm, ws, perm_w=None, stream=None):
+    _check("moe_expert_ffn", load().moe_expert_ffn(
+        ctypes.byref(cfg), _ptr(x_perm), _ptr(offsets), _ptr(W1), _ptr(b1), _ptr(W2), _ptr(b2),
+        _ptr(perm_w), _ptr(y_perm), _ptr(ws), ws.numel(), _stream(stream)))
+
+
+def combine(cfg, y_perm, slot_of, y, stream=None):
+    _check("moe_combine", load().moe_combine(
+        ctypes.byref(cfg), _ptr(y_perm), _ptr(slot_of), _ptr(y), _stream(stream)))
+
+
+def forward(cfg, x, W_r, W1, b1, W2, b2, y, ws, logit_bias=None, aux_out=None,
+            expert_counts=None, logits_out=None, stream=None):
+    _check("moe_forward", load().moe_forward(
+        ctypes.byref(cfg), _ptr(x), _ptr(W_r), _ptr(logit_bias), _ptr(W1), _ptr(b1), _ptr(W2),
+        _ptr(b2), _ptr(y), _ptr(aux_out), _ptr(expert_counts), _ptr(logits_out), _ptr(ws),
+        ws.numel(), _stream(stream)))
+
+
+def launch_count() -> int:
+    """Kernels libmoe has enqueued in this process (diagnostics)."""
+    return int(load().moe_launch_count())
+
+
+def get_device_error(ws, stream=None):
+    """(status, code, info): synchronises the stream, reads and clears the record."""
+    code, info = ctypes.c_int32(0), ctypes.c_int32(0)
+    st = load().moe_get_device_error(_ptr(ws), _stream(stream), ctypes.byref(code),
+                                     ctypes.byref(info))
+    return st, code.value, info.value

@@ -1,0 +1,75 @@
+// Combine: the weighted expert outputs of each token summed back into token
+// order.
+//
+// "Mixture of Experts: Scaling Parameters Without Scaling Compute", section
+// "The MoE layer", step 3 (the output is the weighted combination of the
+// selected experts' outputs; the weights were applied by the second expert
+// GEMM).  A token whose assignments were all dropped by the capacity cap
+// ("The central problem: load balancing") gets zero.
+//
+// One warp per token, fp32 accumulation in slot order, 16-byte loads of the
+// fp32 expert rows and 8- or 16-byte stores of the output row.
+
+#include <cuda_runtime.h>
+
+#include "moe_device.cuh"
+#include "moe_internal.h"
+
+namespace moe {
+namespace {
+
+__device__ __forceinline__ void store4(float* p, float4 v) { *reinterpret_cast<float4*>(p) = v; }
+__device__ __forceinline__ void store4(__nv_bfloat16* p, float4 v) {
+    __nv_bfloat162 lo = __floats2bfloat162_rn(v.x, v.y), hi = __floats2bfloat162_rn(v.z, v.w);
+    uint2 u;
+    u.x = *reinterpret_cast<uint32_t*>(&lo);
+    u.y = *reinterpret_cast<uint32_t*>(&hi);
+    *reinterpret_cast<uint2*>(p) = u;
+}
+
+template <typename TY>
+__global__ void __launch_bounds__(256) combine_kernel(const float* __restrict__ y_perm,
+                                                      const int32_t* __restrict__ slot_of, int T,
+                                                      int k, int d, TY* __restrict__ y) {
+    const int lane = threadIdx.x % 32;
+    const int nwarps = gridDim.x * (blockDim.x / 32);
+    const int nv = d / 4;
+    for (int t = blockIdx.x * (blockDim.x / 32) + threadIdx.x / 32; t < T; t += nwarps) {
+        int slots[kMaxTopK];
+        for (int j = 0; j < k; ++j) {
+            const int sl = __ldg(slot_of + (size_t)t * k + j);
+            slots[j] = sl < T * k ? sl : -1;  // y_perm has T*k rows
+        }
+        for (int v = lane; v < nv; v += 32) {
+            float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+            for (int j = 0; j < k; ++j) {
+                if (slots[j] < 0) continue;
+                const float4 q = __ldg(reinterpret_cast<const float4*>(y_perm + (size_t)slots[j] * d) + v);
+                acc.x += q.x; acc.y += q.y; acc.z += q.z; acc.w += q.w;
+            }
+            store4(y + (size_t)t * d + 4 * v, acc);
+        }
+    }
+}
+
+}  // namespace
+
+cudaError_t launch_combine(const moe_config& c, const float* y_perm, const int32_t* slot_of,
+                           void* y, cudaStream_t s) {
+    if (c.T == 0) return cudaSuccess;
+    int dev = 0, sms = 148;
+    cudaGetDevice(&dev);
+    cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+    int blocks = (c.T + 7) / 8;
+    blocks = blocks < sms * 8 ? blocks : sms * 8;
+    if (c.dtype == MOE_BF16)
+        combine_kernel<__nv_bfloat16><<<blocks, 256, 0, s>>>(y_perm, slot_of, c.T, c.k, c.d,
+                                                             reinterpret_cast<__nv_bfloat16*>(y));
+    else
+        combine_kernel<float><<<blocks, 256, 0, s>>>(y_perm, slot_of, c.T, c.k, c.d,
+                                                     reinterpret_cast<float*>(y));
+    count_launches(1);
+    return cudaGetLastError();
+}
+
+}  // namespace moe

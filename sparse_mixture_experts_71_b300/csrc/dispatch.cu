@@ -1,0 +1,196 @@
+// Dispatch: expert offsets, token-order capacity drop and the gather of token
+// rows into expert-contiguous order.
+//
+// "Mixture of Experts: Scaling Parameters Without Scaling Compute", section
+// "The MoE layer" (each expert receives the rows routed to it, in ascending
+// token order) and section "The central problem: load balancing" (each expert
+// takes at most `capacity` tokens; the overflow is dropped).
+//
+// A stable counting sort keyed by expert, in three kernels:
+//   count   one block per kCountBlock consecutive assignments a = t*k + j:
+//           per-block expert histogram and the rank of each assignment among
+//           the block's earlier assignments to the same expert (warp match +
+//           per-warp histograms; no atomics, so the result is exact).
+//   scan    one block: for every (block, expert) the number of assignments to
+//           that expert in earlier blocks, the per-expert totals, the kept
+//           counts min(total, capacity) and their exclusive prefix sum
+//           (offsets).
+//   permute one warp per assignment: rank = base + local rank; kept iff rank <
+//           capacity; row = offsets[e] + rank; writes slot_of / perm_token /
+//           perm_w and copies the token's row with 16-byte vector accesses.
+
+#include <cuda_runtime.h>
+
+#include "moe_device.cuh"
+#include "moe_internal.h"
+
+namespace moe {
+namespace {
+
+constexpr int kWarps = kCountBlock / 32;
+
+__global__ void __launch_bounds__(kCountBlock) count_kernel(const int32_t* __restrict__ idx, int n,
+                                                            int E, int32_t* __restrict__ blk_hist,
+                                                            int32_t* __restrict__ local_rank,
+                                                            DeviceHeader* hdr) {
+    __shared__ int wh[kWarps][kMaxExperts];
+    const int tid = threadIdx.x, warp = tid / 32, lane = tid % 32;
+    for (int i = tid; i < kWarps * kMaxExperts; i += kCountBlock) (&wh[0][0])[i] = 0;
+    __syncthreads();
+    const int a = blockIdx.x * kCountBlock + tid;
+    int e = -1;
+    if (a < n) {
+        e = __ldg(idx + a);
+        if (e < 0 || e >= E) {
+            record_error(hdr, kErrExpertRange, a);
+            e = -1;
+        }
+    }
+    const unsigned same = __match_any_sync(0xffffffffu, e);
+    const int rank_in_warp = __popc(same & ((1u << lane) - 1u));
+    if (e >= 0 && rank_in_warp == 0) wh[warp][e] = __popc(same);
+    __syncthreads();
+    if (a < n) {
+        int r = -1;
+        if (e >= 0) {
+            r = rank_in_warp;
+            for (int w = 0; w < warp; ++w) r += wh[w][e];
+        }
+        local_rank[a] = r;
+    }
+    for (int x = tid; x < E; x += kCountBlock) {
+        int s = 0;
+#pragma unroll
+        for (int w = 0; w < kWarps; ++w) s += wh[w][x];
+        blk_hist[(size_t)blockIdx.x * E + x] = s;
+    }
+}
+
+// One block of 1024 threads.  Thread (part, e) with part < P = 1024 / E owns
+// a contiguous range of blocks for expert e.
+__global__ void __launch_bounds__(1024) scan_kernel(const int32_t* __restrict__ blk_hist,
+                                                    int nblk, int E, int capacity,
+                                                    int32_t* __restrict__ blk_base,
+                                                    int32_t* __restrict__ offsets) {
+    __shared__ int part_sum[1024];
+    __shared__ int s_total[kMaxExperts];
+    const int tid = threadIdx.x;
+    const int P = 1024 / E;
+    const int part = tid / E, e = tid % E;
+    const bool active = part < P;
+    const int per = (nblk + P - 1) / P;
+    const int b0 = part * per, b1 = min(nblk, b0 + per);
+    int s = 0;
+    if (active)
+        for (int b = b0; b < b1; ++b) s += blk_hist[(size_t)b * E + e];
+    part_sum[tid] = s;
+    __syncthreads();
+    if (tid < E) {  // exclusive scan over parts, per expert
+        int run = 0;
+        for (int p = 0; p < P; ++p) {
+            const int v = part_sum[p * E + tid];
+            part_sum[p * E + tid] = run;
+            run += v;
+        }
+        s_total[tid] = run;
+    }
+    __syncthreads();
+    if (active) {
+        int run = part_sum[tid];
+        for (int b = b0; b < b1; ++b) {
+            blk_base[(size_t)b * E + e] = run;
+            run += blk_hist[(size_t)b * E + e];
+        }
+    }
+    if (tid == 0) {
+        int off = 0;
+        for (int x = 0; x < E; ++x) {
+            offsets[x] = off;
+            const int tot = s_total[x];
+            off += capacity < 0 ? tot : min(tot, capacity);
+        }
+        offsets[E] = off;
+    }
+}
+
+template <typename TX>
+__global__ void __launch_bounds__(256) permute_kernel(
+    const TX* __restrict__ x, const int32_t* __restrict__ idx, const float* __restrict__ topk_w,
+    const int32_t* __restrict__ local_rank, const int32_t* __restrict__ blk_base,
+    const int32_t* __restrict__ offsets, int n, int k, int E, int d, int capacity,
+    int32_t* __restrict__ slot_of, int32_t* __restrict__ perm_token, float* __restrict__ perm_w,
+    TX* __restrict__ x_perm) {
+    const int lane = threadIdx.x % 32;
+    const int nwarps = gridDim.x * (blockDim.x / 32);
+    const int nvec = d * (int)sizeof(TX) / 16;  // 16-byte vectors per row
+    for (int a = blockIdx.x * (blockDim.x / 32) + threadIdx.x / 32; a < n; a += nwarps) {
+        const int r_local = __ldg(local_rank + a);
+        int slot = -1;
+        if (r_local >= 0) {
+            const int e = __ldg(idx + a);
+            const int r = __ldg(blk_base + (size_t)(a / kCountBlock) * E + e) + r_local;
+            if (capacity < 0 || r < capacity) slot = __ldg(offsets + e) + r;
+        }
+        const int t = a / k;
+        if (lane == 0) {
+            slot_of[a] = slot;
+            if (slot >= 0) {
+                perm_token[slot] = t;
+                if (perm_w != nullptr) perm_w[slot] = __ldg(topk_w + a);
+            }
+        }
+        if (slot < 0 || x_perm == nullptr) continue;
+        const uint4* src = reinterpret_cast<const uint4*>(x + (size_t)t * d);
+        uint4* dst = reinterpret_cast<uint4*>(x_perm + (size_t)slot * d);
+        int v = lane;
+        for (; v + 96 < nvec; v += 128) {
+            const uint4 q0 = __ldg(src + v), q1 = __ldg(src + v + 32);
+            const uint4 q2 = __ldg(src + v + 64), q3 = __ldg(src + v + 96);
+            dst[v] = q0; dst[v + 32] = q1; dst[v + 64] = q2; dst[v + 96] = q3;
+        }
+        for (; v < nvec; v += 32) dst[v] = __ldg(src + v);
+    }
+}
+
+}  // namespace
+
+cudaError_t launch_dispatch(const moe_config& c, const void* x, const int32_t* topk_idx,
+                            const float* topk_w, int32_t* offsets, int32_t* slot_of,
+                            int32_t* perm_token, float* perm_w, void* x_perm, void* ws,
+                            const WsLayout& L, cudaStream_t s) {
+    const int n = c.T * c.k;
+    int32_t* blk_hist = at<int32_t>(ws, L.blk_hist);
+    int32_t* blk_base = at<int32_t>(ws, L.blk_base);
+    int32_t* local_rank = at<int32_t>(ws, L.local_rank);
+    DeviceHeader* hdr = at<DeviceHeader>(ws, L.header);
+    if (n > 0) {
+        count_kernel<<<L.count_blocks, kCountBlock, 0, s>>>(topk_idx, n, c.E, blk_hist, local_rank,
+                                                            hdr);
+        count_launches(1);
+    }
+    scan_kernel<<<1, 1024, 0, s>>>(blk_hist, L.count_blocks, c.E, c.capacity, blk_base, offsets);
+    count_launches(1);
+    if (n > 0) {
+        int dev = 0, sms = 148;
+        cudaGetDevice(&dev);
+        cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+        const int warps_needed = n;
+        int blocks = (warps_needed + 7) / 8;
+        blocks = blocks < sms * 8 ? blocks : sms * 8;
+        if (c.dtype == MOE_BF16) {
+            permute_kernel<__nv_bfloat16><<<blocks, 256, 0, s>>>(
+                reinterpret_cast<const __nv_bfloat16*>(x), topk_idx, topk_w, local_rank, blk_base,
+                offsets, n, c.k, c.E, c.d, c.capacity, slot_of, perm_token, perm_w,
+                reinterpret_cast<__nv_bfloat16*>(x_perm));
+        } else {
+            permute_kernel<float><<<blocks, 256, 0, s>>>(
+                reinterpret_cast<const float*>(x), topk_idx, topk_w, local_rank, blk_base, offsets,
+                n, c.k, c.E, c.d, c.capacity, slot_of, perm_token, perm_w,
+                reinterpret_cast<float*>(x_perm));
+        }
+        count_launches(1);
+    }
+    return cudaGetLastError();
+}
+
+}  // namespace moe

@@ -1,0 +1,257 @@
+// C ABI of libmoe: argument validation, workspace layout and kernel launches.
+// The operation each entry point performs is documented in include/moe.h.
+
+#include <cuda_runtime.h>
+#include <stddef.h>
+#include <stdint.h>
+
+#include <atomic>
+
+#include "moe_internal.h"
+
+namespace moe {
+
+static std::atomic<uint64_t> g_launches{0};
+void count_launches(int n) { g_launches.fetch_add((uint64_t)n, std::memory_order_relaxed); }
+
+cudaError_t launch_expert_ffn_simt(const moe_config& c, const void* x_perm, const int32_t* offsets,
+                                   const void* W1, const void* b1, const void* W2, const void* b2,
+                                   const float* perm_w, float* y_perm, void* h, int64_t max_seg,
+                                   int64_t max_rows, cudaStream_t s);
+
+namespace {
+
+size_t align256(size_t v) { return (v + 255) & ~size_t(255); }
+
+size_t elem_size(const moe_config& c) { return c.dtype == MOE_BF16 ? 2 : 4; }
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+moe_status check_config(const moe_config* c) {
+    if (c == nullptr) return MOE_ERR_INVALID_ARG;
+    if (c->T < 0 || c->d <= 0 || c->d_ff <= 0 || c->E <= 0 || c->k <= 0) return MOE_ERR_INVALID_ARG;
+    if (c->dtype != MOE_F32 && c->dtype != MOE_BF16) return MOE_ERR_INVALID_ARG;
+    if (c->renormalize != 0 && c->renormalize != 1) return MOE_ERR_INVALID_ARG;
+    if (c->k > c->E) return MOE_ERR_INVALID_ARG;
+    if (c->E > kMaxExperts || c->k > kMaxTopK) return MOE_ERR_UNSUPPORTED;
+    if (c->d % 8 != 0 || c->d_ff % 8 != 0) return MOE_ERR_ALIGNMENT;
+    if ((int64_t)c->T * c->k > (int64_t)INT32_MAX / 2) return MOE_ERR_UNSUPPORTED;
+    return MOE_OK;
+}
+
+moe_status check_ws(const moe_config& c, void* ws, size_t ws_bytes, WsLayout* L) {
+    *L = ws_layout(c);
+    if (ws == nullptr || (reinterpret_cast<uintptr_t>(ws) & 255u) != 0) return MOE_ERR_WORKSPACE;
+    if (ws_bytes < L->total) return MOE_ERR_WORKSPACE;
+    return MOE_OK;
+}
+
+moe_status from_cuda(cudaError_t e) { return e == cudaSuccess ? MOE_OK : MOE_ERR_CUDA; }
+
+// T == 0: no token, no kernel; counts and the loss are defined as zero.
+moe_status empty_batch(const moe_config& c, int32_t* expert_counts, float* aux_out,
+                       cudaStream_t s) {
+    if (expert_counts && cudaMemsetAsync(expert_counts, 0, sizeof(int32_t) * c.E, s) != cudaSuccess)
+        return MOE_ERR_CUDA;
+    if (aux_out && cudaMemsetAsync(aux_out, 0, sizeof(float), s) != cudaSuccess) return MOE_ERR_CUDA;
+    return MOE_OK;
+}
+
+int64_t max_segment(const moe_config& c) {
+    int64_t m = c.T;  // a token reaches one expert at most once
+    if (c.capacity >= 0 && c.capacity < m) m = c.capacity;
+    return m;
+}
+
+}  // namespace
+
+WsLayout ws_layout(const moe_config& c) {
+    WsLayout L{};
+    const int64_t n = (int64_t)c.T * c.k;
+    L.route_blocks = (int)((c.T + route_tokens_per_block(c.E) - 1) / route_tokens_per_block(c.E));
+    L.count_blocks = (int)((n + kCountBlock - 1) / kCountBlock);
+    L.rows = n;
+    if (c.capacity >= 0 && (int64_t)c.E * c.capacity < L.rows) L.rows = (int64_t)c.E * c.capacity;
+    const size_t es = elem_size(c);
+    size_t o = 0;
+    auto take = [&](size_t bytes) {
+        const size_t at = o;
+        o = align256(o + bytes);
+        return at;
+    };
+    L.header = take(sizeof(DeviceHeader));
+    L.counts = take(sizeof(int32_t) * c.E);
+    L.top1 = take(sizeof(int32_t) * c.E);
+    L.blk_p = take(sizeof(float) * (size_t)L.route_blocks * c.E);
+    L.blk_hist = take(sizeof(int32_t) * (size_t)L.count_blocks * c.E);
+    L.blk_base = take(sizeof(int32_t) * (size_t)L.count_blocks * c.E);
+    L.local_rank = take(sizeof(int32_t) * (size_t)n);
+    L.topk_idx = take(sizeof(int32_t) * (size_t)n);
+    L.topk_w = take(sizeof(float) * (size_t)n);
+    L.offsets = take(sizeof(int32_t) * (size_t)(c.E + 1));
+    L.slot_of = take(sizeof(int32_t) * (size_t)n);
+    L.perm_token = take(sizeof(int32_t) * (size_t)n);
+    L.perm_w = take(sizeof(float) * (size_t)n);
+    L.x_perm = take(es * (size_t)L.rows * c.d);
+    L.h = take(es * (size_t)L.rows * c.d_ff);
+    L.y_perm = take(sizeof(float) * (size_t)L.rows * c.d);
+    L.total = o;
+    return L;
+}
+
+cudaError_t launch_expert_ffn(const moe_config& c, const void* x_perm, const int32_t* offsets,
+                              const void* W1, const void* b1, const void* W2, const void* b2,
+                              const float* perm_w, float* y_perm, void* ws, const WsLayout& L,
+                              cudaStream_t s) {
+    return launch_expert_ffn_simt(c, x_perm, offsets, W1, b1, W2, b2, perm_w, y_perm,
+                                  at<void>(ws, L.h), max_segment(c), L.rows, s);
+}
+
+}  // namespace moe
+
+using namespace moe;
+
+extern "C" {
+
+uint64_t moe_launch_count(void) { return g_launches.load(std::memory_order_relaxed); }
+
+size_t moe_workspace_size(const moe_config* cfg) {
+    if (check_config(cfg) != MOE_OK) return 0;
+    return ws_layout(*cfg).total;
+}
+
+const char* moe_status_string(moe_status s) {
+    switch (s) {
+        case MOE_OK: return "ok";
+        case MOE_ERR_INVALID_ARG: return "invalid argument";
+        case MOE_ERR_ALIGNMENT: return "misaligned pointer or row length";
+        case MOE_ERR_WORKSPACE: return "workspace missing, misaligned or too small";
+        case MOE_ERR_UNSUPPORTED: return "unsupported shape";
+        case MOE_ERR_CUDA: return "CUDA runtime error";
+        case MOE_ERR_DEVICE: return "device-side error recorded";
+    }
+    return "unknown status";
+}
+
+moe_status moe_route(const moe_config* cfg, const void* x, const float* W_r,
+                     const float* logit_bias, const float* logits_in, float* logits_out,
+                     int32_t* topk_idx, float* topk_w, int32_t* expert_counts, float* aux_out,
+                     void* ws, size_t ws_bytes, void* stream) {
+    moe_status st = check_config(cfg);
+    if (st != MOE_OK) return st;
+    const moe_config& c = *cfg;
+    WsLayout L;
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    if (c.T == 0) return empty_batch(c, expert_counts, aux_out, s);
+    if (topk_idx == nullptr || topk_w == nullptr) return MOE_ERR_INVALID_ARG;
+    if (logits_in == nullptr && (x == nullptr || W_r == nullptr)) return MOE_ERR_INVALID_ARG;
+    if (logits_in == nullptr && (!aligned16(x) || !aligned16(W_r))) return MOE_ERR_ALIGNMENT;
+    if ((st = check_ws(c, ws, ws_bytes, &L)) != MOE_OK) return st;
+    return from_cuda(launch_route(c, x, W_r, logit_bias, logits_in, logits_out, topk_idx, topk_w,
+                                  expert_counts, aux_out, ws, L, s));
+}
+
+moe_status moe_dispatch(const moe_config* cfg, const void* x, const int32_t* topk_idx,
+                        const float* topk_w, int32_t* offsets, int32_t* slot_of,
+                        int32_t* perm_token, float* perm_w, void* x_perm,
+                        void* ws, size_t ws_bytes, void* stream) {
+    moe_status st = check_config(cfg);
+    if (st != MOE_OK) return st;
+    const moe_config& c = *cfg;
+    if (offsets == nullptr) return MOE_ERR_INVALID_ARG;
+    if (c.T == 0) {
+        const cudaError_t e = cudaMemsetAsync(offsets, 0, sizeof(int32_t) * (c.E + 1),
+                                              reinterpret_cast<cudaStream_t>(stream));
+        return from_cuda(e);
+    }
+    if (x == nullptr || topk_idx == nullptr || slot_of == nullptr || perm_token == nullptr ||
+        x_perm == nullptr)
+        return MOE_ERR_INVALID_ARG;
+    if (perm_w != nullptr && topk_w == nullptr) return MOE_ERR_INVALID_ARG;
+    if (!aligned16(x) || !aligned16(x_perm)) return MOE_ERR_ALIGNMENT;
+    WsLayout L;
+    if ((st = check_ws(c, ws, ws_bytes, &L)) != MOE_OK) return st;
+    return from_cuda(launch_dispatch(c, x, topk_idx, topk_w, offsets, slot_of, perm_token, perm_w,
+                                     x_perm, ws, L, reinterpret_cast<cudaStream_t>(stream)));
+}
+
+moe_status moe_expert_ffn(const moe_config* cfg, const void* x_perm, const int32_t* offsets,
+                          const void* W1, const void* b1, const void* W2, const void* b2,
+                          const float* perm_w, float* y_perm,
+                          void* ws, size_t ws_bytes, void* stream) {
+    moe_status st = check_config(cfg);
+    if (st != MOE_OK) return st;
+    const moe_config& c = *cfg;
+    if (c.T == 0) return MOE_OK;
+    if (x_perm == nullptr || offsets == nullptr || W1 == nullptr || b1 == nullptr ||
+        W2 == nullptr || b2 == nullptr || y_perm == nullptr)
+        return MOE_ERR_INVALID_ARG;
+    if (!aligned16(x_perm) || !aligned16(W1) || !aligned16(W2) || !aligned16(y_perm))
+        return MOE_ERR_ALIGNMENT;
+    WsLayout L;
+    if ((st = check_ws(c, ws, ws_bytes, &L)) != MOE_OK) return st;
+    return from_cuda(launch_expert_ffn(c, x_perm, offsets, W1, b1, W2, b2, perm_w, y_perm, ws, L,
+                                       reinterpret_cast<cudaStream_t>(stream)));
+}
+
+moe_status moe_combine(const moe_config* cfg, const float* y_perm, const int32_t* slot_of,
+                       void* y, void* stream) {
+    moe_status st = check_config(cfg);
+    if (st != MOE_OK) return st;
+    const moe_config& c = *cfg;
+    if (c.T == 0) return MOE_OK;
+    if (y_perm == nullptr || slot_of == nullptr || y == nullptr) return MOE_ERR_INVALID_ARG;
+    if (!aligned16(y_perm) || !aligned16(y)) return MOE_ERR_ALIGNMENT;
+    return from_cuda(launch_combine(c, y_perm, slot_of, y, reinterpret_cast<cudaStream_t>(stream)));
+}
+
+moe_status moe_forward(const moe_config* cfg, const void* x, const float* W_r,
+                       const float* logit_bias, const void* W1, const void* b1,
+                       const void* W2, const void* b2, void* y, float* aux_out,
+                       int32_t* expert_counts, float* logits_out,
+                       void* ws, size_t ws_bytes, void* stream) {
+    moe_status st = check_config(cfg);
+    if (st != MOE_OK) return st;
+    const moe_config& c = *cfg;
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    if (c.T == 0) return empty_batch(c, expert_counts, aux_out, s);
+    if (x == nullptr || W_r == nullptr || W1 == nullptr || b1 == nullptr || W2 == nullptr ||
+        b2 == nullptr || y == nullptr)
+        return MOE_ERR_INVALID_ARG;
+    if (!aligned16(x) || !aligned16(W_r) || !aligned16(W1) || !aligned16(W2) || !aligned16(y))
+        return MOE_ERR_ALIGNMENT;
+    WsLayout L;
+    if ((st = check_ws(c, ws, ws_bytes, &L)) != MOE_OK) return st;
+    int32_t* idx = at<int32_t>(ws, L.topk_idx);
+    float* w = at<float>(ws, L.topk_w);
+    int32_t* offsets = at<int32_t>(ws, L.offsets);
+    int32_t* slot_of = at<int32_t>(ws, L.slot_of);
+    int32_t* perm_token = at<int32_t>(ws, L.perm_token);
+    float* perm_w = at<float>(ws, L.perm_w);
+    void* x_perm = at<void>(ws, L.x_perm);
+    float* y_perm = at<float>(ws, L.y_perm);
+    cudaError_t e = launch_route(c, x, W_r, logit_bias, nullptr, logits_out, idx, w, expert_counts,
+                                 aux_out, ws, L, s);
+    if (e == cudaSuccess)
+        e = launch_dispatch(c, x, idx, w, offsets, slot_of, perm_token, perm_w, x_perm, ws, L, s);
+    if (e == cudaSuccess)
+        e = launch_expert_ffn(c, x_perm, offsets, W1, b1, W2, b2, perm_w, y_perm, ws, L, s);
+    if (e == cudaSuccess) e = launch_combine(c, y_perm, slot_of, y, s);
+    return from_cuda(e);
+}
+
+moe_status moe_get_device_error(void* ws, void* stream, int32_t* code, int32_t* info) {
+    if (ws == nullptr) return MOE_ERR_INVALID_ARG;
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    if (cudaStreamSynchronize(s) != cudaSuccess) return MOE_ERR_CUDA;
+    DeviceHeader h;
+    if (cudaMemcpy(&h, ws, sizeof(int32_t) * 2, cudaMemcpyDeviceToHost) != cudaSuccess)
+        return MOE_ERR_CUDA;
+    if (code) *code = h.err_code;
+    if (info) *info = h.err_info;
+    if (h.err_code == 0) return MOE_OK;
+    if (cudaMemset(ws, 0, sizeof(int32_t) * 2) != cudaSuccess) return MOE_ERR_CUDA;
+    return MOE_ERR_DEVICE;
+}
+
+}  // extern "C"

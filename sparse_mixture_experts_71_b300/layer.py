@@ -1,0 +1,74 @@
+"""Python-side plumbing around libmoe: device copies of stored inputs and a
+layer object with the interface the pages use.
+
+"Mixture of Experts: Scaling Parameters Without Scaling Compute", section
+"The MoE layer": a layer is built from (d, d_ff, n_experts, k) and its
+forward maps a token batch x of shape (tokens, d) to (output, auxiliary loss).
+Here the weights are caller-provided device tensors and the whole forward
+pass is one ``moe_forward`` call into libmoe; torch only allocates the
+output, the scalars and the workspace.
+"""
+from __future__ import annotations
+
+import numpy as np
+import torch
+
+from . import binding as B
+from .inputs import Inputs
+
+
+def to_torch(a: np.ndarray, device="cuda") -> torch.Tensor:
+    """A stored input array as a torch tensor (uint16 bit patterns -> bf16)."""
+    if a.dtype == np.uint16:
+        return torch.from_numpy(a.view(np.int16)).view(torch.bfloat16).to(device)
+    return torch.from_numpy(np.ascontiguousarray(a)).to(device)
+
+
+def device_inputs(inp: Inputs, device="cuda") -> dict:
+    """Every stored tensor of ``inp`` copied to ``device`` (weights included)."""
+    out = {}
+    for name in ("x", "W_r", "logit_bias", "W1", "b1", "W2", "b2"):
+        a = getattr(inp, name)
+        out[name] = None if a is None else to_torch(a, device)
+    return out
+
+
+class MoELayer:
+    """Sparsely-gated MoE FFN layer whose forward pass runs in libmoe.
+
+    W_r: (E, d) fp32; W1: (E, d_ff, d); b1: (E, d_ff); W2: (E, d, d_ff);
+    b2: (E, d), all on one CUDA device, W1..b2 of one dtype (fp32 or bf16).
+    """
+
+    def __init__(self, W_r, W1, b1, W2, b2, k: int, capacity: int | None = None,
+                 renormalize: bool = True, logit_bias=None):
+        self.E, self.d_ff, self.d = W1.shape
+        self.k = k
+        self.dtype = "bf16" if W1.dtype == torch.bfloat16 else "f32"
+        self.capacity, self.renormalize = capacity, renormalize
+        self.W_r, self.W1, self.b1, self.W2, self.b2 = W_r, W1, b1, W2, b2
+        self.logit_bias = logit_bias
+        self._ws = {}
+
+    def config(self, T: int) -> B.MoeConfig:
+        return B.config(T, self.d, self.d_ff, self.E, self.k, self.dtype, self.capacity,
+                        self.renormalize)
+
+    def workspace(self, T: int) -> torch.Tensor:
+        if T not in self._ws:
+            self._ws[T] = B.workspace(self.config(T), device=self.W1.device)
+        return self._ws[T]
+
+    def forward(self, x, y=None, aux=None, expert_counts=None, logits_out=None, stream=None):
+        """(y, aux) for the token batch x (T, d); optional outputs are filled in place."""
+        T = x.shape[0]
+        if y is None:
+            y = torch.empty_like(x)
+        if aux is None:
+            aux = torch.empty(1, dtype=torch.float32, device=x.device)
+        B.forward(self.config(T), x, self.W_r, self.W1, self.b1, self.W2, self.b2, y,
+                  self.workspace(T), logit_bias=self.logit_bias, aux_out=aux,
+                  expert_counts=expert_counts, logits_out=logits_out, stream=stream)
+        return y, aux
+
+    __call__ = forward

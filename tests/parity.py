@@ -1,0 +1,140 @@
+"""Helpers of the GPU parity tests: run libmoe through its C ABI on stored
+inputs, run the oracle on the same inputs, compare.
+
+Tolerances (end-to-end layer output y against the fp64 oracle):
+  bf16 layers: max |dy| <= 2e-2 and ||dy||_F / ||y||_F <= 5e-3
+  fp32 layers: max |dy| <= 1e-4
+Routing indices, counts, offsets, drop decisions and the dispatch layout are
+compared bit-exactly when both sides route from the same fp32 logits.
+"""
+from __future__ import annotations
+
+import numpy as np
+import torch
+
+from oracle import moe_oracle as O
+from sparse_mixture_experts_71_b300 import binding as B
+from sparse_mixture_experts_71_b300.layer import device_inputs
+
+BF16_MAX_ABS, BF16_REL_FRO, F32_MAX_ABS = 2e-2, 5e-3, 1e-4
+NEAR_TIE = 1e-6
+
+
+def cfg_of(wl):
+    return B.config(wl.T, wl.d, wl.F, wl.E, wl.k, wl.dtype, wl.capacity, wl.renormalize)
+
+
+def y_error(y_gpu: np.ndarray, y_ref: np.ndarray):
+    d = y_gpu.astype(np.float64) - y_ref
+    max_abs = float(np.max(np.abs(d))) if d.size else 0.0
+    nrm = float(np.linalg.norm(y_ref))
+    rel = float(np.linalg.norm(d)) / nrm if nrm > 0 else float(np.linalg.norm(d))
+    return max_abs, rel
+
+
+def assert_y_close(y_gpu, y_ref, dtype):
+    max_abs, rel = y_error(y_gpu, y_ref)
+    if dtype == "f32":
+        assert max_abs <= F32_MAX_ABS, f"max abs {max_abs:.3e}"
+    else:
+        assert max_abs <= BF16_MAX_ABS and rel <= BF16_REL_FRO, f"max abs {max_abs:.3e} rel {rel:.3e}"
+    return max_abs, rel
+
+
+def near_tie_tokens(probs: np.ndarray, k: int) -> np.ndarray:
+    """Tokens whose k-th and (k+1)-th largest probabilities differ by < 1e-6."""
+    E = probs.shape[1]
+    if k >= E:
+        return np.zeros(probs.shape[0], bool)
+    s = -np.sort(-probs, axis=1)
+    return (s[:, k - 1] - s[:, k]) < NEAR_TIE
+
+
+def to_np(t: torch.Tensor) -> np.ndarray:
+    if t.dtype == torch.bfloat16:
+        t = t.float()
+    return t.detach().cpu().numpy()
+
+
+class GpuRun:
+    """Every stage of one layer call through the C ABI, with its outputs."""
+
+    def __init__(self, wl, inp, dev=None, stream=None):
+        self.wl, self.inp = wl, inp
+        self.dev = dev if dev is not None else device_inputs(inp)
+        self.cfg = cfg_of(wl)
+        self.ws = B.workspace(self.cfg)
+        self.stream = stream
+
+    def staged(self, logits_in=None):
+        wl, D, T, k, E = self.wl, self.dev, self.wl.T, self.wl.k, self.wl.E
+        dt = D["x"].dtype
+        cuda = D["x"].device
+        n = T * k
+        r = {}
+        r["logits"] = torch.empty((T, E), dtype=torch.float32, device=cuda)
+        r["idx"] = torch.empty((T, k), dtype=torch.int32, device=cuda)
+        r["w"] = torch.empty((T, k), dtype=torch.float32, device=cuda)
+        r["counts"] = torch.empty(E, dtype=torch.int32, device=cuda)
+        r["aux"] = torch.empty(1, dtype=torch.float32, device=cuda)
+        B.route(self.cfg, D["x"], D["W_r"], r["idx"], r["w"], self.ws, logit_bias=D["logit_bias"],
+                logits_in=logits_in, logits_out=r["logits"], expert_counts=r["counts"],
+                aux_out=r["aux"], stream=self.stream)
+        r["offsets"] = torch.empty(E + 1, dtype=torch.int32, device=cuda)
+        r["slot_of"] = torch.empty((T, k), dtype=torch.int32, device=cuda)
+        r["perm_token"] = torch.full((max(n, 1),), -7, dtype=torch.int32, device=cuda)
+        r["perm_w"] = torch.empty(max(n, 1), dtype=torch.float32, device=cuda)
+        r["x_perm"] = torch.empty((max(n, 1), wl.d), dtype=dt, device=cuda)
+        B.dispatch(self.cfg, D["x"], r["idx"], r["offsets"], r["slot_of"], r["perm_token"],
+                   r["x_perm"], self.ws, topk_w=r["w"], perm_w=r["perm_w"], stream=self.stream)
+        r["y_perm"] = torch.empty((max(n, 1), wl.d), dtype=torch.float32, device=cuda)
+        B.expert_ffn(self.cfg, r["x_perm"], r["offsets"], D["W1"], D["b1"], D["W2"], D["b2"],
+                     r["y_perm"], self.ws, perm_w=r["perm_w"], stream=self.stream)
+        r["y"] = torch.empty((T, wl.d), dtype=dt, device=cuda)
+        B.combine(self.cfg, r["y_perm"], r["slot_of"], r["y"], stream=self.stream)
+        torch.cuda.synchronize()
+        return r
+
+    def forward(self):
+        D, wl = self.dev, self.wl
+        y = torch.empty_like(D["x"])
+        aux = torch.empty(1, dtype=torch.float32, device=y.device)
+        counts = torch.empty(wl.E, dtype=torch.int32, device=y.device)
+        logits = torch.empty((wl.T, wl.E), dtype=torch.float32, device=y.device)
+        B.forward(self.cfg, D["x"], D["W_r"], D["W1"], D["b1"], D["W2"], D["b2"], y, self.ws,
+                  logit_bias=D["logit_bias"], aux_out=aux, expert_counts=counts,
+                  logits_out=logits, stream=self.stream)
+        torch.cuda.synchronize()
+        return dict(y=y, aux=aux, counts=counts, logits=logits)
+
+
+def oracle_on(inp, wl, logits=None, tokens=None, layout=True):
+    """The oracle on stored inputs (optionally routing from given fp32 logits)."""
+    return O.moe_forward(inp.as_f32("x"), inp.W_r, inp.as_f32("W1"), inp.as_f32("b1"),
+                         inp.as_f32("W2"), inp.as_f32("b2"), k=wl.k,
+                         renormalize=wl.renormalize, capacity=wl.capacity,
+                         logit_bias=inp.logit_bias, logits=logits, tokens=tokens, layout=layout)
+
+
+def sample_tokens(wl, ref_route, n: int, seed: int = 0) -> np.ndarray:
+    """A seeded token sample covering every non-empty expert and, under a cap,
+    the last kept and first dropped tokens of every expert that overflowed."""
+    g = np.random.default_rng(seed)
+    T = wl.T
+    pick = set(g.choice(T, size=min(n, T), replace=False).tolist())
+    idx, kept = ref_route.idx, ref_route.kept
+    for e in range(wl.E):
+        toks = np.nonzero((idx == e).any(axis=1))[0]
+        if toks.size:
+            pick.add(int(toks[0]))
+            pick.add(int(toks[-1]))
+        if wl.capacity is not None:
+            sel = (idx == e)
+            kt = np.nonzero((sel & kept).any(axis=1))[0]
+            dt = np.nonzero((sel & ~kept).any(axis=1))[0]
+            if kt.size:
+                pick.add(int(kt[-1]))
+            if dt.size:
+                pick.add(int(dt[0]))
+                pick.add(int(dt[-1]))
+    return np.array(sorted(pick), np.int64)

@@ -1,0 +1,95 @@
+"""The C-ABI library without a GPU: it loads, exports every symbol the header
+declares, sizes workspaces, and rejects invalid calls on the host before any
+launch (only argument combinations that fail validation are passed here)."""
+import ctypes
+import os
+import re
+
+import pytest
+
+from sparse_mixture_experts_71_b300 import binding as B
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+def _declared():
+    names = set()
+    for fn in os.listdir(os.path.join(ROOT, "include")):
+        if fn.endswith(".h"):
+            src = open(os.path.join(ROOT, "include", fn)).read()
+            src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+            names |= set(re.findall(r"\b(moe_\w+)\s*\(", src))
+    return names
+
+
+def test_library_exports_every_declared_symbol():
+    lib = B.load()
+    declared = _declared()
+    assert {"moe_route", "moe_dispatch", "moe_expert_ffn", "moe_combine", "moe_forward"} <= declared
+    for name in declared:
+        assert hasattr(lib, name), name
+    assert set(B.EXPORTED) == declared
+
+
+def test_status_strings():
+    lib = B.load()
+    for code, text in B.STATUS.items():
+        assert lib.moe_status_string(code).decode() == text
+
+
+def test_workspace_size():
+    c = B.config(4096, 1024, 4096, 8, 2)
+    n = B.workspace_size(c)
+    # at least the permuted rows, the hidden activations and the fp32 expert outputs
+    assert n >= 8192 * (1024 * 2 + 4096 * 2 + 1024 * 4)
+    assert n % 256 == 0
+    capped = B.workspace_size(B.config(4096, 1024, 4096, 8, 2, capacity=100))
+    assert capped < n
+    assert B.workspace_size(B.config(4096, 1024, 4096, 8, 9)) == 0  # k > E
+    assert B.workspace_size(B.config(0, 64, 64, 4, 2)) > 0
+
+
+FAKE = 1 << 20  # a 256-aligned address that is never dereferenced (calls fail first)
+
+
+@pytest.mark.parametrize("cfg,status", [
+    (None, 1),
+    (B.config(16, 64, 64, 4, 5), 1),            # k > E
+    (B.config(16, 64, 64, 300, 2), 4),          # E > 256
+    (B.config(16, 64, 64, 16, 9), 4),           # k > 8
+    (B.config(16, 60, 64, 4, 2), 2),            # d not a multiple of 8
+    (B.config(16, 64, 68, 4, 2), 2),            # d_ff not a multiple of 8
+    (B.config(-1, 64, 64, 4, 2), 1),            # T < 0
+])
+def test_forward_rejects_bad_config(cfg, status):
+    lib = B.load()
+    ref = ctypes.byref(cfg) if cfg is not None else None
+    st = lib.moe_forward(ref, FAKE, FAKE, None, FAKE, FAKE, FAKE, FAKE, FAKE, None, None, None,
+                         FAKE, 1 << 40, None)
+    assert st == status
+
+
+def test_calls_reject_null_misaligned_and_small_workspace():
+    lib = B.load()
+    c = B.config(16, 64, 64, 4, 2)
+    cr = ctypes.byref(c)
+    need = B.workspace_size(c)
+    # null required pointer
+    assert lib.moe_forward(cr, None, FAKE, None, FAKE, FAKE, FAKE, FAKE, FAKE, None, None, None,
+                           FAKE, need, None) == 1
+    # misaligned x
+    assert lib.moe_forward(cr, FAKE + 8, FAKE, None, FAKE, FAKE, FAKE, FAKE, FAKE, None, None,
+                           None, FAKE, need, None) == 2
+    # workspace too small / misaligned
+    assert lib.moe_forward(cr, FAKE, FAKE, None, FAKE, FAKE, FAKE, FAKE, FAKE, None, None, None,
+                           FAKE, need - 1, None) == 3
+    assert lib.moe_forward(cr, FAKE, FAKE, None, FAKE, FAKE, FAKE, FAKE, FAKE, None, None, None,
+                           FAKE + 16, need, None) == 3
+    assert lib.moe_route(cr, FAKE, FAKE, None, None, None, None, FAKE, None, None, FAKE, need,
+                         None) == 1
+    assert lib.moe_dispatch(cr, FAKE, FAKE, None, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, need,
+                            None) == 1  # perm_w without topk_w
+    assert lib.moe_expert_ffn(cr, FAKE, FAKE, FAKE, FAKE, FAKE + 4, FAKE, None, FAKE, FAKE, need,
+                              None) == 2
+    assert lib.moe_combine(cr, FAKE, None, FAKE, None) == 1
+    assert lib.moe_get_device_error(None, None, None, None) == 1

@@ -1,0 +1,115 @@
+"""GPU parity on small and degenerate shapes: ragged token counts, one
+expert, k = E, many experts, capacity 0 / 1 / >= T, empty experts, empty
+batch, fp32 and bf16, plus the device-side error record."""
+import numpy as np
+import pytest
+import torch
+
+from parity import GpuRun, assert_y_close, oracle_on, to_np
+from sparse_mixture_experts_71_b300 import binding as B
+from sparse_mixture_experts_71_b300 import inputs as I
+
+pytestmark = pytest.mark.gpu
+
+CASES = [
+    # name, T, d, F, E, k, dtype, capacity, renormalize
+    ("t1", 1, 64, 128, 8, 2, "bf16", None, True),
+    ("t63-f32", 63, 64, 96, 8, 2, "f32", None, True),
+    ("t65-ragged", 65, 24, 40, 5, 2, "bf16", None, True),
+    ("e1-dense", 100, 32, 64, 1, 1, "f32", None, True),
+    ("k-eq-e", 70, 32, 64, 4, 4, "f32", None, True),
+    ("e64-top1-cap", 300, 64, 128, 64, 1, "bf16", 3, False),
+    ("e256-top8", 130, 32, 64, 256, 8, "bf16", None, True),
+    ("e200-top3-cap", 257, 40, 48, 200, 3, "f32", 2, True),
+    ("cap0", 50, 32, 64, 4, 2, "bf16", 0, True),
+    ("cap1-k2", 77, 32, 64, 3, 2, "f32", 1, True),
+    ("cap-ge-T", 90, 32, 64, 4, 2, "bf16", 90, True),
+    ("no-renorm-k2", 64, 64, 64, 8, 2, "f32", None, False),
+    ("big-rows", 2000, 256, 512, 16, 2, "bf16", 200, True),
+]
+
+
+def _wl(name, T, d, F, E, k, dtype, cap, renorm, zipf=0.0):
+    return I.Workload(name, T, d, F, E, k, dtype=dtype, renormalize=renorm, capacity=cap,
+                      zipf_bias=zipf, init="uniform" if dtype == "f32" else "normal")
+
+
+def _check(wl, inp, r):
+    g_logits = to_np(r["logits"])
+    ref = oracle_on(inp, wl, logits=g_logits)
+    assert np.array_equal(to_np(r["idx"]), ref.idx)
+    assert np.array_equal(to_np(r["counts"]), ref.counts)
+    assert np.array_equal(to_np(r["offsets"]), ref.offsets)
+    assert np.array_equal(to_np(r["slot_of"]), ref.slot_of)
+    nk = int(ref.offsets[-1])
+    assert np.array_equal(to_np(r["perm_token"])[:nk], ref.perm_token)
+    assert abs(float(r["aux"][0]) - ref.aux) <= 1e-5 * max(1.0, ref.aux)
+    assert_y_close(to_np(r["y"]), ref.y, wl.dtype)
+    return ref
+
+
+@pytest.mark.parametrize("case", CASES, ids=[c[0] for c in CASES])
+def test_small_shapes(case):
+    wl = _wl(*case)
+    inp = I.make_inputs(wl, seed=11)
+    run = GpuRun(wl, inp)
+    r = run.staged()
+    ref = _check(wl, inp, r)
+    if wl.capacity == 0:
+        assert not torch.any(r["y"].float() != 0)
+    f = run.forward()
+    assert torch.equal(f["y"], r["y"])
+    assert B.get_device_error(run.ws)[0] == 0
+    del ref
+
+
+def test_empty_experts_and_zipf_skew():
+    """A strong per-expert logit bias leaves most experts empty."""
+    wl = _wl("zipf", 500, 64, 128, 16, 1, "bf16", 40, False, zipf=6.0)
+    inp = I.make_inputs(wl, seed=3)
+    r = GpuRun(wl, inp).staged()
+    ref = _check(wl, inp, r)
+    assert np.sum(ref.counts == 0) >= 4 and np.any(~ref.kept)
+
+
+def test_logits_in_routes_identically():
+    """Routing from caller-given logits: ties go to the lower expert index."""
+    wl = _wl("ties", 96, 32, 64, 8, 3, "f32", None, True)
+    inp = I.make_inputs(wl, seed=5)
+    logits = np.round(np.random.default_rng(0).standard_normal((96, 8)), 1).astype(np.float32)
+    logits[::3, 5] = logits[::3, 2]  # exact ties
+    run = GpuRun(wl, inp)
+    r = run.staged(logits_in=torch.from_numpy(logits).cuda())
+    assert np.array_equal(to_np(r["logits"]), logits)
+    ref = oracle_on(inp, wl, logits=logits)
+    assert np.array_equal(to_np(r["idx"]), ref.idx)
+    assert_y_close(to_np(r["y"]), ref.y, wl.dtype)
+
+
+def test_empty_batch():
+    wl = _wl("t0", 0, 32, 64, 4, 2, "bf16", None, True)
+    inp = I.make_inputs(wl, seed=0)
+    run = GpuRun(wl, inp)
+    r = run.staged()
+    assert float(r["aux"][0]) == 0.0 and not torch.any(r["counts"] != 0)
+    assert not torch.any(r["offsets"] != 0)
+
+
+def test_out_of_range_expert_is_flagged_not_written():
+    """An expert index outside [0, E) given to moe_dispatch is skipped and
+    recorded in the workspace; the other assignments are still dispatched."""
+    wl = _wl("bad-idx", 40, 32, 64, 4, 2, "bf16", None, True)
+    inp = I.make_inputs(wl, seed=1)
+    run = GpuRun(wl, inp)
+    r = run.staged()
+    idx = r["idx"].clone()
+    idx[7, 1] = 9
+    off = torch.empty(5, dtype=torch.int32, device="cuda")
+    slot = torch.empty((40, 2), dtype=torch.int32, device="cuda")
+    perm = torch.empty(80, dtype=torch.int32, device="cuda")
+    xp = torch.empty((80, 32), dtype=torch.bfloat16, device="cuda")
+    B.dispatch(run.cfg, run.dev["x"], idx, off, slot, perm, xp, run.ws)
+    st, code, info = B.get_device_error(run.ws)
+    assert (st, code, info) == (6, 1, 7 * 2 + 1)
+    assert int(slot[7, 1]) == -1 and int(off[-1]) == 79
+    assert B.get_device_error(run.ws)[0] == 0  # the record was cleared
