@@ -133,13 +133,27 @@ def dist_setup():
     return world, rank, local
 
 
+def blas_threads() -> int:
+    """Threads the oracle's BLAS calls use (numpy's OpenBLAS)."""
+    try:
+        from threadpoolctl import threadpool_info
+        n = [p.get("num_threads", 1) for p in threadpool_info() if p.get("user_api") == "blas"]
+        if n:
+            return max(n)
+    except Exception:
+        pass
+    for var in ("OPENBLAS_NUM_THREADS", "OMP_NUM_THREADS"):
+        if os.environ.get(var, "").isdigit():
+            return int(os.environ[var])
+    return os.cpu_count() or 1
+
+
 def cpu_oracle_rate(wl, inp, budget_s: float, min_tokens: int = 64):
     """Tokens/s of the oracle on a token sample sized to the time budget.
 
     The sample is the first n tokens of the batch taken as a batch of its own
     (routing, experts, combine and loss all run on it)."""
     from oracle import moe_oracle as O
-    from threadpoolctl import threadpool_info
     x = inp.as_f32("x")
     W1, b1, W2, b2 = (inp.as_f32(n) for n in ("W1", "b1", "W2", "b2"))
 
@@ -153,8 +167,7 @@ def cpu_oracle_rate(wl, inp, budget_s: float, min_tokens: int = 64):
     t0 = run(n0)
     n = int(min(wl.T, max(min_tokens, n0 * budget_s / max(t0, 1e-6))))
     t = run(n) if n != n0 else t0
-    threads = max([p.get("num_threads", 1) for p in threadpool_info()] + [1])
-    return n / t, n, t, threads
+    return n / t, n, t, blas_threads()
 
 
 def bench_reference(args, wl):
@@ -164,7 +177,6 @@ def bench_reference(args, wl):
     inp = I.make_inputs(wl, seed=0)
     per_step = max(0.5, 150.0 / max(1, args.steps + args.warmup))
     from oracle import moe_oracle as O
-    from threadpoolctl import threadpool_info
     x = inp.as_f32("x")
     W1, b1, W2, b2 = (inp.as_f32(n) for n in ("W1", "b1", "W2", "b2"))
     # size the per-step sample from one probe step
@@ -182,7 +194,6 @@ def bench_reference(args, wl):
         t0 = time.perf_counter()
         step()
         times.append(time.perf_counter() - t0)
-    threads = max([p.get("num_threads", 1) for p in threadpool_info()] + [threads])
     total = sum(times)
     value = n * args.steps / total
     sample = f"first {n} of {wl.T} tokens as a batch of their own, per step"

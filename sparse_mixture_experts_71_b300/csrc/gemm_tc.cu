@@ -1,0 +1,432 @@
+// Grouped expert GEMMs on the 5th-generation tensor cores (tcgen05 + TMEM),
+// fed by TMA.
+//
+// "Mixture of Experts: Scaling Parameters Without Scaling Compute", section
+// "The MoE layer": each expert is Linear(d, d_ff) + bias, GELU,
+// Linear(d_ff, d) + bias, applied to the token rows dispatched to it; the
+// weighted combination of the expert outputs follows (the routing weight is
+// applied here, in the second GEMM's epilogue).
+//
+// Orientation ("weights as the M operand"): for expert e and a tile of its
+// token rows r0 .. r0+n-1,
+//     D[f][j] = sum_k W[e][f][k] * X[r0 + j][k]      (f: 128 weight rows)
+// so the 128-row MMA dimension is always full (weight rows) and the token
+// dimension N is set per tile at run time to n rounded up to 16 (the
+// instruction descriptor is a register operand).  Small expert segments
+// (decode, skewed routing) then cost MMA work in proportion to their size.
+//
+// Persistent, warp-specialised kernel (one CTA per SM, 12 warps):
+//   warp 0      TMA producer: per K-step one 128x64 box of W and ceil(n/32)
+//               32x64 boxes of X into a STAGES-deep shared-memory ring
+//               (128-byte swizzle), completion counted on a full barrier;
+//   warp 1      MMA issuer: 4 tcgen05.mma (K=16 each) per stage into one of
+//               two TMEM accumulators; tcgen05.commit frees the stage and,
+//               after the last K-step, signals the epilogue;
+//   warp 2      TMEM allocator;
+//   warp 3      computes the per-expert tile table from the device offsets;
+//   warps 4-11  epilogue: tcgen05.ld of 32 columns per warp (lane quarter
+//               warp%4, column half by warp group), bias + exact GELU
+//               (GEMM1, bf16 out) or bias x routing weight (GEMM2, fp32 out),
+//               transposed through shared memory into 16-byte row stores.
+// The two TMEM accumulators let the epilogue of tile i overlap the MMAs of
+// tile i+1.  Every wait is bounded: past the time limit the kernel records
+// an error in the workspace, drains its in-flight copies and MMAs, frees TMEM
+// and returns.
+
+#include <cuda.h>
+#include <cudaTypedefs.h>
+#include <cuda_runtime.h>
+
+#include "moe_device.cuh"
+#include "moe_internal.h"
+#include "tc_ptx.cuh"
+
+namespace moe {
+namespace {
+
+constexpr int kThreads = 384;
+constexpr int kEpiWarps = 8;
+constexpr int BM = 128;                      // weight rows per tile (MMA M)
+constexpr int BK = 64;                       // K per stage: one 128-byte swizzle row
+constexpr int A_BYTES = BM * BK * 2;         // 16 KB
+constexpr int BOX_ROWS = 32;                 // token rows per TMA box
+constexpr int BOX_BYTES = BOX_ROWS * BK * 2; // 4 KB
+constexpr uint64_t kDrainNs = 2000000000ull; // drain waits on the error path
+
+template <int BN_MAX, int STAGES, bool GEMM1>
+struct Cfg {
+    static constexpr int B_BYTES = BN_MAX * BK * 2;
+    static constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
+    static constexpr int OUT_ES = GEMM1 ? 2 : 4;
+    static constexpr int STAGING = kEpiWarps * 32 * 32 * OUT_ES;
+    static constexpr int TMEM_COLS = 2 * BN_MAX;
+    static constexpr int OFF_STAGING = STAGES * STAGE_BYTES;
+    static constexpr int OFF_BARS = OFF_STAGING + STAGING;
+    static constexpr int NUM_BARS = 2 * STAGES + 5;
+    static constexpr int OFF_MISC = OFF_BARS + NUM_BARS * 8;
+    static constexpr int OFF_TILES = OFF_MISC + 16;
+    static constexpr int SMEM = OFF_TILES + (kMaxExperts + 1) * 4 + 1023;
+    static_assert(STAGE_BYTES % 1024 == 0, "stage alignment");
+    static_assert(SMEM <= 232448, "shared memory budget");
+    static_assert(TMEM_COLS == 128 || TMEM_COLS == 512, "TMEM allocation");
+};
+
+struct Params {
+    const int32_t* offsets;     // [E+1] segment starts (device)
+    const __nv_bfloat16* bias;  // [E][n_out]
+    const float* row_w;         // [rows] routing weight per row (second GEMM) or null
+    void* out;                  // first GEMM: bf16 [rows][n_out]; second: fp32 [rows][n_out]
+    DeviceHeader* hdr;
+    uint64_t timeout_ns;
+    int E, n_out, K, rows_cap;
+};
+
+struct Tile {
+    int e, r0, n, m0;
+};
+
+__device__ __forceinline__ Tile decode_tile(int t, const int* s_tiles, const Params& p, int mt,
+                                            int bn_max) {
+    int lo = 0, hi = p.E - 1;
+    while (lo < hi) {  // last expert whose first tile is <= t
+        const int mid = (lo + hi + 1) >> 1;
+        if (s_tiles[mid] <= t) lo = mid; else hi = mid - 1;
+    }
+    Tile tl;
+    tl.e = lo;
+    const int local = t - s_tiles[lo];
+    const int s0 = min(max(__ldg(p.offsets + lo), 0), p.rows_cap);
+    const int s1 = min(max(__ldg(p.offsets + lo + 1), s0), p.rows_cap);
+    const int nt = (s1 - s0 + bn_max - 1) / bn_max;
+    const int ti = local % nt, mi = local / nt;  // token tile fastest
+    tl.r0 = s0 + ti * bn_max;
+    tl.n = min(bn_max, s1 - tl.r0);
+    tl.m0 = mi * BM;
+    (void)mt;
+    return tl;
+}
+
+// Wait for phase `parity` of `bar`; false if the kernel is aborting or the
+// time limit passed (then the abort flag is raised and the error recorded).
+__device__ __forceinline__ bool wait_bar(uint64_t* bar, uint32_t parity, volatile int* abort_flag,
+                                         const Params& p, int where) {
+    if (tc::mbar_try_wait(bar, parity)) return true;
+    const uint64_t t0 = tc::globaltimer();
+    while (!tc::mbar_try_wait(bar, parity)) {
+        if (*abort_flag) return false;
+        if (tc::globaltimer() - t0 > p.timeout_ns) {
+            *abort_flag = 1;
+            record_error(p.hdr, kErrTimeout, where);
+            return false;
+        }
+    }
+    return true;
+}
+
+// Drain wait: bounded by a fixed limit only (used on the way out).
+__device__ __forceinline__ void drain_bar(uint64_t* bar, uint32_t parity) {
+    const uint64_t t0 = tc::globaltimer();
+    while (!tc::mbar_try_wait(bar, parity)) {
+        if (tc::globaltimer() - t0 > kDrainNs) break;
+    }
+}
+
+template <int BN_MAX, int STAGES, bool GEMM1>
+__global__ void __launch_bounds__(kThreads, 1)
+grouped_gemm_tc(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
+                const Params p) {
+    using C = Cfg<BN_MAX, STAGES, GEMM1>;
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t* smem = reinterpret_cast<uint8_t*>(
+        (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    uint64_t* full = reinterpret_cast<uint64_t*>(smem + C::OFF_BARS);
+    uint64_t* empty = full + STAGES;
+    uint64_t* tfull = empty + STAGES;
+    uint64_t* tempty = tfull + 2;
+    uint64_t* drain = tempty + 2;
+    uint32_t* s_tmem = reinterpret_cast<uint32_t*>(smem + C::OFF_MISC);
+    volatile int* s_abort = reinterpret_cast<volatile int*>(smem + C::OFF_MISC + 4);
+    int* s_tiles = reinterpret_cast<int*>(smem + C::OFF_TILES);
+
+    const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
+    const int mt = (p.n_out + BM - 1) / BM;
+    const int KB = (p.K + BK - 1) / BK;
+
+    if (warp == 0 && lane == 0) {
+        for (int s = 0; s < STAGES; ++s) {
+            tc::mbar_init(&full[s], 1);
+            tc::mbar_init(&empty[s], 1);
+        }
+        for (int a = 0; a < 2; ++a) {
+            tc::mbar_init(&tfull[a], 1);
+            tc::mbar_init(&tempty[a], kEpiWarps);
+        }
+        tc::mbar_init(drain, 1);
+        *s_abort = 0;
+        tc::fence_barrier_init();
+        tc::tma_prefetch_desc(&tmA);
+        tc::tma_prefetch_desc(&tmB);
+    }
+    if (warp == 2) {
+        tc::tmem_alloc(s_tmem, C::TMEM_COLS);
+        tc::tmem_relinquish();
+    }
+    if (warp == 3) {  // exclusive prefix of tiles per expert
+        int run = 0;
+        for (int e0 = 0; e0 < p.E; e0 += 32) {
+            const int e = e0 + lane;
+            int nt = 0;
+            if (e < p.E) {
+                const int s0 = min(max(__ldg(p.offsets + e), 0), p.rows_cap);
+                const int s1 = min(max(__ldg(p.offsets + e + 1), s0), p.rows_cap);
+                nt = ((s1 - s0 + BN_MAX - 1) / BN_MAX) * mt;
+            }
+            int v = nt;
+#pragma unroll
+            for (int o = 1; o < 32; o <<= 1) {
+                const int u = __shfl_up_sync(0xffffffffu, v, o);
+                if (lane >= o) v += u;
+            }
+            if (e < p.E) s_tiles[e] = run + v - nt;
+            run += __shfl_sync(0xffffffffu, v, 31);
+        }
+        if (lane == 0) s_tiles[p.E] = run;
+    }
+    tc::fence_before_sync();
+    __syncthreads();
+    tc::fence_after_sync();
+    const uint32_t tmem_base = *s_tmem;
+    const int total = s_tiles[p.E];
+
+    if (warp == 0) {
+        // ------------------------------------------------ TMA producer
+        if (lane == 0) {
+            int stage = 0;
+            uint32_t phase = 0;
+            long long fills = 0;
+            bool ok = true;
+            for (int t = blockIdx.x; t < total && ok; t += gridDim.x) {
+                const Tile tl = decode_tile(t, s_tiles, p, mt, BN_MAX);
+                const int nb = (tl.n + BOX_ROWS - 1) / BOX_ROWS;
+                const uint32_t bytes = A_BYTES + nb * BOX_BYTES;
+                const int arow = tl.e * p.n_out + tl.m0;
+                for (int kb = 0; kb < KB; ++kb) {
+                    if (!wait_bar(&empty[stage], phase ^ 1, s_abort, p, 1)) { ok = false; break; }
+                    tc::mbar_expect_tx(&full[stage], bytes);
+                    uint8_t* sa = smem + stage * C::STAGE_BYTES;
+                    uint8_t* sb = sa + A_BYTES;
+                    tc::tma_load_2d(sa, &tmA, &full[stage], kb * BK, arow);
+                    for (int b = 0; b < nb; ++b)
+                        tc::tma_load_2d(sb + b * BOX_BYTES, &tmB, &full[stage], kb * BK,
+                                        tl.r0 + b * BOX_ROWS);
+                    ++fills;
+                    if (++stage == STAGES) { stage = 0; phase ^= 1; }
+                }
+            }
+            // every issued copy lands before the CTA can exit
+            const long long last = fills < STAGES ? fills : STAGES;
+            for (long long i = fills - last; i < fills; ++i)
+                drain_bar(&full[i % STAGES], (uint32_t)((i / STAGES) & 1));
+        }
+    } else if (warp == 1) {
+        // ------------------------------------------------ MMA issuer
+        if (lane == 0) {
+            int stage = 0, acc = 0;
+            uint32_t phase = 0, acc_phase = 0;
+            bool ok = true;
+            for (int t = blockIdx.x; t < total && ok; t += gridDim.x) {
+                const Tile tl = decode_tile(t, s_tiles, p, mt, BN_MAX);
+                const uint32_t n_mma = (uint32_t)((tl.n + 15) / 16) * 16;
+                const uint32_t idesc = tc::idesc_bf16_f32(BM, n_mma);
+                if (!wait_bar(&tempty[acc], acc_phase ^ 1, s_abort, p, 2)) break;
+                tc::fence_after_sync();
+                const uint32_t d_tmem = tmem_base + (uint32_t)(acc * BN_MAX);
+                for (int kb = 0; kb < KB; ++kb) {
+                    if (!wait_bar(&full[stage], phase, s_abort, p, 3)) { ok = false; break; }
+                    tc::fence_after_sync();
+                    const uint32_t sa = tc::smem_u32(smem + stage * C::STAGE_BYTES);
+                    const uint32_t sb = sa + A_BYTES;
+#pragma unroll
+                    for (int kk = 0; kk < BK / 16; ++kk) {
+                        tc::mma_bf16(d_tmem, tc::sdesc_k128_sw128(sa + kk * 32),
+                                     tc::sdesc_k128_sw128(sb + kk * 32), idesc,
+                                     (kb | kk) != 0 ? 1u : 0u);
+                    }
+                    tc::mma_commit(&empty[stage]);
+                    if (++stage == STAGES) { stage = 0; phase ^= 1; }
+                }
+                if (!ok) break;
+                tc::mma_commit(&tfull[acc]);
+                acc ^= 1;
+                if (acc == 0) acc_phase ^= 1;
+            }
+            // every issued MMA completes before TMEM is freed
+            tc::mma_commit(drain);
+            drain_bar(drain, 0);
+        }
+    } else if (warp >= 4) {
+        // ------------------------------------------------ epilogue
+        const int ew = warp - 4;
+        const int q = warp & 3;        // TMEM lane quarter this warp may access
+        const int half = ew >> 2;      // which half of the tile's columns
+        uint8_t* stg = smem + C::OFF_STAGING + ew * 32 * 32 * C::OUT_ES;
+        int acc = 0;
+        uint32_t acc_phase = 0;
+        for (int t = blockIdx.x; t < total; t += gridDim.x) {
+            const Tile tl = decode_tile(t, s_tiles, p, mt, BN_MAX);
+            const bool ok = wait_bar(&tfull[acc], acc_phase, s_abort, p, 4);
+            if (!__all_sync(0xffffffffu, ok)) break;
+            tc::fence_after_sync();
+            const int f0 = tl.m0 + q * 32;  // first weight row (output feature) of this warp
+            const int f = f0 + lane;
+            const float bias =
+                f < p.n_out ? __bfloat162float(p.bias[(size_t)tl.e * p.n_out + f]) : 0.f;
+            const int c_begin = half * (BN_MAX / 2), c_end = min(c_begin + BN_MAX / 2, tl.n);
+            for (int c = c_begin; c < c_end; c += 32) {
+                float v[32];
+                tc::tmem_ld_32cols(tmem_base + ((uint32_t)(q * 32) << 16) +
+                                       (uint32_t)(acc * BN_MAX + c),
+                                   v);
+                const int rows_here = min(32, tl.n - c);
+                if (GEMM1) {
+                    __nv_bfloat16* s16 = reinterpret_cast<__nv_bfloat16*>(stg);
+#pragma unroll
+                    for (int j = 0; j < 32; ++j)
+                        s16[j * 32 + lane] = __float2bfloat16_rn(gelu_erf(v[j] + bias));
+                    __syncwarp();
+                    __nv_bfloat16* out = reinterpret_cast<__nv_bfloat16*>(p.out);
+#pragma unroll
+                    for (int i = 0; i < 4; ++i) {
+                        const int ci = lane + 32 * i, j = ci >> 2, part = ci & 3;
+                        const int fc = f0 + part * 8;
+                        if (j < rows_here && fc < p.n_out) {
+                            const uint4 val = *reinterpret_cast<const uint4*>(stg + j * 64 + part * 16);
+                            *reinterpret_cast<uint4*>(out + (size_t)(tl.r0 + c + j) * p.n_out + fc) = val;
+                        }
+                    }
+                } else {
+                    float wl = 1.f;
+                    if (p.row_w != nullptr && lane < rows_here) wl = __ldg(p.row_w + tl.r0 + c + lane);
+                    float* s32 = reinterpret_cast<float*>(stg);
+#pragma unroll
+                    for (int j = 0; j < 32; ++j)
+                        s32[j * 32 + lane] = (v[j] + bias) * __shfl_sync(0xffffffffu, wl, j);
+                    __syncwarp();
+                    float* out = reinterpret_cast<float*>(p.out);
+#pragma unroll
+                    for (int i = 0; i < 8; ++i) {
+                        const int ci = lane + 32 * i, j = ci >> 3, part = ci & 7;
+                        const int fc = f0 + part * 4;
+                        if (j < rows_here && fc < p.n_out) {
+                            const float4 val = *reinterpret_cast<const float4*>(stg + j * 128 + part * 16);
+                            *reinterpret_cast<float4*>(out + (size_t)(tl.r0 + c + j) * p.n_out + fc) = val;
+                        }
+                    }
+                }
+                __syncwarp();
+            }
+            tc::fence_before_sync();
+            __syncwarp();
+            if (lane == 0) tc::mbar_arrive(&tempty[acc]);
+            acc ^= 1;
+            if (acc == 0) acc_phase ^= 1;
+        }
+    }
+
+    tc::fence_before_sync();
+    __syncthreads();
+    if (warp == 2) {
+        tc::fence_after_sync();
+        tc::tmem_dealloc(tmem_base, C::TMEM_COLS);
+    }
+}
+
+PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
+    static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+    if (fn == nullptr) {
+        void* ptr = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000,
+                                             cudaEnableDefault, &q) == cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(ptr);
+    }
+    return fn;
+}
+
+// Row-major bf16 matrix [outer][inner] as a 2-D TMA map with 128-byte swizzle
+// and boxes of box_outer rows x 64 columns; out-of-range elements read as 0.
+bool make_map(CUtensorMap* m, const void* base, uint64_t inner, uint64_t outer,
+              uint32_t box_outer) {
+    auto fn = encode_fn();
+    if (fn == nullptr) return false;
+    cuuint64_t dims[2] = {inner, outer};
+    cuuint64_t strides[1] = {inner * 2};
+    cuuint32_t box[2] = {(cuuint32_t)BK, box_outer};
+    cuuint32_t estr[2] = {1, 1};
+    return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides, box,
+              estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+              CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+int num_sms() {
+    static int sms[64] = {0};
+    int dev = 0;
+    cudaGetDevice(&dev);
+    if (dev < 0 || dev >= 64) dev = 0;
+    if (sms[dev] == 0) {
+        int v = 148;
+        cudaDeviceGetAttribute(&v, cudaDevAttrMultiProcessorCount, dev);
+        sms[dev] = v;
+    }
+    return sms[dev];
+}
+
+template <int BN_MAX, int STAGES, bool GEMM1>
+cudaError_t launch_one(const CUtensorMap& a, const CUtensorMap& b, const Params& p,
+                       cudaStream_t s) {
+    using C = Cfg<BN_MAX, STAGES, GEMM1>;
+    auto kern = grouped_gemm_tc<BN_MAX, STAGES, GEMM1>;
+    cudaError_t err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
+    if (err != cudaSuccess) return err;
+    kern<<<num_sms(), kThreads, C::SMEM, s>>>(a, b, p);
+    count_launches(1);
+    return cudaGetLastError();
+}
+
+template <int BN_MAX, int STAGES>
+cudaError_t launch_pair(const CUtensorMap* maps, const Params& p1, const Params& p2,
+                        cudaStream_t s) {
+    cudaError_t err = launch_one<BN_MAX, STAGES, true>(maps[0], maps[1], p1, s);
+    if (err != cudaSuccess) return err;
+    return launch_one<BN_MAX, STAGES, false>(maps[2], maps[3], p2, s);
+}
+
+}  // namespace
+
+uint64_t g_tc_timeout_ns = 2000000000ull;
+
+cudaError_t launch_expert_ffn_tc(const moe_config& c, const void* x_perm, int64_t x_rows,
+                                 const int32_t* offsets, const void* W1, const void* b1,
+                                 const void* W2, const void* b2, const float* perm_w,
+                                 float* y_perm, void* h, int64_t h_rows, DeviceHeader* hdr,
+                                 cudaStream_t s) {
+    if (h_rows == 0) return cudaSuccess;
+    // tokens per expert on average decides the widest token tile
+    const bool wide = (int64_t)c.T * c.k >= 96LL * c.E;
+    CUtensorMap maps[4];
+    const uint32_t box_w = BM, box_x = BOX_ROWS;
+    if (!make_map(&maps[0], W1, c.d, (uint64_t)c.E * c.d_ff, box_w) ||
+        !make_map(&maps[1], x_perm, c.d, (uint64_t)x_rows, box_x) ||
+        !make_map(&maps[2], W2, c.d_ff, (uint64_t)c.E * c.d, box_w) ||
+        !make_map(&maps[3], h, c.d_ff, (uint64_t)h_rows, box_x))
+        return cudaErrorInvalidValue;
+    Params p1{offsets, reinterpret_cast<const __nv_bfloat16*>(b1), nullptr, h, hdr,
+              g_tc_timeout_ns, c.E, c.d_ff, c.d, (int)h_rows};
+    Params p2{offsets, reinterpret_cast<const __nv_bfloat16*>(b2), perm_w, y_perm, hdr,
+              g_tc_timeout_ns, c.E, c.d, c.d_ff, (int)h_rows};
+    if (wide) return launch_pair<256, 4>(maps, p1, p2, s);
+    return launch_pair<64, 8>(maps, p1, p2, s);
+}
+
+}  // namespace moe

@@ -18,6 +18,11 @@ cudaError_t launch_expert_ffn_simt(const moe_config& c, const void* x_perm, cons
                                    const void* W1, const void* b1, const void* W2, const void* b2,
                                    const float* perm_w, float* y_perm, void* h, int64_t max_seg,
                                    int64_t max_rows, cudaStream_t s);
+cudaError_t launch_expert_ffn_tc(const moe_config& c, const void* x_perm, int64_t x_rows,
+                                 const int32_t* offsets, const void* W1, const void* b1,
+                                 const void* W2, const void* b2, const float* perm_w,
+                                 float* y_perm, void* h, int64_t h_rows, DeviceHeader* hdr,
+                                 cudaStream_t s);
 
 namespace {
 
@@ -99,10 +104,13 @@ WsLayout ws_layout(const moe_config& c) {
     return L;
 }
 
-cudaError_t launch_expert_ffn(const moe_config& c, const void* x_perm, const int32_t* offsets,
-                              const void* W1, const void* b1, const void* W2, const void* b2,
-                              const float* perm_w, float* y_perm, void* ws, const WsLayout& L,
-                              cudaStream_t s) {
+cudaError_t launch_expert_ffn(const moe_config& c, const void* x_perm, int64_t x_rows,
+                              const int32_t* offsets, const void* W1, const void* b1,
+                              const void* W2, const void* b2, const float* perm_w, float* y_perm,
+                              void* ws, const WsLayout& L, cudaStream_t s) {
+    if (c.dtype == MOE_BF16)
+        return launch_expert_ffn_tc(c, x_perm, x_rows, offsets, W1, b1, W2, b2, perm_w, y_perm,
+                                    at<void>(ws, L.h), L.rows, at<DeviceHeader>(ws, L.header), s);
     return launch_expert_ffn_simt(c, x_perm, offsets, W1, b1, W2, b2, perm_w, y_perm,
                                   at<void>(ws, L.h), max_segment(c), L.rows, s);
 }
@@ -190,7 +198,8 @@ moe_status moe_expert_ffn(const moe_config* cfg, const void* x_perm, const int32
         return MOE_ERR_ALIGNMENT;
     WsLayout L;
     if ((st = check_ws(c, ws, ws_bytes, &L)) != MOE_OK) return st;
-    return from_cuda(launch_expert_ffn(c, x_perm, offsets, W1, b1, W2, b2, perm_w, y_perm, ws, L,
+    return from_cuda(launch_expert_ffn(c, x_perm, (int64_t)c.T * c.k, offsets, W1, b1, W2, b2,
+                                       perm_w, y_perm, ws, L,
                                        reinterpret_cast<cudaStream_t>(stream)));
 }
 
@@ -235,7 +244,8 @@ moe_status moe_forward(const moe_config* cfg, const void* x, const float* W_r,
     if (e == cudaSuccess)
         e = launch_dispatch(c, x, idx, w, offsets, slot_of, perm_token, perm_w, x_perm, ws, L, s);
     if (e == cudaSuccess)
-        e = launch_expert_ffn(c, x_perm, offsets, W1, b1, W2, b2, perm_w, y_perm, ws, L, s);
+        e = launch_expert_ffn(c, x_perm, L.rows, offsets, W1, b1, W2, b2, perm_w, y_perm, ws, L,
+                              s);
     if (e == cudaSuccess) e = launch_combine(c, y_perm, slot_of, y, s);
     return from_cuda(e);
 }

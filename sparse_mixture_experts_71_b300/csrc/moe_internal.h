@@ -70,10 +70,10 @@ cudaError_t launch_dispatch(const moe_config& c, const void* x, const int32_t* t
                             int32_t* perm_token, float* perm_w, void* x_perm, void* ws,
                             const WsLayout& L, cudaStream_t s);
 
-cudaError_t launch_expert_ffn(const moe_config& c, const void* x_perm, const int32_t* offsets,
-                              const void* W1, const void* b1, const void* W2, const void* b2,
-                              const float* perm_w, float* y_perm, void* ws, const WsLayout& L,
-                              cudaStream_t s);
+cudaError_t launch_expert_ffn(const moe_config& c, const void* x_perm, int64_t x_rows,
+                              const int32_t* offsets, const void* W1, const void* b1,
+                              const void* W2, const void* b2, const float* perm_w, float* y_perm,
+                              void* ws, const WsLayout& L, cudaStream_t s);
 
 cudaError_t launch_combine(const moe_config& c, const float* y_perm, const int32_t* slot_of,
                            void* y, cudaStream_t s);
