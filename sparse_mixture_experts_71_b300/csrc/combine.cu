@@ -40,14 +40,29 @@ __global__ void __launch_bounds__(256) combine_kernel(const float* __restrict__ 
             const int sl = __ldg(slot_of + (size_t)t * k + j);
             slots[j] = sl < T * k ? sl : -1;  // y_perm has T*k rows
         }
-        for (int v = lane; v < nv; v += 32) {
-            float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+        // four 16-byte columns per lane in flight per row
+        for (int v0 = lane; v0 < nv; v0 += 128) {
+            float4 acc[4];
+#pragma unroll
+            for (int u = 0; u < 4; ++u) acc[u] = make_float4(0.f, 0.f, 0.f, 0.f);
             for (int j = 0; j < k; ++j) {
                 if (slots[j] < 0) continue;
-                const float4 q = __ldg(reinterpret_cast<const float4*>(y_perm + (size_t)slots[j] * d) + v);
-                acc.x += q.x; acc.y += q.y; acc.z += q.z; acc.w += q.w;
+                const float4* row = reinterpret_cast<const float4*>(y_perm + (size_t)slots[j] * d);
+                float4 q[4];
+#pragma unroll
+                for (int u = 0; u < 4; ++u)
+                    if (v0 + 32 * u < nv) q[u] = __ldg(row + v0 + 32 * u);
+#pragma unroll
+                for (int u = 0; u < 4; ++u) {
+                    if (v0 + 32 * u < nv) {
+                        acc[u].x += q[u].x; acc[u].y += q[u].y;
+                        acc[u].z += q[u].z; acc[u].w += q[u].w;
+                    }
+                }
             }
-            store4(y + (size_t)t * d + 4 * v, acc);
+#pragma unroll
+            for (int u = 0; u < 4; ++u)
+                if (v0 + 32 * u < nv) store4(y + (size_t)t * d + 4 * (v0 + 32 * u), acc[u]);
         }
     }
 }
@@ -57,11 +72,8 @@ __global__ void __launch_bounds__(256) combine_kernel(const float* __restrict__ 
 cudaError_t launch_combine(const moe_config& c, const float* y_perm, const int32_t* slot_of,
                            void* y, cudaStream_t s) {
     if (c.T == 0) return cudaSuccess;
-    int dev = 0, sms = 148;
-    cudaGetDevice(&dev);
-    cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
     int blocks = (c.T + 7) / 8;
-    blocks = blocks < sms * 8 ? blocks : sms * 8;
+    blocks = blocks < num_sms() * 8 ? blocks : num_sms() * 8;
     if (c.dtype == MOE_BF16)
         combine_kernel<__nv_bfloat16><<<blocks, 256, 0, s>>>(y_perm, slot_of, c.T, c.k, c.d,
                                                              reinterpret_cast<__nv_bfloat16*>(y));

@@ -118,7 +118,7 @@ __global__ void __launch_bounds__(256) permute_kernel(
     const TX* __restrict__ x, const int32_t* __restrict__ idx, const float* __restrict__ topk_w,
     const int32_t* __restrict__ local_rank, const int32_t* __restrict__ blk_base,
     const int32_t* __restrict__ offsets, int n, int k, int E, int d, int capacity,
-    int32_t* __restrict__ slot_of, int32_t* __restrict__ perm_token, float* __restrict__ perm_w,
+    int asg_per_block, int32_t* __restrict__ slot_of, int32_t* __restrict__ perm_token, float* __restrict__ perm_w,
     TX* __restrict__ x_perm) {
     const int lane = threadIdx.x % 32;
     const int nwarps = gridDim.x * (blockDim.x / 32);
@@ -128,7 +128,7 @@ __global__ void __launch_bounds__(256) permute_kernel(
         int slot = -1;
         if (r_local >= 0) {
             const int e = __ldg(idx + a);
-            const int r = __ldg(blk_base + (size_t)(a / kCountBlock) * E + e) + r_local;
+            const int r = __ldg(blk_base + (size_t)(a / asg_per_block) * E + e) + r_local;
             if (capacity < 0 || r < capacity) slot = __ldg(offsets + e) + r;
         }
         const int t = a / k;
@@ -154,38 +154,41 @@ __global__ void __launch_bounds__(256) permute_kernel(
 
 }  // namespace
 
-cudaError_t launch_dispatch(const moe_config& c, const void* x, const int32_t* topk_idx,
-                            const float* topk_w, int32_t* offsets, int32_t* slot_of,
-                            int32_t* perm_token, float* perm_w, void* x_perm, void* ws,
-                            const WsLayout& L, cudaStream_t s) {
+cudaError_t launch_count(const moe_config& c, const int32_t* topk_idx, void* ws,
+                         const WsLayout& L, cudaStream_t s) {
+    const int n = c.T * c.k;
+    if (n == 0) return cudaSuccess;
+    count_kernel<<<L.count_blocks, kCountBlock, 0, s>>>(topk_idx, n, c.E,
+                                                        at<int32_t>(ws, L.blk_hist),
+                                                        at<int32_t>(ws, L.local_rank),
+                                                        at<DeviceHeader>(ws, L.header));
+    count_launches(1);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_scan_permute(const moe_config& c, const void* x, const int32_t* topk_idx,
+                                const float* topk_w, int asg_per_block, int hist_blocks,
+                                int32_t* offsets, int32_t* slot_of, int32_t* perm_token,
+                                float* perm_w, void* x_perm, void* ws, const WsLayout& L,
+                                cudaStream_t s) {
     const int n = c.T * c.k;
     int32_t* blk_hist = at<int32_t>(ws, L.blk_hist);
     int32_t* blk_base = at<int32_t>(ws, L.blk_base);
     int32_t* local_rank = at<int32_t>(ws, L.local_rank);
-    DeviceHeader* hdr = at<DeviceHeader>(ws, L.header);
-    if (n > 0) {
-        count_kernel<<<L.count_blocks, kCountBlock, 0, s>>>(topk_idx, n, c.E, blk_hist, local_rank,
-                                                            hdr);
-        count_launches(1);
-    }
-    scan_kernel<<<1, 1024, 0, s>>>(blk_hist, L.count_blocks, c.E, c.capacity, blk_base, offsets);
+    scan_kernel<<<1, 1024, 0, s>>>(blk_hist, hist_blocks, c.E, c.capacity, blk_base, offsets);
     count_launches(1);
     if (n > 0) {
-        int dev = 0, sms = 148;
-        cudaGetDevice(&dev);
-        cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
-        const int warps_needed = n;
-        int blocks = (warps_needed + 7) / 8;
-        blocks = blocks < sms * 8 ? blocks : sms * 8;
+        int blocks = (n + 7) / 8;
+        blocks = blocks < num_sms() * 8 ? blocks : num_sms() * 8;
         if (c.dtype == MOE_BF16) {
             permute_kernel<__nv_bfloat16><<<blocks, 256, 0, s>>>(
                 reinterpret_cast<const __nv_bfloat16*>(x), topk_idx, topk_w, local_rank, blk_base,
-                offsets, n, c.k, c.E, c.d, c.capacity, slot_of, perm_token, perm_w,
+                offsets, n, c.k, c.E, c.d, c.capacity, asg_per_block, slot_of, perm_token, perm_w,
                 reinterpret_cast<__nv_bfloat16*>(x_perm));
         } else {
             permute_kernel<float><<<blocks, 256, 0, s>>>(
                 reinterpret_cast<const float*>(x), topk_idx, topk_w, local_rank, blk_base, offsets,
-                n, c.k, c.E, c.d, c.capacity, slot_of, perm_token, perm_w,
+                n, c.k, c.E, c.d, c.capacity, asg_per_block, slot_of, perm_token, perm_w,
                 reinterpret_cast<float*>(x_perm));
         }
         count_launches(1);

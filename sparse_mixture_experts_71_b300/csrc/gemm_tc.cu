@@ -52,6 +52,7 @@ constexpr int A_BYTES = BM * BK * 2;         // 16 KB
 constexpr int BOX_ROWS = 32;                 // token rows per TMA box
 constexpr int BOX_BYTES = BOX_ROWS * BK * 2; // 4 KB
 constexpr uint64_t kDrainNs = 2000000000ull; // drain waits on the error path
+constexpr int kWideCluster = 4;              // CTAs sharing a token tile (wide tiles)
 
 template <int BN_MAX, int STAGES, bool GEMM1>
 struct Cfg {
@@ -85,10 +86,12 @@ struct Tile {
     int e, r0, n, m0;
 };
 
-__device__ __forceinline__ Tile decode_tile(int t, const int* s_tiles, const Params& p, int mt,
-                                            int bn_max) {
+// Work item t of a cluster: expert e, token tile, and a group of CS
+// consecutive 128-row weight tiles of which CTA `rank` takes one.
+__device__ __forceinline__ Tile decode_tile(int t, const int* s_tiles, const Params& p, int bn_max,
+                                            int cs, int rank) {
     int lo = 0, hi = p.E - 1;
-    while (lo < hi) {  // last expert whose first tile is <= t
+    while (lo < hi) {  // last expert whose first item is <= t
         const int mid = (lo + hi + 1) >> 1;
         if (s_tiles[mid] <= t) lo = mid; else hi = mid - 1;
     }
@@ -98,11 +101,10 @@ __device__ __forceinline__ Tile decode_tile(int t, const int* s_tiles, const Par
     const int s0 = min(max(__ldg(p.offsets + lo), 0), p.rows_cap);
     const int s1 = min(max(__ldg(p.offsets + lo + 1), s0), p.rows_cap);
     const int nt = (s1 - s0 + bn_max - 1) / bn_max;
-    const int ti = local % nt, mi = local / nt;  // token tile fastest
+    const int ti = local % nt, gi = local / nt;  // token tile fastest
     tl.r0 = s0 + ti * bn_max;
     tl.n = min(bn_max, s1 - tl.r0);
-    tl.m0 = mi * BM;
-    (void)mt;
+    tl.m0 = (gi * cs + rank) * BM;
     return tl;
 }
 
@@ -131,11 +133,19 @@ __device__ __forceinline__ void drain_bar(uint64_t* bar, uint32_t parity) {
     }
 }
 
-template <int BN_MAX, int STAGES, bool GEMM1>
+// CS > 1: the kernel runs in clusters of CS CTAs that share each token tile:
+// CTA r loads the token boxes b with b % CS == r once and multicasts them to
+// every CTA of the cluster, so each CTA fetches 1/CS of the token tile from
+// L2.  A stage may be refilled only when all CS CTAs have consumed it, so
+// every MMA commit arrives on the stage's empty barrier of all CS CTAs.
+template <int BN_MAX, int STAGES, bool GEMM1, int CS>
 __global__ void __launch_bounds__(kThreads, 1)
 grouped_gemm_tc(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                 const Params p) {
     using C = Cfg<BN_MAX, STAGES, GEMM1>;
+    const int rank = CS > 1 ? (int)tc::cluster_ctarank() : 0;
+    const int cluster = blockIdx.x / CS, nclusters = gridDim.x / CS;
+    constexpr uint16_t kAll = (uint16_t)((1u << CS) - 1u);
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -150,12 +160,13 @@ grouped_gemm_tc(const __grid_constant__ CUtensorMap tmA, const __grid_constant__
 
     const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
     const int mt = (p.n_out + BM - 1) / BM;
+    const int groups = (mt + CS - 1) / CS;  // weight-tile groups per token tile
     const int KB = (p.K + BK - 1) / BK;
 
     if (warp == 0 && lane == 0) {
         for (int s = 0; s < STAGES; ++s) {
             tc::mbar_init(&full[s], 1);
-            tc::mbar_init(&empty[s], 1);
+            tc::mbar_init(&empty[s], CS);
         }
         for (int a = 0; a < 2; ++a) {
             tc::mbar_init(&tfull[a], 1);
@@ -179,7 +190,7 @@ grouped_gemm_tc(const __grid_constant__ CUtensorMap tmA, const __grid_constant__
             if (e < p.E) {
                 const int s0 = min(max(__ldg(p.offsets + e), 0), p.rows_cap);
                 const int s1 = min(max(__ldg(p.offsets + e + 1), s0), p.rows_cap);
-                nt = ((s1 - s0 + BN_MAX - 1) / BN_MAX) * mt;
+                nt = ((s1 - s0 + BN_MAX - 1) / BN_MAX) * groups;
             }
             int v = nt;
 #pragma unroll
@@ -193,7 +204,8 @@ grouped_gemm_tc(const __grid_constant__ CUtensorMap tmA, const __grid_constant__
         if (lane == 0) s_tiles[p.E] = run;
     }
     tc::fence_before_sync();
-    __syncthreads();
+    if (CS > 1) tc::cluster_sync();  // peers' barriers exist before any multicast
+    else __syncthreads();
     tc::fence_after_sync();
     const uint32_t tmem_base = *s_tmem;
     const int total = s_tiles[p.E];
@@ -205,8 +217,8 @@ grouped_gemm_tc(const __grid_constant__ CUtensorMap tmA, const __grid_constant__
             uint32_t phase = 0;
             long long fills = 0;
             bool ok = true;
-            for (int t = blockIdx.x; t < total && ok; t += gridDim.x) {
-                const Tile tl = decode_tile(t, s_tiles, p, mt, BN_MAX);
+            for (int t = cluster; t < total && ok; t += nclusters) {
+                const Tile tl = decode_tile(t, s_tiles, p, BN_MAX, CS, rank);
                 const int nb = (tl.n + BOX_ROWS - 1) / BOX_ROWS;
                 const uint32_t bytes = A_BYTES + nb * BOX_BYTES;
                 const int arow = tl.e * p.n_out + tl.m0;
@@ -216,9 +228,15 @@ grouped_gemm_tc(const __grid_constant__ CUtensorMap tmA, const __grid_constant__
                     uint8_t* sa = smem + stage * C::STAGE_BYTES;
                     uint8_t* sb = sa + A_BYTES;
                     tc::tma_load_2d(sa, &tmA, &full[stage], kb * BK, arow);
-                    for (int b = 0; b < nb; ++b)
-                        tc::tma_load_2d(sb + b * BOX_BYTES, &tmB, &full[stage], kb * BK,
-                                        tl.r0 + b * BOX_ROWS);
+                    if (CS == 1) {
+                        for (int b = 0; b < nb; ++b)
+                            tc::tma_load_2d(sb + b * BOX_BYTES, &tmB, &full[stage], kb * BK,
+                                            tl.r0 + b * BOX_ROWS);
+                    } else {
+                        for (int b = rank; b < nb; b += CS)
+                            tc::tma_load_2d_mc(sb + b * BOX_BYTES, &tmB, &full[stage], kb * BK,
+                                               tl.r0 + b * BOX_ROWS, kAll);
+                    }
                     ++fills;
                     if (++stage == STAGES) { stage = 0; phase ^= 1; }
                 }
@@ -234,8 +252,8 @@ grouped_gemm_tc(const __grid_constant__ CUtensorMap tmA, const __grid_constant__
             int stage = 0, acc = 0;
             uint32_t phase = 0, acc_phase = 0;
             bool ok = true;
-            for (int t = blockIdx.x; t < total && ok; t += gridDim.x) {
-                const Tile tl = decode_tile(t, s_tiles, p, mt, BN_MAX);
+            for (int t = cluster; t < total && ok; t += nclusters) {
+                const Tile tl = decode_tile(t, s_tiles, p, BN_MAX, CS, rank);
                 const uint32_t n_mma = (uint32_t)((tl.n + 15) / 16) * 16;
                 const uint32_t idesc = tc::idesc_bf16_f32(BM, n_mma);
                 if (!wait_bar(&tempty[acc], acc_phase ^ 1, s_abort, p, 2)) break;
@@ -252,7 +270,8 @@ grouped_gemm_tc(const __grid_constant__ CUtensorMap tmA, const __grid_constant__
                                      tc::sdesc_k128_sw128(sb + kk * 32), idesc,
                                      (kb | kk) != 0 ? 1u : 0u);
                     }
-                    tc::mma_commit(&empty[stage]);
+                    if (CS == 1) tc::mma_commit(&empty[stage]);
+                    else tc::mma_commit_mc(&empty[stage], kAll);
                     if (++stage == STAGES) { stage = 0; phase ^= 1; }
                 }
                 if (!ok) break;
@@ -272,8 +291,8 @@ grouped_gemm_tc(const __grid_constant__ CUtensorMap tmA, const __grid_constant__
         uint8_t* stg = smem + C::OFF_STAGING + ew * 32 * 32 * C::OUT_ES;
         int acc = 0;
         uint32_t acc_phase = 0;
-        for (int t = blockIdx.x; t < total; t += gridDim.x) {
-            const Tile tl = decode_tile(t, s_tiles, p, mt, BN_MAX);
+        for (int t = cluster; t < total; t += nclusters) {
+            const Tile tl = decode_tile(t, s_tiles, p, BN_MAX, CS, rank);
             const bool ok = wait_bar(&tfull[acc], acc_phase, s_abort, p, 4);
             if (!__all_sync(0xffffffffu, ok)) break;
             tc::fence_after_sync();
@@ -292,7 +311,7 @@ grouped_gemm_tc(const __grid_constant__ CUtensorMap tmA, const __grid_constant__
                     __nv_bfloat16* s16 = reinterpret_cast<__nv_bfloat16*>(stg);
 #pragma unroll
                     for (int j = 0; j < 32; ++j)
-                        s16[j * 32 + lane] = __float2bfloat16_rn(gelu_erf(v[j] + bias));
+                        s16[j * 32 + lane] = __float2bfloat16_rn(gelu_as7126(v[j] + bias));
                     __syncwarp();
                     __nv_bfloat16* out = reinterpret_cast<__nv_bfloat16*>(p.out);
 #pragma unroll
@@ -339,6 +358,8 @@ grouped_gemm_tc(const __grid_constant__ CUtensorMap tmA, const __grid_constant__
         tc::fence_after_sync();
         tc::tmem_dealloc(tmem_base, C::TMEM_COLS);
     }
+    // no CTA leaves while a peer may still multicast into it or arrive on it
+    if (CS > 1) tc::cluster_sync();
 }
 
 PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
@@ -369,37 +390,69 @@ bool make_map(CUtensorMap* m, const void* base, uint64_t inner, uint64_t outer,
               CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-int num_sms() {
-    static int sms[64] = {0};
+// Clusters of CS CTAs that can be resident at once (one CTA per SM).
+template <auto Kern>
+int resident_clusters(int cs, int smem) {
+    static int cache[64] = {0};
     int dev = 0;
     cudaGetDevice(&dev);
-    if (dev < 0 || dev >= 64) dev = 0;
-    if (sms[dev] == 0) {
-        int v = 148;
-        cudaDeviceGetAttribute(&v, cudaDevAttrMultiProcessorCount, dev);
-        sms[dev] = v;
+    if (dev >= 0 && dev < 64 && cache[dev] > 0) return cache[dev];
+    int n = num_sms() / cs;
+    if (cs > 1) {
+        cudaLaunchConfig_t cfg = {};
+        cfg.gridDim = dim3(cs * n, 1, 1);
+        cfg.blockDim = dim3(kThreads, 1, 1);
+        cfg.dynamicSmemBytes = smem;
+        cudaLaunchAttribute attr;
+        attr.id = cudaLaunchAttributeClusterDimension;
+        attr.val.clusterDim.x = cs;
+        attr.val.clusterDim.y = 1;
+        attr.val.clusterDim.z = 1;
+        cfg.attrs = &attr;
+        cfg.numAttrs = 1;
+        int q = 0;
+        if (cudaOccupancyMaxActiveClusters(&q, Kern, &cfg) == cudaSuccess && q > 0 && q < n) n = q;
+        cudaGetLastError();
     }
-    return sms[dev];
+    if (dev >= 0 && dev < 64) cache[dev] = n;
+    return n;
 }
 
-template <int BN_MAX, int STAGES, bool GEMM1>
+template <int BN_MAX, int STAGES, bool GEMM1, int CS>
 cudaError_t launch_one(const CUtensorMap& a, const CUtensorMap& b, const Params& p,
                        cudaStream_t s) {
     using C = Cfg<BN_MAX, STAGES, GEMM1>;
-    auto kern = grouped_gemm_tc<BN_MAX, STAGES, GEMM1>;
-    cudaError_t err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
+    constexpr auto kern = grouped_gemm_tc<BN_MAX, STAGES, GEMM1, CS>;
+    cudaError_t err = ensure_smem<kern>(C::SMEM);
     if (err != cudaSuccess) return err;
-    kern<<<num_sms(), kThreads, C::SMEM, s>>>(a, b, p);
+    if (CS == 1) {
+        kern<<<num_sms(), kThreads, C::SMEM, s>>>(a, b, p);
+    } else {
+        cudaLaunchConfig_t cfg = {};
+        cfg.gridDim = dim3(CS * resident_clusters<kern>(CS, C::SMEM), 1, 1);
+        cfg.blockDim = dim3(kThreads, 1, 1);
+        cfg.dynamicSmemBytes = C::SMEM;
+        cfg.stream = s;
+        cudaLaunchAttribute attr;
+        attr.id = cudaLaunchAttributeClusterDimension;
+        attr.val.clusterDim.x = CS;
+        attr.val.clusterDim.y = 1;
+        attr.val.clusterDim.z = 1;
+        cfg.attrs = &attr;
+        cfg.numAttrs = 1;
+        err = cudaLaunchKernelEx(&cfg, kern, a, b, p);
+        if (err != cudaSuccess) return err;
+    }
     count_launches(1);
     return cudaGetLastError();
 }
 
-template <int BN_MAX, int STAGES>
+template <int BN_MAX, int STAGES, int CS>
 cudaError_t launch_pair(const CUtensorMap* maps, const Params& p1, const Params& p2,
                         cudaStream_t s) {
-    cudaError_t err = launch_one<BN_MAX, STAGES, true>(maps[0], maps[1], p1, s);
+    cudaError_t err = launch_one<BN_MAX, STAGES, true, CS>(maps[0], maps[1], p1, s);
     if (err != cudaSuccess) return err;
-    return launch_one<BN_MAX, STAGES, false>(maps[2], maps[3], p2, s);
+    return launch_one<BN_MAX, STAGES, false, CS>(maps[2], maps[3], p2, s);
 }
 
 }  // namespace
@@ -425,8 +478,8 @@ cudaError_t launch_expert_ffn_tc(const moe_config& c, const void* x_perm, int64_
               g_tc_timeout_ns, c.E, c.d_ff, c.d, (int)h_rows};
     Params p2{offsets, reinterpret_cast<const __nv_bfloat16*>(b2), perm_w, y_perm, hdr,
               g_tc_timeout_ns, c.E, c.d, c.d_ff, (int)h_rows};
-    if (wide) return launch_pair<256, 4>(maps, p1, p2, s);
-    return launch_pair<64, 8>(maps, p1, p2, s);
+    if (wide) return launch_pair<256, 4, kWideCluster>(maps, p1, p2, s);
+    return launch_pair<64, 8, 1>(maps, p1, p2, s);
 }
 
 }  // namespace moe

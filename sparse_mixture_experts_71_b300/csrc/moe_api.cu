@@ -14,6 +14,19 @@ namespace moe {
 static std::atomic<uint64_t> g_launches{0};
 void count_launches(int n) { g_launches.fetch_add((uint64_t)n, std::memory_order_relaxed); }
 
+int num_sms() {
+    static int sms[64] = {0};
+    int dev = 0;
+    cudaGetDevice(&dev);
+    if (dev < 0 || dev >= 64) dev = 0;
+    if (sms[dev] == 0) {
+        int v = 148;
+        cudaDeviceGetAttribute(&v, cudaDevAttrMultiProcessorCount, dev);
+        sms[dev] = v;
+    }
+    return sms[dev];
+}
+
 cudaError_t launch_expert_ffn_simt(const moe_config& c, const void* x_perm, const int32_t* offsets,
                                    const void* W1, const void* b1, const void* W2, const void* b2,
                                    const float* perm_w, float* y_perm, void* h, int64_t max_seg,
@@ -73,8 +86,9 @@ int64_t max_segment(const moe_config& c) {
 WsLayout ws_layout(const moe_config& c) {
     WsLayout L{};
     const int64_t n = (int64_t)c.T * c.k;
-    L.route_blocks = (int)((c.T + route_tokens_per_block(c.E) - 1) / route_tokens_per_block(c.E));
+    L.route = route_geom(c);
     L.count_blocks = (int)((n + kCountBlock - 1) / kCountBlock);
+    L.hist_blocks = L.route.blocks > L.count_blocks ? L.route.blocks : L.count_blocks;
     L.rows = n;
     if (c.capacity >= 0 && (int64_t)c.E * c.capacity < L.rows) L.rows = (int64_t)c.E * c.capacity;
     const size_t es = elem_size(c);
@@ -87,9 +101,9 @@ WsLayout ws_layout(const moe_config& c) {
     L.header = take(sizeof(DeviceHeader));
     L.counts = take(sizeof(int32_t) * c.E);
     L.top1 = take(sizeof(int32_t) * c.E);
-    L.blk_p = take(sizeof(float) * (size_t)L.route_blocks * c.E);
-    L.blk_hist = take(sizeof(int32_t) * (size_t)L.count_blocks * c.E);
-    L.blk_base = take(sizeof(int32_t) * (size_t)L.count_blocks * c.E);
+    L.blk_p = take(sizeof(float) * (size_t)L.route.blocks * c.E);
+    L.blk_hist = take(sizeof(int32_t) * (size_t)L.hist_blocks * c.E);
+    L.blk_base = take(sizeof(int32_t) * (size_t)L.hist_blocks * c.E);
     L.local_rank = take(sizeof(int32_t) * (size_t)n);
     L.topk_idx = take(sizeof(int32_t) * (size_t)n);
     L.topk_w = take(sizeof(float) * (size_t)n);
@@ -156,7 +170,7 @@ moe_status moe_route(const moe_config* cfg, const void* x, const float* W_r,
     if (logits_in == nullptr && (!aligned16(x) || !aligned16(W_r))) return MOE_ERR_ALIGNMENT;
     if ((st = check_ws(c, ws, ws_bytes, &L)) != MOE_OK) return st;
     return from_cuda(launch_route(c, x, W_r, logit_bias, logits_in, logits_out, topk_idx, topk_w,
-                                  expert_counts, aux_out, ws, L, s));
+                                  expert_counts, aux_out, ws, L, false, s));
 }
 
 moe_status moe_dispatch(const moe_config* cfg, const void* x, const int32_t* topk_idx,
@@ -179,8 +193,12 @@ moe_status moe_dispatch(const moe_config* cfg, const void* x, const int32_t* top
     if (!aligned16(x) || !aligned16(x_perm)) return MOE_ERR_ALIGNMENT;
     WsLayout L;
     if ((st = check_ws(c, ws, ws_bytes, &L)) != MOE_OK) return st;
-    return from_cuda(launch_dispatch(c, x, topk_idx, topk_w, offsets, slot_of, perm_token, perm_w,
-                                     x_perm, ws, L, reinterpret_cast<cudaStream_t>(stream)));
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    cudaError_t e = launch_count(c, topk_idx, ws, L, s);
+    if (e == cudaSuccess)
+        e = launch_scan_permute(c, x, topk_idx, topk_w, kCountBlock, L.count_blocks, offsets,
+                                slot_of, perm_token, perm_w, x_perm, ws, L, s);
+    return from_cuda(e);
 }
 
 moe_status moe_expert_ffn(const moe_config* cfg, const void* x_perm, const int32_t* offsets,
@@ -240,9 +258,10 @@ moe_status moe_forward(const moe_config* cfg, const void* x, const float* W_r,
     void* x_perm = at<void>(ws, L.x_perm);
     float* y_perm = at<float>(ws, L.y_perm);
     cudaError_t e = launch_route(c, x, W_r, logit_bias, nullptr, logits_out, idx, w, expert_counts,
-                                 aux_out, ws, L, s);
+                                 aux_out, ws, L, true, s);
     if (e == cudaSuccess)
-        e = launch_dispatch(c, x, idx, w, offsets, slot_of, perm_token, perm_w, x_perm, ws, L, s);
+        e = launch_scan_permute(c, x, idx, w, L.route.tokens * c.k, L.route.blocks, offsets,
+                                slot_of, perm_token, perm_w, x_perm, ws, L, s);
     if (e == cudaSuccess)
         e = launch_expert_ffn(c, x_perm, L.rows, offsets, W1, b1, W2, b2, perm_w, y_perm, ws, L,
                               s);

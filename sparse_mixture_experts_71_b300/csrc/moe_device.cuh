@@ -40,6 +40,25 @@ __device__ __forceinline__ float gelu_erf(float u) {
     return 0.5f * u * (1.0f + erff(u * 0.70710678118654752440f));
 }
 
+// GELU 0.5 u (1 + erf(z)), z = u / sqrt 2, with erf from the rational
+// approximation of Abramowitz & Stegun, Handbook of Mathematical Functions,
+// formula 7.1.26 (Hastings): for z >= 0, erf(z) = 1 - q(t) exp(-z^2),
+// t = 1 / (1 + p z), q(t) = t (a1 + t (a2 + t (a3 + t (a4 + t a5)))), with
+// |error| <= 1.5e-7.  1 + erf(z) is q e^{-z^2} for z < 0 and 2 - q e^{-z^2}
+// for z >= 0, which keeps the negative tail free of cancellation.  Used where
+// the result is rounded to bf16 (relative step 2^-8), far above the error.
+__device__ __forceinline__ float gelu_as7126(float u) {
+    const float z = fabsf(u) * 0.70710678118654752440f;
+    const float t = __fdividef(1.0f, fmaf(0.3275911f, z, 1.0f));
+    float q = fmaf(t, 1.061405429f, -1.453152027f);
+    q = fmaf(t, q, 1.421413741f);
+    q = fmaf(t, q, -0.284496736f);
+    q = fmaf(t, q, 0.254829592f);
+    q *= t;
+    const float r = q * __expf(-z * z);
+    return 0.5f * u * (u < 0.f ? r : 2.0f - r);
+}
+
 // Record the first device error in the workspace header (later ones are dropped).
 __device__ __forceinline__ void record_error(DeviceHeader* h, int32_t code, int32_t info) {
     if (atomicCAS(&h->err_code, 0, code) == 0) h->err_info = info;

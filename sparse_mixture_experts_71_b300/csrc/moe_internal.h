@@ -11,7 +11,7 @@ namespace moe {
 
 constexpr int kMaxExperts = 256;
 constexpr int kMaxTopK = 8;
-// assignments covered by one block of the counting kernel
+// assignments covered by one block of the stand-alone counting kernel
 constexpr int kCountBlock = 256;
 
 // Device error record at the start of every workspace.
@@ -25,14 +25,25 @@ static_assert(sizeof(DeviceHeader) == 256, "header is one 256-byte line");
 
 enum DeviceError : int32_t { kErrExpertRange = 1, kErrTimeout = 2 };
 
+// How the router kernel tiles the batch: `warp` kernel (E <= 32: one warp per
+// `tw` tokens, 8 warps per block) or `tile` kernel (SIMT GEMM tile).
+struct RouteGeom {
+    bool warp;
+    int tw;            // tokens per warp group (warp kernel)
+    int ds;            // warps splitting one group's d columns (warp kernel)
+    int tokens;        // tokens per block
+    int blocks;
+};
+RouteGeom route_geom(const moe_config& c);
+
 // Byte offsets of the workspace regions for one configuration.
 struct WsLayout {
     size_t header;       // DeviceHeader
     size_t counts;       // int32 [E]   assignments per expert (all slots)
     size_t top1;         // int32 [E]   first-slot choices per expert
-    size_t blk_p;        // fp32 [route_blocks][E] per-block sums of p
-    size_t blk_hist;     // int32 [count_blocks][E]
-    size_t blk_base;     // int32 [count_blocks][E]
+    size_t blk_p;        // fp32 [route.blocks][E] per-block sums of p
+    size_t blk_hist;     // int32 [hist_blocks][E]
+    size_t blk_base;     // int32 [hist_blocks][E]
     size_t local_rank;   // int32 [T*k]
     size_t topk_idx;     // int32 [T*k]     (moe_forward)
     size_t topk_w;       // fp32  [T*k]     (moe_forward)
@@ -44,31 +55,59 @@ struct WsLayout {
     size_t h;            // dtype [rows][d_ff]
     size_t y_perm;       // fp32  [rows][d] (moe_forward)
     size_t total;
-    int route_blocks;
-    int count_blocks;
+    RouteGeom route;
+    int count_blocks;    // blocks of the stand-alone counting kernel
+    int hist_blocks;     // max(route.blocks, count_blocks)
     int64_t rows;        // upper bound of kept assignments
 };
 
 WsLayout ws_layout(const moe_config& c);
-int route_tokens_per_block(int E);
 
 // Kernel launches enqueued so far (moe_launch_count).
 void count_launches(int n);
+int num_sms();
+
+// Raise kernel Kern's dynamic shared-memory limit, once per device.
+template <auto Kern>
+cudaError_t ensure_smem(int bytes) {
+    static bool done[64] = {};
+    int dev = 0;
+    cudaGetDevice(&dev);
+    const bool cacheable = dev >= 0 && dev < 64;
+    if (cacheable && done[dev]) return cudaSuccess;
+    const cudaError_t e =
+        cudaFuncSetAttribute(Kern, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+    if (e == cudaSuccess && cacheable) done[dev] = true;
+    return e;
+}
 
 template <typename T> __host__ __device__ inline T* at(void* base, size_t off) {
     return reinterpret_cast<T*>(reinterpret_cast<char*>(base) + off);
 }
 
-// ---- launchers (kernels live in route.cu, dispatch.cu, gemm_simt.cu, combine.cu)
+// ---- launchers (kernels live in route.cu, dispatch.cu, gemm_*.cu, combine.cu)
+
+// Router.  With `fuse_count` the router also writes, per router block, the
+// expert histogram (blk_hist) and each assignment's rank among the block's
+// earlier assignments to the same expert (local_rank), which the scan and
+// permute kernels consume with granularity route.tokens * k.
 cudaError_t launch_route(const moe_config& c, const void* x, const float* W_r,
                          const float* logit_bias, const float* logits_in, float* logits_out,
                          int32_t* topk_idx, float* topk_w, int32_t* expert_counts,
-                         float* aux_out, void* ws, const WsLayout& L, cudaStream_t s);
+                         float* aux_out, void* ws, const WsLayout& L, bool fuse_count,
+                         cudaStream_t s);
 
-cudaError_t launch_dispatch(const moe_config& c, const void* x, const int32_t* topk_idx,
-                            const float* topk_w, int32_t* offsets, int32_t* slot_of,
-                            int32_t* perm_token, float* perm_w, void* x_perm, void* ws,
-                            const WsLayout& L, cudaStream_t s);
+// Counting kernel over topk_idx (granularity kCountBlock assignments).
+cudaError_t launch_count(const moe_config& c, const int32_t* topk_idx, void* ws,
+                         const WsLayout& L, cudaStream_t s);
+
+// Scan of the block histograms and the permute/gather, given histograms of
+// `hist_blocks` blocks of `asg_per_block` assignments.
+cudaError_t launch_scan_permute(const moe_config& c, const void* x, const int32_t* topk_idx,
+                                const float* topk_w, int asg_per_block, int hist_blocks,
+                                int32_t* offsets, int32_t* slot_of, int32_t* perm_token,
+                                float* perm_w, void* x_perm, void* ws, const WsLayout& L,
+                                cudaStream_t s);
 
 cudaError_t launch_expert_ffn(const moe_config& c, const void* x_perm, int64_t x_rows,
                               const int32_t* offsets, const void* W1, const void* b1,

@@ -1,4 +1,4 @@
-// Router kernel: logits g = W_r x (+ bias), softmax, top-k, gate weights,
+// Router kernels: logits g = W_r x (+ bias), softmax, top-k, gate weights,
 // per-expert counts and the Switch auxiliary loss, fused in one pass over x.
 //
 // "Mixture of Experts: Scaling Parameters Without Scaling Compute", section
@@ -6,13 +6,24 @@
 // balancing" (auxiliary loss E * sum_i f_i P_i, f_i from the top-1 choice,
 // P_i the mean probability).
 //
-// One block owns TB tokens and every expert.  The logits tile is an fp32 SIMT
-// GEMM: x and W_r are staged through shared memory in chunks of KC columns,
-// each thread accumulates a 4-token x 8-expert register tile over a 1/S
-// slice of the chunk columns, and the S partial tiles are summed in a fixed
-// order (deterministic).  Softmax and top-k run one warp per token.  The last
-// block to finish reduces the per-block probability sums (fixed order) and
-// writes the auxiliary loss and the per-expert counts.
+// Two tilings of the logits GEMM (fp32 FMA, exact products, fp32 sums):
+//   warp kernel (E <= 32)  one warp owns TW tokens; lanes split d into
+//                          8-column chunks (16-byte loads of x, W_r rows from
+//                          L1/L2), a butterfly all-reduce gives every lane the
+//                          TW x E logits, and each token's softmax / top-k runs
+//                          in registers.  8 warps per block.  The pass is
+//                          bound by reading x once.
+//   tile kernel (E > 32)   one block owns TB tokens and every expert; x and
+//                          W_r chunks are staged in shared memory and each
+//                          thread accumulates a 4-token x 8-expert register
+//                          tile over a slice of the chunk columns; the partial
+//                          tiles are summed in a fixed order.  Softmax and
+//                          top-k then run one warp per token.
+// Both end alike: per-block sums of p in fixed token order, integer counts,
+// optionally the block's expert histogram and the rank of each assignment
+// among the block's earlier assignments to the same expert (consumed by the
+// dispatch scan), and in the last block to finish the auxiliary loss from the
+// per-block sums taken in block order (deterministic).
 
 #include <cuda_runtime.h>
 #include <float.h>
@@ -24,9 +35,7 @@ namespace moe {
 namespace {
 
 constexpr int kThreads = 256;
-constexpr int KC = 32;   // columns of x / W_r per shared-memory chunk
-constexpr int RT = 4;    // tokens per thread tile
-constexpr int RE = 8;    // experts per thread tile
+constexpr int kWarps = kThreads / 32;
 
 struct RouteArgs {
     const void* x;
@@ -39,11 +48,278 @@ struct RouteArgs {
     int32_t* expert_counts;
     float* aux_out;
     DeviceHeader* hdr;
-    int32_t* counts;     // ws: [E] all-slot assignments
-    int32_t* top1;       // ws: [E] first-slot choices
-    float* blk_p;        // ws: [nblk][E]
+    int32_t* counts;      // ws: [E] all-slot assignments
+    int32_t* top1;        // ws: [E] first-slot choices
+    float* blk_p;         // ws: [nblk][E]
+    int32_t* blk_hist;    // ws: [nblk][E] or null (no fused counting)
+    int32_t* local_rank;  // ws: [T*k]
     int T, d, E, k, renormalize, nblk;
 };
+
+// Histogram of the block's n assignments (expert ids in s_idx, in (token,
+// slot) order) and the rank of each among the earlier ones of its expert.
+template <int EMAX>
+__device__ void block_rank(const int* s_idx, int n, int E, int (*wh)[EMAX], int* carry,
+                           int32_t* hist_row, int32_t* rank_out) {
+    const int tid = threadIdx.x, warp = tid / 32, lane = tid % 32;
+    for (int e = tid; e < E; e += kThreads) carry[e] = 0;
+    for (int base = 0; base < n; base += kThreads) {
+        for (int i = tid; i < kWarps * EMAX; i += kThreads) (&wh[0][0])[i] = 0;
+        __syncthreads();
+        const int a = base + tid;
+        const int e = a < n ? s_idx[a] : -1;
+        const unsigned same = __match_any_sync(0xffffffffu, e);
+        const int r = __popc(same & ((1u << lane) - 1u));
+        if (e >= 0 && r == 0) wh[warp][e] = __popc(same);
+        __syncthreads();
+        if (e >= 0) {
+            int rr = carry[e] + r;
+            for (int w = 0; w < warp; ++w) rr += wh[w][e];
+            rank_out[a] = rr;
+        }
+        __syncthreads();
+        for (int x = tid; x < E; x += kThreads) {
+            int s = 0;
+#pragma unroll
+            for (int w = 0; w < kWarps; ++w) s += wh[w][x];
+            carry[x] += s;
+        }
+        __syncthreads();
+    }
+    for (int e = tid; e < E; e += kThreads) hist_row[e] = carry[e];
+}
+
+// Per-block sums of p (rows of s_p, fixed order), counts, the fused dispatch
+// histogram, and in the last block the loss and the per-expert counts.
+template <int EMAX>
+__device__ void finish_block(const RouteArgs& a, const float* s_p, int lds, int TB,
+                             const int* s_idx, const int* s_cnt, const int* s_top1,
+                             int (*wh)[EMAX], int* carry, double* s_d, double* s_part,
+                             int* s_last) {
+    const int tid = threadIdx.x;
+    const int t0 = blockIdx.x * TB;
+    for (int e = tid; e < a.E; e += kThreads) {
+        float v = 0.f;
+        for (int tok = 0; tok < TB; ++tok) v += s_p[tok * lds + e];
+        a.blk_p[(size_t)blockIdx.x * a.E + e] = v;
+        if (s_cnt[e]) atomicAdd(&a.counts[e], s_cnt[e]);
+        if (s_top1[e]) atomicAdd(&a.top1[e], s_top1[e]);
+    }
+    if (a.blk_hist != nullptr) {
+        const int n = min(TB, a.T - t0) * a.k;
+        block_rank<EMAX>(s_idx, n, a.E, wh, carry, a.blk_hist + (size_t)blockIdx.x * a.E,
+                         a.local_rank + (size_t)t0 * a.k);
+    }
+    __threadfence();
+    __syncthreads();
+    if (tid == 0) *s_last = (atomicAdd(&a.hdr->route_done, 1u) == (unsigned)(a.nblk - 1));
+    __syncthreads();
+    if (!*s_last) return;
+    __threadfence();
+    // the per-block sums, in block order: thread i < stride (a multiple of E)
+    // owns expert i % E and blocks i / E, i / E + per, ...; the partials of an
+    // expert are then added in thread order
+    const int per = kThreads / a.E;
+    const int stride = per * a.E;
+    double v = 0.0;
+    if (tid < stride) {
+        const int e = tid % a.E;
+#pragma unroll 8
+        for (int b = tid / a.E; b < a.nblk; b += per)
+            v += (double)__ldcg(a.blk_p + (size_t)b * a.E + e);
+    }
+    s_part[tid] = v;
+    __syncthreads();
+    for (int e = tid; e < a.E; e += kThreads) {
+        double pe = 0.0;
+        for (int j = 0; j < per; ++j) pe += s_part[j * a.E + e];
+        s_d[e] = (double)__ldcg(a.top1 + e) * pe;
+        if (a.expert_counts != nullptr) a.expert_counts[e] = __ldcg(a.counts + e);
+    }
+    __syncthreads();
+    if (tid == 0 && a.aux_out != nullptr) {
+        double s = 0.0;
+        for (int e = 0; e < a.E; ++e) s += s_d[e];
+        const double Td = (double)a.T;
+        a.aux_out[0] = (float)((double)a.E * s / (Td * Td));
+    }
+}
+
+// ===================================================================== warp kernel
+// DS warps split one token group's d columns (DS > 1 for small batches, so
+// that enough blocks exist); their partial logits meet in shared memory and
+// are added in split order.
+template <typename TX, int EMAX, int TW, int DS>
+__global__ void __launch_bounds__(kThreads) route_warp_kernel(RouteArgs a) {
+    constexpr int G = kWarps / DS;   // token groups per block
+    constexpr int TB = G * TW;       // tokens per block
+    constexpr int LDS = EMAX + 1;
+    __shared__ float s_p[TB * LDS];
+    __shared__ float s_red[DS > 1 ? kWarps * TW * EMAX : 1];
+    __shared__ int s_idx[TB * kMaxTopK];
+    __shared__ int s_cnt[EMAX], s_top1[EMAX], carry[EMAX];
+    __shared__ int wh[kWarps][EMAX];
+    __shared__ double s_d[EMAX];
+    __shared__ double s_part[kThreads];
+    __shared__ int s_last;
+
+    const int tid = threadIdx.x, warp = tid / 32, lane = tid % 32;
+    const int grp = warp / DS, split = warp % DS;
+    if (tid < EMAX) { s_cnt[tid] = 0; s_top1[tid] = 0; }
+    for (int i = tid; i < TB * LDS; i += kThreads) s_p[i] = 0.f;
+    __syncthreads();
+    const int tb = blockIdx.x * TB + grp * TW;  // first token of this warp's group
+
+    float acc[TW][EMAX];
+#pragma unroll
+    for (int i = 0; i < TW; ++i)
+#pragma unroll
+        for (int e = 0; e < EMAX; ++e) acc[i][e] = 0.f;
+
+    if (a.logits_in == nullptr) {
+        const TX* x = reinterpret_cast<const TX*>(a.x);
+        const int nchunk = a.d / 8;
+        for (int ch = split * 32 + lane; ch < nchunk; ch += 32 * DS) {
+            const int c = ch * 8;
+            float xv[TW][8];
+#pragma unroll
+            for (int i = 0; i < TW; ++i) {
+                if (tb + i < a.T) {
+                    load8_f32(x + (size_t)(tb + i) * a.d + c, xv[i]);
+                } else {
+#pragma unroll
+                    for (int q = 0; q < 8; ++q) xv[i][q] = 0.f;
+                }
+            }
+#pragma unroll
+            for (int e = 0; e < EMAX; ++e) {
+                if (e < a.E) {
+                    float wv[8];
+                    load8_f32(a.W_r + (size_t)e * a.d + c, wv);
+#pragma unroll
+                    for (int i = 0; i < TW; ++i)
+#pragma unroll
+                        for (int q = 0; q < 8; ++q) acc[i][e] = fmaf(xv[i][q], wv[q], acc[i][e]);
+                }
+            }
+        }
+#pragma unroll
+        for (int i = 0; i < TW; ++i)
+#pragma unroll
+            for (int e = 0; e < EMAX; ++e)
+#pragma unroll
+                for (int o = 16; o > 0; o >>= 1)
+                    acc[i][e] += __shfl_xor_sync(0xffffffffu, acc[i][e], o);
+        if (DS > 1) {
+            if (lane == 0) {
+#pragma unroll
+                for (int i = 0; i < TW; ++i)
+#pragma unroll
+                    for (int e = 0; e < EMAX; ++e) s_red[(warp * TW + i) * EMAX + e] = acc[i][e];
+            }
+            __syncthreads();
+            if (split == 0) {
+#pragma unroll
+                for (int i = 0; i < TW; ++i)
+#pragma unroll
+                    for (int e = 0; e < EMAX; ++e) {
+                        float v = 0.f;
+#pragma unroll
+                        for (int s2 = 0; s2 < DS; ++s2)
+                            v += s_red[((grp * DS + s2) * TW + i) * EMAX + e];
+                        acc[i][e] = v;
+                    }
+            }
+        }
+        if (a.bias != nullptr) {
+#pragma unroll
+            for (int e = 0; e < EMAX; ++e) {
+                const float b = e < a.E ? __ldg(a.bias + e) : 0.f;
+#pragma unroll
+                for (int i = 0; i < TW; ++i) acc[i][e] += b;
+            }
+        }
+    } else {
+#pragma unroll
+        for (int i = 0; i < TW; ++i)
+#pragma unroll
+            for (int e = 0; e < EMAX; ++e)
+                if (tb + i < a.T && e < a.E) acc[i][e] = __ldg(a.logits_in + (size_t)(tb + i) * a.E + e);
+    }
+
+    // the group's logits go to shared memory; then one thread per token
+    if (split == 0 && lane == 0) {
+#pragma unroll
+        for (int i = 0; i < TW; ++i)
+#pragma unroll
+            for (int e = 0; e < EMAX; ++e) s_p[(grp * TW + i) * LDS + e] = acc[i][e];
+    }
+    __syncthreads();
+    if (tid < TB) {
+        const int t = blockIdx.x * TB + tid;
+        float* prow = s_p + tid * LDS;
+        if (t < a.T) {
+            float g[EMAX];
+            float m = -FLT_MAX;
+#pragma unroll
+            for (int e = 0; e < EMAX; ++e) {
+                g[e] = e < a.E ? prow[e] : -FLT_MAX;
+                m = fmaxf(m, g[e]);
+            }
+            float ex[EMAX];
+            float ssum = 0.f;
+#pragma unroll
+            for (int e = 0; e < EMAX; ++e) {
+                ex[e] = e < a.E ? expf(g[e] - m) : 0.f;
+                ssum += ex[e];
+            }
+            const float inv = 1.0f / ssum;
+            if (a.logits_out != nullptr)
+                for (int e = 0; e < a.E; ++e) a.logits_out[(size_t)t * a.E + e] = prow[e];
+#pragma unroll
+            for (int e = 0; e < EMAX; ++e) prow[e] = ex[e] * inv;  // p replaces g
+            // top-k on the logits, larger first, ties to the lower expert index
+            uint32_t taken = 0;
+            int sel_e[kMaxTopK];
+            float sel_x[kMaxTopK];
+            float sel_sum = 0.f;
+            for (int j = 0; j < a.k; ++j) {
+                float bv = -FLT_MAX, bx = 0.f;
+                int be = -1;
+#pragma unroll
+                for (int e = 0; e < EMAX; ++e) {
+                    if (e < a.E && !((taken >> e) & 1u) && (be < 0 || g[e] > bv)) {
+                        bv = g[e];
+                        bx = ex[e];
+                        be = e;
+                    }
+                }
+                taken |= 1u << be;
+                sel_e[j] = be;
+                sel_x[j] = bx;
+                sel_sum += bx;
+            }
+            const float wden = a.renormalize ? 1.0f / sel_sum : inv;
+            for (int j = 0; j < a.k; ++j) {
+                a.topk_idx[(size_t)t * a.k + j] = sel_e[j];
+                a.topk_w[(size_t)t * a.k + j] = sel_x[j] * wden;
+                s_idx[tid * a.k + j] = sel_e[j];
+                atomicAdd(&s_cnt[sel_e[j]], 1);
+            }
+            atomicAdd(&s_top1[sel_e[0]], 1);
+        } else {
+#pragma unroll
+            for (int e = 0; e < EMAX; ++e) prow[e] = 0.f;
+        }
+    }
+    __syncthreads();
+    finish_block<EMAX>(a, s_p, LDS, TB, s_idx, s_cnt, s_top1, wh, carry, s_d, s_part, &s_last);
+}
+
+// ===================================================================== tile kernel
+constexpr int KC = 32;   // columns of x / W_r per shared-memory chunk
+constexpr int RT = 4;    // tokens per thread tile
+constexpr int RE = 8;    // experts per thread tile
 
 template <int EMAX> struct Geo {
     static constexpr int TB = EMAX > 128 ? 32 : 64;  // tokens per block
@@ -68,7 +344,6 @@ __device__ __forceinline__ void stage_chunk(const RouteArgs& a, int t0, int c0, 
                                             float* wsm) {
     using Gm = Geo<EMAX>;
     const TX* x = reinterpret_cast<const TX*>(a.x);
-    // x: TB tokens x (KC/8) groups of 8 columns
     for (int i = threadIdx.x; i < Gm::TB * (KC / 8); i += kThreads) {
         const int tok = i % Gm::TB, cg = i / Gm::TB;
         const int t = t0 + tok, c = c0 + cg * 8;
@@ -82,7 +357,6 @@ __device__ __forceinline__ void stage_chunk(const RouteArgs& a, int t0, int c0, 
 #pragma unroll
         for (int q = 0; q < 8; ++q) xs[(cg * 8 + q) * Gm::TB + tok] = v[q];
     }
-    // W_r: EMAX experts x (KC/8) groups
     for (int i = threadIdx.x; i < EMAX * (KC / 8); i += kThreads) {
         const int e = i % EMAX, cg = i / EMAX;
         const int c = c0 + cg * 8;
@@ -99,7 +373,7 @@ __device__ __forceinline__ void stage_chunk(const RouteArgs& a, int t0, int c0, 
 }
 
 template <typename TX, int EMAX>
-__global__ void __launch_bounds__(kThreads) route_kernel(RouteArgs a) {
+__global__ void __launch_bounds__(kThreads) route_tile_kernel(RouteArgs a) {
     using Gm = Geo<EMAX>;
     extern __shared__ float4 smem_f4[];
     float* smem = reinterpret_cast<float*>(smem_f4);
@@ -107,8 +381,11 @@ __global__ void __launch_bounds__(kThreads) route_kernel(RouteArgs a) {
     float* wsm = xs + Gm::XS;
     float* lg = wsm + Gm::WS;                 // logits tile [TB][LGS] (after reduction)
     float* red = lg;                          // partial tiles, aliases lg
-    __shared__ int s_cnt[EMAX];
-    __shared__ int s_top1[EMAX];
+    __shared__ int s_idx[Gm::TB * kMaxTopK];
+    __shared__ int s_cnt[EMAX], s_top1[EMAX], carry[EMAX];
+    __shared__ int wh[kWarps][EMAX];
+    __shared__ double s_d[EMAX];
+    __shared__ double s_part[kThreads];
     __shared__ int s_last;
 
     const int tid = threadIdx.x;
@@ -116,7 +393,6 @@ __global__ void __launch_bounds__(kThreads) route_kernel(RouteArgs a) {
     for (int e = tid; e < EMAX; e += kThreads) { s_cnt[e] = 0; s_top1[e] = 0; }
 
     if (a.logits_in == nullptr) {
-        // ---- logits tile: SIMT GEMM with a per-thread 4x8 register tile
         const int g = tid % Gm::G, s = tid / Gm::G;
         const int tg = g % Gm::TG, eg = g / Gm::TG;
         float acc[RT][RE];
@@ -143,16 +419,16 @@ __global__ void __launch_bounds__(kThreads) route_kernel(RouteArgs a) {
         }
         __syncthreads();
         if (Gm::S > 1) {
-            // partial tiles -> red[s][g][RT*RE], then a fixed-order sum over s
 #pragma unroll
             for (int i = 0; i < RT; ++i)
 #pragma unroll
-                for (int j = 0; j < RE; ++j) red[((s * Gm::G) + g) * (RT * RE) + i * RE + j] = acc[i][j];
+                for (int j = 0; j < RE; ++j)
+                    red[((s * Gm::G) + g) * (RT * RE) + i * RE + j] = acc[i][j];
             __syncthreads();
             float out[(Gm::G * RT * RE) / kThreads];
 #pragma unroll
             for (int q = 0; q < (Gm::G * RT * RE) / kThreads; ++q) {
-                const int o = tid + q * kThreads;  // o = gg * (RT*RE) + r
+                const int o = tid + q * kThreads;
                 float v = 0.f;
                 for (int ss = 0; ss < Gm::S; ++ss) v += red[ss * Gm::G * RT * RE + o];
                 out[q] = v;
@@ -188,10 +464,10 @@ __global__ void __launch_bounds__(kThreads) route_kernel(RouteArgs a) {
     }
     __syncthreads();
 
-    // ---- softmax and top-k, one warp per token; lane l owns experts l + 32 i
+    // softmax and top-k, one warp per token; lane l owns experts l + 32 i
     const int warp = tid / 32, lane = tid % 32;
     constexpr int PER_LANE = (EMAX + 31) / 32;
-    for (int tok = warp; tok < Gm::TB; tok += kThreads / 32) {
+    for (int tok = warp; tok < Gm::TB; tok += kWarps) {
         const int t = t0 + tok;
         if (t >= a.T) {
             for (int e = lane; e < EMAX; e += 32) lg[tok * Gm::LGS + e] = 0.f;
@@ -205,8 +481,7 @@ __global__ void __launch_bounds__(kThreads) route_kernel(RouteArgs a) {
             gv[i] = e < a.E ? lg[tok * Gm::LGS + e] : -FLT_MAX;
             if (e < a.E) {
                 m = fmaxf(m, gv[i]);
-                if (a.logits_out != nullptr)
-                    a.logits_out[(size_t)t * a.E + e] = gv[i];
+                if (a.logits_out != nullptr) a.logits_out[(size_t)t * a.E + e] = gv[i];
             }
         }
 #pragma unroll
@@ -222,7 +497,6 @@ __global__ void __launch_bounds__(kThreads) route_kernel(RouteArgs a) {
 #pragma unroll
         for (int o = 16; o > 0; o >>= 1) ssum += __shfl_xor_sync(0xffffffffu, ssum, o);
         const float inv = 1.0f / ssum;
-        // top-k: k rounds of a warp arg-max on the logits (ties -> lower index)
         bool taken[PER_LANE];
 #pragma unroll
         for (int i = 0; i < PER_LANE; ++i) taken[i] = false;
@@ -261,11 +535,11 @@ __global__ void __launch_bounds__(kThreads) route_kernel(RouteArgs a) {
             for (int j = 0; j < a.k; ++j) {
                 a.topk_idx[(size_t)t * a.k + j] = sel_e[j];
                 a.topk_w[(size_t)t * a.k + j] = sel_x[j] * wden;
+                s_idx[tok * a.k + j] = sel_e[j];
                 atomicAdd(&s_cnt[sel_e[j]], 1);
             }
             atomicAdd(&s_top1[sel_e[0]], 1);
         }
-        // probabilities replace the logits in the tile (for the column sums)
 #pragma unroll
         for (int i = 0; i < PER_LANE; ++i) {
             const int e = lane + 32 * i;
@@ -273,70 +547,78 @@ __global__ void __launch_bounds__(kThreads) route_kernel(RouteArgs a) {
         }
     }
     __syncthreads();
-
-    // ---- per-block sums of p (fixed token order) and counts
-    for (int e = tid; e < a.E; e += kThreads) {
-        float v = 0.f;
-        for (int tok = 0; tok < Gm::TB; ++tok) v += lg[tok * Gm::LGS + e];
-        a.blk_p[(size_t)blockIdx.x * a.E + e] = v;
-        if (s_cnt[e]) atomicAdd(&a.counts[e], s_cnt[e]);
-        if (s_top1[e]) atomicAdd(&a.top1[e], s_top1[e]);
-    }
-    __threadfence();
-    __syncthreads();
-    if (tid == 0) s_last = (atomicAdd(&a.hdr->route_done, 1u) == (unsigned)(a.nblk - 1));
-    __syncthreads();
-    if (!s_last) return;
-    __threadfence();
-
-    // ---- last block: P_e over all blocks in block order, then the loss
-    double* dsum = reinterpret_cast<double*>(smem);  // the x chunk region is free now
-    for (int e = tid; e < a.E; e += kThreads) {
-        double v = 0.0;
-        for (int b = 0; b < a.nblk; ++b) v += (double)__ldcg(a.blk_p + (size_t)b * a.E + e);
-        const int c1 = __ldcg(a.top1 + e);
-        dsum[e] = (double)c1 * v;
-        if (a.expert_counts != nullptr) a.expert_counts[e] = __ldcg(a.counts + e);
-    }
-    __syncthreads();
-    if (tid == 0 && a.aux_out != nullptr) {
-        double s = 0.0;
-        for (int e = 0; e < a.E; ++e) s += dsum[e];
-        const double Td = (double)a.T;
-        a.aux_out[0] = (float)((double)a.E * s / (Td * Td));
-    }
+    finish_block<EMAX>(a, lg, Gm::LGS, Gm::TB, s_idx, s_cnt, s_top1, wh, carry, s_d, s_part,
+                       &s_last);
 }
 
 template <typename TX, int EMAX>
-cudaError_t launch_t(const RouteArgs& a, cudaStream_t s) {
+cudaError_t launch_tile(const RouteArgs& a, cudaStream_t s) {
     using Gm = Geo<EMAX>;
     const size_t smem = (size_t)Gm::SMEM_FLOATS * sizeof(float);
-    cudaError_t err = cudaFuncSetAttribute(route_kernel<TX, EMAX>,
-                                           cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    cudaError_t err = ensure_smem<route_tile_kernel<TX, EMAX>>((int)smem);
     if (err != cudaSuccess) return err;
-    route_kernel<TX, EMAX><<<a.nblk, kThreads, smem, s>>>(a);
+    route_tile_kernel<TX, EMAX><<<a.nblk, kThreads, smem, s>>>(a);
     count_launches(1);
     return cudaGetLastError();
 }
 
+template <typename TX, int EMAX, int TW, int DS>
+cudaError_t launch_warp(const RouteArgs& a, cudaStream_t s) {
+    route_warp_kernel<TX, EMAX, TW, DS><<<a.nblk, kThreads, 0, s>>>(a);
+    count_launches(1);
+    return cudaGetLastError();
+}
+
+template <typename TX, int EMAX>
+cudaError_t launch_warp_tw(const RouteArgs& a, const RouteGeom& g, cudaStream_t s) {
+    if (g.tw >= 4) return launch_warp<TX, EMAX, 4, 1>(a, s);
+    if (g.tw == 2) return launch_warp<TX, EMAX, 2, 1>(a, s);
+    if (g.ds >= 8) return launch_warp<TX, EMAX, 1, 8>(a, s);
+    if (g.ds == 4) return launch_warp<TX, EMAX, 1, 4>(a, s);
+    if (g.ds == 2) return launch_warp<TX, EMAX, 1, 2>(a, s);
+    return launch_warp<TX, EMAX, 1, 1>(a, s);
+}
+
 template <typename TX>
-cudaError_t launch_e(const RouteArgs& a, cudaStream_t s) {
-    if (a.E <= 8) return launch_t<TX, 8>(a, s);
-    if (a.E <= 16) return launch_t<TX, 16>(a, s);
-    if (a.E <= 32) return launch_t<TX, 32>(a, s);
-    if (a.E <= 64) return launch_t<TX, 64>(a, s);
-    if (a.E <= 128) return launch_t<TX, 128>(a, s);
-    return launch_t<TX, 256>(a, s);
+cudaError_t launch_e(const RouteArgs& a, const RouteGeom& g, cudaStream_t s) {
+    if (g.warp) {
+        if (a.E <= 8) return launch_warp_tw<TX, 8>(a, g, s);
+        if (a.E <= 16) return launch_warp_tw<TX, 16>(a, g, s);
+        return launch_warp_tw<TX, 32>(a, g, s);
+    }
+    if (a.E <= 64) return launch_tile<TX, 64>(a, s);
+    if (a.E <= 128) return launch_tile<TX, 128>(a, s);
+    return launch_tile<TX, 256>(a, s);
 }
 
 }  // namespace
 
-int route_tokens_per_block(int E) { return E > 128 ? Geo<256>::TB : Geo<8>::TB; }
+RouteGeom route_geom(const moe_config& c) {
+    RouteGeom g{};
+    constexpr int kTargetBlocks = 296;  // two blocks per SM at least, where T allows
+    if (c.E <= 32) {
+        g.warp = true;
+        int tw = c.E <= 16 ? 4 : 2, ds = 1;
+        while (tw > 1 && (c.T + kWarps * tw - 1) / (kWarps * tw) < kTargetBlocks) tw /= 2;
+        while (tw == 1 && ds < kWarps && (c.T * ds + kWarps - 1) / kWarps < kTargetBlocks) ds *= 2;
+        g.tw = tw;
+        g.ds = ds;
+        g.tokens = (kWarps / ds) * tw;
+    } else {
+        g.warp = false;
+        g.tw = 0;
+        g.ds = 1;
+        g.tokens = c.E > 128 ? Geo<256>::TB : Geo<64>::TB;
+    }
+    g.blocks = (c.T + g.tokens - 1) / g.tokens;
+    return g;
+}
 
 cudaError_t launch_route(const moe_config& c, const void* x, const float* W_r,
                          const float* logit_bias, const float* logits_in, float* logits_out,
                          int32_t* topk_idx, float* topk_w, int32_t* expert_counts,
-                         float* aux_out, void* ws, const WsLayout& L, cudaStream_t s) {
+                         float* aux_out, void* ws, const WsLayout& L, bool fuse_count,
+                         cudaStream_t s) {
     RouteArgs a;
     a.x = x; a.W_r = W_r; a.bias = logit_bias; a.logits_in = logits_in; a.logits_out = logits_out;
     a.topk_idx = topk_idx; a.topk_w = topk_w; a.expert_counts = expert_counts; a.aux_out = aux_out;
@@ -344,15 +626,18 @@ cudaError_t launch_route(const moe_config& c, const void* x, const float* W_r,
     a.counts = at<int32_t>(ws, L.counts);
     a.top1 = at<int32_t>(ws, L.top1);
     a.blk_p = at<float>(ws, L.blk_p);
+    a.blk_hist = fuse_count ? at<int32_t>(ws, L.blk_hist) : nullptr;
+    a.local_rank = at<int32_t>(ws, L.local_rank);
     a.T = c.T; a.d = c.d; a.E = c.E; a.k = c.k; a.renormalize = c.renormalize;
-    a.nblk = L.route_blocks;
+    a.nblk = L.route.blocks;
     // per-call counters: route_done and the two count arrays start at zero
     cudaError_t err = cudaMemsetAsync(at<char>(ws, L.header + offsetof(DeviceHeader, route_done)),
                                       0, sizeof(uint32_t), s);
     if (err != cudaSuccess) return err;
     err = cudaMemsetAsync(at<char>(ws, L.counts), 0, L.blk_p - L.counts, s);
     if (err != cudaSuccess) return err;
-    return c.dtype == MOE_BF16 ? launch_e<__nv_bfloat16>(a, s) : launch_e<float>(a, s);
+    return c.dtype == MOE_BF16 ? launch_e<__nv_bfloat16>(a, L.route, s)
+                               : launch_e<float>(a, L.route, s);
 }
 
 }  // namespace moe

@@ -72,3 +72,23 @@ class MoELayer:
         return y, aux
 
     __call__ = forward
+
+
+def capture_graph(fn, stream=None, warmup: int = 2):
+    """Record the libmoe calls made by ``fn(stream)`` into a CUDA graph.
+
+    ``fn`` must enqueue its work on the stream it is given and use fixed
+    buffers; ``graph.replay()`` then re-runs the recorded kernels with one
+    launch.  Warm-up calls run first, outside the capture, so that one-time
+    host work (kernel attributes, driver entry points) is done before it."""
+    side = torch.cuda.Stream() if stream is None else stream
+    side.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(side):
+        for _ in range(warmup):
+            fn(side)
+    torch.cuda.current_stream().wait_stream(side)
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=side, capture_error_mode="thread_local"):
+        fn(torch.cuda.current_stream())
+    return g
