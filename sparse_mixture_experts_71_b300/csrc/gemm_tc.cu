@@ -138,6 +138,65 @@ __device__ __forceinline__ void drain_bar(uint64_t* bar, uint32_t parity) {
 // every CTA of the cluster, so each CTA fetches 1/CS of the token tile from
 // L2.  A stage may be refilled only when all CS CTAs have consumed it, so
 // every MMA commit arrives on the stage's empty barrier of all CS CTAs.
+// Epilogue of one accumulator tile: this warp reads TMEM lanes 32q..32q+31
+// (weight rows fbase + 32q + lane) and the token columns of its half of the
+// COLS-wide tile (columns acc_col + c, c < n), applies bias + GELU (first
+// GEMM, bf16 out) or bias x routing weight (second GEMM, fp32 out), and
+// writes token rows r0 + c through a shared-memory transpose (stg: 32 x 32).
+template <int COLS, bool GEMM1>
+__device__ __forceinline__ void epilogue_tile(const Params& p, int e, int r0, int n, int fbase,
+                                              uint32_t tmem_base, int acc_col, int q, int half,
+                                              int lane, uint8_t* stg) {
+    const int f0 = fbase + q * 32;  // first weight row (output feature) of this warp
+    const int f = f0 + lane;
+    const float bias =
+        f < p.n_out ? __bfloat162float(p.bias[(size_t)e * p.n_out + f]) : 0.f;
+    const int c_begin = half * (COLS / 2), c_end = min(c_begin + COLS / 2, n);
+    for (int c = c_begin; c < c_end; c += 32) {
+        float v[32];
+        tc::tmem_ld_32cols(tmem_base + ((uint32_t)(q * 32) << 16) +
+                               (uint32_t)(acc_col + c),
+                           v);
+        const int rows_here = min(32, n - c);
+        if (GEMM1) {
+            __nv_bfloat16* s16 = reinterpret_cast<__nv_bfloat16*>(stg);
+#pragma unroll
+            for (int j = 0; j < 32; ++j)
+                s16[j * 32 + lane] = __float2bfloat16_rn(gelu_as7126(v[j] + bias));
+            __syncwarp();
+            __nv_bfloat16* out = reinterpret_cast<__nv_bfloat16*>(p.out);
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+                const int ci = lane + 32 * i, j = ci >> 2, part = ci & 3;
+                const int fc = f0 + part * 8;
+                if (j < rows_here && fc < p.n_out) {
+                    const uint4 val = *reinterpret_cast<const uint4*>(stg + j * 64 + part * 16);
+                    *reinterpret_cast<uint4*>(out + (size_t)(r0 + c + j) * p.n_out + fc) = val;
+                }
+            }
+        } else {
+            float wl = 1.f;
+            if (p.row_w != nullptr && lane < rows_here) wl = __ldg(p.row_w + r0 + c + lane);
+            float* s32 = reinterpret_cast<float*>(stg);
+#pragma unroll
+            for (int j = 0; j < 32; ++j)
+                s32[j * 32 + lane] = (v[j] + bias) * __shfl_sync(0xffffffffu, wl, j);
+            __syncwarp();
+            float* out = reinterpret_cast<float*>(p.out);
+#pragma unroll
+            for (int i = 0; i < 8; ++i) {
+                const int ci = lane + 32 * i, j = ci >> 3, part = ci & 7;
+                const int fc = f0 + part * 4;
+                if (j < rows_here && fc < p.n_out) {
+                    const float4 val = *reinterpret_cast<const float4*>(stg + j * 128 + part * 16);
+                    *reinterpret_cast<float4*>(out + (size_t)(r0 + c + j) * p.n_out + fc) = val;
+                }
+            }
+        }
+        __syncwarp();
+    }
+}
+
 template <int BN_MAX, int STAGES, bool GEMM1, int CS>
 __global__ void __launch_bounds__(kThreads, 1)
 grouped_gemm_tc(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
@@ -296,54 +355,8 @@ grouped_gemm_tc(const __grid_constant__ CUtensorMap tmA, const __grid_constant__
             const bool ok = wait_bar(&tfull[acc], acc_phase, s_abort, p, 4);
             if (!__all_sync(0xffffffffu, ok)) break;
             tc::fence_after_sync();
-            const int f0 = tl.m0 + q * 32;  // first weight row (output feature) of this warp
-            const int f = f0 + lane;
-            const float bias =
-                f < p.n_out ? __bfloat162float(p.bias[(size_t)tl.e * p.n_out + f]) : 0.f;
-            const int c_begin = half * (BN_MAX / 2), c_end = min(c_begin + BN_MAX / 2, tl.n);
-            for (int c = c_begin; c < c_end; c += 32) {
-                float v[32];
-                tc::tmem_ld_32cols(tmem_base + ((uint32_t)(q * 32) << 16) +
-                                       (uint32_t)(acc * BN_MAX + c),
-                                   v);
-                const int rows_here = min(32, tl.n - c);
-                if (GEMM1) {
-                    __nv_bfloat16* s16 = reinterpret_cast<__nv_bfloat16*>(stg);
-#pragma unroll
-                    for (int j = 0; j < 32; ++j)
-                        s16[j * 32 + lane] = __float2bfloat16_rn(gelu_as7126(v[j] + bias));
-                    __syncwarp();
-                    __nv_bfloat16* out = reinterpret_cast<__nv_bfloat16*>(p.out);
-#pragma unroll
-                    for (int i = 0; i < 4; ++i) {
-                        const int ci = lane + 32 * i, j = ci >> 2, part = ci & 3;
-                        const int fc = f0 + part * 8;
-                        if (j < rows_here && fc < p.n_out) {
-                            const uint4 val = *reinterpret_cast<const uint4*>(stg + j * 64 + part * 16);
-                            *reinterpret_cast<uint4*>(out + (size_t)(tl.r0 + c + j) * p.n_out + fc) = val;
-                        }
-                    }
-                } else {
-                    float wl = 1.f;
-                    if (p.row_w != nullptr && lane < rows_here) wl = __ldg(p.row_w + tl.r0 + c + lane);
-                    float* s32 = reinterpret_cast<float*>(stg);
-#pragma unroll
-                    for (int j = 0; j < 32; ++j)
-                        s32[j * 32 + lane] = (v[j] + bias) * __shfl_sync(0xffffffffu, wl, j);
-                    __syncwarp();
-                    float* out = reinterpret_cast<float*>(p.out);
-#pragma unroll
-                    for (int i = 0; i < 8; ++i) {
-                        const int ci = lane + 32 * i, j = ci >> 3, part = ci & 7;
-                        const int fc = f0 + part * 4;
-                        if (j < rows_here && fc < p.n_out) {
-                            const float4 val = *reinterpret_cast<const float4*>(stg + j * 128 + part * 16);
-                            *reinterpret_cast<float4*>(out + (size_t)(tl.r0 + c + j) * p.n_out + fc) = val;
-                        }
-                    }
-                }
-                __syncwarp();
-            }
+            epilogue_tile<BN_MAX, GEMM1>(p, tl.e, tl.r0, tl.n, tl.m0, tmem_base, acc * BN_MAX, q,
+                                         half, lane, stg);
             tc::fence_before_sync();
             __syncwarp();
             if (lane == 0) tc::mbar_arrive(&tempty[acc]);
@@ -360,6 +373,206 @@ grouped_gemm_tc(const __grid_constant__ CUtensorMap tmA, const __grid_constant__
     }
     // no CTA leaves while a peer may still multicast into it or arrive on it
     if (CS > 1) tc::cluster_sync();
+}
+
+// ===================================================================== CTA-pair kernel
+// cta_group::2: a cluster of two CTAs (two SMs) computes a 256 x 256 tile
+// D[f][j] (256 weight rows x up to 256 token rows) with one tcgen05.mma of
+// M = 256 per K = 16 step.  CTA r holds weight rows 128r .. 128r+127 (its A)
+// and token rows r*N/2 .. (r+1)*N/2-1 (its half of B) in its own shared
+// memory, and rows 128r .. of the accumulator in its own TMEM.  Per SM and
+// K-step this moves 16 KB of A and 16 KB of B (the single-CTA 128 x 256 tile
+// moves 48 KB).  Each CTA fetches its operands as two whole boxes per K-step
+// (128 x 64 each); rows past a segment's end belong to the next segment or
+// read as zero, and the MMA's N covers only the segment's rows.  Only CTA 0
+// issues MMAs; both CTAs' TMA copies signal CTA 0's full barrier, and CTA 0's
+// commits arrive on both CTAs' barriers (multicast).  Both epilogues arrive
+// on CTA 0's TMEM-empty barrier.
+constexpr int BN2 = 256;  // tokens per pair tile (MMA N, max)
+
+template <int STAGES, bool GEMM1>
+struct Cfg2 {
+    static constexpr int B_BYTES = (BN2 / 2) * BK * 2;  // 16 KB: this CTA's half of B
+    static constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
+    static constexpr int OUT_ES = GEMM1 ? 2 : 4;
+    static constexpr int STAGING = kEpiWarps * 32 * 32 * OUT_ES;
+    static constexpr int TMEM_COLS = 2 * BN2;
+    static constexpr int OFF_STAGING = STAGES * STAGE_BYTES;
+    static constexpr int OFF_BARS = OFF_STAGING + STAGING;
+    static constexpr int NUM_BARS = 2 * STAGES + 5;
+    static constexpr int OFF_MISC = OFF_BARS + NUM_BARS * 8;
+    static constexpr int OFF_TILES = OFF_MISC + 16;
+    static constexpr int SMEM = OFF_TILES + (kMaxExperts + 1) * 4 + 1023;
+    static_assert(STAGE_BYTES % 1024 == 0, "stage alignment");
+    static_assert(SMEM <= 232448, "shared memory budget");
+};
+
+template <int STAGES, bool GEMM1>
+__global__ void __launch_bounds__(kThreads, 1)
+grouped_gemm_pair(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
+                  const Params p) {
+    using C = Cfg2<STAGES, GEMM1>;
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t* smem = reinterpret_cast<uint8_t*>(
+        (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    uint64_t* full = reinterpret_cast<uint64_t*>(smem + C::OFF_BARS);
+    uint64_t* empty = full + STAGES;
+    uint64_t* tfull = empty + STAGES;
+    uint64_t* tempty = tfull + 2;
+    uint64_t* drain = tempty + 2;
+    uint32_t* s_tmem = reinterpret_cast<uint32_t*>(smem + C::OFF_MISC);
+    volatile int* s_abort = reinterpret_cast<volatile int*>(smem + C::OFF_MISC + 4);
+    int* s_tiles = reinterpret_cast<int*>(smem + C::OFF_TILES);
+
+    const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
+    const int rank = (int)tc::cluster_ctarank();
+    const bool leader = rank == 0;
+    const int pair = blockIdx.x / 2, npairs = gridDim.x / 2;
+    const int mt2 = (p.n_out + 2 * BM - 1) / (2 * BM);  // 256-row weight tiles
+    const int KB = (p.K + BK - 1) / BK;
+
+    if (warp == 0 && lane == 0) {
+        for (int s = 0; s < STAGES; ++s) {
+            tc::mbar_init(&full[s], 1);
+            tc::mbar_init(&empty[s], 1);
+        }
+        for (int a = 0; a < 2; ++a) {
+            tc::mbar_init(&tfull[a], 1);
+            tc::mbar_init(&tempty[a], 2 * kEpiWarps);
+        }
+        tc::mbar_init(drain, 1);
+        *s_abort = 0;
+        tc::fence_barrier_init();
+        tc::tma_prefetch_desc(&tmA);
+        tc::tma_prefetch_desc(&tmB);
+    }
+    if (warp == 2) {
+        tc::tmem_alloc_pair(s_tmem, C::TMEM_COLS);
+        tc::tmem_relinquish_pair();
+    }
+    if (warp == 3) {  // exclusive prefix of pair tiles per expert
+        int run = 0;
+        for (int e0 = 0; e0 < p.E; e0 += 32) {
+            const int e = e0 + lane;
+            int nt = 0;
+            if (e < p.E) {
+                const int s0 = min(max(__ldg(p.offsets + e), 0), p.rows_cap);
+                const int s1 = min(max(__ldg(p.offsets + e + 1), s0), p.rows_cap);
+                nt = ((s1 - s0 + BN2 - 1) / BN2) * mt2;
+            }
+            int v = nt;
+#pragma unroll
+            for (int o = 1; o < 32; o <<= 1) {
+                const int u = __shfl_up_sync(0xffffffffu, v, o);
+                if (lane >= o) v += u;
+            }
+            if (e < p.E) s_tiles[e] = run + v - nt;
+            run += __shfl_sync(0xffffffffu, v, 31);
+        }
+        if (lane == 0) s_tiles[p.E] = run;
+    }
+    tc::fence_before_sync();
+    tc::cluster_sync();  // both CTAs' barriers and TMEM exist before any cross-CTA traffic
+    tc::fence_after_sync();
+    const uint32_t tmem_base = *s_tmem;
+    const int total = s_tiles[p.E];
+
+    if (warp == 0) {
+        // ------------------------------------------------ TMA producer (both CTAs)
+        if (lane == 0) {
+            int stage = 0;
+            uint32_t phase = 0;
+            long long fills = 0;
+            bool ok = true;
+            const uint32_t bytes = 2 * (A_BYTES + C::B_BYTES);  // whole boxes of both CTAs
+            for (int t = pair; t < total && ok; t += npairs) {
+                const Tile tl = decode_tile(t, s_tiles, p, BN2, 1, 0);  // m0 in 256-row units / 2
+                const int m0 = (tl.m0 / BM) * 2 * BM;                  // pair tile base row
+                const int half_rows = ((tl.n + 31) & ~31) / 2;
+                const int arow = tl.e * p.n_out + m0 + rank * BM;
+                const int brow = tl.r0 + rank * half_rows;
+                for (int kb = 0; kb < KB; ++kb) {
+                    if (!wait_bar(&empty[stage], phase ^ 1, s_abort, p, 1)) { ok = false; break; }
+                    if (leader) tc::mbar_expect_tx(&full[stage], bytes);
+                    const uint32_t full_l = tc::cluster_addr(&full[stage], 0);
+                    uint8_t* sa = smem + stage * C::STAGE_BYTES;
+                    tc::tma_load_2d_pair(sa, &tmA, full_l, kb * BK, arow);
+                    tc::tma_load_2d_pair(sa + A_BYTES, &tmB, full_l, kb * BK, brow);
+                    ++fills;
+                    if (++stage == STAGES) { stage = 0; phase ^= 1; }
+                }
+            }
+            // the copies of fill i have landed once its stage was released
+            const long long last = fills < STAGES ? fills : STAGES;
+            for (long long i = fills - last; i < fills; ++i)
+                drain_bar(&empty[i % STAGES], (uint32_t)((i / STAGES) & 1));
+        }
+    } else if (warp == 1) {
+        // ------------------------------------------------ MMA issuer (CTA 0)
+        if (lane == 0 && leader) {
+            int stage = 0, acc = 0;
+            uint32_t phase = 0, acc_phase = 0;
+            bool ok = true;
+            for (int t = pair; t < total && ok; t += npairs) {
+                const Tile tl = decode_tile(t, s_tiles, p, BN2, 1, 0);
+                const uint32_t N = (uint32_t)((tl.n + 31) & ~31);
+                const uint32_t idesc = tc::idesc_bf16_f32(2 * BM, N);
+                if (!wait_bar(&tempty[acc], acc_phase ^ 1, s_abort, p, 2)) break;
+                tc::fence_after_sync();
+                const uint32_t d_tmem = tmem_base + (uint32_t)(acc * BN2);
+                for (int kb = 0; kb < KB; ++kb) {
+                    if (!wait_bar(&full[stage], phase, s_abort, p, 3)) { ok = false; break; }
+                    tc::fence_after_sync();
+                    const uint32_t sa = tc::smem_u32(smem + stage * C::STAGE_BYTES);
+                    const uint32_t sb = sa + A_BYTES;
+#pragma unroll
+                    for (int kk = 0; kk < BK / 16; ++kk) {
+                        tc::mma_bf16_pair(d_tmem, tc::sdesc_k128_sw128(sa + kk * 32),
+                                          tc::sdesc_k128_sw128(sb + kk * 32), idesc,
+                                          (kb | kk) != 0 ? 1u : 0u);
+                    }
+                    tc::mma_commit_pair_mc(&empty[stage], 0x3);
+                    if (++stage == STAGES) { stage = 0; phase ^= 1; }
+                }
+                if (!ok) break;
+                tc::mma_commit_pair_mc(&tfull[acc], 0x3);
+                acc ^= 1;
+                if (acc == 0) acc_phase ^= 1;
+            }
+            // every issued MMA completes before either CTA frees its TMEM
+            tc::mma_commit_pair_mc(drain, 0x3);
+        }
+    } else if (warp >= 4) {
+        // ------------------------------------------------ epilogue (both CTAs)
+        const int ew = warp - 4;
+        const int q = warp & 3;
+        const int half = ew >> 2;
+        uint8_t* stg = smem + C::OFF_STAGING + ew * 32 * 32 * C::OUT_ES;
+        int acc = 0;
+        uint32_t acc_phase = 0;
+        for (int t = pair; t < total; t += npairs) {
+            const Tile tl = decode_tile(t, s_tiles, p, BN2, 1, 0);
+            const int m0 = (tl.m0 / BM) * 2 * BM;
+            const bool ok = wait_bar(&tfull[acc], acc_phase, s_abort, p, 4);
+            if (!__all_sync(0xffffffffu, ok)) break;
+            tc::fence_after_sync();
+            epilogue_tile<BN2, GEMM1>(p, tl.e, tl.r0, tl.n, m0 + rank * BM, tmem_base, acc * BN2,
+                                      q, half, lane, stg);
+            tc::fence_before_sync();
+            __syncwarp();
+            if (lane == 0) tc::mbar_arrive_cluster(tc::cluster_addr(&tempty[acc], 0));
+            acc ^= 1;
+            if (acc == 0) acc_phase ^= 1;
+        }
+    }
+
+    if (warp == 1 && lane == 0) drain_bar(drain, 0);
+    tc::fence_before_sync();
+    tc::cluster_sync();  // no cross-CTA arrive or MMA write is still pending
+    if (warp == 2) {
+        tc::fence_after_sync();
+        tc::tmem_dealloc_pair(tmem_base, C::TMEM_COLS);
+    }
 }
 
 PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
@@ -447,6 +660,31 @@ cudaError_t launch_one(const CUtensorMap& a, const CUtensorMap& b, const Params&
     return cudaGetLastError();
 }
 
+template <int STAGES, bool GEMM1>
+cudaError_t launch_one_pair(const CUtensorMap& a, const CUtensorMap& b, const Params& p,
+                            cudaStream_t s) {
+    using C = Cfg2<STAGES, GEMM1>;
+    constexpr auto kern = grouped_gemm_pair<STAGES, GEMM1>;
+    cudaError_t err = ensure_smem<kern>(C::SMEM);
+    if (err != cudaSuccess) return err;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(2 * resident_clusters<kern>(2, C::SMEM), 1, 1);
+    cfg.blockDim = dim3(kThreads, 1, 1);
+    cfg.dynamicSmemBytes = C::SMEM;
+    cfg.stream = s;
+    cudaLaunchAttribute attr;
+    attr.id = cudaLaunchAttributeClusterDimension;
+    attr.val.clusterDim.x = 2;
+    attr.val.clusterDim.y = 1;
+    attr.val.clusterDim.z = 1;
+    cfg.attrs = &attr;
+    cfg.numAttrs = 1;
+    err = cudaLaunchKernelEx(&cfg, kern, a, b, p);
+    if (err != cudaSuccess) return err;
+    count_launches(1);
+    return cudaGetLastError();
+}
+
 template <int BN_MAX, int STAGES, int CS>
 cudaError_t launch_pair(const CUtensorMap* maps, const Params& p1, const Params& p2,
                         cudaStream_t s) {
@@ -478,7 +716,17 @@ cudaError_t launch_expert_ffn_tc(const moe_config& c, const void* x_perm, int64_
               g_tc_timeout_ns, c.E, c.d_ff, c.d, (int)h_rows};
     Params p2{offsets, reinterpret_cast<const __nv_bfloat16*>(b2), perm_w, y_perm, hdr,
               g_tc_timeout_ns, c.E, c.d, c.d_ff, (int)h_rows};
-    if (wide) return launch_pair<256, 4, kWideCluster>(maps, p1, p2, s);
+    if (wide) {
+        CUtensorMap pm[4];  // 128-row token boxes for the pair kernel
+        pm[0] = maps[0];
+        pm[2] = maps[2];
+        if (!make_map(&pm[1], x_perm, c.d, (uint64_t)x_rows, BN2 / 2) ||
+            !make_map(&pm[3], h, c.d_ff, (uint64_t)h_rows, BN2 / 2))
+            return cudaErrorInvalidValue;
+        cudaError_t err = launch_one_pair<6, true>(pm[0], pm[1], p1, s);
+        if (err != cudaSuccess) return err;
+        return launch_one_pair<6, false>(pm[2], pm[3], p2, s);
+    }
     return launch_pair<64, 8, 1>(maps, p1, p2, s);
 }
 

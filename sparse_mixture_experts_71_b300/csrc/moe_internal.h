@@ -28,6 +28,8 @@ enum DeviceError : int32_t { kErrExpertRange = 1, kErrTimeout = 2 };
 // How the router kernel tiles the batch: `warp` kernel (E <= 32: one warp per
 // `tw` tokens, 8 warps per block) or `tile` kernel (SIMT GEMM tile).
 struct RouteGeom {
+    bool mma;          // tensor-core kernel (bf16 x, E <= 64)
+    int mt;            // 16-token tiles per block (tensor-core kernel)
     bool warp;
     int tw;            // tokens per warp group (warp kernel)
     int ds;            // warps splitting one group's d columns (warp kernel)
@@ -35,6 +37,8 @@ struct RouteGeom {
     int blocks;
 };
 RouteGeom route_geom(const moe_config& c);
+// Rows of each router-weight part for the tensor-core router (8 * its n-tiles).
+int router_epad(int E);
 
 // Byte offsets of the workspace regions for one configuration.
 struct WsLayout {
@@ -45,6 +49,7 @@ struct WsLayout {
     size_t blk_hist;     // int32 [hist_blocks][E]
     size_t blk_base;     // int32 [hist_blocks][E]
     size_t local_rank;   // int32 [T*k]
+    size_t wsplit;       // bf16 [3][roundup(E, 8)][d] router weight parts (tensor-core router)
     size_t topk_idx;     // int32 [T*k]     (moe_forward)
     size_t topk_w;       // fp32  [T*k]     (moe_forward)
     size_t offsets;      // int32 [E+1]     (moe_forward)

@@ -145,6 +145,67 @@ __device__ void finish_block(const RouteArgs& a, const float* s_p, int lds, int 
     }
 }
 
+// Softmax, top-k and gate weights of token t from its logits in prow
+// (EMAX slots, E used); the probabilities replace the logits in prow (zeros
+// for a token past the end of the batch).  One thread per token.
+template <int EMAX>
+__device__ __forceinline__ void token_epilogue(const RouteArgs& a, float* prow, int t, int slot,
+                                               int* s_idx, int* s_cnt, int* s_top1) {
+    if (t >= a.T) {
+#pragma unroll
+        for (int e = 0; e < EMAX; ++e) prow[e] = 0.f;
+        return;
+    }
+    float g[EMAX];
+    float m = -FLT_MAX;
+#pragma unroll
+    for (int e = 0; e < EMAX; ++e) {
+        g[e] = e < a.E ? prow[e] : -FLT_MAX;
+        m = fmaxf(m, g[e]);
+    }
+    float ex[EMAX];
+    float ssum = 0.f;
+#pragma unroll
+    for (int e = 0; e < EMAX; ++e) {
+        ex[e] = e < a.E ? expf(g[e] - m) : 0.f;
+        ssum += ex[e];
+    }
+    const float inv = 1.0f / ssum;
+    if (a.logits_out != nullptr)
+        for (int e = 0; e < a.E; ++e) a.logits_out[(size_t)t * a.E + e] = prow[e];
+#pragma unroll
+    for (int e = 0; e < EMAX; ++e) prow[e] = ex[e] * inv;  // p replaces g
+    // top-k on the logits, larger first, ties to the lower expert index
+    uint64_t taken = 0;
+    int sel_e[kMaxTopK];
+    float sel_x[kMaxTopK];
+    float sel_sum = 0.f;
+    for (int j = 0; j < a.k; ++j) {
+        float bv = -FLT_MAX, bx = 0.f;
+        int be = -1;
+#pragma unroll
+        for (int e = 0; e < EMAX; ++e) {
+            if (e < a.E && !((taken >> e) & 1ull) && (be < 0 || g[e] > bv)) {
+                bv = g[e];
+                bx = ex[e];
+                be = e;
+            }
+        }
+        taken |= 1ull << be;
+        sel_e[j] = be;
+        sel_x[j] = bx;
+        sel_sum += bx;
+    }
+    const float wden = a.renormalize ? 1.0f / sel_sum : inv;
+    for (int j = 0; j < a.k; ++j) {
+        a.topk_idx[(size_t)t * a.k + j] = sel_e[j];
+        a.topk_w[(size_t)t * a.k + j] = sel_x[j] * wden;
+        s_idx[slot * a.k + j] = sel_e[j];
+        atomicAdd(&s_cnt[sel_e[j]], 1);
+    }
+    atomicAdd(&s_top1[sel_e[0]], 1);
+}
+
 // ===================================================================== warp kernel
 // DS warps split one token group's d columns (DS > 1 for small batches, so
 // that enough blocks exist); their partial logits meet in shared memory and
@@ -255,65 +316,154 @@ __global__ void __launch_bounds__(kThreads) route_warp_kernel(RouteArgs a) {
             for (int e = 0; e < EMAX; ++e) s_p[(grp * TW + i) * LDS + e] = acc[i][e];
     }
     __syncthreads();
-    if (tid < TB) {
-        const int t = blockIdx.x * TB + tid;
-        float* prow = s_p + tid * LDS;
-        if (t < a.T) {
-            float g[EMAX];
-            float m = -FLT_MAX;
+    if (tid < TB) token_epilogue<EMAX>(a, s_p + tid * LDS, blockIdx.x * TB + tid, tid, s_idx, s_cnt, s_top1);
+    __syncthreads();
+    finish_block<EMAX>(a, s_p, LDS, TB, s_idx, s_cnt, s_top1, wh, carry, s_d, s_part, &s_last);
+}
+
+// ===================================================================== tensor-core kernel
+// bf16 x with E <= 64.  The logits are a skinny GEMM (N = E); each warp owns
+// a 16-token tile and runs mma.sync m16n8k16 (bf16 in, fp32 accumulate)
+// against W_r split into three bf16 parts (hi + mid + lo = W_r exactly), so
+// every product is exact and only the fp32 accumulation rounds, as in the
+// fp32 SIMT path.  The K order inside each 32-column chunk is permuted so
+// that one 16-byte load per row feeds two MMAs: MMA column slots (2t, 2t+1,
+// 2t+8, 2t+9) of lane quad t map to physical columns 8t .. 8t+3 in the first
+// MMA and 8t+4 .. 8t+7 in the second, identically for x and W_r.
+// DS warps split the d columns of one tile when the batch is small; their
+// partial tiles are added in split order.
+
+// W_r (fp32 [E][d]) -> three bf16 parts [3][epad][d], rows >= E zero.
+__global__ void __launch_bounds__(256) split_router_weight(const float* __restrict__ W, int E,
+                                                           int epad, int d,
+                                                           __nv_bfloat16* __restrict__ out) {
+    const size_t n = (size_t)epad * d;
+    for (size_t i = blockIdx.x * (size_t)blockDim.x + threadIdx.x; i < n;
+         i += (size_t)gridDim.x * blockDim.x) {
+        const int e = (int)(i / d);
+        const float w = e < E ? __ldg(W + i) : 0.f;
+        const __nv_bfloat16 hi = __float2bfloat16_rn(w);
+        const float r1 = w - __bfloat162float(hi);
+        const __nv_bfloat16 mid = __float2bfloat16_rn(r1);
+        const float r2 = r1 - __bfloat162float(mid);
+        out[i] = hi;
+        out[n + i] = mid;
+        out[2 * n + i] = __float2bfloat16_rn(r2);
+    }
+}
+
+__device__ __forceinline__ void mma_bf16_16816(float (&d)[4], uint32_t a0, uint32_t a1,
+                                               uint32_t a2, uint32_t a3, uint32_t b0,
+                                               uint32_t b1) {
+    asm volatile(
+        "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0, %1, %2, %3}, "
+        "{%4, %5, %6, %7}, {%8, %9}, {%0, %1, %2, %3};"
+        : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+        : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+}
+
+template <int NT, int MT>
+__global__ void __launch_bounds__(kThreads) route_mma_kernel(RouteArgs a,
+                                                            const __nv_bfloat16* __restrict__ wsp,
+                                                            int epad) {
+    constexpr int EMAX = 8 * NT;
+    constexpr int DS = kWarps / MT;
+    constexpr int TB = 16 * MT;
+    constexpr int LDS = EMAX + 1;
+    constexpr int BUF = (DS > 1 && kWarps * 16 * EMAX > TB * LDS) ? kWarps * 16 * EMAX : TB * LDS;
+    __shared__ float s_buf[BUF];  // split partials, then logits / probabilities [TB][LDS]
+    __shared__ int s_idx[TB * kMaxTopK];
+    __shared__ int s_cnt[EMAX], s_top1[EMAX], carry[EMAX];
+    __shared__ int wh[kWarps][EMAX];
+    __shared__ double s_d[EMAX];
+    __shared__ double s_part[kThreads];
+    __shared__ int s_last;
+
+    const int tid = threadIdx.x, warp = tid / 32, lane = tid % 32;
+    const int mtile = warp / DS, split = warp % DS;
+    const int g = lane >> 2, tq = lane & 3;
+    if (tid < EMAX) { s_cnt[tid] = 0; s_top1[tid] = 0; }
+    const int tok0 = blockIdx.x * TB + mtile * 16;
+    const int r0 = tok0 + g, r1 = tok0 + g + 8;
+
+    float acc[NT][4];
 #pragma unroll
-            for (int e = 0; e < EMAX; ++e) {
-                g[e] = e < a.E ? prow[e] : -FLT_MAX;
-                m = fmaxf(m, g[e]);
+    for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+        for (int q = 0; q < 4; ++q) acc[nt][q] = 0.f;
+
+    if (a.logits_in == nullptr) {
+        const __nv_bfloat16* x = reinterpret_cast<const __nv_bfloat16*>(a.x);
+        const int nchunk = (a.d + 31) / 32;
+        const size_t plane = (size_t)epad * a.d;
+#pragma unroll 2
+        for (int ch = split; ch < nchunk; ch += DS) {
+            const int c = ch * 32 + 8 * tq;
+            const bool cin = c < a.d;
+            uint4 xa = make_uint4(0, 0, 0, 0), xb = make_uint4(0, 0, 0, 0);
+            if (cin && r0 < a.T) xa = __ldg(reinterpret_cast<const uint4*>(x + (size_t)r0 * a.d + c));
+            if (cin && r1 < a.T) xb = __ldg(reinterpret_cast<const uint4*>(x + (size_t)r1 * a.d + c));
+#pragma unroll
+            for (int nt = 0; nt < NT; ++nt) {
+#pragma unroll
+                for (int part = 0; part < 3; ++part) {
+                    uint4 wv = make_uint4(0, 0, 0, 0);
+                    if (cin)
+                        wv = __ldg(reinterpret_cast<const uint4*>(
+                            wsp + part * plane + (size_t)(nt * 8 + g) * a.d + c));
+                    mma_bf16_16816(acc[nt], xa.x, xb.x, xa.y, xb.y, wv.x, wv.y);
+                    mma_bf16_16816(acc[nt], xa.z, xb.z, xa.w, xb.w, wv.z, wv.w);
+                }
             }
-            float ex[EMAX];
-            float ssum = 0.f;
+        }
+        if (DS > 1) {
+            // partial tiles of the splits -> s_buf[warp][16][EMAX]; split 0 adds them in order
 #pragma unroll
-            for (int e = 0; e < EMAX; ++e) {
-                ex[e] = e < a.E ? expf(g[e] - m) : 0.f;
-                ssum += ex[e];
+            for (int nt = 0; nt < NT; ++nt) {
+                float* row0 = s_buf + (warp * 16 + g) * EMAX + nt * 8 + 2 * tq;
+                float* row1 = s_buf + (warp * 16 + g + 8) * EMAX + nt * 8 + 2 * tq;
+                row0[0] = acc[nt][0]; row0[1] = acc[nt][1];
+                row1[0] = acc[nt][2]; row1[1] = acc[nt][3];
             }
-            const float inv = 1.0f / ssum;
-            if (a.logits_out != nullptr)
-                for (int e = 0; e < a.E; ++e) a.logits_out[(size_t)t * a.E + e] = prow[e];
+            __syncthreads();
+            if (split == 0) {
 #pragma unroll
-            for (int e = 0; e < EMAX; ++e) prow[e] = ex[e] * inv;  // p replaces g
-            // top-k on the logits, larger first, ties to the lower expert index
-            uint32_t taken = 0;
-            int sel_e[kMaxTopK];
-            float sel_x[kMaxTopK];
-            float sel_sum = 0.f;
-            for (int j = 0; j < a.k; ++j) {
-                float bv = -FLT_MAX, bx = 0.f;
-                int be = -1;
+                for (int nt = 0; nt < NT; ++nt) {
 #pragma unroll
-                for (int e = 0; e < EMAX; ++e) {
-                    if (e < a.E && !((taken >> e) & 1u) && (be < 0 || g[e] > bv)) {
-                        bv = g[e];
-                        bx = ex[e];
-                        be = e;
+                    for (int q = 0; q < 4; ++q) {
+                        const int row = g + (q >> 1) * 8, col = nt * 8 + 2 * tq + (q & 1);
+                        float v = 0.f;
+                        for (int s2 = 0; s2 < DS; ++s2)
+                            v += s_buf[((mtile * DS + s2) * 16 + row) * EMAX + col];
+                        acc[nt][q] = v;
                     }
                 }
-                taken |= 1u << be;
-                sel_e[j] = be;
-                sel_x[j] = bx;
-                sel_sum += bx;
             }
-            const float wden = a.renormalize ? 1.0f / sel_sum : inv;
-            for (int j = 0; j < a.k; ++j) {
-                a.topk_idx[(size_t)t * a.k + j] = sel_e[j];
-                a.topk_w[(size_t)t * a.k + j] = sel_x[j] * wden;
-                s_idx[tid * a.k + j] = sel_e[j];
-                atomicAdd(&s_cnt[sel_e[j]], 1);
-            }
-            atomicAdd(&s_top1[sel_e[0]], 1);
-        } else {
+            __syncthreads();  // s_buf is rewritten as the logits tile below
+        }
+        if (split == 0) {
 #pragma unroll
-            for (int e = 0; e < EMAX; ++e) prow[e] = 0.f;
+            for (int nt = 0; nt < NT; ++nt) {
+#pragma unroll
+                for (int q = 0; q < 4; ++q) {
+                    const int row = g + (q >> 1) * 8, col = nt * 8 + 2 * tq + (q & 1);
+                    float v = acc[nt][q];
+                    if (a.bias != nullptr && col < a.E) v += __ldg(a.bias + col);
+                    s_buf[(mtile * 16 + row) * LDS + col] = v;
+                }
+            }
+        }
+    } else {
+        for (int i = tid; i < TB * EMAX; i += kThreads) {
+            const int tok = i / EMAX, e = i % EMAX;
+            const int t = blockIdx.x * TB + tok;
+            s_buf[tok * LDS + e] = (t < a.T && e < a.E) ? __ldg(a.logits_in + (size_t)t * a.E + e) : 0.f;
         }
     }
     __syncthreads();
-    finish_block<EMAX>(a, s_p, LDS, TB, s_idx, s_cnt, s_top1, wh, carry, s_d, s_part, &s_last);
+    if (tid < TB) token_epilogue<EMAX>(a, s_buf + tid * LDS, blockIdx.x * TB + tid, tid, s_idx, s_cnt, s_top1);
+    __syncthreads();
+    finish_block<EMAX>(a, s_buf, LDS, TB, s_idx, s_cnt, s_top1, wh, carry, s_d, s_part, &s_last);
 }
 
 // ===================================================================== tile kernel
@@ -579,6 +729,38 @@ cudaError_t launch_warp_tw(const RouteArgs& a, const RouteGeom& g, cudaStream_t 
     return launch_warp<TX, EMAX, 1, 1>(a, s);
 }
 
+template <int NT, int MT>
+cudaError_t launch_mma_t(const RouteArgs& a, const __nv_bfloat16* wsp, int epad, cudaStream_t s) {
+    route_mma_kernel<NT, MT><<<a.nblk, kThreads, 0, s>>>(a, wsp, epad);
+    count_launches(1);
+    return cudaGetLastError();
+}
+
+template <int NT>
+cudaError_t launch_mma_nt(const RouteArgs& a, const RouteGeom& g, const __nv_bfloat16* wsp,
+                          cudaStream_t s) {
+    if (g.mt >= 8) return launch_mma_t<NT, 8>(a, wsp, 8 * NT, s);
+    if (g.mt == 4) return launch_mma_t<NT, 4>(a, wsp, 8 * NT, s);
+    if (g.mt == 2) return launch_mma_t<NT, 2>(a, wsp, 8 * NT, s);
+    return launch_mma_t<NT, 1>(a, wsp, 8 * NT, s);
+}
+
+cudaError_t launch_mma(const RouteArgs& a, const RouteGeom& g, __nv_bfloat16* wsp,
+                       cudaStream_t s) {
+    const int epad = router_epad(a.E);
+    if (a.logits_in == nullptr) {
+        const size_t n = (size_t)epad * a.d;
+        int blocks = (int)((n + 255) / 256);
+        blocks = blocks < num_sms() * 4 ? blocks : num_sms() * 4;
+        split_router_weight<<<blocks, 256, 0, s>>>(a.W_r, a.E, epad, a.d, wsp);
+        count_launches(1);
+    }
+    if (epad <= 8) return launch_mma_nt<1>(a, g, wsp, s);
+    if (epad <= 16) return launch_mma_nt<2>(a, g, wsp, s);
+    if (epad <= 32) return launch_mma_nt<4>(a, g, wsp, s);
+    return launch_mma_nt<8>(a, g, wsp, s);
+}
+
 template <typename TX>
 cudaError_t launch_e(const RouteArgs& a, const RouteGeom& g, cudaStream_t s) {
     if (g.warp) {
@@ -593,10 +775,19 @@ cudaError_t launch_e(const RouteArgs& a, const RouteGeom& g, cudaStream_t s) {
 
 }  // namespace
 
+int router_epad(int E) { return E <= 8 ? 8 : E <= 16 ? 16 : E <= 32 ? 32 : 64; }
+
 RouteGeom route_geom(const moe_config& c) {
     RouteGeom g{};
     constexpr int kTargetBlocks = 296;  // two blocks per SM at least, where T allows
-    if (c.E <= 32) {
+    if (c.dtype == MOE_BF16 && c.E <= 64) {
+        g.mma = true;
+        int mt = 8;
+        while (mt > 1 && (c.T + 16 * mt - 1) / (16 * mt) < kTargetBlocks) mt /= 2;
+        g.mt = mt;
+        g.ds = kWarps / mt;
+        g.tokens = 16 * mt;
+    } else if (c.E <= 32) {
         g.warp = true;
         int tw = c.E <= 16 ? 4 : 2, ds = 1;
         while (tw > 1 && (c.T + kWarps * tw - 1) / (kWarps * tw) < kTargetBlocks) tw /= 2;
@@ -636,6 +827,7 @@ cudaError_t launch_route(const moe_config& c, const void* x, const float* W_r,
     if (err != cudaSuccess) return err;
     err = cudaMemsetAsync(at<char>(ws, L.counts), 0, L.blk_p - L.counts, s);
     if (err != cudaSuccess) return err;
+    if (L.route.mma) return launch_mma(a, L.route, at<__nv_bfloat16>(ws, L.wsplit), s);
     return c.dtype == MOE_BF16 ? launch_e<__nv_bfloat16>(a, L.route, s)
                                : launch_e<float>(a, L.route, s);
 }
