@@ -28,7 +28,9 @@ enum DeviceError : int32_t { kErrExpertRange = 1, kErrTimeout = 2 };
 // How the router kernel tiles the batch: `warp` kernel (E <= 32: one warp per
 // `tw` tokens, 8 warps per block) or `tile` kernel (SIMT GEMM tile).
 struct RouteGeom {
-    bool mma;          // tensor-core kernel (bf16 x, E <= 64)
+    bool tc;           // tcgen05 kernel (bf16 x, 16 < E <= 64)
+    bool mma;          // mma.sync kernel (bf16 x, E <= 16)
+    int epad;          // rows per router-weight part (tensor-core kernels)
     int mt;            // 16-token tiles per block (tensor-core kernel)
     bool warp;
     int tw;            // tokens per warp group (warp kernel)
@@ -37,8 +39,6 @@ struct RouteGeom {
     int blocks;
 };
 RouteGeom route_geom(const moe_config& c);
-// Rows of each router-weight part for the tensor-core router (8 * its n-tiles).
-int router_epad(int E);
 
 // Byte offsets of the workspace regions for one configuration.
 struct WsLayout {

@@ -1,0 +1,192 @@
+// Pieces shared by the router kernels (route.cu, route_tc.cu): argument
+// block, per-token softmax / top-k, per-block statistics and the
+// deterministic auxiliary-loss reduction.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <float.h>
+
+#include "moe_device.cuh"
+#include "moe_internal.h"
+
+namespace moe {
+namespace rt {
+
+constexpr int kThreads = 256;
+constexpr int kWarps = kThreads / 32;
+
+struct RouteArgs {
+    const void* x;
+    const float* W_r;
+    const float* bias;
+    const float* logits_in;
+    float* logits_out;
+    int32_t* topk_idx;
+    float* topk_w;
+    int32_t* expert_counts;
+    float* aux_out;
+    DeviceHeader* hdr;
+    int32_t* counts;      // ws: [E] all-slot assignments
+    int32_t* top1;        // ws: [E] first-slot choices
+    float* blk_p;         // ws: [nblk][E]
+    int32_t* blk_hist;    // ws: [nblk][E] or null (no fused counting)
+    int32_t* local_rank;  // ws: [T*k]
+    int T, d, E, k, renormalize, nblk;
+};
+
+// Histogram of the block's n assignments (expert ids in s_idx, in (token,
+// slot) order) and the rank of each among the earlier ones of its expert.
+template <int EMAX>
+__device__ void block_rank(const int* s_idx, int n, int E, int (*wh)[EMAX], int* carry,
+                           int32_t* hist_row, int32_t* rank_out) {
+    const int tid = threadIdx.x, warp = tid / 32, lane = tid % 32;
+    for (int e = tid; e < E; e += kThreads) carry[e] = 0;
+    for (int base = 0; base < n; base += kThreads) {
+        for (int i = tid; i < kWarps * EMAX; i += kThreads) (&wh[0][0])[i] = 0;
+        __syncthreads();
+        const int a = base + tid;
+        const int e = a < n ? s_idx[a] : -1;
+        const unsigned same = __match_any_sync(0xffffffffu, e);
+        const int r = __popc(same & ((1u << lane) - 1u));
+        if (e >= 0 && r == 0) wh[warp][e] = __popc(same);
+        __syncthreads();
+        if (e >= 0) {
+            int rr = carry[e] + r;
+            for (int w = 0; w < warp; ++w) rr += wh[w][e];
+            rank_out[a] = rr;
+        }
+        __syncthreads();
+        for (int x = tid; x < E; x += kThreads) {
+            int s = 0;
+#pragma unroll
+            for (int w = 0; w < kWarps; ++w) s += wh[w][x];
+            carry[x] += s;
+        }
+        __syncthreads();
+    }
+    for (int e = tid; e < E; e += kThreads) hist_row[e] = carry[e];
+}
+
+// Per-block sums of p (rows of s_p, fixed order), counts, the fused dispatch
+// histogram, and in the last block the loss and the per-expert counts.
+template <int EMAX>
+__device__ void finish_block(const RouteArgs& a, const float* s_p, int lds, int TB,
+                             const int* s_idx, const int* s_cnt, const int* s_top1,
+                             int (*wh)[EMAX], int* carry, double* s_d, double* s_part,
+                             int* s_last) {
+    const int tid = threadIdx.x;
+    const int t0 = blockIdx.x * TB;
+    for (int e = tid; e < a.E; e += kThreads) {
+        float v = 0.f;
+        for (int tok = 0; tok < TB; ++tok) v += s_p[tok * lds + e];
+        a.blk_p[(size_t)blockIdx.x * a.E + e] = v;
+        if (s_cnt[e]) atomicAdd(&a.counts[e], s_cnt[e]);
+        if (s_top1[e]) atomicAdd(&a.top1[e], s_top1[e]);
+    }
+    if (a.blk_hist != nullptr) {
+        const int n = min(TB, a.T - t0) * a.k;
+        block_rank<EMAX>(s_idx, n, a.E, wh, carry, a.blk_hist + (size_t)blockIdx.x * a.E,
+                         a.local_rank + (size_t)t0 * a.k);
+    }
+    __threadfence();
+    __syncthreads();
+    if (tid == 0) *s_last = (atomicAdd(&a.hdr->route_done, 1u) == (unsigned)(a.nblk - 1));
+    __syncthreads();
+    if (!*s_last) return;
+    __threadfence();
+    // the per-block sums, in block order: thread i < stride (a multiple of E)
+    // owns expert i % E and blocks i / E, i / E + per, ...; the partials of an
+    // expert are then added in thread order
+    const int per = kThreads / a.E;
+    const int stride = per * a.E;
+    double v = 0.0;
+    if (tid < stride) {
+        const int e = tid % a.E;
+#pragma unroll 8
+        for (int b = tid / a.E; b < a.nblk; b += per)
+            v += (double)__ldcg(a.blk_p + (size_t)b * a.E + e);
+    }
+    s_part[tid] = v;
+    __syncthreads();
+    for (int e = tid; e < a.E; e += kThreads) {
+        double pe = 0.0;
+        for (int j = 0; j < per; ++j) pe += s_part[j * a.E + e];
+        s_d[e] = (double)__ldcg(a.top1 + e) * pe;
+        if (a.expert_counts != nullptr) a.expert_counts[e] = __ldcg(a.counts + e);
+    }
+    __syncthreads();
+    if (tid == 0 && a.aux_out != nullptr) {
+        double s = 0.0;
+        for (int e = 0; e < a.E; ++e) s += s_d[e];
+        const double Td = (double)a.T;
+        a.aux_out[0] = (float)((double)a.E * s / (Td * Td));
+    }
+}
+
+// Softmax, top-k and gate weights of token t from its logits in prow
+// (EMAX slots, E used); the probabilities replace the logits in prow (zeros
+// for a token past the end of the batch).  One thread per token.
+template <int EMAX>
+__device__ __forceinline__ void token_epilogue(const RouteArgs& a, float* prow, int t, int slot,
+                                               int* s_idx, int* s_cnt, int* s_top1) {
+    if (t >= a.T) {
+#pragma unroll
+        for (int e = 0; e < EMAX; ++e) prow[e] = 0.f;
+        return;
+    }
+    float g[EMAX];
+    float m = -FLT_MAX;
+#pragma unroll
+    for (int e = 0; e < EMAX; ++e) {
+        g[e] = e < a.E ? prow[e] : -FLT_MAX;
+        m = fmaxf(m, g[e]);
+    }
+    float ex[EMAX];
+    float ssum = 0.f;
+#pragma unroll
+    for (int e = 0; e < EMAX; ++e) {
+        ex[e] = e < a.E ? expf(g[e] - m) : 0.f;
+        ssum += ex[e];
+    }
+    const float inv = 1.0f / ssum;
+    if (a.logits_out != nullptr)
+        for (int e = 0; e < a.E; ++e) a.logits_out[(size_t)t * a.E + e] = prow[e];
+#pragma unroll
+    for (int e = 0; e < EMAX; ++e) prow[e] = ex[e] * inv;  // p replaces g
+    // top-k on the logits, larger first, ties to the lower expert index
+    uint64_t taken = 0;
+    int sel_e[kMaxTopK];
+    float sel_x[kMaxTopK];
+    float sel_sum = 0.f;
+    for (int j = 0; j < a.k; ++j) {
+        float bv = -FLT_MAX, bx = 0.f;
+        int be = -1;
+#pragma unroll
+        for (int e = 0; e < EMAX; ++e) {
+            if (e < a.E && !((taken >> e) & 1ull) && (be < 0 || g[e] > bv)) {
+                bv = g[e];
+                bx = ex[e];
+                be = e;
+            }
+        }
+        taken |= 1ull << be;
+        sel_e[j] = be;
+        sel_x[j] = bx;
+        sel_sum += bx;
+    }
+    const float wden = a.renormalize ? 1.0f / sel_sum : inv;
+    for (int j = 0; j < a.k; ++j) {
+        a.topk_idx[(size_t)t * a.k + j] = sel_e[j];
+        a.topk_w[(size_t)t * a.k + j] = sel_x[j] * wden;
+        s_idx[slot * a.k + j] = sel_e[j];
+        atomicAdd(&s_cnt[sel_e[j]], 1);
+    }
+    atomicAdd(&s_top1[sel_e[0]], 1);
+}
+
+// tcgen05 router (route_tc.cu); np = rows per weight part (16, 32 or 64).
+cudaError_t launch_route_tc(const RouteArgs& a, const __nv_bfloat16* wsplit, int np,
+                            cudaStream_t s);
+
+}  // namespace rt
+}  // namespace moe

@@ -1,0 +1,268 @@
+// Router logits on the 5th-generation tensor cores (tcgen05 + TMEM, TMA-fed)
+// for bf16 token batches, followed by the same softmax / top-k / statistics
+// as the other router kernels.
+//
+// "Mixture of Experts: Scaling Parameters Without Scaling Compute", section
+// "The MoE layer", step 1: g = W_r x, p = softmax(g).
+//
+// Each CTA owns 128 tokens (the MMA's M).  W_r (fp32) is split beforehand
+// into three bf16 parts hi + mid + lo that add up to W_r exactly; the three
+// MMAs of a K = 16 step accumulate x.hi^T + x.mid^T + x.lo^T into one fp32
+// TMEM accumulator of NP columns (NP = E rounded up), so every product is
+// exact and only the fp32 accumulation rounds.  Warp 0 streams 64-column
+// slices of x (128 x 64) and of the three parts (NP x 64 each) into a
+// 4-deep ring; warp 1 issues the MMAs; warps 4-7 read the accumulator back
+// (TMEM lane = token) into shared memory.  Then one thread per token does the
+// softmax and top-k, and the block finishes like the other router kernels.
+
+#include <cuda.h>
+#include <cudaTypedefs.h>
+#include <cuda_runtime.h>
+
+#include <cstring>
+
+#include "route_common.cuh"
+#include "tc_ptx.cuh"
+
+namespace moe {
+namespace {
+
+using namespace rt;
+
+constexpr int TM = 128;                  // tokens per CTA
+constexpr int RBK = 64;                  // K per stage
+constexpr int RA_BYTES = TM * RBK * 2;   // 16 KB
+constexpr int RSTAGES = 4;
+constexpr uint64_t kRouteTimeoutNs = 2000000000ull;
+
+template <int NP>
+struct RCfg {
+    static constexpr int PART_BYTES = NP * RBK * 2;
+    static constexpr int STAGE_BYTES = RA_BYTES + 3 * PART_BYTES;
+    static constexpr int LDS = NP + 1;
+    static constexpr int OFF_P = RSTAGES * STAGE_BYTES;
+    static constexpr int OFF_BARS = OFF_P + ((TM * LDS * 4 + 7) / 8) * 8;
+    static constexpr int NUM_BARS = 2 * RSTAGES + 2;
+    static constexpr int SMEM = OFF_BARS + NUM_BARS * 8 + 1023;
+    static constexpr int TMEM_COLS = NP < 32 ? 32 : NP;
+    static_assert(STAGE_BYTES % 1024 == 0, "stage alignment");
+    static_assert(SMEM <= 232448 - 16384, "shared memory budget");
+};
+
+__device__ __forceinline__ bool wait_or_abort(uint64_t* bar, uint32_t parity, volatile int* abort_flag,
+                                              DeviceHeader* hdr, int where) {
+    if (tc::mbar_try_wait(bar, parity)) return true;
+    const uint64_t t0 = tc::globaltimer();
+    while (!tc::mbar_try_wait(bar, parity)) {
+        if (*abort_flag) return false;
+        if (tc::globaltimer() - t0 > kRouteTimeoutNs) {
+            *abort_flag = 1;
+            record_error(hdr, kErrTimeout, 100 + where);
+            return false;
+        }
+    }
+    return true;
+}
+
+__device__ __forceinline__ void drain_wait(uint64_t* bar, uint32_t parity) {
+    const uint64_t t0 = tc::globaltimer();
+    while (!tc::mbar_try_wait(bar, parity))
+        if (tc::globaltimer() - t0 > kRouteTimeoutNs) break;
+}
+
+template <int NP>
+__global__ void __launch_bounds__(kThreads, 1)
+route_tc_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constant__ CUtensorMap tmW,
+                RouteArgs a) {
+    using C = RCfg<NP>;
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t* smem = reinterpret_cast<uint8_t*>(
+        (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    float* s_p = reinterpret_cast<float*>(smem + C::OFF_P);
+    uint64_t* full = reinterpret_cast<uint64_t*>(smem + C::OFF_BARS);
+    uint64_t* empty = full + RSTAGES;
+    uint64_t* tfull = empty + RSTAGES;
+    uint64_t* drain = tfull + 1;
+    __shared__ uint32_t s_tmem;
+    __shared__ int s_abort;
+    __shared__ int s_idx[TM * kMaxTopK];
+    __shared__ int s_cnt[NP], s_top1[NP], carry[NP];
+    __shared__ int wh[kWarps][NP];
+    __shared__ double s_d[NP];
+    __shared__ double s_part[kThreads];
+    __shared__ int s_last;
+
+    const int tid = threadIdx.x, warp = tid / 32, lane = tid % 32;
+    const int t0 = blockIdx.x * TM;
+    const int KB = (a.d + RBK - 1) / RBK;
+    const bool gemm = a.logits_in == nullptr;
+
+    if (tid < NP) { s_cnt[tid] = 0; s_top1[tid] = 0; }
+    if (warp == 0 && lane == 0) {
+        for (int s = 0; s < RSTAGES; ++s) {
+            tc::mbar_init(&full[s], 1);
+            tc::mbar_init(&empty[s], 1);
+        }
+        tc::mbar_init(tfull, 1);
+        tc::mbar_init(drain, 1);
+        s_abort = 0;
+        tc::fence_barrier_init();
+        if (gemm) {
+            tc::tma_prefetch_desc(&tmX);
+            tc::tma_prefetch_desc(&tmW);
+        }
+    }
+    if (warp == 2) {
+        tc::tmem_alloc(&s_tmem, C::TMEM_COLS);
+        tc::tmem_relinquish();
+    }
+    tc::fence_before_sync();
+    __syncthreads();
+    tc::fence_after_sync();
+    const uint32_t tmem_base = s_tmem;
+    volatile int* abort_flag = &s_abort;
+
+    if (!gemm) {
+        for (int i = tid; i < TM * NP; i += kThreads) {
+            const int tok = i / NP, e = i % NP;
+            const int t = t0 + tok;
+            s_p[tok * C::LDS + e] =
+                (t < a.T && e < a.E) ? __ldg(a.logits_in + (size_t)t * a.E + e) : 0.f;
+        }
+    } else if (warp == 0) {
+        if (lane == 0) {  // ---------------------------------------- TMA producer
+            int stage = 0;
+            uint32_t phase = 0;
+            int fills = 0;
+            for (int kb = 0; kb < KB; ++kb) {
+                if (!wait_or_abort(&empty[stage], phase ^ 1, abort_flag, a.hdr, 1)) break;
+                tc::mbar_expect_tx(&full[stage], C::STAGE_BYTES);
+                uint8_t* sa = smem + stage * C::STAGE_BYTES;
+                tc::tma_load_2d(sa, &tmX, &full[stage], kb * RBK, t0);
+#pragma unroll
+                for (int part = 0; part < 3; ++part)
+                    tc::tma_load_2d(sa + RA_BYTES + part * C::PART_BYTES, &tmW, &full[stage],
+                                    kb * RBK, part * NP);
+                ++fills;
+                if (++stage == RSTAGES) { stage = 0; phase ^= 1; }
+            }
+            const int last = fills < RSTAGES ? fills : RSTAGES;
+            for (int i = fills - last; i < fills; ++i)
+                drain_wait(&full[i % RSTAGES], (uint32_t)((i / RSTAGES) & 1));
+        }
+    } else if (warp == 1) {
+        if (lane == 0) {  // ---------------------------------------- MMA issuer
+            const uint32_t idesc = tc::idesc_bf16_f32(TM, NP);
+            int stage = 0;
+            uint32_t phase = 0;
+            bool ok = true;
+            for (int kb = 0; kb < KB && ok; ++kb) {
+                if (!wait_or_abort(&full[stage], phase, abort_flag, a.hdr, 2)) { ok = false; break; }
+                tc::fence_after_sync();
+                const uint32_t sa = tc::smem_u32(smem + stage * C::STAGE_BYTES);
+#pragma unroll
+                for (int kk = 0; kk < RBK / 16; ++kk)
+#pragma unroll
+                    for (int part = 0; part < 3; ++part)
+                        tc::mma_bf16(tmem_base, tc::sdesc_k128_sw128(sa + kk * 32),
+                                     tc::sdesc_k128_sw128(sa + RA_BYTES + part * C::PART_BYTES +
+                                                          kk * 32),
+                                     idesc, (kb | kk | part) != 0 ? 1u : 0u);
+                tc::mma_commit(&empty[stage]);
+                if (++stage == RSTAGES) { stage = 0; phase ^= 1; }
+            }
+            if (ok) tc::mma_commit(tfull);
+            tc::mma_commit(drain);
+            drain_wait(drain, 0);
+        }
+    } else if (warp >= 4) {  // ------------------------------------ accumulator -> smem
+        const int q = warp & 3;
+        const int tok = q * 32 + lane;
+        const bool ok = wait_or_abort(tfull, 0, abort_flag, a.hdr, 3);
+        if (__all_sync(0xffffffffu, ok)) {
+            tc::fence_after_sync();
+#pragma unroll
+            for (int c0 = 0; c0 < NP; c0 += 32) {
+                float v[32];
+                tc::tmem_ld_32cols(tmem_base + ((uint32_t)(q * 32) << 16) + (uint32_t)c0, v);
+#pragma unroll
+                for (int j = 0; j < 32; ++j) {
+                    const int e = c0 + j;
+                    if (e < NP) {
+                        float g = v[j];
+                        if (a.bias != nullptr && e < a.E) g += __ldg(a.bias + e);
+                        s_p[tok * C::LDS + e] = g;
+                    }
+                }
+            }
+        }
+    }
+    tc::fence_before_sync();
+    __syncthreads();
+    if (warp == 2) {
+        tc::fence_after_sync();
+        tc::tmem_dealloc(tmem_base, C::TMEM_COLS);
+    }
+    if (tid < TM) token_epilogue<NP>(a, s_p + tid * C::LDS, t0 + tid, tid, s_idx, s_cnt, s_top1);
+    __syncthreads();
+    finish_block<NP>(a, s_p, C::LDS, TM, s_idx, s_cnt, s_top1, wh, carry, s_d, s_part, &s_last);
+}
+
+PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
+    static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+    if (fn == nullptr) {
+        void* ptr = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000,
+                                             cudaEnableDefault, &q) == cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(ptr);
+    }
+    return fn;
+}
+
+bool make_map(CUtensorMap* m, const void* base, uint64_t inner, uint64_t outer,
+              uint32_t box_outer) {
+    auto fn = encode_fn();
+    if (fn == nullptr) return false;
+    cuuint64_t dims[2] = {inner, outer};
+    cuuint64_t strides[1] = {inner * 2};
+    cuuint32_t box[2] = {(cuuint32_t)RBK, box_outer};
+    cuuint32_t estr[2] = {1, 1};
+    return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides, box,
+              estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+              CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+template <int NP>
+cudaError_t launch_np(const RouteArgs& a, const __nv_bfloat16* wsplit, cudaStream_t s) {
+    using C = RCfg<NP>;
+    CUtensorMap mx, mw;
+    if (a.logits_in == nullptr) {
+        if (!make_map(&mx, a.x, (uint64_t)a.d, (uint64_t)a.T, TM) ||
+            !make_map(&mw, wsplit, (uint64_t)a.d, (uint64_t)3 * NP, NP))
+            return cudaErrorInvalidValue;
+    } else {
+        memset(&mx, 0, sizeof(mx));
+        memset(&mw, 0, sizeof(mw));
+    }
+    constexpr auto kern = route_tc_kernel<NP>;
+    cudaError_t err = ensure_smem<kern>(C::SMEM);
+    if (err != cudaSuccess) return err;
+    kern<<<a.nblk, kThreads, C::SMEM, s>>>(mx, mw, a);
+    count_launches(1);
+    return cudaGetLastError();
+}
+
+}  // namespace
+
+namespace rt {
+cudaError_t launch_route_tc(const RouteArgs& a, const __nv_bfloat16* wsplit, int np,
+                            cudaStream_t s) {
+    if (np <= 16) return launch_np<16>(a, wsplit, s);
+    if (np <= 32) return launch_np<32>(a, wsplit, s);
+    return launch_np<64>(a, wsplit, s);
+}
+}  // namespace rt
+
+}  // namespace moe
