@@ -7,8 +7,8 @@
 // GEMM).  A token whose assignments were all dropped by the capacity cap
 // ("The central problem: load balancing") gets zero.
 //
-// One warp per token, fp32 accumulation in slot order, 16-byte loads of the
-// fp32 expert rows and 8- or 16-byte stores of the output row.
+// One warp per (token, 512-column chunk), fp32 accumulation in slot order,
+// 16-byte loads of the fp32 expert rows and 8- or 16-byte stores of y.
 
 #include <cuda_runtime.h>
 
@@ -33,37 +33,35 @@ __global__ void __launch_bounds__(256) combine_kernel(const float* __restrict__ 
                                                       int k, int d, TY* __restrict__ y) {
     const int lane = threadIdx.x % 32;
     const int nwarps = gridDim.x * (blockDim.x / 32);
-    const int nv = d / 4;
-    for (int t = blockIdx.x * (blockDim.x / 32) + threadIdx.x / 32; t < T; t += nwarps) {
-        int slots[kMaxTopK];
-        for (int j = 0; j < k; ++j) {
-            const int sl = __ldg(slot_of + (size_t)t * k + j);
-            slots[j] = sl < T * k ? sl : -1;  // y_perm has T*k rows
-        }
-        // four 16-byte columns per lane in flight per row
-        for (int v0 = lane; v0 < nv; v0 += 128) {
-            float4 acc[4];
+    const int nv = d / 4;                   // float4 columns per row
+    const int nch = (nv + 127) / 128;       // 128-column chunks per row (4 per lane)
+    const long long tasks = (long long)T * nch;
+    for (long long task = blockIdx.x * (blockDim.x / 32) + threadIdx.x / 32; task < tasks;
+         task += nwarps) {
+        const int t = (int)(task / nch);
+        const int v0 = (int)(task % nch) * 128 + lane;
+        float4 acc[4];
 #pragma unroll
-            for (int u = 0; u < 4; ++u) acc[u] = make_float4(0.f, 0.f, 0.f, 0.f);
-            for (int j = 0; j < k; ++j) {
-                if (slots[j] < 0) continue;
-                const float4* row = reinterpret_cast<const float4*>(y_perm + (size_t)slots[j] * d);
-                float4 q[4];
-#pragma unroll
-                for (int u = 0; u < 4; ++u)
-                    if (v0 + 32 * u < nv) q[u] = __ldg(row + v0 + 32 * u);
-#pragma unroll
-                for (int u = 0; u < 4; ++u) {
-                    if (v0 + 32 * u < nv) {
-                        acc[u].x += q[u].x; acc[u].y += q[u].y;
-                        acc[u].z += q[u].z; acc[u].w += q[u].w;
-                    }
-                }
-            }
+        for (int u = 0; u < 4; ++u) acc[u] = make_float4(0.f, 0.f, 0.f, 0.f);
+        for (int j = 0; j < k; ++j) {  // slot order
+            int sl = __ldg(slot_of + (size_t)t * k + j);
+            if (sl < 0 || sl >= T * k) continue;  // dropped (y_perm has T*k rows)
+            const float4* row = reinterpret_cast<const float4*>(y_perm + (size_t)sl * d);
+            float4 q[4];
 #pragma unroll
             for (int u = 0; u < 4; ++u)
-                if (v0 + 32 * u < nv) store4(y + (size_t)t * d + 4 * (v0 + 32 * u), acc[u]);
+                if (v0 + 32 * u < nv) q[u] = __ldg(row + v0 + 32 * u);
+#pragma unroll
+            for (int u = 0; u < 4; ++u) {
+                if (v0 + 32 * u < nv) {
+                    acc[u].x += q[u].x; acc[u].y += q[u].y;
+                    acc[u].z += q[u].z; acc[u].w += q[u].w;
+                }
+            }
         }
+#pragma unroll
+        for (int u = 0; u < 4; ++u)
+            if (v0 + 32 * u < nv) store4(y + (size_t)t * d + 4 * (v0 + 32 * u), acc[u]);
     }
 }
 
@@ -72,13 +70,14 @@ __global__ void __launch_bounds__(256) combine_kernel(const float* __restrict__ 
 cudaError_t launch_combine(const moe_config& c, const float* y_perm, const int32_t* slot_of,
                            void* y, cudaStream_t s) {
     if (c.T == 0) return cudaSuccess;
-    int blocks = (c.T + 7) / 8;
-    blocks = blocks < num_sms() * 8 ? blocks : num_sms() * 8;
+    const long long tasks = (long long)c.T * ((c.d / 4 + 127) / 128);
+    long long blocks = (tasks + 7) / 8;
+    if (blocks > num_sms() * 8) blocks = num_sms() * 8;
     if (c.dtype == MOE_BF16)
-        combine_kernel<__nv_bfloat16><<<blocks, 256, 0, s>>>(y_perm, slot_of, c.T, c.k, c.d,
+        combine_kernel<__nv_bfloat16><<<(int)blocks, 256, 0, s>>>(y_perm, slot_of, c.T, c.k, c.d,
                                                              reinterpret_cast<__nv_bfloat16*>(y));
     else
-        combine_kernel<float><<<blocks, 256, 0, s>>>(y_perm, slot_of, c.T, c.k, c.d,
+        combine_kernel<float><<<(int)blocks, 256, 0, s>>>(y_perm, slot_of, c.T, c.k, c.d,
                                                      reinterpret_cast<float*>(y));
     count_launches(1);
     return cudaGetLastError();

@@ -68,12 +68,17 @@ __global__ void __launch_bounds__(kCountBlock) count_kernel(const int32_t* __res
 
 // One block of 1024 threads.  Thread (part, e) with part < P = 1024 / E owns
 // a contiguous range of blocks for expert e.
+// With loss.blk_p set it also finishes the router's statistics (loss and
+// per-expert counts), which removes a launch from the layer's forward pass.
 __global__ void __launch_bounds__(1024) scan_kernel(const int32_t* __restrict__ blk_hist,
                                                     int nblk, int E, int capacity,
                                                     int32_t* __restrict__ blk_base,
-                                                    int32_t* __restrict__ offsets) {
+                                                    int32_t* __restrict__ offsets, LossArgs loss) {
     __shared__ int part_sum[1024];
     __shared__ int s_total[kMaxExperts];
+    __shared__ double s_part[256];
+    __shared__ double s_d[kMaxExperts];
+    if (loss.blk_p != nullptr) loss_and_counts(loss, s_part, s_d);
     const int tid = threadIdx.x;
     const int P = 1024 / E;
     const int part = tid / E, e = tid % E;
@@ -170,12 +175,13 @@ cudaError_t launch_scan_permute(const moe_config& c, const void* x, const int32_
                                 const float* topk_w, int asg_per_block, int hist_blocks,
                                 int32_t* offsets, int32_t* slot_of, int32_t* perm_token,
                                 float* perm_w, void* x_perm, void* ws, const WsLayout& L,
-                                cudaStream_t s) {
+                                const LossArgs& loss, cudaStream_t s) {
     const int n = c.T * c.k;
     int32_t* blk_hist = at<int32_t>(ws, L.blk_hist);
     int32_t* blk_base = at<int32_t>(ws, L.blk_base);
     int32_t* local_rank = at<int32_t>(ws, L.local_rank);
-    scan_kernel<<<1, 1024, 0, s>>>(blk_hist, hist_blocks, c.E, c.capacity, blk_base, offsets);
+    scan_kernel<<<1, 1024, 0, s>>>(blk_hist, hist_blocks, c.E, c.capacity, blk_base, offsets,
+                                   loss);
     count_launches(1);
     if (n > 0) {
         int blocks = (n + 7) / 8;

@@ -7,6 +7,7 @@
 
 #include <atomic>
 
+#include "moe_device.cuh"
 #include "moe_internal.h"
 
 namespace moe {
@@ -199,7 +200,7 @@ moe_status moe_dispatch(const moe_config* cfg, const void* x, const int32_t* top
     cudaError_t e = launch_count(c, topk_idx, ws, L, s);
     if (e == cudaSuccess)
         e = launch_scan_permute(c, x, topk_idx, topk_w, kCountBlock, L.count_blocks, offsets,
-                                slot_of, perm_token, perm_w, x_perm, ws, L, s);
+                                slot_of, perm_token, perm_w, x_perm, ws, L, LossArgs{}, s);
     return from_cuda(e);
 }
 
@@ -263,7 +264,8 @@ moe_status moe_forward(const moe_config* cfg, const void* x, const float* W_r,
                                  aux_out, ws, L, true, s);
     if (e == cudaSuccess)
         e = launch_scan_permute(c, x, idx, w, L.route.tokens * c.k, L.route.blocks, offsets,
-                                slot_of, perm_token, perm_w, x_perm, ws, L, s);
+                                slot_of, perm_token, perm_w, x_perm, ws, L,
+                                route_loss_args(c, ws, L, expert_counts, aux_out), s);
     if (e == cudaSuccess)
         e = launch_expert_ffn(c, x_perm, L.rows, offsets, W1, b1, W2, b2, perm_w, y_perm, ws, L,
                               s);

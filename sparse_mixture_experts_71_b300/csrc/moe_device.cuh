@@ -59,6 +59,52 @@ __device__ __forceinline__ float gelu_as7126(float u) {
     return 0.5f * u * (u < 0.f ? r : 2.0f - r);
 }
 
+// Inputs of the auxiliary-loss reduction: per-block sums of p written by the
+// router (blk_p, nblk rows of E) and the first-slot / all-slot counts.
+struct LossArgs {
+    const float* blk_p;
+    const int32_t* top1;
+    const int32_t* counts;
+    int32_t* expert_counts;  // output or null
+    float* aux_out;          // output or null
+    int nblk, E, T;
+};
+
+// Switch auxiliary loss E * sum_e f_e P_e (f_e = top1_e / T, P_e = the mean
+// probability, summed over the router blocks in block order) and the copy of
+// the per-expert counts, by one block.  Only the first 256 threads take part,
+// so the summation order is the same in every kernel that calls it.
+// s_part: 256 doubles, s_d: E doubles of shared memory.
+__device__ __forceinline__ void loss_and_counts(const LossArgs& l, double* s_part, double* s_d) {
+    const int tid = threadIdx.x;
+    const int per = 256 / l.E;  // threads per expert
+    const int stride = per * l.E;
+    if (tid < 256) {
+        double v = 0.0;
+        if (tid < stride) {
+            const int e = tid % l.E;
+#pragma unroll 8
+            for (int b = tid / l.E; b < l.nblk; b += per)
+                v += (double)__ldcg(l.blk_p + (size_t)b * l.E + e);
+        }
+        s_part[tid] = v;
+    }
+    __syncthreads();
+    for (int e = tid; e < l.E; e += blockDim.x) {
+        double pe = 0.0;
+        for (int j = 0; j < per; ++j) pe += s_part[j * l.E + e];
+        s_d[e] = (double)__ldcg(l.top1 + e) * pe;
+        if (l.expert_counts != nullptr) l.expert_counts[e] = __ldcg(l.counts + e);
+    }
+    __syncthreads();
+    if (tid == 0 && l.aux_out != nullptr) {
+        double s = 0.0;
+        for (int e = 0; e < l.E; ++e) s += s_d[e];
+        const double Td = (double)l.T;
+        l.aux_out[0] = (float)((double)l.E * s / (Td * Td));
+    }
+}
+
 // Record the first device error in the workspace header (later ones are dropped).
 __device__ __forceinline__ void record_error(DeviceHeader* h, int32_t code, int32_t info) {
     if (atomicCAS(&h->err_code, 0, code) == 0) h->err_info = info;

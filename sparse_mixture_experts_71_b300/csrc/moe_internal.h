@@ -18,8 +18,7 @@ constexpr int kCountBlock = 256;
 struct DeviceHeader {
     int32_t err_code;   // first error recorded (0 = none)
     int32_t err_info;
-    uint32_t route_done;  // blocks of the route kernel that finished (reset per call)
-    int32_t pad[61];
+    int32_t pad[62];
 };
 static_assert(sizeof(DeviceHeader) == 256, "header is one 256-byte line");
 
@@ -96,6 +95,8 @@ template <typename T> __host__ __device__ inline T* at(void* base, size_t off) {
 // expert histogram (blk_hist) and each assignment's rank among the block's
 // earlier assignments to the same expert (local_rank), which the scan and
 // permute kernels consume with granularity route.tokens * k.
+// Without fuse_count the router also runs its one-block finishing kernel
+// (loss, per-expert counts); with it the caller leaves that to the scan.
 cudaError_t launch_route(const moe_config& c, const void* x, const float* W_r,
                          const float* logit_bias, const float* logits_in, float* logits_out,
                          int32_t* topk_idx, float* topk_w, int32_t* expert_counts,
@@ -108,11 +109,17 @@ cudaError_t launch_count(const moe_config& c, const int32_t* topk_idx, void* ws,
 
 // Scan of the block histograms and the permute/gather, given histograms of
 // `hist_blocks` blocks of `asg_per_block` assignments.
+// With loss.blk_p set, the scan kernel also computes the router's loss and
+// per-expert counts (the forward pass); otherwise loss is ignored.
+struct LossArgs;
 cudaError_t launch_scan_permute(const moe_config& c, const void* x, const int32_t* topk_idx,
                                 const float* topk_w, int asg_per_block, int hist_blocks,
                                 int32_t* offsets, int32_t* slot_of, int32_t* perm_token,
                                 float* perm_w, void* x_perm, void* ws, const WsLayout& L,
-                                cudaStream_t s);
+                                const LossArgs& loss, cudaStream_t s);
+// Loss inputs/outputs of the router's per-block statistics in workspace ws.
+LossArgs route_loss_args(const moe_config& c, void* ws, const WsLayout& L,
+                         int32_t* expert_counts, float* aux_out);
 
 cudaError_t launch_expert_ffn(const moe_config& c, const void* x_perm, int64_t x_rows,
                               const int32_t* offsets, const void* W1, const void* b1,

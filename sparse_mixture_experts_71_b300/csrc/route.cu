@@ -51,9 +51,6 @@ __global__ void __launch_bounds__(kThreads) route_warp_kernel(RouteArgs a) {
     __shared__ int s_idx[TB * kMaxTopK];
     __shared__ int s_cnt[EMAX], s_top1[EMAX], carry[EMAX];
     __shared__ int wh[kWarps][EMAX];
-    __shared__ double s_d[EMAX];
-    __shared__ double s_part[kThreads];
-    __shared__ int s_last;
 
     const int tid = threadIdx.x, warp = tid / 32, lane = tid % 32;
     const int grp = warp / DS, split = warp % DS;
@@ -149,7 +146,7 @@ __global__ void __launch_bounds__(kThreads) route_warp_kernel(RouteArgs a) {
     __syncthreads();
     if (tid < TB) token_epilogue<EMAX>(a, s_p + tid * LDS, blockIdx.x * TB + tid, tid, s_idx, s_cnt, s_top1);
     __syncthreads();
-    finish_block<EMAX>(a, s_p, LDS, TB, s_idx, s_cnt, s_top1, wh, carry, s_d, s_part, &s_last);
+    finish_block<EMAX>(a, s_p, LDS, TB, s_idx, s_cnt, s_top1, wh, carry);
 }
 
 // ===================================================================== tensor-core kernel
@@ -206,9 +203,6 @@ __global__ void __launch_bounds__(kThreads) route_mma_kernel(RouteArgs a,
     __shared__ int s_idx[TB * kMaxTopK];
     __shared__ int s_cnt[EMAX], s_top1[EMAX], carry[EMAX];
     __shared__ int wh[kWarps][EMAX];
-    __shared__ double s_d[EMAX];
-    __shared__ double s_part[kThreads];
-    __shared__ int s_last;
 
     const int tid = threadIdx.x, warp = tid / 32, lane = tid % 32;
     const int mtile = warp / DS, split = warp % DS;
@@ -294,7 +288,7 @@ __global__ void __launch_bounds__(kThreads) route_mma_kernel(RouteArgs a,
     __syncthreads();
     if (tid < TB) token_epilogue<EMAX>(a, s_buf + tid * LDS, blockIdx.x * TB + tid, tid, s_idx, s_cnt, s_top1);
     __syncthreads();
-    finish_block<EMAX>(a, s_buf, LDS, TB, s_idx, s_cnt, s_top1, wh, carry, s_d, s_part, &s_last);
+    finish_block<EMAX>(a, s_buf, LDS, TB, s_idx, s_cnt, s_top1, wh, carry);
 }
 
 // ===================================================================== tile kernel
@@ -365,9 +359,6 @@ __global__ void __launch_bounds__(kThreads) route_tile_kernel(RouteArgs a) {
     __shared__ int s_idx[Gm::TB * kMaxTopK];
     __shared__ int s_cnt[EMAX], s_top1[EMAX], carry[EMAX];
     __shared__ int wh[kWarps][EMAX];
-    __shared__ double s_d[EMAX];
-    __shared__ double s_part[kThreads];
-    __shared__ int s_last;
 
     const int tid = threadIdx.x;
     const int t0 = blockIdx.x * Gm::TB;
@@ -528,8 +519,7 @@ __global__ void __launch_bounds__(kThreads) route_tile_kernel(RouteArgs a) {
         }
     }
     __syncthreads();
-    finish_block<EMAX>(a, lg, Gm::LGS, Gm::TB, s_idx, s_cnt, s_top1, wh, carry, s_d, s_part,
-                       &s_last);
+    finish_block<EMAX>(a, lg, Gm::LGS, Gm::TB, s_idx, s_cnt, s_top1, wh, carry);
 }
 
 template <typename TX, int EMAX>
@@ -609,16 +599,36 @@ cudaError_t launch_e(const RouteArgs& a, const RouteGeom& g, cudaStream_t s) {
     return launch_tile<TX, 256>(a, s);
 }
 
+__global__ void __launch_bounds__(256) route_finish_kernel(LossArgs l) {
+    __shared__ double s_part[256];
+    __shared__ double s_d[kMaxExperts];
+    loss_and_counts(l, s_part, s_d);
+}
+
 }  // namespace
+
+LossArgs route_loss_args(const moe_config& c, void* ws, const WsLayout& L,
+                         int32_t* expert_counts, float* aux_out) {
+    LossArgs l;
+    l.blk_p = at<float>(ws, L.blk_p);
+    l.top1 = at<int32_t>(ws, L.top1);
+    l.counts = at<int32_t>(ws, L.counts);
+    l.expert_counts = expert_counts;
+    l.aux_out = aux_out;
+    l.nblk = L.route.blocks;
+    l.E = c.E;
+    l.T = c.T;
+    return l;
+}
 
 RouteGeom route_geom(const moe_config& c) {
     RouteGeom g{};
     constexpr int kTargetBlocks = 296;  // two blocks per SM at least, where T allows
-    if (c.dtype == MOE_BF16 && c.E > 16 && c.E <= 64) {
+    if (c.dtype == MOE_BF16 && c.E > 16 && c.E <= 64 && c.T >= 1024) {
         g.tc = true;
         g.epad = c.E <= 32 ? 32 : 64;
         g.tokens = 128;
-    } else if (c.dtype == MOE_BF16 && c.E <= 16) {
+    } else if (c.dtype == MOE_BF16 && c.E <= 16 && c.T >= 1024) {
         g.mma = true;
         g.epad = c.E <= 8 ? 8 : 16;
         int mt = 8;
@@ -660,21 +670,23 @@ cudaError_t launch_route(const moe_config& c, const void* x, const float* W_r,
     a.local_rank = at<int32_t>(ws, L.local_rank);
     a.T = c.T; a.d = c.d; a.E = c.E; a.k = c.k; a.renormalize = c.renormalize;
     a.nblk = L.route.blocks;
-    // per-call counters: route_done and the two count arrays start at zero
-    cudaError_t err = cudaMemsetAsync(at<char>(ws, L.header + offsetof(DeviceHeader, route_done)),
-                                      0, sizeof(uint32_t), s);
+    // per-call counters: the two count arrays start at zero
+    cudaError_t err = cudaMemsetAsync(at<char>(ws, L.counts), 0, L.blk_p - L.counts, s);
     if (err != cudaSuccess) return err;
-    err = cudaMemsetAsync(at<char>(ws, L.counts), 0, L.blk_p - L.counts, s);
-    if (err != cudaSuccess) return err;
-    if (L.route.mma) return launch_mma(a, L.route, at<__nv_bfloat16>(ws, L.wsplit), s);
-    if (L.route.tc) {
+    if (L.route.mma) {
+        err = launch_mma(a, L.route, at<__nv_bfloat16>(ws, L.wsplit), s);
+    } else if (L.route.tc) {
         __nv_bfloat16* wsp = at<__nv_bfloat16>(ws, L.wsplit);
         err = launch_split(a, L.route.epad, wsp, s);
-        if (err != cudaSuccess) return err;
-        return launch_route_tc(a, wsp, L.route.epad, s);
+        if (err == cudaSuccess) err = launch_route_tc(a, wsp, L.route.epad, s);
+    } else {
+        err = c.dtype == MOE_BF16 ? launch_e<__nv_bfloat16>(a, L.route, s)
+                                  : launch_e<float>(a, L.route, s);
     }
-    return c.dtype == MOE_BF16 ? launch_e<__nv_bfloat16>(a, L.route, s)
-                               : launch_e<float>(a, L.route, s);
+    if (err != cudaSuccess || fuse_count) return err;
+    route_finish_kernel<<<1, 256, 0, s>>>(route_loss_args(c, ws, L, expert_counts, aux_out));
+    count_launches(1);
+    return cudaGetLastError();
 }
 
 }  // namespace moe

@@ -67,13 +67,12 @@ __device__ void block_rank(const int* s_idx, int n, int E, int (*wh)[EMAX], int*
     for (int e = tid; e < E; e += kThreads) hist_row[e] = carry[e];
 }
 
-// Per-block sums of p (rows of s_p, fixed order), counts, the fused dispatch
-// histogram, and in the last block the loss and the per-expert counts.
+// Per-block sums of p (rows of s_p, fixed order), counts, and the fused
+// dispatch histogram.
 template <int EMAX>
 __device__ void finish_block(const RouteArgs& a, const float* s_p, int lds, int TB,
                              const int* s_idx, const int* s_cnt, const int* s_top1,
-                             int (*wh)[EMAX], int* carry, double* s_d, double* s_part,
-                             int* s_last) {
+                             int (*wh)[EMAX], int* carry) {
     const int tid = threadIdx.x;
     const int t0 = blockIdx.x * TB;
     for (int e = tid; e < a.E; e += kThreads) {
@@ -87,39 +86,6 @@ __device__ void finish_block(const RouteArgs& a, const float* s_p, int lds, int 
         const int n = min(TB, a.T - t0) * a.k;
         block_rank<EMAX>(s_idx, n, a.E, wh, carry, a.blk_hist + (size_t)blockIdx.x * a.E,
                          a.local_rank + (size_t)t0 * a.k);
-    }
-    __threadfence();
-    __syncthreads();
-    if (tid == 0) *s_last = (atomicAdd(&a.hdr->route_done, 1u) == (unsigned)(a.nblk - 1));
-    __syncthreads();
-    if (!*s_last) return;
-    __threadfence();
-    // the per-block sums, in block order: thread i < stride (a multiple of E)
-    // owns expert i % E and blocks i / E, i / E + per, ...; the partials of an
-    // expert are then added in thread order
-    const int per = kThreads / a.E;
-    const int stride = per * a.E;
-    double v = 0.0;
-    if (tid < stride) {
-        const int e = tid % a.E;
-#pragma unroll 8
-        for (int b = tid / a.E; b < a.nblk; b += per)
-            v += (double)__ldcg(a.blk_p + (size_t)b * a.E + e);
-    }
-    s_part[tid] = v;
-    __syncthreads();
-    for (int e = tid; e < a.E; e += kThreads) {
-        double pe = 0.0;
-        for (int j = 0; j < per; ++j) pe += s_part[j * a.E + e];
-        s_d[e] = (double)__ldcg(a.top1 + e) * pe;
-        if (a.expert_counts != nullptr) a.expert_counts[e] = __ldcg(a.counts + e);
-    }
-    __syncthreads();
-    if (tid == 0 && a.aux_out != nullptr) {
-        double s = 0.0;
-        for (int e = 0; e < a.E; ++e) s += s_d[e];
-        const double Td = (double)a.T;
-        a.aux_out[0] = (float)((double)a.E * s / (Td * Td));
     }
 }
 

@@ -88,9 +88,6 @@ route_tc_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constant__
     __shared__ int s_idx[TM * kMaxTopK];
     __shared__ int s_cnt[NP], s_top1[NP], carry[NP];
     __shared__ int wh[kWarps][NP];
-    __shared__ double s_d[NP];
-    __shared__ double s_part[kThreads];
-    __shared__ int s_last;
 
     const int tid = threadIdx.x, warp = tid / 32, lane = tid % 32;
     const int t0 = blockIdx.x * TM;
@@ -205,7 +202,7 @@ route_tc_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constant__
     }
     if (tid < TM) token_epilogue<NP>(a, s_p + tid * C::LDS, t0 + tid, tid, s_idx, s_cnt, s_top1);
     __syncthreads();
-    finish_block<NP>(a, s_p, C::LDS, TM, s_idx, s_cnt, s_top1, wh, carry, s_d, s_part, &s_last);
+    finish_block<NP>(a, s_p, C::LDS, TM, s_idx, s_cnt, s_top1, wh, carry);
 }
 
 PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
