@@ -170,6 +170,32 @@ moe_status moe_forward(const moe_config* cfg, const void* x, const float* W_r,
 moe_status moe_get_device_error(void* ws, void* stream, int32_t* code, int32_t* info);
 
 /*
+ * moe_dispatch without a workspace, for callers that cannot provide one: a
+ * host whose GPU memory is handed out once, up front, by another component
+ * (a serving engine's fixed pool, a plugin host that owns every allocation)
+ * has no allocator to call for scratch space.  The pages have no counterpart
+ * of this call; it is a deployment convenience of this library.
+ *   Arguments and results are those of moe_dispatch, minus ws / ws_bytes.
+ *   Scratch lives in a fixed array inside the library (768.25 KB, held on
+ *   every GPU that loads the library until the process exits), so the call
+ *   allocates nothing: no cudaMalloc, no cudaFree, no allocating library call.
+ *   Limits: T * k <= 65536 and E <= 256; larger problems return
+ *   MOE_ERR_UNSUPPORTED without enqueueing anything.
+ *   The first call on a device, made while that device is current, looks up
+ *   the array's device address (cudaGetSymbolAddress); make that first call
+ *   before any stream capture.
+ *   All calls on a device share the one array: calls whose work overlaps on
+ *   the GPU (different streams without ordering) race and give wrong results.
+ *   Each call clears the part that must start at zero.  An expert index
+ *   outside [0, E) is skipped (slot -1) as in moe_dispatch, but the record of
+ *   it cannot be read back (there is no workspace to pass to
+ *   moe_get_device_error).
+ */
+moe_status moe_dispatch_noalloc(const moe_config* cfg, const void* x, const int32_t* topk_idx,
+                                const float* topk_w, int32_t* offsets, int32_t* slot_of,
+                                int32_t* perm_token, float* perm_w, void* x_perm, void* stream);
+
+/*
  * Diagnostics: number of CUDA kernels libmoe has enqueued in this process
  * since it was loaded (memsets excluded).  No counterpart on the pages.
  */

@@ -23,7 +23,7 @@ STATUS = {0: "ok", 1: "invalid argument", 2: "misaligned pointer or row length",
 
 EXPORTED = ("moe_workspace_size", "moe_status_string", "moe_route", "moe_dispatch",
             "moe_expert_ffn", "moe_combine", "moe_forward", "moe_get_device_error",
-            "moe_launch_count")
+            "moe_launch_count", "moe_dispatch_noalloc")
 
 
 class MoeConfig(ctypes.Structure):
@@ -63,8 +63,10 @@ def load() -> ctypes.CDLL:
         lib.moe_forward.argtypes = [cfgp] + [_P] * 11 + [_P, sz, _P]
         lib.moe_get_device_error.argtypes = [_P, _P, ctypes.POINTER(ctypes.c_int32),
                                              ctypes.POINTER(ctypes.c_int32)]
-        for name in EXPORTED[2:-1]:
+        for name in EXPORTED[2:8]:
             getattr(lib, name).restype = ctypes.c_int
+        lib.moe_dispatch_noalloc.restype = ctypes.c_int
+        lib.moe_dispatch_noalloc.argtypes = [cfgp] + [_P] * 8 + [_P]
         lib.moe_launch_count.restype = ctypes.c_uint64
         lib.moe_launch_count.argtypes = []
         _lib = lib
@@ -126,6 +128,15 @@ def expert_ffn(cfg, x_perm, offsets, W1, b1, W2, b2, y_perm, ws, perm_w=None, st
     _check("moe_expert_ffn", load().moe_expert_ffn(
         ctypes.byref(cfg), _ptr(x_perm), _ptr(offsets), _ptr(W1), _ptr(b1), _ptr(W2), _ptr(b2),
         _ptr(perm_w), _ptr(y_perm), _ptr(ws), ws.numel(), _stream(stream)))
+
+
+def dispatch_noalloc(cfg, x, topk_idx, offsets, slot_of, perm_token, x_perm, topk_w=None,
+                     perm_w=None, stream=None):
+    """moe_dispatch_noalloc: dispatch with the library's own fixed scratch array
+    (no workspace argument; T * k <= 65536, E <= 256)."""
+    _check("moe_dispatch_noalloc", load().moe_dispatch_noalloc(
+        ctypes.byref(cfg), _ptr(x), _ptr(topk_idx), _ptr(topk_w), _ptr(offsets), _ptr(slot_of),
+        _ptr(perm_token), _ptr(perm_w), _ptr(x_perm), _stream(stream)))
 
 
 def combine(cfg, y_perm, slot_of, y, stream=None):
