@@ -9,7 +9,10 @@ combine) over one batch of seeded synthetic inputs of the named workload
 (default: bf16, T=4096 tokens, d=1024, d_ff=4096, E=8, top-2).  The inputs
 and the expert weights are resident in HBM when the timed region starts; L2
 is flushed (a 256 MiB write) before every timed step and the flush is not
-timed.  Rank 0 prints one JSON line.
+timed.  Each step replays a CUDA graph of one moe_forward call; a second
+timed loop replays graphs of the stage calls (route + dispatch, expert FFN,
+combine) for the per-stage times and the expert FFN's roofline.  Rank 0
+prints one JSON line.
 
 Under torchrun (N > 1) every rank runs an independent replica of the layer
 on its own GPU (the layer has no cross-GPU step); the line reports the tokens
@@ -39,6 +42,14 @@ from sparse_mixture_experts_71_b300 import inputs as I  # noqa: E402
 DEFAULT_WORKLOAD = I.MEDIUM.name
 PEAKS_FALLBACK = {"hbm_gbs": 6400.0, "bf16_tflops": 1800.0, "bf16_tflops_sustained": 1400.0}
 METRIC = "MoE-layer fwd tokens/s and achieved TFLOP/s (or HBM GB/s) vs B300 roofline"
+
+# DRAM bytes (read + write) of one expert-FFN launch pair (GEMM1 + GEMM2) from
+# an ncu capture of the current kernels; summaries with the commands are in
+# profiles/grouped_gemm_*.md.  Workloads without a capture report null.
+TRAFFIC_BYTES = {
+    "bf16-T4096-d1024-F4096-E8-top2": (84.051 + 32.474 + 139.404 + 13.855) * 1e6,
+    "decode-bf16-T64-d4096-F14336-E8-top2": (941.743 + 6.241 + 944.322 + 4.556) * 1e6,
+}
 
 
 def peaks():
@@ -405,7 +416,7 @@ def bench_ours(args, wl):
         roof = {"bound": "hbm", "unit": "GB/s"}
     roof.update({"kernel": "expert FFN (grouped GEMM1 + GEMM2)", "achieved": achieved,
                  "peak": peak, "peak_source": pk_kind, "frac": achieved / peak,
-                 "traffic": args.traffic})
+                 "traffic": TRAFFIC_BYTES.get(wl.name)})
 
     line = {"metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world,
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_per_step,
@@ -447,8 +458,6 @@ def main():
     ap.add_argument("--impl", choices=("ours", "reference"), default="ours")
     ap.add_argument("--workload", default=DEFAULT_WORKLOAD, choices=list(I.WORKLOADS))
     ap.add_argument("--no-cpu-baseline", action="store_true")
-    ap.add_argument("--traffic", type=float, default=None,
-                    help="DRAM bytes per expert-FFN launch pair from an ncu capture")
     args = ap.parse_args()
     wl = I.WORKLOADS[args.workload]
     if args.impl == "reference":
