@@ -139,19 +139,19 @@ __device__ __forceinline__ void drain_bar(uint64_t* bar, uint32_t parity) {
 // L2.  A stage may be refilled only when all CS CTAs have consumed it, so
 // every MMA commit arrives on the stage's empty barrier of all CS CTAs.
 // Epilogue of one accumulator tile: this warp reads TMEM lanes 32q..32q+31
-// (weight rows fbase + 32q + lane) and the token columns of its half of the
-// COLS-wide tile (columns acc_col + c, c < n), applies bias + GELU (first
+// (weight rows fbase + 32q + lane) and the token columns of its part (of
+// nparts) of the COLS-wide tile (columns acc_col + c, c < n), applies bias + GELU (first
 // GEMM, bf16 out) or bias x routing weight (second GEMM, fp32 out), and
 // writes token rows r0 + c through a shared-memory transpose (stg: 32 x 32).
 template <int COLS, bool GEMM1>
 __device__ __forceinline__ void epilogue_tile(const Params& p, int e, int r0, int n, int fbase,
-                                              uint32_t tmem_base, int acc_col, int q, int half,
-                                              int lane, uint8_t* stg) {
+                                              uint32_t tmem_base, int acc_col, int q, int part,
+                                              int nparts, int lane, uint8_t* stg) {
     const int f0 = fbase + q * 32;  // first weight row (output feature) of this warp
     const int f = f0 + lane;
     const float bias =
         f < p.n_out ? __bfloat162float(p.bias[(size_t)e * p.n_out + f]) : 0.f;
-    const int c_begin = half * (COLS / 2), c_end = min(c_begin + COLS / 2, n);
+    const int c_begin = part * (COLS / nparts), c_end = min(c_begin + COLS / nparts, n);
     for (int c = c_begin; c < c_end; c += 32) {
         float v[32];
         tc::tmem_ld_32cols(tmem_base + ((uint32_t)(q * 32) << 16) +
@@ -356,7 +356,7 @@ grouped_gemm_tc(const __grid_constant__ CUtensorMap tmA, const __grid_constant__
             if (!__all_sync(0xffffffffu, ok)) break;
             tc::fence_after_sync();
             epilogue_tile<BN_MAX, GEMM1>(p, tl.e, tl.r0, tl.n, tl.m0, tmem_base, acc * BN_MAX, q,
-                                         half, lane, stg);
+                                         half, 2, lane, stg);
             tc::fence_before_sync();
             __syncwarp();
             if (lane == 0) tc::mbar_arrive(&tempty[acc]);
@@ -390,12 +390,13 @@ grouped_gemm_tc(const __grid_constant__ CUtensorMap tmA, const __grid_constant__
 // on CTA 0's TMEM-empty barrier.
 constexpr int BN2 = 256;  // tokens per pair tile (MMA N, max)
 
-template <int STAGES, bool GEMM1>
+template <int STAGES, bool GEMM1, int EW>
 struct Cfg2 {
+    static constexpr int THREADS = (4 + EW) * 32;       // 4 role warps + EW epilogue warps
     static constexpr int B_BYTES = (BN2 / 2) * BK * 2;  // 16 KB: this CTA's half of B
     static constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
     static constexpr int OUT_ES = GEMM1 ? 2 : 4;
-    static constexpr int STAGING = kEpiWarps * 32 * 32 * OUT_ES;
+    static constexpr int STAGING = EW * 32 * 32 * OUT_ES;
     static constexpr int TMEM_COLS = 2 * BN2;
     static constexpr int OFF_STAGING = STAGES * STAGE_BYTES;
     static constexpr int OFF_BARS = OFF_STAGING + STAGING;
@@ -407,11 +408,11 @@ struct Cfg2 {
     static_assert(SMEM <= 232448, "shared memory budget");
 };
 
-template <int STAGES, bool GEMM1>
-__global__ void __launch_bounds__(kThreads, 1)
+template <int STAGES, bool GEMM1, int EW>
+__global__ void __launch_bounds__(Cfg2<STAGES, GEMM1, EW>::THREADS, 1)
 grouped_gemm_pair(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                   const Params p) {
-    using C = Cfg2<STAGES, GEMM1>;
+    using C = Cfg2<STAGES, GEMM1, EW>;
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -438,7 +439,7 @@ grouped_gemm_pair(const __grid_constant__ CUtensorMap tmA, const __grid_constant
         }
         for (int a = 0; a < 2; ++a) {
             tc::mbar_init(&tfull[a], 1);
-            tc::mbar_init(&tempty[a], 2 * kEpiWarps);
+            tc::mbar_init(&tempty[a], 2 * EW);
         }
         tc::mbar_init(drain, 1);
         *s_abort = 0;
@@ -546,7 +547,7 @@ grouped_gemm_pair(const __grid_constant__ CUtensorMap tmA, const __grid_constant
         // ------------------------------------------------ epilogue (both CTAs)
         const int ew = warp - 4;
         const int q = warp & 3;
-        const int half = ew >> 2;
+        const int part = ew >> 2;  // which of the EW/4 column parts of the tile
         uint8_t* stg = smem + C::OFF_STAGING + ew * 32 * 32 * C::OUT_ES;
         int acc = 0;
         uint32_t acc_phase = 0;
@@ -557,7 +558,7 @@ grouped_gemm_pair(const __grid_constant__ CUtensorMap tmA, const __grid_constant
             if (!__all_sync(0xffffffffu, ok)) break;
             tc::fence_after_sync();
             epilogue_tile<BN2, GEMM1>(p, tl.e, tl.r0, tl.n, m0 + rank * BM, tmem_base, acc * BN2,
-                                      q, half, lane, stg);
+                                      q, part, EW / 4, lane, stg);
             tc::fence_before_sync();
             __syncwarp();
             if (lane == 0) tc::mbar_arrive_cluster(tc::cluster_addr(&tempty[acc], 0));
@@ -605,7 +606,7 @@ bool make_map(CUtensorMap* m, const void* base, uint64_t inner, uint64_t outer,
 
 // Clusters of CS CTAs that can be resident at once (one CTA per SM).
 template <auto Kern>
-int resident_clusters(int cs, int smem) {
+int resident_clusters(int cs, int smem, int threads = kThreads) {
     static int cache[64] = {0};
     int dev = 0;
     cudaGetDevice(&dev);
@@ -614,7 +615,7 @@ int resident_clusters(int cs, int smem) {
     if (cs > 1) {
         cudaLaunchConfig_t cfg = {};
         cfg.gridDim = dim3(cs * n, 1, 1);
-        cfg.blockDim = dim3(kThreads, 1, 1);
+        cfg.blockDim = dim3(threads, 1, 1);
         cfg.dynamicSmemBytes = smem;
         cudaLaunchAttribute attr;
         attr.id = cudaLaunchAttributeClusterDimension;
@@ -660,16 +661,16 @@ cudaError_t launch_one(const CUtensorMap& a, const CUtensorMap& b, const Params&
     return cudaGetLastError();
 }
 
-template <int STAGES, bool GEMM1>
+template <int STAGES, bool GEMM1, int EW>
 cudaError_t launch_one_pair(const CUtensorMap& a, const CUtensorMap& b, const Params& p,
                             cudaStream_t s) {
-    using C = Cfg2<STAGES, GEMM1>;
-    constexpr auto kern = grouped_gemm_pair<STAGES, GEMM1>;
+    using C = Cfg2<STAGES, GEMM1, EW>;
+    constexpr auto kern = grouped_gemm_pair<STAGES, GEMM1, EW>;
     cudaError_t err = ensure_smem<kern>(C::SMEM);
     if (err != cudaSuccess) return err;
     cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3(2 * resident_clusters<kern>(2, C::SMEM), 1, 1);
-    cfg.blockDim = dim3(kThreads, 1, 1);
+    cfg.gridDim = dim3(2 * resident_clusters<kern>(2, C::SMEM, C::THREADS), 1, 1);
+    cfg.blockDim = dim3(C::THREADS, 1, 1);
     cfg.dynamicSmemBytes = C::SMEM;
     cfg.stream = s;
     cudaLaunchAttribute attr;
@@ -723,9 +724,9 @@ cudaError_t launch_expert_ffn_tc(const moe_config& c, const void* x_perm, int64_
         if (!make_map(&pm[1], x_perm, c.d, (uint64_t)x_rows, BN2 / 2) ||
             !make_map(&pm[3], h, c.d_ff, (uint64_t)h_rows, BN2 / 2))
             return cudaErrorInvalidValue;
-        cudaError_t err = launch_one_pair<6, true>(pm[0], pm[1], p1, s);
+        cudaError_t err = launch_one_pair<6, true, 16>(pm[0], pm[1], p1, s);
         if (err != cudaSuccess) return err;
-        return launch_one_pair<6, false>(pm[2], pm[3], p2, s);
+        return launch_one_pair<6, false, 8>(pm[2], pm[3], p2, s);
     }
     return launch_pair<64, 8, 1>(maps, p1, p2, s);
 }
