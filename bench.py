@@ -47,7 +47,6 @@ METRIC = "MoE-layer fwd tokens/s and achieved TFLOP/s (or HBM GB/s) vs B300 roof
 # an ncu capture of the current kernels; summaries with the commands are in
 # profiles/grouped_gemm_*.md.  Workloads without a capture report null.
 TRAFFIC_BYTES = {
-    "bf16-T4096-d1024-F4096-E8-top2": (84.051 + 32.474 + 139.404 + 13.855) * 1e6,
     "decode-bf16-T64-d4096-F14336-E8-top2": (941.743 + 6.241 + 944.322 + 4.556) * 1e6,
 }
 

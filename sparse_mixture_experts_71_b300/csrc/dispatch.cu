@@ -76,10 +76,10 @@ __global__ void __launch_bounds__(1024) scan_kernel(const int32_t* __restrict__ 
                                                     int32_t* __restrict__ offsets, LossArgs loss) {
     __shared__ int part_sum[1024];
     __shared__ int s_total[kMaxExperts];
-    __shared__ double s_part[256];
-    __shared__ double s_d[kMaxExperts];
+    __shared__ float s_part[256];
+    __shared__ float s_d[kMaxExperts];
     if (loss.blk_p != nullptr) loss_and_counts(loss, s_part, s_d);
-    const int tid = threadIdx.x;
+    const int tid = threadIdx.x, warp = tid / 32, lane = tid % 32;
     const int P = 1024 / E;
     const int part = tid / E, e = tid % E;
     const bool active = part < P;
@@ -90,14 +90,22 @@ __global__ void __launch_bounds__(1024) scan_kernel(const int32_t* __restrict__ 
         for (int b = b0; b < b1; ++b) s += blk_hist[(size_t)b * E + e];
     part_sum[tid] = s;
     __syncthreads();
-    if (tid < E) {  // exclusive scan over parts, per expert
-        int run = 0;
-        for (int p = 0; p < P; ++p) {
-            const int v = part_sum[p * E + tid];
-            part_sum[p * E + tid] = run;
-            run += v;
+    // exclusive scan over the P parts of each expert: one warp per expert
+    for (int x = warp; x < E; x += 32) {
+        int carry_in = 0;
+        for (int p0 = 0; p0 < P; p0 += 32) {
+            const int p = p0 + lane;
+            const int v = p < P ? part_sum[p * E + x] : 0;
+            int incl = v;
+#pragma unroll
+            for (int o = 1; o < 32; o <<= 1) {
+                const int u = __shfl_up_sync(0xffffffffu, incl, o);
+                if (lane >= o) incl += u;
+            }
+            if (p < P) part_sum[p * E + x] = carry_in + incl - v;
+            carry_in += __shfl_sync(0xffffffffu, incl, 31);
         }
-        s_total[tid] = run;
+        if (lane == 0) s_total[x] = carry_in;
     }
     __syncthreads();
     if (active) {
@@ -107,14 +115,22 @@ __global__ void __launch_bounds__(1024) scan_kernel(const int32_t* __restrict__ 
             run += blk_hist[(size_t)b * E + e];
         }
     }
-    if (tid == 0) {
-        int off = 0;
-        for (int x = 0; x < E; ++x) {
-            offsets[x] = off;
-            const int tot = s_total[x];
-            off += capacity < 0 ? tot : min(tot, capacity);
+    if (warp == 0) {  // offsets: exclusive scan of the kept counts
+        int carry_in = 0;
+        for (int x0 = 0; x0 < E; x0 += 32) {
+            const int x = x0 + lane;
+            const int tot = x < E ? s_total[x] : 0;
+            const int kept = capacity < 0 ? tot : min(tot, capacity);
+            int incl = kept;
+#pragma unroll
+            for (int o = 1; o < 32; o <<= 1) {
+                const int u = __shfl_up_sync(0xffffffffu, incl, o);
+                if (lane >= o) incl += u;
+            }
+            if (x < E) offsets[x] = carry_in + incl - kept;
+            carry_in += __shfl_sync(0xffffffffu, incl, 31);
         }
-        offsets[E] = off;
+        if (lane == 0) offsets[E] = carry_in;
     }
 }
 

@@ -390,11 +390,12 @@ grouped_gemm_tc(const __grid_constant__ CUtensorMap tmA, const __grid_constant__
 // on CTA 0's TMEM-empty barrier.
 constexpr int BN2 = 256;  // tokens per pair tile (MMA N, max)
 
-template <int STAGES, bool GEMM1, int EW>
+template <int STAGES, bool GEMM1, int EW, int ATOMS>
 struct Cfg2 {
     static constexpr int THREADS = (4 + EW) * 32;       // 4 role warps + EW epilogue warps
-    static constexpr int B_BYTES = (BN2 / 2) * BK * 2;  // 16 KB: this CTA's half of B
-    static constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
+    static constexpr int B_BYTES = (BN2 / 2) * BK * 2;  // 16 KB: this CTA's half of B per atom
+    static constexpr int ATOM_BYTES = A_BYTES + B_BYTES;
+    static constexpr int STAGE_BYTES = ATOMS * ATOM_BYTES;  // ATOMS x 64 columns of K
     static constexpr int OUT_ES = GEMM1 ? 2 : 4;
     static constexpr int STAGING = EW * 32 * 32 * OUT_ES;
     static constexpr int TMEM_COLS = 2 * BN2;
@@ -408,11 +409,11 @@ struct Cfg2 {
     static_assert(SMEM <= 232448, "shared memory budget");
 };
 
-template <int STAGES, bool GEMM1, int EW>
-__global__ void __launch_bounds__(Cfg2<STAGES, GEMM1, EW>::THREADS, 1)
+template <int STAGES, bool GEMM1, int EW, int ATOMS>
+__global__ void __launch_bounds__(Cfg2<STAGES, GEMM1, EW, ATOMS>::THREADS, 1)
 grouped_gemm_pair(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                   const Params p) {
-    using C = Cfg2<STAGES, GEMM1, EW>;
+    using C = Cfg2<STAGES, GEMM1, EW, ATOMS>;
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -430,7 +431,7 @@ grouped_gemm_pair(const __grid_constant__ CUtensorMap tmA, const __grid_constant
     const bool leader = rank == 0;
     const int pair = blockIdx.x / 2, npairs = gridDim.x / 2;
     const int mt2 = (p.n_out + 2 * BM - 1) / (2 * BM);  // 256-row weight tiles
-    const int KB = (p.K + BK - 1) / BK;
+    const int KB = (p.K + ATOMS * BK - 1) / (ATOMS * BK);  // stages per tile
 
     if (warp == 0 && lane == 0) {
         for (int s = 0; s < STAGES; ++s) {
@@ -485,7 +486,7 @@ grouped_gemm_pair(const __grid_constant__ CUtensorMap tmA, const __grid_constant
             uint32_t phase = 0;
             long long fills = 0;
             bool ok = true;
-            const uint32_t bytes = 2 * (A_BYTES + C::B_BYTES);  // whole boxes of both CTAs
+            const uint32_t bytes = 2 * C::STAGE_BYTES;  // whole boxes of both CTAs
             for (int t = pair; t < total && ok; t += npairs) {
                 const Tile tl = decode_tile(t, s_tiles, p, BN2, 1, 0);  // m0 in 256-row units / 2
                 const int m0 = (tl.m0 / BM) * 2 * BM;                  // pair tile base row
@@ -496,9 +497,13 @@ grouped_gemm_pair(const __grid_constant__ CUtensorMap tmA, const __grid_constant
                     if (!wait_bar(&empty[stage], phase ^ 1, s_abort, p, 1)) { ok = false; break; }
                     if (leader) tc::mbar_expect_tx(&full[stage], bytes);
                     const uint32_t full_l = tc::cluster_addr(&full[stage], 0);
-                    uint8_t* sa = smem + stage * C::STAGE_BYTES;
-                    tc::tma_load_2d_pair(sa, &tmA, full_l, kb * BK, arow);
-                    tc::tma_load_2d_pair(sa + A_BYTES, &tmB, full_l, kb * BK, brow);
+#pragma unroll
+                    for (int at = 0; at < ATOMS; ++at) {
+                        uint8_t* sa = smem + stage * C::STAGE_BYTES + at * C::ATOM_BYTES;
+                        const int kc = (kb * ATOMS + at) * BK;
+                        tc::tma_load_2d_pair(sa, &tmA, full_l, kc, arow);
+                        tc::tma_load_2d_pair(sa + A_BYTES, &tmB, full_l, kc, brow);
+                    }
                     ++fills;
                     if (++stage == STAGES) { stage = 0; phase ^= 1; }
                 }
@@ -524,13 +529,17 @@ grouped_gemm_pair(const __grid_constant__ CUtensorMap tmA, const __grid_constant
                 for (int kb = 0; kb < KB; ++kb) {
                     if (!wait_bar(&full[stage], phase, s_abort, p, 3)) { ok = false; break; }
                     tc::fence_after_sync();
-                    const uint32_t sa = tc::smem_u32(smem + stage * C::STAGE_BYTES);
-                    const uint32_t sb = sa + A_BYTES;
 #pragma unroll
-                    for (int kk = 0; kk < BK / 16; ++kk) {
-                        tc::mma_bf16_pair(d_tmem, tc::sdesc_k128_sw128(sa + kk * 32),
-                                          tc::sdesc_k128_sw128(sb + kk * 32), idesc,
-                                          (kb | kk) != 0 ? 1u : 0u);
+                    for (int at = 0; at < ATOMS; ++at) {
+                        const uint32_t sa =
+                            tc::smem_u32(smem + stage * C::STAGE_BYTES + at * C::ATOM_BYTES);
+                        const uint32_t sb = sa + A_BYTES;
+#pragma unroll
+                        for (int kk = 0; kk < BK / 16; ++kk) {
+                            tc::mma_bf16_pair(d_tmem, tc::sdesc_k128_sw128(sa + kk * 32),
+                                              tc::sdesc_k128_sw128(sb + kk * 32), idesc,
+                                              (kb | at | kk) != 0 ? 1u : 0u);
+                        }
                     }
                     tc::mma_commit_pair_mc(&empty[stage], 0x3);
                     if (++stage == STAGES) { stage = 0; phase ^= 1; }
@@ -661,11 +670,11 @@ cudaError_t launch_one(const CUtensorMap& a, const CUtensorMap& b, const Params&
     return cudaGetLastError();
 }
 
-template <int STAGES, bool GEMM1, int EW>
+template <int STAGES, bool GEMM1, int EW, int ATOMS>
 cudaError_t launch_one_pair(const CUtensorMap& a, const CUtensorMap& b, const Params& p,
                             cudaStream_t s) {
-    using C = Cfg2<STAGES, GEMM1, EW>;
-    constexpr auto kern = grouped_gemm_pair<STAGES, GEMM1, EW>;
+    using C = Cfg2<STAGES, GEMM1, EW, ATOMS>;
+    constexpr auto kern = grouped_gemm_pair<STAGES, GEMM1, EW, ATOMS>;
     cudaError_t err = ensure_smem<kern>(C::SMEM);
     if (err != cudaSuccess) return err;
     cudaLaunchConfig_t cfg = {};
@@ -724,9 +733,9 @@ cudaError_t launch_expert_ffn_tc(const moe_config& c, const void* x_perm, int64_
         if (!make_map(&pm[1], x_perm, c.d, (uint64_t)x_rows, BN2 / 2) ||
             !make_map(&pm[3], h, c.d_ff, (uint64_t)h_rows, BN2 / 2))
             return cudaErrorInvalidValue;
-        cudaError_t err = launch_one_pair<6, true, 16>(pm[0], pm[1], p1, s);
+        cudaError_t err = launch_one_pair<3, true, 16, 2>(pm[0], pm[1], p1, s);
         if (err != cudaSuccess) return err;
-        return launch_one_pair<6, false, 8>(pm[2], pm[3], p2, s);
+        return launch_one_pair<3, false, 8, 2>(pm[2], pm[3], p2, s);
     }
     return launch_pair<64, 8, 1>(maps, p1, p2, s);
 }

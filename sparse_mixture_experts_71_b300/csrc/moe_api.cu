@@ -106,8 +106,7 @@ WsLayout ws_layout(const moe_config& c) {
     L.blk_hist = take(sizeof(int32_t) * (size_t)L.hist_blocks * c.E);
     L.blk_base = take(sizeof(int32_t) * (size_t)L.hist_blocks * c.E);
     L.local_rank = take(sizeof(int32_t) * (size_t)n);
-    L.wsplit = take((L.route.mma || L.route.tc) ? sizeof(uint16_t) * 3 * (size_t)L.route.epad * c.d
-                                                : 0);
+    L.wsplit = take(L.route.tc ? sizeof(uint16_t) * 3 * (size_t)L.route.epad * c.d : 0);
     L.topk_idx = take(sizeof(int32_t) * (size_t)n);
     L.topk_w = take(sizeof(float) * (size_t)n);
     L.offsets = take(sizeof(int32_t) * (size_t)(c.E + 1));

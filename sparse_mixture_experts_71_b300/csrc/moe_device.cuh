@@ -73,35 +73,44 @@ struct LossArgs {
 // Switch auxiliary loss E * sum_e f_e P_e (f_e = top1_e / T, P_e = the mean
 // probability, summed over the router blocks in block order) and the copy of
 // the per-expert counts, by one block.  Only the first 256 threads take part,
-// so the summation order is the same in every kernel that calls it.
-// s_part: 256 doubles, s_d: E doubles of shared memory.
-__device__ __forceinline__ void loss_and_counts(const LossArgs& l, double* s_part, double* s_d) {
+// so the summation order is the same in every kernel that calls it.  fp32
+// throughout (the sums of at most T probabilities keep ~1e-6 relative error).
+// s_part: 256 floats, s_d: E floats of shared memory.
+__device__ __forceinline__ void loss_and_counts(const LossArgs& l, float* s_part, float* s_d) {
     const int tid = threadIdx.x;
     const int per = 256 / l.E;  // threads per expert
     const int stride = per * l.E;
     if (tid < 256) {
-        double v = 0.0;
+        float v = 0.f;
         if (tid < stride) {
             const int e = tid % l.E;
-#pragma unroll 8
-            for (int b = tid / l.E; b < l.nblk; b += per)
-                v += (double)__ldcg(l.blk_p + (size_t)b * l.E + e);
+            // blocks tid/E, tid/E + per, ... in order; eight loads in flight
+            for (int b0 = tid / l.E; b0 < l.nblk; b0 += 8 * per) {
+                float q[8];
+#pragma unroll
+                for (int u = 0; u < 8; ++u) {
+                    const int b = b0 + u * per;
+                    q[u] = b < l.nblk ? __ldcg(l.blk_p + (size_t)b * l.E + e) : 0.f;
+                }
+#pragma unroll
+                for (int u = 0; u < 8; ++u) v += q[u];
+            }
         }
         s_part[tid] = v;
     }
     __syncthreads();
     for (int e = tid; e < l.E; e += blockDim.x) {
-        double pe = 0.0;
+        float pe = 0.f;
         for (int j = 0; j < per; ++j) pe += s_part[j * l.E + e];
-        s_d[e] = (double)__ldcg(l.top1 + e) * pe;
+        s_d[e] = (float)__ldcg(l.top1 + e) * pe;
         if (l.expert_counts != nullptr) l.expert_counts[e] = __ldcg(l.counts + e);
     }
     __syncthreads();
     if (tid == 0 && l.aux_out != nullptr) {
-        double s = 0.0;
+        float s = 0.f;
         for (int e = 0; e < l.E; ++e) s += s_d[e];
-        const double Td = (double)l.T;
-        l.aux_out[0] = (float)((double)l.E * s / (Td * Td));
+        const float Tf = (float)l.T;
+        l.aux_out[0] = (float)l.E * (s / Tf) / Tf;
     }
 }
 

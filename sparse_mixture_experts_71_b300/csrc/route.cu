@@ -150,11 +150,11 @@ __global__ void __launch_bounds__(kThreads) route_warp_kernel(RouteArgs a) {
 }
 
 // ===================================================================== tensor-core kernel
-// bf16 x with E <= 64.  The logits are a skinny GEMM (N = E); each warp owns
+// bf16 x with E <= 16.  The logits are a skinny GEMM (N = E); each warp owns
 // a 16-token tile and runs mma.sync m16n8k16 (bf16 in, fp32 accumulate)
-// against W_r split into three bf16 parts (hi + mid + lo = W_r exactly), so
-// every product is exact and only the fp32 accumulation rounds, as in the
-// fp32 SIMT path.  The K order inside each 32-column chunk is permuted so
+// against W_r split in registers into three bf16 parts (hi + mid + lo = W_r
+// exactly), so every product is exact and only the fp32 accumulation rounds,
+// as in the fp32 SIMT path.  The K order inside each 32-column chunk is permuted so
 // that one 16-byte load per row feeds two MMAs: MMA column slots (2t, 2t+1,
 // 2t+8, 2t+9) of lane quad t map to physical columns 8t .. 8t+3 in the first
 // MMA and 8t+4 .. 8t+7 in the second, identically for x and W_r.
@@ -191,9 +191,7 @@ __device__ __forceinline__ void mma_bf16_16816(float (&d)[4], uint32_t a0, uint3
 }
 
 template <int NT, int MT>
-__global__ void __launch_bounds__(kThreads) route_mma_kernel(RouteArgs a,
-                                                            const __nv_bfloat16* __restrict__ wsp,
-                                                            int epad) {
+__global__ void __launch_bounds__(kThreads) route_mma_kernel(RouteArgs a) {
     constexpr int EMAX = 8 * NT;
     constexpr int DS = kWarps / MT;
     constexpr int TB = 16 * MT;
@@ -220,7 +218,6 @@ __global__ void __launch_bounds__(kThreads) route_mma_kernel(RouteArgs a,
     if (a.logits_in == nullptr) {
         const __nv_bfloat16* x = reinterpret_cast<const __nv_bfloat16*>(a.x);
         const int nchunk = (a.d + 31) / 32;
-        const size_t plane = (size_t)epad * a.d;
 #pragma unroll 2
         for (int ch = split; ch < nchunk; ch += DS) {
             const int c = ch * 32 + 8 * tq;
@@ -230,14 +227,32 @@ __global__ void __launch_bounds__(kThreads) route_mma_kernel(RouteArgs a,
             if (cin && r1 < a.T) xb = __ldg(reinterpret_cast<const uint4*>(x + (size_t)r1 * a.d + c));
 #pragma unroll
             for (int nt = 0; nt < NT; ++nt) {
+                // this lane's 8 W_r values (expert nt*8+g, columns c..c+7), split
+                // into hi + mid + lo bf16 parts, packed in column pairs
+                float w[8];
+                const int e = nt * 8 + g;
+                if (cin && e < a.E) {
+                    load8_f32(a.W_r + (size_t)e * a.d + c, w);
+                } else {
 #pragma unroll
-                for (int part = 0; part < 3; ++part) {
-                    uint4 wv = make_uint4(0, 0, 0, 0);
-                    if (cin)
-                        wv = __ldg(reinterpret_cast<const uint4*>(
-                            wsp + part * plane + (size_t)(nt * 8 + g) * a.d + c));
-                    mma_bf16_16816(acc[nt], xa.x, xb.x, xa.y, xb.y, wv.x, wv.y);
-                    mma_bf16_16816(acc[nt], xa.z, xb.z, xa.w, xb.w, wv.z, wv.w);
+                    for (int q = 0; q < 8; ++q) w[q] = 0.f;
+                }
+                uint32_t part[3][4];
+#pragma unroll
+                for (int q = 0; q < 8; q += 2) {
+                    const __nv_bfloat162 hi = __floats2bfloat162_rn(w[q], w[q + 1]);
+                    const float r0 = w[q] - __low2float(hi), r1 = w[q + 1] - __high2float(hi);
+                    const __nv_bfloat162 mid = __floats2bfloat162_rn(r0, r1);
+                    const __nv_bfloat162 lo = __floats2bfloat162_rn(r0 - __low2float(mid),
+                                                                   r1 - __high2float(mid));
+                    part[0][q / 2] = *reinterpret_cast<const uint32_t*>(&hi);
+                    part[1][q / 2] = *reinterpret_cast<const uint32_t*>(&mid);
+                    part[2][q / 2] = *reinterpret_cast<const uint32_t*>(&lo);
+                }
+#pragma unroll
+                for (int pp = 0; pp < 3; ++pp) {
+                    mma_bf16_16816(acc[nt], xa.x, xb.x, xa.y, xb.y, part[pp][0], part[pp][1]);
+                    mma_bf16_16816(acc[nt], xa.z, xb.z, xa.w, xb.w, part[pp][2], part[pp][3]);
                 }
             }
         }
@@ -551,19 +566,18 @@ cudaError_t launch_warp_tw(const RouteArgs& a, const RouteGeom& g, cudaStream_t 
 }
 
 template <int NT, int MT>
-cudaError_t launch_mma_t(const RouteArgs& a, const __nv_bfloat16* wsp, int epad, cudaStream_t s) {
-    route_mma_kernel<NT, MT><<<a.nblk, kThreads, 0, s>>>(a, wsp, epad);
+cudaError_t launch_mma_t(const RouteArgs& a, cudaStream_t s) {
+    route_mma_kernel<NT, MT><<<a.nblk, kThreads, 0, s>>>(a);
     count_launches(1);
     return cudaGetLastError();
 }
 
 template <int NT>
-cudaError_t launch_mma_nt(const RouteArgs& a, const RouteGeom& g, const __nv_bfloat16* wsp,
-                          cudaStream_t s) {
-    if (g.mt >= 8) return launch_mma_t<NT, 8>(a, wsp, 8 * NT, s);
-    if (g.mt == 4) return launch_mma_t<NT, 4>(a, wsp, 8 * NT, s);
-    if (g.mt == 2) return launch_mma_t<NT, 2>(a, wsp, 8 * NT, s);
-    return launch_mma_t<NT, 1>(a, wsp, 8 * NT, s);
+cudaError_t launch_mma_nt(const RouteArgs& a, const RouteGeom& g, cudaStream_t s) {
+    if (g.mt >= 8) return launch_mma_t<NT, 8>(a, s);
+    if (g.mt == 4) return launch_mma_t<NT, 4>(a, s);
+    if (g.mt == 2) return launch_mma_t<NT, 2>(a, s);
+    return launch_mma_t<NT, 1>(a, s);
 }
 
 cudaError_t launch_split(const RouteArgs& a, int epad, __nv_bfloat16* wsp, cudaStream_t s) {
@@ -576,15 +590,9 @@ cudaError_t launch_split(const RouteArgs& a, int epad, __nv_bfloat16* wsp, cudaS
     return cudaGetLastError();
 }
 
-cudaError_t launch_mma(const RouteArgs& a, const RouteGeom& g, __nv_bfloat16* wsp,
-                       cudaStream_t s) {
-    const int epad = g.epad;
-    cudaError_t err = launch_split(a, epad, wsp, s);
-    if (err != cudaSuccess) return err;
-    if (epad <= 8) return launch_mma_nt<1>(a, g, wsp, s);
-    if (epad <= 16) return launch_mma_nt<2>(a, g, wsp, s);
-    if (epad <= 32) return launch_mma_nt<4>(a, g, wsp, s);
-    return launch_mma_nt<8>(a, g, wsp, s);
+cudaError_t launch_mma(const RouteArgs& a, const RouteGeom& g, cudaStream_t s) {
+    if (g.epad <= 8) return launch_mma_nt<1>(a, g, s);
+    return launch_mma_nt<2>(a, g, s);
 }
 
 template <typename TX>
@@ -600,8 +608,8 @@ cudaError_t launch_e(const RouteArgs& a, const RouteGeom& g, cudaStream_t s) {
 }
 
 __global__ void __launch_bounds__(256) route_finish_kernel(LossArgs l) {
-    __shared__ double s_part[256];
-    __shared__ double s_d[kMaxExperts];
+    __shared__ float s_part[256];
+    __shared__ float s_d[kMaxExperts];
     loss_and_counts(l, s_part, s_d);
 }
 
@@ -674,7 +682,7 @@ cudaError_t launch_route(const moe_config& c, const void* x, const float* W_r,
     cudaError_t err = cudaMemsetAsync(at<char>(ws, L.counts), 0, L.blk_p - L.counts, s);
     if (err != cudaSuccess) return err;
     if (L.route.mma) {
-        err = launch_mma(a, L.route, at<__nv_bfloat16>(ws, L.wsplit), s);
+        err = launch_mma(a, L.route, s);
     } else if (L.route.tc) {
         __nv_bfloat16* wsp = at<__nv_bfloat16>(ws, L.wsplit);
         err = launch_split(a, L.route.epad, wsp, s);
