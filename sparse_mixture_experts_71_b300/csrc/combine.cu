@@ -31,6 +31,8 @@ template <typename TY>
 __global__ void __launch_bounds__(256) combine_kernel(const float* __restrict__ y_perm,
                                                       const int32_t* __restrict__ slot_of, int T,
                                                       int k, int d, TY* __restrict__ y) {
+    pdl_wait();
+    pdl_trigger();
     const int lane = threadIdx.x % 32;
     const int nwarps = gridDim.x * (blockDim.x / 32);
     const int nv = d / 4;                   // float4 columns per row
@@ -74,13 +76,11 @@ cudaError_t launch_combine(const moe_config& c, const float* y_perm, const int32
     long long blocks = (tasks + 7) / 8;
     if (blocks > num_sms() * 8) blocks = num_sms() * 8;
     if (c.dtype == MOE_BF16)
-        combine_kernel<__nv_bfloat16><<<(int)blocks, 256, 0, s>>>(y_perm, slot_of, c.T, c.k, c.d,
-                                                             reinterpret_cast<__nv_bfloat16*>(y));
-    else
-        combine_kernel<float><<<(int)blocks, 256, 0, s>>>(y_perm, slot_of, c.T, c.k, c.d,
-                                                     reinterpret_cast<float*>(y));
-    count_launches(1);
-    return cudaGetLastError();
+        return launch_kernel(combine_kernel<__nv_bfloat16>, dim3((unsigned)blocks), dim3(256), 0,
+                             s, 1, false, y_perm, slot_of, c.T, c.k, c.d,
+                             reinterpret_cast<__nv_bfloat16*>(y));
+    return launch_kernel(combine_kernel<float>, dim3((unsigned)blocks), dim3(256), 0, s, 1, false,
+                         y_perm, slot_of, c.T, c.k, c.d, reinterpret_cast<float*>(y));
 }
 
 }  // namespace moe

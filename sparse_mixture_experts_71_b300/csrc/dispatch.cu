@@ -36,6 +36,8 @@ __global__ void __launch_bounds__(kCountBlock) count_kernel(const int32_t* __res
     __shared__ int wh[kWarps][kMaxExperts];
     const int tid = threadIdx.x, warp = tid / 32, lane = tid % 32;
     for (int i = tid; i < kWarps * kMaxExperts; i += kCountBlock) (&wh[0][0])[i] = 0;
+    pdl_wait();
+    pdl_trigger();
     __syncthreads();
     const int a = blockIdx.x * kCountBlock + tid;
     int e = -1;
@@ -78,6 +80,8 @@ __global__ void __launch_bounds__(1024) scan_kernel(const int32_t* __restrict__ 
     __shared__ int s_total[kMaxExperts];
     __shared__ float s_part[256];
     __shared__ float s_d[kMaxExperts];
+    pdl_wait();
+    pdl_trigger();
     if (loss.blk_p != nullptr) loss_and_counts(loss, s_part, s_d);
     const int tid = threadIdx.x, warp = tid / 32, lane = tid % 32;
     const int P = 1024 / E;
@@ -141,6 +145,8 @@ __global__ void __launch_bounds__(256) permute_kernel(
     const int32_t* __restrict__ offsets, int n, int k, int E, int d, int capacity,
     int asg_per_block, int32_t* __restrict__ slot_of, int32_t* __restrict__ perm_token, float* __restrict__ perm_w,
     TX* __restrict__ x_perm) {
+    pdl_wait();
+    pdl_trigger();
     const int lane = threadIdx.x % 32;
     const int nwarps = gridDim.x * (blockDim.x / 32);
     const int nvec = d * (int)sizeof(TX) / 16;  // 16-byte vectors per row
@@ -179,12 +185,9 @@ cudaError_t launch_count(const moe_config& c, const int32_t* topk_idx, void* ws,
                          const WsLayout& L, cudaStream_t s) {
     const int n = c.T * c.k;
     if (n == 0) return cudaSuccess;
-    count_kernel<<<L.count_blocks, kCountBlock, 0, s>>>(topk_idx, n, c.E,
-                                                        at<int32_t>(ws, L.blk_hist),
-                                                        at<int32_t>(ws, L.local_rank),
-                                                        at<DeviceHeader>(ws, L.header));
-    count_launches(1);
-    return cudaGetLastError();
+    return launch_kernel(count_kernel, dim3(L.count_blocks), dim3(kCountBlock), 0, s, 1, false,
+                         topk_idx, n, c.E, at<int32_t>(ws, L.blk_hist),
+                         at<int32_t>(ws, L.local_rank), at<DeviceHeader>(ws, L.header));
 }
 
 cudaError_t launch_scan_permute(const moe_config& c, const void* x, const int32_t* topk_idx,
@@ -196,26 +199,24 @@ cudaError_t launch_scan_permute(const moe_config& c, const void* x, const int32_
     int32_t* blk_hist = at<int32_t>(ws, L.blk_hist);
     int32_t* blk_base = at<int32_t>(ws, L.blk_base);
     int32_t* local_rank = at<int32_t>(ws, L.local_rank);
-    scan_kernel<<<1, 1024, 0, s>>>(blk_hist, hist_blocks, c.E, c.capacity, blk_base, offsets,
-                                   loss);
-    count_launches(1);
-    if (n > 0) {
-        int blocks = (n + 7) / 8;
-        blocks = blocks < num_sms() * 8 ? blocks : num_sms() * 8;
-        if (c.dtype == MOE_BF16) {
-            permute_kernel<__nv_bfloat16><<<blocks, 256, 0, s>>>(
-                reinterpret_cast<const __nv_bfloat16*>(x), topk_idx, topk_w, local_rank, blk_base,
-                offsets, n, c.k, c.E, c.d, c.capacity, asg_per_block, slot_of, perm_token, perm_w,
-                reinterpret_cast<__nv_bfloat16*>(x_perm));
-        } else {
-            permute_kernel<float><<<blocks, 256, 0, s>>>(
-                reinterpret_cast<const float*>(x), topk_idx, topk_w, local_rank, blk_base, offsets,
-                n, c.k, c.E, c.d, c.capacity, asg_per_block, slot_of, perm_token, perm_w,
-                reinterpret_cast<float*>(x_perm));
-        }
-        count_launches(1);
-    }
-    return cudaGetLastError();
+    cudaError_t e = launch_kernel(scan_kernel, dim3(1), dim3(1024), 0, s, 1, false,
+                                  (const int32_t*)blk_hist, hist_blocks, c.E, c.capacity, blk_base,
+                                  offsets, loss);
+    if (e != cudaSuccess || n == 0) return e;
+    int blocks = (n + 7) / 8;
+    blocks = blocks < num_sms() * 8 ? blocks : num_sms() * 8;
+    if (c.dtype == MOE_BF16)
+        return launch_kernel(permute_kernel<__nv_bfloat16>, dim3(blocks), dim3(256), 0, s, 1, false,
+                             reinterpret_cast<const __nv_bfloat16*>(x), topk_idx, topk_w,
+                             (const int32_t*)local_rank, (const int32_t*)blk_base,
+                             (const int32_t*)offsets, n, c.k, c.E, c.d, c.capacity,
+                             asg_per_block, slot_of, perm_token, perm_w,
+                             reinterpret_cast<__nv_bfloat16*>(x_perm));
+    return launch_kernel(permute_kernel<float>, dim3(blocks), dim3(256), 0, s, 1, false,
+                         reinterpret_cast<const float*>(x), topk_idx, topk_w,
+                         (const int32_t*)local_rank, (const int32_t*)blk_base,
+                         (const int32_t*)offsets, n, c.k, c.E, c.d, c.capacity, asg_per_block,
+                         slot_of, perm_token, perm_w, reinterpret_cast<float*>(x_perm));
 }
 
 }  // namespace moe

@@ -31,6 +31,8 @@ __global__ void __launch_bounds__(256) grouped_gemm_simt(
     int K, int max_rows) {
     __shared__ float As[BK][BM + PAD];
     __shared__ float Bs[BK][BN + PAD];
+    pdl_wait();
+    pdl_trigger();
     const int e = blockIdx.z;
     // segment bounds, clamped to the buffers (offsets come from device memory)
     const int seg1 = min(__ldg(offsets + e + 1), max_rows);
@@ -94,15 +96,16 @@ cudaError_t launch_t(const moe_config& c, const void* x_perm, const int32_t* off
     const int mt = (int)((max_seg + BM - 1) / BM);
     if (mt == 0) return cudaSuccess;
     dim3 g1((c.d_ff + BN - 1) / BN, mt, c.E), g2((c.d + BN - 1) / BN, mt, c.E);
-    grouped_gemm_simt<TIN, TIN, true><<<g1, 256, 0, s>>>(
+    const cudaError_t e = launch_kernel(
+        grouped_gemm_simt<TIN, TIN, true>, g1, dim3(256), 0, s, 1, false,
         reinterpret_cast<const TIN*>(x_perm), offsets, reinterpret_cast<const TIN*>(W1),
-        reinterpret_cast<const TIN*>(b1), nullptr, reinterpret_cast<TIN*>(h), c.d_ff, c.d,
-        (int)max_rows);
-    grouped_gemm_simt<TIN, float, false><<<g2, 256, 0, s>>>(
-        reinterpret_cast<const TIN*>(h), offsets, reinterpret_cast<const TIN*>(W2),
-        reinterpret_cast<const TIN*>(b2), perm_w, y_perm, c.d, c.d_ff, (int)max_rows);
-    count_launches(2);
-    return cudaGetLastError();
+        reinterpret_cast<const TIN*>(b1), (const float*)nullptr, reinterpret_cast<TIN*>(h),
+        c.d_ff, c.d, (int)max_rows);
+    if (e != cudaSuccess) return e;
+    return launch_kernel(grouped_gemm_simt<TIN, float, false>, g2, dim3(256), 0, s, 1, false,
+                         reinterpret_cast<const TIN*>(h), offsets,
+                         reinterpret_cast<const TIN*>(W2), reinterpret_cast<const TIN*>(b2),
+                         perm_w, y_perm, c.d, c.d_ff, (int)max_rows);
 }
 
 }  // namespace

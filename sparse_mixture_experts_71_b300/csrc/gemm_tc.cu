@@ -161,8 +161,12 @@ __device__ __forceinline__ void epilogue_tile(const Params& p, int e, int r0, in
         if (GEMM1) {
             __nv_bfloat16* s16 = reinterpret_cast<__nv_bfloat16*>(stg);
 #pragma unroll
-            for (int j = 0; j < 32; ++j)
-                s16[j * 32 + lane] = __float2bfloat16_rn(gelu_as7126(v[j] + bias));
+            for (int j = 0; j < 32; j += 2) {
+                const float2 g = gelu2_as7126(
+                    __fadd2_rn(make_float2(v[j], v[j + 1]), make_float2(bias, bias)));
+                s16[j * 32 + lane] = __float2bfloat16_rn(g.x);
+                s16[(j + 1) * 32 + lane] = __float2bfloat16_rn(g.y);
+            }
             __syncwarp();
             __nv_bfloat16* out = reinterpret_cast<__nv_bfloat16*>(p.out);
 #pragma unroll
@@ -241,6 +245,8 @@ grouped_gemm_tc(const __grid_constant__ CUtensorMap tmA, const __grid_constant__
         tc::tmem_alloc(s_tmem, C::TMEM_COLS);
         tc::tmem_relinquish();
     }
+    pdl_wait();  // offsets and the operands come from the previous kernel
+    pdl_trigger();
     if (warp == 3) {  // exclusive prefix of tiles per expert
         int run = 0;
         for (int e0 = 0; e0 < p.E; e0 += 32) {
@@ -359,7 +365,7 @@ grouped_gemm_tc(const __grid_constant__ CUtensorMap tmA, const __grid_constant__
                                          half, 2, lane, stg);
             tc::fence_before_sync();
             __syncwarp();
-            if (lane == 0) tc::mbar_arrive(&tempty[acc]);
+            if (lane == 0) tc::mbar_arrive_relaxed(&tempty[acc]);
             acc ^= 1;
             if (acc == 0) acc_phase ^= 1;
         }
@@ -409,6 +415,28 @@ struct Cfg2 {
     static_assert(SMEM <= 232448, "shared memory budget");
 };
 
+// Pair tile t: expert e (binary search over the per-expert tile prefix),
+// then token tile fastest and 256-row weight tile, so the token tiles that
+// share a weight tile run at about the same time and re-read it from L2.
+__device__ __forceinline__ Tile decode_pair_tile(int t, const int* s_tiles, const Params& p,
+                                                 int mt2) {
+    int lo = 0, hi = p.E - 1;
+    while (lo < hi) {  // last expert whose first tile is <= t
+        const int mid = (lo + hi + 1) >> 1;
+        if (s_tiles[mid] <= t) lo = mid; else hi = mid - 1;
+    }
+    const int s0 = min(max(__ldg(p.offsets + lo), 0), p.rows_cap);
+    const int s1 = min(max(__ldg(p.offsets + lo + 1), s0), p.rows_cap);
+    const int nt = (s1 - s0 + BN2 - 1) / BN2;
+    const int local = t - s_tiles[lo];
+    Tile tl;
+    tl.e = lo;
+    tl.r0 = s0 + (local % nt) * BN2;
+    tl.n = min(BN2, s1 - tl.r0);
+    tl.m0 = (local / nt) * 2 * BM;
+    return tl;
+}
+
 template <int STAGES, bool GEMM1, int EW, int ATOMS>
 __global__ void __launch_bounds__(Cfg2<STAGES, GEMM1, EW, ATOMS>::THREADS, 1)
 grouped_gemm_pair(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
@@ -452,6 +480,8 @@ grouped_gemm_pair(const __grid_constant__ CUtensorMap tmA, const __grid_constant
         tc::tmem_alloc_pair(s_tmem, C::TMEM_COLS);
         tc::tmem_relinquish_pair();
     }
+    pdl_wait();  // offsets and the operands come from the previous kernel
+    pdl_trigger();
     if (warp == 3) {  // exclusive prefix of pair tiles per expert
         int run = 0;
         for (int e0 = 0; e0 < p.E; e0 += 32) {
@@ -488,8 +518,8 @@ grouped_gemm_pair(const __grid_constant__ CUtensorMap tmA, const __grid_constant
             bool ok = true;
             const uint32_t bytes = 2 * C::STAGE_BYTES;  // whole boxes of both CTAs
             for (int t = pair; t < total && ok; t += npairs) {
-                const Tile tl = decode_tile(t, s_tiles, p, BN2, 1, 0);  // m0 in 256-row units / 2
-                const int m0 = (tl.m0 / BM) * 2 * BM;                  // pair tile base row
+                const Tile tl = decode_pair_tile(t, s_tiles, p, mt2);
+                const int m0 = tl.m0;  // pair tile base row
                 const int half_rows = ((tl.n + 31) & ~31) / 2;
                 const int arow = tl.e * p.n_out + m0 + rank * BM;
                 const int brow = tl.r0 + rank * half_rows;
@@ -520,7 +550,7 @@ grouped_gemm_pair(const __grid_constant__ CUtensorMap tmA, const __grid_constant
             uint32_t phase = 0, acc_phase = 0;
             bool ok = true;
             for (int t = pair; t < total && ok; t += npairs) {
-                const Tile tl = decode_tile(t, s_tiles, p, BN2, 1, 0);
+                const Tile tl = decode_pair_tile(t, s_tiles, p, mt2);
                 const uint32_t N = (uint32_t)((tl.n + 31) & ~31);
                 const uint32_t idesc = tc::idesc_bf16_f32(2 * BM, N);
                 if (!wait_bar(&tempty[acc], acc_phase ^ 1, s_abort, p, 2)) break;
@@ -561,8 +591,8 @@ grouped_gemm_pair(const __grid_constant__ CUtensorMap tmA, const __grid_constant
         int acc = 0;
         uint32_t acc_phase = 0;
         for (int t = pair; t < total; t += npairs) {
-            const Tile tl = decode_tile(t, s_tiles, p, BN2, 1, 0);
-            const int m0 = (tl.m0 / BM) * 2 * BM;
+            const Tile tl = decode_pair_tile(t, s_tiles, p, mt2);
+            const int m0 = tl.m0;
             const bool ok = wait_bar(&tfull[acc], acc_phase, s_abort, p, 4);
             if (!__all_sync(0xffffffffu, ok)) break;
             tc::fence_after_sync();
@@ -570,7 +600,7 @@ grouped_gemm_pair(const __grid_constant__ CUtensorMap tmA, const __grid_constant
                                       q, part, EW / 4, lane, stg);
             tc::fence_before_sync();
             __syncwarp();
-            if (lane == 0) tc::mbar_arrive_cluster(tc::cluster_addr(&tempty[acc], 0));
+            if (lane == 0) tc::mbar_arrive_cluster_relaxed(tc::cluster_addr(&tempty[acc], 0));
             acc ^= 1;
             if (acc == 0) acc_phase ^= 1;
         }
@@ -648,26 +678,8 @@ cudaError_t launch_one(const CUtensorMap& a, const CUtensorMap& b, const Params&
     constexpr auto kern = grouped_gemm_tc<BN_MAX, STAGES, GEMM1, CS>;
     cudaError_t err = ensure_smem<kern>(C::SMEM);
     if (err != cudaSuccess) return err;
-    if (CS == 1) {
-        kern<<<num_sms(), kThreads, C::SMEM, s>>>(a, b, p);
-    } else {
-        cudaLaunchConfig_t cfg = {};
-        cfg.gridDim = dim3(CS * resident_clusters<kern>(CS, C::SMEM), 1, 1);
-        cfg.blockDim = dim3(kThreads, 1, 1);
-        cfg.dynamicSmemBytes = C::SMEM;
-        cfg.stream = s;
-        cudaLaunchAttribute attr;
-        attr.id = cudaLaunchAttributeClusterDimension;
-        attr.val.clusterDim.x = CS;
-        attr.val.clusterDim.y = 1;
-        attr.val.clusterDim.z = 1;
-        cfg.attrs = &attr;
-        cfg.numAttrs = 1;
-        err = cudaLaunchKernelEx(&cfg, kern, a, b, p);
-        if (err != cudaSuccess) return err;
-    }
-    count_launches(1);
-    return cudaGetLastError();
+    const int grid = CS == 1 ? num_sms() : CS * resident_clusters<kern>(CS, C::SMEM);
+    return launch_kernel(kern, dim3(grid), dim3(kThreads), C::SMEM, s, CS, true, a, b, p);
 }
 
 template <int STAGES, bool GEMM1, int EW, int ATOMS>
@@ -677,22 +689,8 @@ cudaError_t launch_one_pair(const CUtensorMap& a, const CUtensorMap& b, const Pa
     constexpr auto kern = grouped_gemm_pair<STAGES, GEMM1, EW, ATOMS>;
     cudaError_t err = ensure_smem<kern>(C::SMEM);
     if (err != cudaSuccess) return err;
-    cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3(2 * resident_clusters<kern>(2, C::SMEM, C::THREADS), 1, 1);
-    cfg.blockDim = dim3(C::THREADS, 1, 1);
-    cfg.dynamicSmemBytes = C::SMEM;
-    cfg.stream = s;
-    cudaLaunchAttribute attr;
-    attr.id = cudaLaunchAttributeClusterDimension;
-    attr.val.clusterDim.x = 2;
-    attr.val.clusterDim.y = 1;
-    attr.val.clusterDim.z = 1;
-    cfg.attrs = &attr;
-    cfg.numAttrs = 1;
-    err = cudaLaunchKernelEx(&cfg, kern, a, b, p);
-    if (err != cudaSuccess) return err;
-    count_launches(1);
-    return cudaGetLastError();
+    return launch_kernel(kern, dim3(2 * resident_clusters<kern>(2, C::SMEM, C::THREADS)),
+                         dim3(C::THREADS), C::SMEM, s, 2, true, a, b, p);
 }
 
 template <int BN_MAX, int STAGES, int CS>

@@ -15,6 +15,11 @@ namespace moe {
 static std::atomic<uint64_t> g_launches{0};
 void count_launches(int n) { g_launches.fetch_add((uint64_t)n, std::memory_order_relaxed); }
 
+// Position of the next launch in the calling thread's current chain.
+static thread_local int t_chain_pos = 0;
+void chain_begin() { t_chain_pos = 0; }
+bool chain_next() { return t_chain_pos++ > 0; }
+
 int num_sms() {
     static int sms[64] = {0};
     int dev = 0;
@@ -171,6 +176,7 @@ moe_status moe_route(const moe_config* cfg, const void* x, const float* W_r,
     if (logits_in == nullptr && (x == nullptr || W_r == nullptr)) return MOE_ERR_INVALID_ARG;
     if (logits_in == nullptr && (!aligned16(x) || !aligned16(W_r))) return MOE_ERR_ALIGNMENT;
     if ((st = check_ws(c, ws, ws_bytes, &L)) != MOE_OK) return st;
+    chain_begin();
     return from_cuda(launch_route(c, x, W_r, logit_bias, logits_in, logits_out, topk_idx, topk_w,
                                   expert_counts, aux_out, ws, L, false, s));
 }
@@ -196,6 +202,7 @@ moe_status moe_dispatch(const moe_config* cfg, const void* x, const int32_t* top
     WsLayout L;
     if ((st = check_ws(c, ws, ws_bytes, &L)) != MOE_OK) return st;
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    chain_begin();
     cudaError_t e = launch_count(c, topk_idx, ws, L, s);
     if (e == cudaSuccess)
         e = launch_scan_permute(c, x, topk_idx, topk_w, kCountBlock, L.count_blocks, offsets,
@@ -218,6 +225,7 @@ moe_status moe_expert_ffn(const moe_config* cfg, const void* x_perm, const int32
         return MOE_ERR_ALIGNMENT;
     WsLayout L;
     if ((st = check_ws(c, ws, ws_bytes, &L)) != MOE_OK) return st;
+    chain_begin();
     return from_cuda(launch_expert_ffn(c, x_perm, (int64_t)c.T * c.k, offsets, W1, b1, W2, b2,
                                        perm_w, y_perm, ws, L,
                                        reinterpret_cast<cudaStream_t>(stream)));
@@ -231,6 +239,7 @@ moe_status moe_combine(const moe_config* cfg, const float* y_perm, const int32_t
     if (c.T == 0) return MOE_OK;
     if (y_perm == nullptr || slot_of == nullptr || y == nullptr) return MOE_ERR_INVALID_ARG;
     if (!aligned16(y_perm) || !aligned16(y)) return MOE_ERR_ALIGNMENT;
+    chain_begin();
     return from_cuda(launch_combine(c, y_perm, slot_of, y, reinterpret_cast<cudaStream_t>(stream)));
 }
 
@@ -259,6 +268,7 @@ moe_status moe_forward(const moe_config* cfg, const void* x, const float* W_r,
     float* perm_w = at<float>(ws, L.perm_w);
     void* x_perm = at<void>(ws, L.x_perm);
     float* y_perm = at<float>(ws, L.y_perm);
+    chain_begin();
     cudaError_t e = launch_route(c, x, W_r, logit_bias, nullptr, logits_out, idx, w, expert_counts,
                                  aux_out, ws, L, true, s);
     if (e == cudaSuccess)

@@ -8,6 +8,19 @@
 
 namespace moe {
 
+// Programmatic dependent launch.  Inside one entry-point call every kernel
+// after the first is launched with programmatic stream serialization (see
+// launch_kernel), so the GPU may make its blocks resident while the previous
+// kernel is still running.  Each kernel therefore calls pdl_wait() before its
+// first access to global memory: it returns once the previous kernel has
+// completed and its writes are visible.  pdl_trigger() then allows the next
+// kernel to be scheduled.  Both are no-ops for a kernel launched without the
+// attribute.
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void pdl_trigger() {
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
 // Widen 8 consecutive stored elements (16 bytes of bf16, or 32 bytes of fp32)
 // to fp32.  `p` is 16-byte aligned.
 __device__ __forceinline__ void load8_f32(const __nv_bfloat16* p, float v[8]) {
@@ -40,23 +53,40 @@ __device__ __forceinline__ float gelu_erf(float u) {
     return 0.5f * u * (1.0f + erff(u * 0.70710678118654752440f));
 }
 
-// GELU 0.5 u (1 + erf(z)), z = u / sqrt 2, with erf from the rational
+// GELU 0.5 u (1 + erf(u / sqrt 2)) for two values at once, with packed fp32
+// arithmetic (two lanes per instruction).  erf comes from the rational
 // approximation of Abramowitz & Stegun, Handbook of Mathematical Functions,
 // formula 7.1.26 (Hastings): for z >= 0, erf(z) = 1 - q(t) exp(-z^2),
 // t = 1 / (1 + p z), q(t) = t (a1 + t (a2 + t (a3 + t (a4 + t a5)))), with
-// |error| <= 1.5e-7.  1 + erf(z) is q e^{-z^2} for z < 0 and 2 - q e^{-z^2}
-// for z >= 0, which keeps the negative tail free of cancellation.  Used where
-// the result is rounded to bf16 (relative step 2^-8), far above the error.
-__device__ __forceinline__ float gelu_as7126(float u) {
-    const float z = fabsf(u) * 0.70710678118654752440f;
-    const float t = __fdividef(1.0f, fmaf(0.3275911f, z, 1.0f));
-    float q = fmaf(t, 1.061405429f, -1.453152027f);
-    q = fmaf(t, q, 1.421413741f);
-    q = fmaf(t, q, -0.284496736f);
-    q = fmaf(t, q, 0.254829592f);
-    q *= t;
-    const float r = q * __expf(-z * z);
-    return 0.5f * u * (u < 0.f ? r : 2.0f - r);
+// |error| <= 1.5e-7.  With z = |u| / sqrt 2 the GELU is u - 0.5 u q e^{-z^2}
+// for u >= 0 and 0.5 u q e^{-z^2} for u < 0, i.e.
+//   gelu(u) = max(u, 0) - 0.5 |u| q(t) e^{-z^2},
+// which has no cancellation in the negative tail and needs no select.  With
+// y = |u| sqrt(log2(e) / 2), e^{-z^2} is 2^{-y^2} and p z is
+// (p / sqrt(log2 e)) y; the factor -0.5 |u| / y is folded into the
+// coefficients.  Used where the result is rounded to bf16 (relative step
+// 2^-8), far above the approximation error.
+__device__ __forceinline__ float ex2_approx(float x) {
+    float y;
+    asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+    return y;
+}
+__device__ __forceinline__ float2 gelu2_as7126(float2 u) {
+    constexpr float c = 0.84932180028801904f;  // sqrt(log2(e) / 2)
+    constexpr float pz = 0.27273748f;          // 0.3275911 / sqrt(log2 e)
+    constexpr float k = -0.5f / c;             // -0.5 |u| = k y
+    const float2 y = make_float2(fabsf(u.x) * c, fabsf(u.y) * c);
+    const float2 den = __ffma2_rn(y, make_float2(pz, pz), make_float2(1.f, 1.f));
+    const float2 t = make_float2(__fdividef(1.0f, den.x), __fdividef(1.0f, den.y));
+    float2 q = __ffma2_rn(t, make_float2(k * 1.061405429f, k * 1.061405429f),
+                          make_float2(k * -1.453152027f, k * -1.453152027f));
+    q = __ffma2_rn(t, q, make_float2(k * 1.421413741f, k * 1.421413741f));
+    q = __ffma2_rn(t, q, make_float2(k * -0.284496736f, k * -0.284496736f));
+    q = __ffma2_rn(t, q, make_float2(k * 0.254829592f, k * 0.254829592f));
+    q = __fmul2_rn(q, t);
+    const float2 s = __fmul2_rn(y, y);
+    const float2 e = make_float2(ex2_approx(-s.x), ex2_approx(-s.y));
+    return __ffma2_rn(y, __fmul2_rn(q, e), make_float2(fmaxf(u.x, 0.f), fmaxf(u.y, 0.f)));
 }
 
 // Inputs of the auxiliary-loss reduction: per-block sums of p written by the

@@ -85,6 +85,54 @@ cudaError_t ensure_smem(int bytes) {
     return e;
 }
 
+// ---- kernel launches
+// The kernels one entry point enqueues form a chain: the first is launched
+// normally (it waits for whatever the caller enqueued before it), every later
+// one with programmatic stream serialization, so its blocks may become
+// resident and run their set-up while the previous kernel finishes; the
+// kernel's pdl_wait() orders its memory accesses after the previous kernel.
+// chain_begin() starts a new chain (at each entry point, and after any memset
+// an entry point enqueues between kernels); chain_next() reports whether the
+// next launch may use the attribute and advances the chain.
+void chain_begin();
+bool chain_next();
+
+// Launch `kern` on stream s; cluster > 1 launches clusters of that many
+// blocks along x.  `programmatic` lets the launch use programmatic stream
+// serialization when it is not the first of its chain; the tensor-core
+// kernels ask for it (their set-up - barriers, TMEM allocation, tensor-map
+// prefetch - then overlaps the previous kernel's tail).  The short SIMT
+// kernels do not: chained programmatically they ran slower on B300.
+template <typename... KArgs, typename... Args>
+cudaError_t launch_kernel(void (*kern)(KArgs...), dim3 grid, dim3 block, size_t smem,
+                          cudaStream_t s, int cluster, bool programmatic, Args... args) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = block;
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = s;
+    cudaLaunchAttribute attr[2];
+    int n = 0;
+    if (cluster > 1) {
+        attr[n].id = cudaLaunchAttributeClusterDimension;
+        attr[n].val.clusterDim.x = (unsigned)cluster;
+        attr[n].val.clusterDim.y = 1;
+        attr[n].val.clusterDim.z = 1;
+        ++n;
+    }
+    if (chain_next() && programmatic) {
+        attr[n].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+        attr[n].val.programmaticStreamSerializationAllowed = 1;
+        ++n;
+    }
+    cfg.attrs = attr;
+    cfg.numAttrs = n;
+    const cudaError_t e = cudaLaunchKernelEx(&cfg, kern, args...);
+    if (e != cudaSuccess) return e;
+    count_launches(1);
+    return cudaGetLastError();
+}
+
 template <typename T> __host__ __device__ inline T* at(void* base, size_t off) {
     return reinterpret_cast<T*>(reinterpret_cast<char*>(base) + off);
 }

@@ -91,6 +91,7 @@ extern "C" moe_status moe_dispatch_noalloc(const moe_config* cfg, const void* x,
     // The error record must start at zero; the kernels overwrite everything
     // else they read.
     if (cudaMemsetAsync(scratch, 0, sizeof(DeviceHeader), s) != cudaSuccess) return MOE_ERR_CUDA;
+    chain_begin();  // the first kernel follows the memset
     cudaError_t e = launch_count(c, topk_idx, scratch, L, s);
     if (e == cudaSuccess)
         e = launch_scan_permute(c, x, topk_idx, topk_w, kCountBlock, L.count_blocks, offsets,

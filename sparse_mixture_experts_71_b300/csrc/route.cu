@@ -43,6 +43,8 @@ using namespace rt;
 // are added in split order.
 template <typename TX, int EMAX, int TW, int DS>
 __global__ void __launch_bounds__(kThreads) route_warp_kernel(RouteArgs a) {
+    pdl_wait();
+    pdl_trigger();
     constexpr int G = kWarps / DS;   // token groups per block
     constexpr int TB = G * TW;       // tokens per block
     constexpr int LDS = EMAX + 1;
@@ -165,6 +167,8 @@ __global__ void __launch_bounds__(kThreads) route_warp_kernel(RouteArgs a) {
 __global__ void __launch_bounds__(256) split_router_weight(const float* __restrict__ W, int E,
                                                            int epad, int d,
                                                            __nv_bfloat16* __restrict__ out) {
+    pdl_wait();
+    pdl_trigger();
     const size_t n = (size_t)epad * d;
     for (size_t i = blockIdx.x * (size_t)blockDim.x + threadIdx.x; i < n;
          i += (size_t)gridDim.x * blockDim.x) {
@@ -192,6 +196,8 @@ __device__ __forceinline__ void mma_bf16_16816(float (&d)[4], uint32_t a0, uint3
 
 template <int NT, int MT>
 __global__ void __launch_bounds__(kThreads) route_mma_kernel(RouteArgs a) {
+    pdl_wait();
+    pdl_trigger();
     constexpr int EMAX = 8 * NT;
     constexpr int DS = kWarps / MT;
     constexpr int TB = 16 * MT;
@@ -364,6 +370,8 @@ __device__ __forceinline__ void stage_chunk(const RouteArgs& a, int t0, int c0, 
 
 template <typename TX, int EMAX>
 __global__ void __launch_bounds__(kThreads) route_tile_kernel(RouteArgs a) {
+    pdl_wait();
+    pdl_trigger();
     using Gm = Geo<EMAX>;
     extern __shared__ float4 smem_f4[];
     float* smem = reinterpret_cast<float*>(smem_f4);
@@ -543,16 +551,13 @@ cudaError_t launch_tile(const RouteArgs& a, cudaStream_t s) {
     const size_t smem = (size_t)Gm::SMEM_FLOATS * sizeof(float);
     cudaError_t err = ensure_smem<route_tile_kernel<TX, EMAX>>((int)smem);
     if (err != cudaSuccess) return err;
-    route_tile_kernel<TX, EMAX><<<a.nblk, kThreads, smem, s>>>(a);
-    count_launches(1);
-    return cudaGetLastError();
+    return launch_kernel(route_tile_kernel<TX, EMAX>, dim3(a.nblk), dim3(kThreads), smem, s, 1, false, a);
 }
 
 template <typename TX, int EMAX, int TW, int DS>
 cudaError_t launch_warp(const RouteArgs& a, cudaStream_t s) {
-    route_warp_kernel<TX, EMAX, TW, DS><<<a.nblk, kThreads, 0, s>>>(a);
-    count_launches(1);
-    return cudaGetLastError();
+    return launch_kernel(route_warp_kernel<TX, EMAX, TW, DS>, dim3(a.nblk), dim3(kThreads), 0, s,
+                         1, false, a);
 }
 
 template <typename TX, int EMAX>
@@ -567,9 +572,7 @@ cudaError_t launch_warp_tw(const RouteArgs& a, const RouteGeom& g, cudaStream_t 
 
 template <int NT, int MT>
 cudaError_t launch_mma_t(const RouteArgs& a, cudaStream_t s) {
-    route_mma_kernel<NT, MT><<<a.nblk, kThreads, 0, s>>>(a);
-    count_launches(1);
-    return cudaGetLastError();
+    return launch_kernel(route_mma_kernel<NT, MT>, dim3(a.nblk), dim3(kThreads), 0, s, 1, false, a);
 }
 
 template <int NT>
@@ -585,9 +588,8 @@ cudaError_t launch_split(const RouteArgs& a, int epad, __nv_bfloat16* wsp, cudaS
     const size_t n = (size_t)epad * a.d;
     int blocks = (int)((n + 255) / 256);
     blocks = blocks < num_sms() * 4 ? blocks : num_sms() * 4;
-    split_router_weight<<<blocks, 256, 0, s>>>(a.W_r, a.E, epad, a.d, wsp);
-    count_launches(1);
-    return cudaGetLastError();
+    return launch_kernel(split_router_weight, dim3(blocks), dim3(256), 0, s, 1, false, a.W_r, a.E, epad,
+                         a.d, wsp);
 }
 
 cudaError_t launch_mma(const RouteArgs& a, const RouteGeom& g, cudaStream_t s) {
@@ -608,6 +610,8 @@ cudaError_t launch_e(const RouteArgs& a, const RouteGeom& g, cudaStream_t s) {
 }
 
 __global__ void __launch_bounds__(256) route_finish_kernel(LossArgs l) {
+    pdl_wait();
+    pdl_trigger();
     __shared__ float s_part[256];
     __shared__ float s_d[kMaxExperts];
     loss_and_counts(l, s_part, s_d);
@@ -681,6 +685,7 @@ cudaError_t launch_route(const moe_config& c, const void* x, const float* W_r,
     // per-call counters: the two count arrays start at zero
     cudaError_t err = cudaMemsetAsync(at<char>(ws, L.counts), 0, L.blk_p - L.counts, s);
     if (err != cudaSuccess) return err;
+    chain_begin();  // the next kernel follows the memset
     if (L.route.mma) {
         err = launch_mma(a, L.route, s);
     } else if (L.route.tc) {
@@ -692,9 +697,8 @@ cudaError_t launch_route(const moe_config& c, const void* x, const float* W_r,
                                   : launch_e<float>(a, L.route, s);
     }
     if (err != cudaSuccess || fuse_count) return err;
-    route_finish_kernel<<<1, 256, 0, s>>>(route_loss_args(c, ws, L, expert_counts, aux_out));
-    count_launches(1);
-    return cudaGetLastError();
+    return launch_kernel(route_finish_kernel, dim3(1), dim3(256), 0, s, 1, false,
+                         route_loss_args(c, ws, L, expert_counts, aux_out));
 }
 
 }  // namespace moe

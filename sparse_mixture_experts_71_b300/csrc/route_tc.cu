@@ -116,6 +116,8 @@ route_tc_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constant__
     tc::fence_before_sync();
     __syncthreads();
     tc::fence_after_sync();
+    pdl_wait();
+    pdl_trigger();
     const uint32_t tmem_base = s_tmem;
     volatile int* abort_flag = &s_abort;
 
@@ -246,9 +248,7 @@ cudaError_t launch_np(const RouteArgs& a, const __nv_bfloat16* wsplit, cudaStrea
     constexpr auto kern = route_tc_kernel<NP>;
     cudaError_t err = ensure_smem<kern>(C::SMEM);
     if (err != cudaSuccess) return err;
-    kern<<<a.nblk, kThreads, C::SMEM, s>>>(mx, mw, a);
-    count_launches(1);
-    return cudaGetLastError();
+    return launch_kernel(kern, dim3(a.nblk), dim3(kThreads), C::SMEM, s, 1, true, mx, mw, a);
 }
 
 }  // namespace

@@ -113,3 +113,28 @@ def test_out_of_range_expert_is_flagged_not_written():
     assert (st, code, info) == (6, 1, 7 * 2 + 1)
     assert int(slot[7, 1]) == -1 and int(off[-1]) == 79
     assert B.get_device_error(run.ws)[0] == 0  # the record was cleared
+
+
+def test_segment_sizes_around_tile_boundaries():
+    """Expert segments of chosen sizes around the grouped GEMMs' token-tile
+    sizes (32, 128, 256 rows) in one batch, routed from caller-given logits
+    with the experts interleaved in token order: every kind of tile (full,
+    partial, nearly empty, empty expert) meets in one launch of the wide
+    (CTA-pair) GEMMs."""
+    sizes = [0, 1, 127, 128, 129, 255, 256, 257, 300, 640, 31, 32, 33, 95, 96, 97]
+    T, E = sum(sizes), len(sizes)
+    wl = _wl("tile-sizes", T, 128, 384, E, 1, "bf16", None, False)
+    assert T * wl.k >= 96 * E  # the CTA-pair GEMM path
+    inp = I.make_inputs(wl, seed=4)
+    expert = np.repeat(np.arange(E), sizes)
+    np.random.default_rng(1).shuffle(expert)
+    logits = np.random.default_rng(2).standard_normal((T, E)).astype(np.float32)
+    logits[np.arange(T), expert] = 8.0  # the chosen expert is the top-1
+    run = GpuRun(wl, inp)
+    r = run.staged(logits_in=torch.from_numpy(logits).cuda())
+    ref = oracle_on(inp, wl, logits=logits)
+    assert np.array_equal(to_np(r["counts"]), np.array(sizes))
+    assert np.array_equal(to_np(r["offsets"]), ref.offsets)
+    assert np.array_equal(to_np(r["perm_token"])[:T], ref.perm_token)
+    assert_y_close(to_np(r["y"]), ref.y, wl.dtype)
+    assert B.get_device_error(run.ws)[0] == 0
