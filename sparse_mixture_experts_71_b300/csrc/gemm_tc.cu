@@ -52,7 +52,6 @@ constexpr int A_BYTES = BM * BK * 2;         // 16 KB
 constexpr int BOX_ROWS = 32;                 // token rows per TMA box
 constexpr int BOX_BYTES = BOX_ROWS * BK * 2; // 4 KB
 constexpr uint64_t kDrainNs = 2000000000ull; // drain waits on the error path
-constexpr int kWideCluster = 4;              // CTAs sharing a token tile (wide tiles)
 
 template <int BN_MAX, int STAGES, bool GEMM1>
 struct Cfg {
@@ -143,10 +142,16 @@ __device__ __forceinline__ void drain_bar(uint64_t* bar, uint32_t parity) {
 // nparts) of the COLS-wide tile (columns acc_col + c, c < n), applies bias + GELU (first
 // GEMM, bf16 out) or bias x routing weight (second GEMM, fp32 out), and
 // writes token rows r0 + c through a shared-memory transpose (stg: 32 x 32).
+// With tm_out a full 32-row chunk leaves shared memory by a TMA tensor store
+// issued by lane 0 (box 32 weight rows x 32 token rows of the output), so
+// the warp neither reads the staging back nor issues the global stores; a
+// partial chunk (the end of an expert's segment: the rows after it belong to
+// the next segment) is stored by the lanes as before.
 template <int COLS, bool GEMM1>
 __device__ __forceinline__ void epilogue_tile(const Params& p, int e, int r0, int n, int fbase,
                                               uint32_t tmem_base, int acc_col, int q, int part,
-                                              int nparts, int lane, uint8_t* stg) {
+                                              int nparts, int lane, uint8_t* stg,
+                                              const CUtensorMap* tm_out = nullptr) {
     const int f0 = fbase + q * 32;  // first weight row (output feature) of this warp
     const int f = f0 + lane;
     const float bias =
@@ -160,12 +165,30 @@ __device__ __forceinline__ void epilogue_tile(const Params& p, int e, int r0, in
         const int rows_here = min(32, n - c);
         if (GEMM1) {
             __nv_bfloat16* s16 = reinterpret_cast<__nv_bfloat16*>(stg);
+            __nv_bfloat162 hv[16];
 #pragma unroll
             for (int j = 0; j < 32; j += 2) {
                 const float2 g = gelu2_as7126(
                     __fadd2_rn(make_float2(v[j], v[j + 1]), make_float2(bias, bias)));
-                s16[j * 32 + lane] = __float2bfloat16_rn(g.x);
-                s16[(j + 1) * 32 + lane] = __float2bfloat16_rn(g.y);
+                hv[j / 2] = __floats2bfloat162_rn(g.x, g.y);
+            }
+            if (tm_out != nullptr) {  // the previous chunk's store has read the staging rows
+                if (lane == 0) tc::bulk_wait_read_all();
+                __syncwarp();
+            }
+#pragma unroll
+            for (int j = 0; j < 32; j += 2) {
+                s16[j * 32 + lane] = hv[j / 2].x;
+                s16[(j + 1) * 32 + lane] = hv[j / 2].y;
+            }
+            if (tm_out != nullptr && rows_here == 32 && f0 < p.n_out) {
+                tc::fence_proxy_async_smem();
+                __syncwarp();
+                if (lane == 0) {
+                    tc::tma_store_2d(tm_out, stg, f0, r0 + c);
+                    tc::bulk_commit();
+                }
+                continue;
             }
             __syncwarp();
             __nv_bfloat16* out = reinterpret_cast<__nv_bfloat16*>(p.out);
@@ -181,10 +204,24 @@ __device__ __forceinline__ void epilogue_tile(const Params& p, int e, int r0, in
         } else {
             float wl = 1.f;
             if (p.row_w != nullptr && lane < rows_here) wl = __ldg(p.row_w + r0 + c + lane);
+#pragma unroll
+            for (int j = 0; j < 32; ++j) v[j] = (v[j] + bias) * __shfl_sync(0xffffffffu, wl, j);
+            if (tm_out != nullptr) {  // the previous chunk's store has read the staging rows
+                if (lane == 0) tc::bulk_wait_read_all();
+                __syncwarp();
+            }
             float* s32 = reinterpret_cast<float*>(stg);
 #pragma unroll
-            for (int j = 0; j < 32; ++j)
-                s32[j * 32 + lane] = (v[j] + bias) * __shfl_sync(0xffffffffu, wl, j);
+            for (int j = 0; j < 32; ++j) s32[j * 32 + lane] = v[j];
+            if (tm_out != nullptr && rows_here == 32 && f0 < p.n_out) {
+                tc::fence_proxy_async_smem();
+                __syncwarp();
+                if (lane == 0) {
+                    tc::tma_store_2d(tm_out, stg, f0, r0 + c);
+                    tc::bulk_commit();
+                }
+                continue;
+            }
             __syncwarp();
             float* out = reinterpret_cast<float*>(p.out);
 #pragma unroll
@@ -440,7 +477,7 @@ __device__ __forceinline__ Tile decode_pair_tile(int t, const int* s_tiles, cons
 template <int STAGES, bool GEMM1, int EW, int ATOMS>
 __global__ void __launch_bounds__(Cfg2<STAGES, GEMM1, EW, ATOMS>::THREADS, 1)
 grouped_gemm_pair(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
-                  const Params p) {
+                  const __grid_constant__ CUtensorMap tmO, const Params p) {
     using C = Cfg2<STAGES, GEMM1, EW, ATOMS>;
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>(
@@ -597,7 +634,7 @@ grouped_gemm_pair(const __grid_constant__ CUtensorMap tmA, const __grid_constant
             if (!__all_sync(0xffffffffu, ok)) break;
             tc::fence_after_sync();
             epilogue_tile<BN2, GEMM1>(p, tl.e, tl.r0, tl.n, m0 + rank * BM, tmem_base, acc * BN2,
-                                      q, part, EW / 4, lane, stg);
+                                      q, part, EW / 4, lane, stg, &tmO);
             tc::fence_before_sync();
             __syncwarp();
             if (lane == 0) tc::mbar_arrive_cluster_relaxed(tc::cluster_addr(&tempty[acc], 0));
@@ -606,6 +643,7 @@ grouped_gemm_pair(const __grid_constant__ CUtensorMap tmA, const __grid_constant
         }
     }
 
+    if (warp >= 4 && lane == 0) tc::bulk_wait_all();  // the output is written before exit
     if (warp == 1 && lane == 0) drain_bar(drain, 0);
     tc::fence_before_sync();
     tc::cluster_sync();  // no cross-CTA arrive or MMA write is still pending
@@ -641,6 +679,21 @@ bool make_map(CUtensorMap* m, const void* base, uint64_t inner, uint64_t outer,
     return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides, box,
               estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
               CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+// Row-major bf16 or fp32 matrix [outer][inner] as the destination of 32 x 32
+// tensor stores (no swizzle: the staging rows are plain 64- or 128-byte rows).
+bool make_store_map(CUtensorMap* m, void* base, uint64_t inner, uint64_t outer, bool f32) {
+    auto fn = encode_fn();
+    if (fn == nullptr) return false;
+    cuuint64_t dims[2] = {inner, outer};
+    cuuint64_t strides[1] = {inner * (f32 ? 4 : 2)};
+    cuuint32_t box[2] = {32, 32};
+    cuuint32_t estr[2] = {1, 1};
+    return fn(m, f32 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, base,
+              dims, strides, box, estr,
+              CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
+              CU_TENSOR_MAP_L2_PROMOTION_NONE, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
 // Clusters of CS CTAs that can be resident at once (one CTA per SM).
@@ -683,14 +736,14 @@ cudaError_t launch_one(const CUtensorMap& a, const CUtensorMap& b, const Params&
 }
 
 template <int STAGES, bool GEMM1, int EW, int ATOMS>
-cudaError_t launch_one_pair(const CUtensorMap& a, const CUtensorMap& b, const Params& p,
-                            cudaStream_t s) {
+cudaError_t launch_one_pair(const CUtensorMap& a, const CUtensorMap& b, const CUtensorMap& o,
+                            const Params& p, cudaStream_t s) {
     using C = Cfg2<STAGES, GEMM1, EW, ATOMS>;
     constexpr auto kern = grouped_gemm_pair<STAGES, GEMM1, EW, ATOMS>;
     cudaError_t err = ensure_smem<kern>(C::SMEM);
     if (err != cudaSuccess) return err;
     return launch_kernel(kern, dim3(2 * resident_clusters<kern>(2, C::SMEM, C::THREADS)),
-                         dim3(C::THREADS), C::SMEM, s, 2, true, a, b, p);
+                         dim3(C::THREADS), C::SMEM, s, 2, true, a, b, o, p);
 }
 
 template <int BN_MAX, int STAGES, int CS>
@@ -725,15 +778,18 @@ cudaError_t launch_expert_ffn_tc(const moe_config& c, const void* x_perm, int64_
     Params p2{offsets, reinterpret_cast<const __nv_bfloat16*>(b2), perm_w, y_perm, hdr,
               g_tc_timeout_ns, c.E, c.d, c.d_ff, (int)h_rows};
     if (wide) {
-        CUtensorMap pm[4];  // 128-row token boxes for the pair kernel
+        // 128-row token boxes for the pair kernel; h and y_perm as store targets
+        CUtensorMap pm[6];
         pm[0] = maps[0];
         pm[2] = maps[2];
         if (!make_map(&pm[1], x_perm, c.d, (uint64_t)x_rows, BN2 / 2) ||
-            !make_map(&pm[3], h, c.d_ff, (uint64_t)h_rows, BN2 / 2))
+            !make_map(&pm[3], h, c.d_ff, (uint64_t)h_rows, BN2 / 2) ||
+            !make_store_map(&pm[4], h, c.d_ff, (uint64_t)h_rows, false) ||
+            !make_store_map(&pm[5], y_perm, c.d, (uint64_t)h_rows, true))
             return cudaErrorInvalidValue;
-        cudaError_t err = launch_one_pair<3, true, 16, 2>(pm[0], pm[1], p1, s);
+        cudaError_t err = launch_one_pair<3, true, 16, 2>(pm[0], pm[1], pm[4], p1, s);
         if (err != cudaSuccess) return err;
-        return launch_one_pair<3, false, 8, 2>(pm[2], pm[3], p2, s);
+        return launch_one_pair<3, false, 8, 2>(pm[2], pm[3], pm[5], p2, s);
     }
     return launch_pair<64, 8, 1>(maps, p1, p2, s);
 }
