@@ -81,6 +81,14 @@ struct Params {
     int E, n_out, K, rows_cap;
 };
 
+// Rows of an expert's segment (offsets clamped to the buffers).
+__device__ __forceinline__ int seg_rows(const Params& p, int e) {
+    const int s0 = min(max(__ldg(p.offsets + e), 0), p.rows_cap);
+    const int s1 = min(max(__ldg(p.offsets + e + 1), s0), p.rows_cap);
+    return s1 - s0;
+}
+
+
 struct Tile {
     int e, r0, n, m0;
 };
@@ -142,11 +150,12 @@ __device__ __forceinline__ void drain_bar(uint64_t* bar, uint32_t parity) {
 // nparts) of the COLS-wide tile (columns acc_col + c, c < n), applies bias + GELU (first
 // GEMM, bf16 out) or bias x routing weight (second GEMM, fp32 out), and
 // writes token rows r0 + c through a shared-memory transpose (stg: 32 x 32).
-// With tm_out a full 32-row chunk leaves shared memory by a TMA tensor store
-// issued by lane 0 (box 32 weight rows x 32 token rows of the output), so
-// the warp neither reads the staging back nor issues the global stores; a
-// partial chunk (the end of an expert's segment: the rows after it belong to
-// the next segment) is stored by the lanes as before.
+// With tm_out (second GEMM of the pair kernel) a full 32-row chunk leaves
+// shared memory by a TMA tensor store issued by lane 0 (box 32 weight rows x
+// 32 token rows of the output), so the warp neither reads the staging back
+// nor issues the global stores; a partial chunk (the end of an expert's
+// segment: the rows after it belong to the next segment) is stored by the
+// lanes.
 template <int COLS, bool GEMM1>
 __device__ __forceinline__ void epilogue_tile(const Params& p, int e, int r0, int n, int fbase,
                                               uint32_t tmem_base, int acc_col, int q, int part,
@@ -165,30 +174,12 @@ __device__ __forceinline__ void epilogue_tile(const Params& p, int e, int r0, in
         const int rows_here = min(32, n - c);
         if (GEMM1) {
             __nv_bfloat16* s16 = reinterpret_cast<__nv_bfloat16*>(stg);
-            __nv_bfloat162 hv[16];
 #pragma unroll
             for (int j = 0; j < 32; j += 2) {
                 const float2 g = gelu2_as7126(
                     __fadd2_rn(make_float2(v[j], v[j + 1]), make_float2(bias, bias)));
-                hv[j / 2] = __floats2bfloat162_rn(g.x, g.y);
-            }
-            if (tm_out != nullptr) {  // the previous chunk's store has read the staging rows
-                if (lane == 0) tc::bulk_wait_read_all();
-                __syncwarp();
-            }
-#pragma unroll
-            for (int j = 0; j < 32; j += 2) {
-                s16[j * 32 + lane] = hv[j / 2].x;
-                s16[(j + 1) * 32 + lane] = hv[j / 2].y;
-            }
-            if (tm_out != nullptr && rows_here == 32 && f0 < p.n_out) {
-                tc::fence_proxy_async_smem();
-                __syncwarp();
-                if (lane == 0) {
-                    tc::tma_store_2d(tm_out, stg, f0, r0 + c);
-                    tc::bulk_commit();
-                }
-                continue;
+                s16[j * 32 + lane] = __float2bfloat16_rn(g.x);
+                s16[(j + 1) * 32 + lane] = __float2bfloat16_rn(g.y);
             }
             __syncwarp();
             __nv_bfloat16* out = reinterpret_cast<__nv_bfloat16*>(p.out);
@@ -262,7 +253,6 @@ grouped_gemm_tc(const __grid_constant__ CUtensorMap tmA, const __grid_constant__
     const int mt = (p.n_out + BM - 1) / BM;
     const int groups = (mt + CS - 1) / CS;  // weight-tile groups per token tile
     const int KB = (p.K + BK - 1) / BK;
-
     if (warp == 0 && lane == 0) {
         for (int s = 0; s < STAGES; ++s) {
             tc::mbar_init(&full[s], 1);
@@ -290,9 +280,7 @@ grouped_gemm_tc(const __grid_constant__ CUtensorMap tmA, const __grid_constant__
             const int e = e0 + lane;
             int nt = 0;
             if (e < p.E) {
-                const int s0 = min(max(__ldg(p.offsets + e), 0), p.rows_cap);
-                const int s1 = min(max(__ldg(p.offsets + e + 1), s0), p.rows_cap);
-                nt = ((s1 - s0 + BN_MAX - 1) / BN_MAX) * groups;
+                nt = ((seg_rows(p, e) + BN_MAX - 1) / BN_MAX) * groups;
             }
             int v = nt;
 #pragma unroll
@@ -418,6 +406,85 @@ grouped_gemm_tc(const __grid_constant__ CUtensorMap tmA, const __grid_constant__
     if (CS > 1) tc::cluster_sync();
 }
 
+// First-GEMM epilogue of the CTA-pair kernel for this CTA's 128 weight rows x
+// n tokens of one accumulator.  Work items are 16 TMEM lanes (weight rows) x
+// 32 columns (tokens); the NPQ warps of lane quarter q take the quarter's
+// items round robin.  Per item a warp loads the accumulator in the fragment
+// layout (tcgen05.ld 16x256b), adds the bias, applies GELU two values per
+// instruction, packs token pairs to bf16x2 and writes the transpose to its
+// staging rows with stmatrix (32 token rows of 16 weight rows = 32 bytes; the
+// two 16-byte halves of a row swap when bit 2 of the token is set, which is
+// the 32-byte TMA swizzle and keeps each stored 8 x 8 matrix on distinct
+// banks).  A full item then leaves by one TMA tensor store (box 16 x 32) from
+// lane 0; a partial one (the end of an expert's segment) by lane stores.
+// Compared with 32 scalar shared stores and a read-back per 32 x 32 chunk this
+// halves the epilogue's shared-memory traffic, which competes with the MMA
+// operand reads and the TMA fills.
+template <int NPQ>
+__device__ __forceinline__ void epilogue_gelu(const Params& p, int e, int r0, int n, int fbase,
+                                              uint32_t tmem_base, int acc_col, int q, int wq,
+                                              int lane, uint8_t* stg, const CUtensorMap* tm_out) {
+    const int g = lane >> 2;
+    const int items = 2 * ((n + 31) / 32);
+    const __nv_bfloat16* bias = p.bias + (size_t)e * p.n_out;
+    __nv_bfloat16* out = reinterpret_cast<__nv_bfloat16*>(p.out);
+    const uint32_t stg_s = tc::smem_u32(stg);
+    // this lane's stmatrix row address (matrix lane/8, row lane%8) for the two stores
+    const int mi = lane >> 3, rr = lane & 7;
+    uint32_t st_addr[2];
+#pragma unroll
+    for (int k = 0; k < 2; ++k) {
+        const int b = 2 * k + (mi >> 1), sh = mi & 1, tok = 8 * b + rr;
+        st_addr[k] = stg_s + tok * 32 + ((sh ^ ((tok >> 2) & 1)) << 4);
+    }
+    for (int it = wq; it < items; it += NPQ) {
+        const int h = it & 1, c = (it >> 1) * 32;
+        const int fr = fbase + q * 32 + h * 16;  // first weight row of the item
+        const float ba = fr + g < p.n_out ? __bfloat162float(bias[fr + g]) : 0.f;
+        const float bb = fr + 8 + g < p.n_out ? __bfloat162float(bias[fr + 8 + g]) : 0.f;
+        uint32_t r[16];
+        tc::tmem_ld_16x32(tmem_base + ((uint32_t)(q * 32 + h * 16) << 16) + (uint32_t)(acc_col + c), r);
+        uint32_t pk[8];  // pk[2b]: rows g, pk[2b+1]: rows g + 8; tokens 8b + 2(lane%4), +1
+#pragma unroll
+        for (int b = 0; b < 4; ++b) {
+            const float2 ga = gelu2_as7126(__fadd2_rn(
+                make_float2(__uint_as_float(r[4 * b]), __uint_as_float(r[4 * b + 1])), make_float2(ba, ba)));
+            const float2 gb = gelu2_as7126(__fadd2_rn(
+                make_float2(__uint_as_float(r[4 * b + 2]), __uint_as_float(r[4 * b + 3])), make_float2(bb, bb)));
+            const __nv_bfloat162 pa = __floats2bfloat162_rn(ga.x, ga.y);
+            const __nv_bfloat162 pb = __floats2bfloat162_rn(gb.x, gb.y);
+            pk[2 * b] = *reinterpret_cast<const uint32_t*>(&pa);
+            pk[2 * b + 1] = *reinterpret_cast<const uint32_t*>(&pb);
+        }
+        if (lane == 0) tc::bulk_wait_read_all();  // the previous store has read the rows
+        __syncwarp();
+        tc::stmatrix_x4_trans(st_addr[0], pk[0], pk[1], pk[2], pk[3]);
+        tc::stmatrix_x4_trans(st_addr[1], pk[4], pk[5], pk[6], pk[7]);
+        const int rows_here = min(32, n - c);
+        if (rows_here == 32 && fr < p.n_out) {
+            tc::fence_proxy_async_smem();
+            __syncwarp();
+            if (lane == 0) {
+                tc::tma_store_2d(tm_out, stg, fr, r0 + c);
+                tc::bulk_commit();
+            }
+            continue;
+        }
+        __syncwarp();
+#pragma unroll
+        for (int j = 0; j < 2; ++j) {
+            const int ci = lane + 32 * j, tok = ci >> 1, sh = ci & 1;
+            const int fc = fr + 8 * sh;
+            if (c + tok < n && fc < p.n_out) {
+                const uint4 val = *reinterpret_cast<const uint4*>(
+                    stg + tok * 32 + ((sh ^ ((tok >> 2) & 1)) << 4));
+                *reinterpret_cast<uint4*>(out + (size_t)(r0 + c + tok) * p.n_out + fc) = val;
+            }
+        }
+        __syncwarp();
+    }
+}
+
 // ===================================================================== CTA-pair kernel
 // cta_group::2: a cluster of two CTAs (two SMs) computes a 256 x 256 tile
 // D[f][j] (256 weight rows x up to 256 token rows) with one tcgen05.mma of
@@ -497,7 +564,6 @@ grouped_gemm_pair(const __grid_constant__ CUtensorMap tmA, const __grid_constant
     const int pair = blockIdx.x / 2, npairs = gridDim.x / 2;
     const int mt2 = (p.n_out + 2 * BM - 1) / (2 * BM);  // 256-row weight tiles
     const int KB = (p.K + ATOMS * BK - 1) / (ATOMS * BK);  // stages per tile
-
     if (warp == 0 && lane == 0) {
         for (int s = 0; s < STAGES; ++s) {
             tc::mbar_init(&full[s], 1);
@@ -525,9 +591,7 @@ grouped_gemm_pair(const __grid_constant__ CUtensorMap tmA, const __grid_constant
             const int e = e0 + lane;
             int nt = 0;
             if (e < p.E) {
-                const int s0 = min(max(__ldg(p.offsets + e), 0), p.rows_cap);
-                const int s1 = min(max(__ldg(p.offsets + e + 1), s0), p.rows_cap);
-                nt = ((s1 - s0 + BN2 - 1) / BN2) * mt2;
+                nt = ((seg_rows(p, e) + BN2 - 1) / BN2) * mt2;
             }
             int v = nt;
 #pragma unroll
@@ -633,7 +697,11 @@ grouped_gemm_pair(const __grid_constant__ CUtensorMap tmA, const __grid_constant
             const bool ok = wait_bar(&tfull[acc], acc_phase, s_abort, p, 4);
             if (!__all_sync(0xffffffffu, ok)) break;
             tc::fence_after_sync();
-            epilogue_tile<BN2, GEMM1>(p, tl.e, tl.r0, tl.n, m0 + rank * BM, tmem_base, acc * BN2,
+            if (GEMM1)
+                epilogue_gelu<EW / 4>(p, tl.e, tl.r0, tl.n, m0 + rank * BM, tmem_base, acc * BN2,
+                                      q, part, lane, stg, &tmO);
+            else
+                epilogue_tile<BN2, GEMM1>(p, tl.e, tl.r0, tl.n, m0 + rank * BM, tmem_base, acc * BN2,
                                       q, part, EW / 4, lane, stg, &tmO);
             tc::fence_before_sync();
             __syncwarp();
@@ -681,17 +749,30 @@ bool make_map(CUtensorMap* m, const void* base, uint64_t inner, uint64_t outer,
               CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-// Row-major bf16 or fp32 matrix [outer][inner] as the destination of 32 x 32
-// tensor stores (no swizzle: the staging rows are plain 64- or 128-byte rows).
-bool make_store_map(CUtensorMap* m, void* base, uint64_t inner, uint64_t outer, bool f32) {
+// Row-major bf16 matrix [outer][inner] as the destination of 16 x 32 tensor
+// stores from staging rows in the 32-byte swizzle.
+bool make_store_map_sw32(CUtensorMap* m, void* base, uint64_t inner, uint64_t outer) {
     auto fn = encode_fn();
     if (fn == nullptr) return false;
     cuuint64_t dims[2] = {inner, outer};
-    cuuint64_t strides[1] = {inner * (f32 ? 4 : 2)};
+    cuuint64_t strides[1] = {inner * 2};
+    cuuint32_t box[2] = {16, 32};
+    cuuint32_t estr[2] = {1, 1};
+    return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, base, dims, strides, box, estr,
+              CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_32B,
+              CU_TENSOR_MAP_L2_PROMOTION_NONE, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+// Row-major fp32 matrix [outer][inner] as the destination of 32 x 32 tensor
+// stores (no swizzle: the staging rows are plain 128-byte rows).
+bool make_store_map_f32(CUtensorMap* m, void* base, uint64_t inner, uint64_t outer) {
+    auto fn = encode_fn();
+    if (fn == nullptr) return false;
+    cuuint64_t dims[2] = {inner, outer};
+    cuuint64_t strides[1] = {inner * 4};
     cuuint32_t box[2] = {32, 32};
     cuuint32_t estr[2] = {1, 1};
-    return fn(m, f32 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, base,
-              dims, strides, box, estr,
+    return fn(m, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2, base, dims, strides, box, estr,
               CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
               CU_TENSOR_MAP_L2_PROMOTION_NONE, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
@@ -784,8 +865,8 @@ cudaError_t launch_expert_ffn_tc(const moe_config& c, const void* x_perm, int64_
         pm[2] = maps[2];
         if (!make_map(&pm[1], x_perm, c.d, (uint64_t)x_rows, BN2 / 2) ||
             !make_map(&pm[3], h, c.d_ff, (uint64_t)h_rows, BN2 / 2) ||
-            !make_store_map(&pm[4], h, c.d_ff, (uint64_t)h_rows, false) ||
-            !make_store_map(&pm[5], y_perm, c.d, (uint64_t)h_rows, true))
+            !make_store_map_sw32(&pm[4], h, c.d_ff, (uint64_t)h_rows) ||
+            !make_store_map_f32(&pm[5], y_perm, c.d, (uint64_t)h_rows))
             return cudaErrorInvalidValue;
         cudaError_t err = launch_one_pair<3, true, 16, 2>(pm[0], pm[1], pm[4], p1, s);
         if (err != cudaSuccess) return err;

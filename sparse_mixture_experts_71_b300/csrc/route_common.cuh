@@ -107,34 +107,33 @@ __device__ __forceinline__ void token_epilogue(const RouteArgs& a, float* prow, 
         g[e] = e < a.E ? prow[e] : -FLT_MAX;
         m = fmaxf(m, g[e]);
     }
-    float ex[EMAX];
+    // exp(g - m) is evaluated where it is needed rather than kept (one more
+    // register array would not fit at two tcgen05-router CTAs per SM); expf
+    // gives the same value for the same argument each time
     float ssum = 0.f;
 #pragma unroll
-    for (int e = 0; e < EMAX; ++e) {
-        ex[e] = e < a.E ? expf(g[e] - m) : 0.f;
-        ssum += ex[e];
-    }
+    for (int e = 0; e < EMAX; ++e) ssum += e < a.E ? expf(g[e] - m) : 0.f;
     const float inv = 1.0f / ssum;
     if (a.logits_out != nullptr)
         for (int e = 0; e < a.E; ++e) a.logits_out[(size_t)t * a.E + e] = prow[e];
 #pragma unroll
-    for (int e = 0; e < EMAX; ++e) prow[e] = ex[e] * inv;  // p replaces g
+    for (int e = 0; e < EMAX; ++e) prow[e] = (e < a.E ? expf(g[e] - m) : 0.f) * inv;  // p replaces g
     // top-k on the logits, larger first, ties to the lower expert index
     uint64_t taken = 0;
     int sel_e[kMaxTopK];
     float sel_x[kMaxTopK];
     float sel_sum = 0.f;
     for (int j = 0; j < a.k; ++j) {
-        float bv = -FLT_MAX, bx = 0.f;
+        float bv = -FLT_MAX, bx;
         int be = -1;
 #pragma unroll
         for (int e = 0; e < EMAX; ++e) {
             if (e < a.E && !((taken >> e) & 1ull) && (be < 0 || g[e] > bv)) {
                 bv = g[e];
-                bx = ex[e];
                 be = e;
             }
         }
+        bx = expf(bv - m);
         taken |= 1ull << be;
         sel_e[j] = be;
         sel_x[j] = bx;

@@ -11,7 +11,7 @@
 // TMEM accumulator of NP columns (NP = E rounded up), so every product is
 // exact and only the fp32 accumulation rounds.  Warp 0 streams 64-column
 // slices of x (128 x 64) and of the three parts (NP x 64 each) into a
-// 4-deep ring; warp 1 issues the MMAs; warps 4-7 read the accumulator back
+// 2-deep ring; warp 1 issues the MMAs; warps 4-7 read the accumulator back
 // (TMEM lane = token) into shared memory.  Then one thread per token does the
 // softmax and top-k, and the block finishes like the other router kernels.
 
@@ -32,7 +32,11 @@ using namespace rt;
 constexpr int TM = 128;                  // tokens per CTA
 constexpr int RBK = 64;                  // K per stage
 constexpr int RA_BYTES = TM * RBK * 2;   // 16 KB
-constexpr int RSTAGES = 4;
+// Two stages, and the logits tile reuses the ring once the MMAs are done, so
+// two CTAs fit on an SM: a batch of T / 128 CTAs then runs in one wave on the
+// 148 SMs (T = 32768: 256 CTAs) instead of 1.7 waves of one CTA per SM, with
+// the same bytes in flight per SM.
+constexpr int RSTAGES = 2;
 constexpr uint64_t kRouteTimeoutNs = 2000000000ull;
 
 template <int NP>
@@ -40,13 +44,15 @@ struct RCfg {
     static constexpr int PART_BYTES = NP * RBK * 2;
     static constexpr int STAGE_BYTES = RA_BYTES + 3 * PART_BYTES;
     static constexpr int LDS = NP + 1;
-    static constexpr int OFF_P = RSTAGES * STAGE_BYTES;
-    static constexpr int OFF_BARS = OFF_P + ((TM * LDS * 4 + 7) / 8) * 8;
+    static constexpr int OFF_P = 0;  // logits tile [TM][LDS] fp32, over the stage ring
+    static constexpr int RING = RSTAGES * STAGE_BYTES;
+    static constexpr int P_BYTES = ((TM * LDS * 4 + 1023) / 1024) * 1024;
+    static constexpr int OFF_BARS = RING > P_BYTES ? RING : P_BYTES;
     static constexpr int NUM_BARS = 2 * RSTAGES + 2;
     static constexpr int SMEM = OFF_BARS + NUM_BARS * 8 + 1023;
     static constexpr int TMEM_COLS = NP < 32 ? 32 : NP;
     static_assert(STAGE_BYTES % 1024 == 0, "stage alignment");
-    static_assert(SMEM <= 232448 - 16384, "shared memory budget");
+    static_assert(2 * (SMEM + 8192) <= 233472, "two CTAs per SM");
 };
 
 __device__ __forceinline__ bool wait_or_abort(uint64_t* bar, uint32_t parity, volatile int* abort_flag,
@@ -71,7 +77,7 @@ __device__ __forceinline__ void drain_wait(uint64_t* bar, uint32_t parity) {
 }
 
 template <int NP>
-__global__ void __launch_bounds__(kThreads, 1)
+__global__ void __launch_bounds__(kThreads, 2)
 route_tc_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constant__ CUtensorMap tmW,
                 RouteArgs a) {
     using C = RCfg<NP>;
@@ -175,6 +181,8 @@ route_tc_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constant__
             drain_wait(drain, 0);
         }
     } else if (warp >= 4) {  // ------------------------------------ accumulator -> smem
+        // s_p overlays the stage ring: written only after tfull, when every
+        // TMA fill has been consumed by the MMAs
         const int q = warp & 3;
         const int tok = q * 32 + lane;
         const bool ok = wait_or_abort(tfull, 0, abort_flag, a.hdr, 3);

@@ -305,5 +305,31 @@ __device__ __forceinline__ void tmem_ld_32cols(uint32_t taddr, float (&v)[32]) {
     for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(r[i]);
 }
 
+// 16 TMEM lanes x 32 fp32 columns (warp-collective), waiting for the load in
+// the same asm statement.  Thread t receives, for b = 0..3, r[4b], r[4b+1] =
+// lane base + t/4, columns 8b + 2(t%4), +1 and r[4b+2], r[4b+3] = lane
+// base + 8 + t/4, the same columns (the m16n8 accumulator-fragment layout).
+__device__ __forceinline__ void tmem_ld_16x32(uint32_t taddr, uint32_t (&r)[16]) {
+    asm volatile(
+        "tcgen05.ld.sync.aligned.16x256b.x4.b32 "
+        "{%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15}, [%16];\n\t"
+        "tcgen05.wait::ld.sync.aligned;"
+        : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
+          "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]),
+          "=r"(r[14]), "=r"(r[15])
+        : "r"(taddr)
+        : "memory");
+}
+// Four 8x8 b16 matrices stored transposed: register i of every thread holds
+// two consecutive elements of row t/4, columns 2(t%4), +1 of matrix i; row j
+// of the transposed matrix i (16 bytes) goes to the address given by thread
+// 8i + j.
+__device__ __forceinline__ void stmatrix_x4_trans(uint32_t addr, uint32_t m0, uint32_t m1,
+                                                  uint32_t m2, uint32_t m3) {
+    asm volatile("stmatrix.sync.aligned.m8n8.x4.trans.shared.b16 [%0], {%1, %2, %3, %4};" ::"r"(
+                     addr),
+                 "r"(m0), "r"(m1), "r"(m2), "r"(m3)
+                 : "memory");
+}
 }  // namespace tc
 }  // namespace moe

@@ -115,16 +115,27 @@ def test_out_of_range_expert_is_flagged_not_written():
     assert B.get_device_error(run.ws)[0] == 0  # the record was cleared
 
 
-def test_segment_sizes_around_tile_boundaries():
+SEGMENTS = {
+    # 16 experts: every expert on the CTA-pair GEMMs, all tile kinds in one launch
+    "pair-tiles": [0, 1, 127, 128, 129, 255, 256, 257, 300, 640, 31, 32, 33, 95, 96, 97],
+    # 20 experts: full, partial and nearly empty experts side by side
+    "e20-mixed": [640, 300, 256, 129, 128, 127, 100, 64, 63, 33, 32, 31, 17, 5, 1, 1, 0, 0,
+                  200, 400],
+    "e20-all-150": [150] * 20,  # one full and one partial token tile each
+    "e20-all-100": [100] * 20,  # every expert a single partial token tile
+}
+
+
+@pytest.mark.parametrize("name", list(SEGMENTS))
+def test_segment_sizes_around_tile_boundaries(name):
     """Expert segments of chosen sizes around the grouped GEMMs' token-tile
-    sizes (32, 128, 256 rows) in one batch, routed from caller-given logits
-    with the experts interleaved in token order: every kind of tile (full,
-    partial, nearly empty, empty expert) meets in one launch of the wide
-    (CTA-pair) GEMMs."""
-    sizes = [0, 1, 127, 128, 129, 255, 256, 257, 300, 640, 31, 32, 33, 95, 96, 97]
+    sizes (32, 64, 128, 256 rows) in one batch, routed from caller-given
+    logits with the experts interleaved in token order, on the wide-batch
+    GEMM path (T*k >= 96*E)."""
+    sizes = SEGMENTS[name]
     T, E = sum(sizes), len(sizes)
-    wl = _wl("tile-sizes", T, 128, 384, E, 1, "bf16", None, False)
-    assert T * wl.k >= 96 * E  # the CTA-pair GEMM path
+    wl = _wl(name, T, 128, 384, E, 1, "bf16", None, False)
+    assert T * wl.k >= 96 * E
     inp = I.make_inputs(wl, seed=4)
     expert = np.repeat(np.arange(E), sizes)
     np.random.default_rng(1).shuffle(expert)
