@@ -47,8 +47,9 @@ METRIC = "MoE-layer fwd tokens/s and achieved TFLOP/s (or HBM GB/s) vs B300 roof
 # an ncu capture of the current kernels; summaries with the commands are in
 # profiles/grouped_gemm_*.md.  Workloads without a capture report null.
 TRAFFIC_BYTES = {
-    "bf16-T4096-d1024-F4096-E8-top2": (84.049 + 31.686 + 139.628 + 11.349) * 1e6,
-    "decode-bf16-T64-d4096-F14336-E8-top2": (941.605 + 6.071 + 944.296 + 1.555) * 1e6,
+    "bf16-T4096-d1024-F4096-E8-top2": (84.050 + 31.683 + 139.586 + 12.432) * 1e6,
+    "decode-bf16-T64-d4096-F14336-E8-top2": (941.866 + 6.017 + 944.308 + 1.891) * 1e6,
+    "switch-bf16-T32768-d2048-F8192-E64-top1-cap640": (719.386 + 56.738 + 778.406 + 26.803) * 1e6,
 }
 
 

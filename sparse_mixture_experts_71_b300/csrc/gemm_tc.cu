@@ -11,23 +11,30 @@
 // token rows r0 .. r0+n-1,
 //     D[f][j] = sum_k W[e][f][k] * X[r0 + j][k]      (f: 128 weight rows)
 // so the 128-row MMA dimension is always full (weight rows) and the token
-// dimension N is set per tile at run time to n rounded up to 16 (the
-// instruction descriptor is a register operand).  Small expert segments
+// dimension N is set per tile at run time to n rounded up to 16 (single CTA)
+// or 32 (CTA pair; the instruction descriptor is a register operand).  Small expert segments
 // (decode, skewed routing) then cost MMA work in proportion to their size.
 //
-// Persistent, warp-specialised kernel (one CTA per SM, 12 warps):
-//   warp 0      TMA producer: per K-step one 128x64 box of W and ceil(n/32)
-//               32x64 boxes of X into a STAGES-deep shared-memory ring
-//               (128-byte swizzle), completion counted on a full barrier;
-//   warp 1      MMA issuer: 4 tcgen05.mma (K=16 each) per stage into one of
-//               two TMEM accumulators; tcgen05.commit frees the stage and,
-//               after the last K-step, signals the epilogue;
+// Two persistent, warp-specialised kernels share these roles:
+//   warp 0      TMA producer: weight and token boxes (64 K columns, 128-byte
+//               swizzle) into a shared-memory ring, completion counted on a
+//               full barrier;
+//   warp 1      MMA issuer: tcgen05.mma (K = 16 each) into one of two TMEM
+//               accumulators; tcgen05.commit frees a stage and, after the
+//               last K-step of a tile, signals the epilogue;
 //   warp 2      TMEM allocator;
 //   warp 3      computes the per-expert tile table from the device offsets;
-//   warps 4-11  epilogue: tcgen05.ld of 32 columns per warp (lane quarter
-//               warp%4, column half by warp group), bias + exact GELU
-//               (GEMM1, bf16 out) or bias x routing weight (GEMM2, fp32 out),
-//               transposed through shared memory into 16-byte row stores.
+//   warps 4..   epilogue: tcgen05.ld of the accumulator, bias + GELU (first
+//               GEMM, bf16 h) or bias x routing weight (second GEMM, fp32
+//               y_perm), transposed through shared memory into row-major
+//               output.
+//   grouped_gemm_pair (token tiles of up to 256 rows): a cluster of two CTAs
+//               computes 256 weight rows x 256 tokens with cta_group::2
+//               MMAs (M = 256); three stages of two K atoms; 16 (first GEMM)
+//               or 8 (second) epilogue warps; output by TMA tensor stores.
+//   grouped_gemm_tc (decode-sized batches, token tiles of up to 64 rows):
+//               one CTA per SM, M = 128, eight stages; 8 epilogue warps;
+//               output by 16-byte lane stores.
 // The two TMEM accumulators let the epilogue of tile i overlap the MMAs of
 // tile i+1.  Every wait is bounded: past the time limit the kernel records
 // an error in the workspace, drains its in-flight copies and MMAs, frees TMEM
