@@ -26,7 +26,10 @@ the combine and of the auxiliary loss did not survive extraction):
   (token, slot) ascending order; a dropped assignment contributes 0 (the
   residual add is outside the layer) and surviving weights are not
   renormalised again;
-* f_i of the auxiliary loss counts the top-1 choice only, before any drop.
+* f_i of the auxiliary loss counts the top-1 choice only, before any drop;
+* the router z-loss, which the pages name without a formula ("penalise large
+  router logits"), is the mean over tokens of the squared log-sum-exp of the
+  token's router logits (the logits that enter the softmax, bias included).
 
 Parity: the routing, capacity, auxiliary-loss and combine functions are pinned
 by the pages' worked examples, closed forms and brute force (tests).  The
@@ -165,6 +168,21 @@ def aux_loss(probs, idx, E: int) -> float:
     return float(E * np.sum(f * P))
 
 
+def router_z_loss(logits) -> float:
+    """Router z-loss: mean over tokens of (log sum_e exp g_{t,e})^2.
+
+    [LECTURE] "The central problem: load balancing" (router z-loss penalises
+    large router logits).  The log-sum-exp is taken stably around the row
+    maximum.  Returns 0 for an empty batch.
+    """
+    g = np.asarray(logits, f64)
+    if g.shape[0] == 0:
+        return 0.0
+    m = g.max(axis=1)
+    lse = m + np.log(np.exp(g - m[:, None]).sum(axis=1))
+    return float(np.mean(lse * lse))
+
+
 def dispatch_layout(idx, kept, E: int):
     """Expert-contiguous order of the kept assignments.
 
@@ -213,6 +231,7 @@ class OracleResult:
     aux: float
     y: np.ndarray           # (len(tokens), d) fp64
     tokens: np.ndarray      # rows of the layer output held in y
+    z_loss: float = 0.0     # router z-loss
 
 
 def moe_forward(x, W_r, W1, b1, W2, b2, k: int, renormalize: bool = True,
@@ -259,4 +278,4 @@ def moe_forward(x, W_r, W1, b1, W2, b2, k: int, renormalize: bool = True,
         y[rows] += we[:, None] * out
     aux = aux_loss(probs, idx, E)
     return OracleResult(logits, probs, idx, w, kept, counts, kept_count, offsets, slot_of,
-                        perm_token, aux, y, tokens)
+                        perm_token, aux, y, tokens, router_z_loss(logits))

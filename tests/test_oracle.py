@@ -131,6 +131,33 @@ def test_softmax_matches_torch():
     np.testing.assert_allclose(O.softmax(g), want, rtol=1e-13, atol=0)
 
 
+# ---------------------------------------------------------- router z-loss pins
+
+@pytest.mark.parametrize("E,c", [(1, 0.0), (8, 0.0), (8, -2.5), (64, 3.25)])
+def test_z_loss_equal_logits_closed_form(E, c):
+    """All logits equal to c: log-sum-exp = c + ln E for every token, so the
+    z-loss is (c + ln E)^2 ("penalise large router logits")."""
+    g = np.full((50, E), c, np.float32)
+    assert abs(O.router_z_loss(g) - (c + math.log(E)) ** 2) <= 1e-12 * max(1.0, (c + math.log(E)) ** 2)
+
+
+def test_z_loss_matches_library_logsumexp():
+    """Reduces to torch.logsumexp (fp64) squared and averaged over tokens."""
+    g = (rng.standard_normal((333, 16)) * 4.0).astype(np.float32)
+    lse = torch.logsumexp(torch.from_numpy(g).double(), dim=1)
+    want = float((lse * lse).mean())
+    assert abs(O.router_z_loss(g) - want) <= 1e-12 * want
+
+
+def test_z_loss_dominant_logit_and_empty_batch():
+    """One logit L far above the others: log-sum-exp -> L, z -> L^2; and an
+    empty batch contributes 0."""
+    g = np.zeros((10, 8), np.float32)
+    g[:, 3] = 60.0
+    assert abs(O.router_z_loss(g) - 3600.0) <= 1e-9
+    assert O.router_z_loss(np.zeros((0, 8), np.float32)) == 0.0
+
+
 # ---------------------------------------------------------- auxiliary loss pins
 
 @pytest.mark.parametrize("E,k", [(1, 1), (4, 2), (8, 2), (64, 1), (8, 8)])
