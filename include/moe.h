@@ -85,9 +85,9 @@ size_t moe_workspace_size(const moe_config* cfg);
 const char* moe_status_string(moe_status s);
 
 /*
- * Router: logits, softmax, top-k and gate weights, per-expert counts and the
- * auxiliary loss ("The MoE layer", steps 1-2; "The central problem: load
- * balancing", auxiliary loss).
+ * Router: logits, softmax, top-k and gate weights, per-expert counts, the
+ * auxiliary loss and the router z-loss ("The MoE layer", steps 1-2; "The
+ * central problem: load balancing", auxiliary loss and router z-loss).
  *   x           [T][d] dtype          token batch
  *   W_r         [E][d] fp32           router weight
  *   logit_bias  [E] fp32 or NULL      added to every token's logits
@@ -100,11 +100,14 @@ const char* moe_status_string(moe_status s);
  *                                     before any capacity drop
  *   aux_out     [1] fp32 or NULL      E * sum_i f_i P_i, f_i from the first
  *                                     slot; 0 when T == 0
+ *   z_loss_out  [1] fp32 or NULL      router z-loss: the mean over tokens of
+ *                                     (log sum_e exp g[t][e])^2 over the
+ *                                     logits used for routing; 0 when T == 0
  */
 moe_status moe_route(const moe_config* cfg, const void* x, const float* W_r,
                      const float* logit_bias, const float* logits_in, float* logits_out,
                      int32_t* topk_idx, float* topk_w, int32_t* expert_counts, float* aux_out,
-                     void* ws, size_t ws_bytes, void* stream);
+                     float* z_loss_out, void* ws, size_t ws_bytes, void* stream);
 
 /*
  * Dispatch: expert offsets, the capacity drop and the gather of token rows
@@ -153,12 +156,13 @@ moe_status moe_combine(const moe_config* cfg, const float* y_perm, const int32_t
 
 /*
  * The whole layer: route, dispatch, experts, combine.  Intermediates live in
- * the workspace.  aux_out, expert_counts and logits_out may be NULL.
+ * the workspace.  aux_out, expert_counts, logits_out and z_loss_out (as in
+ * moe_route) may be NULL.
  */
 moe_status moe_forward(const moe_config* cfg, const void* x, const float* W_r,
                        const float* logit_bias, const void* W1, const void* b1,
                        const void* W2, const void* b2, void* y, float* aux_out,
-                       int32_t* expert_counts, float* logits_out,
+                       int32_t* expert_counts, float* logits_out, float* z_loss_out,
                        void* ws, size_t ws_bytes, void* stream);
 
 /*
@@ -200,6 +204,19 @@ moe_status moe_dispatch_noalloc(const moe_config* cfg, const void* x, const int3
  * since it was loaded (memsets excluded).  No counterpart on the pages.
  */
 uint64_t moe_launch_count(void);
+
+/*
+ * Diagnostics: runs the bounded pipeline wait of the tensor-core GEMMs (the
+ * mbarrier wait their producer, MMA and epilogue warps use) on a barrier that
+ * nothing completes, with a limit of timeout_ns (clamped to 1 s), in one
+ * single-thread kernel on `stream`.  The wait gives up and records the
+ * time-out in the error record of workspace `ws` exactly as a stalled
+ * pipeline would, so moe_get_device_error then reports MOE_ERR_DEVICE with
+ * code 2 (info 900) and the context stays usable.  `ws`: at least 256 bytes
+ * of device memory (only the error record is touched).  No counterpart on
+ * the pages.
+ */
+moe_status moe_check_wait_timeout(void* ws, uint64_t timeout_ns, void* stream);
 
 #ifdef __cplusplus
 }

@@ -23,7 +23,7 @@ STATUS = {0: "ok", 1: "invalid argument", 2: "misaligned pointer or row length",
 
 EXPORTED = ("moe_workspace_size", "moe_status_string", "moe_route", "moe_dispatch",
             "moe_expert_ffn", "moe_combine", "moe_forward", "moe_get_device_error",
-            "moe_launch_count", "moe_dispatch_noalloc")
+            "moe_launch_count", "moe_dispatch_noalloc", "moe_check_wait_timeout")
 
 
 class MoeConfig(ctypes.Structure):
@@ -56,11 +56,11 @@ def load() -> ctypes.CDLL:
         lib.moe_status_string.argtypes = [ctypes.c_int]
         cfgp = ctypes.POINTER(MoeConfig)
         sz = ctypes.c_size_t
-        lib.moe_route.argtypes = [cfgp] + [_P] * 9 + [_P, sz, _P]
+        lib.moe_route.argtypes = [cfgp] + [_P] * 10 + [_P, sz, _P]
         lib.moe_dispatch.argtypes = [cfgp] + [_P] * 8 + [_P, sz, _P]
         lib.moe_expert_ffn.argtypes = [cfgp] + [_P] * 8 + [_P, sz, _P]
         lib.moe_combine.argtypes = [cfgp, _P, _P, _P, _P]
-        lib.moe_forward.argtypes = [cfgp] + [_P] * 11 + [_P, sz, _P]
+        lib.moe_forward.argtypes = [cfgp] + [_P] * 12 + [_P, sz, _P]
         lib.moe_get_device_error.argtypes = [_P, _P, ctypes.POINTER(ctypes.c_int32),
                                              ctypes.POINTER(ctypes.c_int32)]
         for name in EXPORTED[2:8]:
@@ -69,6 +69,8 @@ def load() -> ctypes.CDLL:
         lib.moe_dispatch_noalloc.argtypes = [cfgp] + [_P] * 8 + [_P]
         lib.moe_launch_count.restype = ctypes.c_uint64
         lib.moe_launch_count.argtypes = []
+        lib.moe_check_wait_timeout.restype = ctypes.c_int
+        lib.moe_check_wait_timeout.argtypes = [_P, ctypes.c_uint64, _P]
         _lib = lib
     return _lib
 
@@ -110,11 +112,11 @@ def workspace(cfg: MoeConfig, device="cuda") -> torch.Tensor:
 
 
 def route(cfg, x, W_r, topk_idx, topk_w, ws, logit_bias=None, logits_in=None, logits_out=None,
-          expert_counts=None, aux_out=None, stream=None):
+          expert_counts=None, aux_out=None, z_loss_out=None, stream=None):
     _check("moe_route", load().moe_route(
         ctypes.byref(cfg), _ptr(x), _ptr(W_r), _ptr(logit_bias), _ptr(logits_in), _ptr(logits_out),
-        _ptr(topk_idx), _ptr(topk_w), _ptr(expert_counts), _ptr(aux_out), _ptr(ws),
-        ws.numel(), _stream(stream)))
+        _ptr(topk_idx), _ptr(topk_w), _ptr(expert_counts), _ptr(aux_out), _ptr(z_loss_out),
+        _ptr(ws), ws.numel(), _stream(stream)))
 
 
 def dispatch(cfg, x, topk_idx, offsets, slot_of, perm_token, x_perm, ws, topk_w=None,
@@ -145,16 +147,23 @@ def combine(cfg, y_perm, slot_of, y, stream=None):
 
 
 def forward(cfg, x, W_r, W1, b1, W2, b2, y, ws, logit_bias=None, aux_out=None,
-            expert_counts=None, logits_out=None, stream=None):
+            expert_counts=None, logits_out=None, z_loss_out=None, stream=None):
     _check("moe_forward", load().moe_forward(
         ctypes.byref(cfg), _ptr(x), _ptr(W_r), _ptr(logit_bias), _ptr(W1), _ptr(b1), _ptr(W2),
-        _ptr(b2), _ptr(y), _ptr(aux_out), _ptr(expert_counts), _ptr(logits_out), _ptr(ws),
-        ws.numel(), _stream(stream)))
+        _ptr(b2), _ptr(y), _ptr(aux_out), _ptr(expert_counts), _ptr(logits_out),
+        _ptr(z_loss_out), _ptr(ws), ws.numel(), _stream(stream)))
 
 
 def launch_count() -> int:
     """Kernels libmoe has enqueued in this process (diagnostics)."""
     return int(load().moe_launch_count())
+
+
+def check_wait_timeout(ws, timeout_ns: int, stream=None) -> None:
+    """Run one bounded pipeline wait that times out (diagnostics); the time-out
+    is recorded in ws's error record (read it with get_device_error)."""
+    _check("moe_check_wait_timeout",
+           load().moe_check_wait_timeout(_ptr(ws), ctypes.c_uint64(timeout_ns), _stream(stream)))
 
 
 def get_device_error(ws, stream=None):

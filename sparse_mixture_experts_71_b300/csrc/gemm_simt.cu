@@ -43,10 +43,11 @@ __global__ void __launch_bounds__(256) grouped_gemm_simt(
     const TIN* We = W + (size_t)e * N * K;
     const int tid = threadIdx.x, tx = tid % 16, ty = tid / 16;
     float acc[4][4] = {};
-    // loader: 64 rows x 16 columns per operand = 1024 elements, 4 per thread
+    // loader: 64 rows x 16 columns per operand = 1024 elements, 4 per thread;
+    // the next K slice is loaded into registers while this one is multiplied
     const int lr = tid / 4, lc = (tid % 4) * 4;
-    for (int k0 = 0; k0 < K; k0 += BK) {
-        float av[4], bv[4];
+    float av[4], bv[4];
+    auto load = [&](int k0) {
         const int kk = k0 + lc;
 #pragma unroll
         for (int q = 0; q < 4; ++q) {
@@ -54,6 +55,9 @@ __global__ void __launch_bounds__(256) grouped_gemm_simt(
             av[q] = (m0 + lr < seg1 && kin) ? to_f32(A[(size_t)(m0 + lr) * K + kk + q]) : 0.f;
             bv[q] = (n0 + lr < N && kin) ? to_f32(We[(size_t)(n0 + lr) * K + kk + q]) : 0.f;
         }
+    };
+    load(0);
+    for (int k0 = 0; k0 < K; k0 += BK) {
         __syncthreads();
 #pragma unroll
         for (int q = 0; q < 4; ++q) {
@@ -61,6 +65,7 @@ __global__ void __launch_bounds__(256) grouped_gemm_simt(
             Bs[lc + q][lr] = bv[q];
         }
         __syncthreads();
+        if (k0 + BK < K) load(k0 + BK);
 #pragma unroll
         for (int kq = 0; kq < BK; ++kq) {
             const float4 a4 = *reinterpret_cast<const float4*>(&As[kq][ty * 4]);

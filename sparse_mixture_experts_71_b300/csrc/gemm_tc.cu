@@ -728,6 +728,21 @@ grouped_gemm_pair(const __grid_constant__ CUtensorMap tmA, const __grid_constant
     }
 }
 
+// One bounded pipeline wait on a barrier nothing arrives on: gives up after
+// timeout_ns and records the time-out (where = 900) like a stalled pipeline.
+__global__ void __launch_bounds__(32) wait_timeout_probe(DeviceHeader* hdr, uint64_t timeout_ns) {
+    __shared__ uint64_t bar;
+    __shared__ int abort_flag;
+    if (threadIdx.x != 0) return;
+    tc::mbar_init(&bar, 1);
+    abort_flag = 0;
+    tc::fence_barrier_init();
+    Params p{};
+    p.hdr = hdr;
+    p.timeout_ns = timeout_ns;
+    wait_bar(&bar, 0, &abort_flag, p, 900);
+}
+
 PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
     static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
     if (fn == nullptr) {
@@ -845,6 +860,12 @@ cudaError_t launch_pair(const CUtensorMap* maps, const Params& p1, const Params&
 }  // namespace
 
 uint64_t g_tc_timeout_ns = 2000000000ull;
+
+cudaError_t launch_wait_timeout_probe(DeviceHeader* hdr, uint64_t timeout_ns, cudaStream_t s) {
+    wait_timeout_probe<<<1, 32, 0, s>>>(hdr, timeout_ns);
+    count_launches(1);
+    return cudaGetLastError();
+}
 
 cudaError_t launch_expert_ffn_tc(const moe_config& c, const void* x_perm, int64_t x_rows,
                                  const int32_t* offsets, const void* W1, const void* b1,

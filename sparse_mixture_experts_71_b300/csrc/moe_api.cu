@@ -37,6 +37,7 @@ cudaError_t launch_expert_ffn_simt(const moe_config& c, const void* x_perm, cons
                                    const void* W1, const void* b1, const void* W2, const void* b2,
                                    const float* perm_w, float* y_perm, void* h, int64_t max_seg,
                                    int64_t max_rows, cudaStream_t s);
+cudaError_t launch_wait_timeout_probe(DeviceHeader* hdr, uint64_t timeout_ns, cudaStream_t s);
 cudaError_t launch_expert_ffn_tc(const moe_config& c, const void* x_perm, int64_t x_rows,
                                  const int32_t* offsets, const void* W1, const void* b1,
                                  const void* W2, const void* b2, const float* perm_w,
@@ -74,10 +75,12 @@ moe_status from_cuda(cudaError_t e) { return e == cudaSuccess ? MOE_OK : MOE_ERR
 
 // T == 0: no token, no kernel; counts and the loss are defined as zero.
 moe_status empty_batch(const moe_config& c, int32_t* expert_counts, float* aux_out,
-                       cudaStream_t s) {
+                       float* z_loss_out, cudaStream_t s) {
     if (expert_counts && cudaMemsetAsync(expert_counts, 0, sizeof(int32_t) * c.E, s) != cudaSuccess)
         return MOE_ERR_CUDA;
     if (aux_out && cudaMemsetAsync(aux_out, 0, sizeof(float), s) != cudaSuccess) return MOE_ERR_CUDA;
+    if (z_loss_out && cudaMemsetAsync(z_loss_out, 0, sizeof(float), s) != cudaSuccess)
+        return MOE_ERR_CUDA;
     return MOE_OK;
 }
 
@@ -108,6 +111,7 @@ WsLayout ws_layout(const moe_config& c) {
     L.counts = take(sizeof(int32_t) * c.E);
     L.top1 = take(sizeof(int32_t) * c.E);
     L.blk_p = take(sizeof(float) * (size_t)L.route.blocks * c.E);
+    L.blk_z = take(sizeof(float) * (size_t)L.route.blocks);
     L.blk_hist = take(sizeof(int32_t) * (size_t)L.hist_blocks * c.E);
     L.blk_base = take(sizeof(int32_t) * (size_t)L.hist_blocks * c.E);
     L.local_rank = take(sizeof(int32_t) * (size_t)n);
@@ -165,20 +169,20 @@ const char* moe_status_string(moe_status s) {
 moe_status moe_route(const moe_config* cfg, const void* x, const float* W_r,
                      const float* logit_bias, const float* logits_in, float* logits_out,
                      int32_t* topk_idx, float* topk_w, int32_t* expert_counts, float* aux_out,
-                     void* ws, size_t ws_bytes, void* stream) {
+                     float* z_loss_out, void* ws, size_t ws_bytes, void* stream) {
     moe_status st = check_config(cfg);
     if (st != MOE_OK) return st;
     const moe_config& c = *cfg;
     WsLayout L;
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
-    if (c.T == 0) return empty_batch(c, expert_counts, aux_out, s);
+    if (c.T == 0) return empty_batch(c, expert_counts, aux_out, z_loss_out, s);
     if (topk_idx == nullptr || topk_w == nullptr) return MOE_ERR_INVALID_ARG;
     if (logits_in == nullptr && (x == nullptr || W_r == nullptr)) return MOE_ERR_INVALID_ARG;
     if (logits_in == nullptr && (!aligned16(x) || !aligned16(W_r))) return MOE_ERR_ALIGNMENT;
     if ((st = check_ws(c, ws, ws_bytes, &L)) != MOE_OK) return st;
     chain_begin();
     return from_cuda(launch_route(c, x, W_r, logit_bias, logits_in, logits_out, topk_idx, topk_w,
-                                  expert_counts, aux_out, ws, L, false, s));
+                                  expert_counts, aux_out, z_loss_out, ws, L, false, s));
 }
 
 moe_status moe_dispatch(const moe_config* cfg, const void* x, const int32_t* topk_idx,
@@ -246,13 +250,13 @@ moe_status moe_combine(const moe_config* cfg, const float* y_perm, const int32_t
 moe_status moe_forward(const moe_config* cfg, const void* x, const float* W_r,
                        const float* logit_bias, const void* W1, const void* b1,
                        const void* W2, const void* b2, void* y, float* aux_out,
-                       int32_t* expert_counts, float* logits_out,
+                       int32_t* expert_counts, float* logits_out, float* z_loss_out,
                        void* ws, size_t ws_bytes, void* stream) {
     moe_status st = check_config(cfg);
     if (st != MOE_OK) return st;
     const moe_config& c = *cfg;
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
-    if (c.T == 0) return empty_batch(c, expert_counts, aux_out, s);
+    if (c.T == 0) return empty_batch(c, expert_counts, aux_out, z_loss_out, s);
     if (x == nullptr || W_r == nullptr || W1 == nullptr || b1 == nullptr || W2 == nullptr ||
         b2 == nullptr || y == nullptr)
         return MOE_ERR_INVALID_ARG;
@@ -270,16 +274,25 @@ moe_status moe_forward(const moe_config* cfg, const void* x, const float* W_r,
     float* y_perm = at<float>(ws, L.y_perm);
     chain_begin();
     cudaError_t e = launch_route(c, x, W_r, logit_bias, nullptr, logits_out, idx, w, expert_counts,
-                                 aux_out, ws, L, true, s);
+                                 aux_out, z_loss_out, ws, L, true, s);
     if (e == cudaSuccess)
         e = launch_scan_permute(c, x, idx, w, L.route.tokens * c.k, L.route.blocks, offsets,
                                 slot_of, perm_token, perm_w, x_perm, ws, L,
-                                route_loss_args(c, ws, L, expert_counts, aux_out), s);
+                                route_loss_args(c, ws, L, expert_counts, aux_out, z_loss_out),
+                                s);
     if (e == cudaSuccess)
         e = launch_expert_ffn(c, x_perm, L.rows, offsets, W1, b1, W2, b2, perm_w, y_perm, ws, L,
                               s);
     if (e == cudaSuccess) e = launch_combine(c, y_perm, slot_of, y, s);
     return from_cuda(e);
+}
+
+moe_status moe_check_wait_timeout(void* ws, uint64_t timeout_ns, void* stream) {
+    if (ws == nullptr) return MOE_ERR_INVALID_ARG;
+    if ((reinterpret_cast<uintptr_t>(ws) & 255u) != 0) return MOE_ERR_WORKSPACE;
+    if (timeout_ns > 1000000000ull) timeout_ns = 1000000000ull;
+    return from_cuda(launch_wait_timeout_probe(reinterpret_cast<DeviceHeader*>(ws), timeout_ns,
+                                               reinterpret_cast<cudaStream_t>(stream)));
 }
 
 moe_status moe_get_device_error(void* ws, void* stream, int32_t* code, int32_t* info) {

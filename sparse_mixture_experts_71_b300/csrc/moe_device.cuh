@@ -93,10 +93,12 @@ __device__ __forceinline__ float2 gelu2_as7126(float2 u) {
 // router (blk_p, nblk rows of E) and the first-slot / all-slot counts.
 struct LossArgs {
     const float* blk_p;
+    const float* blk_z;      // per-block sums of the squared log-sum-exp
     const int32_t* top1;
     const int32_t* counts;
     int32_t* expert_counts;  // output or null
     float* aux_out;          // output or null
+    float* z_out;            // router z-loss output or null
     int nblk, E, T;
 };
 
@@ -141,6 +143,20 @@ __device__ __forceinline__ void loss_and_counts(const LossArgs& l, float* s_part
         for (int e = 0; e < l.E; ++e) s += s_d[e];
         const float Tf = (float)l.T;
         l.aux_out[0] = (float)l.E * (s / Tf) / Tf;
+    }
+    if (l.z_out != nullptr) {  // router z-loss: the block sums, 256 strided parts in order
+        __syncthreads();
+        if (tid < 256) {
+            float v = 0.f;
+            for (int b = tid; b < l.nblk; b += 256) v += __ldcg(l.blk_z + b);
+            s_part[tid] = v;
+        }
+        __syncthreads();
+        if (tid == 0) {
+            float s = 0.f;
+            for (int i = 0; i < 256; ++i) s += s_part[i];
+            l.z_out[0] = s / (float)l.T;
+        }
     }
 }
 

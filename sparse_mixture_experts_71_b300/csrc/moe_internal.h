@@ -45,6 +45,7 @@ struct WsLayout {
     size_t counts;       // int32 [E]   assignments per expert (all slots)
     size_t top1;         // int32 [E]   first-slot choices per expert
     size_t blk_p;        // fp32 [route.blocks][E] per-block sums of p
+    size_t blk_z;        // fp32 [route.blocks] per-block sums of the squared log-sum-exp
     size_t blk_hist;     // int32 [hist_blocks][E]
     size_t blk_base;     // int32 [hist_blocks][E]
     size_t local_rank;   // int32 [T*k]
@@ -148,8 +149,8 @@ template <typename T> __host__ __device__ inline T* at(void* base, size_t off) {
 cudaError_t launch_route(const moe_config& c, const void* x, const float* W_r,
                          const float* logit_bias, const float* logits_in, float* logits_out,
                          int32_t* topk_idx, float* topk_w, int32_t* expert_counts,
-                         float* aux_out, void* ws, const WsLayout& L, bool fuse_count,
-                         cudaStream_t s);
+                         float* aux_out, float* z_loss_out, void* ws, const WsLayout& L,
+                         bool fuse_count, cudaStream_t s);
 
 // Counting kernel over topk_idx (granularity kCountBlock assignments).
 cudaError_t launch_count(const moe_config& c, const int32_t* topk_idx, void* ws,
@@ -167,7 +168,7 @@ cudaError_t launch_scan_permute(const moe_config& c, const void* x, const int32_
                                 const LossArgs& loss, cudaStream_t s);
 // Loss inputs/outputs of the router's per-block statistics in workspace ws.
 LossArgs route_loss_args(const moe_config& c, void* ws, const WsLayout& L,
-                         int32_t* expert_counts, float* aux_out);
+                         int32_t* expert_counts, float* aux_out, float* z_loss_out);
 
 cudaError_t launch_expert_ffn(const moe_config& c, const void* x_perm, int64_t x_rows,
                               const int32_t* offsets, const void* W1, const void* b1,

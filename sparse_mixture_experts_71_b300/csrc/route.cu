@@ -465,7 +465,7 @@ __global__ void __launch_bounds__(kThreads) route_tile_kernel(RouteArgs a) {
     for (int tok = warp; tok < Gm::TB; tok += kWarps) {
         const int t = t0 + tok;
         if (t >= a.T) {
-            for (int e = lane; e < EMAX; e += 32) lg[tok * Gm::LGS + e] = 0.f;
+            for (int e = lane; e <= EMAX; e += 32) lg[tok * Gm::LGS + e] = 0.f;
             continue;
         }
         float gv[PER_LANE];
@@ -492,6 +492,10 @@ __global__ void __launch_bounds__(kThreads) route_tile_kernel(RouteArgs a) {
 #pragma unroll
         for (int o = 16; o > 0; o >>= 1) ssum += __shfl_xor_sync(0xffffffffu, ssum, o);
         const float inv = 1.0f / ssum;
+        if (lane == 0) {  // squared log-sum-exp (router z-loss) in the pad column
+            const float lse = m + logf(ssum);
+            lg[tok * Gm::LGS + EMAX] = lse * lse;
+        }
         bool taken[PER_LANE];
 #pragma unroll
         for (int i = 0; i < PER_LANE; ++i) taken[i] = false;
@@ -620,9 +624,11 @@ __global__ void __launch_bounds__(256) route_finish_kernel(LossArgs l) {
 }  // namespace
 
 LossArgs route_loss_args(const moe_config& c, void* ws, const WsLayout& L,
-                         int32_t* expert_counts, float* aux_out) {
+                         int32_t* expert_counts, float* aux_out, float* z_loss_out) {
     LossArgs l;
     l.blk_p = at<float>(ws, L.blk_p);
+    l.blk_z = at<float>(ws, L.blk_z);
+    l.z_out = z_loss_out;
     l.top1 = at<int32_t>(ws, L.top1);
     l.counts = at<int32_t>(ws, L.counts);
     l.expert_counts = expert_counts;
@@ -669,8 +675,8 @@ RouteGeom route_geom(const moe_config& c) {
 cudaError_t launch_route(const moe_config& c, const void* x, const float* W_r,
                          const float* logit_bias, const float* logits_in, float* logits_out,
                          int32_t* topk_idx, float* topk_w, int32_t* expert_counts,
-                         float* aux_out, void* ws, const WsLayout& L, bool fuse_count,
-                         cudaStream_t s) {
+                         float* aux_out, float* z_loss_out, void* ws, const WsLayout& L,
+                         bool fuse_count, cudaStream_t s) {
     RouteArgs a;
     a.x = x; a.W_r = W_r; a.bias = logit_bias; a.logits_in = logits_in; a.logits_out = logits_out;
     a.topk_idx = topk_idx; a.topk_w = topk_w; a.expert_counts = expert_counts; a.aux_out = aux_out;
@@ -678,6 +684,7 @@ cudaError_t launch_route(const moe_config& c, const void* x, const float* W_r,
     a.counts = at<int32_t>(ws, L.counts);
     a.top1 = at<int32_t>(ws, L.top1);
     a.blk_p = at<float>(ws, L.blk_p);
+    a.blk_z = at<float>(ws, L.blk_z);
     a.blk_hist = fuse_count ? at<int32_t>(ws, L.blk_hist) : nullptr;
     a.local_rank = at<int32_t>(ws, L.local_rank);
     a.T = c.T; a.d = c.d; a.E = c.E; a.k = c.k; a.renormalize = c.renormalize;
@@ -698,7 +705,7 @@ cudaError_t launch_route(const moe_config& c, const void* x, const float* W_r,
     }
     if (err != cudaSuccess || fuse_count) return err;
     return launch_kernel(route_finish_kernel, dim3(1), dim3(256), 0, s, 1, false,
-                         route_loss_args(c, ws, L, expert_counts, aux_out));
+                         route_loss_args(c, ws, L, expert_counts, aux_out, z_loss_out));
 }
 
 }  // namespace moe

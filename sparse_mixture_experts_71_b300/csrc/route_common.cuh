@@ -29,6 +29,7 @@ struct RouteArgs {
     int32_t* counts;      // ws: [E] all-slot assignments
     int32_t* top1;        // ws: [E] first-slot choices
     float* blk_p;         // ws: [nblk][E]
+    float* blk_z;         // ws: [nblk] per-block sums of the squared log-sum-exp
     int32_t* blk_hist;    // ws: [nblk][E] or null (no fused counting)
     int32_t* local_rank;  // ws: [T*k]
     int T, d, E, k, renormalize, nblk;
@@ -67,7 +68,8 @@ __device__ void block_rank(const int* s_idx, int n, int E, int (*wh)[EMAX], int*
     for (int e = tid; e < E; e += kThreads) hist_row[e] = carry[e];
 }
 
-// Per-block sums of p (rows of s_p, fixed order), counts, and the fused
+// Per-block sums of p (rows of s_p, fixed order) and of the squared
+// log-sum-exp (column EMAX of s_p, the rows' pad slot), counts, and the fused
 // dispatch histogram.
 template <int EMAX>
 __device__ void finish_block(const RouteArgs& a, const float* s_p, int lds, int TB,
@@ -75,6 +77,13 @@ __device__ void finish_block(const RouteArgs& a, const float* s_p, int lds, int 
                              int (*wh)[EMAX], int* carry) {
     const int tid = threadIdx.x;
     const int t0 = blockIdx.x * TB;
+    if (tid < 32) {  // warp 0: tokens tid, tid + 32, ... then a fixed shuffle tree
+        float z = 0.f;
+        for (int tok = tid; tok < TB; tok += 32) z += s_p[tok * lds + EMAX];
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) z += __shfl_xor_sync(0xffffffffu, z, o);
+        if (tid == 0) a.blk_z[blockIdx.x] = z;
+    }
     for (int e = tid; e < a.E; e += kThreads) {
         float v = 0.f;
         for (int tok = 0; tok < TB; ++tok) v += s_p[tok * lds + e];
@@ -97,7 +106,7 @@ __device__ __forceinline__ void token_epilogue(const RouteArgs& a, float* prow, 
                                                int* s_idx, int* s_cnt, int* s_top1) {
     if (t >= a.T) {
 #pragma unroll
-        for (int e = 0; e < EMAX; ++e) prow[e] = 0.f;
+        for (int e = 0; e <= EMAX; ++e) prow[e] = 0.f;
         return;
     }
     float g[EMAX];
@@ -114,6 +123,8 @@ __device__ __forceinline__ void token_epilogue(const RouteArgs& a, float* prow, 
 #pragma unroll
     for (int e = 0; e < EMAX; ++e) ssum += e < a.E ? expf(g[e] - m) : 0.f;
     const float inv = 1.0f / ssum;
+    const float lse = m + logf(ssum);
+    prow[EMAX] = lse * lse;  // squared log-sum-exp (router z-loss), the row's pad slot
     if (a.logits_out != nullptr)
         for (int e = 0; e < a.E; ++e) a.logits_out[(size_t)t * a.E + e] = prow[e];
 #pragma unroll

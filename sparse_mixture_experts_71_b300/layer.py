@@ -59,8 +59,10 @@ class MoELayer:
             self._ws[T] = B.workspace(self.config(T), device=self.W1.device)
         return self._ws[T]
 
-    def forward(self, x, y=None, aux=None, expert_counts=None, logits_out=None, stream=None):
-        """(y, aux) for the token batch x (T, d); optional outputs are filled in place."""
+    def forward(self, x, y=None, aux=None, expert_counts=None, logits_out=None, z_loss=None,
+                stream=None):
+        """(y, aux) for the token batch x (T, d); optional outputs (expert_counts,
+        logits_out, z_loss: the router z-loss, one fp32) are filled in place."""
         T = x.shape[0]
         if y is None:
             y = torch.empty_like(x)
@@ -68,7 +70,8 @@ class MoELayer:
             aux = torch.empty(1, dtype=torch.float32, device=x.device)
         B.forward(self.config(T), x, self.W_r, self.W1, self.b1, self.W2, self.b2, y,
                   self.workspace(T), logit_bias=self.logit_bias, aux_out=aux,
-                  expert_counts=expert_counts, logits_out=logits_out, stream=stream)
+                  expert_counts=expert_counts, logits_out=logits_out, z_loss_out=z_loss,
+                  stream=stream)
         return y, aux
 
     __call__ = forward

@@ -77,9 +77,10 @@ class GpuRun:
         r["w"] = torch.empty((T, k), dtype=torch.float32, device=cuda)
         r["counts"] = torch.empty(E, dtype=torch.int32, device=cuda)
         r["aux"] = torch.empty(1, dtype=torch.float32, device=cuda)
+        r["z"] = torch.full((1,), -1.0, dtype=torch.float32, device=cuda)
         B.route(self.cfg, D["x"], D["W_r"], r["idx"], r["w"], self.ws, logit_bias=D["logit_bias"],
                 logits_in=logits_in, logits_out=r["logits"], expert_counts=r["counts"],
-                aux_out=r["aux"], stream=self.stream)
+                aux_out=r["aux"], z_loss_out=r["z"], stream=self.stream)
         r["offsets"] = torch.empty(E + 1, dtype=torch.int32, device=cuda)
         r["slot_of"] = torch.empty((T, k), dtype=torch.int32, device=cuda)
         r["perm_token"] = torch.full((max(n, 1),), -7, dtype=torch.int32, device=cuda)
@@ -101,11 +102,12 @@ class GpuRun:
         aux = torch.empty(1, dtype=torch.float32, device=y.device)
         counts = torch.empty(wl.E, dtype=torch.int32, device=y.device)
         logits = torch.empty((wl.T, wl.E), dtype=torch.float32, device=y.device)
+        z = torch.full((1,), -1.0, dtype=torch.float32, device=y.device)
         B.forward(self.cfg, D["x"], D["W_r"], D["W1"], D["b1"], D["W2"], D["b2"], y, self.ws,
                   logit_bias=D["logit_bias"], aux_out=aux, expert_counts=counts,
-                  logits_out=logits, stream=self.stream)
+                  logits_out=logits, z_loss_out=z, stream=self.stream)
         torch.cuda.synchronize()
-        return dict(y=y, aux=aux, counts=counts, logits=logits)
+        return dict(y=y, aux=aux, counts=counts, logits=logits, z=z)
 
 
 def oracle_on(inp, wl, logits=None, tokens=None, layout=True):

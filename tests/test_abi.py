@@ -65,7 +65,7 @@ def test_forward_rejects_bad_config(cfg, status):
     lib = B.load()
     ref = ctypes.byref(cfg) if cfg is not None else None
     st = lib.moe_forward(ref, FAKE, FAKE, None, FAKE, FAKE, FAKE, FAKE, FAKE, None, None, None,
-                         FAKE, 1 << 40, None)
+                         None, FAKE, 1 << 40, None)
     assert st == status
 
 
@@ -76,20 +76,22 @@ def test_calls_reject_null_misaligned_and_small_workspace():
     need = B.workspace_size(c)
     # null required pointer
     assert lib.moe_forward(cr, None, FAKE, None, FAKE, FAKE, FAKE, FAKE, FAKE, None, None, None,
-                           FAKE, need, None) == 1
+                           None, FAKE, need, None) == 1
     # misaligned x
     assert lib.moe_forward(cr, FAKE + 8, FAKE, None, FAKE, FAKE, FAKE, FAKE, FAKE, None, None,
-                           None, FAKE, need, None) == 2
+                           None, None, FAKE, need, None) == 2
     # workspace too small / misaligned
     assert lib.moe_forward(cr, FAKE, FAKE, None, FAKE, FAKE, FAKE, FAKE, FAKE, None, None, None,
-                           FAKE, need - 1, None) == 3
+                           None, FAKE, need - 1, None) == 3
     assert lib.moe_forward(cr, FAKE, FAKE, None, FAKE, FAKE, FAKE, FAKE, FAKE, None, None, None,
-                           FAKE + 16, need, None) == 3
-    assert lib.moe_route(cr, FAKE, FAKE, None, None, None, None, FAKE, None, None, FAKE, need,
-                         None) == 1
+                           None, FAKE + 16, need, None) == 3
+    assert lib.moe_route(cr, FAKE, FAKE, None, None, None, None, FAKE, None, None, None, FAKE,
+                         need, None) == 1
     assert lib.moe_dispatch(cr, FAKE, FAKE, None, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, need,
                             None) == 1  # perm_w without topk_w
     assert lib.moe_expert_ffn(cr, FAKE, FAKE, FAKE, FAKE, FAKE + 4, FAKE, None, FAKE, FAKE, need,
                               None) == 2
     assert lib.moe_combine(cr, FAKE, None, FAKE, None) == 1
     assert lib.moe_get_device_error(None, None, None, None) == 1
+    assert lib.moe_check_wait_timeout(None, ctypes.c_uint64(1000), None) == 1
+    assert lib.moe_check_wait_timeout(FAKE + 16, ctypes.c_uint64(1000), None) == 3

@@ -44,6 +44,7 @@ def _check(wl, inp, r):
     nk = int(ref.offsets[-1])
     assert np.array_equal(to_np(r["perm_token"])[:nk], ref.perm_token)
     assert abs(float(r["aux"][0]) - ref.aux) <= 1e-5 * max(1.0, ref.aux)
+    assert abs(float(r["z"][0]) - ref.z_loss) <= 1e-5 * max(1.0, ref.z_loss)
     assert_y_close(to_np(r["y"]), ref.y, wl.dtype)
     return ref
 
@@ -59,6 +60,7 @@ def test_small_shapes(case):
         assert not torch.any(r["y"].float() != 0)
     f = run.forward()
     assert torch.equal(f["y"], r["y"])
+    assert torch.equal(f["z"], r["z"])
     assert B.get_device_error(run.ws)[0] == 0
     del ref
 
@@ -92,6 +94,7 @@ def test_empty_batch():
     run = GpuRun(wl, inp)
     r = run.staged()
     assert float(r["aux"][0]) == 0.0 and not torch.any(r["counts"] != 0)
+    assert float(r["z"][0]) == 0.0
     assert not torch.any(r["offsets"] != 0)
 
 
@@ -148,4 +151,20 @@ def test_segment_sizes_around_tile_boundaries(name):
     assert np.array_equal(to_np(r["offsets"]), ref.offsets)
     assert np.array_equal(to_np(r["perm_token"])[:T], ref.perm_token)
     assert_y_close(to_np(r["y"]), ref.y, wl.dtype)
+    assert B.get_device_error(run.ws)[0] == 0
+
+
+def test_stalled_pipeline_wait_reports_time_out_and_context_survives():
+    """The bounded mbarrier wait the tensor-core pipelines use, on a barrier
+    nothing completes, gives up after its limit and records code 2 (time-out)
+    in the workspace; the error record reads back, clears, and the next layer
+    call on the same workspace and context runs normally."""
+    wl = _wl("after-timeout", 2048, 64, 128, 8, 2, "bf16", None, True)
+    inp = I.make_inputs(wl, seed=6)
+    run = GpuRun(wl, inp)
+    B.check_wait_timeout(run.ws, 2_000_000)  # 2 ms
+    assert B.get_device_error(run.ws) == (6, 2, 900)
+    assert B.get_device_error(run.ws)[0] == 0  # cleared
+    r = run.staged()
+    _check(wl, inp, r)
     assert B.get_device_error(run.ws)[0] == 0

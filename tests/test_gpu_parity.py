@@ -54,6 +54,7 @@ def test_workload_parity(wl):
     assert np.array_equal(to_np(r["counts"]), ref.counts)
     np.testing.assert_allclose(to_np(r["w"]), ref.w, rtol=3e-6, atol=1e-7)
     assert abs(float(r["aux"][0]) - ref.aux) <= 1e-5 * max(1.0, ref.aux)
+    assert abs(float(r["z"][0]) - ref.z_loss) <= 1e-5 * max(1.0, ref.z_loss)
     # 3. dispatch layout: bit-exact
     assert np.array_equal(to_np(r["offsets"]), ref.offsets)
     assert np.array_equal(to_np(r["slot_of"]), ref.slot_of)
@@ -88,5 +89,6 @@ def test_forward_matches_staged_calls(wl):
     assert torch.equal(f["logits"], r["logits"])
     assert torch.equal(f["counts"], r["counts"])
     assert torch.equal(f["aux"], r["aux"])
+    assert torch.equal(f["z"], r["z"])
     # and the forward pass is deterministic
     assert torch.equal(run.forward()["y"], f["y"])
