@@ -29,7 +29,10 @@ the combine and of the auxiliary loss did not survive extraction):
 * f_i of the auxiliary loss counts the top-1 choice only, before any drop;
 * the router z-loss, which the pages name without a formula ("penalise large
   router logits"), is the mean over tokens of the squared log-sum-exp of the
-  token's router logits (the logits that enter the softmax, bias included).
+  token's router logits (the logits that enter the softmax, bias included);
+* noisy gating adds a caller-drawn (T, E) noise tensor to the router logits
+  before the softmax and the top-k (the pages give no distribution; the
+  caller chooses it).
 
 Parity: the routing, capacity, auxiliary-loss and combine functions are pinned
 by the pages' worked examples, closed forms and brute force (tests).  The
@@ -48,18 +51,23 @@ from scipy.special import erf
 f64 = np.float64
 
 
-def router_logits(x, W_r, logit_bias=None) -> np.ndarray:
-    """g = W_r x (+ per-expert bias), computed in fp64 and rounded to fp32.
+def router_logits(x, W_r, logit_bias=None, logit_noise=None) -> np.ndarray:
+    """g = W_r x (+ per-expert bias) (+ per-token noise), computed in fp64 and
+    rounded to fp32.
 
     [LECTURE] "The MoE layer", step 1 (router logits, an ``nn.Linear`` with no
     bias in its listing).  The optional additive per-expert bias is the fixed
     logit offset of the Switch workload (the mechanism [LECTURE] "The central
-    problem: load balancing" names for bias-based balancing).
+    problem: load balancing" names for bias-based balancing).  The optional
+    (T, E) noise is noisy gating ("The central problem: load balancing": noise
+    added to the router logits during training); the caller draws it.
     x: (T, d); W_r: (E, d); returns (T, E) fp32.
     """
     g = np.asarray(x, f64) @ np.asarray(W_r, f64).T
     if logit_bias is not None:
         g = g + np.asarray(logit_bias, f64)[None, :]
+    if logit_noise is not None:
+        g = g + np.asarray(logit_noise, f64)
     return g.astype(np.float32)
 
 
@@ -236,7 +244,7 @@ class OracleResult:
 
 def moe_forward(x, W_r, W1, b1, W2, b2, k: int, renormalize: bool = True,
                 capacity: int | None = None, logit_bias=None, logits=None,
-                tokens=None, layout: bool = True) -> OracleResult:
+                tokens=None, layout: bool = True, logit_noise=None) -> OracleResult:
     """The MoE layer forward pass, looping over experts.
 
     [LECTURE] "The MoE layer": router logits and softmax, top-k selection,
@@ -255,7 +263,7 @@ def moe_forward(x, W_r, W1, b1, W2, b2, k: int, renormalize: bool = True,
     T, d = x.shape
     E = np.asarray(W_r).shape[0]
     if logits is None:
-        logits = router_logits(x, W_r, logit_bias)
+        logits = router_logits(x, W_r, logit_bias, logit_noise)
     logits = np.asarray(logits, np.float32)
     probs = softmax(logits)
     idx = top_k(logits, k)

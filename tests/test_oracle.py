@@ -131,6 +131,32 @@ def test_softmax_matches_torch():
     np.testing.assert_allclose(O.softmax(g), want, rtol=1e-13, atol=0)
 
 
+# ---------------------------------------------------------- noisy gating pins
+
+def test_noise_equal_to_a_bias_row_is_the_bias_and_zero_noise_is_none():
+    """Noise that is the same per-expert offset for every token gives exactly
+    the logits of that offset as logit bias; zero noise changes nothing."""
+    g = np.random.default_rng(8)
+    x, W = g.standard_normal((40, 32)), g.standard_normal((6, 32))
+    c = g.standard_normal(6)
+    assert np.array_equal(O.router_logits(x, W, logit_noise=np.tile(c, (40, 1))),
+                          O.router_logits(x, W, logit_bias=c))
+    assert np.array_equal(O.router_logits(x, W, logit_noise=np.zeros((40, 6))),
+                          O.router_logits(x, W))
+
+
+def test_large_noise_on_one_expert_selects_it():
+    """Noise far above the logit spread on expert j makes j every token's
+    first choice ("add noise to router logits ... to encourage exploration")."""
+    g = np.random.default_rng(9)
+    x, W = g.standard_normal((64, 16)), g.standard_normal((8, 16)) * 0.1
+    noise = np.zeros((64, 8))
+    noise[:, 5] = 1e3
+    r = O.moe_forward(x, W, np.zeros((8, 4, 16)), np.zeros((8, 4)), np.zeros((8, 16, 4)),
+                      np.zeros((8, 16)), k=2, logit_noise=noise)
+    assert np.all(r.idx[:, 0] == 5)
+
+
 # ---------------------------------------------------------- router z-loss pins
 
 @pytest.mark.parametrize("E,c", [(1, 0.0), (8, 0.0), (8, -2.5), (64, 3.25)])
