@@ -91,8 +91,13 @@ const char* moe_status_string(moe_status s);
  *   x           [T][d] dtype          token batch
  *   W_r         [E][d] fp32           router weight
  *   logit_bias  [E] fp32 or NULL      added to every token's logits
- *   logits_in   [T][E] fp32 or NULL   if given, used as the logits (x, W_r
- *                                     and logit_bias are then not read)
+ *   logit_noise [T][E] fp32 or NULL   noisy gating: added to the logits
+ *                                     before the softmax and the top-k (the
+ *                                     caller draws it; "The central problem:
+ *                                     load balancing", noisy gating)
+ *   logits_in   [T][E] fp32 or NULL   if given, used as the logits (x, W_r,
+ *                                     logit_bias and logit_noise are then
+ *                                     not read)
  *   logits_out  [T][E] fp32 or NULL   receives the logits used for routing
  *   topk_idx    [T][k] int32          selected experts, best first
  *   topk_w      [T][k] fp32           gate weights of the selected experts
@@ -105,7 +110,8 @@ const char* moe_status_string(moe_status s);
  *                                     logits used for routing; 0 when T == 0
  */
 moe_status moe_route(const moe_config* cfg, const void* x, const float* W_r,
-                     const float* logit_bias, const float* logits_in, float* logits_out,
+                     const float* logit_bias, const float* logit_noise,
+                     const float* logits_in, float* logits_out,
                      int32_t* topk_idx, float* topk_w, int32_t* expert_counts, float* aux_out,
                      float* z_loss_out, void* ws, size_t ws_bytes, void* stream);
 
@@ -156,11 +162,12 @@ moe_status moe_combine(const moe_config* cfg, const float* y_perm, const int32_t
 
 /*
  * The whole layer: route, dispatch, experts, combine.  Intermediates live in
- * the workspace.  aux_out, expert_counts, logits_out and z_loss_out (as in
- * moe_route) may be NULL.
+ * the workspace.  logit_noise, aux_out, expert_counts, logits_out and
+ * z_loss_out (as in moe_route) may be NULL.
  */
 moe_status moe_forward(const moe_config* cfg, const void* x, const float* W_r,
-                       const float* logit_bias, const void* W1, const void* b1,
+                       const float* logit_bias, const float* logit_noise,
+                       const void* W1, const void* b1,
                        const void* W2, const void* b2, void* y, float* aux_out,
                        int32_t* expert_counts, float* logits_out, float* z_loss_out,
                        void* ws, size_t ws_bytes, void* stream);

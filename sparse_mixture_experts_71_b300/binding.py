@@ -56,11 +56,11 @@ def load() -> ctypes.CDLL:
         lib.moe_status_string.argtypes = [ctypes.c_int]
         cfgp = ctypes.POINTER(MoeConfig)
         sz = ctypes.c_size_t
-        lib.moe_route.argtypes = [cfgp] + [_P] * 10 + [_P, sz, _P]
+        lib.moe_route.argtypes = [cfgp] + [_P] * 11 + [_P, sz, _P]
         lib.moe_dispatch.argtypes = [cfgp] + [_P] * 8 + [_P, sz, _P]
         lib.moe_expert_ffn.argtypes = [cfgp] + [_P] * 8 + [_P, sz, _P]
         lib.moe_combine.argtypes = [cfgp, _P, _P, _P, _P]
-        lib.moe_forward.argtypes = [cfgp] + [_P] * 12 + [_P, sz, _P]
+        lib.moe_forward.argtypes = [cfgp] + [_P] * 13 + [_P, sz, _P]
         lib.moe_get_device_error.argtypes = [_P, _P, ctypes.POINTER(ctypes.c_int32),
                                              ctypes.POINTER(ctypes.c_int32)]
         for name in EXPORTED[2:8]:
@@ -112,9 +112,10 @@ def workspace(cfg: MoeConfig, device="cuda") -> torch.Tensor:
 
 
 def route(cfg, x, W_r, topk_idx, topk_w, ws, logit_bias=None, logits_in=None, logits_out=None,
-          expert_counts=None, aux_out=None, z_loss_out=None, stream=None):
+          expert_counts=None, aux_out=None, z_loss_out=None, logit_noise=None, stream=None):
     _check("moe_route", load().moe_route(
-        ctypes.byref(cfg), _ptr(x), _ptr(W_r), _ptr(logit_bias), _ptr(logits_in), _ptr(logits_out),
+        ctypes.byref(cfg), _ptr(x), _ptr(W_r), _ptr(logit_bias), _ptr(logit_noise),
+        _ptr(logits_in), _ptr(logits_out),
         _ptr(topk_idx), _ptr(topk_w), _ptr(expert_counts), _ptr(aux_out), _ptr(z_loss_out),
         _ptr(ws), ws.numel(), _stream(stream)))
 
@@ -147,9 +148,11 @@ def combine(cfg, y_perm, slot_of, y, stream=None):
 
 
 def forward(cfg, x, W_r, W1, b1, W2, b2, y, ws, logit_bias=None, aux_out=None,
-            expert_counts=None, logits_out=None, z_loss_out=None, stream=None):
+            expert_counts=None, logits_out=None, z_loss_out=None, logit_noise=None,
+            stream=None):
     _check("moe_forward", load().moe_forward(
-        ctypes.byref(cfg), _ptr(x), _ptr(W_r), _ptr(logit_bias), _ptr(W1), _ptr(b1), _ptr(W2),
+        ctypes.byref(cfg), _ptr(x), _ptr(W_r), _ptr(logit_bias), _ptr(logit_noise), _ptr(W1),
+        _ptr(b1), _ptr(W2),
         _ptr(b2), _ptr(y), _ptr(aux_out), _ptr(expert_counts), _ptr(logits_out),
         _ptr(z_loss_out), _ptr(ws), ws.numel(), _stream(stream)))
 

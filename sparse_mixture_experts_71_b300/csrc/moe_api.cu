@@ -167,7 +167,8 @@ const char* moe_status_string(moe_status s) {
 }
 
 moe_status moe_route(const moe_config* cfg, const void* x, const float* W_r,
-                     const float* logit_bias, const float* logits_in, float* logits_out,
+                     const float* logit_bias, const float* logit_noise,
+                     const float* logits_in, float* logits_out,
                      int32_t* topk_idx, float* topk_w, int32_t* expert_counts, float* aux_out,
                      float* z_loss_out, void* ws, size_t ws_bytes, void* stream) {
     moe_status st = check_config(cfg);
@@ -181,8 +182,9 @@ moe_status moe_route(const moe_config* cfg, const void* x, const float* W_r,
     if (logits_in == nullptr && (!aligned16(x) || !aligned16(W_r))) return MOE_ERR_ALIGNMENT;
     if ((st = check_ws(c, ws, ws_bytes, &L)) != MOE_OK) return st;
     chain_begin();
-    return from_cuda(launch_route(c, x, W_r, logit_bias, logits_in, logits_out, topk_idx, topk_w,
-                                  expert_counts, aux_out, z_loss_out, ws, L, false, s));
+    return from_cuda(launch_route(c, x, W_r, logit_bias, logit_noise, logits_in, logits_out,
+                                  topk_idx, topk_w, expert_counts, aux_out, z_loss_out, ws, L,
+                                  false, s));
 }
 
 moe_status moe_dispatch(const moe_config* cfg, const void* x, const int32_t* topk_idx,
@@ -248,7 +250,8 @@ moe_status moe_combine(const moe_config* cfg, const float* y_perm, const int32_t
 }
 
 moe_status moe_forward(const moe_config* cfg, const void* x, const float* W_r,
-                       const float* logit_bias, const void* W1, const void* b1,
+                       const float* logit_bias, const float* logit_noise,
+                       const void* W1, const void* b1,
                        const void* W2, const void* b2, void* y, float* aux_out,
                        int32_t* expert_counts, float* logits_out, float* z_loss_out,
                        void* ws, size_t ws_bytes, void* stream) {
@@ -273,8 +276,8 @@ moe_status moe_forward(const moe_config* cfg, const void* x, const float* W_r,
     void* x_perm = at<void>(ws, L.x_perm);
     float* y_perm = at<float>(ws, L.y_perm);
     chain_begin();
-    cudaError_t e = launch_route(c, x, W_r, logit_bias, nullptr, logits_out, idx, w, expert_counts,
-                                 aux_out, z_loss_out, ws, L, true, s);
+    cudaError_t e = launch_route(c, x, W_r, logit_bias, logit_noise, nullptr, logits_out, idx, w,
+                                 expert_counts, aux_out, z_loss_out, ws, L, true, s);
     if (e == cudaSuccess)
         e = launch_scan_permute(c, x, idx, w, L.route.tokens * c.k, L.route.blocks, offsets,
                                 slot_of, perm_token, perm_w, x_perm, ws, L,

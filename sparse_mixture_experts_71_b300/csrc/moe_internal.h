@@ -147,7 +147,8 @@ template <typename T> __host__ __device__ inline T* at(void* base, size_t off) {
 // Without fuse_count the router also runs its one-block finishing kernel
 // (loss, per-expert counts); with it the caller leaves that to the scan.
 cudaError_t launch_route(const moe_config& c, const void* x, const float* W_r,
-                         const float* logit_bias, const float* logits_in, float* logits_out,
+                         const float* logit_bias, const float* logit_noise,
+                         const float* logits_in, float* logits_out,
                          int32_t* topk_idx, float* topk_w, int32_t* expert_counts,
                          float* aux_out, float* z_loss_out, void* ws, const WsLayout& L,
                          bool fuse_count, cudaStream_t s);

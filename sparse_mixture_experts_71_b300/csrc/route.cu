@@ -474,6 +474,7 @@ __global__ void __launch_bounds__(kThreads) route_tile_kernel(RouteArgs a) {
         for (int i = 0; i < PER_LANE; ++i) {
             const int e = lane + 32 * i;
             gv[i] = e < a.E ? lg[tok * Gm::LGS + e] : -FLT_MAX;
+            if (e < a.E && a.noise != nullptr) gv[i] += __ldg(a.noise + (size_t)t * a.E + e);
             if (e < a.E) {
                 m = fmaxf(m, gv[i]);
                 if (a.logits_out != nullptr) a.logits_out[(size_t)t * a.E + e] = gv[i];
@@ -673,12 +674,14 @@ RouteGeom route_geom(const moe_config& c) {
 }
 
 cudaError_t launch_route(const moe_config& c, const void* x, const float* W_r,
-                         const float* logit_bias, const float* logits_in, float* logits_out,
+                         const float* logit_bias, const float* logit_noise,
+                         const float* logits_in, float* logits_out,
                          int32_t* topk_idx, float* topk_w, int32_t* expert_counts,
                          float* aux_out, float* z_loss_out, void* ws, const WsLayout& L,
                          bool fuse_count, cudaStream_t s) {
     RouteArgs a;
     a.x = x; a.W_r = W_r; a.bias = logit_bias; a.logits_in = logits_in; a.logits_out = logits_out;
+    a.noise = logits_in != nullptr ? nullptr : logit_noise;  // logits_in replaces all terms
     a.topk_idx = topk_idx; a.topk_w = topk_w; a.expert_counts = expert_counts; a.aux_out = aux_out;
     a.hdr = at<DeviceHeader>(ws, L.header);
     a.counts = at<int32_t>(ws, L.counts);

@@ -19,6 +19,7 @@ struct RouteArgs {
     const void* x;
     const float* W_r;
     const float* bias;
+    const float* noise;   // [T][E] added to the logits (noisy gating) or null
     const float* logits_in;
     float* logits_out;
     int32_t* topk_idx;
@@ -114,6 +115,10 @@ __device__ __forceinline__ void token_epilogue(const RouteArgs& a, float* prow, 
 #pragma unroll
     for (int e = 0; e < EMAX; ++e) {
         g[e] = e < a.E ? prow[e] : -FLT_MAX;
+        if (a.noise != nullptr && e < a.E) {
+            g[e] += __ldg(a.noise + (size_t)t * a.E + e);
+            prow[e] = g[e];  // the logits used for routing (logits_out)
+        }
         m = fmaxf(m, g[e]);
     }
     // exp(g - m) is evaluated where it is needed rather than kept (one more

@@ -83,10 +83,12 @@ WORKLOADS: dict[str, Workload] = {
                  note="top-1, capacity drop in token order, Zipf-skewed load"),
         Workload("decode-bf16-T64-d4096-F14336-E8-top2", 64, 4096, 14336, 8, 2,
                  note="decode-sized batch, HBM weight streaming"),
+        Workload("finegrained-bf16-T4096-d2048-F1024-E64-top6", 4096, 2048, 1024, 64, 6,
+                 note="fine-grained experts: many small experts, larger k"),
     )
 }
 
-TINY, MEDIUM, LARGE, SWITCH, DECODE = WORKLOADS.values()
+TINY, MEDIUM, LARGE, SWITCH, DECODE, FINEGRAINED = WORKLOADS.values()
 
 
 @dataclass
@@ -108,6 +110,13 @@ class Inputs:
         if a is None:
             return None
         return bf16_bits_to_f32(a) if a.dtype == np.uint16 else a
+
+
+def router_noise(T: int, E: int, sigma: float, seed: int) -> np.ndarray:
+    """(T, E) fp32 Gaussian noise of standard deviation sigma for noisy
+    gating, drawn from its own stream (the caller of the layer draws it)."""
+    g = np.random.Generator(np.random.PCG64(np.random.SeedSequence([seed, 7, 0])))
+    return (g.standard_normal((T, E)) * sigma).astype(np.float32)
 
 
 def f32_to_bf16_bits(a: np.ndarray) -> np.ndarray:

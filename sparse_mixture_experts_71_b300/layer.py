@@ -60,9 +60,10 @@ class MoELayer:
         return self._ws[T]
 
     def forward(self, x, y=None, aux=None, expert_counts=None, logits_out=None, z_loss=None,
-                stream=None):
+                logit_noise=None, stream=None):
         """(y, aux) for the token batch x (T, d); optional outputs (expert_counts,
-        logits_out, z_loss: the router z-loss, one fp32) are filled in place."""
+        logits_out, z_loss: the router z-loss, one fp32) are filled in place;
+        logit_noise (T, E fp32) is added to the router logits (noisy gating)."""
         T = x.shape[0]
         if y is None:
             y = torch.empty_like(x)
@@ -71,7 +72,7 @@ class MoELayer:
         B.forward(self.config(T), x, self.W_r, self.W1, self.b1, self.W2, self.b2, y,
                   self.workspace(T), logit_bias=self.logit_bias, aux_out=aux,
                   expert_counts=expert_counts, logits_out=logits_out, z_loss_out=z_loss,
-                  stream=stream)
+                  logit_noise=logit_noise, stream=stream)
         return y, aux
 
     __call__ = forward

@@ -66,7 +66,7 @@ class GpuRun:
         self.ws = B.workspace(self.cfg)
         self.stream = stream
 
-    def staged(self, logits_in=None):
+    def staged(self, logits_in=None, noise=None):
         wl, D, T, k, E = self.wl, self.dev, self.wl.T, self.wl.k, self.wl.E
         dt = D["x"].dtype
         cuda = D["x"].device
@@ -80,7 +80,7 @@ class GpuRun:
         r["z"] = torch.full((1,), -1.0, dtype=torch.float32, device=cuda)
         B.route(self.cfg, D["x"], D["W_r"], r["idx"], r["w"], self.ws, logit_bias=D["logit_bias"],
                 logits_in=logits_in, logits_out=r["logits"], expert_counts=r["counts"],
-                aux_out=r["aux"], z_loss_out=r["z"], stream=self.stream)
+                aux_out=r["aux"], z_loss_out=r["z"], logit_noise=noise, stream=self.stream)
         r["offsets"] = torch.empty(E + 1, dtype=torch.int32, device=cuda)
         r["slot_of"] = torch.empty((T, k), dtype=torch.int32, device=cuda)
         r["perm_token"] = torch.full((max(n, 1),), -7, dtype=torch.int32, device=cuda)
@@ -96,7 +96,7 @@ class GpuRun:
         torch.cuda.synchronize()
         return r
 
-    def forward(self):
+    def forward(self, noise=None):
         D, wl = self.dev, self.wl
         y = torch.empty_like(D["x"])
         aux = torch.empty(1, dtype=torch.float32, device=y.device)
@@ -105,7 +105,7 @@ class GpuRun:
         z = torch.full((1,), -1.0, dtype=torch.float32, device=y.device)
         B.forward(self.cfg, D["x"], D["W_r"], D["W1"], D["b1"], D["W2"], D["b2"], y, self.ws,
                   logit_bias=D["logit_bias"], aux_out=aux, expert_counts=counts,
-                  logits_out=logits, z_loss_out=z, stream=self.stream)
+                  logits_out=logits, z_loss_out=z, logit_noise=noise, stream=self.stream)
         torch.cuda.synchronize()
         return dict(y=y, aux=aux, counts=counts, logits=logits, z=z)
 

@@ -64,7 +64,7 @@ FAKE = 1 << 20  # a 256-aligned address that is never dereferenced (calls fail f
 def test_forward_rejects_bad_config(cfg, status):
     lib = B.load()
     ref = ctypes.byref(cfg) if cfg is not None else None
-    st = lib.moe_forward(ref, FAKE, FAKE, None, FAKE, FAKE, FAKE, FAKE, FAKE, None, None, None,
+    st = lib.moe_forward(ref, FAKE, FAKE, None, None, FAKE, FAKE, FAKE, FAKE, FAKE, None, None, None,
                          None, FAKE, 1 << 40, None)
     assert st == status
 
@@ -75,17 +75,17 @@ def test_calls_reject_null_misaligned_and_small_workspace():
     cr = ctypes.byref(c)
     need = B.workspace_size(c)
     # null required pointer
-    assert lib.moe_forward(cr, None, FAKE, None, FAKE, FAKE, FAKE, FAKE, FAKE, None, None, None,
+    assert lib.moe_forward(cr, None, FAKE, None, None, FAKE, FAKE, FAKE, FAKE, FAKE, None, None, None,
                            None, FAKE, need, None) == 1
     # misaligned x
-    assert lib.moe_forward(cr, FAKE + 8, FAKE, None, FAKE, FAKE, FAKE, FAKE, FAKE, None, None,
+    assert lib.moe_forward(cr, FAKE + 8, FAKE, None, None, FAKE, FAKE, FAKE, FAKE, FAKE, None, None,
                            None, None, FAKE, need, None) == 2
     # workspace too small / misaligned
-    assert lib.moe_forward(cr, FAKE, FAKE, None, FAKE, FAKE, FAKE, FAKE, FAKE, None, None, None,
+    assert lib.moe_forward(cr, FAKE, FAKE, None, None, FAKE, FAKE, FAKE, FAKE, FAKE, None, None, None,
                            None, FAKE, need - 1, None) == 3
-    assert lib.moe_forward(cr, FAKE, FAKE, None, FAKE, FAKE, FAKE, FAKE, FAKE, None, None, None,
+    assert lib.moe_forward(cr, FAKE, FAKE, None, None, FAKE, FAKE, FAKE, FAKE, FAKE, None, None, None,
                            None, FAKE + 16, need, None) == 3
-    assert lib.moe_route(cr, FAKE, FAKE, None, None, None, None, FAKE, None, None, None, FAKE,
+    assert lib.moe_route(cr, FAKE, FAKE, None, None, None, None, None, FAKE, None, None, None, FAKE,
                          need, None) == 1
     assert lib.moe_dispatch(cr, FAKE, FAKE, None, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, need,
                             None) == 1  # perm_w without topk_w

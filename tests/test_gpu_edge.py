@@ -5,6 +5,7 @@ import numpy as np
 import pytest
 import torch
 
+from oracle import moe_oracle as O
 from parity import GpuRun, assert_y_close, oracle_on, to_np
 from sparse_mixture_experts_71_b300 import binding as B
 from sparse_mixture_experts_71_b300 import inputs as I
@@ -168,3 +169,33 @@ def test_stalled_pipeline_wait_reports_time_out_and_context_survives():
     r = run.staged()
     _check(wl, inp, r)
     assert B.get_device_error(run.ws)[0] == 0
+
+
+NOISY = [
+    # name, T, d, F, E, k, dtype: one case per router kernel
+    ("noise-mma", 2048, 256, 256, 8, 2, "bf16"),    # mma.sync router (E <= 16)
+    ("noise-tc", 2048, 256, 256, 40, 2, "bf16"),    # tcgen05 router (16 < E <= 64)
+    ("noise-warp", 300, 64, 64, 8, 2, "f32"),       # warp router
+    ("noise-tile", 200, 64, 64, 100, 3, "bf16"),    # tile router (E > 64)
+]
+
+
+@pytest.mark.parametrize("case", NOISY, ids=[c[0] for c in NOISY])
+def test_noisy_gating(case):
+    """Caller-drawn noise added to the router logits (noisy gating): the
+    logits used for routing match the oracle's x W_r + noise, routing from
+    them is bit-exact, and forward equals the staged calls."""
+    name, T, d, F, E, k, dt = case
+    wl = _wl(name, T, d, F, E, k, dt, None, True)
+    inp = I.make_inputs(wl, seed=12)
+    noise_np = I.router_noise(T, E, 0.5, seed=3)
+    noise = torch.from_numpy(noise_np).cuda()
+    run = GpuRun(wl, inp)
+    r = run.staged(noise=noise)
+    g = to_np(r["logits"])
+    want = O.router_logits(inp.as_f32("x"), inp.W_r, None, noise_np)
+    assert np.max(np.abs(g - want)) <= 2e-5 * max(1.0, float(np.max(np.abs(want))))
+    assert np.max(np.abs(g - O.router_logits(inp.as_f32("x"), inp.W_r))) > 0.1  # noise applied
+    _check(wl, inp, r)
+    f = run.forward(noise=noise)
+    assert torch.equal(f["y"], r["y"]) and torch.equal(f["logits"], r["logits"])
