@@ -32,7 +32,10 @@ the combine and of the auxiliary loss did not survive extraction):
   token's router logits (the logits that enter the softmax, bias included);
 * noisy gating adds a caller-drawn (T, E) noise tensor to the router logits
   before the softmax and the top-k (the pages give no distribution; the
-  caller chooses it).
+  caller chooses it);
+* auxiliary-loss-free balancing moves the per-expert logit bias by a fixed
+  step toward balanced load after a batch: minus the step for an expert
+  above the mean assignment count, plus it below, unchanged at the mean.
 
 Parity: the routing, capacity, auxiliary-loss and combine functions are pinned
 by the pages' worked examples, closed forms and brute force (tests).  The
@@ -174,6 +177,23 @@ def aux_loss(probs, idx, E: int) -> float:
     f = np.bincount(idx[:, 0].astype(np.int64), minlength=E).astype(f64) / T
     P = np.asarray(probs, f64).mean(axis=0)
     return float(E * np.sum(f * P))
+
+
+def balance_bias_update(logit_bias, counts, gamma: float) -> np.ndarray:
+    """Auxiliary-loss-free balancing: move each expert's logit bias by gamma
+    toward balanced load.
+
+    [LECTURE] "The central problem: load balancing" (adjust per-expert bias
+    terms dynamically based on load).  An expert with more assignments than
+    the mean loses gamma, one with fewer gains gamma, one at the mean keeps
+    its bias.  Returns the new (E,) fp32 bias.
+    """
+    b = np.asarray(logit_bias, f64)
+    c = np.asarray(counts, np.int64)
+    E = c.shape[0]
+    total = int(c.sum())
+    step = np.where(c * E > total, -1.0, np.where(c * E < total, 1.0, 0.0))
+    return (b + gamma * step).astype(np.float32)
 
 
 def router_z_loss(logits) -> float:

@@ -131,6 +131,39 @@ def test_softmax_matches_torch():
     np.testing.assert_allclose(O.softmax(g), want, rtol=1e-13, atol=0)
 
 
+# ---------------------------------------------------------- bias balancing pins
+
+def test_balance_bias_update_by_hand():
+    """Loads 10/2/2/2 (mean 4): the overloaded expert's bias drops by the step,
+    the others rise by it; loads at the mean keep their bias."""
+    b = np.array([0.5, -1.0, 0.0, 2.0], np.float32)
+    np.testing.assert_array_equal(O.balance_bias_update(b, [10, 2, 2, 2], 0.25),
+                                  np.array([0.25, -0.75, 0.25, 2.25], np.float32))
+    np.testing.assert_array_equal(O.balance_bias_update(b, [4, 4, 4, 4], 0.25), b)
+    np.testing.assert_array_equal(O.balance_bias_update(b, [6, 4, 2, 4], 1.0),
+                                  np.array([-0.5, -1.0, 1.0, 2.0], np.float32))
+
+
+def test_balance_bias_updates_even_out_a_skewed_router():
+    """Repeated updates on a router skewed by a Zipf-like logit offset bring
+    the top-1 loads toward balance (the purpose of the mechanism)."""
+    g = np.random.default_rng(21)
+    T, d, E = 2048, 32, 8
+    x, W = g.standard_normal((T, d)), g.standard_normal((E, d)) * 0.05
+    skew = -1.5 * np.log(np.arange(1, E + 1))
+    b = np.zeros(E, np.float32)
+    def imbalance(bias):
+        idx = O.top_k(O.router_logits(x, W, skew + bias), 1)
+        c = np.bincount(idx[:, 0], minlength=E)
+        return c, c.max() / (T / E)
+    c0, first = imbalance(b)
+    for _ in range(60):
+        c, _ = imbalance(b)
+        b = O.balance_bias_update(b, c, 0.05)
+    _, last = imbalance(b)
+    assert first > 3.0 and last < 1.5
+
+
 # ---------------------------------------------------------- noisy gating pins
 
 def test_noise_equal_to_a_bias_row_is_the_bias_and_zero_noise_is_none():
