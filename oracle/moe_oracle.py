@@ -119,13 +119,14 @@ def expert_capacity(capacity_factor: float, T: int, E: int) -> int:
     return int(math.ceil(capacity_factor * T / E))
 
 
-def capacity_keep(idx, E: int, capacity: int | None) -> np.ndarray:
+def capacity_keep(idx, E: int, capacity: int | None, n_shared: int = 0) -> np.ndarray:
     """Which assignments survive the per-expert capacity cap.
 
     [LECTURE] "The central problem: load balancing" (overflow tokens are
     dropped); [GLOSSARY] expert capacity.  Assignments are visited in token
     order, then slot order; each expert keeps its first ``capacity``.
-    ``capacity=None`` keeps everything.  Returns (T, k) bool.
+    ``capacity=None`` keeps everything.  Shared experts (ids below
+    ``n_shared``, always active) are not capped.  Returns (T, k) bool.
     """
     idx = np.asarray(idx)
     T, k = idx.shape
@@ -136,6 +137,8 @@ def capacity_keep(idx, E: int, capacity: int | None) -> np.ndarray:
     for t in range(T):
         for j in range(k):
             e = int(idx[t, j])
+            if e < n_shared:
+                continue
             if taken[e] < capacity:
                 taken[e] += 1
             else:
@@ -264,7 +267,8 @@ class OracleResult:
 
 def moe_forward(x, W_r, W1, b1, W2, b2, k: int, renormalize: bool = True,
                 capacity: int | None = None, logit_bias=None, logits=None,
-                tokens=None, layout: bool = True, logit_noise=None) -> OracleResult:
+                tokens=None, layout: bool = True, logit_noise=None,
+                n_shared: int = 0) -> OracleResult:
     """The MoE layer forward pass, looping over experts.
 
     [LECTURE] "The MoE layer": router logits and softmax, top-k selection,
@@ -278,17 +282,30 @@ def moe_forward(x, W_r, W1, b1, W2, b2, k: int, renormalize: bool = True,
     identical logits).  ``tokens`` restricts the expert computation (not the
     routing, cap or loss, which always cover the whole batch) to a subset of
     token rows; ``y`` then holds those rows in that order.
+
+    ``n_shared`` > 0: experts 0 .. n_shared-1 of the E in W1..b2 are shared
+    ([LECTURE] "Design variations": always active for every token, weight 1,
+    never capped); the router (W_r with E - n_shared rows, the logits, the
+    softmax, the top-k, the loss) covers the routed experts n_shared .. E-1.
+    idx, w and kept then have k + n_shared columns: the k routed choices, then
+    the shared experts.
     """
     x = np.asarray(x)
     T, d = x.shape
-    E = np.asarray(W_r).shape[0]
     if logits is None:
         logits = router_logits(x, W_r, logit_bias, logit_noise)
     logits = np.asarray(logits, np.float32)
+    E_r = logits.shape[1]
+    E = E_r + n_shared
     probs = softmax(logits)
-    idx = top_k(logits, k)
-    w = gate_weights(probs, idx, renormalize)
-    kept = capacity_keep(idx, E, capacity)
+    idx_r = top_k(logits, k)
+    w = gate_weights(probs, idx_r, renormalize)
+    aux = aux_loss(probs, idx_r, E_r)
+    idx = idx_r + n_shared
+    if n_shared:
+        idx = np.concatenate([idx, np.tile(np.arange(n_shared, dtype=idx.dtype), (T, 1))], 1)
+        w = np.concatenate([w, np.ones((T, n_shared))], 1)
+    kept = capacity_keep(idx, E, capacity, n_shared)
     if layout:
         counts, kept_count, offsets, slot_of, perm_token = dispatch_layout(idx, kept, E)
     else:
@@ -304,6 +321,5 @@ def moe_forward(x, W_r, W1, b1, W2, b2, k: int, renormalize: bool = True,
         out = expert_ffn(x[tokens[rows]], W1[e], b1[e], W2[e], b2[e])
         we = (sub_w * sel)[rows].sum(axis=1)
         y[rows] += we[:, None] * out
-    aux = aux_loss(probs, idx, E)
     return OracleResult(logits, probs, idx, w, kept, counts, kept_count, offsets, slot_of,
                         perm_token, aux, y, tokens, router_z_loss(logits))

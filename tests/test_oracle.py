@@ -384,6 +384,38 @@ def test_forward_equals_dense_masked_brute_force(k, renorm, cap):
     np.testing.assert_allclose(r.y, want, rtol=1e-12, atol=1e-12)
 
 
+def test_shared_experts_add_their_dense_ffn():
+    """n_shared experts always active ("Design variations": shared experts):
+    y = the routed layer over experts n_shared.. (the pinned path above) +
+    sum over the shared experts of their plain FFN (torch, fp64), and the
+    routing, weights and loss are those of the routed layer alone."""
+    L = _rand_layer(T=17, d=8, F=12, E=5, seed=31)
+    W_r = L["W_r"][:3]  # router over the 3 routed experts
+    both = dict(L, W_r=W_r)
+    r = O.moe_forward(**both, k=2, renormalize=True, n_shared=2)
+    routed = O.moe_forward(L["x"], W_r, L["W1"][2:], L["b1"][2:], L["W2"][2:], L["b2"][2:],
+                           k=2, renormalize=True)
+    t = {n: torch.from_numpy(v) for n, v in L.items()}
+    shared = sum(TF.linear(TF.gelu(TF.linear(t["x"], t["W1"][e], t["b1"][e])), t["W2"][e],
+                           t["b2"][e]) for e in range(2))
+    np.testing.assert_allclose(r.y, routed.y + shared.numpy(), rtol=1e-12, atol=1e-12)
+    assert np.array_equal(r.idx[:, :2], routed.idx + 2)
+    assert np.array_equal(r.idx[:, 2:], np.tile([0, 1], (17, 1)))
+    assert np.array_equal(r.w[:, 2:], np.ones((17, 2))) and np.array_equal(r.w[:, :2], routed.w)
+    assert r.aux == routed.aux and r.z_loss == routed.z_loss
+    assert np.array_equal(r.counts, np.concatenate([[17, 17], routed.counts]))
+
+
+def test_shared_experts_are_not_capped():
+    """Capacity 1: each routed expert keeps one assignment, the shared
+    expert keeps every token."""
+    L = _rand_layer(T=10, d=6, F=5, E=4, seed=32)
+    r = O.moe_forward(**dict(L, W_r=L["W_r"][:3]), k=1, renormalize=False, capacity=1,
+                      n_shared=1)
+    assert r.kept[:, 1].all() and r.kept_count[0] == 10
+    assert np.all(r.kept_count[1:] <= 1) and r.kept[:, 0].sum() == r.kept_count[1:].sum()
+
+
 def test_single_expert_is_dense_ffn():
     """E = 1, k = 1, renormalised -> the plain Linear-GELU-Linear FFN
     (torch.nn.functional on CPU, fp64)."""
