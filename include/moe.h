@@ -76,7 +76,22 @@ typedef struct moe_config {
     int32_t dtype;       /* moe_dtype of x, W1, b1, W2, b2, y */
     int32_t capacity;    /* < 0: no cap; >= 0: kept assignments per expert at most */
     int32_t renormalize; /* 1: w = p_sel / sum(p_sel); 0: w = p_sel */
+    int32_t n_shared;    /* shared experts, 0 .. E-1 (see below); 0 for a plain layer */
 } moe_config;
+
+/*
+ * Shared experts ("Design variations": one or more experts always active):
+ * with n_shared > 0, experts 0 .. n_shared-1 of the E in W1, b1, W2, b2 are
+ * applied to every token with weight 1 and are never capped; the router
+ * covers the other E - n_shared experts (W_r, logit_bias, logit_noise,
+ * logits_in and logits_out have E - n_shared rows / columns; softmax, top-k,
+ * the auxiliary loss and the z-loss are over them) and picks k of them.
+ * Every per-assignment array below then has K = k + n_shared columns per
+ * token ([T][K]: topk_idx, topk_w, slot_of; T*K: perm_token, perm_w, x_perm,
+ * y_perm): the k routed choices (expert ids n_shared .. E-1, best first),
+ * then the shared experts 0 .. n_shared-1.  k + n_shared <= 8.  With
+ * n_shared = 0, K = k and everything below reads as written.
+ */
 
 /* Bytes of workspace any call below needs for this configuration. */
 size_t moe_workspace_size(const moe_config* cfg);
@@ -205,6 +220,20 @@ moe_status moe_get_device_error(void* ws, void* stream, int32_t* code, int32_t* 
 moe_status moe_dispatch_noalloc(const moe_config* cfg, const void* x, const int32_t* topk_idx,
                                 const float* topk_w, int32_t* offsets, int32_t* slot_of,
                                 int32_t* perm_token, float* perm_w, void* x_perm, void* stream);
+
+/*
+ * Auxiliary-loss-free balancing ("The central problem: load balancing":
+ * adjust per-expert bias terms dynamically based on load): after a batch,
+ * moves each expert's router logit bias by `step` toward balanced load -
+ *   logit_bias[e] -= step  if expert_counts[e] > mean count,
+ *   logit_bias[e] += step  if expert_counts[e] < mean count,
+ * unchanged at the mean (mean = sum of the E counts / E, compared exactly in
+ * integers).  expert_counts [E] int32 as written by moe_route/moe_forward;
+ * logit_bias [E] fp32, updated in place, for the next call's logit_bias.
+ * cfg supplies E.  No workspace.
+ */
+moe_status moe_update_balance_bias(const moe_config* cfg, const int32_t* expert_counts,
+                                   float* logit_bias, float step, void* stream);
 
 /*
  * Diagnostics: number of CUDA kernels libmoe has enqueued in this process

@@ -23,13 +23,15 @@ STATUS = {0: "ok", 1: "invalid argument", 2: "misaligned pointer or row length",
 
 EXPORTED = ("moe_workspace_size", "moe_status_string", "moe_route", "moe_dispatch",
             "moe_expert_ffn", "moe_combine", "moe_forward", "moe_get_device_error",
-            "moe_launch_count", "moe_dispatch_noalloc", "moe_check_wait_timeout")
+            "moe_launch_count", "moe_dispatch_noalloc", "moe_check_wait_timeout",
+            "moe_update_balance_bias")
 
 
 class MoeConfig(ctypes.Structure):
     _fields_ = [("T", ctypes.c_int32), ("d", ctypes.c_int32), ("d_ff", ctypes.c_int32),
                 ("E", ctypes.c_int32), ("k", ctypes.c_int32), ("dtype", ctypes.c_int32),
-                ("capacity", ctypes.c_int32), ("renormalize", ctypes.c_int32)]
+                ("capacity", ctypes.c_int32), ("renormalize", ctypes.c_int32),
+                ("n_shared", ctypes.c_int32)]
 
 
 class MoeError(RuntimeError):
@@ -71,13 +73,17 @@ def load() -> ctypes.CDLL:
         lib.moe_launch_count.argtypes = []
         lib.moe_check_wait_timeout.restype = ctypes.c_int
         lib.moe_check_wait_timeout.argtypes = [_P, ctypes.c_uint64, _P]
+        lib.moe_update_balance_bias.restype = ctypes.c_int
+        lib.moe_update_balance_bias.argtypes = [cfgp, _P, _P, ctypes.c_float, _P]
         _lib = lib
     return _lib
 
 
-def config(T, d, d_ff, E, k, dtype="bf16", capacity=None, renormalize=True) -> MoeConfig:
+def config(T, d, d_ff, E, k, dtype="bf16", capacity=None, renormalize=True,
+           n_shared=0) -> MoeConfig:
     return MoeConfig(T, d, d_ff, E, k, MOE_BF16 if dtype == "bf16" else MOE_F32,
-                     -1 if capacity is None else int(capacity), 1 if renormalize else 0)
+                     -1 if capacity is None else int(capacity), 1 if renormalize else 0,
+                     int(n_shared))
 
 
 def _ptr(t):
@@ -160,6 +166,14 @@ def forward(cfg, x, W_r, W1, b1, W2, b2, y, ws, logit_bias=None, aux_out=None,
 def launch_count() -> int:
     """Kernels libmoe has enqueued in this process (diagnostics)."""
     return int(load().moe_launch_count())
+
+
+def update_balance_bias(cfg, expert_counts, logit_bias, step: float, stream=None) -> None:
+    """Auxiliary-loss-free balancing step on logit_bias (in place) from the
+    per-expert assignment counts of a routed batch."""
+    _check("moe_update_balance_bias", load().moe_update_balance_bias(
+        ctypes.byref(cfg), _ptr(expert_counts), _ptr(logit_bias), ctypes.c_float(step),
+        _stream(stream)))
 
 
 def check_wait_timeout(ws, timeout_ns: int, stream=None) -> None:

@@ -13,8 +13,8 @@
 //           per-warp histograms; no atomics, so the result is exact).
 //   scan    one block: for every (block, expert) the number of assignments to
 //           that expert in earlier blocks, the per-expert totals, the kept
-//           counts min(total, capacity) and their exclusive prefix sum
-//           (offsets).
+//           counts min(total, capacity) (shared experts: total) and their
+//           exclusive prefix sum (offsets).
 //   permute one warp per assignment: rank = base + local rank; kept iff rank <
 //           capacity; row = offsets[e] + rank; writes slot_of / perm_token /
 //           perm_w and copies the token's row with 16-byte vector accesses.
@@ -73,7 +73,7 @@ __global__ void __launch_bounds__(kCountBlock) count_kernel(const int32_t* __res
 // With loss.blk_p set it also finishes the router's statistics (loss and
 // per-expert counts), which removes a launch from the layer's forward pass.
 __global__ void __launch_bounds__(1024) scan_kernel(const int32_t* __restrict__ blk_hist,
-                                                    int nblk, int E, int capacity,
+                                                    int nblk, int E, int capacity, int n_shared,
                                                     int32_t* __restrict__ blk_base,
                                                     int32_t* __restrict__ offsets, LossArgs loss) {
     __shared__ int part_sum[1024];
@@ -124,7 +124,7 @@ __global__ void __launch_bounds__(1024) scan_kernel(const int32_t* __restrict__ 
         for (int x0 = 0; x0 < E; x0 += 32) {
             const int x = x0 + lane;
             const int tot = x < E ? s_total[x] : 0;
-            const int kept = capacity < 0 ? tot : min(tot, capacity);
+            const int kept = capacity < 0 || x < n_shared ? tot : min(tot, capacity);
             int incl = kept;
 #pragma unroll
             for (int o = 1; o < 32; o <<= 1) {
@@ -142,7 +142,7 @@ template <typename TX>
 __global__ void __launch_bounds__(256) permute_kernel(
     const TX* __restrict__ x, const int32_t* __restrict__ idx, const float* __restrict__ topk_w,
     const int32_t* __restrict__ local_rank, const int32_t* __restrict__ blk_base,
-    const int32_t* __restrict__ offsets, int n, int k, int E, int d, int capacity,
+    const int32_t* __restrict__ offsets, int n, int k, int E, int d, int capacity, int n_shared,
     int asg_per_block, int32_t* __restrict__ slot_of, int32_t* __restrict__ perm_token, float* __restrict__ perm_w,
     TX* __restrict__ x_perm) {
     pdl_wait();
@@ -156,7 +156,7 @@ __global__ void __launch_bounds__(256) permute_kernel(
         if (r_local >= 0) {
             const int e = __ldg(idx + a);
             const int r = __ldg(blk_base + (size_t)(a / asg_per_block) * E + e) + r_local;
-            if (capacity < 0 || r < capacity) slot = __ldg(offsets + e) + r;
+            if (capacity < 0 || r < capacity || e < n_shared) slot = __ldg(offsets + e) + r;
         }
         const int t = a / k;
         if (lane == 0) {
@@ -200,8 +200,8 @@ cudaError_t launch_scan_permute(const moe_config& c, const void* x, const int32_
     int32_t* blk_base = at<int32_t>(ws, L.blk_base);
     int32_t* local_rank = at<int32_t>(ws, L.local_rank);
     cudaError_t e = launch_kernel(scan_kernel, dim3(1), dim3(1024), 0, s, 1, false,
-                                  (const int32_t*)blk_hist, hist_blocks, c.E, c.capacity, blk_base,
-                                  offsets, loss);
+                                  (const int32_t*)blk_hist, hist_blocks, c.E, c.capacity,
+                                  c.n_shared, blk_base, offsets, loss);
     if (e != cudaSuccess || n == 0) return e;
     int blocks = (n + 7) / 8;
     blocks = blocks < num_sms() * 8 ? blocks : num_sms() * 8;
@@ -210,12 +210,13 @@ cudaError_t launch_scan_permute(const moe_config& c, const void* x, const int32_
                              reinterpret_cast<const __nv_bfloat16*>(x), topk_idx, topk_w,
                              (const int32_t*)local_rank, (const int32_t*)blk_base,
                              (const int32_t*)offsets, n, c.k, c.E, c.d, c.capacity,
-                             asg_per_block, slot_of, perm_token, perm_w,
+                             c.n_shared, asg_per_block, slot_of, perm_token, perm_w,
                              reinterpret_cast<__nv_bfloat16*>(x_perm));
     return launch_kernel(permute_kernel<float>, dim3(blocks), dim3(256), 0, s, 1, false,
                          reinterpret_cast<const float*>(x), topk_idx, topk_w,
                          (const int32_t*)local_rank, (const int32_t*)blk_base,
-                         (const int32_t*)offsets, n, c.k, c.E, c.d, c.capacity, asg_per_block,
+                         (const int32_t*)offsets, n, c.k, c.E, c.d, c.capacity, c.n_shared,
+                         asg_per_block,
                          slot_of, perm_token, perm_w, reinterpret_cast<float*>(x_perm));
 }
 

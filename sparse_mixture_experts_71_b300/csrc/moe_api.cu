@@ -57,10 +57,11 @@ moe_status check_config(const moe_config* c) {
     if (c->T < 0 || c->d <= 0 || c->d_ff <= 0 || c->E <= 0 || c->k <= 0) return MOE_ERR_INVALID_ARG;
     if (c->dtype != MOE_F32 && c->dtype != MOE_BF16) return MOE_ERR_INVALID_ARG;
     if (c->renormalize != 0 && c->renormalize != 1) return MOE_ERR_INVALID_ARG;
-    if (c->k > c->E) return MOE_ERR_INVALID_ARG;
-    if (c->E > kMaxExperts || c->k > kMaxTopK) return MOE_ERR_UNSUPPORTED;
+    if (c->n_shared < 0 || c->n_shared >= c->E) return MOE_ERR_INVALID_ARG;
+    if (c->k > c->E - c->n_shared) return MOE_ERR_INVALID_ARG;
+    if (c->E > kMaxExperts || c->k + c->n_shared > kMaxTopK) return MOE_ERR_UNSUPPORTED;
     if (c->d % 8 != 0 || c->d_ff % 8 != 0) return MOE_ERR_ALIGNMENT;
-    if ((int64_t)c->T * c->k > (int64_t)INT32_MAX / 2) return MOE_ERR_UNSUPPORTED;
+    if ((int64_t)c->T * (c->k + c->n_shared) > (int64_t)INT32_MAX / 2) return MOE_ERR_UNSUPPORTED;
     return MOE_OK;
 }
 
@@ -94,12 +95,16 @@ int64_t max_segment(const moe_config& c) {
 
 WsLayout ws_layout(const moe_config& c) {
     WsLayout L{};
-    const int64_t n = (int64_t)c.T * c.k;
-    L.route = route_geom(c);
+    const moe_config cr = routed_config(c);
+    const int64_t n = (int64_t)c.T * (c.k + c.n_shared);
+    L.route = route_geom(cr);
     L.count_blocks = (int)((n + kCountBlock - 1) / kCountBlock);
     L.hist_blocks = L.route.blocks > L.count_blocks ? L.route.blocks : L.count_blocks;
     L.rows = n;
-    if (c.capacity >= 0 && (int64_t)c.E * c.capacity < L.rows) L.rows = (int64_t)c.E * c.capacity;
+    if (c.capacity >= 0) {  // shared experts keep every token, routed ones at most capacity
+        const int64_t cap_rows = (int64_t)c.n_shared * c.T + (int64_t)cr.E * c.capacity;
+        if (cap_rows < L.rows) L.rows = cap_rows;
+    }
     const size_t es = elem_size(c);
     size_t o = 0;
     auto take = [&](size_t bytes) {
@@ -110,12 +115,15 @@ WsLayout ws_layout(const moe_config& c) {
     L.header = take(sizeof(DeviceHeader));
     L.counts = take(sizeof(int32_t) * c.E);
     L.top1 = take(sizeof(int32_t) * c.E);
-    L.blk_p = take(sizeof(float) * (size_t)L.route.blocks * c.E);
+    L.blk_p = take(sizeof(float) * (size_t)L.route.blocks * cr.E);
     L.blk_z = take(sizeof(float) * (size_t)L.route.blocks);
     L.blk_hist = take(sizeof(int32_t) * (size_t)L.hist_blocks * c.E);
     L.blk_base = take(sizeof(int32_t) * (size_t)L.hist_blocks * c.E);
     L.local_rank = take(sizeof(int32_t) * (size_t)n);
     L.wsplit = take(L.route.tc ? sizeof(uint16_t) * 3 * (size_t)L.route.epad * c.d : 0);
+    const size_t nr = c.n_shared > 0 ? (size_t)c.T * c.k : 0;
+    L.route_idx = take(sizeof(int32_t) * nr);
+    L.route_w = take(sizeof(float) * nr);
     L.topk_idx = take(sizeof(int32_t) * (size_t)n);
     L.topk_w = take(sizeof(float) * (size_t)n);
     L.offsets = take(sizeof(int32_t) * (size_t)(c.E + 1));
@@ -182,9 +190,20 @@ moe_status moe_route(const moe_config* cfg, const void* x, const float* W_r,
     if (logits_in == nullptr && (!aligned16(x) || !aligned16(W_r))) return MOE_ERR_ALIGNMENT;
     if ((st = check_ws(c, ws, ws_bytes, &L)) != MOE_OK) return st;
     chain_begin();
-    return from_cuda(launch_route(c, x, W_r, logit_bias, logit_noise, logits_in, logits_out,
-                                  topk_idx, topk_w, expert_counts, aux_out, z_loss_out, ws, L,
-                                  false, s));
+    if (c.n_shared == 0)
+        return from_cuda(launch_route(c, x, W_r, logit_bias, logit_noise, logits_in, logits_out,
+                                      topk_idx, topk_w, expert_counts, aux_out, z_loss_out, ws,
+                                      L, false, s));
+    // shared experts: route the routed experts into the workspace, then join
+    int32_t* idx_r = at<int32_t>(ws, L.route_idx);
+    float* w_r = at<float>(ws, L.route_w);
+    cudaError_t e = launch_route(routed_config(c), x, W_r, logit_bias, logit_noise, logits_in,
+                                 logits_out, idx_r, w_r, nullptr, aux_out, z_loss_out, ws, L,
+                                 false, s);
+    if (e == cudaSuccess)
+        e = launch_join_shared(c, idx_r, w_r, topk_idx, topk_w, at<int32_t>(ws, L.counts),
+                               expert_counts, s);
+    return from_cuda(e);
 }
 
 moe_status moe_dispatch(const moe_config* cfg, const void* x, const int32_t* topk_idx,
@@ -208,10 +227,11 @@ moe_status moe_dispatch(const moe_config* cfg, const void* x, const int32_t* top
     WsLayout L;
     if ((st = check_ws(c, ws, ws_bytes, &L)) != MOE_OK) return st;
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    const moe_config cd = dispatch_config(c);
     chain_begin();
-    cudaError_t e = launch_count(c, topk_idx, ws, L, s);
+    cudaError_t e = launch_count(cd, topk_idx, ws, L, s);
     if (e == cudaSuccess)
-        e = launch_scan_permute(c, x, topk_idx, topk_w, kCountBlock, L.count_blocks, offsets,
+        e = launch_scan_permute(cd, x, topk_idx, topk_w, kCountBlock, L.count_blocks, offsets,
                                 slot_of, perm_token, perm_w, x_perm, ws, L, LossArgs{}, s);
     return from_cuda(e);
 }
@@ -231,8 +251,9 @@ moe_status moe_expert_ffn(const moe_config* cfg, const void* x_perm, const int32
         return MOE_ERR_ALIGNMENT;
     WsLayout L;
     if ((st = check_ws(c, ws, ws_bytes, &L)) != MOE_OK) return st;
+    const moe_config cd = dispatch_config(c);
     chain_begin();
-    return from_cuda(launch_expert_ffn(c, x_perm, (int64_t)c.T * c.k, offsets, W1, b1, W2, b2,
+    return from_cuda(launch_expert_ffn(cd, x_perm, (int64_t)cd.T * cd.k, offsets, W1, b1, W2, b2,
                                        perm_w, y_perm, ws, L,
                                        reinterpret_cast<cudaStream_t>(stream)));
 }
@@ -246,7 +267,8 @@ moe_status moe_combine(const moe_config* cfg, const float* y_perm, const int32_t
     if (y_perm == nullptr || slot_of == nullptr || y == nullptr) return MOE_ERR_INVALID_ARG;
     if (!aligned16(y_perm) || !aligned16(y)) return MOE_ERR_ALIGNMENT;
     chain_begin();
-    return from_cuda(launch_combine(c, y_perm, slot_of, y, reinterpret_cast<cudaStream_t>(stream)));
+    return from_cuda(launch_combine(dispatch_config(c), y_perm, slot_of, y,
+                                    reinterpret_cast<cudaStream_t>(stream)));
 }
 
 moe_status moe_forward(const moe_config* cfg, const void* x, const float* W_r,
@@ -275,19 +297,47 @@ moe_status moe_forward(const moe_config* cfg, const void* x, const float* W_r,
     float* perm_w = at<float>(ws, L.perm_w);
     void* x_perm = at<void>(ws, L.x_perm);
     float* y_perm = at<float>(ws, L.y_perm);
+    const moe_config cd = dispatch_config(c);
     chain_begin();
-    cudaError_t e = launch_route(c, x, W_r, logit_bias, logit_noise, nullptr, logits_out, idx, w,
-                                 expert_counts, aux_out, z_loss_out, ws, L, true, s);
+    cudaError_t e;
+    if (c.n_shared == 0) {
+        // the router also counts (blk_hist, local_rank) and the scan finishes its loss
+        e = launch_route(c, x, W_r, logit_bias, logit_noise, nullptr, logits_out, idx, w,
+                         expert_counts, aux_out, z_loss_out, ws, L, true, s);
+        if (e == cudaSuccess)
+            e = launch_scan_permute(c, x, idx, w, L.route.tokens * c.k, L.route.blocks, offsets,
+                                    slot_of, perm_token, perm_w, x_perm, ws, L,
+                                    route_loss_args(c, ws, L, expert_counts, aux_out, z_loss_out),
+                                    s);
+    } else {
+        // shared experts: route the routed experts, join the shared ones, count all
+        int32_t* idx_r = at<int32_t>(ws, L.route_idx);
+        float* w_r = at<float>(ws, L.route_w);
+        e = launch_route(routed_config(c), x, W_r, logit_bias, logit_noise, nullptr, logits_out,
+                         idx_r, w_r, nullptr, aux_out, z_loss_out, ws, L, false, s);
+        if (e == cudaSuccess)
+            e = launch_join_shared(c, idx_r, w_r, idx, w, at<int32_t>(ws, L.counts),
+                                   expert_counts, s);
+        if (e == cudaSuccess) e = launch_count(cd, idx, ws, L, s);
+        if (e == cudaSuccess)
+            e = launch_scan_permute(cd, x, idx, w, kCountBlock, L.count_blocks, offsets, slot_of,
+                                    perm_token, perm_w, x_perm, ws, L, LossArgs{}, s);
+    }
     if (e == cudaSuccess)
-        e = launch_scan_permute(c, x, idx, w, L.route.tokens * c.k, L.route.blocks, offsets,
-                                slot_of, perm_token, perm_w, x_perm, ws, L,
-                                route_loss_args(c, ws, L, expert_counts, aux_out, z_loss_out),
-                                s);
-    if (e == cudaSuccess)
-        e = launch_expert_ffn(c, x_perm, L.rows, offsets, W1, b1, W2, b2, perm_w, y_perm, ws, L,
-                              s);
-    if (e == cudaSuccess) e = launch_combine(c, y_perm, slot_of, y, s);
+        e = launch_expert_ffn(cd, x_perm, L.rows, offsets, W1, b1, W2, b2, perm_w, y_perm, ws,
+                              L, s);
+    if (e == cudaSuccess) e = launch_combine(cd, y_perm, slot_of, y, s);
     return from_cuda(e);
+}
+
+moe_status moe_update_balance_bias(const moe_config* cfg, const int32_t* expert_counts,
+                                   float* logit_bias, float step, void* stream) {
+    moe_status st = check_config(cfg);
+    if (st != MOE_OK) return st;
+    if (expert_counts == nullptr || logit_bias == nullptr) return MOE_ERR_INVALID_ARG;
+    chain_begin();
+    return from_cuda(launch_balance_bias(*cfg, expert_counts, logit_bias, step,
+                                         reinterpret_cast<cudaStream_t>(stream)));
 }
 
 moe_status moe_check_wait_timeout(void* ws, uint64_t timeout_ns, void* stream) {

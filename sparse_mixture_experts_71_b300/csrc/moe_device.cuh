@@ -144,18 +144,21 @@ __device__ __forceinline__ void loss_and_counts(const LossArgs& l, float* s_part
         const float Tf = (float)l.T;
         l.aux_out[0] = (float)l.E * (s / Tf) / Tf;
     }
-    if (l.z_out != nullptr) {  // router z-loss: the block sums, 256 strided parts in order
+    if (l.z_out != nullptr) {  // router z-loss: block sums in 256 strided parts, then a fixed tree
         __syncthreads();
         if (tid < 256) {
             float v = 0.f;
             for (int b = tid; b < l.nblk; b += 256) v += __ldcg(l.blk_z + b);
-            s_part[tid] = v;
+#pragma unroll
+            for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+            if ((tid & 31) == 0) s_part[tid >> 5] = v;
         }
         __syncthreads();
-        if (tid == 0) {
-            float s = 0.f;
-            for (int i = 0; i < 256; ++i) s += s_part[i];
-            l.z_out[0] = s / (float)l.T;
+        if (tid < 32) {
+            float v = tid < 8 ? s_part[tid] : 0.f;
+#pragma unroll
+            for (int o = 4; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+            if (tid == 0) l.z_out[0] = v / (float)l.T;
         }
     }
 }

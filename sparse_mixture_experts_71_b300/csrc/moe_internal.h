@@ -24,6 +24,22 @@ static_assert(sizeof(DeviceHeader) == 256, "header is one 256-byte line");
 
 enum DeviceError : int32_t { kErrExpertRange = 1, kErrTimeout = 2 };
 
+// Shared experts: the router sees the routed experts only (E - n_shared of
+// them, k picks); dispatch, the expert GEMMs and the combine see all E
+// experts with K = k + n_shared assignments per token.  Both views equal the
+// caller's config when n_shared == 0.
+inline moe_config routed_config(const moe_config& c) {
+    moe_config r = c;
+    r.E = c.E - c.n_shared;
+    r.n_shared = 0;
+    return r;
+}
+inline moe_config dispatch_config(const moe_config& c) {
+    moe_config r = c;
+    r.k = c.k + c.n_shared;
+    return r;
+}
+
 // How the router kernel tiles the batch: `warp` kernel (E <= 32: one warp per
 // `tw` tokens, 8 warps per block) or `tile` kernel (SIMT GEMM tile).
 struct RouteGeom {
@@ -50,7 +66,9 @@ struct WsLayout {
     size_t blk_base;     // int32 [hist_blocks][E]
     size_t local_rank;   // int32 [T*k]
     size_t wsplit;       // bf16 [3][roundup(E, 8)][d] router weight parts (tensor-core router)
-    size_t topk_idx;     // int32 [T*k]     (moe_forward)
+    size_t route_idx;    // int32 [T*k] routed choices before the shared experts join (n_shared > 0)
+    size_t route_w;      // fp32  [T*k]
+    size_t topk_idx;     // int32 [T*K]     (moe_forward; K = k + n_shared)
     size_t topk_w;       // fp32  [T*k]     (moe_forward)
     size_t offsets;      // int32 [E+1]     (moe_forward)
     size_t slot_of;      // int32 [T*k]     (moe_forward)
@@ -152,6 +170,17 @@ cudaError_t launch_route(const moe_config& c, const void* x, const float* W_r,
                          int32_t* topk_idx, float* topk_w, int32_t* expert_counts,
                          float* aux_out, float* z_loss_out, void* ws, const WsLayout& L,
                          bool fuse_count, cudaStream_t s);
+
+// Shared experts: K = k + n_shared columns per token from the router's k
+// routed choices (ids offset by n_shared) followed by the shared experts with
+// weight 1, and the per-expert counts over all E experts (shared: T).
+cudaError_t launch_join_shared(const moe_config& c, const int32_t* idx_r, const float* w_r,
+                               int32_t* topk_idx, float* topk_w, const int32_t* counts_r,
+                               int32_t* expert_counts, cudaStream_t s);
+
+// Auxiliary-loss-free balancing step on the router logit bias.
+cudaError_t launch_balance_bias(const moe_config& c, const int32_t* counts, float* bias,
+                                float step, cudaStream_t s);
 
 // Counting kernel over topk_idx (granularity kCountBlock assignments).
 cudaError_t launch_count(const moe_config& c, const int32_t* topk_idx, void* ws,

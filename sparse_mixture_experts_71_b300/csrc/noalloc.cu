@@ -63,12 +63,14 @@ extern "C" moe_status moe_dispatch_noalloc(const moe_config* cfg, const void* x,
                                            void* stream) {
     if (cfg == nullptr) return MOE_ERR_INVALID_ARG;
     const moe_config& c = *cfg;
-    if (c.T < 0 || c.d <= 0 || c.d_ff <= 0 || c.E <= 0 || c.k <= 0 || c.k > c.E ||
-        (c.dtype != MOE_F32 && c.dtype != MOE_BF16) || (c.renormalize != 0 && c.renormalize != 1))
+    if (c.T < 0 || c.d <= 0 || c.d_ff <= 0 || c.E <= 0 || c.k <= 0 ||
+        (c.dtype != MOE_F32 && c.dtype != MOE_BF16) || (c.renormalize != 0 && c.renormalize != 1) ||
+        c.n_shared < 0 || c.n_shared >= c.E || c.k > c.E - c.n_shared)
         return MOE_ERR_INVALID_ARG;
-    if (c.E > kMaxExperts || c.k > kMaxTopK) return MOE_ERR_UNSUPPORTED;
+    if (c.E > kMaxExperts || c.k + c.n_shared > kMaxTopK) return MOE_ERR_UNSUPPORTED;
     if (c.d % 8 != 0 || c.d_ff % 8 != 0) return MOE_ERR_ALIGNMENT;
-    if ((int64_t)c.T * c.k > kNoAllocMaxAssignments) return MOE_ERR_UNSUPPORTED;  // scratch bound
+    const moe_config cd = dispatch_config(c);  // K = k + n_shared assignments per token
+    if ((int64_t)cd.T * cd.k > kNoAllocMaxAssignments) return MOE_ERR_UNSUPPORTED;  // scratch bound
     if (offsets == nullptr) return MOE_ERR_INVALID_ARG;
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
     if (c.T == 0) return cudaMemsetAsync(offsets, 0, sizeof(int32_t) * (c.E + 1), s) == cudaSuccess
@@ -92,9 +94,9 @@ extern "C" moe_status moe_dispatch_noalloc(const moe_config* cfg, const void* x,
     // else they read.
     if (cudaMemsetAsync(scratch, 0, sizeof(DeviceHeader), s) != cudaSuccess) return MOE_ERR_CUDA;
     chain_begin();  // the first kernel follows the memset
-    cudaError_t e = launch_count(c, topk_idx, scratch, L, s);
+    cudaError_t e = launch_count(cd, topk_idx, scratch, L, s);
     if (e == cudaSuccess)
-        e = launch_scan_permute(c, x, topk_idx, topk_w, kCountBlock, L.count_blocks, offsets,
+        e = launch_scan_permute(cd, x, topk_idx, topk_w, kCountBlock, L.count_blocks, offsets,
                                 slot_of, perm_token, perm_w, x_perm, scratch, L, LossArgs{}, s);
     return e == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;
 }

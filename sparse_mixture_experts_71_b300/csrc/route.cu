@@ -622,7 +622,72 @@ __global__ void __launch_bounds__(256) route_finish_kernel(LossArgs l) {
     loss_and_counts(l, s_part, s_d);
 }
 
+// Shared experts: token t's K = k + ns columns are its k routed choices (ids
+// offset by ns, weights as routed) and then experts 0 .. ns-1 with weight 1;
+// block 0 also writes the per-expert counts over all E experts (a shared
+// expert takes every token).
+__global__ void __launch_bounds__(256) join_shared_kernel(
+    const int32_t* __restrict__ idx_r, const float* __restrict__ w_r, int T, int k, int ns,
+    int32_t* __restrict__ idx, float* __restrict__ w, const int32_t* __restrict__ counts_r,
+    int32_t* __restrict__ expert_counts, int E) {
+    pdl_wait();
+    pdl_trigger();
+    const int K = k + ns;
+    for (int t = blockIdx.x * blockDim.x + threadIdx.x; t < T; t += gridDim.x * blockDim.x) {
+        for (int j = 0; j < k; ++j) {
+            idx[(size_t)t * K + j] = __ldg(idx_r + (size_t)t * k + j) + ns;
+            w[(size_t)t * K + j] = __ldg(w_r + (size_t)t * k + j);
+        }
+        for (int j = 0; j < ns; ++j) {
+            idx[(size_t)t * K + k + j] = j;
+            w[(size_t)t * K + k + j] = 1.0f;
+        }
+    }
+    if (blockIdx.x == 0 && expert_counts != nullptr)
+        for (int e = threadIdx.x; e < E; e += blockDim.x)
+            expert_counts[e] = e < ns ? T : __ldcg(counts_r + e - ns);
+}
+
+// One block: sum of the counts (int64, in order by thread then tree), then
+// each expert's step against the exact mean.
+__global__ void __launch_bounds__(256) balance_bias_kernel(const int32_t* __restrict__ counts,
+                                                           int E, float* __restrict__ bias,
+                                                           float step) {
+    pdl_wait();
+    pdl_trigger();
+    __shared__ long long s_sum[256];
+    long long v = 0;
+    for (int e = threadIdx.x; e < E; e += 256) v += counts[e];
+    s_sum[threadIdx.x] = v;
+    __syncthreads();
+    for (int o = 128; o > 0; o >>= 1) {
+        if (threadIdx.x < o) s_sum[threadIdx.x] += s_sum[threadIdx.x + o];
+        __syncthreads();
+    }
+    const long long total = s_sum[0];
+    for (int e = threadIdx.x; e < E; e += 256) {
+        const long long scaled = (long long)counts[e] * E;
+        if (scaled > total) bias[e] -= step;
+        else if (scaled < total) bias[e] += step;
+    }
+}
+
 }  // namespace
+
+cudaError_t launch_join_shared(const moe_config& c, const int32_t* idx_r, const float* w_r,
+                               int32_t* topk_idx, float* topk_w, const int32_t* counts_r,
+                               int32_t* expert_counts, cudaStream_t s) {
+    int blocks = (c.T + 255) / 256;
+    blocks = blocks < num_sms() * 4 ? blocks : num_sms() * 4;
+    return launch_kernel(join_shared_kernel, dim3(blocks), dim3(256), 0, s, 1, false, idx_r, w_r,
+                         c.T, c.k, c.n_shared, topk_idx, topk_w, counts_r, expert_counts, c.E);
+}
+
+cudaError_t launch_balance_bias(const moe_config& c, const int32_t* counts, float* bias,
+                                float step, cudaStream_t s) {
+    return launch_kernel(balance_bias_kernel, dim3(1), dim3(256), 0, s, 1, false, counts, c.E,
+                         bias, step);
+}
 
 LossArgs route_loss_args(const moe_config& c, void* ws, const WsLayout& L,
                          int32_t* expert_counts, float* aux_out, float* z_loss_out) {

@@ -10,7 +10,7 @@ Layouts follow ``nn.Linear`` (out, in), as in the PyTorch layer printed on
 "The MoE layer":
 
 * ``x``    (T, d)        token representations, row-major
-* ``W_r``  (E, d)  fp32  router weight (no bias)
+* ``W_r``  (E - n_shared, d)  fp32  router weight (no bias; over the routed experts)
 * ``W1``   (E, F, d)     first expert Linear, ``b1`` (E, F)
 * ``W2``   (E, d, F)     second expert Linear, ``b2`` (E, d)
 
@@ -63,6 +63,7 @@ class Workload:
     capacity_factor: float | None = None
     zipf_bias: float = 0.0
     init: str = "normal"
+    n_shared: int = 0  # experts 0 .. n_shared-1 always active (the router covers the rest)
     note: str = field(default="", compare=False)
 
     def with_(self, **kw) -> "Workload":
@@ -174,17 +175,18 @@ def zipf_logit_bias(E: int, scale: float) -> np.ndarray:
 def make_inputs(wl: Workload, seed: int = 0) -> Inputs:
     """Draw every stored input of workload ``wl`` from ``seed``."""
     T, d, F, E = wl.T, wl.d, wl.F, wl.E
+    Er = E - wl.n_shared  # experts the router covers
     x = _draw(seed, _S_X, T * d, "normal", 1.0).reshape(T, d)
     if wl.init == "uniform":
-        W_r = _draw(seed, _S_WR, E * d, "uniform", 1.0 / math.sqrt(d)).reshape(E, d)
+        W_r = _draw(seed, _S_WR, Er * d, "uniform", 1.0 / math.sqrt(d)).reshape(Er, d)
         W1 = _draw(seed, _S_W1, E * F * d, "uniform", 1.0 / math.sqrt(d)).reshape(E, F, d)
         W2 = _draw(seed, _S_W2, E * d * F, "uniform", 1.0 / math.sqrt(F)).reshape(E, d, F)
     else:
-        W_r = _draw(seed, _S_WR, E * d, "normal", 0.02).reshape(E, d)
+        W_r = _draw(seed, _S_WR, Er * d, "normal", 0.02).reshape(Er, d)
         W1 = _draw(seed, _S_W1, E * F * d, "normal", 1.0 / math.sqrt(d)).reshape(E, F, d)
         W2 = _draw(seed, _S_W2, E * d * F, "normal", 1.0 / math.sqrt(F)).reshape(E, d, F)
     b1 = _draw(seed, _S_B1, E * F, "uniform", 1.0 / math.sqrt(d)).reshape(E, F)
     b2 = _draw(seed, _S_B2, E * d, "uniform", 1.0 / math.sqrt(F)).reshape(E, d)
-    bias = zipf_logit_bias(E, wl.zipf_bias) if wl.zipf_bias else None
+    bias = zipf_logit_bias(Er, wl.zipf_bias) if wl.zipf_bias else None
     return Inputs(wl, _store(x, wl.dtype), W_r, bias, _store(W1, wl.dtype), _store(b1, wl.dtype),
                   _store(W2, wl.dtype), _store(b2, wl.dtype))

@@ -21,7 +21,8 @@ NEAR_TIE = 1e-6
 
 
 def cfg_of(wl):
-    return B.config(wl.T, wl.d, wl.F, wl.E, wl.k, wl.dtype, wl.capacity, wl.renormalize)
+    return B.config(wl.T, wl.d, wl.F, wl.E, wl.k, wl.dtype, wl.capacity, wl.renormalize,
+                    wl.n_shared)
 
 
 def y_error(y_gpu: np.ndarray, y_ref: np.ndarray):
@@ -67,12 +68,13 @@ class GpuRun:
         self.stream = stream
 
     def staged(self, logits_in=None, noise=None):
-        wl, D, T, k, E = self.wl, self.dev, self.wl.T, self.wl.k, self.wl.E
+        wl, D, T, E = self.wl, self.dev, self.wl.T, self.wl.E
+        k = wl.k + wl.n_shared  # columns per token (routed, then shared)
         dt = D["x"].dtype
         cuda = D["x"].device
         n = T * k
         r = {}
-        r["logits"] = torch.empty((T, E), dtype=torch.float32, device=cuda)
+        r["logits"] = torch.empty((T, E - wl.n_shared), dtype=torch.float32, device=cuda)
         r["idx"] = torch.empty((T, k), dtype=torch.int32, device=cuda)
         r["w"] = torch.empty((T, k), dtype=torch.float32, device=cuda)
         r["counts"] = torch.empty(E, dtype=torch.int32, device=cuda)
@@ -101,7 +103,7 @@ class GpuRun:
         y = torch.empty_like(D["x"])
         aux = torch.empty(1, dtype=torch.float32, device=y.device)
         counts = torch.empty(wl.E, dtype=torch.int32, device=y.device)
-        logits = torch.empty((wl.T, wl.E), dtype=torch.float32, device=y.device)
+        logits = torch.empty((wl.T, wl.E - wl.n_shared), dtype=torch.float32, device=y.device)
         z = torch.full((1,), -1.0, dtype=torch.float32, device=y.device)
         B.forward(self.cfg, D["x"], D["W_r"], D["W1"], D["b1"], D["W2"], D["b2"], y, self.ws,
                   logit_bias=D["logit_bias"], aux_out=aux, expert_counts=counts,
@@ -115,7 +117,8 @@ def oracle_on(inp, wl, logits=None, tokens=None, layout=True):
     return O.moe_forward(inp.as_f32("x"), inp.W_r, inp.as_f32("W1"), inp.as_f32("b1"),
                          inp.as_f32("W2"), inp.as_f32("b2"), k=wl.k,
                          renormalize=wl.renormalize, capacity=wl.capacity,
-                         logit_bias=inp.logit_bias, logits=logits, tokens=tokens, layout=layout)
+                         logit_bias=inp.logit_bias, logits=logits, tokens=tokens, layout=layout,
+                         n_shared=wl.n_shared)
 
 
 def sample_tokens(wl, ref_route, n: int, seed: int = 0) -> np.ndarray:

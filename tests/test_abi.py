@@ -47,6 +47,9 @@ def test_workspace_size():
     assert capped < n
     assert B.workspace_size(B.config(4096, 1024, 4096, 8, 9)) == 0  # k > E
     assert B.workspace_size(B.config(0, 64, 64, 4, 2)) > 0
+    # shared experts: K = k + n_shared assignments per token
+    assert B.workspace_size(B.config(4096, 1024, 4096, 9, 2, n_shared=1)) > \
+        B.workspace_size(B.config(4096, 1024, 4096, 9, 2))
 
 
 FAKE = 1 << 20  # a 256-aligned address that is never dereferenced (calls fail first)
@@ -60,6 +63,10 @@ FAKE = 1 << 20  # a 256-aligned address that is never dereferenced (calls fail f
     (B.config(16, 60, 64, 4, 2), 2),            # d not a multiple of 8
     (B.config(16, 64, 68, 4, 2), 2),            # d_ff not a multiple of 8
     (B.config(-1, 64, 64, 4, 2), 1),            # T < 0
+    (B.config(16, 64, 64, 4, 1, n_shared=4), 1),   # every expert shared
+    (B.config(16, 64, 64, 4, 2, n_shared=3), 1),   # k > routed experts
+    (B.config(16, 64, 64, 16, 6, n_shared=3), 4),  # k + n_shared > 8
+    (B.config(16, 64, 64, 4, 1, n_shared=-1), 1),  # n_shared < 0
 ])
 def test_forward_rejects_bad_config(cfg, status):
     lib = B.load()
@@ -94,4 +101,5 @@ def test_calls_reject_null_misaligned_and_small_workspace():
     assert lib.moe_combine(cr, FAKE, None, FAKE, None) == 1
     assert lib.moe_get_device_error(None, None, None, None) == 1
     assert lib.moe_check_wait_timeout(None, ctypes.c_uint64(1000), None) == 1
+    assert lib.moe_update_balance_bias(cr, None, FAKE, ctypes.c_float(0.1), None) == 1
     assert lib.moe_check_wait_timeout(FAKE + 16, ctypes.c_uint64(1000), None) == 3

@@ -199,3 +199,61 @@ def test_noisy_gating(case):
     _check(wl, inp, r)
     f = run.forward(noise=noise)
     assert torch.equal(f["y"], r["y"]) and torch.equal(f["logits"], r["logits"])
+
+
+def test_balance_bias_update_matches_oracle_and_evens_out_load():
+    """Auxiliary-loss-free balancing: the bias step from a routed batch's
+    counts equals the oracle's, and repeating route + step on a Zipf-skewed
+    router brings the first-choice loads toward balance."""
+    wl = _wl("balance", 2048, 64, 64, 16, 2, "bf16", None, True, zipf=1.0)
+    inp = I.make_inputs(wl, seed=9)
+    run = GpuRun(wl, inp)
+    bias = run.dev["logit_bias"].clone()
+    idx = torch.empty((wl.T, wl.k), dtype=torch.int32, device="cuda")
+    w = torch.empty((wl.T, wl.k), dtype=torch.float32, device="cuda")
+    counts = torch.empty(wl.E, dtype=torch.int32, device="cuda")
+
+    def route():
+        B.route(run.cfg, run.dev["x"], run.dev["W_r"], idx, w, run.ws, logit_bias=bias,
+                expert_counts=counts)
+        top1 = torch.bincount(idx[:, 0].long(), minlength=wl.E)
+        return float(top1.max()) / (wl.T / wl.E)
+
+    first = route()
+    want = O.balance_bias_update(to_np(bias), to_np(counts), 0.02)
+    B.update_balance_bias(run.cfg, counts, bias, 0.02)
+    torch.cuda.synchronize()
+    assert np.array_equal(to_np(bias), want)
+    for _ in range(99):
+        route()
+        B.update_balance_bias(run.cfg, counts, bias, 0.02)
+    last = route()
+    assert first > 3.0 and last < 1.6
+
+
+SHARED = [
+    # name, T, d, F, E, k, n_shared, dtype, capacity
+    ("shared1-tc", 2048, 128, 256, 9, 2, 1, "bf16", None),    # CTA-pair GEMMs, mma router
+    ("shared2-cap", 600, 64, 128, 10, 2, 2, "bf16", 50),      # capacity: shared experts uncapped
+    ("shared1-f32", 100, 32, 64, 6, 1, 1, "f32", None),       # SIMT path
+]
+
+
+@pytest.mark.parametrize("case", SHARED, ids=[c[0] for c in SHARED])
+def test_shared_experts(case):
+    """Shared experts (always active, weight 1, never capped) beside k routed
+    ones: routing, counts, the dispatch layout and y against the oracle, and
+    forward equal to the staged calls."""
+    name, T, d, F, E, k, ns, dt, cap = case
+    wl = I.Workload(name, T, d, F, E, k, dtype=dt, renormalize=True, capacity=cap,
+                    init="uniform" if dt == "f32" else "normal", n_shared=ns)
+    inp = I.make_inputs(wl, seed=13)
+    run = GpuRun(wl, inp)
+    r = run.staged()
+    ref = _check(wl, inp, r)
+    assert np.array_equal(to_np(r["idx"])[:, k:], np.tile(np.arange(ns), (T, 1)))
+    assert np.all(to_np(r["w"])[:, k:] == 1.0)
+    assert np.all(ref.kept[:, k:]) and np.all(ref.kept_count[:ns] == T)
+    f = run.forward()
+    assert torch.equal(f["y"], r["y"]) and torch.equal(f["counts"], r["counts"])
+    assert torch.equal(f["aux"], r["aux"]) and torch.equal(f["z"], r["z"])
