@@ -100,10 +100,10 @@ struct Tile {
     int e, r0, n, m0;
 };
 
-// Work item t of a cluster: expert e, token tile, and a group of CS
-// consecutive 128-row weight tiles of which CTA `rank` takes one.
-__device__ __forceinline__ Tile decode_tile(int t, const int* s_tiles, const Params& p, int bn_max,
-                                            int cs, int rank) {
+// Work item t of the single-CTA kernel: expert e, token tile (fastest) and
+// 128-row weight tile.
+__device__ __forceinline__ Tile decode_tile(int t, const int* s_tiles, const Params& p,
+                                            int bn_max) {
     int lo = 0, hi = p.E - 1;
     while (lo < hi) {  // last expert whose first item is <= t
         const int mid = (lo + hi + 1) >> 1;
@@ -118,7 +118,7 @@ __device__ __forceinline__ Tile decode_tile(int t, const int* s_tiles, const Par
     const int ti = local % nt, gi = local / nt;  // token tile fastest
     tl.r0 = s0 + ti * bn_max;
     tl.n = min(bn_max, s1 - tl.r0);
-    tl.m0 = (gi * cs + rank) * BM;
+    tl.m0 = gi * BM;
     return tl;
 }
 
@@ -147,11 +147,6 @@ __device__ __forceinline__ void drain_bar(uint64_t* bar, uint32_t parity) {
     }
 }
 
-// CS > 1: the kernel runs in clusters of CS CTAs that share each token tile:
-// CTA r loads the token boxes b with b % CS == r once and multicasts them to
-// every CTA of the cluster, so each CTA fetches 1/CS of the token tile from
-// L2.  A stage may be refilled only when all CS CTAs have consumed it, so
-// every MMA commit arrives on the stage's empty barrier of all CS CTAs.
 // Epilogue of one accumulator tile: this warp reads TMEM lanes 32q..32q+31
 // (weight rows fbase + 32q + lane) and the token columns of its part (of
 // nparts) of the COLS-wide tile (columns acc_col + c, c < n), applies bias + GELU (first
@@ -236,14 +231,12 @@ __device__ __forceinline__ void epilogue_tile(const Params& p, int e, int r0, in
     }
 }
 
-template <int BN_MAX, int STAGES, bool GEMM1, int CS>
+template <int BN_MAX, int STAGES, bool GEMM1>
 __global__ void __launch_bounds__(kThreads, 1)
 grouped_gemm_tc(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                 const Params p) {
     using C = Cfg<BN_MAX, STAGES, GEMM1>;
-    const int rank = CS > 1 ? (int)tc::cluster_ctarank() : 0;
-    const int cluster = blockIdx.x / CS, nclusters = gridDim.x / CS;
-    constexpr uint16_t kAll = (uint16_t)((1u << CS) - 1u);
+    const int cta = blockIdx.x, nctas = gridDim.x;
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -258,12 +251,11 @@ grouped_gemm_tc(const __grid_constant__ CUtensorMap tmA, const __grid_constant__
 
     const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
     const int mt = (p.n_out + BM - 1) / BM;
-    const int groups = (mt + CS - 1) / CS;  // weight-tile groups per token tile
     const int KB = (p.K + BK - 1) / BK;
     if (warp == 0 && lane == 0) {
         for (int s = 0; s < STAGES; ++s) {
             tc::mbar_init(&full[s], 1);
-            tc::mbar_init(&empty[s], CS);
+            tc::mbar_init(&empty[s], 1);
         }
         for (int a = 0; a < 2; ++a) {
             tc::mbar_init(&tfull[a], 1);
@@ -287,7 +279,7 @@ grouped_gemm_tc(const __grid_constant__ CUtensorMap tmA, const __grid_constant__
             const int e = e0 + lane;
             int nt = 0;
             if (e < p.E) {
-                nt = ((seg_rows(p, e) + BN_MAX - 1) / BN_MAX) * groups;
+                nt = ((seg_rows(p, e) + BN_MAX - 1) / BN_MAX) * mt;
             }
             int v = nt;
 #pragma unroll
@@ -301,8 +293,7 @@ grouped_gemm_tc(const __grid_constant__ CUtensorMap tmA, const __grid_constant__
         if (lane == 0) s_tiles[p.E] = run;
     }
     tc::fence_before_sync();
-    if (CS > 1) tc::cluster_sync();  // peers' barriers exist before any multicast
-    else __syncthreads();
+    __syncthreads();
     tc::fence_after_sync();
     const uint32_t tmem_base = *s_tmem;
     const int total = s_tiles[p.E];
@@ -314,8 +305,8 @@ grouped_gemm_tc(const __grid_constant__ CUtensorMap tmA, const __grid_constant__
             uint32_t phase = 0;
             long long fills = 0;
             bool ok = true;
-            for (int t = cluster; t < total && ok; t += nclusters) {
-                const Tile tl = decode_tile(t, s_tiles, p, BN_MAX, CS, rank);
+            for (int t = cta; t < total && ok; t += nctas) {
+                const Tile tl = decode_tile(t, s_tiles, p, BN_MAX);
                 const int nb = (tl.n + BOX_ROWS - 1) / BOX_ROWS;
                 const uint32_t bytes = A_BYTES + nb * BOX_BYTES;
                 const int arow = tl.e * p.n_out + tl.m0;
@@ -325,15 +316,9 @@ grouped_gemm_tc(const __grid_constant__ CUtensorMap tmA, const __grid_constant__
                     uint8_t* sa = smem + stage * C::STAGE_BYTES;
                     uint8_t* sb = sa + A_BYTES;
                     tc::tma_load_2d(sa, &tmA, &full[stage], kb * BK, arow);
-                    if (CS == 1) {
-                        for (int b = 0; b < nb; ++b)
-                            tc::tma_load_2d(sb + b * BOX_BYTES, &tmB, &full[stage], kb * BK,
-                                            tl.r0 + b * BOX_ROWS);
-                    } else {
-                        for (int b = rank; b < nb; b += CS)
-                            tc::tma_load_2d_mc(sb + b * BOX_BYTES, &tmB, &full[stage], kb * BK,
-                                               tl.r0 + b * BOX_ROWS, kAll);
-                    }
+                    for (int b = 0; b < nb; ++b)
+                        tc::tma_load_2d(sb + b * BOX_BYTES, &tmB, &full[stage], kb * BK,
+                                        tl.r0 + b * BOX_ROWS);
                     ++fills;
                     if (++stage == STAGES) { stage = 0; phase ^= 1; }
                 }
@@ -349,8 +334,8 @@ grouped_gemm_tc(const __grid_constant__ CUtensorMap tmA, const __grid_constant__
             int stage = 0, acc = 0;
             uint32_t phase = 0, acc_phase = 0;
             bool ok = true;
-            for (int t = cluster; t < total && ok; t += nclusters) {
-                const Tile tl = decode_tile(t, s_tiles, p, BN_MAX, CS, rank);
+            for (int t = cta; t < total && ok; t += nctas) {
+                const Tile tl = decode_tile(t, s_tiles, p, BN_MAX);
                 const uint32_t n_mma = (uint32_t)((tl.n + 15) / 16) * 16;
                 const uint32_t idesc = tc::idesc_bf16_f32(BM, n_mma);
                 if (!wait_bar(&tempty[acc], acc_phase ^ 1, s_abort, p, 2)) break;
@@ -367,8 +352,7 @@ grouped_gemm_tc(const __grid_constant__ CUtensorMap tmA, const __grid_constant__
                                      tc::sdesc_k128_sw128(sb + kk * 32), idesc,
                                      (kb | kk) != 0 ? 1u : 0u);
                     }
-                    if (CS == 1) tc::mma_commit(&empty[stage]);
-                    else tc::mma_commit_mc(&empty[stage], kAll);
+                    tc::mma_commit(&empty[stage]);
                     if (++stage == STAGES) { stage = 0; phase ^= 1; }
                 }
                 if (!ok) break;
@@ -388,8 +372,8 @@ grouped_gemm_tc(const __grid_constant__ CUtensorMap tmA, const __grid_constant__
         uint8_t* stg = smem + C::OFF_STAGING + ew * 32 * 32 * C::OUT_ES;
         int acc = 0;
         uint32_t acc_phase = 0;
-        for (int t = cluster; t < total; t += nclusters) {
-            const Tile tl = decode_tile(t, s_tiles, p, BN_MAX, CS, rank);
+        for (int t = cta; t < total; t += nctas) {
+            const Tile tl = decode_tile(t, s_tiles, p, BN_MAX);
             const bool ok = wait_bar(&tfull[acc], acc_phase, s_abort, p, 4);
             if (!__all_sync(0xffffffffu, ok)) break;
             tc::fence_after_sync();
@@ -409,8 +393,6 @@ grouped_gemm_tc(const __grid_constant__ CUtensorMap tmA, const __grid_constant__
         tc::fence_after_sync();
         tc::tmem_dealloc(tmem_base, C::TMEM_COLS);
     }
-    // no CTA leaves while a peer may still multicast into it or arrive on it
-    if (CS > 1) tc::cluster_sync();
 }
 
 // First-GEMM epilogue of the CTA-pair kernel for this CTA's 128 weight rows x
@@ -704,7 +686,7 @@ grouped_gemm_pair(const __grid_constant__ CUtensorMap tmA, const __grid_constant
             const bool ok = wait_bar(&tfull[acc], acc_phase, s_abort, p, 4);
             if (!__all_sync(0xffffffffu, ok)) break;
             tc::fence_after_sync();
-            if (GEMM1)
+            if constexpr (GEMM1)
                 epilogue_gelu<EW / 4>(p, tl.e, tl.r0, tl.n, m0 + rank * BM, tmem_base, acc * BN2,
                                       q, part, lane, stg, &tmO);
             else
@@ -827,15 +809,14 @@ int resident_clusters(int cs, int smem, int threads = kThreads) {
     return n;
 }
 
-template <int BN_MAX, int STAGES, bool GEMM1, int CS>
+template <int BN_MAX, int STAGES, bool GEMM1>
 cudaError_t launch_one(const CUtensorMap& a, const CUtensorMap& b, const Params& p,
                        cudaStream_t s) {
     using C = Cfg<BN_MAX, STAGES, GEMM1>;
-    constexpr auto kern = grouped_gemm_tc<BN_MAX, STAGES, GEMM1, CS>;
+    constexpr auto kern = grouped_gemm_tc<BN_MAX, STAGES, GEMM1>;
     cudaError_t err = ensure_smem<kern>(C::SMEM);
     if (err != cudaSuccess) return err;
-    const int grid = CS == 1 ? num_sms() : CS * resident_clusters<kern>(CS, C::SMEM);
-    return launch_kernel(kern, dim3(grid), dim3(kThreads), C::SMEM, s, CS, true, a, b, p);
+    return launch_kernel(kern, dim3(num_sms()), dim3(kThreads), C::SMEM, s, 1, true, a, b, p);
 }
 
 template <int STAGES, bool GEMM1, int EW, int ATOMS>
@@ -849,12 +830,12 @@ cudaError_t launch_one_pair(const CUtensorMap& a, const CUtensorMap& b, const CU
                          dim3(C::THREADS), C::SMEM, s, 2, true, a, b, o, p);
 }
 
-template <int BN_MAX, int STAGES, int CS>
+template <int BN_MAX, int STAGES>
 cudaError_t launch_pair(const CUtensorMap* maps, const Params& p1, const Params& p2,
                         cudaStream_t s) {
-    cudaError_t err = launch_one<BN_MAX, STAGES, true, CS>(maps[0], maps[1], p1, s);
+    cudaError_t err = launch_one<BN_MAX, STAGES, true>(maps[0], maps[1], p1, s);
     if (err != cudaSuccess) return err;
-    return launch_one<BN_MAX, STAGES, false, CS>(maps[2], maps[3], p2, s);
+    return launch_one<BN_MAX, STAGES, false>(maps[2], maps[3], p2, s);
 }
 
 }  // namespace
@@ -900,7 +881,7 @@ cudaError_t launch_expert_ffn_tc(const moe_config& c, const void* x_perm, int64_
         if (err != cudaSuccess) return err;
         return launch_one_pair<3, false, 8, 2>(pm[2], pm[3], pm[5], p2, s);
     }
-    return launch_pair<64, 8, 1>(maps, p1, p2, s);
+    return launch_pair<64, 8>(maps, p1, p2, s);
 }
 
 }  // namespace moe
