@@ -1,4 +1,5 @@
-"""Thin ctypes binding of libmoe (the C ABI declared in include/moe.h).
+"""Thin ctypes binding of libmoe (the C ABI declared in include/moe.h and
+include/moe_pipeline.h).
 
 Argument marshalling only: every step of the layer runs in libmoe's CUDA
 kernels.  PyTorch supplies device memory and the current CUDA stream.  The
@@ -24,7 +25,8 @@ STATUS = {0: "ok", 1: "invalid argument", 2: "misaligned pointer or row length",
 EXPORTED = ("moe_workspace_size", "moe_status_string", "moe_route", "moe_dispatch",
             "moe_expert_ffn", "moe_combine", "moe_forward", "moe_get_device_error",
             "moe_launch_count", "moe_dispatch_noalloc", "moe_check_wait_timeout",
-            "moe_update_balance_bias")
+            "moe_update_balance_bias", "moe_pipeline_workspace_size", "moe_pipeline_create",
+            "moe_pipeline_submit", "moe_pipeline_join", "moe_pipeline_destroy")
 
 
 class MoeConfig(ctypes.Structure):
@@ -75,6 +77,17 @@ def load() -> ctypes.CDLL:
         lib.moe_check_wait_timeout.argtypes = [_P, ctypes.c_uint64, _P]
         lib.moe_update_balance_bias.restype = ctypes.c_int
         lib.moe_update_balance_bias.argtypes = [cfgp, _P, _P, ctypes.c_float, _P]
+        lib.moe_pipeline_workspace_size.restype = ctypes.c_size_t
+        lib.moe_pipeline_workspace_size.argtypes = [cfgp, ctypes.c_int32]
+        lib.moe_pipeline_create.restype = ctypes.c_int
+        lib.moe_pipeline_create.argtypes = [cfgp, ctypes.c_int32] + [_P] * 7 + [sz, _P,
+                                                                               ctypes.POINTER(_P)]
+        lib.moe_pipeline_submit.restype = ctypes.c_int
+        lib.moe_pipeline_submit.argtypes = [_P, _P, _P, _P]
+        lib.moe_pipeline_join.restype = ctypes.c_int
+        lib.moe_pipeline_join.argtypes = [_P]
+        lib.moe_pipeline_destroy.restype = ctypes.c_int
+        lib.moe_pipeline_destroy.argtypes = [_P]
         _lib = lib
     return _lib
 
@@ -189,3 +202,53 @@ def get_device_error(ws, stream=None):
     st = load().moe_get_device_error(_ptr(ws), _stream(stream), ctypes.byref(code),
                                      ctypes.byref(info))
     return st, code.value, info.value
+
+
+def pipeline_workspace_size(cfg: MoeConfig, depth: int = 2) -> int:
+    return int(load().moe_pipeline_workspace_size(ctypes.byref(cfg), depth))
+
+
+class Pipeline:
+    """Host-buffer executor (moe_pipeline_*): batches of cfg.T tokens in host
+    memory in, y and the auxiliary loss to host memory out, the copies of
+    neighbouring batches overlapping the forward pass on ``stream``.
+
+    Keeps the workspace it allocates (and the weights it is given) alive;
+    ``close()`` (or garbage collection) destroys the executor."""
+
+    def __init__(self, cfg: MoeConfig, W_r, W1, b1, W2, b2, logit_bias=None, depth: int = 2,
+                 stream=None, device="cuda"):
+        n = pipeline_workspace_size(cfg, depth)
+        if n == 0:
+            raise MoeError("moe_pipeline_workspace_size", 1)
+        self.cfg, self.depth = cfg, depth
+        self.ws = torch.zeros(n, dtype=torch.uint8, device=device)
+        self._keep = (W_r, W1, b1, W2, b2, logit_bias)
+        self._stream = stream
+        h = _P()
+        _check("moe_pipeline_create", load().moe_pipeline_create(
+            ctypes.byref(cfg), depth, _ptr(W_r), _ptr(logit_bias), _ptr(W1), _ptr(b1), _ptr(W2),
+            _ptr(b2), _ptr(self.ws), n, _stream(stream), ctypes.byref(h)))
+        self._h = h
+
+    def submit(self, x_host, y_host, aux_host=None) -> None:
+        """Enqueue one batch; x_host / y_host (T, d) and aux_host (1,) are host
+        tensors (pinned for overlap) that must stay alive until after join()."""
+        _check("moe_pipeline_submit", load().moe_pipeline_submit(
+            self._h, _ptr(x_host), _ptr(y_host), _ptr(aux_host)))
+
+    def join(self) -> None:
+        """The stream waits for the outputs of every submitted batch."""
+        _check("moe_pipeline_join", load().moe_pipeline_join(self._h))
+
+    def close(self) -> None:
+        if getattr(self, "_h", None):
+            st = load().moe_pipeline_destroy(self._h)
+            self._h = None
+            _check("moe_pipeline_destroy", st)
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass

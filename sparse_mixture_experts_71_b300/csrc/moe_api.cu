@@ -93,6 +93,8 @@ int64_t max_segment(const moe_config& c) {
 
 }  // namespace
 
+moe_status config_status(const moe_config* c) { return check_config(c); }
+
 WsLayout ws_layout(const moe_config& c) {
     WsLayout L{};
     const moe_config cr = routed_config(c);

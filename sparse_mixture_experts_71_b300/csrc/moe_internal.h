@@ -86,6 +86,10 @@ struct WsLayout {
 
 WsLayout ws_layout(const moe_config& c);
 
+// Host validation of a configuration (the status every entry point returns
+// for an invalid one).
+moe_status config_status(const moe_config* c);
+
 // Kernel launches enqueued so far (moe_launch_count).
 void count_launches(int n);
 int num_sms();

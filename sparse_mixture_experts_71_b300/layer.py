@@ -77,6 +77,14 @@ class MoELayer:
 
     __call__ = forward
 
+    def host_pipeline(self, T: int, depth: int = 2, stream=None) -> B.Pipeline:
+        """An executor for batches of T tokens in host memory (moe_pipeline_*):
+        ``submit(x_host, y_host, aux_host)`` per batch, ``join()`` to make the
+        stream wait for the outputs; the copies overlap the forward passes."""
+        return B.Pipeline(self.config(T), self.W_r, self.W1, self.b1, self.W2, self.b2,
+                          logit_bias=self.logit_bias, depth=depth, stream=stream,
+                          device=self.W1.device)
+
 
 def capture_graph(fn, stream=None, warmup: int = 2):
     """Record the libmoe calls made by ``fn(stream)`` into a CUDA graph.

@@ -103,3 +103,35 @@ def test_calls_reject_null_misaligned_and_small_workspace():
     assert lib.moe_check_wait_timeout(None, ctypes.c_uint64(1000), None) == 1
     assert lib.moe_update_balance_bias(cr, None, FAKE, ctypes.c_float(0.1), None) == 1
     assert lib.moe_check_wait_timeout(FAKE + 16, ctypes.c_uint64(1000), None) == 3
+
+
+def test_pipeline_workspace_and_host_rejections():
+    lib = B.load()
+    c = B.config(64, 64, 128, 4, 2)
+    one, two = B.pipeline_workspace_size(c, 1), B.pipeline_workspace_size(c, 2)
+    tile = 64 * 64 * 2
+    # the forward workspace plus per slot x, y (bf16 [T][d]) and the loss
+    assert one >= B.workspace_size(c) + 2 * tile and one % 256 == 0
+    assert two - one >= 2 * tile
+    assert B.pipeline_workspace_size(c, 0) == 0 and B.pipeline_workspace_size(c, 5) == 0
+    assert B.pipeline_workspace_size(B.config(0, 64, 128, 4, 2), 2) == 0  # T = 0
+    assert B.pipeline_workspace_size(B.config(64, 64, 128, 4, 5), 2) == 0  # k > E
+    cr = ctypes.byref(c)
+    h = ctypes.c_void_p()
+    out = ctypes.byref(h)
+    args = (FAKE, None, FAKE, FAKE, FAKE, FAKE)  # W_r, logit_bias, W1, b1, W2, b2
+    assert lib.moe_pipeline_create(cr, 2, *args, FAKE, two, None, None) == 1  # no out
+    assert lib.moe_pipeline_create(None, 2, *args, FAKE, two, None, out) == 1
+    assert lib.moe_pipeline_create(ctypes.byref(B.config(64, 64, 128, 300, 2)), 2, *args, FAKE,
+                                   1 << 40, None, out) == 4
+    assert lib.moe_pipeline_create(cr, 0, *args, FAKE, two, None, out) == 1  # depth
+    assert lib.moe_pipeline_create(cr, 2, FAKE, None, None, FAKE, FAKE, FAKE, FAKE, two, None,
+                                   out) == 1  # W1 missing
+    assert lib.moe_pipeline_create(cr, 2, FAKE, None, FAKE + 8, FAKE, FAKE, FAKE, FAKE, two,
+                                   None, out) == 2
+    assert lib.moe_pipeline_create(cr, 2, *args, FAKE, two - 1, None, out) == 3
+    assert lib.moe_pipeline_create(cr, 2, *args, FAKE + 16, two, None, out) == 3
+    assert h.value is None
+    assert lib.moe_pipeline_submit(None, FAKE, FAKE, None) == 1
+    assert lib.moe_pipeline_join(None) == 1
+    assert lib.moe_pipeline_destroy(None) == 0
