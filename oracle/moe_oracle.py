@@ -35,7 +35,16 @@ the combine and of the auxiliary loss did not survive extraction):
   caller chooses it);
 * auxiliary-loss-free balancing moves the per-expert logit bias by a fixed
   step toward balanced load after a batch: minus the step for an expert
-  above the mean assignment count, plus it below, unchanged at the mean.
+  above the mean assignment count, plus it below, unchanged at the mean;
+* expert-choice routing ("experts choose their top tokens") ranks, for each
+  expert, the batch's tokens by their router probability p[t, e] (the same
+  softmax over experts as token choice), larger first and the lower token
+  index first among equals, and keeps the first C; C is the capacity when one
+  is given, else ceil(T k / E) (the average load top-k token choice would
+  put on an expert), at most T.  A token's output is the sum, over the
+  experts that chose it, of p[t, e] times the expert's output (no
+  renormalisation); a token no expert chose gets 0.  Balance holds by
+  construction, so no balancing loss is defined (reported as 0).
 
 Parity: the routing, capacity, auxiliary-loss and combine functions are pinned
 by the pages' worked examples, closed forms and brute force (tests).  The
@@ -323,3 +332,88 @@ def moe_forward(x, W_r, W1, b1, W2, b2, k: int, renormalize: bool = True,
         y[rows] += we[:, None] * out
     return OracleResult(logits, probs, idx, w, kept, counts, kept_count, offsets, slot_of,
                         perm_token, aux, y, tokens, router_z_loss(logits))
+
+
+def expert_choice_capacity(T: int, E: int, k: int, capacity: int | None = None) -> int:
+    """C, the tokens each expert takes under expert-choice routing.
+
+    [LECTURE] "Design variations" (expert-choice routing) and "The central
+    problem: load balancing" (capacity factor x tokens / experts): the given
+    capacity, else ceil(T k / E), the load top-k token choice averages per
+    expert; never more than the T tokens of the batch.
+    """
+    c = int(math.ceil(T * k / E)) if capacity is None else int(capacity)
+    return max(0, min(c, T))
+
+
+def expert_choice_select(probs, C: int) -> np.ndarray:
+    """For each expert, the C tokens with the largest router probability.
+
+    [LECTURE] "Design variations": each expert chooses its top tokens (a
+    top-C over the token axis of p instead of a top-k over the expert axis).
+    Among equal probabilities the lower token index ranks first.  Each row
+    of the result lists the chosen tokens in ascending token order.
+    probs: (T, E); returns (E, C) int64.
+    """
+    p = np.asarray(probs, f64)
+    T, E = p.shape
+    sel = np.zeros((E, C), np.int64)
+    for e in range(E):
+        order = np.lexsort((np.arange(T), -p[:, e]))  # by -p, then by token
+        sel[e] = np.sort(order[:C])
+    return sel
+
+
+@dataclass
+class ExpertChoiceResult:
+    logits: np.ndarray      # (T, E) fp32 routing input
+    probs: np.ndarray       # (T, E) fp64
+    C: int                  # tokens per expert
+    sel: np.ndarray         # (E, C) chosen tokens, ascending
+    w: np.ndarray           # (E, C) fp64 p[sel, e]
+    slot_of: np.ndarray     # (T, E) row e*C + j of (token, expert), -1 if not chosen
+    y: np.ndarray           # (len(tokens), d) fp64
+    tokens: np.ndarray
+    z_loss: float
+
+
+def expert_choice_forward(x, W_r, W1, b1, W2, b2, k: int, capacity: int | None = None,
+                          logit_bias=None, logit_noise=None, logits=None, sel=None,
+                          tokens=None) -> ExpertChoiceResult:
+    """The MoE layer with expert-choice routing, looping over experts.
+
+    [LECTURE] "Design variations" (experts choose their top tokens,
+    guaranteeing balance) on the layer of "The MoE layer" (router logits and
+    softmax, expert FFNs, weighted sum of the experts' outputs).  ``logits``
+    replaces the router GEMM when given; ``sel`` (E, C) replaces the
+    selection (to evaluate the layer on another valid choice among equal
+    probabilities); ``tokens`` restricts the output rows as in moe_forward.
+    """
+    x = np.asarray(x)
+    T, d = x.shape
+    if logits is None:
+        logits = router_logits(x, W_r, logit_bias, logit_noise)
+    logits = np.asarray(logits, np.float32)
+    E = logits.shape[1]
+    probs = softmax(logits)
+    C = expert_choice_capacity(T, E, k, capacity)
+    if sel is None:
+        sel = expert_choice_select(probs, C)
+    sel = np.asarray(sel, np.int64)
+    w = np.take_along_axis(probs.T, sel, axis=1) if C else np.zeros((E, 0))
+    slot_of = np.full((T, E), -1, np.int64)
+    for e in range(E):
+        slot_of[sel[e], e] = e * C + np.arange(C)
+    tokens = np.arange(T) if tokens is None else np.asarray(tokens, np.int64)
+    pos = {int(t): i for i, t in enumerate(tokens)}
+    y = np.zeros((len(tokens), d), f64)
+    for e in range(E):
+        rows = [j for j in range(C) if int(sel[e, j]) in pos]
+        if not rows:
+            continue
+        toks = sel[e, rows]
+        out = expert_ffn(x[toks], W1[e], b1[e], W2[e], b2[e])
+        for r, t in enumerate(toks):
+            y[pos[int(t)]] += w[e, rows[r]] * out[r]
+    return ExpertChoiceResult(logits, probs, C, sel, w, slot_of, y, tokens,
+                              router_z_loss(logits))

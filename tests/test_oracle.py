@@ -520,3 +520,148 @@ def test_planted_mistakes_are_caught(monkeypatch):
     with pytest.raises(AssertionError):
         test_single_expert_is_dense_ffn()
     monkeypatch.setattr(O, "gelu", good_gelu)
+
+
+# ---- expert-choice routing ("Design variations": experts choose their top
+# tokens); the readings are listed in the oracle's header
+
+def test_expert_choice_capacity_values():
+    """C = ceil(T k / E) without a cap, the cap when given, never above T."""
+    assert O.expert_choice_capacity(4096, 8, 2) == 1024
+    assert O.expert_choice_capacity(10, 3, 1) == 4      # ceil(10/3)
+    assert O.expert_choice_capacity(10, 3, 2) == 7      # ceil(20/3)
+    assert O.expert_choice_capacity(5, 1, 2) == 5       # ceil(10/1) > T
+    assert O.expert_choice_capacity(10, 3, 1, capacity=2) == 2
+    assert O.expert_choice_capacity(10, 3, 1, capacity=50) == 10
+    assert O.expert_choice_capacity(10, 3, 1, capacity=0) == 0
+
+
+def test_expert_choice_hand_worked():
+    """Two experts, four tokens, logits (a_t, 0): p[t, 0] = sigmoid(a_t).
+    a = (2, -1, 0.5, 0): p0 = (.881, .269, .622, .5), p1 = 1 - p0; C = 2.
+    Expert 0 takes tokens 0 and 2, expert 1 tokens 1 and 3 (worked by hand);
+    each token's output is its one expert's FFN scaled by that p."""
+    L = _rand_layer(T=4, d=3, F=5, E=2, seed=41)
+    g = np.array([[2.0, 0.0], [-1.0, 0.0], [0.5, 0.0], [0.0, 0.0]], np.float32)
+    r = O.expert_choice_forward(**L, k=1, logits=g)
+    assert r.C == 2
+    assert r.sel.tolist() == [[0, 2], [1, 3]]
+    assert r.slot_of.tolist() == [[0, -1], [-1, 2], [1, -1], [-1, 3]]
+    sig = [1 / (1 + math.exp(-a)) for a in (2.0, -1.0, 0.5, 0.0)]
+    assert np.allclose(r.w, [[sig[0], sig[2]], [1 - sig[1], 1 - sig[3]]], rtol=1e-15)
+    t = {n: torch.from_numpy(v) for n, v in L.items()}
+    for tok, e in ((0, 0), (1, 1), (2, 0), (3, 1)):
+        fe = TF.linear(TF.gelu(TF.linear(t["x"][tok], t["W1"][e], t["b1"][e])), t["W2"][e],
+                       t["b2"][e]).numpy()
+        pe = sig[tok] if e == 0 else 1 - sig[tok]
+        np.testing.assert_allclose(r.y[tok], pe * fe, rtol=1e-12, atol=1e-15)
+
+
+def test_expert_choice_ties_go_to_lower_token():
+    """Equal logits: p = 1/E everywhere, so every expert takes tokens 0..C-1;
+    E = 1 is the same (p = 1) and tokens from C on get y = 0."""
+    r = O.expert_choice_select(np.full((9, 3), 1 / 3), 4)
+    assert r.tolist() == [[0, 1, 2, 3]] * 3
+    L = _rand_layer(T=7, d=4, F=6, E=1, seed=42)
+    r1 = O.expert_choice_forward(**L, k=1, capacity=3)
+    assert r1.sel.tolist() == [[0, 1, 2]]
+    assert not r1.y[3:].any()
+    t = {n: torch.from_numpy(v) for n, v in L.items()}
+    want = TF.linear(TF.gelu(TF.linear(t["x"][:3], t["W1"][0], t["b1"][0])), t["W2"][0],
+                     t["b2"][0])
+    np.testing.assert_allclose(r1.y[:3], want.numpy(), rtol=1e-12, atol=1e-15)
+
+
+def test_expert_choice_brute_force_selection():
+    """With distinct probabilities each expert's chosen set is the unique
+    C-subset of tokens with the largest total probability (enumerated)."""
+    import itertools
+    rng = np.random.default_rng(43)
+    for T, E, C in ((6, 3, 2), (7, 2, 3), (5, 4, 1), (6, 2, 6)):
+        p = rng.random((T, E))
+        sel = O.expert_choice_select(p, C)
+        for e in range(E):
+            best = max(itertools.combinations(range(T), C), key=lambda s: sum(p[i, e] for i in s))
+            assert sel[e].tolist() == list(best)
+
+
+def test_expert_choice_all_tokens_is_soft_mixture():
+    """C = T (every expert takes every token): y = sum_e p_e f_e(x), the soft
+    mixture (torch, fp64); balance: every expert takes exactly C tokens."""
+    L = _rand_layer(T=13, d=6, F=10, E=4, seed=44)
+    r = O.expert_choice_forward(**L, k=4)  # ceil(13 * 4 / 4) = 13 = T
+    assert r.C == 13 and all(sorted(s) == list(range(13)) for s in r.sel.tolist())
+    t = {n: torch.from_numpy(v) for n, v in L.items()}
+    p = torch.softmax(torch.from_numpy(r.logits).double(), -1)
+    want = torch.zeros_like(t["x"])
+    for e in range(4):
+        fe = TF.linear(TF.gelu(TF.linear(t["x"], t["W1"][e], t["b1"][e])), t["W2"][e], t["b2"][e])
+        want += p[:, e:e + 1] * fe
+    np.testing.assert_allclose(r.y, want.numpy(), rtol=1e-12, atol=1e-12)
+
+
+def test_expert_choice_dense_masked_brute_force():
+    """Every expert on every token with plain loops, masked by the column-wise
+    top-C of p computed by sorting each column in pure Python."""
+    L = _rand_layer(T=11, d=4, F=5, E=3, seed=45)
+    logits, _ = _brute_force_dense(L, 1, False, None)
+    r = O.expert_choice_forward(**L, k=2)  # C = ceil(22 / 3) = 8
+    assert np.array_equal(r.logits, logits) and r.C == 8
+    T, E = logits.shape
+    p = [[0.0] * E for _ in range(T)]
+    for t in range(T):
+        m = max(float(v) for v in logits[t])
+        ex = [math.exp(float(v) - m) for v in logits[t]]
+        p[t] = [v / sum(ex) for v in ex]
+    x, W1, b1, W2, b2 = (L[n] for n in ("x", "W1", "b1", "W2", "b2"))
+    want = np.zeros_like(r.y)
+    for e in range(E):
+        chosen = sorted(range(T), key=lambda t: (-p[t][e], t))[:8]
+        for tok in chosen:
+            h = [0.5 * u * (1 + math.erf(u / math.sqrt(2)))
+                 for u in (b1[e, f] + sum(W1[e, f, j] * x[tok, j] for j in range(4))
+                           for f in range(5))]
+            for i in range(4):
+                want[tok, i] += p[tok][e] * (b2[e, i] + sum(W2[e, i, f] * h[f] for f in range(5)))
+    np.testing.assert_allclose(r.y, want, rtol=1e-12, atol=1e-12)
+    # a token outside every expert's choice gets zero; counts per expert are C
+    assert (r.slot_of >= 0).sum(axis=0).tolist() == [8, 8, 8]
+
+
+def test_expert_choice_token_subset_and_given_selection():
+    """Restricting output rows or passing the oracle's own selection back
+    changes nothing."""
+    L = _rand_layer(T=20, d=6, F=8, E=4, seed=46)
+    a = O.expert_choice_forward(**L, k=2, capacity=7)
+    b = O.expert_choice_forward(**L, k=2, capacity=7, tokens=[19, 3, 8])
+    np.testing.assert_allclose(b.y, a.y[[19, 3, 8]], rtol=1e-12, atol=1e-14)
+    c = O.expert_choice_forward(**L, k=2, capacity=7, sel=a.sel)
+    np.testing.assert_array_equal(c.y, a.y)
+
+
+def test_planted_expert_choice_mistakes_are_caught(monkeypatch):
+    """Plausible expert-choice mistakes, planted on the CPU, fail a pin."""
+    good = O.expert_choice_select
+
+    def ties_to_higher(p, C):  # equal probabilities: the higher token first
+        p = np.asarray(p)
+        T, E = p.shape
+        return np.array([np.sort(np.lexsort((-np.arange(T), -p[:, e]))[:C]) for e in range(E)])
+    monkeypatch.setattr(O, "expert_choice_select", ties_to_higher)
+    with pytest.raises(AssertionError):
+        test_expert_choice_ties_go_to_lower_token()
+
+    def by_logit_rank_per_token(p, C):  # top-C of the token-wise rank instead of p
+        p = np.asarray(p)
+        r = np.argsort(np.argsort(-p, axis=1), axis=1).astype(float)
+        return good(-r + 1e-9 * p, C)
+    monkeypatch.setattr(O, "expert_choice_select", by_logit_rank_per_token)
+    with pytest.raises(AssertionError):
+        test_expert_choice_brute_force_selection()
+    monkeypatch.setattr(O, "expert_choice_select", good)
+
+    good_cap = O.expert_choice_capacity
+    monkeypatch.setattr(O, "expert_choice_capacity",
+                        lambda T, E, k, capacity=None: good_cap(T, E, 1, capacity))  # k ignored
+    with pytest.raises(AssertionError):
+        test_expert_choice_all_tokens_is_soft_mixture()
