@@ -195,19 +195,30 @@ def blas_threads() -> int:
     return os.cpu_count() or 1
 
 
+def oracle_layer(wl, inp):
+    """fn(n): the oracle's layer on the first n tokens as a batch of their own."""
+    from oracle import moe_oracle as O
+    x = inp.as_f32("x")
+    W1, b1, W2, b2 = (inp.as_f32(n) for n in ("W1", "b1", "W2", "b2"))
+    if wl.routing == "expert":
+        return lambda n: O.expert_choice_forward(x[:n], inp.W_r, W1, b1, W2, b2, k=wl.k,
+                                                 capacity=wl.capacity,
+                                                 logit_bias=inp.logit_bias)
+    return lambda n: O.moe_forward(x[:n], inp.W_r, W1, b1, W2, b2, k=wl.k,
+                                   renormalize=wl.renormalize, capacity=wl.capacity,
+                                   logit_bias=inp.logit_bias, layout=False)
+
+
 def cpu_oracle_rate(wl, inp, budget_s: float, min_tokens: int = 64):
     """Tokens/s of the oracle on a token sample sized to the time budget.
 
     The sample is the first n tokens of the batch taken as a batch of its own
     (routing, experts, combine and loss all run on it)."""
-    from oracle import moe_oracle as O
-    x = inp.as_f32("x")
-    W1, b1, W2, b2 = (inp.as_f32(n) for n in ("W1", "b1", "W2", "b2"))
+    layer = oracle_layer(wl, inp)
 
     def run(n):
         t0 = time.perf_counter()
-        O.moe_forward(x[:n], inp.W_r, W1, b1, W2, b2, k=wl.k, renormalize=wl.renormalize,
-                      capacity=wl.capacity, logit_bias=inp.logit_bias, layout=False)
+        layer(n)
         return time.perf_counter() - t0
 
     n0 = min(wl.T, 256)
@@ -223,16 +234,13 @@ def bench_reference(args, wl):
         return 0
     inp = I.make_inputs(wl, seed=0)
     per_step = max(0.5, 150.0 / max(1, args.steps + args.warmup))
-    from oracle import moe_oracle as O
-    x = inp.as_f32("x")
-    W1, b1, W2, b2 = (inp.as_f32(n) for n in ("W1", "b1", "W2", "b2"))
+    layer = oracle_layer(wl, inp)
     # size the per-step sample from one probe step
     rate, n, _, threads = cpu_oracle_rate(wl, inp, per_step)
     n = max(1, min(wl.T, int(rate * per_step)))
 
     def step():
-        O.moe_forward(x[:n], inp.W_r, W1, b1, W2, b2, k=wl.k, renormalize=wl.renormalize,
-                      capacity=wl.capacity, logit_bias=inp.logit_bias, layout=False)
+        layer(n)
 
     for _ in range(args.warmup):
         step()
@@ -273,12 +281,13 @@ def bench_ours(args, wl):
     inp = I.make_inputs(wl, seed=0)
     D = device_inputs(inp, dev)
     layer = MoELayer(D["W_r"], D["W1"], D["b1"], D["W2"], D["b2"], k=wl.k, capacity=wl.capacity,
-                     renormalize=wl.renormalize, logit_bias=D["logit_bias"])
+                     renormalize=wl.renormalize, logit_bias=D["logit_bias"], routing=wl.routing)
     cfg = layer.config(wl.T)
     ws = layer.workspace(wl.T)
     stream = torch.cuda.current_stream(dev)
     T, k, E, d = wl.T, wl.k, wl.E, wl.d
-    n = T * k
+    ec = wl.routing == "expert"
+    n = E * B.expert_choice_capacity(cfg) if ec else T * k  # permuted rows
     i32, f32 = torch.int32, torch.float32
     dt = D["x"].dtype
     buf = dict(idx=torch.empty((T, k), dtype=i32, device=dev),
@@ -286,7 +295,7 @@ def bench_ours(args, wl):
                counts=torch.empty(E, dtype=i32, device=dev),
                aux=torch.empty(1, dtype=f32, device=dev),
                offsets=torch.empty(E + 1, dtype=i32, device=dev),
-               slot_of=torch.empty((T, k), dtype=i32, device=dev),
+               slot_of=torch.empty((T, E if ec else k), dtype=i32, device=dev),
                perm_token=torch.empty(n, dtype=i32, device=dev),
                perm_w=torch.empty(n, dtype=f32, device=dev),
                x_perm=torch.empty((n, d), dtype=dt, device=dev),
@@ -296,6 +305,12 @@ def bench_ours(args, wl):
 
     def stage_route(st):
         b = buf
+        if ec:
+            B.route_expert_choice(cfg, D["x"], D["W_r"], b["offsets"], b["perm_token"],
+                                  b["perm_w"], b["slot_of"], ws, x_perm=b["x_perm"],
+                                  logit_bias=D["logit_bias"], expert_counts=b["counts"],
+                                  stream=st)
+            return
         B.route(cfg, D["x"], D["W_r"], b["idx"], b["w"], ws, logit_bias=D["logit_bias"],
                 expert_counts=b["counts"], aux_out=b["aux"], stream=st)
         B.dispatch(cfg, D["x"], b["idx"], b["offsets"], b["slot_of"], b["perm_token"],
@@ -444,7 +459,8 @@ def bench_ours(args, wl):
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
             "dtype": "bf16" if wl.dtype == "bf16" else "f32", "data": "synthetic",
             "config": {"workload": wl.name, "T": T, "d": d, "d_ff": wl.F, "E": E, "k": k,
-                       "capacity": wl.capacity, "parallelism": f"replicas{world}",
+                       "capacity": wl.capacity, "routing": wl.routing,
+                       "parallelism": f"replicas{world}",
                        "l2": "flushed before every timed step (256 MiB write, untimed)"},
             "tflops": work["flops"] / (ms_per_step * 1e-3) / 1e12 * world,
             "hbm_gbs_algorithmic": work["bytes"] / (ms_per_step * 1e-3) / 1e9 * world,

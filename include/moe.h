@@ -77,7 +77,10 @@ typedef struct moe_config {
     int32_t capacity;    /* < 0: no cap; >= 0: kept assignments per expert at most */
     int32_t renormalize; /* 1: w = p_sel / sum(p_sel); 0: w = p_sel */
     int32_t n_shared;    /* shared experts, 0 .. E-1 (see below); 0 for a plain layer */
+    int32_t routing;     /* moe_routing: MOE_TOKEN_CHOICE (0) or MOE_EXPERT_CHOICE (1) */
 } moe_config;
+
+typedef enum moe_routing { MOE_TOKEN_CHOICE = 0, MOE_EXPERT_CHOICE = 1 } moe_routing;
 
 /*
  * Shared experts ("Design variations": one or more experts always active):
@@ -91,6 +94,30 @@ typedef struct moe_config {
  * y_perm): the k routed choices (expert ids n_shared .. E-1, best first),
  * then the shared experts 0 .. n_shared-1.  k + n_shared <= 8.  With
  * n_shared = 0, K = k and everything below reads as written.
+ */
+
+/*
+ * Expert-choice routing ("Design variations": experts choose their top
+ * tokens, guaranteeing balance), cfg->routing = MOE_EXPERT_CHOICE: the
+ * router computes p = softmax(g) as for token choice, then every expert e
+ * takes the C tokens with the largest p[t][e] - larger first, the lower
+ * token index first among equal p - where
+ *   C = min(T, cfg->capacity)          if cfg->capacity >= 0,
+ *   C = min(T, ceil(T * cfg->k / E))   otherwise (k: experts per token on
+ *                                      average, as top-k token choice);
+ * see moe_expert_choice_capacity.  Expert e's rows are e*C .. e*C + C - 1,
+ * its chosen tokens in ascending token order; a token's output is the sum,
+ * over the experts that chose it (any number, 0 .. E), of p[t][e] times the
+ * expert's output, unnormalised; a token no expert chose gets 0.  There is
+ * no balancing loss: aux_out receives 0; expert_counts receives C for every
+ * expert; the z-loss and logits_out are as for token choice.  The
+ * per-assignment arrays have the expert-choice shapes:
+ *   offsets [E+1] (= e*C), perm_token / perm_w / x_perm / y_perm [E*C],
+ *   slot_of [T][E] (row of (t, e), -1 if e did not choose t).
+ * Calls: moe_route_expert_choice (route + dispatch), then moe_expert_ffn and
+ * moe_combine with the same cfg, or moe_forward.  moe_route, moe_dispatch
+ * and moe_dispatch_noalloc are token-choice steps and return
+ * MOE_ERR_UNSUPPORTED for it; so does n_shared > 0.
  */
 
 /* Bytes of workspace any call below needs for this configuration. */
@@ -151,6 +178,30 @@ moe_status moe_dispatch(const moe_config* cfg, const void* x, const int32_t* top
                         void* ws, size_t ws_bytes, void* stream);
 
 /*
+ * Expert-choice route and dispatch (cfg->routing = MOE_EXPERT_CHOICE; see
+ * above): router logits and p as in moe_route, each expert's top-C tokens,
+ * the row layout and, when x_perm is not NULL, the gather of the rows.
+ *   x, W_r, logit_bias, logit_noise, logits_in, logits_out   as moe_route
+ *   offsets     [E+1] int32           e*C
+ *   perm_token  [E*C] int32           chosen tokens, ascending per expert
+ *   perm_w      [E*C] fp32            p[token][e] of each row
+ *   slot_of     [T][E] int32          row of (t, e), -1 if e did not choose t
+ *   x_perm      [E*C][d] dtype or NULL   x rows of perm_token
+ *   expert_counts [E] int32 or NULL   C for every expert
+ *   z_loss_out  [1] fp32 or NULL      router z-loss as in moe_route
+ */
+moe_status moe_route_expert_choice(const moe_config* cfg, const void* x, const float* W_r,
+                                   const float* logit_bias, const float* logit_noise,
+                                   const float* logits_in, float* logits_out, int32_t* offsets,
+                                   int32_t* perm_token, float* perm_w, int32_t* slot_of,
+                                   void* x_perm, int32_t* expert_counts, float* z_loss_out,
+                                   void* ws, size_t ws_bytes, void* stream);
+
+/* C, the tokens each expert takes under expert-choice routing (formula
+ * above); -1 for an invalid cfg. */
+int32_t moe_expert_choice_capacity(const moe_config* cfg);
+
+/*
  * Experts: for every expert segment, y_perm = w * (GELU(x_perm W1^T + b1)
  * W2^T + b2) ("The MoE layer", expert = Linear, GELU, Linear).
  *   x_perm      [T*k][d] dtype        rows grouped by expert (moe_dispatch)
@@ -159,6 +210,7 @@ moe_status moe_dispatch(const moe_config* cfg, const void* x, const int32_t* top
  *   perm_w      [T*k] fp32 or NULL    per-row weight; NULL means 1
  *   y_perm      [T*k][d] fp32         expert outputs (first offsets[E] rows)
  * The hidden activations live in the workspace (bf16 for bf16 layers).
+ * Expert choice: E*C rows instead of T*k.
  */
 moe_status moe_expert_ffn(const moe_config* cfg, const void* x_perm, const int32_t* offsets,
                           const void* W1, const void* b1, const void* W2, const void* b2,
@@ -171,6 +223,8 @@ moe_status moe_expert_ffn(const moe_config* cfg, const void* x_perm, const int32
  * token with every assignment dropped gets 0 ("The MoE layer", weighted
  * combination; the weights were applied by moe_expert_ffn).
  *   y_perm [T*k][d] fp32, slot_of [T][k] int32, y [T][d] dtype.
+ * Expert choice: k reads E (slot_of [T][E], slots in expert order) and
+ * y_perm has E*C rows.
  */
 moe_status moe_combine(const moe_config* cfg, const float* y_perm, const int32_t* slot_of,
                        void* y, void* stream);

@@ -18,6 +18,7 @@ import torch
 _LIB_PATH = os.path.join(os.path.dirname(os.path.abspath(__file__)), "libmoe.so")
 
 MOE_F32, MOE_BF16 = 0, 1
+MOE_TOKEN_CHOICE, MOE_EXPERT_CHOICE = 0, 1
 STATUS = {0: "ok", 1: "invalid argument", 2: "misaligned pointer or row length",
           3: "workspace missing, misaligned or too small", 4: "unsupported shape",
           5: "CUDA runtime error", 6: "device-side error recorded"}
@@ -26,14 +27,15 @@ EXPORTED = ("moe_workspace_size", "moe_status_string", "moe_route", "moe_dispatc
             "moe_expert_ffn", "moe_combine", "moe_forward", "moe_get_device_error",
             "moe_launch_count", "moe_dispatch_noalloc", "moe_check_wait_timeout",
             "moe_update_balance_bias", "moe_pipeline_workspace_size", "moe_pipeline_create",
-            "moe_pipeline_submit", "moe_pipeline_join", "moe_pipeline_destroy")
+            "moe_pipeline_submit", "moe_pipeline_join", "moe_pipeline_destroy",
+            "moe_route_expert_choice", "moe_expert_choice_capacity")
 
 
 class MoeConfig(ctypes.Structure):
     _fields_ = [("T", ctypes.c_int32), ("d", ctypes.c_int32), ("d_ff", ctypes.c_int32),
                 ("E", ctypes.c_int32), ("k", ctypes.c_int32), ("dtype", ctypes.c_int32),
                 ("capacity", ctypes.c_int32), ("renormalize", ctypes.c_int32),
-                ("n_shared", ctypes.c_int32)]
+                ("n_shared", ctypes.c_int32), ("routing", ctypes.c_int32)]
 
 
 class MoeError(RuntimeError):
@@ -77,6 +79,10 @@ def load() -> ctypes.CDLL:
         lib.moe_check_wait_timeout.argtypes = [_P, ctypes.c_uint64, _P]
         lib.moe_update_balance_bias.restype = ctypes.c_int
         lib.moe_update_balance_bias.argtypes = [cfgp, _P, _P, ctypes.c_float, _P]
+        lib.moe_route_expert_choice.restype = ctypes.c_int
+        lib.moe_route_expert_choice.argtypes = [cfgp] + [_P] * 13 + [_P, sz, _P]
+        lib.moe_expert_choice_capacity.restype = ctypes.c_int32
+        lib.moe_expert_choice_capacity.argtypes = [cfgp]
         lib.moe_pipeline_workspace_size.restype = ctypes.c_size_t
         lib.moe_pipeline_workspace_size.argtypes = [cfgp, ctypes.c_int32]
         lib.moe_pipeline_create.restype = ctypes.c_int
@@ -93,10 +99,14 @@ def load() -> ctypes.CDLL:
 
 
 def config(T, d, d_ff, E, k, dtype="bf16", capacity=None, renormalize=True,
-           n_shared=0) -> MoeConfig:
+           n_shared=0, routing="token") -> MoeConfig:
+    """routing: "token" (each token picks its top-k experts) or "expert" (each
+    expert picks its top-C tokens)."""
+    if routing not in ("token", "expert"):
+        raise ValueError(f"routing must be 'token' or 'expert', not {routing!r}")
     return MoeConfig(T, d, d_ff, E, k, MOE_BF16 if dtype == "bf16" else MOE_F32,
                      -1 if capacity is None else int(capacity), 1 if renormalize else 0,
-                     int(n_shared))
+                     int(n_shared), MOE_EXPERT_CHOICE if routing == "expert" else MOE_TOKEN_CHOICE)
 
 
 def _ptr(t):
@@ -174,6 +184,24 @@ def forward(cfg, x, W_r, W1, b1, W2, b2, y, ws, logit_bias=None, aux_out=None,
         _ptr(b1), _ptr(W2),
         _ptr(b2), _ptr(y), _ptr(aux_out), _ptr(expert_counts), _ptr(logits_out),
         _ptr(z_loss_out), _ptr(ws), ws.numel(), _stream(stream)))
+
+
+def route_expert_choice(cfg, x, W_r, offsets, perm_token, perm_w, slot_of, ws, x_perm=None,
+                        logit_bias=None, logit_noise=None, logits_in=None, logits_out=None,
+                        expert_counts=None, z_loss_out=None, stream=None):
+    """Expert-choice route + dispatch: every expert's top-C tokens, the rows
+    (offsets [E+1], perm_token / perm_w [E*C], slot_of [T][E]) and, with
+    x_perm [E*C][d], the gathered rows."""
+    _check("moe_route_expert_choice", load().moe_route_expert_choice(
+        ctypes.byref(cfg), _ptr(x), _ptr(W_r), _ptr(logit_bias), _ptr(logit_noise),
+        _ptr(logits_in), _ptr(logits_out), _ptr(offsets), _ptr(perm_token), _ptr(perm_w),
+        _ptr(slot_of), _ptr(x_perm), _ptr(expert_counts), _ptr(z_loss_out), _ptr(ws),
+        ws.numel(), _stream(stream)))
+
+
+def expert_choice_capacity(cfg: MoeConfig) -> int:
+    """C, the tokens each expert takes under expert-choice routing."""
+    return int(load().moe_expert_choice_capacity(ctypes.byref(cfg)))
 
 
 def launch_count() -> int:

@@ -30,7 +30,8 @@ __device__ __forceinline__ void store4(__nv_bfloat16* p, float4 v) {
 template <typename TY>
 __global__ void __launch_bounds__(256) combine_kernel(const float* __restrict__ y_perm,
                                                       const int32_t* __restrict__ slot_of, int T,
-                                                      int k, int d, TY* __restrict__ y) {
+                                                      int k, int d, long long rows,
+                                                      TY* __restrict__ y) {
     pdl_wait();
     pdl_trigger();
     const int lane = threadIdx.x % 32;
@@ -47,7 +48,7 @@ __global__ void __launch_bounds__(256) combine_kernel(const float* __restrict__ 
         for (int u = 0; u < 4; ++u) acc[u] = make_float4(0.f, 0.f, 0.f, 0.f);
         for (int j = 0; j < k; ++j) {  // slot order
             int sl = __ldg(slot_of + (size_t)t * k + j);
-            if (sl < 0 || sl >= T * k) continue;  // dropped (y_perm has T*k rows)
+            if (sl < 0 || sl >= rows) continue;  // dropped (or outside y_perm)
             const float4* row = reinterpret_cast<const float4*>(y_perm + (size_t)sl * d);
             float4 q[4];
 #pragma unroll
@@ -70,17 +71,18 @@ __global__ void __launch_bounds__(256) combine_kernel(const float* __restrict__ 
 }  // namespace
 
 cudaError_t launch_combine(const moe_config& c, const float* y_perm, const int32_t* slot_of,
-                           void* y, cudaStream_t s) {
+                           void* y, int64_t rows, cudaStream_t s) {
     if (c.T == 0) return cudaSuccess;
     const long long tasks = (long long)c.T * ((c.d / 4 + 127) / 128);
     long long blocks = (tasks + 7) / 8;
     if (blocks > num_sms() * 8) blocks = num_sms() * 8;
     if (c.dtype == MOE_BF16)
         return launch_kernel(combine_kernel<__nv_bfloat16>, dim3((unsigned)blocks), dim3(256), 0,
-                             s, 1, false, y_perm, slot_of, c.T, c.k, c.d,
+                             s, 1, false, y_perm, slot_of, c.T, c.k, c.d, (long long)rows,
                              reinterpret_cast<__nv_bfloat16*>(y));
     return launch_kernel(combine_kernel<float>, dim3((unsigned)blocks), dim3(256), 0, s, 1, false,
-                         y_perm, slot_of, c.T, c.k, c.d, reinterpret_cast<float*>(y));
+                         y_perm, slot_of, c.T, c.k, c.d, (long long)rows,
+                         reinterpret_cast<float*>(y));
 }
 
 }  // namespace moe

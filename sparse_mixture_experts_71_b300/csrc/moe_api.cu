@@ -57,12 +57,41 @@ moe_status check_config(const moe_config* c) {
     if (c->T < 0 || c->d <= 0 || c->d_ff <= 0 || c->E <= 0 || c->k <= 0) return MOE_ERR_INVALID_ARG;
     if (c->dtype != MOE_F32 && c->dtype != MOE_BF16) return MOE_ERR_INVALID_ARG;
     if (c->renormalize != 0 && c->renormalize != 1) return MOE_ERR_INVALID_ARG;
+    if (c->routing != MOE_TOKEN_CHOICE && c->routing != MOE_EXPERT_CHOICE) return MOE_ERR_INVALID_ARG;
     if (c->n_shared < 0 || c->n_shared >= c->E) return MOE_ERR_INVALID_ARG;
     if (c->k > c->E - c->n_shared) return MOE_ERR_INVALID_ARG;
     if (c->E > kMaxExperts || c->k + c->n_shared > kMaxTopK) return MOE_ERR_UNSUPPORTED;
     if (c->d % 8 != 0 || c->d_ff % 8 != 0) return MOE_ERR_ALIGNMENT;
     if ((int64_t)c->T * (c->k + c->n_shared) > (int64_t)INT32_MAX / 2) return MOE_ERR_UNSUPPORTED;
+    if (c->routing == MOE_EXPERT_CHOICE &&
+        (c->n_shared != 0 || (int64_t)c->T * c->E > (int64_t)INT32_MAX / 2))
+        return MOE_ERR_UNSUPPORTED;
     return MOE_OK;
+}
+
+bool expert_choice(const moe_config& c) { return c.routing == MOE_EXPERT_CHOICE; }
+
+// Router view of an expert-choice layer: p and the z-loss only (its top-1
+// outputs go to scratch and are not used).
+moe_config ec_router_config(const moe_config& c) {
+    moe_config r = c;
+    r.k = 1;
+    r.capacity = -1;
+    r.routing = MOE_TOKEN_CHOICE;
+    return r;
+}
+
+// The combine's view: K slots per token (expert choice: one per expert).
+moe_config combine_config(const moe_config& c) {
+    moe_config r = dispatch_config(c);
+    if (expert_choice(c)) r.k = c.E;
+    return r;
+}
+
+// Rows of the permuted buffers a stand-alone call may address: T*K for token
+// choice (K = k + n_shared), E*C for expert choice.
+int64_t call_rows(const moe_config& c) {
+    return expert_choice(c) ? (int64_t)c.E * ec_capacity(c) : (int64_t)c.T * (c.k + c.n_shared);
 }
 
 moe_status check_ws(const moe_config& c, void* ws, size_t ws_bytes, WsLayout* L) {
@@ -86,6 +115,7 @@ moe_status empty_batch(const moe_config& c, int32_t* expert_counts, float* aux_o
 }
 
 int64_t max_segment(const moe_config& c) {
+    if (expert_choice(c)) return ec_capacity(c);
     int64_t m = c.T;  // a token reaches one expert at most once
     if (c.capacity >= 0 && c.capacity < m) m = c.capacity;
     return m;
@@ -97,16 +127,22 @@ moe_status config_status(const moe_config* c) { return check_config(c); }
 
 WsLayout ws_layout(const moe_config& c) {
     WsLayout L{};
-    const moe_config cr = routed_config(c);
-    const int64_t n = (int64_t)c.T * (c.k + c.n_shared);
+    const bool ec = expert_choice(c);
+    const moe_config cr = ec ? ec_router_config(c) : routed_config(c);
+    // assignments of the router's top-k (token choice: all of them)
+    const int64_t n = (int64_t)c.T * (ec ? 1 : c.k + c.n_shared);
     L.route = route_geom(cr);
     L.count_blocks = (int)((n + kCountBlock - 1) / kCountBlock);
     L.hist_blocks = L.route.blocks > L.count_blocks ? L.route.blocks : L.count_blocks;
     L.rows = n;
-    if (c.capacity >= 0) {  // shared experts keep every token, routed ones at most capacity
+    if (ec) {
+        L.rows = (int64_t)c.E * ec_capacity(c);
+    } else if (c.capacity >= 0) {  // shared experts keep every token, routed ones at most capacity
         const int64_t cap_rows = (int64_t)c.n_shared * c.T + (int64_t)cr.E * c.capacity;
         if (cap_rows < L.rows) L.rows = cap_rows;
     }
+    const int64_t slots = ec ? (int64_t)c.T * c.E : n;    // slot_of entries
+    const int64_t perm = ec ? L.rows : n;                 // perm_token / perm_w entries
     const size_t es = elem_size(c);
     size_t o = 0;
     auto take = [&](size_t bytes) {
@@ -129,12 +165,13 @@ WsLayout ws_layout(const moe_config& c) {
     L.topk_idx = take(sizeof(int32_t) * (size_t)n);
     L.topk_w = take(sizeof(float) * (size_t)n);
     L.offsets = take(sizeof(int32_t) * (size_t)(c.E + 1));
-    L.slot_of = take(sizeof(int32_t) * (size_t)n);
-    L.perm_token = take(sizeof(int32_t) * (size_t)n);
-    L.perm_w = take(sizeof(float) * (size_t)n);
+    L.slot_of = take(sizeof(int32_t) * (size_t)slots);
+    L.perm_token = take(sizeof(int32_t) * (size_t)perm);
+    L.perm_w = take(sizeof(float) * (size_t)perm);
     L.x_perm = take(es * (size_t)L.rows * c.d);
     L.h = take(es * (size_t)L.rows * c.d_ff);
     L.y_perm = take(sizeof(float) * (size_t)L.rows * c.d);
+    L.probs_t = take(ec ? sizeof(float) * (size_t)c.E * c.T : 0);
     L.total = o;
     return L;
 }
@@ -184,6 +221,7 @@ moe_status moe_route(const moe_config* cfg, const void* x, const float* W_r,
     moe_status st = check_config(cfg);
     if (st != MOE_OK) return st;
     const moe_config& c = *cfg;
+    if (expert_choice(c)) return MOE_ERR_UNSUPPORTED;  // moe_route_expert_choice
     WsLayout L;
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
     if (c.T == 0) return empty_batch(c, expert_counts, aux_out, z_loss_out, s);
@@ -215,6 +253,7 @@ moe_status moe_dispatch(const moe_config* cfg, const void* x, const int32_t* top
     moe_status st = check_config(cfg);
     if (st != MOE_OK) return st;
     const moe_config& c = *cfg;
+    if (expert_choice(c)) return MOE_ERR_UNSUPPORTED;  // moe_route_expert_choice
     if (offsets == nullptr) return MOE_ERR_INVALID_ARG;
     if (c.T == 0) {
         const cudaError_t e = cudaMemsetAsync(offsets, 0, sizeof(int32_t) * (c.E + 1),
@@ -255,7 +294,7 @@ moe_status moe_expert_ffn(const moe_config* cfg, const void* x_perm, const int32
     if ((st = check_ws(c, ws, ws_bytes, &L)) != MOE_OK) return st;
     const moe_config cd = dispatch_config(c);
     chain_begin();
-    return from_cuda(launch_expert_ffn(cd, x_perm, (int64_t)cd.T * cd.k, offsets, W1, b1, W2, b2,
+    return from_cuda(launch_expert_ffn(cd, x_perm, call_rows(c), offsets, W1, b1, W2, b2,
                                        perm_w, y_perm, ws, L,
                                        reinterpret_cast<cudaStream_t>(stream)));
 }
@@ -269,7 +308,7 @@ moe_status moe_combine(const moe_config* cfg, const float* y_perm, const int32_t
     if (y_perm == nullptr || slot_of == nullptr || y == nullptr) return MOE_ERR_INVALID_ARG;
     if (!aligned16(y_perm) || !aligned16(y)) return MOE_ERR_ALIGNMENT;
     chain_begin();
-    return from_cuda(launch_combine(dispatch_config(c), y_perm, slot_of, y,
+    return from_cuda(launch_combine(combine_config(c), y_perm, slot_of, y, call_rows(c),
                                     reinterpret_cast<cudaStream_t>(stream)));
 }
 
@@ -300,6 +339,24 @@ moe_status moe_forward(const moe_config* cfg, const void* x, const float* W_r,
     void* x_perm = at<void>(ws, L.x_perm);
     float* y_perm = at<float>(ws, L.y_perm);
     const moe_config cd = dispatch_config(c);
+    if (expert_choice(c)) {
+        // no balancing loss under expert choice: aux is 0
+        if (aux_out && cudaMemsetAsync(aux_out, 0, sizeof(float), s) != cudaSuccess)
+            return MOE_ERR_CUDA;
+        chain_begin();
+        cudaError_t e = launch_route(ec_router_config(c), x, W_r, logit_bias, logit_noise, nullptr,
+                                     logits_out, idx, w, nullptr, nullptr, z_loss_out, ws, L,
+                                     false, s, at<float>(ws, L.probs_t));
+        if (e == cudaSuccess)
+            e = launch_ec_select(c, at<float>(ws, L.probs_t), offsets, perm_token, perm_w,
+                                 slot_of, expert_counts, s);
+        if (e == cudaSuccess) e = launch_ec_gather(c, x, perm_token, x_perm, s);
+        if (e == cudaSuccess)
+            e = launch_expert_ffn(c, x_perm, L.rows, offsets, W1, b1, W2, b2, perm_w, y_perm, ws,
+                                  L, s);
+        if (e == cudaSuccess) e = launch_combine(combine_config(c), y_perm, slot_of, y, L.rows, s);
+        return from_cuda(e);
+    }
     chain_begin();
     cudaError_t e;
     if (c.n_shared == 0) {
@@ -328,8 +385,49 @@ moe_status moe_forward(const moe_config* cfg, const void* x, const float* W_r,
     if (e == cudaSuccess)
         e = launch_expert_ffn(cd, x_perm, L.rows, offsets, W1, b1, W2, b2, perm_w, y_perm, ws,
                               L, s);
-    if (e == cudaSuccess) e = launch_combine(cd, y_perm, slot_of, y, s);
+    if (e == cudaSuccess) e = launch_combine(cd, y_perm, slot_of, y, L.rows, s);
     return from_cuda(e);
+}
+
+moe_status moe_route_expert_choice(const moe_config* cfg, const void* x, const float* W_r,
+                                   const float* logit_bias, const float* logit_noise,
+                                   const float* logits_in, float* logits_out, int32_t* offsets,
+                                   int32_t* perm_token, float* perm_w, int32_t* slot_of,
+                                   void* x_perm, int32_t* expert_counts, float* z_loss_out,
+                                   void* ws, size_t ws_bytes, void* stream) {
+    moe_status st = check_config(cfg);
+    if (st != MOE_OK) return st;
+    const moe_config& c = *cfg;
+    if (!expert_choice(c)) return MOE_ERR_INVALID_ARG;
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    if (offsets == nullptr) return MOE_ERR_INVALID_ARG;
+    if (c.T == 0) {
+        if (cudaMemsetAsync(offsets, 0, sizeof(int32_t) * (c.E + 1), s) != cudaSuccess)
+            return MOE_ERR_CUDA;
+        return empty_batch(c, expert_counts, nullptr, z_loss_out, s);
+    }
+    if (perm_token == nullptr || perm_w == nullptr || slot_of == nullptr) return MOE_ERR_INVALID_ARG;
+    if (logits_in == nullptr && (x == nullptr || W_r == nullptr)) return MOE_ERR_INVALID_ARG;
+    if (x_perm != nullptr && x == nullptr) return MOE_ERR_INVALID_ARG;
+    if (logits_in == nullptr && (!aligned16(x) || !aligned16(W_r))) return MOE_ERR_ALIGNMENT;
+    if (x_perm != nullptr && (!aligned16(x) || !aligned16(x_perm))) return MOE_ERR_ALIGNMENT;
+    WsLayout L;
+    if ((st = check_ws(c, ws, ws_bytes, &L)) != MOE_OK) return st;
+    chain_begin();
+    cudaError_t e = launch_route(ec_router_config(c), x, W_r, logit_bias, logit_noise, logits_in,
+                                 logits_out, at<int32_t>(ws, L.topk_idx), at<float>(ws, L.topk_w),
+                                 nullptr, nullptr, z_loss_out, ws, L, false, s,
+                                 at<float>(ws, L.probs_t));
+    if (e == cudaSuccess)
+        e = launch_ec_select(c, at<float>(ws, L.probs_t), offsets, perm_token, perm_w, slot_of,
+                             expert_counts, s);
+    if (e == cudaSuccess && x_perm != nullptr) e = launch_ec_gather(c, x, perm_token, x_perm, s);
+    return from_cuda(e);
+}
+
+int32_t moe_expert_choice_capacity(const moe_config* cfg) {
+    if (check_config(cfg) != MOE_OK) return -1;
+    return ec_capacity(*cfg);
 }
 
 moe_status moe_update_balance_bias(const moe_config* cfg, const int32_t* expert_counts,

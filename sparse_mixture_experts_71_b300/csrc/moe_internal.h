@@ -77,6 +77,7 @@ struct WsLayout {
     size_t x_perm;       // dtype [rows][d] (moe_forward)
     size_t h;            // dtype [rows][d_ff]
     size_t y_perm;       // fp32  [rows][d] (moe_forward)
+    size_t probs_t;      // fp32  [E][T] router probabilities (expert choice)
     size_t total;
     RouteGeom route;
     int count_blocks;    // blocks of the stand-alone counting kernel
@@ -173,7 +174,17 @@ cudaError_t launch_route(const moe_config& c, const void* x, const float* W_r,
                          const float* logits_in, float* logits_out,
                          int32_t* topk_idx, float* topk_w, int32_t* expert_counts,
                          float* aux_out, float* z_loss_out, void* ws, const WsLayout& L,
-                         bool fuse_count, cudaStream_t s);
+                         bool fuse_count, cudaStream_t s, float* probs_t = nullptr);
+
+// Expert choice (expert_choice.cu): C; the per-expert top-C selection from
+// the router probabilities probs_t [E][T] (offsets, rows, slot_of [T][E]);
+// the gather of the E*C rows.
+int ec_capacity(const moe_config& c);
+cudaError_t launch_ec_select(const moe_config& c, const float* probs_t, int32_t* offsets,
+                             int32_t* perm_token, float* perm_w, int32_t* slot_of,
+                             int32_t* expert_counts, cudaStream_t s);
+cudaError_t launch_ec_gather(const moe_config& c, const void* x, const int32_t* perm_token,
+                             void* x_perm, cudaStream_t s);
 
 // Shared experts: K = k + n_shared columns per token from the router's k
 // routed choices (ids offset by n_shared) followed by the shared experts with
@@ -209,7 +220,8 @@ cudaError_t launch_expert_ffn(const moe_config& c, const void* x_perm, int64_t x
                               const void* W2, const void* b2, const float* perm_w, float* y_perm,
                               void* ws, const WsLayout& L, cudaStream_t s);
 
+// rows: rows of y_perm (slots at or past it are skipped as dropped).
 cudaError_t launch_combine(const moe_config& c, const float* y_perm, const int32_t* slot_of,
-                           void* y, cudaStream_t s);
+                           void* y, int64_t rows, cudaStream_t s);
 
 }  // namespace moe

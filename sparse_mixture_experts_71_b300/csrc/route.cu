@@ -743,8 +743,9 @@ cudaError_t launch_route(const moe_config& c, const void* x, const float* W_r,
                          const float* logits_in, float* logits_out,
                          int32_t* topk_idx, float* topk_w, int32_t* expert_counts,
                          float* aux_out, float* z_loss_out, void* ws, const WsLayout& L,
-                         bool fuse_count, cudaStream_t s) {
+                         bool fuse_count, cudaStream_t s, float* probs_t) {
     RouteArgs a;
+    a.probs_t = probs_t;
     a.x = x; a.W_r = W_r; a.bias = logit_bias; a.logits_in = logits_in; a.logits_out = logits_out;
     a.noise = logits_in != nullptr ? nullptr : logit_noise;  // logits_in replaces all terms
     a.topk_idx = topk_idx; a.topk_w = topk_w; a.expert_counts = expert_counts; a.aux_out = aux_out;
@@ -772,6 +773,7 @@ cudaError_t launch_route(const moe_config& c, const void* x, const float* W_r,
                                   : launch_e<float>(a, L.route, s);
     }
     if (err != cudaSuccess || fuse_count) return err;
+    if (expert_counts == nullptr && aux_out == nullptr && z_loss_out == nullptr) return err;
     return launch_kernel(route_finish_kernel, dim3(1), dim3(256), 0, s, 1, false,
                          route_loss_args(c, ws, L, expert_counts, aux_out, z_loss_out));
 }

@@ -22,6 +22,7 @@ struct RouteArgs {
     const float* noise;   // [T][E] added to the logits (noisy gating) or null
     const float* logits_in;
     float* logits_out;
+    float* probs_t;       // [E][T] router probabilities (expert choice) or null
     int32_t* topk_idx;
     float* topk_w;
     int32_t* expert_counts;
@@ -84,6 +85,13 @@ __device__ void finish_block(const RouteArgs& a, const float* s_p, int lds, int 
 #pragma unroll
         for (int o = 16; o > 0; o >>= 1) z += __shfl_xor_sync(0xffffffffu, z, o);
         if (tid == 0) a.blk_z[blockIdx.x] = z;
+    }
+    if (a.probs_t != nullptr) {  // transposed, token-contiguous per expert
+        const int n = min(TB, a.T - t0);
+        for (int i = tid; i < n * a.E; i += kThreads) {
+            const int e = i / n, tok = i % n;
+            a.probs_t[(size_t)e * a.T + t0 + tok] = s_p[tok * lds + e];
+        }
     }
     for (int e = tid; e < a.E; e += kThreads) {
         float v = 0.f;

@@ -64,6 +64,7 @@ class Workload:
     zipf_bias: float = 0.0
     init: str = "normal"
     n_shared: int = 0  # experts 0 .. n_shared-1 always active (the router covers the rest)
+    routing: str = "token"  # "token": top-k experts per token; "expert": top-C tokens per expert
     note: str = field(default="", compare=False)
 
     def with_(self, **kw) -> "Workload":
@@ -86,10 +87,13 @@ WORKLOADS: dict[str, Workload] = {
                  note="decode-sized batch, HBM weight streaming"),
         Workload("finegrained-bf16-T4096-d2048-F1024-E64-top6", 4096, 2048, 1024, 64, 6,
                  note="fine-grained experts: many small experts, larger k"),
+        Workload("expertchoice-bf16-T4096-d1024-F4096-E8-C1024", 4096, 1024, 4096, 8, 2,
+                 routing="expert", note="expert-choice routing: each expert takes its top "
+                 "C = T k / E = 1024 tokens (the default workload's shape)"),
     )
 }
 
-TINY, MEDIUM, LARGE, SWITCH, DECODE, FINEGRAINED = WORKLOADS.values()
+TINY, MEDIUM, LARGE, SWITCH, DECODE, FINEGRAINED, EXPERTCHOICE = WORKLOADS.values()
 
 
 @dataclass

@@ -22,7 +22,7 @@ NEAR_TIE = 1e-6
 
 def cfg_of(wl):
     return B.config(wl.T, wl.d, wl.F, wl.E, wl.k, wl.dtype, wl.capacity, wl.renormalize,
-                    wl.n_shared)
+                    wl.n_shared, routing=wl.routing)
 
 
 def y_error(y_gpu: np.ndarray, y_ref: np.ndarray):
@@ -91,6 +91,35 @@ class GpuRun:
         B.dispatch(self.cfg, D["x"], r["idx"], r["offsets"], r["slot_of"], r["perm_token"],
                    r["x_perm"], self.ws, topk_w=r["w"], perm_w=r["perm_w"], stream=self.stream)
         r["y_perm"] = torch.empty((max(n, 1), wl.d), dtype=torch.float32, device=cuda)
+        B.expert_ffn(self.cfg, r["x_perm"], r["offsets"], D["W1"], D["b1"], D["W2"], D["b2"],
+                     r["y_perm"], self.ws, perm_w=r["perm_w"], stream=self.stream)
+        r["y"] = torch.empty((T, wl.d), dtype=dt, device=cuda)
+        B.combine(self.cfg, r["y_perm"], r["slot_of"], r["y"], stream=self.stream)
+        torch.cuda.synchronize()
+        return r
+
+    def staged_ec(self, logits_in=None, noise=None):
+        """Expert choice: route_expert_choice (with the gather), expert_ffn,
+        combine."""
+        wl, D, T, E = self.wl, self.dev, self.wl.T, self.wl.E
+        C = B.expert_choice_capacity(self.cfg)
+        R = max(E * C, 1)
+        dt, cuda = D["x"].dtype, D["x"].device
+        r = {"C": C}
+        r["logits"] = torch.empty((T, E), dtype=torch.float32, device=cuda)
+        r["offsets"] = torch.full((E + 1,), -7, dtype=torch.int32, device=cuda)
+        r["perm_token"] = torch.full((R,), -7, dtype=torch.int32, device=cuda)
+        r["perm_w"] = torch.empty(R, dtype=torch.float32, device=cuda)
+        r["slot_of"] = torch.full((T, E), -7, dtype=torch.int32, device=cuda)
+        r["x_perm"] = torch.empty((R, wl.d), dtype=dt, device=cuda)
+        r["counts"] = torch.full((E,), -7, dtype=torch.int32, device=cuda)
+        r["z"] = torch.full((1,), -1.0, dtype=torch.float32, device=cuda)
+        B.route_expert_choice(self.cfg, D["x"], D["W_r"], r["offsets"], r["perm_token"],
+                              r["perm_w"], r["slot_of"], self.ws, x_perm=r["x_perm"],
+                              logit_bias=D["logit_bias"], logit_noise=noise,
+                              logits_in=logits_in, logits_out=r["logits"],
+                              expert_counts=r["counts"], z_loss_out=r["z"], stream=self.stream)
+        r["y_perm"] = torch.empty((R, wl.d), dtype=torch.float32, device=cuda)
         B.expert_ffn(self.cfg, r["x_perm"], r["offsets"], D["W1"], D["b1"], D["W2"], D["b2"],
                      r["y_perm"], self.ws, perm_w=r["perm_w"], stream=self.stream)
         r["y"] = torch.empty((T, wl.d), dtype=dt, device=cuda)

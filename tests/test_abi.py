@@ -135,3 +135,36 @@ def test_pipeline_workspace_and_host_rejections():
     assert lib.moe_pipeline_submit(None, FAKE, FAKE, None) == 1
     assert lib.moe_pipeline_join(None) == 1
     assert lib.moe_pipeline_destroy(None) == 0
+
+
+def test_expert_choice_host_side():
+    lib = B.load()
+    ec = B.config(4096, 1024, 4096, 8, 2, routing="expert")
+    assert B.expert_choice_capacity(ec) == 1024                                   # ceil(T k / E)
+    assert B.expert_choice_capacity(B.config(10, 64, 64, 3, 1, routing="expert")) == 4
+    assert B.expert_choice_capacity(B.config(10, 64, 64, 3, 1, capacity=50, routing="expert")) == 10
+    assert B.expert_choice_capacity(B.config(10, 64, 64, 3, 1, capacity=0, routing="expert")) == 0
+    assert B.expert_choice_capacity(B.config(10, 64, 64, 3, 9, routing="expert")) == -1
+    # E*C permuted rows, a [T][E] slot map and the [E][T] probabilities
+    assert B.workspace_size(ec) >= 8 * 1024 * (1024 * 2 + 4096 * 2 + 1024 * 4) + 2 * 4096 * 8 * 4
+    bad = B.config(16, 64, 64, 4, 2)
+    bad.routing = 2
+    assert B.workspace_size(bad) == 0
+    cr = ctypes.byref(B.config(16, 64, 64, 4, 2, routing="expert"))
+    need = B.workspace_size(B.config(16, 64, 64, 4, 2, routing="expert"))
+    # the token-choice steps refuse an expert-choice layer, and the reverse
+    assert lib.moe_route(cr, FAKE, FAKE, None, None, None, None, FAKE, FAKE, None, None, None, FAKE,
+                         need, None) == 4
+    assert lib.moe_dispatch(cr, FAKE, FAKE, None, FAKE, FAKE, FAKE, None, FAKE, FAKE, need,
+                            None) == 4
+    assert lib.moe_dispatch_noalloc(cr, FAKE, FAKE, None, FAKE, FAKE, FAKE, None, FAKE, None) == 4
+    tc = ctypes.byref(B.config(16, 64, 64, 4, 2))
+    args = (FAKE, FAKE, None, None, None, None, FAKE, FAKE, FAKE, FAKE, None, None, None)
+    assert lib.moe_route_expert_choice(tc, *args, FAKE, need, None) == 1
+    assert lib.moe_route_expert_choice(cr, *args, FAKE, need - 1, None) == 3
+    assert lib.moe_route_expert_choice(cr, FAKE, FAKE, None, None, None, None, FAKE, None, FAKE,
+                                       FAKE, None, None, None, FAKE, need, None) == 1
+    # shared experts are not combined with expert choice
+    sh = ctypes.byref(B.config(16, 64, 64, 4, 1, n_shared=1, routing="expert"))
+    assert lib.moe_forward(sh, FAKE, FAKE, None, None, FAKE, FAKE, FAKE, FAKE, FAKE, None, None,
+                           None, None, FAKE, 1 << 40, None) == 4
