@@ -36,6 +36,16 @@ the combine and of the auxiliary loss did not survive extraction):
 * auxiliary-loss-free balancing moves the per-expert logit bias by a fixed
   step toward balanced load after a batch: minus the step for an expert
   above the mean assignment count, plus it below, unchanged at the mean;
+* rerouting on overflow ("passed to the next-best expert") is one hop: after
+  the drop pass above, the r-th dropped slot of a token (r = 0, 1, ...) is
+  offered to the token's (k + r)-th ranked expert (the best one it does not
+  use); offers are visited in (token, slot) order and an expert accepts them
+  while its kept assignments plus accepted offers stay below the capacity;
+  a refused offer is dropped.  The slot's weight becomes the new expert's
+  probability, with the same normalisation as the token's other weights
+  (divided by the sum over its k choices when renormalising).  An expert's
+  rows are its first-pass assignments in token order, then the offers it
+  accepted in token order;
 * expert-choice routing ("experts choose their top tokens") ranks, for each
   expert, the batch's tokens by their router probability p[t, e] (the same
   softmax over experts as token choice), larger first and the lower token
@@ -153,6 +163,66 @@ def capacity_keep(idx, E: int, capacity: int | None, n_shared: int = 0) -> np.nd
             else:
                 kept[t, j] = False
     return kept
+
+
+def reroute_keep(ranked, k: int, E: int, capacity: int | None):
+    """Drop, then offer each dropped slot once to the token's next-best expert.
+
+    [LECTURE] "The central problem: load balancing" (overflow tokens are
+    dropped or rerouted); [GLOSSARY] expert capacity (tokens may be passed to
+    the next-best expert).  ``ranked`` (T, K2) lists each token's experts best
+    first, its k choices then the next K2 - k.  First pass: ``capacity_keep``
+    on the k choices.  Second pass: the r-th dropped slot of token t is
+    offered to ranked[t, k + r] (when k + r < K2); offers in (token, slot)
+    order; expert e accepts while first-pass keeps + accepted offers <
+    capacity.  Returns final (T, k) expert ids (-1: dropped) and the pass
+    (T, k) that placed each slot (1, 2; 0 if dropped).
+    """
+    ranked = np.asarray(ranked)
+    T, K2 = ranked.shape
+    first = ranked[:, :k]
+    kept = capacity_keep(first, E, capacity)
+    final = np.where(kept, first, -1).astype(np.int64)
+    phase = kept.astype(np.int64)
+    if capacity is None:
+        return final, phase
+    load = np.bincount(first[kept].astype(np.int64), minlength=E)
+    for t in range(T):
+        r = 0
+        for j in range(k):
+            if kept[t, j]:
+                continue
+            if k + r < K2:
+                e = int(ranked[t, k + r])
+                if load[e] < capacity:
+                    load[e] += 1
+                    final[t, j] = e
+                    phase[t, j] = 2
+            r += 1
+    return final, phase
+
+
+def reroute_layout(final, phase, E: int):
+    """Rows of a rerouted batch: per expert, its first-pass slots in token
+    order, then the offers it accepted in token order.  Returns offsets
+    (E+1,), slot_of (T, k) and perm_token (n_kept,)."""
+    final, phase = np.asarray(final), np.asarray(phase)
+    T, k = final.shape
+    offsets = np.zeros(E + 1, np.int64)
+    for e in range(E):
+        offsets[e + 1] = offsets[e] + int(np.sum(final == e))
+    slot_of = np.full((T, k), -1, np.int64)
+    perm_token = np.zeros(int(offsets[E]), np.int64)
+    for e in range(E):
+        pos = int(offsets[e])
+        for ph in (1, 2):
+            for t in range(T):
+                for j in range(k):
+                    if final[t, j] == e and phase[t, j] == ph:
+                        slot_of[t, j] = pos
+                        perm_token[pos] = t
+                        pos += 1
+    return offsets, slot_of, perm_token
 
 
 def gelu(u) -> np.ndarray:
@@ -277,7 +347,7 @@ class OracleResult:
 def moe_forward(x, W_r, W1, b1, W2, b2, k: int, renormalize: bool = True,
                 capacity: int | None = None, logit_bias=None, logits=None,
                 tokens=None, layout: bool = True, logit_noise=None,
-                n_shared: int = 0) -> OracleResult:
+                n_shared: int = 0, reroute: bool = False) -> OracleResult:
     """The MoE layer forward pass, looping over experts.
 
     [LECTURE] "The MoE layer": router logits and softmax, top-k selection,
@@ -298,6 +368,12 @@ def moe_forward(x, W_r, W1, b1, W2, b2, k: int, renormalize: bool = True,
     softmax, the top-k, the loss) covers the routed experts n_shared .. E-1.
     idx, w and kept then have k + n_shared columns: the k routed choices, then
     the shared experts.
+
+    ``reroute``: an assignment the cap drops is offered to the token's
+    next-best expert (``reroute_keep``); ``idx`` then holds each slot's final
+    expert (the original choice when not dropped), ``w`` its weight and
+    ``kept`` whether it survived; ``counts`` stay those of the k choices; the
+    layout follows ``reroute_layout``.  Not combined with shared experts.
     """
     x = np.asarray(x)
     T, d = x.shape
@@ -314,10 +390,28 @@ def moe_forward(x, W_r, W1, b1, W2, b2, k: int, renormalize: bool = True,
     if n_shared:
         idx = np.concatenate([idx, np.tile(np.arange(n_shared, dtype=idx.dtype), (T, 1))], 1)
         w = np.concatenate([w, np.ones((T, n_shared))], 1)
-    kept = capacity_keep(idx, E, capacity, n_shared)
-    if layout:
+    if reroute:
+        if n_shared:
+            raise ValueError("rerouting is not combined with shared experts")
+        ranked = top_k(logits, min(2 * k, E))
+        final, phase = reroute_keep(ranked, k, E, capacity)
+        counts = np.bincount(idx.ravel().astype(np.int64), minlength=E)
+        rows = np.arange(T)[:, None]
+        den = probs[rows, idx].sum(axis=1, keepdims=True) if renormalize else np.ones((T, 1))
+        moved = phase == 2
+        w = np.where(moved, probs[rows, np.maximum(final, 0)] / den, w)
+        idx = np.where(moved, final, idx).astype(idx.dtype)
+        kept = final >= 0
+        kept_count = np.bincount(final[kept], minlength=E)
+        if layout:
+            offsets, slot_of, perm_token = reroute_layout(final, phase, E)
+        else:
+            offsets = slot_of = perm_token = None
+    elif layout:
+        kept = capacity_keep(idx, E, capacity, n_shared)
         counts, kept_count, offsets, slot_of, perm_token = dispatch_layout(idx, kept, E)
     else:
+        kept = capacity_keep(idx, E, capacity, n_shared)
         counts = kept_count = offsets = slot_of = perm_token = None
     tokens = np.arange(T) if tokens is None else np.asarray(tokens, np.int64)
     y = np.zeros((len(tokens), d), f64)

@@ -665,3 +665,157 @@ def test_planted_expert_choice_mistakes_are_caught(monkeypatch):
                         lambda T, E, k, capacity=None: good_cap(T, E, 1, capacity))  # k ignored
     with pytest.raises(AssertionError):
         test_expert_choice_all_tokens_is_soft_mixture()
+
+
+# ---- rerouting on overflow ("passed to the next-best expert"); the reading
+# (one hop, offers after the drop pass, in token order) is in the oracle's header
+
+def test_reroute_hand_worked():
+    """Capacity 1, three experts, four tokens that all prefer expert 0, with
+    second choices 1, 1, 2, 1.  Drop pass: token 0 keeps expert 0, tokens
+    1-3 are dropped.  Offers in token order: token 1 -> expert 1 (room),
+    token 2 -> expert 2 (room), token 3 -> expert 1 (full: dropped).
+    Rows: expert 0 [t0], expert 1 [t1], expert 2 [t2]."""
+    ranked = np.array([[0, 1], [0, 1], [0, 2], [0, 1]])
+    final, phase = O.reroute_keep(ranked, 1, 3, 1)
+    assert final[:, 0].tolist() == [0, 1, 2, -1]
+    assert phase[:, 0].tolist() == [1, 2, 2, 0]
+    offsets, slot_of, perm_token = O.reroute_layout(final, phase, 3)
+    assert offsets.tolist() == [0, 1, 2, 3]
+    assert slot_of[:, 0].tolist() == [0, 1, 2, -1]
+    assert perm_token.tolist() == [0, 1, 2]
+
+
+def test_reroute_two_slot_order_and_rows():
+    """k = 2, capacity 2, E = 4.  Token choices (best first, then next-best):
+    t0 (0,1 | 2,3), t1 (0,1 | 3,2), t2 (0,1 | 2,3), t3 (1,0 | 2,3).
+    Drop pass keeps t0 and t1 on experts 0 and 1 and drops all of t2, t3.
+    Offers: t2 slot 0 -> its 3rd expert 2 (ok), t2 slot 1 -> its 4th expert 3
+    (ok), t3 slot 0 -> 2 (ok: 2 is at 1 of 2), t3 slot 1 -> 3 (ok).  Expert 2
+    rows [t2, t3] and expert 3 rows [t2, t3], all after the (empty) drop-pass
+    rows."""
+    ranked = np.array([[0, 1, 2, 3], [0, 1, 3, 2], [0, 1, 2, 3], [1, 0, 2, 3]])
+    final, phase = O.reroute_keep(ranked, 2, 4, 2)
+    assert final.tolist() == [[0, 1], [0, 1], [2, 3], [2, 3]]
+    assert phase.tolist() == [[1, 1], [1, 1], [2, 2], [2, 2]]
+    offsets, slot_of, perm_token = O.reroute_layout(final, phase, 4)
+    assert offsets.tolist() == [0, 2, 4, 6, 8]
+    assert perm_token.tolist() == [0, 1, 0, 1, 2, 3, 2, 3]
+    assert slot_of.tolist() == [[0, 2], [1, 3], [4, 6], [5, 7]]
+
+
+@pytest.mark.parametrize("n0,C", [(700, 400), (300, 400), (900, 300), (1000, 1000), (500, 0)])
+def test_reroute_two_experts_closed_form(n0, C):
+    """Top-1 over two experts, n0 of 1000 tokens prefer expert 0: the drop
+    pass keeps min(n0, C) and min(n1, C); each expert then accepts the other's
+    overflow up to its spare room, so the kept totals are
+    min(n0, C) + min(n1 - min(n1, C), C - min(n0, C)) on expert 0 and the
+    mirror on expert 1."""
+    T = 1000
+    rng = np.random.default_rng(n0 + C)
+    first = np.zeros(T, np.int64)
+    first[rng.permutation(T)[:T - n0]] = 1
+    ranked = np.stack([first, 1 - first], axis=1)
+    final, _ = O.reroute_keep(ranked, 1, 2, C)
+    n1 = T - n0
+    k0, k1 = min(n0, C), min(n1, C)
+    want0 = k0 + min(n1 - k1, C - k0)
+    want1 = k1 + min(n0 - k0, C - k1)
+    assert int(np.sum(final == 0)) == want0 and int(np.sum(final == 1)) == want1
+    # invariants: a moved token went to its other expert, none exceeds C
+    assert np.all((final[:, 0] == -1) | (final[:, 0] == first) | (final[:, 0] == 1 - first))
+
+
+def test_reroute_invariants_random():
+    """Random rankings: the drop pass is capacity_keep's, no expert exceeds
+    the cap, a moved slot lands on the token's (k + r)-th expert, and an offer
+    is refused only when its expert was full at that point in token order."""
+    rng = np.random.default_rng(47)
+    for T, E, k, C in ((40, 5, 2, 6), (60, 8, 1, 5), (30, 4, 2, 3), (25, 6, 3, 4)):
+        ranked = np.array([rng.permutation(E)[:min(2 * k, E)] for _ in range(T)])
+        final, phase = O.reroute_keep(ranked, k, E, C)
+        kept1 = O.capacity_keep(ranked[:, :k], E, C)
+        assert np.array_equal(phase == 1, kept1)
+        assert np.all(np.bincount(final[final >= 0], minlength=E) <= C)
+        load = np.bincount(ranked[:, :k][kept1], minlength=E)
+        for t in range(T):
+            r = 0
+            for j in range(k):
+                if kept1[t, j]:
+                    continue
+                if k + r < ranked.shape[1]:
+                    e = ranked[t, k + r]
+                    if phase[t, j] == 2:
+                        assert final[t, j] == e and load[e] < C
+                        load[e] += 1
+                    else:
+                        assert final[t, j] == -1 and load[e] >= C
+                r += 1
+
+
+def test_reroute_forward():
+    """No cap or a cap >= T: rerouting changes nothing.  With a cap: the
+    moved slot carries the new expert's renormalised probability, the layer
+    equals the dense masked evaluation with those gates (torch, fp64), and
+    it keeps at least as many assignments as dropping."""
+    L = _rand_layer(T=24, d=6, F=8, E=4, seed=48)
+    a = O.moe_forward(**L, k=2)
+    b = O.moe_forward(**L, k=2, capacity=24, reroute=True)
+    assert np.array_equal(a.y, b.y) and np.array_equal(a.slot_of, b.slot_of)
+    bias = np.array([2.0, 0.0, 0.0, -1.0], np.float32)  # expert 0 overflows, 3 has room
+    r = O.moe_forward(**L, k=2, capacity=14, reroute=True, logit_bias=bias)
+    d = O.moe_forward(**L, k=2, capacity=14, logit_bias=bias)
+    assert r.kept.sum() > d.kept.sum()
+    assert np.array_equal(r.counts, d.counts)  # counts are the k choices'
+    p = r.probs
+    top = O.top_k(r.logits, 2)
+    den = np.take_along_axis(p, top, 1).sum(1)
+    t = {n: torch.from_numpy(v) for n, v in L.items()}
+    want = np.zeros_like(r.y)
+    for tok in range(24):
+        for j in range(2):
+            if not r.kept[tok, j]:
+                continue
+            e = int(r.idx[tok, j])
+            assert abs(r.w[tok, j] - p[tok, e] / den[tok]) <= 1e-15
+            fe = TF.linear(TF.gelu(TF.linear(t["x"][tok], t["W1"][e], t["b1"][e])), t["W2"][e],
+                           t["b2"][e]).numpy()
+            want[tok] += r.w[tok, j] * fe
+    np.testing.assert_allclose(r.y, want, rtol=1e-12, atol=1e-14)
+    # the moved slots are exactly the dropped slots whose next-best had room
+    moved = r.kept & ~d.kept
+    assert moved.sum() > 0 and np.all(r.idx[moved] != top[moved])
+
+
+def test_planted_reroute_mistakes_are_caught(monkeypatch):
+    """Offers that ignore the drop pass's load, or that go to the token's
+    (k+1)-th expert for every dropped slot, fail a reroute pin."""
+    good = O.reroute_keep
+
+    def fresh_load(ranked, k, E, capacity):  # room counted from zero, not after the drop pass
+        ranked = np.asarray(ranked)
+        final, phase = good(ranked, k, E, capacity)
+        kept = O.capacity_keep(ranked[:, :k], E, capacity)
+        load = np.zeros(E, np.int64)
+        for t in range(ranked.shape[0]):
+            r = 0
+            for j in range(k):
+                if kept[t, j]:
+                    continue
+                if k + r < ranked.shape[1] and load[ranked[t, k + r]] < capacity:
+                    load[ranked[t, k + r]] += 1
+                    final[t, j], phase[t, j] = ranked[t, k + r], 2
+                r += 1
+        return final, phase
+    monkeypatch.setattr(O, "reroute_keep", fresh_load)
+    with pytest.raises(AssertionError):
+        test_reroute_two_experts_closed_form(700, 400)
+    monkeypatch.setattr(O, "reroute_keep", good)
+
+    def same_alternate(ranked, k, E, capacity):  # every dropped slot offered to rank k
+        ranked = np.array(ranked)
+        ranked[:, k + 1:] = ranked[:, k:k + 1]
+        return good(ranked, k, E, capacity)
+    monkeypatch.setattr(O, "reroute_keep", same_alternate)
+    with pytest.raises(AssertionError):
+        test_reroute_two_slot_order_and_rows()
