@@ -206,7 +206,8 @@ def oracle_layer(wl, inp):
                                                  logit_bias=inp.logit_bias)
     return lambda n: O.moe_forward(x[:n], inp.W_r, W1, b1, W2, b2, k=wl.k,
                                    renormalize=wl.renormalize, capacity=wl.capacity,
-                                   logit_bias=inp.logit_bias, layout=False)
+                                   logit_bias=inp.logit_bias, layout=False,
+                                   reroute=wl.overflow == "reroute")
 
 
 def cpu_oracle_rate(wl, inp, budget_s: float, min_tokens: int = 64):
@@ -281,7 +282,8 @@ def bench_ours(args, wl):
     inp = I.make_inputs(wl, seed=0)
     D = device_inputs(inp, dev)
     layer = MoELayer(D["W_r"], D["W1"], D["b1"], D["W2"], D["b2"], k=wl.k, capacity=wl.capacity,
-                     renormalize=wl.renormalize, logit_bias=D["logit_bias"], routing=wl.routing)
+                     renormalize=wl.renormalize, logit_bias=D["logit_bias"], routing=wl.routing,
+                     overflow=wl.overflow)
     cfg = layer.config(wl.T)
     ws = layer.workspace(wl.T)
     stream = torch.cuda.current_stream(dev)
@@ -290,8 +292,9 @@ def bench_ours(args, wl):
     n = E * B.expert_choice_capacity(cfg) if ec else T * k  # permuted rows
     i32, f32 = torch.int32, torch.float32
     dt = D["x"].dtype
-    buf = dict(idx=torch.empty((T, k), dtype=i32, device=dev),
-               w=torch.empty((T, k), dtype=f32, device=dev),
+    kr = B.ranked_columns(cfg)  # router columns (rerouting: the next-best experts too)
+    buf = dict(idx=torch.empty((T, kr), dtype=i32, device=dev),
+               w=torch.empty((T, kr), dtype=f32, device=dev),
                counts=torch.empty(E, dtype=i32, device=dev),
                aux=torch.empty(1, dtype=f32, device=dev),
                offsets=torch.empty(E + 1, dtype=i32, device=dev),
@@ -459,7 +462,7 @@ def bench_ours(args, wl):
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
             "dtype": "bf16" if wl.dtype == "bf16" else "f32", "data": "synthetic",
             "config": {"workload": wl.name, "T": T, "d": d, "d_ff": wl.F, "E": E, "k": k,
-                       "capacity": wl.capacity, "routing": wl.routing,
+                       "capacity": wl.capacity, "routing": wl.routing, "overflow": wl.overflow,
                        "parallelism": f"replicas{world}",
                        "l2": "flushed before every timed step (256 MiB write, untimed)"},
             "tflops": work["flops"] / (ms_per_step * 1e-3) / 1e12 * world,

@@ -78,9 +78,31 @@ typedef struct moe_config {
     int32_t renormalize; /* 1: w = p_sel / sum(p_sel); 0: w = p_sel */
     int32_t n_shared;    /* shared experts, 0 .. E-1 (see below); 0 for a plain layer */
     int32_t routing;     /* moe_routing: MOE_TOKEN_CHOICE (0) or MOE_EXPERT_CHOICE (1) */
+    int32_t overflow;    /* moe_overflow: MOE_DROP (0) or MOE_REROUTE (1); see below */
 } moe_config;
 
 typedef enum moe_routing { MOE_TOKEN_CHOICE = 0, MOE_EXPERT_CHOICE = 1 } moe_routing;
+typedef enum moe_overflow { MOE_DROP = 0, MOE_REROUTE = 1 } moe_overflow;
+
+/*
+ * Rerouting on overflow ("The central problem: load balancing": overflow
+ * tokens are dropped or rerouted; passed to the next-best expert),
+ * cfg->overflow = MOE_REROUTE, token choice only, n_shared = 0: after the
+ * capacity drop (as above), the r-th dropped slot of a token (r = 0, 1, ...)
+ * is offered once to the token's (k + r)-th ranked expert, the best one it
+ * does not use; offers are taken in (token, slot) order and an expert
+ * accepts them while its kept assignments plus accepted offers stay below
+ * the capacity; a refused offer is dropped.  An accepted slot's weight is
+ * the new expert's probability with the normalisation of the token's other
+ * weights (divided by the sum over its k choices when renormalising).
+ * Expert e's rows are its kept slots in token order, then the offers it
+ * accepted in token order.  The router then ranks K2 = min(2k, E) experts
+ * per token: moe_route writes topk_idx / topk_w with K2 columns (the k
+ * choices, then the next K2 - k, weights normalised as the choices'), and
+ * moe_dispatch reads them so; expert_counts and the auxiliary loss count the
+ * k choices only.  slot_of, perm_* and the other per-assignment arrays keep
+ * their k columns (slot_of[t][j]: the row slot j ended in).  K2 <= 8.
+ */
 
 /*
  * Shared experts ("Design variations": one or more experts always active):
@@ -141,7 +163,8 @@ const char* moe_status_string(moe_status s);
  *                                     logit_bias and logit_noise are then
  *                                     not read)
  *   logits_out  [T][E] fp32 or NULL   receives the logits used for routing
- *   topk_idx    [T][k] int32          selected experts, best first
+ *   topk_idx    [T][k] int32          selected experts, best first ([T][K2]
+ *                                     with MOE_REROUTE, see above)
  *   topk_w      [T][k] fp32           gate weights of the selected experts
  *   expert_counts [E] int32 or NULL   assignments per expert, all k slots,
  *                                     before any capacity drop
@@ -163,7 +186,8 @@ moe_status moe_route(const moe_config* cfg, const void* x, const float* W_r,
  * tokens; "The central problem: load balancing", capacity).
  *   x           [T][d] dtype
  *   topk_idx    [T][k] int32          from moe_route (values outside [0, E)
- *                                     are skipped and flagged)
+ *                                     are skipped and flagged; [T][K2] with
+ *                                     MOE_REROUTE, and so topk_w)
  *   topk_w      [T][k] fp32 or NULL   gate weights; if given, copied to perm_w
  *   offsets     [E+1] int32           segment starts; offsets[E] = kept total
  *   slot_of     [T][k] int32          row of each assignment, -1 if dropped

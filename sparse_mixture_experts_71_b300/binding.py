@@ -19,6 +19,7 @@ _LIB_PATH = os.path.join(os.path.dirname(os.path.abspath(__file__)), "libmoe.so"
 
 MOE_F32, MOE_BF16 = 0, 1
 MOE_TOKEN_CHOICE, MOE_EXPERT_CHOICE = 0, 1
+MOE_DROP, MOE_REROUTE = 0, 1
 STATUS = {0: "ok", 1: "invalid argument", 2: "misaligned pointer or row length",
           3: "workspace missing, misaligned or too small", 4: "unsupported shape",
           5: "CUDA runtime error", 6: "device-side error recorded"}
@@ -35,7 +36,8 @@ class MoeConfig(ctypes.Structure):
     _fields_ = [("T", ctypes.c_int32), ("d", ctypes.c_int32), ("d_ff", ctypes.c_int32),
                 ("E", ctypes.c_int32), ("k", ctypes.c_int32), ("dtype", ctypes.c_int32),
                 ("capacity", ctypes.c_int32), ("renormalize", ctypes.c_int32),
-                ("n_shared", ctypes.c_int32), ("routing", ctypes.c_int32)]
+                ("n_shared", ctypes.c_int32), ("routing", ctypes.c_int32),
+                ("overflow", ctypes.c_int32)]
 
 
 class MoeError(RuntimeError):
@@ -99,14 +101,24 @@ def load() -> ctypes.CDLL:
 
 
 def config(T, d, d_ff, E, k, dtype="bf16", capacity=None, renormalize=True,
-           n_shared=0, routing="token") -> MoeConfig:
+           n_shared=0, routing="token", overflow="drop") -> MoeConfig:
     """routing: "token" (each token picks its top-k experts) or "expert" (each
-    expert picks its top-C tokens)."""
+    expert picks its top-C tokens); overflow: "drop" or "reroute" (a slot the
+    cap drops is offered to the token's next-best expert)."""
     if routing not in ("token", "expert"):
         raise ValueError(f"routing must be 'token' or 'expert', not {routing!r}")
+    if overflow not in ("drop", "reroute"):
+        raise ValueError(f"overflow must be 'drop' or 'reroute', not {overflow!r}")
     return MoeConfig(T, d, d_ff, E, k, MOE_BF16 if dtype == "bf16" else MOE_F32,
                      -1 if capacity is None else int(capacity), 1 if renormalize else 0,
-                     int(n_shared), MOE_EXPERT_CHOICE if routing == "expert" else MOE_TOKEN_CHOICE)
+                     int(n_shared), MOE_EXPERT_CHOICE if routing == "expert" else MOE_TOKEN_CHOICE,
+                     MOE_REROUTE if overflow == "reroute" else MOE_DROP)
+
+
+def ranked_columns(cfg: MoeConfig) -> int:
+    """Columns of moe_route's topk_idx / topk_w: k, or min(2k, E) when
+    rerouting (the k choices, then the next-best experts)."""
+    return min(2 * cfg.k, cfg.E) if cfg.overflow == MOE_REROUTE else cfg.k + cfg.n_shared
 
 
 def _ptr(t):

@@ -29,8 +29,11 @@ namespace {
 
 constexpr int kWarps = kCountBlock / 32;
 
+// Assignment a = t*k + j reads idx[t*ld + j]; with skip_none an id of -1 is
+// "no assignment" (skipped without an error record).
 __global__ void __launch_bounds__(kCountBlock) count_kernel(const int32_t* __restrict__ idx, int n,
-                                                            int E, int32_t* __restrict__ blk_hist,
+                                                            int k, int ld, int E, bool skip_none,
+                                                            int32_t* __restrict__ blk_hist,
                                                             int32_t* __restrict__ local_rank,
                                                             DeviceHeader* hdr) {
     __shared__ int wh[kWarps][kMaxExperts];
@@ -42,9 +45,9 @@ __global__ void __launch_bounds__(kCountBlock) count_kernel(const int32_t* __res
     const int a = blockIdx.x * kCountBlock + tid;
     int e = -1;
     if (a < n) {
-        e = __ldg(idx + a);
+        e = __ldg(idx + (size_t)(a / k) * ld + a % k);
         if (e < 0 || e >= E) {
-            record_error(hdr, kErrExpertRange, a);
+            if (!(skip_none && e == -1)) record_error(hdr, kErrExpertRange, a);
             e = -1;
         }
     }
@@ -186,8 +189,25 @@ cudaError_t launch_count(const moe_config& c, const int32_t* topk_idx, void* ws,
     const int n = c.T * c.k;
     if (n == 0) return cudaSuccess;
     return launch_kernel(count_kernel, dim3(L.count_blocks), dim3(kCountBlock), 0, s, 1, false,
-                         topk_idx, n, c.E, at<int32_t>(ws, L.blk_hist),
+                         topk_idx, n, c.k, c.k, c.E, false, at<int32_t>(ws, L.blk_hist),
                          at<int32_t>(ws, L.local_rank), at<DeviceHeader>(ws, L.header));
+}
+
+cudaError_t launch_count_strided(const int32_t* idx, int T, int k, int ld, int E, bool skip_none,
+                                 int32_t* blk_hist, int32_t* local_rank, DeviceHeader* hdr,
+                                 cudaStream_t s) {
+    const int n = T * k;
+    if (n == 0) return cudaSuccess;
+    return launch_kernel(count_kernel, dim3((n + kCountBlock - 1) / kCountBlock),
+                         dim3(kCountBlock), 0, s, 1, false, idx, n, k, ld, E, skip_none, blk_hist,
+                         local_rank, hdr);
+}
+
+cudaError_t launch_scan(const int32_t* blk_hist, int nblk, int E, int capacity,
+                        int32_t* blk_base, int32_t* offsets, const LossArgs& loss,
+                        cudaStream_t s) {
+    return launch_kernel(scan_kernel, dim3(1), dim3(1024), 0, s, 1, false, blk_hist, nblk, E,
+                         capacity, 0, blk_base, offsets, loss);
 }
 
 cudaError_t launch_scan_permute(const moe_config& c, const void* x, const int32_t* topk_idx,

@@ -58,6 +58,7 @@ moe_status check_config(const moe_config* c) {
     if (c->dtype != MOE_F32 && c->dtype != MOE_BF16) return MOE_ERR_INVALID_ARG;
     if (c->renormalize != 0 && c->renormalize != 1) return MOE_ERR_INVALID_ARG;
     if (c->routing != MOE_TOKEN_CHOICE && c->routing != MOE_EXPERT_CHOICE) return MOE_ERR_INVALID_ARG;
+    if (c->overflow != MOE_DROP && c->overflow != MOE_REROUTE) return MOE_ERR_INVALID_ARG;
     if (c->n_shared < 0 || c->n_shared >= c->E) return MOE_ERR_INVALID_ARG;
     if (c->k > c->E - c->n_shared) return MOE_ERR_INVALID_ARG;
     if (c->E > kMaxExperts || c->k + c->n_shared > kMaxTopK) return MOE_ERR_UNSUPPORTED;
@@ -66,7 +67,21 @@ moe_status check_config(const moe_config* c) {
     if (c->routing == MOE_EXPERT_CHOICE &&
         (c->n_shared != 0 || (int64_t)c->T * c->E > (int64_t)INT32_MAX / 2))
         return MOE_ERR_UNSUPPORTED;
+    if (c->overflow == MOE_REROUTE &&
+        (c->routing != MOE_TOKEN_CHOICE || c->n_shared != 0 || reroute_ranked(*c) > kMaxTopK))
+        return MOE_ERR_UNSUPPORTED;
     return MOE_OK;
+}
+
+bool rerouting(const moe_config& c) { return c.overflow == MOE_REROUTE; }
+
+// Router view of a rerouting layer: K2 ranked experts per token (the first k
+// are the choices; moe_route / launch_route get knorm = k).
+moe_config reroute_router_config(const moe_config& c) {
+    moe_config r = c;
+    r.k = reroute_ranked(c);
+    r.overflow = MOE_DROP;
+    return r;
 }
 
 bool expert_choice(const moe_config& c) { return c.routing == MOE_EXPERT_CHOICE; }
@@ -162,8 +177,9 @@ WsLayout ws_layout(const moe_config& c) {
     const size_t nr = c.n_shared > 0 ? (size_t)c.T * c.k : 0;
     L.route_idx = take(sizeof(int32_t) * nr);
     L.route_w = take(sizeof(float) * nr);
-    L.topk_idx = take(sizeof(int32_t) * (size_t)n);
-    L.topk_w = take(sizeof(float) * (size_t)n);
+    const int64_t ranked = rerouting(c) ? (int64_t)c.T * reroute_ranked(c) : n;
+    L.topk_idx = take(sizeof(int32_t) * (size_t)ranked);
+    L.topk_w = take(sizeof(float) * (size_t)ranked);
     L.offsets = take(sizeof(int32_t) * (size_t)(c.E + 1));
     L.slot_of = take(sizeof(int32_t) * (size_t)slots);
     L.perm_token = take(sizeof(int32_t) * (size_t)perm);
@@ -172,6 +188,14 @@ WsLayout ws_layout(const moe_config& c) {
     L.h = take(es * (size_t)L.rows * c.d_ff);
     L.y_perm = take(sizeof(float) * (size_t)L.rows * c.d);
     L.probs_t = take(ec ? sizeof(float) * (size_t)c.E * c.T : 0);
+    const bool rr = rerouting(c);
+    L.rr_hist = take(rr ? sizeof(int32_t) * (size_t)L.count_blocks * c.E : 0);
+    L.rr_base = take(rr ? sizeof(int32_t) * (size_t)L.count_blocks * c.E : 0);
+    L.rr_rank = take(rr ? sizeof(int32_t) * (size_t)n : 0);
+    L.rr_kept = take(rr ? sizeof(int32_t) * (size_t)n : 0);
+    L.rr_alt = take(rr ? sizeof(int32_t) * (size_t)n : 0);
+    L.rr_off1 = take(rr ? sizeof(int32_t) * (size_t)(c.E + 1) : 0);
+    L.rr_off2 = take(rr ? sizeof(int32_t) * (size_t)(c.E + 1) : 0);
     L.total = o;
     return L;
 }
@@ -230,6 +254,10 @@ moe_status moe_route(const moe_config* cfg, const void* x, const float* W_r,
     if (logits_in == nullptr && (!aligned16(x) || !aligned16(W_r))) return MOE_ERR_ALIGNMENT;
     if ((st = check_ws(c, ws, ws_bytes, &L)) != MOE_OK) return st;
     chain_begin();
+    if (rerouting(c))  // K2 ranked experts per token, the first k the choices
+        return from_cuda(launch_route(reroute_router_config(c), x, W_r, logit_bias, logit_noise,
+                                      logits_in, logits_out, topk_idx, topk_w, expert_counts,
+                                      aux_out, z_loss_out, ws, L, false, s, nullptr, c.k));
     if (c.n_shared == 0)
         return from_cuda(launch_route(c, x, W_r, logit_bias, logit_noise, logits_in, logits_out,
                                       topk_idx, topk_w, expert_counts, aux_out, z_loss_out, ws,
@@ -270,6 +298,10 @@ moe_status moe_dispatch(const moe_config* cfg, const void* x, const int32_t* top
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
     const moe_config cd = dispatch_config(c);
     chain_begin();
+    if (rerouting(c))
+        return from_cuda(launch_reroute_dispatch(c, reroute_ranked(c), x, topk_idx, topk_w,
+                                                 offsets, slot_of, perm_token, perm_w, x_perm, ws,
+                                                 L, LossArgs{}, s));
     cudaError_t e = launch_count(cd, topk_idx, ws, L, s);
     if (e == cudaSuccess)
         e = launch_scan_permute(cd, x, topk_idx, topk_w, kCountBlock, L.count_blocks, offsets,
@@ -359,7 +391,17 @@ moe_status moe_forward(const moe_config* cfg, const void* x, const float* W_r,
     }
     chain_begin();
     cudaError_t e;
-    if (c.n_shared == 0) {
+    if (rerouting(c) && c.capacity >= 0) {
+        // K2 ranked experts per token; the drop pass (whose scan also
+        // finishes the loss and counts), the offers, the layout
+        e = launch_route(reroute_router_config(c), x, W_r, logit_bias, logit_noise, nullptr,
+                         logits_out, idx, w, nullptr, nullptr, nullptr, ws, L, false, s,
+                         nullptr, c.k);
+        if (e == cudaSuccess)
+            e = launch_reroute_dispatch(
+                c, reroute_ranked(c), x, idx, w, offsets, slot_of, perm_token, perm_w, x_perm, ws,
+                L, route_loss_args(c, ws, L, expert_counts, aux_out, z_loss_out), s);
+    } else if (c.n_shared == 0) {  // (rerouting without a cap drops nothing: this path)
         // the router also counts (blk_hist, local_rank) and the scan finishes its loss
         e = launch_route(c, x, W_r, logit_bias, logit_noise, nullptr, logits_out, idx, w,
                          expert_counts, aux_out, z_loss_out, ws, L, true, s);

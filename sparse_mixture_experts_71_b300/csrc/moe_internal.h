@@ -78,6 +78,13 @@ struct WsLayout {
     size_t h;            // dtype [rows][d_ff]
     size_t y_perm;       // fp32  [rows][d] (moe_forward)
     size_t probs_t;      // fp32  [E][T] router probabilities (expert choice)
+    size_t rr_hist;      // int32 [count_blocks][E] offer histograms (rerouting)
+    size_t rr_base;      // int32 [count_blocks][E]
+    size_t rr_rank;      // int32 [T*k] offer ranks within their block
+    size_t rr_kept;      // int32 [T*k] drop-pass rank of a kept slot, -1 if dropped
+    size_t rr_alt;       // int32 [T*k] expert a dropped slot is offered to, -1 if none
+    size_t rr_off1;      // int32 [E+1] drop-pass offsets
+    size_t rr_off2;      // int32 [E+1] offer-count prefix
     size_t total;
     RouteGeom route;
     int count_blocks;    // blocks of the stand-alone counting kernel
@@ -174,7 +181,35 @@ cudaError_t launch_route(const moe_config& c, const void* x, const float* W_r,
                          const float* logits_in, float* logits_out,
                          int32_t* topk_idx, float* topk_w, int32_t* expert_counts,
                          float* aux_out, float* z_loss_out, void* ws, const WsLayout& L,
-                         bool fuse_count, cudaStream_t s, float* probs_t = nullptr);
+                         bool fuse_count, cudaStream_t s, float* probs_t = nullptr,
+                         int knorm = 0);
+// knorm > 0 (rerouting): the router ranks c.k experts per token, of which the
+// first knorm are the choices (counts, loss and weight normalisation) and the
+// rest the next-best experts.
+
+// Counting kernel over a strided id array (a = t*k + j reads idx[t*ld + j];
+// skip_none: -1 means no assignment) and the scan of its block histograms
+// (no shared experts; with loss.blk_p set it also finishes the router's
+// loss and counts); granularity kCountBlock assignments.
+struct LossArgs;
+cudaError_t launch_count_strided(const int32_t* idx, int T, int k, int ld, int E, bool skip_none,
+                                 int32_t* blk_hist, int32_t* local_rank, DeviceHeader* hdr,
+                                 cudaStream_t s);
+cudaError_t launch_scan(const int32_t* blk_hist, int nblk, int E, int capacity,
+                        int32_t* blk_base, int32_t* offsets, const LossArgs& loss,
+                        cudaStream_t s);
+
+// Rerouting on overflow (reroute.cu): the drop pass, the offers of dropped
+// slots to each token's next-best experts, and the layout and gather, from
+// the router's K2 = ld ranked experts per token.
+// With loss.blk_p set, the drop-pass scan also finishes the router's loss
+// and counts (the forward pass).
+cudaError_t launch_reroute_dispatch(const moe_config& c, int ld, const void* x,
+                                    const int32_t* topk_idx, const float* topk_w,
+                                    int32_t* offsets, int32_t* slot_of, int32_t* perm_token,
+                                    float* perm_w, void* x_perm, void* ws, const WsLayout& L,
+                                    const LossArgs& loss, cudaStream_t s);
+inline int reroute_ranked(const moe_config& c) { return 2 * c.k < c.E ? 2 * c.k : c.E; }
 
 // Expert choice (expert_choice.cu): C; the per-expert top-C selection from
 // the router probabilities probs_t [E][T] (offsets, rows, slot_of [T][E]);

@@ -64,7 +64,8 @@ extern "C" moe_status moe_dispatch_noalloc(const moe_config* cfg, const void* x,
     const moe_status cs = config_status(cfg);
     if (cs != MOE_OK) return cs;
     const moe_config& c = *cfg;
-    if (c.routing != MOE_TOKEN_CHOICE) return MOE_ERR_UNSUPPORTED;  // a token-choice step
+    if (c.routing != MOE_TOKEN_CHOICE || c.overflow != MOE_DROP)
+        return MOE_ERR_UNSUPPORTED;  // a token-choice step that drops on overflow
     if (c.T < 0 || c.d <= 0 || c.d_ff <= 0 || c.E <= 0 || c.k <= 0 ||
         (c.dtype != MOE_F32 && c.dtype != MOE_BF16) || (c.renormalize != 0 && c.renormalize != 1) ||
         c.n_shared < 0 || c.n_shared >= c.E || c.k > c.E - c.n_shared)

@@ -528,7 +528,7 @@ __global__ void __launch_bounds__(kThreads) route_tile_kernel(RouteArgs a) {
             xe = __shfl_sync(0xffffffffu, xe, be % 32);
             sel_e[j] = be;
             sel_x[j] = xe;
-            sel_sum += xe;
+            sel_sum += j < a.knorm ? xe : 0.f;
         }
         if (lane == 0) {
             const float wden = a.renormalize ? 1.0f / sel_sum : inv;
@@ -536,7 +536,7 @@ __global__ void __launch_bounds__(kThreads) route_tile_kernel(RouteArgs a) {
                 a.topk_idx[(size_t)t * a.k + j] = sel_e[j];
                 a.topk_w[(size_t)t * a.k + j] = sel_x[j] * wden;
                 s_idx[tok * a.k + j] = sel_e[j];
-                atomicAdd(&s_cnt[sel_e[j]], 1);
+                if (j < a.knorm) atomicAdd(&s_cnt[sel_e[j]], 1);
             }
             atomicAdd(&s_top1[sel_e[0]], 1);
         }
@@ -743,9 +743,10 @@ cudaError_t launch_route(const moe_config& c, const void* x, const float* W_r,
                          const float* logits_in, float* logits_out,
                          int32_t* topk_idx, float* topk_w, int32_t* expert_counts,
                          float* aux_out, float* z_loss_out, void* ws, const WsLayout& L,
-                         bool fuse_count, cudaStream_t s, float* probs_t) {
+                         bool fuse_count, cudaStream_t s, float* probs_t, int knorm) {
     RouteArgs a;
     a.probs_t = probs_t;
+    a.knorm = knorm > 0 ? knorm : c.k;
     a.x = x; a.W_r = W_r; a.bias = logit_bias; a.logits_in = logits_in; a.logits_out = logits_out;
     a.noise = logits_in != nullptr ? nullptr : logit_noise;  // logits_in replaces all terms
     a.topk_idx = topk_idx; a.topk_w = topk_w; a.expert_counts = expert_counts; a.aux_out = aux_out;

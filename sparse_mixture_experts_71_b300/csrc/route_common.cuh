@@ -35,6 +35,7 @@ struct RouteArgs {
     int32_t* blk_hist;    // ws: [nblk][E] or null (no fused counting)
     int32_t* local_rank;  // ws: [T*k]
     int T, d, E, k, renormalize, nblk;
+    int knorm;            // slots that are choices (the rest: next-best experts)
 };
 
 // Histogram of the block's n assignments (expert ids in s_idx, in (token,
@@ -161,14 +162,14 @@ __device__ __forceinline__ void token_epilogue(const RouteArgs& a, float* prow, 
         taken |= 1ull << be;
         sel_e[j] = be;
         sel_x[j] = bx;
-        sel_sum += bx;
+        sel_sum += j < a.knorm ? bx : 0.f;
     }
     const float wden = a.renormalize ? 1.0f / sel_sum : inv;
     for (int j = 0; j < a.k; ++j) {
         a.topk_idx[(size_t)t * a.k + j] = sel_e[j];
         a.topk_w[(size_t)t * a.k + j] = sel_x[j] * wden;
         s_idx[slot * a.k + j] = sel_e[j];
-        atomicAdd(&s_cnt[sel_e[j]], 1);
+        if (j < a.knorm) atomicAdd(&s_cnt[sel_e[j]], 1);
     }
     atomicAdd(&s_top1[sel_e[0]], 1);
 }

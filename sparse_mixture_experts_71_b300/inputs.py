@@ -65,6 +65,7 @@ class Workload:
     init: str = "normal"
     n_shared: int = 0  # experts 0 .. n_shared-1 always active (the router covers the rest)
     routing: str = "token"  # "token": top-k experts per token; "expert": top-C tokens per expert
+    overflow: str = "drop"  # "drop" or "reroute" (capped slots offered to the next-best expert)
     note: str = field(default="", compare=False)
 
     def with_(self, **kw) -> "Workload":
@@ -90,10 +91,15 @@ WORKLOADS: dict[str, Workload] = {
         Workload("expertchoice-bf16-T4096-d1024-F4096-E8-C1024", 4096, 1024, 4096, 8, 2,
                  routing="expert", note="expert-choice routing: each expert takes its top "
                  "C = T k / E = 1024 tokens (the default workload's shape)"),
+        Workload("switch-reroute-bf16-T32768-d2048-F8192-E64-top1-cap640", 32768, 2048, 8192, 64,
+                 1, renormalize=False, capacity=640, capacity_factor=1.25, zipf_bias=1.5,
+                 overflow="reroute", note="the Switch workload with overflow rerouted to each "
+                 "token's next-best expert instead of dropped"),
     )
 }
 
-TINY, MEDIUM, LARGE, SWITCH, DECODE, FINEGRAINED, EXPERTCHOICE = WORKLOADS.values()
+(TINY, MEDIUM, LARGE, SWITCH, DECODE, FINEGRAINED, EXPERTCHOICE,
+ SWITCH_REROUTE) = WORKLOADS.values()
 
 
 @dataclass

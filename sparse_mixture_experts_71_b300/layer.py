@@ -40,13 +40,17 @@ class MoELayer:
     b2: (E, d), all on one CUDA device, W1..b2 of one dtype (fp32 or bf16).
     routing: "token" (top-k experts per token) or "expert" (each expert takes
     its top-C tokens; k then sets C = ceil(T k / E) unless a capacity is given).
+    overflow: "drop" (the capacity cap drops overflow) or "reroute" (a dropped
+    slot is offered to the token's next-best expert).
     """
 
     def __init__(self, W_r, W1, b1, W2, b2, k: int, capacity: int | None = None,
-                 renormalize: bool = True, logit_bias=None, routing: str = "token"):
+                 renormalize: bool = True, logit_bias=None, routing: str = "token",
+                 overflow: str = "drop"):
         self.E, self.d_ff, self.d = W1.shape
         self.k = k
         self.routing = routing
+        self.overflow = overflow
         self.dtype = "bf16" if W1.dtype == torch.bfloat16 else "f32"
         self.capacity, self.renormalize = capacity, renormalize
         self.W_r, self.W1, self.b1, self.W2, self.b2 = W_r, W1, b1, W2, b2
@@ -55,7 +59,7 @@ class MoELayer:
 
     def config(self, T: int) -> B.MoeConfig:
         return B.config(T, self.d, self.d_ff, self.E, self.k, self.dtype, self.capacity,
-                        self.renormalize, routing=self.routing)
+                        self.renormalize, routing=self.routing, overflow=self.overflow)
 
     def workspace(self, T: int) -> torch.Tensor:
         if T not in self._ws:

@@ -22,7 +22,7 @@ NEAR_TIE = 1e-6
 
 def cfg_of(wl):
     return B.config(wl.T, wl.d, wl.F, wl.E, wl.k, wl.dtype, wl.capacity, wl.renormalize,
-                    wl.n_shared, routing=wl.routing)
+                    wl.n_shared, routing=wl.routing, overflow=wl.overflow)
 
 
 def y_error(y_gpu: np.ndarray, y_ref: np.ndarray):
@@ -70,13 +70,14 @@ class GpuRun:
     def staged(self, logits_in=None, noise=None):
         wl, D, T, E = self.wl, self.dev, self.wl.T, self.wl.E
         k = wl.k + wl.n_shared  # columns per token (routed, then shared)
+        kr = B.ranked_columns(self.cfg)  # router columns (rerouting: the next-best too)
         dt = D["x"].dtype
         cuda = D["x"].device
         n = T * k
         r = {}
         r["logits"] = torch.empty((T, E - wl.n_shared), dtype=torch.float32, device=cuda)
-        r["idx"] = torch.empty((T, k), dtype=torch.int32, device=cuda)
-        r["w"] = torch.empty((T, k), dtype=torch.float32, device=cuda)
+        r["idx"] = torch.empty((T, kr), dtype=torch.int32, device=cuda)
+        r["w"] = torch.empty((T, kr), dtype=torch.float32, device=cuda)
         r["counts"] = torch.empty(E, dtype=torch.int32, device=cuda)
         r["aux"] = torch.empty(1, dtype=torch.float32, device=cuda)
         r["z"] = torch.full((1,), -1.0, dtype=torch.float32, device=cuda)
@@ -147,7 +148,7 @@ def oracle_on(inp, wl, logits=None, tokens=None, layout=True):
                          inp.as_f32("W2"), inp.as_f32("b2"), k=wl.k,
                          renormalize=wl.renormalize, capacity=wl.capacity,
                          logit_bias=inp.logit_bias, logits=logits, tokens=tokens, layout=layout,
-                         n_shared=wl.n_shared)
+                         n_shared=wl.n_shared, reroute=wl.overflow == "reroute")
 
 
 def sample_tokens(wl, ref_route, n: int, seed: int = 0) -> np.ndarray:

@@ -18,7 +18,8 @@ from sparse_mixture_experts_71_b300 import inputs as I
 
 pytestmark = pytest.mark.gpu
 
-FULL = [w for w in I.WORKLOADS.values() if w.routing == "token"]  # expert choice: its own file
+# expert choice and rerouting have their own files
+FULL = [w for w in I.WORKLOADS.values() if w.routing == "token" and w.overflow == "drop"]
 _cache = {}
 
 
