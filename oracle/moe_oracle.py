@@ -46,6 +46,12 @@ the combine and of the auxiliary loss did not survive extraction):
   (divided by the sum over its k choices when renormalising).  An expert's
   rows are its first-pass assignments in token order, then the offers it
   accepted in token order;
+* the backward pass (gradients of the layer, which the pages name as part
+  of training) treats the routing decisions (top-k, capacity) as constants,
+  as autograd does: the loss is <dy, y> + aux_grad * aux + z_grad * z_loss
+  for caller-given dy and scalar weights; the gate weights carry gradient to
+  the logits through the softmax (and the renormalisation), the auxiliary
+  loss through P (f holds counts) and the z-loss through the log-sum-exp;
 * expert-choice routing ("experts choose their top tokens") ranks, for each
   expert, the batch's tokens by their router probability p[t, e] (the same
   softmax over experts as token choice), larger first and the lower token
@@ -511,3 +517,86 @@ def expert_choice_forward(x, W_r, W1, b1, W2, b2, k: int, capacity: int | None =
             y[pos[int(t)]] += w[e, rows[r]] * out[r]
     return ExpertChoiceResult(logits, probs, C, sel, w, slot_of, y, tokens,
                               router_z_loss(logits))
+
+
+def gelu_grad(u) -> np.ndarray:
+    """d/du of the exact GELU: Phi(u) + u phi(u).
+
+    Derivative of [LECTURE] "The MoE layer"'s GELU (``nn.GELU()``)."""
+    u = np.asarray(u, f64)
+    return 0.5 * (1.0 + erf(u / math.sqrt(2.0))) + u * np.exp(-0.5 * u * u) / math.sqrt(2 * math.pi)
+
+
+def moe_backward(x, W_r, W1, b1, W2, b2, dy, k: int, renormalize: bool = True,
+                 capacity: int | None = None, logit_bias=None, logits=None,
+                 aux_grad: float = 0.0, z_grad: float = 0.0) -> dict:
+    """Gradients of L = <dy, y> + aux_grad * aux + z_grad * z_loss.
+
+    The training step behind [LECTURE] "The MoE layer" (the layer is trained
+    end to end with the load-balancing loss of "The central problem: load
+    balancing"; [DAY59] "Load-balancing losses encourage better routing").
+    Routing decisions (top-k, capacity) are constants.  Per kept assignment
+    (token t, expert e, weight w): u = W1_e x + b1_e, h = GELU(u),
+    o = W2_e h + b2_e, y_t += w o; hence do = w dy_t, dW2_e += do h^T,
+    db2_e += do, du = (W2_e^T do) * GELU'(u), dW1_e += du x^T, db1_e += du,
+    dx_t += W1_e^T du, and s = <dy_t, w o> feeds the logits: with the weights
+    a softmax over the token's k choices (renormalised) dg_e = s_e - w_e
+    sum_j s_j on the choices and 0 elsewhere; with w = p (not renormalised)
+    dg_e = s_e - p_e sum_j s_j.  The auxiliary loss adds
+    aux_grad E / T * p_e (f_e - sum_i f_i p_i), the z-loss
+    z_grad 2 / T * lse_t p_e.  Then dW_r = dg^T x and dx += dg W_r.
+    ``logits`` replaces the router GEMM as in moe_forward (W_r still gets
+    its gradient from dg).  Returns dx (T, d), dW_r (E, d), dW1, db1, dW2,
+    db2, all fp64, and dg (T, E).
+    """
+    x = np.asarray(x, f64)
+    dy = np.asarray(dy, f64)
+    T, d = x.shape
+    r = moe_forward(x, W_r, W1, b1, W2, b2, k=k, renormalize=renormalize, capacity=capacity,
+                    logit_bias=logit_bias, logits=logits, layout=False)
+    E = r.logits.shape[1]
+    p = r.probs
+    g = np.asarray(r.logits, f64)
+    W1, b1, W2, b2 = (np.asarray(a, f64) for a in (W1, b1, W2, b2))
+    dx = np.zeros((T, d))
+    dW1, db1 = np.zeros_like(W1), np.zeros_like(b1)
+    dW2, db2 = np.zeros_like(W2), np.zeros_like(b2)
+    s = np.zeros((T, k))  # <dy_t, w o> per slot (0 when dropped)
+    for t in range(T):
+        for j in range(k):
+            if not r.kept[t, j]:
+                continue
+            e, w = int(r.idx[t, j]), r.w[t, j]
+            u = W1[e] @ x[t] + b1[e]
+            h = gelu(u)
+            o = W2[e] @ h + b2[e]
+            s[t, j] = w * float(dy[t] @ o)
+            do = w * dy[t]
+            dW2[e] += np.outer(do, h)
+            db2[e] += do
+            du = (W2[e].T @ do) * gelu_grad(u)
+            dW1[e] += np.outer(du, x[t])
+            db1[e] += du
+            dx[t] += W1[e].T @ du
+    dg = np.zeros((T, E))
+    for t in range(T):
+        sel = r.idx[t]
+        tot = s[t].sum()
+        if renormalize:
+            for j in range(k):
+                dg[t, sel[j]] += s[t, j] - r.w[t, j] * tot
+        else:
+            dg[t] -= p[t] * tot
+            for j in range(k):
+                dg[t, sel[j]] += s[t, j]
+    if aux_grad:
+        f = np.bincount(np.asarray(r.idx[:, 0], np.int64), minlength=E) / T
+        fp = (p * f[None, :]).sum(axis=1, keepdims=True)
+        dg += aux_grad * E / T * p * (f[None, :] - fp)
+    if z_grad:
+        m = g.max(axis=1, keepdims=True)
+        lse = m + np.log(np.exp(g - m).sum(axis=1, keepdims=True))
+        dg += z_grad * 2.0 / T * lse * p
+    dW_r = dg.T @ x
+    dx += dg @ np.asarray(W_r, f64)
+    return dict(dx=dx, dW_r=dW_r, dW1=dW1, db1=db1, dW2=dW2, db2=db2, dg=dg)

@@ -819,3 +819,114 @@ def test_planted_reroute_mistakes_are_caught(monkeypatch):
     monkeypatch.setattr(O, "reroute_keep", same_alternate)
     with pytest.raises(AssertionError):
         test_reroute_two_slot_order_and_rows()
+
+
+# ---- backward pass: the oracle's hand-derived gradients against torch
+# autograd of the same layer (routing decisions held fixed), and against
+# central finite differences
+
+def _torch_loss(L, dy, k, renorm, cap, aux_grad, z_grad, bias=None):
+    """<dy, y> + aux_grad aux + z_grad z in torch fp64, the routing (top-k and
+    capacity keep) taken from the oracle as constants; the fp32 rounding of
+    the oracle's logits is added as a constant so the values match."""
+    r = O.moe_forward(**L, k=k, renormalize=renorm, capacity=cap, logit_bias=bias)
+    t = {n: torch.tensor(np.asarray(v, np.float64), requires_grad=True) for n, v in L.items()}
+    g64 = t["x"] @ t["W_r"].T
+    if bias is not None:
+        g64 = g64 + torch.tensor(np.asarray(bias, np.float64))
+    g = g64 + (torch.tensor(r.logits.astype(np.float64)) - g64).detach()
+    p = torch.softmax(g, dim=1)
+    idx = torch.tensor(r.idx, dtype=torch.int64)
+    sel = p.gather(1, idx)
+    w = sel / sel.sum(1, keepdim=True) if renorm else sel
+    T, E = g.shape
+    ys = []
+    for tok in range(T):
+        yt = torch.zeros(t["x"].shape[1], dtype=torch.float64)
+        for j in range(k):
+            if r.kept[tok, j]:
+                e = int(r.idx[tok, j])
+                h = TF.gelu(t["W1"][e] @ t["x"][tok] + t["b1"][e])
+                yt = yt + w[tok, j] * (t["W2"][e] @ h + t["b2"][e])
+        ys.append(yt)
+    y = torch.stack(ys)
+    f = torch.tensor(np.bincount(r.idx[:, 0], minlength=E) / T)
+    aux = E * (f * p.mean(0)).sum()
+    z = torch.logsumexp(g, dim=1).pow(2).mean()
+    loss = (torch.tensor(dy) * y).sum() + aux_grad * aux + z_grad * z
+    loss.backward()
+    return {n: t[n].grad.numpy() for n in t}, float(loss.detach())
+
+
+@pytest.mark.parametrize("k,renorm,cap,aux_grad,z_grad", [
+    (2, True, None, 0.0, 0.0), (1, False, None, 0.0, 0.0), (2, True, 3, 0.3, 0.0),
+    (1, False, 4, 0.01, 0.5), (3, True, None, 1.0, 1.0), (2, False, 2, 0.0, 2.0)])
+def test_backward_matches_torch_autograd(k, renorm, cap, aux_grad, z_grad):
+    L = _rand_layer(T=11, d=6, F=7, E=4, seed=50 + k)
+    dy = np.random.default_rng(51).standard_normal((11, 6))
+    want, _ = _torch_loss(L, dy, k, renorm, cap, aux_grad, z_grad)
+    got = O.moe_backward(**L, dy=dy, k=k, renormalize=renorm, capacity=cap, aux_grad=aux_grad,
+                         z_grad=z_grad)
+    for n, gname in (("x", "dx"), ("W_r", "dW_r"), ("W1", "dW1"), ("b1", "db1"), ("W2", "dW2"),
+                     ("b2", "db2")):
+        np.testing.assert_allclose(got[gname], want[n], rtol=1e-10, atol=1e-12, err_msg=gname)
+
+
+def test_backward_with_logit_bias_and_dense_expert():
+    """A logit bias shifts the routing but not the formulas; E = 1 is the
+    plain FFN's backward."""
+    L = _rand_layer(T=9, d=5, F=6, E=3, seed=52)
+    dy = np.random.default_rng(53).standard_normal((9, 5))
+    bias = np.array([0.4, -0.2, 0.0], np.float32)
+    want, _ = _torch_loss(L, dy, 2, True, 4, 0.2, 0.1, bias=bias)
+    got = O.moe_backward(**L, dy=dy, k=2, renormalize=True, capacity=4, logit_bias=bias,
+                         aux_grad=0.2, z_grad=0.1)
+    np.testing.assert_allclose(got["dx"], want["x"], rtol=1e-10, atol=1e-12)
+    np.testing.assert_allclose(got["dW_r"], want["W_r"], rtol=1e-10, atol=1e-12)
+    L1 = _rand_layer(T=7, d=4, F=5, E=1, seed=54)
+    dy1 = np.random.default_rng(55).standard_normal((7, 4))
+    got1 = O.moe_backward(**L1, dy=dy1, k=1, renormalize=True)
+    t = {n: torch.tensor(np.asarray(v, np.float64), requires_grad=True) for n, v in L1.items()}
+    y = TF.linear(TF.gelu(TF.linear(t["x"], t["W1"][0], t["b1"][0])), t["W2"][0], t["b2"][0])
+    (torch.tensor(dy1) * y).sum().backward()
+    np.testing.assert_allclose(got1["dW1"][0], t["W1"].grad[0].numpy(), rtol=1e-10, atol=1e-13)
+    np.testing.assert_allclose(got1["dx"], t["x"].grad.numpy(), rtol=1e-10, atol=1e-13)
+    assert not got1["dW_r"].any()  # one expert: w = 1 whatever the logit
+
+
+def test_backward_finite_differences():
+    """Central differences of the loss in x, W1, W_r and b2 (steps small
+    enough to keep the routing, large enough that the fp32 rounding of the
+    logits stays below the tolerance) agree with the oracle's gradients."""
+    L = _rand_layer(T=6, d=4, F=5, E=3, seed=56)
+    dy = np.random.default_rng(57).standard_normal((6, 4))
+    kw = dict(k=2, renormalize=True, capacity=None)
+    got = O.moe_backward(**L, dy=dy, aux_grad=0.5, z_grad=0.25, **kw)
+
+    def loss(LL):
+        r = O.moe_forward(**LL, **kw)
+        f = np.bincount(r.idx[:, 0], minlength=3) / 6
+        return float((dy * r.y).sum() + 0.5 * 3 * (f * r.probs.mean(0)).sum()
+                     + 0.25 * r.z_loss)
+
+    base = O.moe_forward(**L, **kw)
+    eps = 1e-3
+    for name, gname, pos in (("x", "dx", (2, 1)), ("W1", "dW1", (1, 3, 2)), ("W_r", "dW_r", (0, 3)),
+                             ("b2", "db2", (2, 0))):
+        a = {n: np.array(v, np.float64) for n, v in L.items()}
+        b = {n: np.array(v, np.float64) for n, v in L.items()}
+        a[name][pos] += eps
+        b[name][pos] -= eps
+        for LL in (a, b):  # the steps keep every routing decision
+            assert np.array_equal(O.moe_forward(**LL, **kw).idx, base.idx)
+        fd = (loss(a) - loss(b)) / (2 * eps)
+        assert abs(fd - got[gname][pos]) <= 5e-5 * max(1.0, abs(fd)), (name, fd, got[gname][pos])
+
+
+def test_planted_backward_mistakes_are_caught(monkeypatch):
+    """A GELU derivative without its u phi(u) term fails the autograd pin."""
+    good = O.gelu_grad
+    monkeypatch.setattr(O, "gelu_grad", lambda u: 0.5 * (1.0 + O.erf(np.asarray(u) / math.sqrt(2))))
+    with pytest.raises(AssertionError):
+        test_backward_matches_torch_autograd(2, True, None, 0.0, 0.0)
+    monkeypatch.setattr(O, "gelu_grad", good)
