@@ -495,6 +495,102 @@ def bench_ours(args, wl):
     return 0
 
 
+def bench_backward(args, wl):
+    """One step = one moe_backward call (it recomputes the forward
+    intermediates it needs) on the workload's inputs and a seeded dy."""
+    import torch
+    import torch.distributed as dist
+    from sparse_mixture_experts_71_b300 import binding as B
+    from sparse_mixture_experts_71_b300.layer import MoELayer, capture_graph, device_inputs
+
+    world, rank, local = dist_setup()
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    if world > 1:
+        dist.init_process_group("nccl", device_id=dev)
+    if not (wl.dtype == "bf16" and wl.routing == "token" and wl.overflow == "drop"
+            and wl.n_shared == 0):
+        raise SystemExit(f"{wl.name}: the backward pass covers bf16 token-choice layers that "
+                         "drop on overflow")
+    inp = I.make_inputs(wl, seed=0)
+    D = device_inputs(inp, dev)
+    layer = MoELayer(D["W_r"], D["W1"], D["b1"], D["W2"], D["b2"], k=wl.k, capacity=wl.capacity,
+                     renormalize=wl.renormalize, logit_bias=D["logit_bias"])
+    cfg = layer.config(wl.T)
+    T, d, F, E = wl.T, wl.d, wl.F, wl.E
+    ws = B.backward_workspace(cfg, device=dev)
+    dy = torch.from_numpy(I.router_noise(T, d, 1.0, seed=1)).to(torch.bfloat16).to(dev)
+    f32 = dict(dtype=torch.float32, device=dev)
+    g = dict(dx=torch.empty_like(D["x"]), dW_r=torch.empty((E, d), **f32),
+             dW1=torch.empty((E, F, d), **f32), db1=torch.empty((E, F), **f32),
+             dW2=torch.empty((E, d, F), **f32), db2=torch.empty((E, d), **f32))
+    flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
+    stream = torch.cuda.current_stream(dev)
+
+    def step(st):
+        B.backward(cfg, D["x"], D["W_r"], D["W1"], D["b1"], D["W2"], D["b2"], dy, g["dx"],
+                   g["dW_r"], g["dW1"], g["db1"], g["dW2"], g["db2"], ws,
+                   logit_bias=D["logit_bias"], aux_grad=0.01, z_grad=0.001, stream=st)
+
+    c0 = B.launch_count()
+    step(stream)
+    torch.cuda.synchronize(dev)
+    kernels = B.launch_count() - c0
+    graph = capture_graph(step, warmup=1)
+    for _ in range(max(args.warmup, 3)):
+        flush.fill_(1)
+        graph.replay()
+    torch.cuda.synchronize(dev)
+    # kept assignments of this batch, from the forward layer call
+    counts = torch.empty(E, dtype=torch.int32, device=dev)
+    layer.forward(D["x"], expert_counts=counts)
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in range(args.steps)]
+    sampler = ClockSampler(local)
+    if world > 1:
+        dist.barrier()
+    torch.cuda.synchronize(dev)
+    with sampler:
+        for s_ in range(args.steps):
+            flush.fill_(s_ & 0xFF)
+            ev[s_][0].record(stream)
+            graph.replay()
+            ev[s_][1].record(stream)
+        torch.cuda.synchronize(dev)
+    total_ms = sum(e0.elapsed_time(e1) for e0, e1 in ev)
+    if world > 1:
+        t = torch.tensor([total_ms], dtype=torch.float64, device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        total_ms = float(t.item())
+    ms = total_ms / args.steps
+    cnt = counts.cpu().numpy()
+    kept = int(np.minimum(cnt, wl.capacity).sum()) if wl.capacity is not None else int(cnt.sum())
+    # 2 forward GEMMs recomputed + dH, dX and the two weight-gradient GEMMs
+    flops = 12.0 * kept * d * F + 3 * 2.0 * T * d * E
+    pk, pk_kind = peaks()
+    clocks = sampler.summary()
+    achieved = flops / (ms * 1e-3) / 1e12
+    line = {"metric": "MoE-layer backward tokens/s (gradients of x, W_r, W1, b1, W2, b2)",
+            "value": world * T / (ms * 1e-3), "unit": "tokens/s", "n_gpus": world,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+            "data": "synthetic",
+            "config": {"workload": wl.name, "pass": "backward", "T": T, "d": d, "d_ff": F,
+                       "E": E, "k": wl.k, "capacity": wl.capacity,
+                       "parallelism": f"replicas{world}",
+                       "l2": "flushed before every timed step (256 MiB write, untimed)"},
+            "kernels_per_step": kernels, "kept_assignments": kept,
+            "roofline": {"bound": "tensor", "kernel": f"whole backward call ({kernels} launches)",
+                         "achieved": achieved, "peak": pk["bf16_tflops"],
+                         "peak_source": pk_kind + " burst", "unit": "TFLOP/s",
+                         "frac": achieved / pk["bf16_tflops"], "traffic": None},
+            "gpu_launches": kernels * args.steps, "clocks": clocks}
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        dist.destroy_process_group()
+    return 0
+
+
 def main():
     ap = argparse.ArgumentParser(description=__doc__.split("\n")[0])
     ap.add_argument("--gpus", type=int, default=1)
@@ -503,10 +599,14 @@ def main():
     ap.add_argument("--impl", choices=("ours", "reference"), default="ours")
     ap.add_argument("--workload", default=DEFAULT_WORKLOAD, choices=list(I.WORKLOADS))
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--pass", dest="pass_", choices=("forward", "backward"), default="forward",
+                    help="backward: time moe_backward instead of the forward pass")
     args = ap.parse_args()
     wl = I.WORKLOADS[args.workload]
     if args.impl == "reference":
         return bench_reference(args, wl)
+    if args.pass_ == "backward":
+        return bench_backward(args, wl)
     return bench_ours(args, wl)
 
 

@@ -1,0 +1,75 @@
+/*
+ * moe_backward.h -- backward pass of the MoE layer of moe.h (bf16 layers).
+ *
+ * The pages train the layer end to end ("Mixture of Experts: Scaling
+ * Parameters Without Scaling Compute", section "The MoE layer"; the
+ * load-balancing loss of section "The central problem: load balancing"):
+ * this call gives the gradients of
+ *     L = <dy, y> + aux_grad * aux + z_grad * z_loss
+ * for the forward pass moe_forward computes on the same inputs, where dy is
+ * the caller's upstream gradient of the layer output and aux_grad, z_grad
+ * the weights of the two router losses.  The routing decisions (top-k and
+ * the capacity drop) are held fixed, as automatic differentiation treats
+ * them; the gate weights carry gradient to the router logits through the
+ * softmax (and the renormalisation over the k choices), the auxiliary loss
+ * through the mean probabilities P (the counts f are constants) and the
+ * z-loss through the log-sum-exp.  Per kept assignment (token t, expert e,
+ * weight w; u = W1_e x + b1_e, h = GELU(u), o = W2_e h + b2_e):
+ *     dW2_e += (w dy_t) h^T, db2_e += w dy_t,
+ *     du = (W2_e^T (w dy_t)) * GELU'(u), dW1_e += du x_t^T, db1_e += du,
+ *     dx_t += W1_e^T du,
+ * and with s = <dy_t, w o> per slot the logit gradient dg (renormalised:
+ * s_e - w_e sum_j s_j on the choices; raw probabilities: s_e [e chosen] -
+ * p_e sum_j s_j) plus the two loss terms gives dW_r = dg^T x and
+ * dx += dg W_r.
+ *
+ * The call recomputes the forward intermediates it needs (routing, dispatch,
+ * the expert pre-activations, the expert outputs) from x and the weights:
+ * it does not read a previous moe_forward's workspace.
+ *
+ * Supported: cfg->dtype = MOE_BF16, token choice, drop on overflow,
+ * n_shared = 0 (others return MOE_ERR_UNSUPPORTED).
+ *
+ * Arguments (device pointers, caller-owned, layouts as in moe.h):
+ *   x [T][d] bf16; W_r [E][d] fp32; logit_bias [E] fp32 or NULL;
+ *   W1 [E][d_ff][d], b1 [E][d_ff], W2 [E][d][d_ff], b2 [E][d] bf16;
+ *   dy [T][d] bf16                       upstream gradient of y
+ *   aux_grad, z_grad                     weights of the two losses in L
+ *   dx [T][d] bf16                       written (not accumulated)
+ *   dW_r [E][d], dW1 [E][d_ff][d], db1 [E][d_ff], dW2 [E][d][d_ff],
+ *   db2 [E][d]                           fp32, written (not accumulated)
+ *   ws, ws_bytes                         at least
+ *                                        moe_backward_workspace_size(cfg)
+ *                                        bytes, 256-byte aligned, whose first
+ *                                        256 bytes hold the device error
+ *                                        record (moe_get_device_error)
+ * Alignment: x, dy, dx, W1, W2 16-byte aligned; d and d_ff multiples of 8.
+ * Asynchronous on `stream`; invalid arguments return a status before
+ * anything is enqueued.  T = 0 writes zero gradients.
+ */
+#ifndef MOE_BACKWARD_H
+#define MOE_BACKWARD_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#include "moe.h"
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Bytes of workspace moe_backward needs for this configuration (0 if the
+ * configuration is invalid or unsupported). */
+size_t moe_backward_workspace_size(const moe_config* cfg);
+
+moe_status moe_backward(const moe_config* cfg, const void* x, const float* W_r,
+                        const float* logit_bias, const void* W1, const void* b1, const void* W2,
+                        const void* b2, const void* dy, float aux_grad, float z_grad, void* dx,
+                        float* dW_r, float* dW1, float* db1, float* dW2, float* db2, void* ws,
+                        size_t ws_bytes, void* stream);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* MOE_BACKWARD_H */

@@ -1,5 +1,5 @@
-"""Thin ctypes binding of libmoe (the C ABI declared in include/moe.h and
-include/moe_pipeline.h).
+"""Thin ctypes binding of libmoe (the C ABI declared in include/moe.h,
+include/moe_pipeline.h and include/moe_backward.h).
 
 Argument marshalling only: every step of the layer runs in libmoe's CUDA
 kernels.  PyTorch supplies device memory and the current CUDA stream.  The
@@ -29,7 +29,8 @@ EXPORTED = ("moe_workspace_size", "moe_status_string", "moe_route", "moe_dispatc
             "moe_launch_count", "moe_dispatch_noalloc", "moe_check_wait_timeout",
             "moe_update_balance_bias", "moe_pipeline_workspace_size", "moe_pipeline_create",
             "moe_pipeline_submit", "moe_pipeline_join", "moe_pipeline_destroy",
-            "moe_route_expert_choice", "moe_expert_choice_capacity")
+            "moe_route_expert_choice", "moe_expert_choice_capacity",
+            "moe_backward_workspace_size", "moe_backward")
 
 
 class MoeConfig(ctypes.Structure):
@@ -85,6 +86,11 @@ def load() -> ctypes.CDLL:
         lib.moe_route_expert_choice.argtypes = [cfgp] + [_P] * 13 + [_P, sz, _P]
         lib.moe_expert_choice_capacity.restype = ctypes.c_int32
         lib.moe_expert_choice_capacity.argtypes = [cfgp]
+        lib.moe_backward_workspace_size.restype = ctypes.c_size_t
+        lib.moe_backward_workspace_size.argtypes = [cfgp]
+        lib.moe_backward.restype = ctypes.c_int
+        lib.moe_backward.argtypes = ([cfgp] + [_P] * 8 + [ctypes.c_float, ctypes.c_float]
+                                     + [_P] * 7 + [sz, _P])
         lib.moe_pipeline_workspace_size.restype = ctypes.c_size_t
         lib.moe_pipeline_workspace_size.argtypes = [cfgp, ctypes.c_int32]
         lib.moe_pipeline_create.restype = ctypes.c_int
@@ -214,6 +220,25 @@ def route_expert_choice(cfg, x, W_r, offsets, perm_token, perm_w, slot_of, ws, x
 def expert_choice_capacity(cfg: MoeConfig) -> int:
     """C, the tokens each expert takes under expert-choice routing."""
     return int(load().moe_expert_choice_capacity(ctypes.byref(cfg)))
+
+
+def backward_workspace(cfg: MoeConfig, device="cuda") -> torch.Tensor:
+    """A zero-filled workspace for moe_backward."""
+    n = int(load().moe_backward_workspace_size(ctypes.byref(cfg)))
+    if n == 0:
+        raise MoeError("moe_backward_workspace_size", 4)
+    return torch.zeros(n, dtype=torch.uint8, device=device)
+
+
+def backward(cfg, x, W_r, W1, b1, W2, b2, dy, dx, dW_r, dW1, db1, dW2, db2, ws, logit_bias=None,
+             aux_grad: float = 0.0, z_grad: float = 0.0, stream=None):
+    """Gradients of <dy, y> + aux_grad aux + z_grad z_loss (moe_backward):
+    dx (layer dtype), dW_r, dW1, db1, dW2, db2 (fp32), written in place."""
+    _check("moe_backward", load().moe_backward(
+        ctypes.byref(cfg), _ptr(x), _ptr(W_r), _ptr(logit_bias), _ptr(W1), _ptr(b1), _ptr(W2),
+        _ptr(b2), _ptr(dy), ctypes.c_float(aux_grad), ctypes.c_float(z_grad), _ptr(dx),
+        _ptr(dW_r), _ptr(dW1), _ptr(db1), _ptr(dW2), _ptr(db2), _ptr(ws), ws.numel(),
+        _stream(stream)))
 
 
 def launch_count() -> int:

@@ -1,0 +1,730 @@
+// Backward pass of the layer (include/moe_backward.h): the gradients of
+// <dy, y> + aux_grad * aux + z_grad * z_loss with the routing held fixed.
+//
+// "Mixture of Experts: Scaling Parameters Without Scaling Compute", section
+// "The MoE layer" (the layer being trained) and "The central problem: load
+// balancing" (the auxiliary loss and the router z-loss it is trained with).
+//
+// Steps (one stream):
+//   recompute   router (logits kept) + dispatch, GEMM1 without GELU -> U,
+//               H = GELU(U), GEMM2 -> y_perm = w * o
+//   router      one warp per token: s_j = <dy_t, y_perm[slot_j]>, the logit
+//               gradient dg (softmax / renormalisation, auxiliary loss,
+//               z-loss) and dY_perm[slot_j] = w_j dy_t
+//   dx path     W2, W1 transposed per expert; dH = dY_perm W2_e (the
+//               forward's tcgen05 GEMM with W2^T as its weight), dU = dH *
+//               GELU'(U), dX_perm = dU W1_e (W1^T); dx = sum over the
+//               token's slots of dX_perm + dg W_r
+//   weights     dW2_e = dY_perm_e^T H_e and dW1_e = dU_e^T X_perm_e on the
+//               CTA-pair tcgen05 kernel in its segment-reduction mode (both
+//               operands transposed per expert segment, K = the segment's
+//               rows), dW_r = dg^T x on CUDA cores (row-slice partials summed
+//               in a fixed order), db2, db1 = column sums over each expert's
+//               rows
+
+#include <cuda_runtime.h>
+#include <cuda_bf16.h>
+
+#include "../../include/moe_backward.h"
+#include "moe_device.cuh"
+#include "moe_internal.h"
+
+namespace moe {
+
+cudaError_t launch_grouped_gemm_tc(const moe_config& c, bool bf16_out, bool act, const void* A,
+                                   int64_t a_rows, const int32_t* offsets, const void* W,
+                                   const void* bias, const float* row_w, void* out,
+                                   int64_t out_rows, int n_out, int K, DeviceHeader* hdr,
+                                   cudaStream_t s);
+cudaError_t launch_segment_reduction_tc(int E, const int32_t* offsets, int64_t rows_cap,
+                                        const int32_t* koff, const void* TOK, int tok_rows,
+                                        const void* WT, int n_out, int64_t kcols, float* out,
+                                        DeviceHeader* hdr, cudaStream_t s);
+
+namespace {
+
+constexpr int kSegPad = 128;  // K columns per stage of the CTA-pair kernel
+
+using bf16 = __nv_bfloat16;
+
+__device__ __forceinline__ float gelu_grad(float u) {
+    // d/du of u Phi(u): Phi(u) + u phi(u)
+    return 0.5f * (1.0f + erff(u * 0.70710678118654752f)) +
+           u * 0.39894228040143268f * expf(-0.5f * u * u);
+}
+
+__device__ __forceinline__ void unpack8(uint4 q, float* f) {
+    const __nv_bfloat162* h = reinterpret_cast<const __nv_bfloat162*>(&q);
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        const float2 v = __bfloat1622float2(h[i]);
+        f[2 * i] = v.x;
+        f[2 * i + 1] = v.y;
+    }
+}
+
+__device__ __forceinline__ uint4 pack8(const float* f) {
+    uint4 q;
+    __nv_bfloat162* h = reinterpret_cast<__nv_bfloat162*>(&q);
+#pragma unroll
+    for (int i = 0; i < 4; ++i) h[i] = __floats2bfloat162_rn(f[2 * i], f[2 * i + 1]);
+    return q;
+}
+
+// H = GELU(U) over the kept rows (offsets[E] rows of F columns), 8 a thread.
+__global__ void __launch_bounds__(256) gelu_rows_kernel(const bf16* __restrict__ U,
+                                                         const int32_t* __restrict__ offsets,
+                                                         int E, int F, int64_t rows_cap,
+                                                         bf16* __restrict__ H) {
+    pdl_wait();
+    pdl_trigger();
+    const int64_t rows = min((int64_t)max(__ldg(offsets + E), 0), rows_cap);
+    const int64_t n8 = rows * F / 8;
+    for (int64_t i = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; i < n8;
+         i += (int64_t)gridDim.x * blockDim.x) {
+        float f[8];
+        unpack8(__ldg(reinterpret_cast<const uint4*>(U) + i), f);
+#pragma unroll
+        for (int j = 0; j < 8; ++j) f[j] = gelu_erf(f[j]);
+        reinterpret_cast<uint4*>(H)[i] = pack8(f);
+    }
+}
+
+// dU = dH * GELU'(U) in place over dH.
+__global__ void __launch_bounds__(256) gelu_grad_rows_kernel(const bf16* __restrict__ U,
+                                                              const int32_t* __restrict__ offsets,
+                                                              int E, int F, int64_t rows_cap,
+                                                              bf16* __restrict__ dH) {
+    pdl_wait();
+    pdl_trigger();
+    const int64_t rows = min((int64_t)max(__ldg(offsets + E), 0), rows_cap);
+    const int64_t n8 = rows * F / 8;
+    for (int64_t i = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; i < n8;
+         i += (int64_t)gridDim.x * blockDim.x) {
+        float u[8], g[8];
+        unpack8(__ldg(reinterpret_cast<const uint4*>(U) + i), u);
+        unpack8(reinterpret_cast<const uint4*>(dH)[i], g);
+#pragma unroll
+        for (int j = 0; j < 8; ++j) g[j] *= gelu_grad(u[j]);
+        reinterpret_cast<uint4*>(dH)[i] = pack8(g);
+    }
+}
+
+// One warp per token: the slot scores s_j, dY_perm rows and the logit
+// gradient dg[t][:].
+__global__ void __launch_bounds__(256) router_grad_kernel(
+    const float* __restrict__ logits, const int32_t* __restrict__ idx,
+    const float* __restrict__ topk_w, const int32_t* __restrict__ slot_of,
+    const float* __restrict__ y_perm, const bf16* __restrict__ dy,
+    const int32_t* __restrict__ top1, int T, int E, int k, int d, int64_t rows_cap,
+    int renormalize, float aux_grad, float z_grad, float* __restrict__ dg,
+    bf16* __restrict__ dY_perm) {
+    pdl_wait();
+    pdl_trigger();
+    const int lane = threadIdx.x % 32;
+    const int nwarps = gridDim.x * (blockDim.x / 32);
+    const int nv = d / 8;  // 8-column groups
+    for (int t = blockIdx.x * (blockDim.x / 32) + threadIdx.x / 32; t < T; t += nwarps) {
+        const uint4* dyr = reinterpret_cast<const uint4*>(dy + (size_t)t * d);
+        float s[kMaxTopK];
+        float stot = 0.f;
+        for (int j = 0; j < k; ++j) {
+            const int slot = __ldg(slot_of + (size_t)t * k + j);
+            float dot = 0.f;
+            if (slot >= 0 && slot < rows_cap) {
+                const float w = __ldg(topk_w + (size_t)t * k + j);
+                const float4* yr = reinterpret_cast<const float4*>(y_perm + (size_t)slot * d);
+                uint4* dyp = reinterpret_cast<uint4*>(dY_perm + (size_t)slot * d);
+                for (int v = lane; v < nv; v += 32) {
+                    float f[8];
+                    unpack8(__ldg(dyr + v), f);
+                    const float4 a = __ldg(yr + 2 * v), b = __ldg(yr + 2 * v + 1);
+                    dot += f[0] * a.x + f[1] * a.y + f[2] * a.z + f[3] * a.w + f[4] * b.x +
+                           f[5] * b.y + f[6] * b.z + f[7] * b.w;
+#pragma unroll
+                    for (int q = 0; q < 8; ++q) f[q] *= w;
+                    dyp[v] = pack8(f);
+                }
+#pragma unroll
+                for (int o = 16; o > 0; o >>= 1) dot += __shfl_xor_sync(0xffffffffu, dot, o);
+            }
+            s[j] = dot;
+            stot += dot;
+        }
+        // softmax statistics of the token's logits
+        const float* g = logits + (size_t)t * E;
+        float m = -3.402823466e38f;
+        for (int e = lane; e < E; e += 32) m = fmaxf(m, __ldg(g + e));
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
+        float ssum = 0.f, fp = 0.f;
+        for (int e = lane; e < E; e += 32) {
+            const float ex = expf(__ldg(g + e) - m);
+            ssum += ex;
+            fp += ex * (float)__ldg(top1 + e);
+        }
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) {
+            ssum += __shfl_xor_sync(0xffffffffu, ssum, o);
+            fp += __shfl_xor_sync(0xffffffffu, fp, o);
+        }
+        const float inv = 1.0f / ssum;
+        const float lse = m + logf(ssum);
+        fp *= inv / (float)T;  // sum_i f_i p_i
+        for (int e = lane; e < E; e += 32) {
+            const float pe = expf(__ldg(g + e) - m) * inv;
+            float v;
+            if (renormalize) {
+                v = 0.f;
+                for (int j = 0; j < k; ++j)
+                    if (__ldg(idx + (size_t)t * k + j) == e)
+                        v = s[j] - __ldg(topk_w + (size_t)t * k + j) * stot;
+            } else {
+                v = -pe * stot;
+                for (int j = 0; j < k; ++j)
+                    if (__ldg(idx + (size_t)t * k + j) == e) v += s[j];
+            }
+            const float fe = (float)__ldg(top1 + e) / (float)T;
+            v += aux_grad * (float)E / (float)T * pe * (fe - fp);
+            v += z_grad * 2.0f / (float)T * lse * pe;
+            dg[(size_t)t * E + e] = v;
+        }
+    }
+}
+
+// 64 x 64 bf16 tile transposes: 16-byte global loads and stores, the tile
+// in shared memory with an odd word stride (33 words a row) so that the
+// column reads spread over the banks.
+constexpr int TP = 64, TP_LD = 66;  // tile side, shared row length (bf16)
+
+// Stage rows src(i) (i < 64; null: zeros), columns c0 .. c0 + 63 of a
+// row-major matrix with `ld` columns, into tile[i][.].
+template <typename RowPtr>
+__device__ __forceinline__ void tile_load(bf16 (*tile)[TP_LD], RowPtr src, int c0, int C) {
+    const int t = threadIdx.x;
+#pragma unroll
+    for (int h = 0; h < 2; ++h) {
+        const int i = t / 8 + 32 * h, cg = (t % 8) * 8;
+        const bf16* row = src(i);
+        uint4 q = make_uint4(0, 0, 0, 0);
+        if (row != nullptr && c0 + cg < C) q = __ldg(reinterpret_cast<const uint4*>(row + c0 + cg));
+        const uint32_t* w = reinterpret_cast<const uint32_t*>(&q);
+        uint32_t* dst = reinterpret_cast<uint32_t*>(&tile[i][cg]);
+#pragma unroll
+        for (int k = 0; k < 4; ++k) dst[k] = w[k];
+    }
+}
+
+// Write the transposed tile: out row (c0 + j) gets tile[0..63][j] at
+// columns r_out .. r_out + 63 (dst(j): the row's start, null: skip).
+template <typename RowPtr>
+__device__ __forceinline__ void tile_store(bf16 (*tile)[TP_LD], RowPtr dst) {
+    const int t = threadIdx.x;
+#pragma unroll
+    for (int h = 0; h < 2; ++h) {
+        const int j = t / 8 + 32 * h, rg = (t % 8) * 8;
+        bf16* row = dst(j);
+        if (row == nullptr) continue;
+        uint4 q;
+        bf16* v = reinterpret_cast<bf16*>(&q);
+#pragma unroll
+        for (int k = 0; k < 8; ++k) v[k] = tile[rg + k][j];
+        *reinterpret_cast<uint4*>(row + rg) = q;
+    }
+}
+
+// out[e][c][r] = in[e][r][c] for R x C bf16 matrices (R, C multiples of 8).
+__global__ void __launch_bounds__(256) transpose_kernel(const bf16* __restrict__ in, int R, int C,
+                                                        bf16* __restrict__ out) {
+    __shared__ __align__(16) bf16 tile[TP][TP_LD];
+    pdl_wait();
+    pdl_trigger();
+    const size_t base = (size_t)blockIdx.z * R * C;
+    const int c0 = blockIdx.x * TP, r0 = blockIdx.y * TP;
+    tile_load(tile, [&](int i) -> const bf16* {
+        return r0 + i < R ? in + base + (size_t)(r0 + i) * C : nullptr;
+    }, c0, C);
+    __syncthreads();
+    // rows of the output are columns of the input; a partial last group of
+    // 8 output columns (R not a multiple of 64) is written element by element
+    const int t = threadIdx.x;
+#pragma unroll
+    for (int h = 0; h < 2; ++h) {
+        const int j = t / 8 + 32 * h, rg = (t % 8) * 8;
+        if (c0 + j >= C || r0 + rg >= R) continue;
+        bf16* row = out + base + (size_t)(c0 + j) * R + r0;
+        uint4 q;
+        bf16* v = reinterpret_cast<bf16*>(&q);
+#pragma unroll
+        for (int k = 0; k < 8; ++k) v[k] = tile[rg + k][j];
+        *reinterpret_cast<uint4*>(row + rg) = q;  // R % 8 == 0: the group is whole
+    }
+}
+
+__device__ __forceinline__ void store4(float* p, float4 v) { *reinterpret_cast<float4*>(p) = v; }
+__device__ __forceinline__ void store4(bf16* p, float4 v) {
+    __nv_bfloat162 lo = __floats2bfloat162_rn(v.x, v.y), hi = __floats2bfloat162_rn(v.z, v.w);
+    uint2 u;
+    u.x = *reinterpret_cast<uint32_t*>(&lo);
+    u.y = *reinterpret_cast<uint32_t*>(&hi);
+    *reinterpret_cast<uint2*>(p) = u;
+}
+
+// dx[t] = sum over the token's slots of dX_perm rows + sum_e dg[t][e] W_r[e];
+// one warp per (token, 512-column chunk).
+__global__ void __launch_bounds__(256) dx_kernel(const float* __restrict__ dX_perm,
+                                                  const int32_t* __restrict__ slot_of,
+                                                  const float* __restrict__ dg,
+                                                  const float* __restrict__ W_r, int T, int k,
+                                                  int E, int d, int64_t rows_cap,
+                                                  bf16* __restrict__ dx) {
+    pdl_wait();
+    pdl_trigger();
+    const int lane = threadIdx.x % 32;
+    const int nwarps = gridDim.x * (blockDim.x / 32);
+    const int nv = d / 4;
+    const int nch = (nv + 127) / 128;
+    const long long tasks = (long long)T * nch;
+    for (long long task = blockIdx.x * (blockDim.x / 32) + threadIdx.x / 32; task < tasks;
+         task += nwarps) {
+        const int t = (int)(task / nch);
+        const int v0 = (int)(task % nch) * 128 + lane;
+        float4 acc[4];
+#pragma unroll
+        for (int u = 0; u < 4; ++u) acc[u] = make_float4(0.f, 0.f, 0.f, 0.f);
+        for (int j = 0; j < k; ++j) {
+            const int sl = __ldg(slot_of + (size_t)t * k + j);
+            if (sl < 0 || sl >= rows_cap) continue;
+            const float4* row = reinterpret_cast<const float4*>(dX_perm + (size_t)sl * d);
+#pragma unroll
+            for (int u = 0; u < 4; ++u) {
+                if (v0 + 32 * u < nv) {
+                    const float4 q = __ldg(row + v0 + 32 * u);
+                    acc[u].x += q.x; acc[u].y += q.y; acc[u].z += q.z; acc[u].w += q.w;
+                }
+            }
+        }
+        for (int e = 0; e < E; ++e) {
+            const float ge = __ldg(dg + (size_t)t * E + e);
+            const float4* wr = reinterpret_cast<const float4*>(W_r + (size_t)e * d);
+#pragma unroll
+            for (int u = 0; u < 4; ++u) {
+                if (v0 + 32 * u < nv) {
+                    const float4 q = __ldg(wr + v0 + 32 * u);
+                    acc[u].x = fmaf(ge, q.x, acc[u].x); acc[u].y = fmaf(ge, q.y, acc[u].y);
+                    acc[u].z = fmaf(ge, q.z, acc[u].z); acc[u].w = fmaf(ge, q.w, acc[u].w);
+                }
+            }
+        }
+#pragma unroll
+        for (int u = 0; u < 4; ++u)
+            if (v0 + 32 * u < nv) store4(dx + (size_t)t * d + 4 * (v0 + 32 * u), acc[u]);
+    }
+}
+
+// Segment-reduction GEMM: C[e][m][n] = sum over rows r of segment e of
+// A[r][m] * B[r][n] (fp32 accumulation and output).  64 x 64 output tiles,
+// 4 x 4 per thread, 16-row slices staged in shared memory (the next slice is
+// loaded into registers while this one is used).  seg_len > 0: slice z =
+// blockIdx.z of seg_len rows (partial sums of one segment of `rows` rows);
+// else offsets, or (null) one segment of `rows` rows.
+constexpr int WG_BM = 64, WG_BN = 64, WG_BK = 16;
+
+template <typename TA, typename TB>
+__global__ void __launch_bounds__(256) wgrad_kernel(const TA* __restrict__ A,
+                                                     const TB* __restrict__ B,
+                                                     const int32_t* __restrict__ offsets,
+                                                     int rows, int64_t rows_cap, int M, int N,
+                                                     int seg_len, float* __restrict__ Cout) {
+    __shared__ float As[WG_BK][WG_BM + 4];
+    __shared__ float Bs[WG_BK][WG_BN + 4];
+    pdl_wait();
+    pdl_trigger();
+    const int e = blockIdx.z;
+    int r0 = 0, r1 = rows;
+    if (seg_len > 0) {  // slice z of `rows` rows (partial sums)
+        r0 = min(e * seg_len, rows);
+        r1 = min(r0 + seg_len, rows);
+    } else if (offsets != nullptr) {
+        r1 = (int)min((int64_t)max(__ldg(offsets + e + 1), 0), rows_cap);
+        r0 = min(max(__ldg(offsets + e), 0), r1);
+    }
+    const int m0 = blockIdx.y * WG_BM, n0 = blockIdx.x * WG_BN;
+    const int tid = threadIdx.x, tx = tid % 16, ty = tid / 16;
+    // loader: 16 rows x 64 columns per operand, 4 consecutive columns a thread
+    const int lr = tid / 16, lc = (tid % 16) * 4;
+    float av[4], bv[4];
+    auto load = [&](int rb) {
+        const int r = rb + lr;
+        const bool in = r < r1;
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+            av[q] = (in && m0 + lc + q < M) ? to_f32(A[(size_t)r * M + m0 + lc + q]) : 0.f;
+            bv[q] = (in && n0 + lc + q < N) ? to_f32(B[(size_t)r * N + n0 + lc + q]) : 0.f;
+        }
+    };
+    float acc[4][4] = {};
+    if (r0 < r1) load(r0);
+    for (int rb = r0; rb < r1; rb += WG_BK) {
+        __syncthreads();
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+            As[lr][lc + q] = av[q];
+            Bs[lr][lc + q] = bv[q];
+        }
+        __syncthreads();
+        if (rb + WG_BK < r1) load(rb + WG_BK);
+#pragma unroll
+        for (int kq = 0; kq < WG_BK; ++kq) {
+            const float4 a4 = *reinterpret_cast<const float4*>(&As[kq][ty * 4]);
+            const float4 b4 = *reinterpret_cast<const float4*>(&Bs[kq][tx * 4]);
+            const float ar[4] = {a4.x, a4.y, a4.z, a4.w};
+            const float br[4] = {b4.x, b4.y, b4.z, b4.w};
+#pragma unroll
+            for (int i = 0; i < 4; ++i)
+#pragma unroll
+                for (int j = 0; j < 4; ++j) acc[i][j] = fmaf(ar[i], br[j], acc[i][j]);
+        }
+    }
+    float* Ce = Cout + (size_t)e * M * N;
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        const int m = m0 + ty * 4 + i;
+        if (m >= M) continue;
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+            const int n = n0 + tx * 4 + j;
+            if (n < N) Ce[(size_t)m * N + n] = acc[i][j];
+        }
+    }
+}
+
+// out[e][m] = sum over the rows of segment e of A[r][m]: a block per (64
+// columns, expert); warp w sums rows w, w + 8, ... (two columns a lane),
+// then the eight partial sums are added in warp order.
+__global__ void __launch_bounds__(256) colsum_kernel(const bf16* __restrict__ A,
+                                                      const int32_t* __restrict__ offsets,
+                                                      int64_t rows_cap, int M,
+                                                      float* __restrict__ out) {
+    __shared__ float part[8][64];
+    pdl_wait();
+    pdl_trigger();
+    const int e = blockIdx.y, warp = threadIdx.x / 32, lane = threadIdx.x % 32;
+    const int m = blockIdx.x * 64 + 2 * lane;
+    const int r1 = (int)min((int64_t)max(__ldg(offsets + e + 1), 0), rows_cap);
+    const int r0 = min(max(__ldg(offsets + e), 0), r1);
+    float a = 0.f, b = 0.f;
+    if (m < M)  // M is even (a multiple of 8)
+        for (int r = r0 + warp; r < r1; r += 8) {
+            const float2 v = __bfloat1622float2(
+                *reinterpret_cast<const __nv_bfloat162*>(A + (size_t)r * M + m));
+            a += v.x;
+            b += v.y;
+        }
+    part[warp][2 * lane] = a;
+    part[warp][2 * lane + 1] = b;
+    __syncthreads();
+    const int c = threadIdx.x;
+    if (c < 64 && blockIdx.x * 64 + c < M) {
+        float v = 0.f;
+#pragma unroll
+        for (int w = 0; w < 8; ++w) v += part[w][c];
+        out[(size_t)e * M + blockIdx.x * 64 + c] = v;
+    }
+}
+
+// koff[e] = sum over e' < e of the segment lengths rounded up to kSegPad
+// (koff[E]: the total), one warp.
+__global__ void __launch_bounds__(32) seg_koff_kernel(const int32_t* __restrict__ offsets, int E,
+                                                      int64_t rows_cap,
+                                                      int32_t* __restrict__ koff) {
+    pdl_wait();
+    pdl_trigger();
+    const int lane = threadIdx.x;
+    int carry = 0;
+    for (int e0 = 0; e0 < E; e0 += 32) {
+        const int e = e0 + lane;
+        int v = 0;
+        if (e < E) {
+            const int r1 = (int)min((int64_t)max(__ldg(offsets + e + 1), 0), rows_cap);
+            const int r0 = min(max(__ldg(offsets + e), 0), r1);
+            v = (r1 - r0 + kSegPad - 1) / kSegPad * kSegPad;
+        }
+        int incl = v;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            const int u = __shfl_up_sync(0xffffffffu, incl, o);
+            if (lane >= o) incl += u;
+        }
+        if (e < E) koff[e] = carry + incl - v;
+        carry += __shfl_sync(0xffffffffu, incl, 31);
+    }
+    if (lane == 0) koff[E] = carry;
+}
+
+// Every expert segment of A [rows][M] transposed into out [M][kcols]:
+// out[m][koff[e] + j] = A[offsets[e] + j][m] for j < the segment's length,
+// 0 for the rest of its padded window.  64 x 64 tiles (a tile never spans
+// two windows: they start at multiples of kSegPad).
+__global__ void __launch_bounds__(256) seg_transpose_kernel(const bf16* __restrict__ A,
+                                                             const int32_t* __restrict__ offsets,
+                                                             const int32_t* __restrict__ koff,
+                                                             int E, int M, int64_t rows_cap,
+                                                             int64_t kcols, bf16* __restrict__ out) {
+    __shared__ __align__(16) bf16 tile[TP][TP_LD];
+    pdl_wait();
+    pdl_trigger();
+    const int c0 = blockIdx.x * TP, m0 = blockIdx.y * TP;
+    if (c0 >= __ldg(koff + E)) return;  // past the last window: never read
+    int lo = 0, hi = E - 1;
+    while (lo < hi) {  // last expert whose window starts at or before c0
+        const int mid = (lo + hi + 1) >> 1;
+        if (__ldg(koff + mid) <= c0) lo = mid; else hi = mid - 1;
+    }
+    const int r1 = (int)min((int64_t)max(__ldg(offsets + lo + 1), 0), rows_cap);
+    const int r0 = min(max(__ldg(offsets + lo), 0), r1);
+    const int j0 = c0 - __ldg(koff + lo);
+    // tile[i][.] = source row r0 + j0 + i (zeros past the segment), columns m0 ..
+    tile_load(tile, [&](int i) -> const bf16* {
+        const int r = r0 + j0 + i;
+        return r < r1 ? A + (size_t)r * M : nullptr;
+    }, m0, M);
+    __syncthreads();
+    tile_store(tile, [&](int j) -> bf16* {
+        return m0 + j < M ? out + (size_t)(m0 + j) * kcols + c0 : nullptr;
+    });
+}
+
+// out[i] = sum over z < S of part[z][i], in z order.
+__global__ void __launch_bounds__(256) sum_parts_kernel(const float* __restrict__ part, int S,
+                                                         int64_t n, float* __restrict__ out) {
+    pdl_wait();
+    pdl_trigger();
+    for (int64_t i = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; i < n;
+         i += (int64_t)gridDim.x * blockDim.x) {
+        float v = 0.f;
+        for (int z = 0; z < S; ++z) v += __ldg(part + (size_t)z * n + i);
+        out[i] = v;
+    }
+}
+
+int grid_for(int64_t work, int per_block) {
+    int64_t b = (work + per_block - 1) / per_block;
+    const int64_t cap = (int64_t)num_sms() * 8;
+    if (b > cap) b = cap;
+    return (int)(b < 1 ? 1 : b);
+}
+
+// Backward workspace: the forward layout, then these regions.
+struct BwdLayout {
+    size_t logits, u, dyp, dh, w1t, w2t, dg, koff, tt_d, tt_f, parts, total;
+    int64_t kcols;     // columns of the segment-transposed operands
+    int wr_slices;     // row slices of the router-weight gradient
+};
+
+// Row slices of dW_r = dg^T x (partial sums, then a fixed-order sum).
+int wr_slice_rows(int T) {
+    const int s = (T + 63) / 64;
+    return s > 256 ? s : 256;
+}
+
+size_t align256(size_t v) { return (v + 255) & ~size_t(255); }
+
+BwdLayout bwd_layout(const moe_config& c, const WsLayout& L) {
+    BwdLayout B{};
+    size_t o = align256(L.total);
+    auto take = [&](size_t bytes) {
+        const size_t at = o;
+        o = align256(o + bytes);
+        return at;
+    };
+    const size_t rows = (size_t)L.rows;
+    B.logits = take(sizeof(float) * (size_t)c.T * c.E);
+    B.u = take(2 * rows * c.d_ff);
+    B.dyp = take(2 * rows * c.d);
+    B.dh = take(2 * rows * c.d_ff);
+    B.w1t = take(2 * (size_t)c.E * c.d * c.d_ff);
+    B.w2t = take(2 * (size_t)c.E * c.d * c.d_ff);
+    B.dg = take(sizeof(float) * (size_t)c.T * c.E);
+    B.koff = take(sizeof(int32_t) * (size_t)(c.E + 1));
+    B.kcols = (L.rows + (int64_t)kSegPad * c.E + kSegPad - 1) / kSegPad * kSegPad;
+    B.tt_d = take(2 * (size_t)c.d * B.kcols);
+    B.tt_f = take(2 * (size_t)c.d_ff * B.kcols);
+    const int chunk = wr_slice_rows(c.T);
+    B.wr_slices = (c.T + chunk - 1) / chunk;
+    B.parts = take(sizeof(float) * (size_t)B.wr_slices * c.E * c.d);
+    B.total = o;
+    return B;
+}
+
+bool backward_supported(const moe_config& c) {
+    return c.dtype == MOE_BF16 && c.routing == MOE_TOKEN_CHOICE && c.overflow == MOE_DROP &&
+           c.n_shared == 0;
+}
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+}  // namespace
+}  // namespace moe
+
+using namespace moe;
+
+extern "C" {
+
+size_t moe_backward_workspace_size(const moe_config* cfg) {
+    if (config_status(cfg) != MOE_OK || !backward_supported(*cfg)) return 0;
+    const WsLayout L = ws_layout(*cfg);
+    return bwd_layout(*cfg, L).total;
+}
+
+moe_status moe_backward(const moe_config* cfg, const void* x, const float* W_r,
+                        const float* logit_bias, const void* W1, const void* b1, const void* W2,
+                        const void* b2, const void* dy, float aux_grad, float z_grad, void* dx,
+                        float* dW_r, float* dW1, float* db1, float* dW2, float* db2, void* ws,
+                        size_t ws_bytes, void* stream) {
+    moe_status st = config_status(cfg);
+    if (st != MOE_OK) return st;
+    const moe_config& c = *cfg;
+    if (!backward_supported(c)) return MOE_ERR_UNSUPPORTED;
+    if (dW_r == nullptr || dW1 == nullptr || db1 == nullptr || dW2 == nullptr || db2 == nullptr)
+        return MOE_ERR_INVALID_ARG;
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    const int E = c.E, d = c.d, F = c.d_ff, T = c.T, k = c.k;
+    // (an empty batch reads no token array: x, dy and dx may be null then)
+    if (T > 0 && (x == nullptr || W_r == nullptr || W1 == nullptr || b1 == nullptr ||
+                  W2 == nullptr || b2 == nullptr || dy == nullptr || dx == nullptr))
+        return MOE_ERR_INVALID_ARG;
+    if (T > 0 && (!aligned16(x) || !aligned16(dy) || !aligned16(dx) || !aligned16(W_r) ||
+                  !aligned16(W1) || !aligned16(W2)))
+        return MOE_ERR_ALIGNMENT;
+    const WsLayout L = ws_layout(c);
+    const BwdLayout Bw = bwd_layout(c, L);
+    if (ws == nullptr || (reinterpret_cast<uintptr_t>(ws) & 255u) != 0 || ws_bytes < Bw.total)
+        return MOE_ERR_WORKSPACE;
+    if (T == 0) {  // no token: every gradient is zero
+        const size_t wsz = sizeof(float) * (size_t)E * d * F;
+        if (cudaMemsetAsync(dW_r, 0, sizeof(float) * (size_t)E * d, s) != cudaSuccess ||
+            cudaMemsetAsync(dW1, 0, wsz, s) != cudaSuccess ||
+            cudaMemsetAsync(dW2, 0, wsz, s) != cudaSuccess ||
+            cudaMemsetAsync(db1, 0, sizeof(float) * (size_t)E * F, s) != cudaSuccess ||
+            cudaMemsetAsync(db2, 0, sizeof(float) * (size_t)E * d, s) != cudaSuccess)
+            return MOE_ERR_CUDA;
+        return MOE_OK;
+    }
+    DeviceHeader* hdr = at<DeviceHeader>(ws, L.header);
+    int32_t* idx = at<int32_t>(ws, L.topk_idx);
+    float* w = at<float>(ws, L.topk_w);
+    int32_t* offsets = at<int32_t>(ws, L.offsets);
+    int32_t* slot_of = at<int32_t>(ws, L.slot_of);
+    int32_t* perm_token = at<int32_t>(ws, L.perm_token);
+    float* perm_w = at<float>(ws, L.perm_w);
+    bf16* x_perm = at<bf16>(ws, L.x_perm);
+    bf16* H = at<bf16>(ws, L.h);
+    float* y_perm = at<float>(ws, L.y_perm);  // w * o, then dX_perm
+    float* logits = at<float>(ws, Bw.logits);
+    bf16* U = at<bf16>(ws, Bw.u);
+    bf16* dYp = at<bf16>(ws, Bw.dyp);
+    bf16* dH = at<bf16>(ws, Bw.dh);
+    bf16* W1T = at<bf16>(ws, Bw.w1t);
+    bf16* W2T = at<bf16>(ws, Bw.w2t);
+    float* dg = at<float>(ws, Bw.dg);
+    const int64_t rows = L.rows;
+
+    chain_begin();
+    // ---- recompute the forward intermediates
+    cudaError_t e = launch_route(c, x, W_r, logit_bias, nullptr, nullptr, logits, idx, w, nullptr,
+                                 nullptr, nullptr, ws, L, true, s);
+    if (e == cudaSuccess)
+        e = launch_scan_permute(c, x, idx, w, L.route.tokens * k, L.route.blocks, offsets, slot_of,
+                                perm_token, perm_w, x_perm, ws, L,
+                                route_loss_args(c, ws, L, nullptr, nullptr, nullptr), s);
+    if (e == cudaSuccess)
+        e = launch_grouped_gemm_tc(c, true, false, x_perm, rows, offsets, W1, b1, nullptr, U, rows,
+                                   F, d, hdr, s);
+    if (e == cudaSuccess)
+        e = launch_kernel(gelu_rows_kernel, dim3(grid_for(rows * F / 8, 256)), dim3(256), 0, s, 1,
+                          false, (const bf16*)U, (const int32_t*)offsets, E, F, rows, H);
+    if (e == cudaSuccess)
+        e = launch_grouped_gemm_tc(c, false, false, H, rows, offsets, W2, b2, perm_w, y_perm, rows,
+                                   d, F, hdr, s);
+    // ---- router gradient and the scaled upstream rows
+    if (e == cudaSuccess)
+        e = launch_kernel(router_grad_kernel, dim3(grid_for(T, 8)), dim3(256), 0, s, 1, false,
+                          (const float*)logits, (const int32_t*)idx, (const float*)w,
+                          (const int32_t*)slot_of, (const float*)y_perm,
+                          reinterpret_cast<const bf16*>(dy), (const int32_t*)at<int32_t>(ws, L.top1),
+                          T, E, k, d, rows, c.renormalize, aux_grad, z_grad, dg, dYp);
+    // ---- dx path: transposed weights, dH, GELU', dX_perm, dx
+    if (e == cudaSuccess)
+        e = launch_kernel(transpose_kernel, dim3((F + TP - 1) / TP, (d + TP - 1) / TP, E),
+                          dim3(256), 0, s, 1, false, reinterpret_cast<const bf16*>(W2), d, F, W2T);
+    if (e == cudaSuccess)
+        e = launch_kernel(transpose_kernel, dim3((d + TP - 1) / TP, (F + TP - 1) / TP, E),
+                          dim3(256), 0, s, 1, false, reinterpret_cast<const bf16*>(W1), F, d, W1T);
+    if (e == cudaSuccess)
+        e = launch_grouped_gemm_tc(c, true, false, dYp, rows, offsets, W2T, nullptr, nullptr, dH,
+                                   rows, F, d, hdr, s);
+    if (e == cudaSuccess)
+        e = launch_kernel(gelu_grad_rows_kernel, dim3(grid_for(rows * F / 8, 256)), dim3(256), 0,
+                          s, 1, false, (const bf16*)U, (const int32_t*)offsets, E, F, rows, dH);
+    if (e == cudaSuccess)
+        e = launch_grouped_gemm_tc(c, false, false, dH, rows, offsets, W1T, nullptr, nullptr,
+                                   y_perm, rows, d, F, hdr, s);
+    if (e == cudaSuccess) {
+        const long long tasks = (long long)T * ((d / 4 + 127) / 128);
+        e = launch_kernel(dx_kernel, dim3(grid_for(tasks, 8)), dim3(256), 0, s, 1, false,
+                          (const float*)y_perm, (const int32_t*)slot_of, (const float*)dg, W_r, T,
+                          k, E, d, rows, reinterpret_cast<bf16*>(dx));
+    }
+    // ---- weight gradients
+    int32_t* koff = at<int32_t>(ws, Bw.koff);
+    bf16* TTd = at<bf16>(ws, Bw.tt_d);
+    bf16* TTf = at<bf16>(ws, Bw.tt_f);
+    const int64_t kc = Bw.kcols;
+    const dim3 tgrid_d((unsigned)(kc / TP), (unsigned)((d + TP - 1) / TP));
+    const dim3 tgrid_f((unsigned)(kc / TP), (unsigned)((F + TP - 1) / TP));
+    if (e == cudaSuccess)  // dW_r = dg^T x: row-slice partials, then their sum
+        e = launch_kernel(wgrad_kernel<float, bf16>,
+                          dim3((d + 63) / 64, (E + 63) / 64, Bw.wr_slices), dim3(256), 0, s, 1,
+                          false, (const float*)dg, reinterpret_cast<const bf16*>(x),
+                          (const int32_t*)nullptr, T, (int64_t)T, E, d, wr_slice_rows(T),
+                          at<float>(ws, Bw.parts));
+    if (e == cudaSuccess)
+        e = launch_kernel(sum_parts_kernel, dim3(grid_for((int64_t)E * d, 256)), dim3(256), 0, s,
+                          1, false, (const float*)at<float>(ws, Bw.parts), Bw.wr_slices,
+                          (int64_t)E * d, dW_r);
+    if (e == cudaSuccess)
+        e = launch_kernel(seg_koff_kernel, dim3(1), dim3(32), 0, s, 1, false,
+                          (const int32_t*)offsets, E, rows, koff);
+    // dW2_e = dY_perm_e^T H_e: both operands segment-transposed
+    if (e == cudaSuccess)
+        e = launch_kernel(seg_transpose_kernel, tgrid_d, dim3(256), 0, s, 1, false,
+                          (const bf16*)dYp, (const int32_t*)offsets, (const int32_t*)koff, E, d,
+                          rows, kc, TTd);
+    if (e == cudaSuccess)
+        e = launch_kernel(seg_transpose_kernel, tgrid_f, dim3(256), 0, s, 1, false,
+                          (const bf16*)H, (const int32_t*)offsets, (const int32_t*)koff, E, F,
+                          rows, kc, TTf);
+    if (e == cudaSuccess)
+        e = launch_segment_reduction_tc(E, offsets, rows, koff, TTd, d, TTf, F, kc, dW2, hdr, s);
+    // dW1_e = dU_e^T X_perm_e
+    if (e == cudaSuccess)
+        e = launch_kernel(seg_transpose_kernel, tgrid_d, dim3(256), 0, s, 1, false,
+                          (const bf16*)x_perm, (const int32_t*)offsets, (const int32_t*)koff, E,
+                          d, rows, kc, TTd);
+    if (e == cudaSuccess)
+        e = launch_kernel(seg_transpose_kernel, tgrid_f, dim3(256), 0, s, 1, false,
+                          (const bf16*)dH, (const int32_t*)offsets, (const int32_t*)koff, E, F,
+                          rows, kc, TTf);
+    if (e == cudaSuccess)
+        e = launch_segment_reduction_tc(E, offsets, rows, koff, TTf, F, TTd, d, kc, dW1, hdr, s);
+    if (e == cudaSuccess)
+        e = launch_kernel(colsum_kernel, dim3((d + 63) / 64, E), dim3(256), 0, s, 1, false,
+                          (const bf16*)dYp, (const int32_t*)offsets, rows, d, db2);
+    if (e == cudaSuccess)
+        e = launch_kernel(colsum_kernel, dim3((F + 63) / 64, E), dim3(256), 0, s, 1, false,
+                          (const bf16*)dH, (const int32_t*)offsets, rows, F, db1);
+    return e == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;
+}
+
+}  // extern "C"

@@ -8,7 +8,7 @@
 // meet an fp32 tolerance) and the path for shapes the tcgen05 kernels do not
 // tile.  Each block computes a 64 x 64 tile C = A B^T of one expert segment
 // (A: segment rows x K, B: that expert's weight, N x K, both K-major), with a
-// 4 x 4 register tile per thread and 16-column shared-memory chunks.  The
+// 4 x 4 register tile per thread and 64-column shared-memory chunks.  The
 // grid covers the largest possible segment; blocks past the end of their
 // segment exit at once (offsets are read on the device).
 //   GEMM1 epilogue: h = GELU(acc + b1) stored as the layer dtype.
@@ -22,7 +22,8 @@
 namespace moe {
 namespace {
 
-constexpr int BM = 64, BN = 64, BK = 16, PAD = 4;
+constexpr int BM = 64, BN = 64, BK = 64, PAD = 4;
+constexpr int KQ = BK / 16;  // 4-column groups each thread loads per operand and K slice
 
 template <typename TIN, typename TOUT, bool GEMM1>
 __global__ void __launch_bounds__(256) grouped_gemm_simt(
@@ -43,27 +44,34 @@ __global__ void __launch_bounds__(256) grouped_gemm_simt(
     const TIN* We = W + (size_t)e * N * K;
     const int tid = threadIdx.x, tx = tid % 16, ty = tid / 16;
     float acc[4][4] = {};
-    // loader: 64 rows x 16 columns per operand = 1024 elements, 4 per thread;
-    // the next K slice is loaded into registers while this one is multiplied
+    // loader: 64 rows x BK columns per operand, KQ groups of 4 consecutive
+    // columns per thread; the next K slice is loaded into registers while
+    // this one is multiplied (few, long K slices: the short fp32 layers are
+    // latency-bound, one slice per load round trip)
     const int lr = tid / 4, lc = (tid % 4) * 4;
-    float av[4], bv[4];
+    float av[KQ][4], bv[KQ][4];
     auto load = [&](int k0) {
-        const int kk = k0 + lc;
 #pragma unroll
-        for (int q = 0; q < 4; ++q) {
-            const bool kin = kk + q < K;
-            av[q] = (m0 + lr < seg1 && kin) ? to_f32(A[(size_t)(m0 + lr) * K + kk + q]) : 0.f;
-            bv[q] = (n0 + lr < N && kin) ? to_f32(We[(size_t)(n0 + lr) * K + kk + q]) : 0.f;
+        for (int g = 0; g < KQ; ++g) {
+            const int kk = k0 + lc + 16 * g;
+#pragma unroll
+            for (int q = 0; q < 4; ++q) {
+                const bool kin = kk + q < K;
+                av[g][q] = (m0 + lr < seg1 && kin) ? to_f32(A[(size_t)(m0 + lr) * K + kk + q]) : 0.f;
+                bv[g][q] = (n0 + lr < N && kin) ? to_f32(We[(size_t)(n0 + lr) * K + kk + q]) : 0.f;
+            }
         }
     };
     load(0);
     for (int k0 = 0; k0 < K; k0 += BK) {
         __syncthreads();
 #pragma unroll
-        for (int q = 0; q < 4; ++q) {
-            As[lc + q][lr] = av[q];
-            Bs[lc + q][lr] = bv[q];
-        }
+        for (int g = 0; g < KQ; ++g)
+#pragma unroll
+            for (int q = 0; q < 4; ++q) {
+                As[lc + 16 * g + q][lr] = av[g][q];
+                Bs[lc + 16 * g + q][lr] = bv[g][q];
+            }
         __syncthreads();
         if (k0 + BK < K) load(k0 + BK);
 #pragma unroll

@@ -80,12 +80,22 @@ struct Cfg {
 
 struct Params {
     const int32_t* offsets;     // [E+1] segment starts (device)
-    const __nv_bfloat16* bias;  // [E][n_out]
+    const __nv_bfloat16* bias;  // [E][n_out] or null (no bias)
     const float* row_w;         // [rows] routing weight per row (second GEMM) or null
     void* out;                  // first GEMM: bf16 [rows][n_out]; second: fp32 [rows][n_out]
     DeviceHeader* hdr;
     uint64_t timeout_ns;
     int E, n_out, K, rows_cap;
+    int act;                    // first GEMM: 1 = GELU, 0 = none (the pre-activation)
+    // Segment-reduction mode (CTA-pair kernel, second-GEMM epilogue; koff not
+    // null): out[e*tok_rows + i][n] = sum over the rows r of expert e's
+    // segment (offsets) of TOK[i][koff[e] + r] * WT[n][koff[e] + r], where
+    // the token operand TOK [tok_rows][*] and the weight operand WT
+    // [n_out][*] hold every segment transposed, starting at column koff[e]
+    // and zero-padded to a multiple of 128 columns.  An empty segment gives
+    // zeros.
+    const int32_t* koff;
+    int tok_rows;
 };
 
 // Rows of an expert's segment (offsets clamped to the buffers).
@@ -162,11 +172,13 @@ template <int COLS, bool GEMM1>
 __device__ __forceinline__ void epilogue_tile(const Params& p, int e, int r0, int n, int fbase,
                                               uint32_t tmem_base, int acc_col, int q, int part,
                                               int nparts, int lane, uint8_t* stg,
-                                              const CUtensorMap* tm_out = nullptr) {
+                                              const CUtensorMap* tm_out = nullptr,
+                                              bool zero = false) {
     const int f0 = fbase + q * 32;  // first weight row (output feature) of this warp
     const int f = f0 + lane;
-    const float bias =
-        f < p.n_out ? __bfloat162float(p.bias[(size_t)e * p.n_out + f]) : 0.f;
+    const float bias = f < p.n_out && p.bias != nullptr
+                           ? __bfloat162float(p.bias[(size_t)e * p.n_out + f])
+                           : 0.f;
     const int c_begin = part * (COLS / nparts), c_end = min(c_begin + COLS / nparts, n);
     for (int c = c_begin; c < c_end; c += 32) {
         float v[32];
@@ -178,8 +190,8 @@ __device__ __forceinline__ void epilogue_tile(const Params& p, int e, int r0, in
             __nv_bfloat16* s16 = reinterpret_cast<__nv_bfloat16*>(stg);
 #pragma unroll
             for (int j = 0; j < 32; j += 2) {
-                const float2 g = gelu2_as7126(
-                    __fadd2_rn(make_float2(v[j], v[j + 1]), make_float2(bias, bias)));
+                const float2 u = __fadd2_rn(make_float2(v[j], v[j + 1]), make_float2(bias, bias));
+                const float2 g = p.act ? gelu2_as7126(u) : u;
                 s16[j * 32 + lane] = __float2bfloat16_rn(g.x);
                 s16[(j + 1) * 32 + lane] = __float2bfloat16_rn(g.y);
             }
@@ -197,6 +209,7 @@ __device__ __forceinline__ void epilogue_tile(const Params& p, int e, int r0, in
         } else {
             float wl = 1.f;
             if (p.row_w != nullptr && lane < rows_here) wl = __ldg(p.row_w + r0 + c + lane);
+            if (zero) wl = 0.f;  // no MMA wrote this accumulator
 #pragma unroll
             for (int j = 0; j < 32; ++j) v[j] = (v[j] + bias) * __shfl_sync(0xffffffffu, wl, j);
             if (tm_out != nullptr) {  // the previous chunk's store has read the staging rows
@@ -415,7 +428,7 @@ __device__ __forceinline__ void epilogue_gelu(const Params& p, int e, int r0, in
                                               int lane, uint8_t* stg, const CUtensorMap* tm_out) {
     const int g = lane >> 2;
     const int items = 2 * ((n + 31) / 32);
-    const __nv_bfloat16* bias = p.bias + (size_t)e * p.n_out;
+    const __nv_bfloat16* bias = p.bias != nullptr ? p.bias + (size_t)e * p.n_out : nullptr;
     __nv_bfloat16* out = reinterpret_cast<__nv_bfloat16*>(p.out);
     const uint32_t stg_s = tc::smem_u32(stg);
     // this lane's stmatrix row address (matrix lane/8, row lane%8) for the two stores
@@ -429,17 +442,22 @@ __device__ __forceinline__ void epilogue_gelu(const Params& p, int e, int r0, in
     for (int it = wq; it < items; it += NPQ) {
         const int h = it & 1, c = (it >> 1) * 32;
         const int fr = fbase + q * 32 + h * 16;  // first weight row of the item
-        const float ba = fr + g < p.n_out ? __bfloat162float(bias[fr + g]) : 0.f;
-        const float bb = fr + 8 + g < p.n_out ? __bfloat162float(bias[fr + 8 + g]) : 0.f;
+        const float ba = bias != nullptr && fr + g < p.n_out ? __bfloat162float(bias[fr + g]) : 0.f;
+        const float bb =
+            bias != nullptr && fr + 8 + g < p.n_out ? __bfloat162float(bias[fr + 8 + g]) : 0.f;
         uint32_t r[16];
         tc::tmem_ld_16x32(tmem_base + ((uint32_t)(q * 32 + h * 16) << 16) + (uint32_t)(acc_col + c), r);
         uint32_t pk[8];  // pk[2b]: rows g, pk[2b+1]: rows g + 8; tokens 8b + 2(lane%4), +1
 #pragma unroll
         for (int b = 0; b < 4; ++b) {
-            const float2 ga = gelu2_as7126(__fadd2_rn(
-                make_float2(__uint_as_float(r[4 * b]), __uint_as_float(r[4 * b + 1])), make_float2(ba, ba)));
-            const float2 gb = gelu2_as7126(__fadd2_rn(
-                make_float2(__uint_as_float(r[4 * b + 2]), __uint_as_float(r[4 * b + 3])), make_float2(bb, bb)));
+            float2 ga = __fadd2_rn(
+                make_float2(__uint_as_float(r[4 * b]), __uint_as_float(r[4 * b + 1])), make_float2(ba, ba));
+            float2 gb = __fadd2_rn(
+                make_float2(__uint_as_float(r[4 * b + 2]), __uint_as_float(r[4 * b + 3])), make_float2(bb, bb));
+            if (p.act) {
+                ga = gelu2_as7126(ga);
+                gb = gelu2_as7126(gb);
+            }
             const __nv_bfloat162 pa = __floats2bfloat162_rn(ga.x, ga.y);
             const __nv_bfloat162 pb = __floats2bfloat162_rn(gb.x, gb.y);
             pk[2 * b] = *reinterpret_cast<const uint32_t*>(&pa);
@@ -518,8 +536,14 @@ __device__ __forceinline__ Tile decode_pair_tile(int t, const int* s_tiles, cons
         const int mid = (lo + hi + 1) >> 1;
         if (s_tiles[mid] <= t) lo = mid; else hi = mid - 1;
     }
-    const int s0 = min(max(__ldg(p.offsets + lo), 0), p.rows_cap);
-    const int s1 = min(max(__ldg(p.offsets + lo + 1), s0), p.rows_cap);
+    int s0, s1;
+    if (p.koff != nullptr) {  // segment reduction: tok_rows output rows per expert
+        s0 = lo * p.tok_rows;
+        s1 = s0 + p.tok_rows;
+    } else {
+        s0 = min(max(__ldg(p.offsets + lo), 0), p.rows_cap);
+        s1 = min(max(__ldg(p.offsets + lo + 1), s0), p.rows_cap);
+    }
     const int nt = (s1 - s0 + BN2 - 1) / BN2;
     const int local = t - s_tiles[lo];
     Tile tl;
@@ -580,7 +604,8 @@ grouped_gemm_pair(const __grid_constant__ CUtensorMap tmA, const __grid_constant
             const int e = e0 + lane;
             int nt = 0;
             if (e < p.E) {
-                nt = ((seg_rows(p, e) + BN2 - 1) / BN2) * mt2;
+                const int rows_e = p.koff != nullptr ? p.tok_rows : seg_rows(p, e);
+                nt = ((rows_e + BN2 - 1) / BN2) * mt2;
             }
             int v = nt;
 #pragma unroll
@@ -611,16 +636,19 @@ grouped_gemm_pair(const __grid_constant__ CUtensorMap tmA, const __grid_constant
                 const Tile tl = decode_pair_tile(t, s_tiles, p, mt2);
                 const int m0 = tl.m0;  // pair tile base row
                 const int half_rows = ((tl.n + 31) & ~31) / 2;
-                const int arow = tl.e * p.n_out + m0 + rank * BM;
-                const int brow = tl.r0 + rank * half_rows;
-                for (int kb = 0; kb < KB; ++kb) {
+                const bool red = p.koff != nullptr;
+                const int arow = (red ? 0 : tl.e * p.n_out) + m0 + rank * BM;
+                const int brow = (red ? tl.r0 - tl.e * p.tok_rows : tl.r0) + rank * half_rows;
+                const int k0 = red ? __ldg(p.koff + tl.e) : 0;
+                const int KBt = red ? (seg_rows(p, tl.e) + ATOMS * BK - 1) / (ATOMS * BK) : KB;
+                for (int kb = 0; kb < KBt; ++kb) {
                     if (!wait_bar(&empty[stage], phase ^ 1, s_abort, p, 1)) { ok = false; break; }
                     if (leader) tc::mbar_expect_tx(&full[stage], bytes);
                     const uint32_t full_l = tc::cluster_addr(&full[stage], 0);
 #pragma unroll
                     for (int at = 0; at < ATOMS; ++at) {
                         uint8_t* sa = smem + stage * C::STAGE_BYTES + at * C::ATOM_BYTES;
-                        const int kc = (kb * ATOMS + at) * BK;
+                        const int kc = k0 + (kb * ATOMS + at) * BK;
                         tc::tma_load_2d_pair(sa, &tmA, full_l, kc, arow);
                         tc::tma_load_2d_pair(sa + A_BYTES, &tmB, full_l, kc, brow);
                     }
@@ -646,7 +674,10 @@ grouped_gemm_pair(const __grid_constant__ CUtensorMap tmA, const __grid_constant
                 if (!wait_bar(&tempty[acc], acc_phase ^ 1, s_abort, p, 2)) break;
                 tc::fence_after_sync();
                 const uint32_t d_tmem = tmem_base + (uint32_t)(acc * BN2);
-                for (int kb = 0; kb < KB; ++kb) {
+                const int KBt = p.koff != nullptr
+                                    ? (seg_rows(p, tl.e) + ATOMS * BK - 1) / (ATOMS * BK)
+                                    : KB;
+                for (int kb = 0; kb < KBt; ++kb) {
                     if (!wait_bar(&full[stage], phase, s_abort, p, 3)) { ok = false; break; }
                     tc::fence_after_sync();
 #pragma unroll
@@ -691,7 +722,8 @@ grouped_gemm_pair(const __grid_constant__ CUtensorMap tmA, const __grid_constant
                                       q, part, lane, stg, &tmO);
             else
                 epilogue_tile<BN2, GEMM1>(p, tl.e, tl.r0, tl.n, m0 + rank * BM, tmem_base, acc * BN2,
-                                      q, part, EW / 4, lane, stg, &tmO);
+                                      q, part, EW / 4, lane, stg, &tmO,
+                                      p.koff != nullptr && seg_rows(p, tl.e) == 0);
             tc::fence_before_sync();
             __syncwarp();
             if (lane == 0) tc::mbar_arrive_cluster_relaxed(tc::cluster_addr(&tempty[acc], 0));
@@ -864,9 +896,9 @@ cudaError_t launch_expert_ffn_tc(const moe_config& c, const void* x_perm, int64_
         !make_map(&maps[3], h, c.d_ff, (uint64_t)h_rows, box_x))
         return cudaErrorInvalidValue;
     Params p1{offsets, reinterpret_cast<const __nv_bfloat16*>(b1), nullptr, h, hdr,
-              g_tc_timeout_ns, c.E, c.d_ff, c.d, (int)h_rows};
+              g_tc_timeout_ns, c.E, c.d_ff, c.d, (int)h_rows, 1, nullptr, 0};
     Params p2{offsets, reinterpret_cast<const __nv_bfloat16*>(b2), perm_w, y_perm, hdr,
-              g_tc_timeout_ns, c.E, c.d, c.d_ff, (int)h_rows};
+              g_tc_timeout_ns, c.E, c.d, c.d_ff, (int)h_rows, 0, nullptr, 0};
     if (wide) {
         // 128-row token boxes for the pair kernel; h and y_perm as store targets
         CUtensorMap pm[6];
@@ -882,6 +914,55 @@ cudaError_t launch_expert_ffn_tc(const moe_config& c, const void* x_perm, int64_
         return launch_one_pair<3, false, 8, 2>(pm[2], pm[3], pm[5], p2, s);
     }
     return launch_pair<64, 8>(maps, p1, p2, s);
+}
+
+// One grouped GEMM out[r][n] = sum_k A[r][k] W_e[n][k] (+ bias_e[n]) over the
+// expert segments of A (the forward pass's kernels, for the backward pass):
+// bf16_out: bf16 out, optional GELU (act); else fp32 out times row_w[r]
+// (row_w null: 1).  A: [a_rows][K] bf16, W: [E][n_out][K] bf16, out:
+// [out_rows][n_out].  `wide` picks the CTA-pair kernel (as the forward does).
+cudaError_t launch_grouped_gemm_tc(const moe_config& c, bool bf16_out, bool act, const void* A,
+                                   int64_t a_rows, const int32_t* offsets, const void* W,
+                                   const void* bias, const float* row_w, void* out,
+                                   int64_t out_rows, int n_out, int K, DeviceHeader* hdr,
+                                   cudaStream_t s) {
+    if (out_rows == 0) return cudaSuccess;
+    const bool wide = (int64_t)c.T * c.k >= 96LL * c.E;
+    Params p{offsets, reinterpret_cast<const __nv_bfloat16*>(bias), bf16_out ? nullptr : row_w,
+             out, hdr, g_tc_timeout_ns, c.E, n_out, K, (int)out_rows, act ? 1 : 0, nullptr, 0};
+    CUtensorMap mw;
+    if (!make_map(&mw, W, (uint64_t)K, (uint64_t)c.E * n_out, BM)) return cudaErrorInvalidValue;
+    if (wide) {
+        CUtensorMap ma, mo;
+        if (!make_map(&ma, A, (uint64_t)K, (uint64_t)a_rows, BN2 / 2)) return cudaErrorInvalidValue;
+        if (bf16_out) {
+            if (!make_store_map_sw32(&mo, out, (uint64_t)n_out, (uint64_t)out_rows))
+                return cudaErrorInvalidValue;
+            return launch_one_pair<3, true, 16, 2>(mw, ma, mo, p, s);
+        }
+        if (!make_store_map_f32(&mo, out, (uint64_t)n_out, (uint64_t)out_rows))
+            return cudaErrorInvalidValue;
+        return launch_one_pair<3, false, 8, 2>(mw, ma, mo, p, s);
+    }
+    CUtensorMap ma;
+    if (!make_map(&ma, A, (uint64_t)K, (uint64_t)a_rows, BOX_ROWS)) return cudaErrorInvalidValue;
+    return bf16_out ? launch_one<64, 8, true>(mw, ma, p, s) : launch_one<64, 8, false>(mw, ma, p, s);
+}
+
+// Segment reduction on the CTA-pair kernel (see Params::koff): out fp32
+// [E*tok_rows][n_out], TOK [tok_rows][kcols] and WT [n_out][kcols] bf16.
+cudaError_t launch_segment_reduction_tc(int E, const int32_t* offsets, int64_t rows_cap,
+                                        const int32_t* koff, const void* TOK, int tok_rows,
+                                        const void* WT, int n_out, int64_t kcols, float* out,
+                                        DeviceHeader* hdr, cudaStream_t s) {
+    Params p{offsets, nullptr, nullptr, out, hdr, g_tc_timeout_ns, E, n_out, 0, (int)rows_cap, 0,
+             koff, tok_rows};
+    CUtensorMap mw, mt, mo;
+    if (!make_map(&mw, WT, (uint64_t)kcols, (uint64_t)n_out, BM) ||
+        !make_map(&mt, TOK, (uint64_t)kcols, (uint64_t)tok_rows, BN2 / 2) ||
+        !make_store_map_f32(&mo, out, (uint64_t)n_out, (uint64_t)E * tok_rows))
+        return cudaErrorInvalidValue;
+    return launch_one_pair<3, false, 8, 2>(mw, mt, mo, p, s);
 }
 
 }  // namespace moe

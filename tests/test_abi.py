@@ -168,3 +168,25 @@ def test_expert_choice_host_side():
     sh = ctypes.byref(B.config(16, 64, 64, 4, 1, n_shared=1, routing="expert"))
     assert lib.moe_forward(sh, FAKE, FAKE, None, None, FAKE, FAKE, FAKE, FAKE, FAKE, None, None,
                            None, None, FAKE, 1 << 40, None) == 4
+
+
+def test_backward_host_side():
+    lib = B.load()
+    c = B.config(64, 64, 128, 4, 2)
+    n = lib.moe_backward_workspace_size(ctypes.byref(c))
+    assert n >= B.workspace_size(c) and n % 256 == 0
+    for bad in (B.config(64, 64, 128, 4, 2, dtype="f32"), B.config(64, 64, 128, 4, 2, routing="expert"),
+                B.config(64, 64, 128, 4, 1, n_shared=1), B.config(64, 64, 128, 4, 2, capacity=5,
+                                                                   overflow="reroute")):
+        assert lib.moe_backward_workspace_size(ctypes.byref(bad)) == 0
+        assert lib.moe_backward(ctypes.byref(bad), *([FAKE] * 8), ctypes.c_float(0),
+                                ctypes.c_float(0), *([FAKE] * 6), FAKE, 1 << 40, None) == 4
+    cr = ctypes.byref(c)
+    args = [FAKE] * 8
+    outs = [FAKE] * 6  # dx, dW_r, dW1, db1, dW2, db2
+    assert lib.moe_backward(cr, *args, ctypes.c_float(0), ctypes.c_float(0), *outs, FAKE, n - 1,
+                            None) == 3
+    assert lib.moe_backward(cr, *args[:7], None, ctypes.c_float(0), ctypes.c_float(0), *outs, FAKE,
+                            n, None) == 1  # no dy
+    assert lib.moe_backward(cr, FAKE + 8, *args[1:], ctypes.c_float(0), ctypes.c_float(0), *outs,
+                            FAKE, n, None) == 2

@@ -1,0 +1,94 @@
+"""GPU parity of the backward pass (moe_backward) against the oracle's fp64
+gradients, routing from the kernels' own fp32 logits.
+
+Tolerance: the kernels keep the expert pre-activations, activations and the
+scaled upstream rows in bf16 (as the forward keeps H) and accumulate in fp32,
+so each gradient is compared by its relative Frobenius error, at most 2e-2
+(a handful of bf16 roundings, 2^-9 each, on the way), and its largest
+element error relative to the gradient's largest magnitude, at most 5e-2."""
+import numpy as np
+import pytest
+import torch
+
+from oracle import moe_oracle as O
+from parity import GpuRun, to_np
+from sparse_mixture_experts_71_b300 import binding as B
+from sparse_mixture_experts_71_b300 import inputs as I
+
+pytestmark = pytest.mark.gpu
+
+REL_FRO, REL_MAX = 2e-2, 5e-2
+
+CASES = [
+    # name, T, d, F, E, k, capacity, renormalize, zipf, aux_grad, z_grad
+    ("bwd-k2", 300, 256, 512, 8, 2, None, True, 0.0, 0.0, 0.0),
+    ("bwd-k2-losses", 300, 256, 512, 8, 2, None, True, 0.0, 0.7, 0.3),
+    ("bwd-top1-cap", 400, 128, 256, 8, 1, 40, False, 1.5, 0.5, 0.0),
+    ("bwd-decode", 64, 256, 512, 8, 2, None, True, 0.0, 0.0, 0.0),     # single-CTA GEMMs
+    ("bwd-e64-tc-router", 1100, 128, 128, 64, 2, 30, True, 1.0, 0.1, 0.1),
+    ("bwd-ragged", 1500, 64, 192, 5, 2, 500, True, 1.0, 0.0, 0.0),
+]
+
+
+def _close(name, got, want):
+    got = np.asarray(got, np.float64)
+    d = got - want
+    fro = np.linalg.norm(d) / max(np.linalg.norm(want), 1e-30)
+    mx = np.max(np.abs(d)) / max(np.max(np.abs(want)), 1e-30)
+    assert fro <= REL_FRO and mx <= REL_MAX, f"{name}: rel fro {fro:.3e}, rel max {mx:.3e}"
+    return fro
+
+
+@pytest.mark.parametrize("case", CASES, ids=[c[0] for c in CASES])
+def test_backward_matches_oracle(case):
+    name, T, d, F, E, k, cap, renorm, zipf, aux_grad, z_grad = case
+    wl = I.Workload(name, T, d, F, E, k, capacity=cap, renormalize=renorm, zipf_bias=zipf)
+    inp = I.make_inputs(wl, seed=41)
+    run = GpuRun(wl, inp)
+    D = run.dev
+    g = run.forward()["logits"]
+    dy_np = I.router_noise(T, d, 1.0, seed=42)  # any seeded (T, d) draw serves as dy
+    dy = torch.from_numpy(dy_np).to(torch.bfloat16).cuda()
+    cfg = run.cfg
+    ws = B.backward_workspace(cfg)
+    f32 = dict(dtype=torch.float32, device="cuda")
+    out = dict(dx=torch.empty_like(D["x"]), dW_r=torch.empty((E, d), **f32),
+               dW1=torch.empty((E, F, d), **f32), db1=torch.empty((E, F), **f32),
+               dW2=torch.empty((E, d, F), **f32), db2=torch.empty((E, d), **f32))
+    B.backward(cfg, D["x"], D["W_r"], D["W1"], D["b1"], D["W2"], D["b2"], dy, out["dx"],
+               out["dW_r"], out["dW1"], out["db1"], out["dW2"], out["db2"], ws,
+               logit_bias=D["logit_bias"], aux_grad=aux_grad, z_grad=z_grad)
+    torch.cuda.synchronize()
+    assert B.get_device_error(ws)[0] == 0
+    ref = O.moe_backward(inp.as_f32("x"), inp.W_r, inp.as_f32("W1"), inp.as_f32("b1"),
+                         inp.as_f32("W2"), inp.as_f32("b2"),
+                         dy.float().cpu().numpy(), k=k, renormalize=renorm, capacity=cap,
+                         logit_bias=inp.logit_bias, logits=to_np(g), aux_grad=aux_grad,
+                         z_grad=z_grad)
+    errs = {n: _close(n, to_np(out[n]), ref[n]) for n in out}
+    print(name, " ".join(f"{n} {v:.2e}" for n, v in errs.items()))
+    # deterministic: a second call gives the same bits
+    again = {n: torch.empty_like(v) for n, v in out.items()}
+    B.backward(cfg, D["x"], D["W_r"], D["W1"], D["b1"], D["W2"], D["b2"], dy, again["dx"],
+               again["dW_r"], again["dW1"], again["db1"], again["dW2"], again["db2"], ws,
+               logit_bias=D["logit_bias"], aux_grad=aux_grad, z_grad=z_grad)
+    torch.cuda.synchronize()
+    for n in out:
+        assert torch.equal(out[n], again[n]), n
+
+
+def test_backward_empty_batch_is_zero():
+    wl = I.Workload("bwd-empty", 0, 64, 128, 4, 2)
+    cfg = B.config(0, 64, 128, 4, 2)
+    ws = B.backward_workspace(cfg)
+    f32 = dict(dtype=torch.float32, device="cuda")
+    outs = [torch.full(s, 7.0, **f32) for s in ((4, 64), (4, 128, 64), (4, 128), (4, 64, 128),
+                                                  (4, 64))]
+    x = torch.empty((0, 64), dtype=torch.bfloat16, device="cuda")
+    w = torch.zeros((4, 128, 64), dtype=torch.bfloat16, device="cuda")
+    B.backward(cfg, x, torch.zeros((4, 64), **f32), w, torch.zeros((4, 128), dtype=torch.bfloat16,
+               device="cuda"), torch.zeros((4, 64, 128), dtype=torch.bfloat16, device="cuda"),
+               torch.zeros((4, 64), dtype=torch.bfloat16, device="cuda"), x, x, *outs, ws)
+    torch.cuda.synchronize()
+    assert all(not o.any() for o in outs)
+    assert wl.T == 0
