@@ -48,12 +48,17 @@ PEAKS_FALLBACK = {"hbm_gbs": 6400.0, "bf16_tflops": 1800.0, "bf16_tflops_sustain
 METRIC = "MoE-layer fwd tokens/s and achieved TFLOP/s (or HBM GB/s) vs B300 roofline"
 
 # DRAM bytes (read + write) of one expert-FFN launch pair (GEMM1 + GEMM2) from
-# an ncu capture of the current kernels; summaries with the commands are in
-# profiles/grouped_gemm_*.md.  Workloads without a capture report null.
+# an ncu capture of the current kernels; the summary with the commands is
+# profiles/grouped_gemm_dram_traffic.md.  Workloads without a capture report
+# null.
 TRAFFIC_BYTES = {
-    "bf16-T4096-d1024-F4096-E8-top2": (84.050 + 31.683 + 139.586 + 12.432) * 1e6,
-    "decode-bf16-T64-d4096-F14336-E8-top2": (941.866 + 6.017 + 944.308 + 1.891) * 1e6,
-    "switch-bf16-T32768-d2048-F8192-E64-top1-cap640": (719.386 + 56.738 + 778.406 + 26.803) * 1e6,
+    "bf16-T4096-d1024-F4096-E8-top2": (84.054 + 31.461 + 139.353 + 11.425) * 1e6,
+    "decode-bf16-T64-d4096-F14336-E8-top2": (941.527 + 6.074 + 944.296 + 1.548) * 1e6,
+    "switch-bf16-T32768-d2048-F8192-E64-top1-cap640": (719.259 + 56.750 + 779.743 + 26.946) * 1e6,
+    "finegrained-bf16-T4096-d2048-F1024-E64-top6": (372.038 + 39.568 + 325.019 + 160.830) * 1e6,
+    "expertchoice-bf16-T4096-d1024-F4096-E8-C1024": (83.999 + 31.100 + 143.555 + 9.596) * 1e6,
+    "switch-reroute-bf16-T32768-d2048-F8192-E64-top1-cap640":
+        (997.822 + 97.153 + 1104.171 + 47.158) * 1e6,
 }
 
 
