@@ -57,7 +57,7 @@ def to_np(t: torch.Tensor) -> np.ndarray:
     return t.detach().cpu().numpy()
 
 
-class GpuRun:
+class LibRun:
     """Every stage of one layer call through the C ABI, with its outputs."""
 
     def __init__(self, wl, inp, dev=None, stream=None):

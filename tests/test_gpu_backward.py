@@ -11,7 +11,7 @@ import pytest
 import torch
 
 from oracle import moe_oracle as O
-from parity import GpuRun, to_np
+from parity import LibRun, to_np
 from sparse_mixture_experts_71_b300 import binding as B
 from sparse_mixture_experts_71_b300 import inputs as I
 
@@ -44,7 +44,7 @@ def test_backward_matches_oracle(case):
     name, T, d, F, E, k, cap, renorm, zipf, aux_grad, z_grad = case
     wl = I.Workload(name, T, d, F, E, k, capacity=cap, renormalize=renorm, zipf_bias=zipf)
     inp = I.make_inputs(wl, seed=41)
-    run = GpuRun(wl, inp)
+    run = LibRun(wl, inp)
     D = run.dev
     g = run.forward()["logits"]
     dy_np = I.router_noise(T, d, 1.0, seed=42)  # any seeded (T, d) draw serves as dy

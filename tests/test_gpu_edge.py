@@ -6,7 +6,7 @@ import pytest
 import torch
 
 from oracle import moe_oracle as O
-from parity import GpuRun, assert_y_close, oracle_on, to_np
+from parity import LibRun, assert_y_close, oracle_on, to_np
 from sparse_mixture_experts_71_b300 import binding as B
 from sparse_mixture_experts_71_b300 import inputs as I
 
@@ -54,7 +54,7 @@ def _check(wl, inp, r):
 def test_small_shapes(case):
     wl = _wl(*case)
     inp = I.make_inputs(wl, seed=11)
-    run = GpuRun(wl, inp)
+    run = LibRun(wl, inp)
     r = run.staged()
     ref = _check(wl, inp, r)
     if wl.capacity == 0:
@@ -70,7 +70,7 @@ def test_empty_experts_and_zipf_skew():
     """A strong per-expert logit bias leaves most experts empty."""
     wl = _wl("zipf", 500, 64, 128, 16, 1, "bf16", 40, False, zipf=6.0)
     inp = I.make_inputs(wl, seed=3)
-    r = GpuRun(wl, inp).staged()
+    r = LibRun(wl, inp).staged()
     ref = _check(wl, inp, r)
     assert np.sum(ref.counts == 0) >= 4 and np.any(~ref.kept)
 
@@ -81,7 +81,7 @@ def test_logits_in_routes_identically():
     inp = I.make_inputs(wl, seed=5)
     logits = np.round(np.random.default_rng(0).standard_normal((96, 8)), 1).astype(np.float32)
     logits[::3, 5] = logits[::3, 2]  # exact ties
-    run = GpuRun(wl, inp)
+    run = LibRun(wl, inp)
     r = run.staged(logits_in=torch.from_numpy(logits).cuda())
     assert np.array_equal(to_np(r["logits"]), logits)
     ref = oracle_on(inp, wl, logits=logits)
@@ -92,7 +92,7 @@ def test_logits_in_routes_identically():
 def test_empty_batch():
     wl = _wl("t0", 0, 32, 64, 4, 2, "bf16", None, True)
     inp = I.make_inputs(wl, seed=0)
-    run = GpuRun(wl, inp)
+    run = LibRun(wl, inp)
     r = run.staged()
     assert float(r["aux"][0]) == 0.0 and not torch.any(r["counts"] != 0)
     assert float(r["z"][0]) == 0.0
@@ -104,7 +104,7 @@ def test_out_of_range_expert_is_flagged_not_written():
     recorded in the workspace; the other assignments are still dispatched."""
     wl = _wl("bad-idx", 40, 32, 64, 4, 2, "bf16", None, True)
     inp = I.make_inputs(wl, seed=1)
-    run = GpuRun(wl, inp)
+    run = LibRun(wl, inp)
     r = run.staged()
     idx = r["idx"].clone()
     idx[7, 1] = 9
@@ -145,7 +145,7 @@ def test_segment_sizes_around_tile_boundaries(name):
     np.random.default_rng(1).shuffle(expert)
     logits = np.random.default_rng(2).standard_normal((T, E)).astype(np.float32)
     logits[np.arange(T), expert] = 8.0  # the chosen expert is the top-1
-    run = GpuRun(wl, inp)
+    run = LibRun(wl, inp)
     r = run.staged(logits_in=torch.from_numpy(logits).cuda())
     ref = oracle_on(inp, wl, logits=logits)
     assert np.array_equal(to_np(r["counts"]), np.array(sizes))
@@ -162,7 +162,7 @@ def test_stalled_pipeline_wait_reports_time_out_and_context_survives():
     call on the same workspace and context runs normally."""
     wl = _wl("after-timeout", 2048, 64, 128, 8, 2, "bf16", None, True)
     inp = I.make_inputs(wl, seed=6)
-    run = GpuRun(wl, inp)
+    run = LibRun(wl, inp)
     B.check_wait_timeout(run.ws, 2_000_000)  # 2 ms
     assert B.get_device_error(run.ws) == (6, 2, 900)
     assert B.get_device_error(run.ws)[0] == 0  # cleared
@@ -190,7 +190,7 @@ def test_noisy_gating(case):
     inp = I.make_inputs(wl, seed=12)
     noise_np = I.router_noise(T, E, 0.5, seed=3)
     noise = torch.from_numpy(noise_np).cuda()
-    run = GpuRun(wl, inp)
+    run = LibRun(wl, inp)
     r = run.staged(noise=noise)
     g = to_np(r["logits"])
     want = O.router_logits(inp.as_f32("x"), inp.W_r, None, noise_np)
@@ -207,7 +207,7 @@ def test_balance_bias_update_matches_oracle_and_evens_out_load():
     router brings the first-choice loads toward balance."""
     wl = _wl("balance", 2048, 64, 64, 16, 2, "bf16", None, True, zipf=1.0)
     inp = I.make_inputs(wl, seed=9)
-    run = GpuRun(wl, inp)
+    run = LibRun(wl, inp)
     bias = run.dev["logit_bias"].clone()
     idx = torch.empty((wl.T, wl.k), dtype=torch.int32, device="cuda")
     w = torch.empty((wl.T, wl.k), dtype=torch.float32, device="cuda")
@@ -248,7 +248,7 @@ def test_shared_experts(case):
     wl = I.Workload(name, T, d, F, E, k, dtype=dt, renormalize=True, capacity=cap,
                     init="uniform" if dt == "f32" else "normal", n_shared=ns)
     inp = I.make_inputs(wl, seed=13)
-    run = GpuRun(wl, inp)
+    run = LibRun(wl, inp)
     r = run.staged()
     ref = _check(wl, inp, r)
     assert np.array_equal(to_np(r["idx"])[:, k:], np.tile(np.arange(ns), (T, 1)))

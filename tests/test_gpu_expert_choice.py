@@ -14,7 +14,7 @@ import pytest
 import torch
 
 from oracle import moe_oracle as O
-from parity import GpuRun, assert_y_close, to_np
+from parity import LibRun, assert_y_close, to_np
 from sparse_mixture_experts_71_b300 import binding as B
 from sparse_mixture_experts_71_b300 import inputs as I
 
@@ -89,7 +89,7 @@ def _check(wl, inp, run, r):
 def test_expert_choice_small_shapes(case):
     wl = _wl(*case)
     inp = I.make_inputs(wl, seed=21)
-    run = GpuRun(wl, inp)
+    run = LibRun(wl, inp)
     r = run.staged_ec()
     ref, gsel = _check(wl, inp, run, r)
     if wl.E == 1:  # equal probabilities: the first C tokens
@@ -107,7 +107,7 @@ def test_expert_choice_small_shapes(case):
 def test_expert_choice_full_workload():
     wl = I.EXPERTCHOICE
     inp = I.make_inputs(wl, seed=0)
-    run = GpuRun(wl, inp)
+    run = LibRun(wl, inp)
     r = run.staged_ec()
     g = to_np(r["logits"])
     ref_logits = O.router_logits(inp.as_f32("x"), inp.W_r, inp.logit_bias)
@@ -120,7 +120,7 @@ def test_expert_choice_logits_in_and_noise():
     """Caller logits replace the router; noise shifts the logits it uses."""
     wl = _wl("ec-logits", 200, 64, 96, 8, 2, "bf16", None)
     inp = I.make_inputs(wl, seed=22)
-    run = GpuRun(wl, inp)
+    run = LibRun(wl, inp)
     base = run.staged_ec()
     again = run.staged_ec(logits_in=base["logits"])
     assert torch.equal(again["perm_token"], base["perm_token"])

@@ -13,7 +13,7 @@ import pytest
 import torch
 
 from oracle import moe_oracle as O
-from parity import (GpuRun, assert_y_close, near_tie_tokens, oracle_on, sample_tokens, to_np)
+from parity import (LibRun, assert_y_close, near_tie_tokens, oracle_on, sample_tokens, to_np)
 from sparse_mixture_experts_71_b300 import inputs as I
 
 pytestmark = pytest.mark.gpu
@@ -28,7 +28,7 @@ def _run(wl):
         _cache.clear()
         torch.cuda.empty_cache()
         inp = I.make_inputs(wl, seed=0)
-        run = GpuRun(wl, inp)
+        run = LibRun(wl, inp)
         _cache[wl.name] = (inp, run, run.staged())
     return _cache[wl.name]
 

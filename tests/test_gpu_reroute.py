@@ -8,7 +8,7 @@ import pytest
 import torch
 
 from oracle import moe_oracle as O
-from parity import GpuRun, assert_y_close, oracle_on, to_np
+from parity import LibRun, assert_y_close, oracle_on, to_np
 from sparse_mixture_experts_71_b300 import binding as B
 from sparse_mixture_experts_71_b300 import inputs as I
 
@@ -39,7 +39,7 @@ def test_reroute(case):
     wl = _wl(*case)
     T, E, k = wl.T, wl.E, wl.k
     inp = I.make_inputs(wl, seed=31)
-    run = GpuRun(wl, inp)
+    run = LibRun(wl, inp)
     r = run.staged()
     g = to_np(r["logits"])
     ref = oracle_on(inp, wl, logits=g)
@@ -79,7 +79,7 @@ def test_reroute_moves_slots_on_a_skewed_router():
     """The skewed cases above reroute a good share of the dropped slots."""
     wl = _wl(*CASES[0])
     inp = I.make_inputs(wl, seed=31)
-    r = GpuRun(wl, inp).staged()
+    r = LibRun(wl, inp).staged()
     ref = oracle_on(inp, wl, logits=to_np(r["logits"]), tokens=np.array([], np.int64))
     drop = O.moe_forward(inp.as_f32("x"), inp.W_r, inp.as_f32("W1"), inp.as_f32("b1"),
                          inp.as_f32("W2"), inp.as_f32("b2"), k=wl.k, capacity=wl.capacity,
@@ -93,7 +93,7 @@ def test_reroute_full_switch_workload():
     from parity import sample_tokens
     wl = I.SWITCH_REROUTE
     inp = I.make_inputs(wl, seed=0)
-    run = GpuRun(wl, inp)
+    run = LibRun(wl, inp)
     r = run.staged()
     g = to_np(r["logits"])
     ref = oracle_on(inp, wl, logits=g, tokens=np.array([], np.int64))
