@@ -20,7 +20,8 @@
 //               operands transposed per expert segment, K = the segment's
 //               rows), dW_r = dg^T x on CUDA cores (row-slice partials summed
 //               in a fixed order), db2, db1 = column sums over each expert's
-//               rows
+//               rows.  GELU and GELU' use the forward epilogue's
+//               Abramowitz & Stegun 7.1.26 erf.
 
 #include <cuda_runtime.h>
 #include <cuda_bf16.h>
@@ -47,10 +48,26 @@ constexpr int kSegPad = 128;  // K columns per stage of the CTA-pair kernel
 
 using bf16 = __nv_bfloat16;
 
+// d/du of the GELU u Phi(u): Phi(u) + u phi(u).  Phi from the erf
+// approximation of Abramowitz & Stegun, formula 7.1.26 (|erf error| <=
+// 1.5e-7, the form the forward GEMM's epilogue uses): with z = |u| / sqrt 2,
+// erf(z) = 1 - q(t) e^{-z^2}, t = 1 / (1 + p z), so Phi(u) = 1 - h for
+// u >= 0 and h for u < 0, h = 0.5 q(t) e^{-u^2/2}; phi(u) = e^{-u^2/2} /
+// sqrt(2 pi) shares the exponential.  e^{-u^2/2} = 2^{-y^2} with
+// y = |u| sqrt(log2(e) / 2), and p z = (p / sqrt(log2 e)) y.
 __device__ __forceinline__ float gelu_grad(float u) {
-    // d/du of u Phi(u): Phi(u) + u phi(u)
-    return 0.5f * (1.0f + erff(u * 0.70710678118654752f)) +
-           u * 0.39894228040143268f * expf(-0.5f * u * u);
+    constexpr float c = 0.84932180028801904f;  // sqrt(log2(e) / 2)
+    constexpr float pz = 0.27273748f;          // 0.3275911 / sqrt(log2 e)
+    const float y = fabsf(u) * c;
+    const float t = __fdividef(1.0f, fmaf(y, pz, 1.0f));
+    float q = fmaf(t, 1.061405429f, -1.453152027f);
+    q = fmaf(t, q, 1.421413741f);
+    q = fmaf(t, q, -0.284496736f);
+    q = fmaf(t, q, 0.254829592f);
+    q *= t;
+    const float e = ex2_approx(-y * y);
+    const float h = 0.5f * q * e;
+    return (u >= 0.f ? 1.0f - h : h) + u * e * 0.39894228040143268f;
 }
 
 __device__ __forceinline__ void unpack8(uint4 q, float* f) {
@@ -85,7 +102,11 @@ __global__ void __launch_bounds__(256) gelu_rows_kernel(const bf16* __restrict__
         float f[8];
         unpack8(__ldg(reinterpret_cast<const uint4*>(U) + i), f);
 #pragma unroll
-        for (int j = 0; j < 8; ++j) f[j] = gelu_erf(f[j]);
+        for (int j = 0; j < 8; j += 2) {  // the forward epilogue's GELU
+            const float2 g = gelu2_as7126(make_float2(f[j], f[j + 1]));
+            f[j] = g.x;
+            f[j + 1] = g.y;
+        }
         reinterpret_cast<uint4*>(H)[i] = pack8(f);
     }
 }
@@ -322,80 +343,46 @@ __global__ void __launch_bounds__(256) dx_kernel(const float* __restrict__ dX_pe
     }
 }
 
-// Segment-reduction GEMM: C[e][m][n] = sum over rows r of segment e of
-// A[r][m] * B[r][n] (fp32 accumulation and output).  64 x 64 output tiles,
-// 4 x 4 per thread, 16-row slices staged in shared memory (the next slice is
-// loaded into registers while this one is used).  seg_len > 0: slice z =
-// blockIdx.z of seg_len rows (partial sums of one segment of `rows` rows);
-// else offsets, or (null) one segment of `rows` rows.
-constexpr int WG_BM = 64, WG_BN = 64, WG_BK = 16;
+// Partial router-weight gradients: part[z][e][j] = sum over the tokens t of
+// row slice z of dg[t][e] x[t][j].  A thread per column j (256 a block),
+// EG experts per pass with their accumulators in registers, 64-token chunks
+// of dg staged in shared memory.
+constexpr int WR_CHUNK = 64;
 
-template <typename TA, typename TB>
-__global__ void __launch_bounds__(256) wgrad_kernel(const TA* __restrict__ A,
-                                                     const TB* __restrict__ B,
-                                                     const int32_t* __restrict__ offsets,
-                                                     int rows, int64_t rows_cap, int M, int N,
-                                                     int seg_len, float* __restrict__ Cout) {
-    __shared__ float As[WG_BK][WG_BM + 4];
-    __shared__ float Bs[WG_BK][WG_BN + 4];
+template <int WR_EG>
+__global__ void __launch_bounds__(256) wr_grad_kernel(const float* __restrict__ dg,
+                                                       const bf16* __restrict__ x, int T, int E,
+                                                       int d, int slice, float* __restrict__ part) {
+    __shared__ float sg[WR_CHUNK][WR_EG];
     pdl_wait();
     pdl_trigger();
-    const int e = blockIdx.z;
-    int r0 = 0, r1 = rows;
-    if (seg_len > 0) {  // slice z of `rows` rows (partial sums)
-        r0 = min(e * seg_len, rows);
-        r1 = min(r0 + seg_len, rows);
-    } else if (offsets != nullptr) {
-        r1 = (int)min((int64_t)max(__ldg(offsets + e + 1), 0), rows_cap);
-        r0 = min(max(__ldg(offsets + e), 0), r1);
-    }
-    const int m0 = blockIdx.y * WG_BM, n0 = blockIdx.x * WG_BN;
-    const int tid = threadIdx.x, tx = tid % 16, ty = tid / 16;
-    // loader: 16 rows x 64 columns per operand, 4 consecutive columns a thread
-    const int lr = tid / 16, lc = (tid % 16) * 4;
-    float av[4], bv[4];
-    auto load = [&](int rb) {
-        const int r = rb + lr;
-        const bool in = r < r1;
+    const int j = blockIdx.x * blockDim.x + threadIdx.x;
+    const int z = blockIdx.y;
+    const int t0 = min(z * slice, T), t1 = min(t0 + slice, T);
+    for (int e0 = 0; e0 < E; e0 += WR_EG) {
+        float acc[WR_EG];
 #pragma unroll
-        for (int q = 0; q < 4; ++q) {
-            av[q] = (in && m0 + lc + q < M) ? to_f32(A[(size_t)r * M + m0 + lc + q]) : 0.f;
-            bv[q] = (in && n0 + lc + q < N) ? to_f32(B[(size_t)r * N + n0 + lc + q]) : 0.f;
+        for (int c = 0; c < WR_EG; ++c) acc[c] = 0.f;
+        for (int tb = t0; tb < t1; tb += WR_CHUNK) {
+            __syncthreads();
+            for (int i = threadIdx.x; i < WR_CHUNK * WR_EG; i += blockDim.x) {
+                const int r = i / WR_EG, c = i % WR_EG;
+                sg[r][c] = (tb + r < t1 && e0 + c < E) ? __ldg(dg + (size_t)(tb + r) * E + e0 + c)
+                                                       : 0.f;
+            }
+            __syncthreads();
+            if (j < d) {
+                const int rows = min(WR_CHUNK, t1 - tb);
+                for (int r = 0; r < rows; ++r) {
+                    const float xv = __bfloat162float(x[(size_t)(tb + r) * d + j]);
+#pragma unroll
+                    for (int c = 0; c < WR_EG; ++c) acc[c] = fmaf(sg[r][c], xv, acc[c]);
+                }
+            }
         }
-    };
-    float acc[4][4] = {};
-    if (r0 < r1) load(r0);
-    for (int rb = r0; rb < r1; rb += WG_BK) {
-        __syncthreads();
-#pragma unroll
-        for (int q = 0; q < 4; ++q) {
-            As[lr][lc + q] = av[q];
-            Bs[lr][lc + q] = bv[q];
-        }
-        __syncthreads();
-        if (rb + WG_BK < r1) load(rb + WG_BK);
-#pragma unroll
-        for (int kq = 0; kq < WG_BK; ++kq) {
-            const float4 a4 = *reinterpret_cast<const float4*>(&As[kq][ty * 4]);
-            const float4 b4 = *reinterpret_cast<const float4*>(&Bs[kq][tx * 4]);
-            const float ar[4] = {a4.x, a4.y, a4.z, a4.w};
-            const float br[4] = {b4.x, b4.y, b4.z, b4.w};
-#pragma unroll
-            for (int i = 0; i < 4; ++i)
-#pragma unroll
-                for (int j = 0; j < 4; ++j) acc[i][j] = fmaf(ar[i], br[j], acc[i][j]);
-        }
-    }
-    float* Ce = Cout + (size_t)e * M * N;
-#pragma unroll
-    for (int i = 0; i < 4; ++i) {
-        const int m = m0 + ty * 4 + i;
-        if (m >= M) continue;
-#pragma unroll
-        for (int j = 0; j < 4; ++j) {
-            const int n = n0 + tx * 4 + j;
-            if (n < N) Ce[(size_t)m * N + n] = acc[i][j];
-        }
+        if (j < d)
+            for (int c = 0; c < WR_EG && e0 + c < E; ++c)
+                part[((size_t)z * E + e0 + c) * d + j] = acc[c];
     }
 }
 
@@ -522,10 +509,11 @@ struct BwdLayout {
     int wr_slices;     // row slices of the router-weight gradient
 };
 
-// Row slices of dW_r = dg^T x (partial sums, then a fixed-order sum).
+// Row slices of dW_r = dg^T x (partial sums, then a fixed-order sum): 64
+// rows, or T / 256 for the largest batches (at most 256 slices).
 int wr_slice_rows(int T) {
-    const int s = (T + 63) / 64;
-    return s > 256 ? s : 256;
+    const int s = (T + 255) / 256;
+    return s > 64 ? s : 64;
 }
 
 size_t align256(size_t v) { return (v + 255) & ~size_t(255); }
@@ -684,11 +672,10 @@ moe_status moe_backward(const moe_config* cfg, const void* x, const float* W_r,
     const dim3 tgrid_d((unsigned)(kc / TP), (unsigned)((d + TP - 1) / TP));
     const dim3 tgrid_f((unsigned)(kc / TP), (unsigned)((F + TP - 1) / TP));
     if (e == cudaSuccess)  // dW_r = dg^T x: row-slice partials, then their sum
-        e = launch_kernel(wgrad_kernel<float, bf16>,
-                          dim3((d + 63) / 64, (E + 63) / 64, Bw.wr_slices), dim3(256), 0, s, 1,
-                          false, (const float*)dg, reinterpret_cast<const bf16*>(x),
-                          (const int32_t*)nullptr, T, (int64_t)T, E, d, wr_slice_rows(T),
-                          at<float>(ws, Bw.parts));
+        e = launch_kernel(E <= 8 ? wr_grad_kernel<8> : wr_grad_kernel<32>,
+                          dim3((d + 255) / 256, Bw.wr_slices), dim3(256), 0, s, 1, false,
+                          (const float*)dg, reinterpret_cast<const bf16*>(x), T, E, d,
+                          wr_slice_rows(T), at<float>(ws, Bw.parts));
     if (e == cudaSuccess)
         e = launch_kernel(sum_parts_kernel, dim3(grid_for((int64_t)E * d, 256)), dim3(256), 0, s,
                           1, false, (const float*)at<float>(ws, Bw.parts), Bw.wr_slices,
