@@ -7,13 +7,15 @@
 //
 // Steps (one stream):
 //   recompute   router (logits kept) + dispatch, GEMM1 without GELU -> U,
-//               H = GELU(U), GEMM2 -> y_perm = w * o
+//               H = GELU(U) (with H transposed per segment for dW2), GEMM2 ->
+//               y_perm = w * o
 //   router      one warp per token: s_j = <dy_t, y_perm[slot_j]>, the logit
 //               gradient dg (softmax / renormalisation, auxiliary loss,
 //               z-loss) and dY_perm[slot_j] = w_j dy_t
 //   dx path     W2, W1 transposed per expert; dH = dY_perm W2_e (the
 //               forward's tcgen05 GEMM with W2^T as its weight), dU = dH *
-//               GELU'(U), dX_perm = dU W1_e (W1^T); dx = sum over the
+//               GELU'(U) (with dU transposed per segment for dW1),
+//               dX_perm = dU W1_e (W1^T); dx = sum over the
 //               token's slots of dX_perm + dg W_r
 //   weights     dW2_e = dY_perm_e^T H_e and dW1_e = dU_e^T X_perm_e on the
 //               CTA-pair tcgen05 kernel in its segment-reduction mode (both
@@ -86,49 +88,6 @@ __device__ __forceinline__ uint4 pack8(const float* f) {
 #pragma unroll
     for (int i = 0; i < 4; ++i) h[i] = __floats2bfloat162_rn(f[2 * i], f[2 * i + 1]);
     return q;
-}
-
-// H = GELU(U) over the kept rows (offsets[E] rows of F columns), 8 a thread.
-__global__ void __launch_bounds__(256) gelu_rows_kernel(const bf16* __restrict__ U,
-                                                         const int32_t* __restrict__ offsets,
-                                                         int E, int F, int64_t rows_cap,
-                                                         bf16* __restrict__ H) {
-    pdl_wait();
-    pdl_trigger();
-    const int64_t rows = min((int64_t)max(__ldg(offsets + E), 0), rows_cap);
-    const int64_t n8 = rows * F / 8;
-    for (int64_t i = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; i < n8;
-         i += (int64_t)gridDim.x * blockDim.x) {
-        float f[8];
-        unpack8(__ldg(reinterpret_cast<const uint4*>(U) + i), f);
-#pragma unroll
-        for (int j = 0; j < 8; j += 2) {  // the forward epilogue's GELU
-            const float2 g = gelu2_as7126(make_float2(f[j], f[j + 1]));
-            f[j] = g.x;
-            f[j + 1] = g.y;
-        }
-        reinterpret_cast<uint4*>(H)[i] = pack8(f);
-    }
-}
-
-// dU = dH * GELU'(U) in place over dH.
-__global__ void __launch_bounds__(256) gelu_grad_rows_kernel(const bf16* __restrict__ U,
-                                                              const int32_t* __restrict__ offsets,
-                                                              int E, int F, int64_t rows_cap,
-                                                              bf16* __restrict__ dH) {
-    pdl_wait();
-    pdl_trigger();
-    const int64_t rows = min((int64_t)max(__ldg(offsets + E), 0), rows_cap);
-    const int64_t n8 = rows * F / 8;
-    for (int64_t i = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; i < n8;
-         i += (int64_t)gridDim.x * blockDim.x) {
-        float u[8], g[8];
-        unpack8(__ldg(reinterpret_cast<const uint4*>(U) + i), u);
-        unpack8(reinterpret_cast<const uint4*>(dH)[i], g);
-#pragma unroll
-        for (int j = 0; j < 8; ++j) g[j] *= gelu_grad(u[j]);
-        reinterpret_cast<uint4*>(dH)[i] = pack8(g);
-    }
 }
 
 // One warp per token: the slot scores s_j, dY_perm rows and the logit
@@ -449,11 +408,20 @@ __global__ void __launch_bounds__(32) seg_koff_kernel(const int32_t* __restrict_
     if (lane == 0) koff[E] = carry;
 }
 
-// Every expert segment of A [rows][M] transposed into out [M][kcols]:
-// out[m][koff[e] + j] = A[offsets[e] + j][m] for j < the segment's length,
-// 0 for the rest of its padded window.  64 x 64 tiles (a tile never spans
-// two windows: they start at multiples of kSegPad).
+// Every expert segment of a [rows][M] matrix transposed into out [M][kcols]:
+// out[m][koff[e] + j] = V[offsets[e] + j][m] for j < the segment's length,
+// 0 for the rest of its padded window, where V is
+//   kSegCopy      A itself;
+//   kSegGelu      GELU(A) (A = U), also written row-major to rowout (H);
+//   kSegGeluGrad  rowout * GELU'(A) (A = U, rowout = dH, overwritten in
+//                 place with dU).
+// 64 x 64 tiles (a tile never spans two windows: they start at multiples of
+// kSegPad); every kept row is covered by exactly one window position.
+enum SegOp { kSegCopy = 0, kSegGelu = 1, kSegGeluGrad = 2 };
+
+template <int OP>
 __global__ void __launch_bounds__(256) seg_transpose_kernel(const bf16* __restrict__ A,
+                                                             bf16* __restrict__ rowout,
                                                              const int32_t* __restrict__ offsets,
                                                              const int32_t* __restrict__ koff,
                                                              int E, int M, int64_t rows_cap,
@@ -471,11 +439,40 @@ __global__ void __launch_bounds__(256) seg_transpose_kernel(const bf16* __restri
     const int r1 = (int)min((int64_t)max(__ldg(offsets + lo + 1), 0), rows_cap);
     const int r0 = min(max(__ldg(offsets + lo), 0), r1);
     const int j0 = c0 - __ldg(koff + lo);
-    // tile[i][.] = source row r0 + j0 + i (zeros past the segment), columns m0 ..
-    tile_load(tile, [&](int i) -> const bf16* {
+    const int t = threadIdx.x;
+#pragma unroll
+    for (int h = 0; h < 2; ++h) {  // tile[i][.] = V row r0 + j0 + i (zeros past the segment)
+        const int i = t / 8 + 32 * h, cg = (t % 8) * 8;
         const int r = r0 + j0 + i;
-        return r < r1 ? A + (size_t)r * M : nullptr;
-    }, m0, M);
+        uint4 q = make_uint4(0, 0, 0, 0);
+        if (r < r1 && m0 + cg < M) {
+            const size_t at_ = (size_t)r * M + m0 + cg;
+            q = __ldg(reinterpret_cast<const uint4*>(A + at_));
+            if (OP != kSegCopy) {
+                float f[8];
+                unpack8(q, f);
+                if (OP == kSegGelu) {
+#pragma unroll
+                    for (int j = 0; j < 8; j += 2) {  // the forward epilogue's GELU
+                        const float2 g = gelu2_as7126(make_float2(f[j], f[j + 1]));
+                        f[j] = g.x;
+                        f[j + 1] = g.y;
+                    }
+                } else {
+                    float g[8];
+                    unpack8(*reinterpret_cast<const uint4*>(rowout + at_), g);
+#pragma unroll
+                    for (int j = 0; j < 8; ++j) f[j] = g[j] * gelu_grad(f[j]);
+                }
+                q = pack8(f);
+                *reinterpret_cast<uint4*>(rowout + at_) = q;
+            }
+        }
+        const uint32_t* w = reinterpret_cast<const uint32_t*>(&q);
+        uint32_t* dst = reinterpret_cast<uint32_t*>(&tile[i][cg]);
+#pragma unroll
+        for (int kq = 0; kq < 4; ++kq) dst[kq] = w[kq];
+    }
     __syncthreads();
     tile_store(tile, [&](int j) -> bf16* {
         return m0 + j < M ? out + (size_t)(m0 + j) * kcols + c0 : nullptr;
@@ -626,12 +623,22 @@ moe_status moe_backward(const moe_config* cfg, const void* x, const float* W_r,
         e = launch_scan_permute(c, x, idx, w, L.route.tokens * k, L.route.blocks, offsets, slot_of,
                                 perm_token, perm_w, x_perm, ws, L,
                                 route_loss_args(c, ws, L, nullptr, nullptr, nullptr), s);
+    int32_t* koff = at<int32_t>(ws, Bw.koff);
+    bf16* TTd = at<bf16>(ws, Bw.tt_d);  // segment-transposed [d][kcols] operands
+    bf16* TTf = at<bf16>(ws, Bw.tt_f);  // segment-transposed [d_ff][kcols] operands
+    const int64_t kc = Bw.kcols;
+    const dim3 tgrid_d((unsigned)(kc / TP), (unsigned)((d + TP - 1) / TP));
+    const dim3 tgrid_f((unsigned)(kc / TP), (unsigned)((F + TP - 1) / TP));
+    if (e == cudaSuccess)
+        e = launch_kernel(seg_koff_kernel, dim3(1), dim3(32), 0, s, 1, false,
+                          (const int32_t*)offsets, E, rows, koff);
     if (e == cudaSuccess)
         e = launch_grouped_gemm_tc(c, true, false, x_perm, rows, offsets, W1, b1, nullptr, U, rows,
                                    F, d, hdr, s);
-    if (e == cudaSuccess)
-        e = launch_kernel(gelu_rows_kernel, dim3(grid_for(rows * F / 8, 256)), dim3(256), 0, s, 1,
-                          false, (const bf16*)U, (const int32_t*)offsets, E, F, rows, H);
+    if (e == cudaSuccess)  // H = GELU(U) row-major, and H^T for dW2
+        e = launch_kernel(seg_transpose_kernel<kSegGelu>, tgrid_f, dim3(256), 0, s, 1, false,
+                          (const bf16*)U, H, (const int32_t*)offsets, (const int32_t*)koff, E, F,
+                          rows, kc, TTf);
     if (e == cudaSuccess)
         e = launch_grouped_gemm_tc(c, false, false, H, rows, offsets, W2, b2, perm_w, y_perm, rows,
                                    d, F, hdr, s);
@@ -642,6 +649,16 @@ moe_status moe_backward(const moe_config* cfg, const void* x, const float* W_r,
                           (const int32_t*)slot_of, (const float*)y_perm,
                           reinterpret_cast<const bf16*>(dy), (const int32_t*)at<int32_t>(ws, L.top1),
                           T, E, k, d, rows, c.renormalize, aux_grad, z_grad, dg, dYp);
+    // ---- dW2_e = dY_perm_e^T H_e, db2
+    if (e == cudaSuccess)
+        e = launch_kernel(seg_transpose_kernel<kSegCopy>, tgrid_d, dim3(256), 0, s, 1, false,
+                          (const bf16*)dYp, (bf16*)nullptr, (const int32_t*)offsets,
+                          (const int32_t*)koff, E, d, rows, kc, TTd);
+    if (e == cudaSuccess)
+        e = launch_segment_reduction_tc(E, offsets, rows, koff, TTd, d, TTf, F, kc, dW2, hdr, s);
+    if (e == cudaSuccess)
+        e = launch_kernel(colsum_kernel, dim3((d + 63) / 64, E), dim3(256), 0, s, 1, false,
+                          (const bf16*)dYp, (const int32_t*)offsets, rows, d, db2);
     // ---- dx path: transposed weights, dH, GELU', dX_perm, dx
     if (e == cudaSuccess)
         e = launch_kernel(transpose_kernel, dim3((F + TP - 1) / TP, (d + TP - 1) / TP, E),
@@ -652,9 +669,10 @@ moe_status moe_backward(const moe_config* cfg, const void* x, const float* W_r,
     if (e == cudaSuccess)
         e = launch_grouped_gemm_tc(c, true, false, dYp, rows, offsets, W2T, nullptr, nullptr, dH,
                                    rows, F, d, hdr, s);
-    if (e == cudaSuccess)
-        e = launch_kernel(gelu_grad_rows_kernel, dim3(grid_for(rows * F / 8, 256)), dim3(256), 0,
-                          s, 1, false, (const bf16*)U, (const int32_t*)offsets, E, F, rows, dH);
+    if (e == cudaSuccess)  // dU = dH * GELU'(U) in place, and dU^T for dW1
+        e = launch_kernel(seg_transpose_kernel<kSegGeluGrad>, tgrid_f, dim3(256), 0, s, 1, false,
+                          (const bf16*)U, dH, (const int32_t*)offsets, (const int32_t*)koff, E, F,
+                          rows, kc, TTf);
     if (e == cudaSuccess)
         e = launch_grouped_gemm_tc(c, false, false, dH, rows, offsets, W1T, nullptr, nullptr,
                                    y_perm, rows, d, F, hdr, s);
@@ -664,14 +682,18 @@ moe_status moe_backward(const moe_config* cfg, const void* x, const float* W_r,
                           (const float*)y_perm, (const int32_t*)slot_of, (const float*)dg, W_r, T,
                           k, E, d, rows, reinterpret_cast<bf16*>(dx));
     }
-    // ---- weight gradients
-    int32_t* koff = at<int32_t>(ws, Bw.koff);
-    bf16* TTd = at<bf16>(ws, Bw.tt_d);
-    bf16* TTf = at<bf16>(ws, Bw.tt_f);
-    const int64_t kc = Bw.kcols;
-    const dim3 tgrid_d((unsigned)(kc / TP), (unsigned)((d + TP - 1) / TP));
-    const dim3 tgrid_f((unsigned)(kc / TP), (unsigned)((F + TP - 1) / TP));
-    if (e == cudaSuccess)  // dW_r = dg^T x: row-slice partials, then their sum
+    // ---- dW1_e = dU_e^T X_perm_e, db1
+    if (e == cudaSuccess)
+        e = launch_kernel(seg_transpose_kernel<kSegCopy>, tgrid_d, dim3(256), 0, s, 1, false,
+                          (const bf16*)x_perm, (bf16*)nullptr, (const int32_t*)offsets,
+                          (const int32_t*)koff, E, d, rows, kc, TTd);
+    if (e == cudaSuccess)
+        e = launch_segment_reduction_tc(E, offsets, rows, koff, TTf, F, TTd, d, kc, dW1, hdr, s);
+    if (e == cudaSuccess)
+        e = launch_kernel(colsum_kernel, dim3((F + 63) / 64, E), dim3(256), 0, s, 1, false,
+                          (const bf16*)dH, (const int32_t*)offsets, rows, F, db1);
+    // ---- dW_r = dg^T x: row-slice partials, then their sum
+    if (e == cudaSuccess)
         e = launch_kernel(E <= 8 ? wr_grad_kernel<8> : wr_grad_kernel<32>,
                           dim3((d + 255) / 256, Bw.wr_slices), dim3(256), 0, s, 1, false,
                           (const float*)dg, reinterpret_cast<const bf16*>(x), T, E, d,
@@ -680,37 +702,6 @@ moe_status moe_backward(const moe_config* cfg, const void* x, const float* W_r,
         e = launch_kernel(sum_parts_kernel, dim3(grid_for((int64_t)E * d, 256)), dim3(256), 0, s,
                           1, false, (const float*)at<float>(ws, Bw.parts), Bw.wr_slices,
                           (int64_t)E * d, dW_r);
-    if (e == cudaSuccess)
-        e = launch_kernel(seg_koff_kernel, dim3(1), dim3(32), 0, s, 1, false,
-                          (const int32_t*)offsets, E, rows, koff);
-    // dW2_e = dY_perm_e^T H_e: both operands segment-transposed
-    if (e == cudaSuccess)
-        e = launch_kernel(seg_transpose_kernel, tgrid_d, dim3(256), 0, s, 1, false,
-                          (const bf16*)dYp, (const int32_t*)offsets, (const int32_t*)koff, E, d,
-                          rows, kc, TTd);
-    if (e == cudaSuccess)
-        e = launch_kernel(seg_transpose_kernel, tgrid_f, dim3(256), 0, s, 1, false,
-                          (const bf16*)H, (const int32_t*)offsets, (const int32_t*)koff, E, F,
-                          rows, kc, TTf);
-    if (e == cudaSuccess)
-        e = launch_segment_reduction_tc(E, offsets, rows, koff, TTd, d, TTf, F, kc, dW2, hdr, s);
-    // dW1_e = dU_e^T X_perm_e
-    if (e == cudaSuccess)
-        e = launch_kernel(seg_transpose_kernel, tgrid_d, dim3(256), 0, s, 1, false,
-                          (const bf16*)x_perm, (const int32_t*)offsets, (const int32_t*)koff, E,
-                          d, rows, kc, TTd);
-    if (e == cudaSuccess)
-        e = launch_kernel(seg_transpose_kernel, tgrid_f, dim3(256), 0, s, 1, false,
-                          (const bf16*)dH, (const int32_t*)offsets, (const int32_t*)koff, E, F,
-                          rows, kc, TTf);
-    if (e == cudaSuccess)
-        e = launch_segment_reduction_tc(E, offsets, rows, koff, TTf, F, TTd, d, kc, dW1, hdr, s);
-    if (e == cudaSuccess)
-        e = launch_kernel(colsum_kernel, dim3((d + 63) / 64, E), dim3(256), 0, s, 1, false,
-                          (const bf16*)dYp, (const int32_t*)offsets, rows, d, db2);
-    if (e == cudaSuccess)
-        e = launch_kernel(colsum_kernel, dim3((F + 63) / 64, E), dim3(256), 0, s, 1, false,
-                          (const bf16*)dH, (const int32_t*)offsets, rows, F, db1);
     return e == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;
 }
 
