@@ -178,6 +178,25 @@ class ClockSampler:
                 "source": self.mode}
 
 
+def slowest_rank_ms(ms: float, world: int, device=None) -> float:
+    """The job's time: the largest of the ranks' timings (an all-reduce MAX
+    over the process group when there is more than one rank; NCCL on the GPU
+    box, gloo in the CPU tests)."""
+    if world <= 1:
+        return ms
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([ms], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def job_tokens_per_s(world: int, tokens: int, steps: int, total_ms: float) -> float:
+    """Whole-job throughput: every rank's tokens over the slowest rank's time
+    (each rank runs an independent replica on a batch of `tokens`)."""
+    return world * tokens * steps / (total_ms * 1e-3)
+
+
 def dist_setup():
     world = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))
@@ -389,13 +408,9 @@ def bench_ours(args, wl):
     ffn_ms = [e[1].elapsed_time(e[2]) for e in evs]
     route_ms = [e[0].elapsed_time(e[1]) for e in evs]
     comb_ms = [e[2].elapsed_time(e[3]) for e in evs]
-    total_ms = sum(step_ms)
-    if world > 1:
-        t = torch.tensor([total_ms], dtype=torch.float64, device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        total_ms = float(t.item())
+    total_ms = slowest_rank_ms(sum(step_ms), world, dev)
     ms_per_step = total_ms / args.steps
-    value = world * T * args.steps / (total_ms * 1e-3)
+    value = job_tokens_per_s(world, T, args.steps, total_ms)
 
     # end to end through the host-buffer executor of the C ABI (moe_pipeline_*):
     # per step the pinned host batch is copied in, the layer runs, y and the
@@ -430,13 +445,9 @@ def bench_ours(args, wl):
     pipe.join()
     e1.record(stream)
     e1.synchronize()
-    e2e_ms = e0.elapsed_time(e1)
+    e2e_ms = slowest_rank_ms(e0.elapsed_time(e1), world, dev)
     pipe.close()
-    if world > 1:
-        t = torch.tensor([e2e_ms], dtype=torch.float64, device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        e2e_ms = float(t.item())
-    e2e_value = world * T * args.steps / (e2e_ms * 1e-3)
+    e2e_value = job_tokens_per_s(world, T, args.steps, e2e_ms)
 
     pk, pk_kind = peaks()
     clocks = sampler.summary()
@@ -561,11 +572,7 @@ def bench_backward(args, wl):
             graph.replay()
             ev[s_][1].record(stream)
         torch.cuda.synchronize(dev)
-    total_ms = sum(e0.elapsed_time(e1) for e0, e1 in ev)
-    if world > 1:
-        t = torch.tensor([total_ms], dtype=torch.float64, device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        total_ms = float(t.item())
+    total_ms = slowest_rank_ms(sum(e0.elapsed_time(e1) for e0, e1 in ev), world, dev)
     ms = total_ms / args.steps
     cnt = counts.cpu().numpy()
     kept = int(np.minimum(cnt, wl.capacity).sum()) if wl.capacity is not None else int(cnt.sum())
@@ -575,7 +582,7 @@ def bench_backward(args, wl):
     clocks = sampler.summary()
     achieved = flops / (ms * 1e-3) / 1e12
     line = {"metric": "MoE-layer backward tokens/s (gradients of x, W_r, W1, b1, W2, b2)",
-            "value": world * T / (ms * 1e-3), "unit": "tokens/s", "n_gpus": world,
+            "value": job_tokens_per_s(world, T, 1, ms), "unit": "tokens/s", "n_gpus": world,
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms,
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
             "data": "synthetic",
