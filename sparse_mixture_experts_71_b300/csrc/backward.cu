@@ -241,7 +241,6 @@ __global__ void __launch_bounds__(256) transpose_kernel(const bf16* __restrict__
     }
 }
 
-__device__ __forceinline__ void store4(float* p, float4 v) { *reinterpret_cast<float4*>(p) = v; }
 __device__ __forceinline__ void store4(bf16* p, float4 v) {
     __nv_bfloat162 lo = __floats2bfloat162_rn(v.x, v.y), hi = __floats2bfloat162_rn(v.z, v.w);
     uint2 u;
