@@ -213,12 +213,21 @@ __device__ __forceinline__ void tile_store(bf16 (*tile)[TP_LD], RowPtr dst) {
     }
 }
 
-// out[e][c][r] = in[e][r][c] for R x C bf16 matrices (R, C multiples of 8).
+// out[e][c][r] = in[e][r][c] for R x C bf16 matrices (R, C multiples of 8);
+// an expert whose segment is empty is skipped (no GEMM reads its copy).
 __global__ void __launch_bounds__(256) transpose_kernel(const bf16* __restrict__ in, int R, int C,
+                                                        const int32_t* __restrict__ offsets,
+                                                        int64_t rows_cap,
                                                         bf16* __restrict__ out) {
     __shared__ __align__(16) bf16 tile[TP][TP_LD];
     pdl_wait();
     pdl_trigger();
+    {
+        const int e = blockIdx.z;
+        const int64_t r1 = min((int64_t)max(__ldg(offsets + e + 1), 0), rows_cap);
+        const int64_t r0 = min((int64_t)max(__ldg(offsets + e), 0), r1);
+        if (r1 == r0) return;
+    }
     const size_t base = (size_t)blockIdx.z * R * C;
     const int c0 = blockIdx.x * TP, r0 = blockIdx.y * TP;
     tile_load(tile, [&](int i) -> const bf16* {
@@ -661,10 +670,12 @@ moe_status moe_backward(const moe_config* cfg, const void* x, const float* W_r,
     // ---- dx path: transposed weights, dH, GELU', dX_perm, dx
     if (e == cudaSuccess)
         e = launch_kernel(transpose_kernel, dim3((F + TP - 1) / TP, (d + TP - 1) / TP, E),
-                          dim3(256), 0, s, 1, false, reinterpret_cast<const bf16*>(W2), d, F, W2T);
+                          dim3(256), 0, s, 1, false, reinterpret_cast<const bf16*>(W2), d, F,
+                          (const int32_t*)offsets, rows, W2T);
     if (e == cudaSuccess)
         e = launch_kernel(transpose_kernel, dim3((d + TP - 1) / TP, (F + TP - 1) / TP, E),
-                          dim3(256), 0, s, 1, false, reinterpret_cast<const bf16*>(W1), F, d, W1T);
+                          dim3(256), 0, s, 1, false, reinterpret_cast<const bf16*>(W1), F, d,
+                          (const int32_t*)offsets, rows, W1T);
     if (e == cudaSuccess)
         e = launch_grouped_gemm_tc(c, true, false, dYp, rows, offsets, W2T, nullptr, nullptr, dH,
                                    rows, F, d, hdr, s);
