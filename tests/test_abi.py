@@ -190,3 +190,31 @@ def test_backward_host_side():
                             n, None) == 1  # no dy
     assert lib.moe_backward(cr, FAKE + 8, *args[1:], ctypes.c_float(0), ctypes.c_float(0), *outs,
                             FAKE, n, None) == 2
+
+
+@pytest.mark.parametrize("header", sorted(h for h in os.listdir(os.path.join(ROOT, "include"))
+                                          if h.endswith(".h")))
+def test_header_is_plain_c(header, tmp_path):
+    """Each public header compiles on its own as C99 (a C ABI, no C++ or torch
+    types), warnings as errors."""
+    import shutil
+    import subprocess
+    gcc = shutil.which("gcc")
+    if gcc is None:
+        pytest.skip("no C compiler")
+    src = tmp_path / "t.c"
+    src.write_text(f'#include "{header}"\nint main(void) {{ return 0; }}\n')
+    r = subprocess.run([gcc, "-std=c99", "-Wall", "-Wextra", "-pedantic", "-Werror",
+                        "-fsyntax-only", "-I", os.path.join(ROOT, "include"), str(src)],
+                       capture_output=True, text=True)
+    assert r.returncode == 0, r.stderr
+
+
+def test_product_path_never_imports_the_oracle():
+    """The oracle is test infrastructure: nothing in the package imports it."""
+    pkg = os.path.join(ROOT, "sparse_mixture_experts_71_b300")
+    for dirpath, _, files in os.walk(pkg):
+        for fn in files:
+            if fn.endswith(".py"):
+                src = open(os.path.join(dirpath, fn)).read()
+                assert not re.search(r"^\s*(from|import)\s+oracle\b", src, re.M), fn
