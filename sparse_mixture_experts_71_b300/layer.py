@@ -84,6 +84,27 @@ class MoELayer:
 
     __call__ = forward
 
+    def backward(self, x, dy, aux_grad: float = 0.0, z_grad: float = 0.0, stream=None) -> dict:
+        """Gradients of <dy, y> + aux_grad * aux + z_grad * z_loss for the batch
+        x (moe_backward; bf16 token-choice layers that drop on overflow):
+        {"dx", "dW_r", "dW1", "db1", "dW2", "db2"}, dx in the layer dtype, the
+        weight gradients fp32.  The routing decisions are held fixed."""
+        T = x.shape[0]
+        cfg = self.config(T)
+        key = ("backward", T)
+        if key not in self._ws:
+            self._ws[key] = B.backward_workspace(cfg, device=self.W1.device)
+        f32 = dict(dtype=torch.float32, device=self.W1.device)
+        g = dict(dx=torch.empty_like(x), dW_r=torch.empty((self.E, self.d), **f32),
+                 dW1=torch.empty((self.E, self.d_ff, self.d), **f32),
+                 db1=torch.empty((self.E, self.d_ff), **f32),
+                 dW2=torch.empty((self.E, self.d, self.d_ff), **f32),
+                 db2=torch.empty((self.E, self.d), **f32))
+        B.backward(cfg, x, self.W_r, self.W1, self.b1, self.W2, self.b2, dy, g["dx"], g["dW_r"],
+                   g["dW1"], g["db1"], g["dW2"], g["db2"], self._ws[key],
+                   logit_bias=self.logit_bias, aux_grad=aux_grad, z_grad=z_grad, stream=stream)
+        return g
+
     def host_pipeline(self, T: int, depth: int = 2, stream=None) -> B.Pipeline:
         """An executor for batches of T tokens in host memory (moe_pipeline_*):
         ``submit(x_host, y_host, aux_host)`` per batch, ``join()`` to make the

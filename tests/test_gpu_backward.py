@@ -92,3 +92,24 @@ def test_backward_empty_batch_is_zero():
     torch.cuda.synchronize()
     assert all(not o.any() for o in outs)
     assert wl.T == 0
+
+
+def test_layer_backward_matches_the_c_call():
+    """MoELayer.backward (the Python layer API) gives the C call's bits."""
+    from sparse_mixture_experts_71_b300.layer import MoELayer
+    wl = I.Workload("bwd-layer", 200, 128, 256, 8, 2)
+    inp = I.make_inputs(wl, seed=43)
+    run = LibRun(wl, inp)
+    D = run.dev
+    layer = MoELayer(D["W_r"], D["W1"], D["b1"], D["W2"], D["b2"], k=2,
+                     logit_bias=D["logit_bias"])
+    dy = torch.from_numpy(I.router_noise(200, 128, 1.0, seed=44)).to(torch.bfloat16).cuda()
+    g = layer.backward(D["x"], dy, aux_grad=0.2, z_grad=0.05)
+    ws = B.backward_workspace(run.cfg)
+    want = {n: torch.empty_like(v) for n, v in g.items()}
+    B.backward(run.cfg, D["x"], D["W_r"], D["W1"], D["b1"], D["W2"], D["b2"], dy, want["dx"],
+               want["dW_r"], want["dW1"], want["db1"], want["dW2"], want["db2"], ws,
+               logit_bias=D["logit_bias"], aux_grad=0.2, z_grad=0.05)
+    torch.cuda.synchronize()
+    for n in g:
+        assert torch.equal(g[n], want[n]), n
