@@ -218,3 +218,43 @@ def test_product_path_never_imports_the_oracle():
             if fn.endswith(".py"):
                 src = open(os.path.join(dirpath, fn)).read()
                 assert not re.search(r"^\s*(from|import)\s+oracle\b", src, re.M), fn
+
+
+C_PROGRAM = r"""
+#include <stdio.h>
+#include "moe.h"
+#include "moe_pipeline.h"
+#include "moe_backward.h"
+int main(void) {
+    moe_config c = {4096, 1024, 4096, 8, 2, MOE_BF16, -1, 1, 0, MOE_TOKEN_CHOICE, MOE_DROP};
+    size_t ws = moe_workspace_size(&c);
+    size_t wb = moe_backward_workspace_size(&c);
+    size_t wp = moe_pipeline_workspace_size(&c, 2);
+    c.routing = MOE_EXPERT_CHOICE;
+    int C = moe_expert_choice_capacity(&c);
+    moe_status bad = moe_forward(&c, 0, 0, 0, 0, 0, 0, 0, 0, 0, 0, 0, 0, 0, 0, 0, 0);
+    printf("%zu %zu %zu %d %d %s\n", ws, wb, wp, C, (int)bad, moe_status_string(bad));
+    return (ws > 0 && wb > ws && wp > ws && C == 1024 && bad == MOE_ERR_INVALID_ARG) ? 0 : 1;
+}
+"""
+
+
+def test_c_program_links_and_calls_the_library(tmp_path):
+    """A plain C99 program builds against the headers, links libmoe.so and
+    calls its host-side entry points (no GPU needed for these)."""
+    import shutil
+    import subprocess
+    gcc = shutil.which("gcc")
+    if gcc is None:
+        pytest.skip("no C compiler")
+    B.load()  # the library is built
+    libdir = os.path.join(ROOT, "sparse_mixture_experts_71_b300")
+    src, exe = tmp_path / "t.c", tmp_path / "t"
+    src.write_text(C_PROGRAM)
+    r = subprocess.run([gcc, "-std=c99", "-Wall", "-Werror", "-I", os.path.join(ROOT, "include"),
+                        str(src), "-L", libdir, "-lmoe", f"-Wl,-rpath,{libdir}", "-o", str(exe)],
+                       capture_output=True, text=True)
+    assert r.returncode == 0, r.stderr
+    r = subprocess.run([str(exe)], capture_output=True, text=True, timeout=60)
+    assert r.returncode == 0, r.stdout + r.stderr
+    assert r.stdout.split()[3] == "1024"
