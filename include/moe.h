@@ -85,9 +85,9 @@ typedef enum moe_routing { MOE_TOKEN_CHOICE = 0, MOE_EXPERT_CHOICE = 1 } moe_rou
 typedef enum moe_overflow { MOE_DROP = 0, MOE_REROUTE = 1 } moe_overflow;
 
 /*
- * Rerouting on overflow ("The central problem: load balancing": overflow
- * tokens are dropped or rerouted; passed to the next-best expert),
- * cfg->overflow = MOE_REROUTE, token choice only, n_shared = 0: after the
+ * Rerouting on overflow ("The central problem: load balancing" and the
+ * inferensys glossary's expert capacity: an overflowing token may go to its
+ * next-ranked expert instead of being dropped), cfg->overflow = MOE_REROUTE, token choice only, n_shared = 0: after the
  * capacity drop (as above), the r-th dropped slot of a token (r = 0, 1, ...)
  * is offered once to the token's (k + r)-th ranked expert, the best one it
  * does not use; offers are taken in (token, slot) order and an expert
@@ -105,7 +105,7 @@ typedef enum moe_overflow { MOE_DROP = 0, MOE_REROUTE = 1 } moe_overflow;
  */
 
 /*
- * Shared experts ("Design variations": one or more experts always active):
+ * Shared experts ("Design variations": experts that every token uses):
  * with n_shared > 0, experts 0 .. n_shared-1 of the E in W1, b1, W2, b2 are
  * applied to every token with weight 1 and are never capped; the router
  * covers the other E - n_shared experts (W_r, logit_bias, logit_noise,
@@ -119,8 +119,9 @@ typedef enum moe_overflow { MOE_DROP = 0, MOE_REROUTE = 1 } moe_overflow;
  */
 
 /*
- * Expert-choice routing ("Design variations": experts choose their top
- * tokens, guaranteeing balance), cfg->routing = MOE_EXPERT_CHOICE: the
+ * Expert-choice routing ("Design variations": the experts select the tokens,
+ * which balances the load by construction), cfg->routing = MOE_EXPERT_CHOICE:
+ * the
  * router computes p = softmax(g) as for token choice, then every expert e
  * takes the C tokens with the largest p[t][e] - larger first, the lower
  * token index first among equal p - where
@@ -301,7 +302,7 @@ moe_status moe_dispatch_noalloc(const moe_config* cfg, const void* x, const int3
 
 /*
  * Auxiliary-loss-free balancing ("The central problem: load balancing":
- * adjust per-expert bias terms dynamically based on load): after a batch,
+ * per-expert bias terms that follow the observed load): after a batch,
  * moves each expert's router logit bias by `step` toward balanced load -
  *   logit_bias[e] -= step  if expert_counts[e] > mean count,
  *   logit_bias[e] += step  if expert_counts[e] < mean count,

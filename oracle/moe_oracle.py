@@ -27,8 +27,8 @@ the combine and of the auxiliary loss did not survive extraction):
   residual add is outside the layer) and surviving weights are not
   renormalised again;
 * f_i of the auxiliary loss counts the top-1 choice only, before any drop;
-* the router z-loss, which the pages name without a formula ("penalise large
-  router logits"), is the mean over tokens of the squared log-sum-exp of the
+* the router z-loss, which the pages name without a formula (a penalty that
+  keeps the router logits small), is the mean over tokens of the squared log-sum-exp of the
   token's router logits (the logits that enter the softmax, bias included);
 * noisy gating adds a caller-drawn (T, E) noise tensor to the router logits
   before the softmax and the top-k (the pages give no distribution; the
@@ -36,7 +36,8 @@ the combine and of the auxiliary loss did not survive extraction):
 * auxiliary-loss-free balancing moves the per-expert logit bias by a fixed
   step toward balanced load after a batch: minus the step for an expert
   above the mean assignment count, plus it below, unchanged at the mean;
-* rerouting on overflow ("passed to the next-best expert") is one hop: after
+* rerouting on overflow (an overflowing token goes to its next-ranked
+  expert instead of being dropped) is one hop: after
   the drop pass above, the r-th dropped slot of a token (r = 0, 1, ...) is
   offered to the token's (k + r)-th ranked expert (the best one it does not
   use); offers are visited in (token, slot) order and an expert accepts them
@@ -52,7 +53,8 @@ the combine and of the auxiliary loss did not survive extraction):
   for caller-given dy and scalar weights; the gate weights carry gradient to
   the logits through the softmax (and the renormalisation), the auxiliary
   loss through P (f holds counts) and the z-loss through the log-sum-exp;
-* expert-choice routing ("experts choose their top tokens") ranks, for each
+* expert-choice routing (the experts, not the tokens, do the selecting)
+  ranks, for each
   expert, the batch's tokens by their router probability p[t, e] (the same
   softmax over experts as token choice), larger first and the lower token
   index first among equals, and keeps the first C; C is the capacity when one
@@ -87,8 +89,9 @@ def router_logits(x, W_r, logit_bias=None, logit_noise=None) -> np.ndarray:
     bias in its listing).  The optional additive per-expert bias is the fixed
     logit offset of the Switch workload (the mechanism [LECTURE] "The central
     problem: load balancing" names for bias-based balancing).  The optional
-    (T, E) noise is noisy gating ("The central problem: load balancing": noise
-    added to the router logits during training); the caller draws it.
+    (T, E) noise is noisy gating ("The central problem: load balancing":
+    random perturbation of the router's logits while training, so that it
+    explores); the caller draws it.
     x: (T, d); W_r: (E, d); returns (T, E) fp32.
     """
     g = np.asarray(x, f64) @ np.asarray(W_r, f64).T
@@ -125,7 +128,8 @@ def top_k(logits, k: int) -> np.ndarray:
 def gate_weights(probs, idx, renormalize: bool) -> np.ndarray:
     """Weights of the selected experts: p_sel / sum(p_sel), or p_sel as is.
 
-    [LECTURE] "The MoE layer" ("selected probabilities (often renormalised)");
+    [LECTURE] "The MoE layer" (the chosen experts' probabilities, usually
+    rescaled to sum to one);
     [DAY59] "Replace one MLP with many experts".  Returns (T, k) fp64.
     """
     sel = np.take_along_axis(np.asarray(probs, f64), np.asarray(idx, np.int64), axis=1)
@@ -137,8 +141,9 @@ def gate_weights(probs, idx, renormalize: bool) -> np.ndarray:
 def expert_capacity(capacity_factor: float, T: int, E: int) -> int:
     """C = ceil(capacity_factor * T / E).
 
-    [LECTURE] "The central problem: load balancing" (capacity factor x tokens
-    / experts); rounding up is the reading taken (the display formula of
+    [LECTURE] "The central problem: load balancing" (the capacity factor
+    scales each expert's even share of the tokens); rounding up is the
+    reading taken (the display formula of
     [DAY59] "Experts also have capacity limits" is lost).
     """
     return int(math.ceil(capacity_factor * T / E))
@@ -174,9 +179,9 @@ def capacity_keep(idx, E: int, capacity: int | None, n_shared: int = 0) -> np.nd
 def reroute_keep(ranked, k: int, E: int, capacity: int | None):
     """Drop, then offer each dropped slot once to the token's next-best expert.
 
-    [LECTURE] "The central problem: load balancing" (overflow tokens are
-    dropped or rerouted); [GLOSSARY] expert capacity (tokens may be passed to
-    the next-best expert).  ``ranked`` (T, K2) lists each token's experts best
+    [LECTURE] "The central problem: load balancing" (an overflowing token is
+    either dropped or sent elsewhere); [GLOSSARY] expert capacity (one option
+    sends it to its next-ranked expert).  ``ranked`` (T, K2) lists each token's experts best
     first, its k choices then the next K2 - k.  First pass: ``capacity_keep``
     on the k choices.  Second pass: the r-th dropped slot of token t is
     offered to ranked[t, k + r] (when k + r < K2); offers in (token, slot)
@@ -271,8 +276,8 @@ def balance_bias_update(logit_bias, counts, gamma: float) -> np.ndarray:
     """Auxiliary-loss-free balancing: move each expert's logit bias by gamma
     toward balanced load.
 
-    [LECTURE] "The central problem: load balancing" (adjust per-expert bias
-    terms dynamically based on load).  An expert with more assignments than
+    [LECTURE] "The central problem: load balancing" (per-expert bias terms
+    that follow the observed load).  An expert with more assignments than
     the mean loses gamma, one with fewer gains gamma, one at the mean keeps
     its bias.  Returns the new (E,) fp32 bias.
     """
@@ -287,8 +292,8 @@ def balance_bias_update(logit_bias, counts, gamma: float) -> np.ndarray:
 def router_z_loss(logits) -> float:
     """Router z-loss: mean over tokens of (log sum_e exp g_{t,e})^2.
 
-    [LECTURE] "The central problem: load balancing" (router z-loss penalises
-    large router logits).  The log-sum-exp is taken stably around the row
+    [LECTURE] "The central problem: load balancing" (a z-loss term on the
+    router that keeps its logits small, for numerical stability).  The log-sum-exp is taken stably around the row
     maximum.  Returns 0 for an empty batch.
     """
     g = np.asarray(logits, f64)
@@ -438,7 +443,8 @@ def expert_choice_capacity(T: int, E: int, k: int, capacity: int | None = None) 
     """C, the tokens each expert takes under expert-choice routing.
 
     [LECTURE] "Design variations" (expert-choice routing) and "The central
-    problem: load balancing" (capacity factor x tokens / experts): the given
+    problem: load balancing" (capacity as a multiple of the even share): the
+    given
     capacity, else ceil(T k / E), the load top-k token choice averages per
     expert; never more than the T tokens of the batch.
     """
@@ -482,8 +488,9 @@ def expert_choice_forward(x, W_r, W1, b1, W2, b2, k: int, capacity: int | None =
                           tokens=None) -> ExpertChoiceResult:
     """The MoE layer with expert-choice routing, looping over experts.
 
-    [LECTURE] "Design variations" (experts choose their top tokens,
-    guaranteeing balance) on the layer of "The MoE layer" (router logits and
+    [LECTURE] "Design variations" (each expert selects the tokens it takes,
+    which balances the load by construction) on the layer of "The MoE layer"
+    (router logits and
     softmax, expert FFNs, weighted sum of the experts' outputs).  ``logits``
     replaces the router GEMM when given; ``sel`` (E, C) replaces the
     selection (to evaluate the layer on another valid choice among equal

@@ -3,8 +3,8 @@
 // expert-contiguous order.
 //
 // "Mixture of Experts: Scaling Parameters Without Scaling Compute", section
-// "Design variations" (experts choose their top tokens, guaranteeing
-// balance).  Larger p first, the lower token index first among equal p; each
+// "Design variations" (each expert selects the tokens it takes, which
+// balances the load by construction).  Larger p first, the lower token index first among equal p; each
 // expert's rows are its chosen tokens in ascending token order, so expert e
 // owns rows e*C .. e*C + C - 1.
 //

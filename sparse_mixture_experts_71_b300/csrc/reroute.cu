@@ -2,9 +2,10 @@
 // token's next-best expert.
 //
 // "Mixture of Experts: Scaling Parameters Without Scaling Compute", section
-// "The central problem: load balancing" (overflow tokens are dropped or
-// rerouted) and "Mixture of Experts (MoE)" (inferensys glossary), expert
-// capacity (tokens may be passed to the next-best expert).  One hop: after
+// "The central problem: load balancing" (an overflowing token is dropped or
+// sent elsewhere) and "Mixture of Experts (MoE)" (inferensys glossary),
+// expert capacity (one option sends it to its next-ranked expert).  One hop:
+// after
 // the drop pass, the r-th dropped slot of a token goes to the token's
 // (k + r)-th ranked expert; offers are taken in (token, slot) order while the
 // expert's kept slots plus accepted offers stay below the capacity.

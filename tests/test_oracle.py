@@ -180,7 +180,7 @@ def test_noise_equal_to_a_bias_row_is_the_bias_and_zero_noise_is_none():
 
 def test_large_noise_on_one_expert_selects_it():
     """Noise far above the logit spread on expert j makes j every token's
-    first choice ("add noise to router logits ... to encourage exploration")."""
+    first choice (the noise is there to make the router explore)."""
     g = np.random.default_rng(9)
     x, W = g.standard_normal((64, 16)), g.standard_normal((8, 16)) * 0.1
     noise = np.zeros((64, 8))
@@ -195,7 +195,7 @@ def test_large_noise_on_one_expert_selects_it():
 @pytest.mark.parametrize("E,c", [(1, 0.0), (8, 0.0), (8, -2.5), (64, 3.25)])
 def test_z_loss_equal_logits_closed_form(E, c):
     """All logits equal to c: log-sum-exp = c + ln E for every token, so the
-    z-loss is (c + ln E)^2 ("penalise large router logits")."""
+    z-loss is (c + ln E)^2 (the term that keeps router logits small)."""
     g = np.full((50, E), c, np.float32)
     assert abs(O.router_z_loss(g) - (c + math.log(E)) ** 2) <= 1e-12 * max(1.0, (c + math.log(E)) ** 2)
 
@@ -667,7 +667,7 @@ def test_planted_expert_choice_mistakes_are_caught(monkeypatch):
         test_expert_choice_all_tokens_is_soft_mixture()
 
 
-# ---- rerouting on overflow ("passed to the next-best expert"); the reading
+# ---- rerouting on overflow (overflow sent to the next-ranked expert); the reading
 # (one hop, offers after the drop pass, in token order) is in the oracle's header
 
 def test_reroute_hand_worked():
