@@ -286,9 +286,13 @@ moe_status moe_get_device_error(void* ws, void* stream, int32_t* code, int32_t* 
  *   allocates nothing: no cudaMalloc, no cudaFree, no allocating library call.
  *   Limits: T * k <= 65536 and E <= 256; larger problems return
  *   MOE_ERR_UNSUPPORTED without enqueueing anything.
- *   The first call on a device, made while that device is current, looks up
- *   the array's device address (cudaGetSymbolAddress); make that first call
- *   before any stream capture.
+ *   The first call in a CUDA context, made while that context is current,
+ *   looks up the array's device address (cudaGetSymbolAddress); make that
+ *   first call before any stream capture.  Any context works: the primary
+ *   context the runtime uses, contexts the host creates with the driver
+ *   API, several contexts on one device, and the new primary context after
+ *   a device reset each get their own lookup (keyed on the context's unique
+ *   ID, the last 16 contexts remembered).
  *   All calls on a device share the one array: calls whose work overlaps on
  *   the GPU (different streams without ordering) race and give wrong results.
  *   Each call clears the part that must start at zero.  An expert index

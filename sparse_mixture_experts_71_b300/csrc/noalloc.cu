@@ -11,9 +11,14 @@
 // The array lives in this file as a __device__ variable, so every GPU that
 // loads the library holds it until the process exits.  Host code cannot use
 // its name as a device address; the device address is looked up with
-// cudaGetSymbolAddress once per device (on the first call made while that
-// device is current) and passed to the kernels.
+// cudaGetSymbolAddress once per CUDA context (on the first call made while
+// that context is current) and passed to the kernels.  A module symbol's
+// address belongs to a context, not to a device ordinal: a host that creates
+// its own driver-API contexts, switches between several on one device, or
+// resets the device (which replaces the primary context) gets a lookup of its
+// own, keyed on the context's process-unique ID.
 
+#include <cuda.h>
 #include <cuda_runtime.h>
 
 #include <mutex>
@@ -33,22 +38,63 @@ constexpr size_t kScratchBytes = sizeof(DeviceHeader) + 2 * kHistBytes +
 
 static __device__ __align__(256) unsigned char g_dispatch_scratch[kScratchBytes];
 
-constexpr int kMaxDevices = 64;
-void* g_scratch_ptr[kMaxDevices] = {};
+// Symbol addresses already looked up, keyed on the context's unique ID (a
+// context that is destroyed never has its ID reused).  Sixteen entries; the
+// oldest is replaced when a seventeenth context calls.
+constexpr int kCacheEntries = 16;
+struct ScratchEntry {
+    unsigned long long ctx_id;
+    void* ptr;
+};
+ScratchEntry g_scratch_cache[kCacheEntries] = {};
+int g_scratch_next = 0;
 std::mutex g_scratch_mu;
 
-// Device address of the scratch array on the current device (looked up once
-// per device), or null if the lookup failed.
-void* scratch_for_current_device() {
-    int dev = 0;
-    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return nullptr;
+using CtxGetCurrentFn = CUresult (*)(CUcontext*);
+using CtxGetIdFn = CUresult (*)(CUcontext, unsigned long long*);
+
+template <typename Fn>
+Fn driver_fn(const char* name) {
+    void* ptr = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion(name, &ptr, 12000, cudaEnableDefault, &q) != cudaSuccess ||
+        q != cudaDriverEntryPointSuccess)
+        return nullptr;
+    return reinterpret_cast<Fn>(ptr);
+}
+
+// ID of the calling thread's current context, or 0 if there is none or the
+// driver does not say.
+unsigned long long current_context_id() {
+    static const CtxGetCurrentFn get_current = driver_fn<CtxGetCurrentFn>("cuCtxGetCurrent");
+    static const CtxGetIdFn get_id = driver_fn<CtxGetIdFn>("cuCtxGetId");
+    if (get_current == nullptr || get_id == nullptr) return 0;
+    CUcontext ctx = nullptr;
+    unsigned long long id = 0;
+    if (get_current(&ctx) != CUDA_SUCCESS || ctx == nullptr) return 0;
+    if (get_id(ctx, &id) != CUDA_SUCCESS) return 0;
+    return id;
+}
+
+// Device address of the scratch array in the current context, or null if the
+// lookup failed.  Looked up once per context; without a context ID (no
+// context current yet: the lookup itself makes the device's primary context
+// current) the result is cached under the ID of the context the lookup left
+// current.
+void* scratch_for_current_context() {
     std::lock_guard<std::mutex> lock(g_scratch_mu);
-    if (g_scratch_ptr[dev] == nullptr) {
-        void* p = nullptr;
-        if (cudaGetSymbolAddress(&p, g_dispatch_scratch) != cudaSuccess) return nullptr;
-        g_scratch_ptr[dev] = p;
+    unsigned long long id = current_context_id();
+    if (id != 0)
+        for (const ScratchEntry& en : g_scratch_cache)
+            if (en.ctx_id == id) return en.ptr;
+    void* p = nullptr;
+    if (cudaGetSymbolAddress(&p, g_dispatch_scratch) != cudaSuccess || p == nullptr) return nullptr;
+    if (id == 0) id = current_context_id();
+    if (id != 0) {
+        g_scratch_cache[g_scratch_next] = ScratchEntry{id, p};
+        g_scratch_next = (g_scratch_next + 1) % kCacheEntries;
     }
-    return g_scratch_ptr[dev];
+    return p;
 }
 
 }  // namespace
@@ -66,12 +112,6 @@ extern "C" moe_status moe_dispatch_noalloc(const moe_config* cfg, const void* x,
     const moe_config& c = *cfg;
     if (c.routing != MOE_TOKEN_CHOICE || c.overflow != MOE_DROP)
         return MOE_ERR_UNSUPPORTED;  // a token-choice step that drops on overflow
-    if (c.T < 0 || c.d <= 0 || c.d_ff <= 0 || c.E <= 0 || c.k <= 0 ||
-        (c.dtype != MOE_F32 && c.dtype != MOE_BF16) || (c.renormalize != 0 && c.renormalize != 1) ||
-        c.n_shared < 0 || c.n_shared >= c.E || c.k > c.E - c.n_shared)
-        return MOE_ERR_INVALID_ARG;
-    if (c.E > kMaxExperts || c.k + c.n_shared > kMaxTopK) return MOE_ERR_UNSUPPORTED;
-    if (c.d % 8 != 0 || c.d_ff % 8 != 0) return MOE_ERR_ALIGNMENT;
     const moe_config cd = dispatch_config(c);  // K = k + n_shared assignments per token
     if ((int64_t)cd.T * cd.k > kNoAllocMaxAssignments) return MOE_ERR_UNSUPPORTED;  // scratch bound
     if (offsets == nullptr) return MOE_ERR_INVALID_ARG;
@@ -85,7 +125,7 @@ extern "C" moe_status moe_dispatch_noalloc(const moe_config* cfg, const void* x,
     if ((reinterpret_cast<uintptr_t>(x) & 15u) != 0 || (reinterpret_cast<uintptr_t>(x_perm) & 15u) != 0)
         return MOE_ERR_ALIGNMENT;
 
-    void* scratch = scratch_for_current_device();
+    void* scratch = scratch_for_current_context();
     if (scratch == nullptr) return MOE_ERR_CUDA;
     // The scratch regions the dispatch kernels use, laid out in the array.
     WsLayout L = ws_layout(c);
