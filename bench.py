@@ -2,20 +2,26 @@
 """Throughput of the MoE-layer forward pass on B300 (libmoe, sm_103a).
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
-                    [--workload NAME] [--no-cpu-baseline]
+                    [--workload NAME] [--no-cpu-baseline] [--no-per-config]
+                    [--pass forward|backward]
 
 A step is one forward pass of the layer (route, dispatch, expert FFN,
 combine) over one batch of seeded synthetic inputs of the named workload
-(default: bf16, T=4096 tokens, d=1024, d_ff=4096, E=8, top-2).  The inputs
-and the expert weights are resident in HBM when the timed region starts; L2
-is flushed (a 256 MiB write) before every timed step and the flush is not
-timed.  Each step replays a CUDA graph of one moe_forward call; a second
-timed loop replays graphs of the stage calls (route + dispatch, expert FFN,
-combine) for the per-stage times and the expert FFN's roofline.  The
-end-to-end figure (`e2e`) runs the same steps through the host-buffer
+(default: the large-FFN layer, bf16, T=16384 tokens, d=4096, d_ff=14336,
+E=8, top-2).  The inputs and the expert weights are resident in HBM when the
+timed region starts; L2 is flushed (a 256 MiB write, untimed) before every
+timed step.  Each timed iteration replays a CUDA graph of one moe_forward
+call and then, after a second flush, the graphs of the stage calls (route +
+dispatch, expert FFN, combine), so the step and its stages are timed under
+the same clocks; the expert FFN's stage time gives the dominant kernel's
+roofline (against the measured bf16 burst peak, the sustained one as a
+note).  The same steps back to back without a flush give the warm-L2
+figure.  The end-to-end figure (`e2e`) runs the steps through the host-buffer
 executor (moe_pipeline_*): pinned host batch in, y and the loss out, the
-copies of neighbouring steps overlapping the forward pass.  Rank 0 prints one
-JSON line.
+copies of neighbouring steps overlapping the forward pass.  With the default
+workload, `per_config` adds the other graded workloads (the T=4096 layer,
+Switch routing with the capacity drop, the decode-sized batch), timed the
+same way.  Rank 0 prints one JSON line.
 
 Under torchrun (N > 1) every rank runs an independent replica of the layer
 on its own GPU (the layer has no cross-GPU step); the line reports the tokens
@@ -30,6 +36,7 @@ import argparse
 import json
 import math
 import os
+import re
 import statistics
 import sys
 import threading
@@ -42,25 +49,10 @@ sys.path.insert(0, ROOT)
 
 from sparse_mixture_experts_71_b300 import inputs as I  # noqa: E402
 
-DEFAULT_WORKLOAD = I.MEDIUM.name
+DEFAULT_WORKLOAD = I.LARGE.name
 L2_BYTES = 126 << 20  # B300 L2
 PEAKS_FALLBACK = {"hbm_gbs": 6400.0, "bf16_tflops": 1800.0, "bf16_tflops_sustained": 1400.0}
 METRIC = "MoE-layer fwd tokens/s and achieved TFLOP/s (or HBM GB/s) vs B300 roofline"
-
-# DRAM bytes (read + write) of one expert-FFN launch pair (GEMM1 + GEMM2) from
-# an ncu capture of the current kernels; the summary with the commands is
-# profiles/grouped_gemm_dram_traffic.md.  Workloads without a capture report
-# null.
-TRAFFIC_BYTES = {
-    "bf16-T4096-d1024-F4096-E8-top2": (84.054 + 31.461 + 139.353 + 11.425) * 1e6,
-    "decode-bf16-T64-d4096-F14336-E8-top2": (941.527 + 6.074 + 944.296 + 1.548) * 1e6,
-    "switch-bf16-T32768-d2048-F8192-E64-top1-cap640": (719.259 + 56.750 + 779.743 + 26.946) * 1e6,
-    "finegrained-bf16-T4096-d2048-F1024-E64-top6": (372.038 + 39.568 + 325.019 + 160.830) * 1e6,
-    "expertchoice-bf16-T4096-d1024-F4096-E8-C1024": (83.999 + 31.100 + 143.555 + 9.596) * 1e6,
-    "switch-reroute-bf16-T32768-d2048-F8192-E64-top1-cap640":
-        (997.822 + 97.153 + 1104.171 + 47.158) * 1e6,
-}
-
 
 def peaks():
     p = os.path.join(ROOT, "MEASURED_PEAKS.json")
@@ -234,7 +226,7 @@ def oracle_layer(wl, inp):
                                    reroute=wl.overflow == "reroute")
 
 
-def cpu_oracle_rate(wl, inp, budget_s: float, min_tokens: int = 64):
+def cpu_oracle_rate(wl, inp, budget_s: float, min_tokens: int = 16, probe: int = 256):
     """Tokens/s of the oracle on a token sample sized to the time budget.
 
     The sample is the first n tokens of the batch taken as a batch of its own
@@ -246,7 +238,7 @@ def cpu_oracle_rate(wl, inp, budget_s: float, min_tokens: int = 64):
         layer(n)
         return time.perf_counter() - t0
 
-    n0 = min(wl.T, 256)
+    n0 = min(wl.T, probe)
     t0 = run(n0)
     n = int(min(wl.T, max(min_tokens, n0 * budget_s / max(t0, 1e-6))))
     t = run(n) if n != n0 else t0
@@ -291,17 +283,76 @@ def bench_reference(args, wl):
     return 0
 
 
-def bench_ours(args, wl):
+def _stats(ms):
+    return {"mean": statistics.mean(ms), "median": statistics.median(ms), "min": min(ms)}
+
+
+def ffn_roofline(wl, work, ffn_ms, pk, pk_kind):
+    """Roofline of the expert FFN (the grouped GEMM1 + GEMM2 launch pair, the
+    dominant kernel): against the measured bf16 burst peak when its arithmetic
+    intensity is above the ridge (the stage is timed on its own, in its own
+    graph), else its algorithmic bytes against the measured HBM copy rate."""
+    ffn_s = ffn_ms * 1e-3
+    ridge = pk["bf16_tflops"] * 1e12 / (pk["hbm_gbs"] * 1e9)  # flop per byte
+    traffic, traffic_src = committed_traffic(wl.name)
+    if wl.dtype == "bf16" and work["flops_ffn"] / work["ffn_bytes"] >= ridge:
+        achieved = work["flops_ffn"] / ffn_s / 1e12
+        peak = pk["bf16_tflops"]
+        roof = {"bound": "tensor", "unit": "TFLOP/s", "peak_source": pk_kind + " bf16 burst",
+                "frac_of_sustained": achieved / pk["bf16_tflops_sustained"],
+                "algorithmic": f"4*d*d_ff*kept = {work['flops_ffn']:.4g} flop per launch pair"}
+    else:
+        achieved = work["ffn_bytes"] / ffn_s / 1e9
+        peak = pk["hbm_gbs"]
+        roof = {"bound": "hbm", "unit": "GB/s", "peak_source": pk_kind + " HBM copy",
+                "frac_of_8tbs_nominal": achieved / 8000.0,
+                "algorithmic": f"used-expert weights + kept rows in and out = "
+                               f"{work['ffn_bytes']:.4g} B per launch pair"}
+    roof.update({"kernel": "expert FFN (grouped GEMM1 + GEMM2)", "achieved": achieved,
+                 "peak": peak, "frac": achieved / peak, "traffic": traffic,
+                 "traffic_source": traffic_src})
+    return roof
+
+
+TRAFFIC_SUMMARY = os.path.join("profiles", "grouped_gemm_dram_traffic.md")
+
+
+def committed_traffic(workload):
+    """DRAM bytes (read + write) of one expert-FFN launch pair of `workload`
+    from the committed ncu summary (its forward GEMM1 and GEMM2 rows), with
+    the summary's path; (None, None) when it has no capture of the workload."""
+    path = os.path.join(ROOT, TRAFFIC_SUMMARY)
+    if not os.path.exists(path):
+        return None, None
+    total, rows = 0.0, 0
+    with open(path) as f:
+        for line in f:
+            cols = [c.strip() for c in line.strip().strip("|").split("|")]
+            if len(cols) < 5 or cols[0].strip("`") != workload:
+                continue
+            if not re.search(r"\bGEMM[12]\b", cols[1]) or "backward" in cols[1]:
+                continue
+            try:
+                total += (float(cols[3]) + float(cols[4])) * 1e6
+                rows += 1
+            except ValueError:
+                continue
+    if rows != 2:
+        return None, None
+    return total, TRAFFIC_SUMMARY
+
+
+def measure_workload(args, wl, dev, stream, flush, world, e2e=True):
+    """Device-timed forward steps of one workload: W warm-up steps, then K
+    timed steps in which each iteration replays the moe_forward graph and,
+    after a second L2 flush, the stage graphs (route + dispatch, expert FFN,
+    combine), so both see the same clocks; then K steps back to back without a
+    flush (warm L2); then, optionally, K end-to-end steps through the
+    host-buffer executor.  Returns the per-workload record."""
     import torch
     import torch.distributed as dist
     from sparse_mixture_experts_71_b300 import binding as B
     from sparse_mixture_experts_71_b300.layer import MoELayer, capture_graph, device_inputs
-
-    world, rank, local = dist_setup()
-    torch.cuda.set_device(local)
-    dev = torch.device("cuda", local)
-    if world > 1:
-        dist.init_process_group("nccl", device_id=dev)
 
     inp = I.make_inputs(wl, seed=0)
     D = device_inputs(inp, dev)
@@ -310,7 +361,6 @@ def bench_ours(args, wl):
                      overflow=wl.overflow)
     cfg = layer.config(wl.T)
     ws = layer.workspace(wl.T)
-    stream = torch.cuda.current_stream(dev)
     T, k, E, d = wl.T, wl.k, wl.E, wl.d
     ec = wl.routing == "expert"
     n = E * B.expert_choice_capacity(cfg) if ec else T * k  # permuted rows
@@ -328,7 +378,6 @@ def bench_ours(args, wl):
                x_perm=torch.empty((n, d), dtype=dt, device=dev),
                y_perm=torch.empty((n, d), dtype=f32, device=dev),
                y=torch.empty((T, d), dtype=dt, device=dev))
-    flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
 
     def stage_route(st):
         b = buf
@@ -360,6 +409,7 @@ def bench_ours(args, wl):
     # every step is one CUDA-graph replay of the layer call (no host launch cost
     # inside the timed region); the stage graphs time the stages separately
     graphs, kernels = {}, {}
+    stages = ("route+dispatch", "expert_ffn", "combine")
     for name, fn in (("forward", full_forward), ("route+dispatch", stage_route),
                      ("expert_ffn", stage_ffn), ("combine", stage_combine)):
         c0 = B.launch_count()
@@ -373,48 +423,87 @@ def bench_ours(args, wl):
     for _ in range(max(args.warmup, 3)):
         flush.fill_(1)
         graphs["forward"].replay()
-        for name in ("route+dispatch", "expert_ffn", "combine"):
+        flush.fill_(1)
+        for name in stages:
             graphs[name].replay()
     torch.cuda.synchronize(dev)
     kept = [int(v) for v in torch.diff(buf["offsets"]).cpu().tolist()]
     work = algorithmic_work(wl, kept)
 
-    ev_f = [[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in range(args.steps)]
-    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(args.steps)]
-    sampler = ClockSampler(local)
+    K = args.steps
+    mk = lambda: torch.cuda.Event(enable_timing=True)  # noqa: E731
+    ev_f = [[mk(), mk()] for _ in range(K)]
+    evs = [[mk() for _ in range(4)] for _ in range(K)]
+    ev_w = [[mk(), mk()] for _ in range(K)]
+    sampler = ClockSampler(torch.cuda.current_device())
     if world > 1:
         dist.barrier()
     torch.cuda.synchronize(dev)
     with sampler:
-        for s in range(args.steps):
+        for s in range(K):
             flush.fill_(s & 0xFF)
             ev_f[s][0].record(stream)
             graphs["forward"].replay()
             ev_f[s][1].record(stream)
-        for s in range(args.steps):
-            flush.fill_(s & 0xFF)
+            flush.fill_((s + 1) & 0xFF)
             evs[s][0].record(stream)
-            graphs["route+dispatch"].replay()
-            evs[s][1].record(stream)
-            graphs["expert_ffn"].replay()
-            evs[s][2].record(stream)
-            graphs["combine"].replay()
-            evs[s][3].record(stream)
+            for j, name in enumerate(stages):
+                graphs[name].replay()
+                evs[s][j + 1].record(stream)
         torch.cuda.synchronize(dev)
     if world > 1:
         dist.barrier()
-    launches = args.steps * sum(kernels.values())
+    for s in range(K):  # warm L2: the same steps back to back, no flush
+        ev_w[s][0].record(stream)
+        graphs["forward"].replay()
+        ev_w[s][1].record(stream)
+    torch.cuda.synchronize(dev)
     step_ms = [e[0].elapsed_time(e[1]) for e in ev_f]
-    ffn_ms = [e[1].elapsed_time(e[2]) for e in evs]
-    route_ms = [e[0].elapsed_time(e[1]) for e in evs]
-    comb_ms = [e[2].elapsed_time(e[3]) for e in evs]
+    stage_ms = {name: [e[j].elapsed_time(e[j + 1]) for e in evs] for j, name in enumerate(stages)}
+    warm_ms = [e[0].elapsed_time(e[1]) for e in ev_w]
     total_ms = slowest_rank_ms(sum(step_ms), world, dev)
-    ms_per_step = total_ms / args.steps
-    value = job_tokens_per_s(world, T, args.steps, total_ms)
+    ms_per_step = total_ms / K
+    pk, pk_kind = peaks()
+    rec = {"workload": wl.name, "T": T, "d": d, "d_ff": wl.F, "E": E, "k": k,
+           "capacity": wl.capacity, "routing": wl.routing, "overflow": wl.overflow,
+           "value": job_tokens_per_s(world, T, K, total_ms), "unit": "tokens/s",
+           "ms_per_step": ms_per_step, "ms_per_step_stats": _stats(step_ms),
+           "tflops": work["flops"] / (ms_per_step * 1e-3) / 1e12 * world,
+           "hbm_gbs_algorithmic": work["bytes"] / (ms_per_step * 1e-3) / 1e9 * world,
+           "whole_call": {"algorithmic_bytes": work["bytes"], "algorithmic_flops": work["flops"],
+                          "gbs": work["bytes"] / (ms_per_step * 1e-3) / 1e9,
+                          "frac_of_measured_hbm": work["bytes"] / (ms_per_step * 1e-3) / 1e9
+                          / pk["hbm_gbs"],
+                          "frac_of_8tbs_nominal": work["bytes"] / (ms_per_step * 1e-3) / 8e12,
+                          "frac_of_bf16_burst": work["flops"] / (ms_per_step * 1e-3) / 1e12
+                          / pk["bf16_tflops"]},
+           "warm_l2": {"ms_per_step": statistics.mean(warm_ms),
+                       "ms_per_step_median": statistics.median(warm_ms),
+                       "value": T * world / (statistics.mean(warm_ms) * 1e-3)},
+           "kernels_per_step": kernels["forward"],
+           "stages_ms": {name: statistics.mean(v) for name, v in stage_ms.items()},
+           "stages_ms_median": {name: statistics.median(v) for name, v in stage_ms.items()},
+           "kept_assignments": work["kept"], "experts_used": work["experts_used"],
+           "roofline": ffn_roofline(wl, work, statistics.mean(stage_ms["expert_ffn"]), pk,
+                                    pk_kind),
+           "gpu_launches": K * sum(kernels.values()) + (3 if e2e else 2) * K * kernels["forward"],
+           "clocks": sampler.summary(),
+           "l2": "flushed before every timed step and before every stage-graph step "
+                 "(256 MiB write, untimed); warm_l2: no flush"}
+    if e2e:
+        rec["e2e"] = measure_e2e(args, wl, inp, layer, dev, stream, flush, world, dt)
+    rec["_inputs"] = inp
+    return rec
 
-    # end to end through the host-buffer executor of the C ABI (moe_pipeline_*):
-    # per step the pinned host batch is copied in, the layer runs, y and the
-    # loss are copied out; neighbouring steps' copies overlap the forward pass
+
+def measure_e2e(args, wl, inp, layer, dev, stream, flush, world, dt):
+    """End to end through the host-buffer executor of the C ABI
+    (moe_pipeline_*): per step the pinned host batch is copied in, the layer
+    runs, y and the loss are copied out; neighbouring steps' copies overlap
+    the forward pass."""
+    import torch
+    import torch.distributed as dist
+    T, d, E = wl.T, wl.d, wl.E
     es = 2 if dt == torch.bfloat16 else 4
     x_np = inp.x.view(np.int16) if inp.x.dtype == np.uint16 else inp.x
     x_host = []
@@ -422,7 +511,7 @@ def bench_ours(args, wl):
         t = torch.from_numpy(x_np.copy())
         x_host.append((t.view(torch.bfloat16) if inp.x.dtype == np.uint16 else t).pin_memory())
     y_host = [torch.empty((T, d), dtype=dt).pin_memory() for _ in range(2)]
-    aux_host = [torch.empty(1, dtype=f32).pin_memory() for _ in range(2)]
+    aux_host = [torch.empty(1, dtype=torch.float32).pin_memory() for _ in range(2)]
     pipe = layer.host_pipeline(T, depth=2, stream=stream)
     # the expert weights are the data a step could find in L2 from the step
     # before; below twice the L2 size the L2 is flushed between steps (on the
@@ -447,63 +536,79 @@ def bench_ours(args, wl):
     e1.synchronize()
     e2e_ms = slowest_rank_ms(e0.elapsed_time(e1), world, dev)
     pipe.close()
-    e2e_value = job_tokens_per_s(world, T, args.steps, e2e_ms)
+    return {"value": job_tokens_per_s(world, T, args.steps, e2e_ms), "unit": "tokens/s",
+            "ms_per_step": e2e_ms / args.steps,
+            "h2d_bytes_per_step": T * d * es, "d2h_bytes_per_step": T * d * es + 4,
+            "path": "moe_pipeline_submit (pinned host x in, y and loss out; copies of "
+                    "neighbouring steps overlap the forward pass)",
+            "l2": ("flushed before every step, inside the timed region" if e2e_flush
+                   else f"not flushed: expert weights ({w_bytes / 2**20:.0f} MiB) exceed "
+                        "twice the L2")}
 
-    pk, pk_kind = peaks()
-    clocks = sampler.summary()
-    ffn_s = statistics.mean(ffn_ms) * 1e-3
-    ridge = pk["bf16_tflops"] * 1e12 / (pk["hbm_gbs"] * 1e9)  # flop per byte
-    if wl.dtype == "bf16" and work["flops_ffn"] / work["ffn_bytes"] >= ridge:
-        achieved = work["flops_ffn"] / ffn_s / 1e12
-        # the burst figure for a contraction that runs below the power cap; the
-        # sustained one (cuBLAS back to back for seconds) when the power cap
-        # held the clocks down during the timed region
-        if "sw_power_cap" in clocks.get("reasons", []):
-            peak = pk["bf16_tflops_sustained"]
-            pk_kind += " sustained (sw_power_cap active in the timed region)"
-        else:
-            peak = pk["bf16_tflops"]
-            pk_kind += " burst"
-        roof = {"bound": "tensor", "unit": "TFLOP/s"}
-    else:
-        achieved = work["ffn_bytes"] / ffn_s / 1e9
-        peak = pk["hbm_gbs"]
-        roof = {"bound": "hbm", "unit": "GB/s"}
-    roof.update({"kernel": "expert FFN (grouped GEMM1 + GEMM2)", "achieved": achieved,
-                 "peak": peak, "peak_source": pk_kind, "frac": achieved / peak,
-                 "traffic": TRAFFIC_BYTES.get(wl.name)})
 
-    line = {"metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world,
-            "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_per_step,
+def cpu_baselines(wl, inp, budget_s=10.0):
+    """The oracle on the host cores, single-threaded and with every BLAS
+    thread, each on a token sample sized to about budget_s."""
+    from threadpoolctl import threadpool_limits
+    out = {}
+    with threadpool_limits(limits=1, user_api="blas"):
+        rate1, n1, t1, _ = cpu_oracle_rate(wl, inp, budget_s, probe=16)
+    rate, n, t, threads = cpu_oracle_rate(wl, inp, budget_s, probe=64)
+    out = {"value": rate, "unit": "tokens/s", "cores": threads, "kind": "oracle",
+           "sample": f"first {n} of {wl.T} tokens as a batch of their own, {t:.1f} s "
+                     f"({threads} BLAS threads)",
+           "single_thread": {"value": rate1, "cores": 1,
+                             "sample": f"first {n1} of {wl.T} tokens, {t1:.1f} s"},
+           "host_cores": os.cpu_count()}
+    return out
+
+
+PER_CONFIG = ("bf16-T4096-d1024-F4096-E8-top2", "switch-bf16-T32768-d2048-F8192-E64-top1-cap640",
+              "decode-bf16-T64-d4096-F14336-E8-top2")
+
+
+def bench_ours(args, wl):
+    import torch
+    import torch.distributed as dist
+
+    world, rank, local = dist_setup()
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    if world > 1:
+        dist.init_process_group("nccl", device_id=dev)
+    stream = torch.cuda.current_stream(dev)
+    flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
+
+    rec = measure_workload(args, wl, dev, stream, flush, world)
+    inp = rec.pop("_inputs")
+    line = {"metric": METRIC, "value": rec["value"], "unit": "tokens/s", "n_gpus": world,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": rec["ms_per_step"],
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
             "dtype": "bf16" if wl.dtype == "bf16" else "f32", "data": "synthetic",
-            "config": {"workload": wl.name, "T": T, "d": d, "d_ff": wl.F, "E": E, "k": k,
-                       "capacity": wl.capacity, "routing": wl.routing, "overflow": wl.overflow,
-                       "parallelism": f"replicas{world}",
-                       "l2": "flushed before every timed step (256 MiB write, untimed)"},
-            "tflops": work["flops"] / (ms_per_step * 1e-3) / 1e12 * world,
-            "hbm_gbs_algorithmic": work["bytes"] / (ms_per_step * 1e-3) / 1e9 * world,
-            "kernels_per_step": kernels["forward"],
-            "stages_ms": {"route+dispatch": statistics.mean(route_ms),
-                          "expert_ffn": statistics.mean(ffn_ms),
-                          "combine": statistics.mean(comb_ms)},
-            "kept_assignments": work["kept"],
-            "roofline": roof,
-            "e2e": {"value": e2e_value, "unit": "tokens/s",
-                    "h2d_bytes_per_step": T * d * es, "d2h_bytes_per_step": T * d * es + 4,
-                    "path": "moe_pipeline_submit (pinned host x in, y and loss out; "
-                            "copies of neighbouring steps overlap the forward pass)",
-                    "l2": ("flushed before every step, inside the timed region" if e2e_flush
-                           else f"not flushed: expert weights ({w_bytes / 2**20:.0f} MiB) "
-                                "exceed twice the L2")},
-            "gpu_launches": launches,
-            "clocks": clocks}
+            "config": {"workload": wl.name, "T": wl.T, "d": wl.d, "d_ff": wl.F, "E": wl.E,
+                       "k": wl.k, "capacity": wl.capacity, "routing": wl.routing,
+                       "overflow": wl.overflow, "parallelism": f"replicas{world}",
+                       "l2": rec["l2"]}}
+    for key in ("ms_per_step_stats", "tflops", "hbm_gbs_algorithmic", "whole_call", "warm_l2",
+                "kernels_per_step", "stages_ms", "stages_ms_median", "kept_assignments",
+                "roofline", "e2e", "gpu_launches", "clocks"):
+        line[key] = rec[key]
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
-        rate, n_tok, t, threads = cpu_oracle_rate(wl, inp, budget_s=12.0)
-        line["cpu_baseline"] = {"value": rate, "unit": "tokens/s", "cores": threads,
-                                "kind": "oracle",
-                                "sample": f"first {n_tok} of {T} tokens as a batch of their "
-                                          f"own, {t:.1f} s"}
+        line["cpu_baseline"] = cpu_baselines(wl, inp)
+    del inp
+    if args.per_config and wl.name == DEFAULT_WORKLOAD:
+        # the other graded workloads, device-timed the same way (no CPU baseline)
+        per = {}
+        for name in PER_CONFIG:
+            torch.cuda.empty_cache()
+            r = measure_workload(args, I.WORKLOADS[name], dev, stream, flush, world)
+            r.pop("_inputs")
+            per[name] = {key: r[key] for key in (
+                "value", "unit", "ms_per_step", "ms_per_step_stats", "tflops",
+                "hbm_gbs_algorithmic", "whole_call", "warm_l2", "stages_ms", "stages_ms_median",
+                "kept_assignments", "experts_used", "roofline", "e2e", "kernels_per_step",
+                "clocks")}
+        line["per_config"] = per
     if rank == 0:
         print(json.dumps(line), flush=True)
     if world > 1:
@@ -611,6 +716,8 @@ def main():
     ap.add_argument("--impl", choices=("ours", "reference"), default="ours")
     ap.add_argument("--workload", default=DEFAULT_WORKLOAD, choices=list(I.WORKLOADS))
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-per-config", dest="per_config", action="store_false",
+                    help="skip the per_config block (the other graded workloads)")
     ap.add_argument("--pass", dest="pass_", choices=("forward", "backward"), default="forward",
                     help="backward: time moe_backward instead of the forward pass")
     args = ap.parse_args()

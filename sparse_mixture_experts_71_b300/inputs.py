@@ -138,17 +138,38 @@ def f32_to_bf16_bits(a: np.ndarray) -> np.ndarray:
 
 
 def bf16_bits_to_f32(u: np.ndarray) -> np.ndarray:
-    """Widen bf16 bit patterns exactly to fp32."""
-    return (np.asarray(u, dtype=np.uint16).astype(np.uint32) << np.uint32(16)).view(np.float32)
+    """Widen bf16 bit patterns exactly to fp32 (in chunks, on threads for
+    large arrays, without full-size temporaries)."""
+    u = np.ascontiguousarray(u, dtype=np.uint16)
+    out = np.empty(u.shape, dtype=np.uint32)
+    src, dst = u.reshape(-1), out.reshape(-1)
+
+    def conv(c: int) -> None:
+        lo, hi = c * _CHUNK, min(src.size, (c + 1) * _CHUNK)
+        d = dst[lo:hi]
+        d[...] = src[lo:hi]
+        d <<= np.uint32(16)
+
+    nchunks = (src.size + _CHUNK - 1) // _CHUNK
+    if nchunks <= 1:
+        for c in range(nchunks):
+            conv(c)
+    else:
+        with ThreadPoolExecutor(_threads()) as ex:
+            list(ex.map(conv, range(nchunks)))
+    return out.view(np.float32)
 
 
 def _threads() -> int:
     return max(1, min(16, os.cpu_count() or 1))
 
 
-def _draw(seed: int, stream: int, n: int, kind: str, scale: float) -> np.ndarray:
-    """n fp32 values: kind "normal" -> N(0, scale^2); "uniform" -> U(-scale, scale)."""
-    out = np.empty(n, dtype=np.float32)
+def _draw(seed: int, stream: int, n: int, kind: str, scale: float,
+          dtype: str = "f32") -> np.ndarray:
+    """n values: kind "normal" -> N(0, scale^2); "uniform" -> U(-scale, scale),
+    drawn in fp32; dtype "bf16" returns them rounded to bf16 bit patterns
+    (each chunk rounded in the thread that drew it)."""
+    out = np.empty(n, dtype=np.uint16 if dtype == "bf16" else np.float32)
 
     def fill(c: int) -> None:
         lo, hi = c * _CHUNK, min(n, (c + 1) * _CHUNK)
@@ -160,7 +181,7 @@ def _draw(seed: int, stream: int, n: int, kind: str, scale: float) -> np.ndarray
             v = g.random(hi - lo, dtype=np.float32)
             v *= np.float32(2.0 * scale)
             v -= np.float32(scale)
-        out[lo:hi] = v
+        out[lo:hi] = f32_to_bf16_bits(v) if dtype == "bf16" else v
 
     nchunks = (n + _CHUNK - 1) // _CHUNK
     if nchunks <= 1:
@@ -170,10 +191,6 @@ def _draw(seed: int, stream: int, n: int, kind: str, scale: float) -> np.ndarray
         with ThreadPoolExecutor(_threads()) as ex:
             list(ex.map(fill, range(nchunks)))
     return out
-
-
-def _store(a: np.ndarray, dtype: str) -> np.ndarray:
-    return f32_to_bf16_bits(a) if dtype == "bf16" else a
 
 
 def zipf_logit_bias(E: int, scale: float) -> np.ndarray:
@@ -186,17 +203,17 @@ def make_inputs(wl: Workload, seed: int = 0) -> Inputs:
     """Draw every stored input of workload ``wl`` from ``seed``."""
     T, d, F, E = wl.T, wl.d, wl.F, wl.E
     Er = E - wl.n_shared  # experts the router covers
-    x = _draw(seed, _S_X, T * d, "normal", 1.0).reshape(T, d)
+    dt = wl.dtype
+    x = _draw(seed, _S_X, T * d, "normal", 1.0, dt).reshape(T, d)
     if wl.init == "uniform":
         W_r = _draw(seed, _S_WR, Er * d, "uniform", 1.0 / math.sqrt(d)).reshape(Er, d)
-        W1 = _draw(seed, _S_W1, E * F * d, "uniform", 1.0 / math.sqrt(d)).reshape(E, F, d)
-        W2 = _draw(seed, _S_W2, E * d * F, "uniform", 1.0 / math.sqrt(F)).reshape(E, d, F)
+        W1 = _draw(seed, _S_W1, E * F * d, "uniform", 1.0 / math.sqrt(d), dt).reshape(E, F, d)
+        W2 = _draw(seed, _S_W2, E * d * F, "uniform", 1.0 / math.sqrt(F), dt).reshape(E, d, F)
     else:
         W_r = _draw(seed, _S_WR, Er * d, "normal", 0.02).reshape(Er, d)
-        W1 = _draw(seed, _S_W1, E * F * d, "normal", 1.0 / math.sqrt(d)).reshape(E, F, d)
-        W2 = _draw(seed, _S_W2, E * d * F, "normal", 1.0 / math.sqrt(F)).reshape(E, d, F)
-    b1 = _draw(seed, _S_B1, E * F, "uniform", 1.0 / math.sqrt(d)).reshape(E, F)
-    b2 = _draw(seed, _S_B2, E * d, "uniform", 1.0 / math.sqrt(F)).reshape(E, d)
+        W1 = _draw(seed, _S_W1, E * F * d, "normal", 1.0 / math.sqrt(d), dt).reshape(E, F, d)
+        W2 = _draw(seed, _S_W2, E * d * F, "normal", 1.0 / math.sqrt(F), dt).reshape(E, d, F)
+    b1 = _draw(seed, _S_B1, E * F, "uniform", 1.0 / math.sqrt(d), dt).reshape(E, F)
+    b2 = _draw(seed, _S_B2, E * d, "uniform", 1.0 / math.sqrt(F), dt).reshape(E, d)
     bias = zipf_logit_bias(Er, wl.zipf_bias) if wl.zipf_bias else None
-    return Inputs(wl, _store(x, wl.dtype), W_r, bias, _store(W1, wl.dtype), _store(b1, wl.dtype),
-                  _store(W2, wl.dtype), _store(b2, wl.dtype))
+    return Inputs(wl, x, W_r, bias, W1, b1, W2, b2)

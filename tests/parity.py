@@ -151,19 +151,28 @@ def oracle_on(inp, wl, logits=None, tokens=None, layout=True):
                          n_shared=wl.n_shared, reroute=wl.overflow == "reroute")
 
 
-def sample_tokens(wl, ref_route, n: int, seed: int = 0) -> np.ndarray:
-    """A seeded token sample covering every non-empty expert and, under a cap,
-    the last kept and first dropped tokens of every expert that overflowed."""
+def sample_tokens(wl, ref_route, n_kept: int = 1024, tile: int = 256, per_tile: int = 4,
+                  n_dropped: int = 64, seed: int = 0) -> np.ndarray:
+    """A seeded token sample for the largest workloads: in every `tile`-row
+    tile of every expert's segment of the permuted rows (the GEMMs' token
+    tiles), the tokens of its first and last rows and of `per_tile` - 2 random
+    rows; under a cap, the last kept and first and last dropped tokens of every
+    expert that overflowed; then random tokens with at least one kept
+    assignment until `n_kept` of them are in, and `n_dropped` random tokens
+    whose every assignment was dropped (their output must be 0).
+    `ref_route` is the oracle's result with the dispatch layout."""
     g = np.random.default_rng(seed)
     T = wl.T
-    pick = set(g.choice(T, size=min(n, T), replace=False).tolist())
+    pick = set()
+    off, perm = ref_route.offsets, ref_route.perm_token
+    for e in range(len(off) - 1):
+        for r0 in range(int(off[e]), int(off[e + 1]), tile):
+            r1 = min(r0 + tile, int(off[e + 1]))
+            rows = {r0, r1 - 1} | set(g.integers(r0, r1, size=max(per_tile - 2, 0)).tolist())
+            pick |= {int(perm[r]) for r in rows}
     idx, kept = ref_route.idx, ref_route.kept
-    for e in range(wl.E):
-        toks = np.nonzero((idx == e).any(axis=1))[0]
-        if toks.size:
-            pick.add(int(toks[0]))
-            pick.add(int(toks[-1]))
-        if wl.capacity is not None:
+    if wl.capacity is not None:
+        for e in range(wl.E):
             sel = (idx == e)
             kt = np.nonzero((sel & kept).any(axis=1))[0]
             dt = np.nonzero((sel & ~kept).any(axis=1))[0]
@@ -172,4 +181,13 @@ def sample_tokens(wl, ref_route, n: int, seed: int = 0) -> np.ndarray:
             if dt.size:
                 pick.add(int(dt[0]))
                 pick.add(int(dt[-1]))
+    any_kept = kept.any(axis=1)
+    kept_tokens = np.nonzero(any_kept)[0]
+    have = sum(1 for t in pick if any_kept[t])
+    if have < n_kept:
+        rest = np.setdiff1d(kept_tokens, np.fromiter(pick, np.int64, len(pick)))
+        pick |= set(g.choice(rest, size=min(n_kept - have, rest.size), replace=False).tolist())
+    dropped = np.nonzero(~any_kept)[0]
+    if dropped.size:
+        pick |= set(g.choice(dropped, size=min(n_dropped, dropped.size), replace=False).tolist())
     return np.array(sorted(pick), np.int64)

@@ -27,6 +27,9 @@ CASES = [
     ("bwd-decode", 64, 256, 512, 8, 2, None, True, 0.0, 0.0, 0.0),     # single-CTA GEMMs
     ("bwd-e64-tc-router", 1100, 128, 128, 64, 2, 30, True, 1.0, 0.1, 0.1),
     ("bwd-ragged", 1500, 64, 192, 5, 2, 500, True, 1.0, 0.0, 0.0),
+    # mid size: ~1024 rows per expert, so the weight-gradient GEMMs' segment
+    # reduction walks 8 K tiles of 128 per expert, on both GEMM kernels' wide path
+    ("bwd-mid", 4096, 512, 2048, 8, 2, None, True, 0.0, 0.01, 0.001),
 ]
 
 

@@ -102,7 +102,7 @@ def test_reroute_full_switch_workload():
     assert np.array_equal(to_np(r["slot_of"]), ref.slot_of)
     nk = int(ref.offsets[-1])
     assert np.array_equal(to_np(r["perm_token"])[:nk], ref.perm_token)
-    tokens = sample_tokens(wl, ref, n=192)
+    tokens = sample_tokens(wl, ref)
     # and the rerouted tokens among the sample
     moved = np.nonzero(ref.kept[:, 0] & (ref.idx[:, 0] != O.top_k(g, 1)[:, 0]))[0]
     tokens = np.unique(np.concatenate([tokens, moved[:64]]))
