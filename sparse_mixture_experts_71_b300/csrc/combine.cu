@@ -68,7 +68,87 @@ __global__ void __launch_bounds__(256) combine_kernel(const float* __restrict__ 
     }
 }
 
+// Combine of the dense decode path (see moe_forward): token t's output is the
+// sum, over its kept slots j in slot order, of w[t][j] * y_all[e * T + t]
+// with e = idx[t][j] (fp32; the product and the sum rounded separately, so
+// the result is the sparse path's, whose second GEMM multiplies by the
+// weight and whose combine adds in slot order), 0 if every slot was dropped.
+// A slot is kept when fewer than `capacity` earlier assignments, in (token,
+// slot) order, went to its expert (capacity < 0: no cap) - the rank the
+// sparse dispatch computes, counted here directly (T <= 64).  An expert index
+// outside [0, E) is skipped and recorded.  Block 0 then finishes the router's
+// auxiliary loss, z-loss and per-expert counts (do_loss).
+template <typename TY>
+__global__ void __launch_bounds__(256) dense_combine_kernel(
+    const float* __restrict__ y_all, const int32_t* __restrict__ idx, const float* __restrict__ w,
+    int T, int k, int d, int E, int capacity, TY* __restrict__ y, DeviceHeader* hdr, LossArgs loss,
+    int do_loss) {
+    pdl_wait();
+    pdl_trigger();
+    __shared__ float s_part[256];
+    __shared__ float s_d[kMaxExperts];
+    const int lane = threadIdx.x % 32;
+    const int nwarps = gridDim.x * (blockDim.x / 32);
+    const int nv = d / 4;
+    const int nch = (nv + 127) / 128;
+    const long long tasks = (long long)T * nch;
+    for (long long task = blockIdx.x * (blockDim.x / 32) + threadIdx.x / 32; task < tasks;
+         task += nwarps) {
+        const int t = (int)(task / nch);
+        const int v0 = (int)(task % nch) * 128 + lane;
+        float4 acc[4];
+#pragma unroll
+        for (int u = 0; u < 4; ++u) acc[u] = make_float4(0.f, 0.f, 0.f, 0.f);
+        for (int j = 0; j < k; ++j) {  // slot order
+            const int a = t * k + j;
+            const int e = __ldg(idx + a);
+            if (e < 0 || e >= E) {
+                if (lane == 0 && task % nch == 0) record_error(hdr, kErrExpertRange, t);
+                continue;
+            }
+            if (capacity >= 0) {
+                int before = 0;
+                for (int b = lane; b < a; b += 32) before += __ldg(idx + b) == e;
+#pragma unroll
+                for (int o = 16; o > 0; o >>= 1) before += __shfl_xor_sync(0xffffffffu, before, o);
+                if (before >= capacity) continue;  // dropped
+            }
+            const float wj = __ldg(w + a);
+            const float4* row = reinterpret_cast<const float4*>(y_all + ((size_t)e * T + t) * d);
+#pragma unroll
+            for (int u = 0; u < 4; ++u) {
+                if (v0 + 32 * u < nv) {
+                    const float4 q = __ldg(row + v0 + 32 * u);
+                    acc[u].x = __fadd_rn(acc[u].x, __fmul_rn(wj, q.x));
+                    acc[u].y = __fadd_rn(acc[u].y, __fmul_rn(wj, q.y));
+                    acc[u].z = __fadd_rn(acc[u].z, __fmul_rn(wj, q.z));
+                    acc[u].w = __fadd_rn(acc[u].w, __fmul_rn(wj, q.w));
+                }
+            }
+        }
+#pragma unroll
+        for (int u = 0; u < 4; ++u)
+            if (v0 + 32 * u < nv) store4(y + (size_t)t * d + 4 * (v0 + 32 * u), acc[u]);
+    }
+    if (do_loss && blockIdx.x == 0) {
+        __syncthreads();
+        loss_and_counts(loss, s_part, s_d);
+    }
+}
+
 }  // namespace
+
+cudaError_t launch_dense_combine(const moe_config& c, const float* y_all, const int32_t* idx,
+                                 const float* w, void* y, DeviceHeader* hdr, const LossArgs& loss,
+                                 bool do_loss, cudaStream_t s) {
+    if (c.T == 0) return cudaSuccess;
+    const long long tasks = (long long)c.T * ((c.d / 4 + 127) / 128);
+    long long blocks = (tasks + 7) / 8;
+    if (blocks > num_sms() * 8) blocks = num_sms() * 8;
+    return launch_kernel(dense_combine_kernel<__nv_bfloat16>, dim3((unsigned)blocks), dim3(256), 0,
+                         s, 1, false, y_all, idx, w, c.T, c.k, c.d, c.E, c.capacity,
+                         reinterpret_cast<__nv_bfloat16*>(y), hdr, loss, do_loss ? 1 : 0);
+}
 
 cudaError_t launch_combine(const moe_config& c, const float* y_perm, const int32_t* slot_of,
                            void* y, int64_t rows, cudaStream_t s) {

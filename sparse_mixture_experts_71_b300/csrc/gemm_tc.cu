@@ -96,10 +96,20 @@ struct Params {
     // zeros.
     const int32_t* koff;
     int tok_rows;
+    // Dense mode (single-CTA kernel, dense_T > 0): every expert e takes
+    // dense_T rows - input rows [0, dense_T) of the token operand when
+    // dense_shared_in (the layer input, shared by all experts), else rows
+    // e*dense_T .. - and writes output rows e*dense_T + j; offsets unused.
+    // With dense_shared_in the kernel reads only the layer's inputs, so it
+    // does not wait for the previous kernel of its chain before starting; the
+    // other dense GEMM loads its first weight stages before that wait.
+    int dense_T;
+    int dense_shared_in;
 };
 
 // Rows of an expert's segment (offsets clamped to the buffers).
 __device__ __forceinline__ int seg_rows(const Params& p, int e) {
+    if (p.dense_T > 0) return p.dense_T;
     const int s0 = min(max(__ldg(p.offsets + e), 0), p.rows_cap);
     const int s1 = min(max(__ldg(p.offsets + e + 1), s0), p.rows_cap);
     return s1 - s0;
@@ -108,6 +118,7 @@ __device__ __forceinline__ int seg_rows(const Params& p, int e) {
 
 struct Tile {
     int e, r0, n, m0;
+    int o0;  // first output row (r0 except in dense mode)
 };
 
 // Work item t of the single-CTA kernel: expert e, token tile (fastest) and
@@ -122,11 +133,20 @@ __device__ __forceinline__ Tile decode_tile(int t, const int* s_tiles, const Par
     Tile tl;
     tl.e = lo;
     const int local = t - s_tiles[lo];
-    const int s0 = min(max(__ldg(p.offsets + lo), 0), p.rows_cap);
-    const int s1 = min(max(__ldg(p.offsets + lo + 1), s0), p.rows_cap);
+    int s0, s1, ob;
+    if (p.dense_T > 0) {
+        s0 = p.dense_shared_in ? 0 : lo * p.dense_T;
+        s1 = s0 + p.dense_T;
+        ob = lo * p.dense_T;
+    } else {
+        s0 = min(max(__ldg(p.offsets + lo), 0), p.rows_cap);
+        s1 = min(max(__ldg(p.offsets + lo + 1), s0), p.rows_cap);
+        ob = s0;
+    }
     const int nt = (s1 - s0 + bn_max - 1) / bn_max;
     const int ti = local % nt, gi = local / nt;  // token tile fastest
     tl.r0 = s0 + ti * bn_max;
+    tl.o0 = ob + ti * bn_max;
     tl.n = min(bn_max, s1 - tl.r0);
     tl.m0 = gi * BM;
     return tl;
@@ -160,8 +180,9 @@ __device__ __forceinline__ void drain_bar(uint64_t* bar, uint32_t parity) {
 // Epilogue of one accumulator tile: this warp reads TMEM lanes 32q..32q+31
 // (weight rows fbase + 32q + lane) and the token columns of its part (of
 // nparts) of the COLS-wide tile (columns acc_col + c, c < n), applies bias + GELU (first
-// GEMM, bf16 out) or bias x routing weight (second GEMM, fp32 out), and
-// writes token rows r0 + c through a shared-memory transpose (stg: 32 x 32).
+// GEMM, bf16 out) or bias x routing weight (second GEMM, fp32 out; the
+// weight of input row r0 + c), and writes output rows o0 + c through a
+// shared-memory transpose (stg: 32 x 32).
 // With tm_out (second GEMM of the pair kernel) a full 32-row chunk leaves
 // shared memory by a TMA tensor store issued by lane 0 (box 32 weight rows x
 // 32 token rows of the output), so the warp neither reads the staging back
@@ -169,7 +190,8 @@ __device__ __forceinline__ void drain_bar(uint64_t* bar, uint32_t parity) {
 // segment: the rows after it belong to the next segment) is stored by the
 // lanes.
 template <int COLS, bool GEMM1>
-__device__ __forceinline__ void epilogue_tile(const Params& p, int e, int r0, int n, int fbase,
+__device__ __forceinline__ void epilogue_tile(const Params& p, int e, int r0, int o0, int n,
+                                              int fbase,
                                               uint32_t tmem_base, int acc_col, int q, int part,
                                               int nparts, int lane, uint8_t* stg,
                                               const CUtensorMap* tm_out = nullptr,
@@ -203,7 +225,7 @@ __device__ __forceinline__ void epilogue_tile(const Params& p, int e, int r0, in
                 const int fc = f0 + part * 8;
                 if (j < rows_here && fc < p.n_out) {
                     const uint4 val = *reinterpret_cast<const uint4*>(stg + j * 64 + part * 16);
-                    *reinterpret_cast<uint4*>(out + (size_t)(r0 + c + j) * p.n_out + fc) = val;
+                    *reinterpret_cast<uint4*>(out + (size_t)(o0 + c + j) * p.n_out + fc) = val;
                 }
             }
         } else {
@@ -223,7 +245,7 @@ __device__ __forceinline__ void epilogue_tile(const Params& p, int e, int r0, in
                 tc::fence_proxy_async_smem();
                 __syncwarp();
                 if (lane == 0) {
-                    tc::tma_store_2d(tm_out, stg, f0, r0 + c);
+                    tc::tma_store_2d(tm_out, stg, f0, o0 + c);
                     tc::bulk_commit();
                 }
                 continue;
@@ -236,7 +258,7 @@ __device__ __forceinline__ void epilogue_tile(const Params& p, int e, int r0, in
                 const int fc = f0 + part * 4;
                 if (j < rows_here && fc < p.n_out) {
                     const float4 val = *reinterpret_cast<const float4*>(stg + j * 128 + part * 16);
-                    *reinterpret_cast<float4*>(out + (size_t)(r0 + c + j) * p.n_out + fc) = val;
+                    *reinterpret_cast<float4*>(out + (size_t)(o0 + c + j) * p.n_out + fc) = val;
                 }
             }
         }
@@ -284,7 +306,8 @@ grouped_gemm_tc(const __grid_constant__ CUtensorMap tmA, const __grid_constant__
         tc::tmem_alloc(s_tmem, C::TMEM_COLS);
         tc::tmem_relinquish();
     }
-    pdl_wait();  // offsets and the operands come from the previous kernel
+    const bool dense = p.dense_T > 0;
+    if (!dense) pdl_wait();  // offsets and the operands come from the previous kernel
     pdl_trigger();
     if (warp == 3) {  // exclusive prefix of tiles per expert
         int run = 0;
@@ -318,12 +341,37 @@ grouped_gemm_tc(const __grid_constant__ CUtensorMap tmA, const __grid_constant__
             uint32_t phase = 0;
             long long fills = 0;
             bool ok = true;
+            int pre = 0;  // K steps of the first tile issued in the prologue
+            if (dense && !p.dense_shared_in) {
+                // the token operand comes from the previous kernel, the
+                // weights do not: the first stages' weight boxes are loaded
+                // before the wait, their token boxes after it
+                if (cta < total) {
+                    const Tile tl = decode_tile(cta, s_tiles, p, BN_MAX);
+                    const int nb = (tl.n + BOX_ROWS - 1) / BOX_ROWS;
+                    const uint32_t bytes = A_BYTES + nb * BOX_BYTES;
+                    const int arow = tl.e * p.n_out + tl.m0;
+                    pre = KB < STAGES ? KB : STAGES;
+                    for (int kb = 0; kb < pre; ++kb) {  // fresh stages: nothing to wait for
+                        tc::mbar_expect_tx(&full[kb], bytes);
+                        tc::tma_load_2d(smem + kb * C::STAGE_BYTES, &tmA, &full[kb], kb * BK, arow);
+                    }
+                    pdl_wait();
+                    for (int kb = 0; kb < pre; ++kb)
+                        for (int b = 0; b < nb; ++b)
+                            tc::tma_load_2d(smem + kb * C::STAGE_BYTES + A_BYTES + b * BOX_BYTES,
+                                            &tmB, &full[kb], kb * BK, tl.r0 + b * BOX_ROWS);
+                    fills = pre;
+                    stage = pre % STAGES;
+                    phase = pre == STAGES ? 1u : 0u;
+                }
+            }
             for (int t = cta; t < total && ok; t += nctas) {
                 const Tile tl = decode_tile(t, s_tiles, p, BN_MAX);
                 const int nb = (tl.n + BOX_ROWS - 1) / BOX_ROWS;
                 const uint32_t bytes = A_BYTES + nb * BOX_BYTES;
                 const int arow = tl.e * p.n_out + tl.m0;
-                for (int kb = 0; kb < KB; ++kb) {
+                for (int kb = t == cta ? pre : 0; kb < KB; ++kb) {
                     if (!wait_bar(&empty[stage], phase ^ 1, s_abort, p, 1)) { ok = false; break; }
                     tc::mbar_expect_tx(&full[stage], bytes);
                     uint8_t* sa = smem + stage * C::STAGE_BYTES;
@@ -390,8 +438,8 @@ grouped_gemm_tc(const __grid_constant__ CUtensorMap tmA, const __grid_constant__
             const bool ok = wait_bar(&tfull[acc], acc_phase, s_abort, p, 4);
             if (!__all_sync(0xffffffffu, ok)) break;
             tc::fence_after_sync();
-            epilogue_tile<BN_MAX, GEMM1>(p, tl.e, tl.r0, tl.n, tl.m0, tmem_base, acc * BN_MAX, q,
-                                         half, 2, lane, stg);
+            epilogue_tile<BN_MAX, GEMM1>(p, tl.e, tl.r0, tl.o0, tl.n, tl.m0, tmem_base,
+                                         acc * BN_MAX, q, half, 2, lane, stg);
             tc::fence_before_sync();
             __syncwarp();
             if (lane == 0) tc::mbar_arrive_relaxed(&tempty[acc]);
@@ -406,6 +454,292 @@ grouped_gemm_tc(const __grid_constant__ CUtensorMap tmA, const __grid_constant__
         tc::fence_after_sync();
         tc::tmem_dealloc(tmem_base, C::TMEM_COLS);
     }
+    // dense mode: this grid completes only after the previous kernel of the
+    // chain (which the first dense GEMM never waited for)
+    if (dense && threadIdx.x == 0) pdl_wait();
+}
+
+// ===================================================================== dense decode FFN
+// Both expert GEMMs of a decode-sized batch in one persistent kernel (dense
+// mode: every expert on all T <= 64 tokens; see launch_dense_gemm1).  Work
+// items 0 .. N1-1 are the first GEMM's 128-row weight tiles (expert
+// e = i / mt1: h_all[e*T + t] = GELU(x[t] W1_e^T + b1_e), bf16), items
+// N1 .. N1+N2-1 the second's (e = (i - N1) / mt2: y_all[e*T + t] =
+// h_all[e*T + t] W2_e^T + b2_e, fp32).  The producer claims items in order
+// from a counter in the workspace (so every item is claimed only after all
+// earlier ones, by a CTA that is running) and hands each to the MMA and
+// epilogue warps through a small ring in shared memory.  A second-GEMM item of
+// expert e loads its first weight stages, then waits (bounded) until every
+// epilogue warp of every first-GEMM item of e has stored its rows of h_all and
+// counted itself in ready[e]; so the second GEMM starts on the SMs the first
+// one frees, expert by expert, with no launch boundary or tail in between.
+// A first-GEMM item never waits on anything but its own pipeline, so the
+// waits always end.
+struct DenseFfn {
+    Params g1, g2;    // the two GEMMs (dense mode, as the two-launch form)
+    int32_t* sched;   // [0] claim counter, [1 + e] ready arrivals of expert e (zero at launch)
+    int T, n1, n2, mt1, mt2;
+};
+
+constexpr int kRing = 4;  // claimed items in flight between the roles
+
+struct DenseCfg {
+    using C = Cfg<64, 8, false>;  // 8 stages of a 128 x 64 weight box + two 32 x 64 token boxes
+    static constexpr int STAGES = 8;
+    static constexpr int OFF_RING = C::OFF_MISC + 16;          // ring: kRing ints
+    static constexpr int OFF_RBARS = OFF_RING + kRing * 4;     // kRing full + kRing empty barriers
+    static constexpr int SMEM = OFF_RBARS + 2 * kRing * 8 + 1023;
+    static_assert(OFF_RBARS % 8 == 0, "barrier alignment");
+    static_assert(SMEM <= 232448, "shared memory budget");
+};
+
+__device__ __forceinline__ int ld_acquire_gpu(const int32_t* p) {
+    int v;
+    asm volatile("ld.acquire.gpu.global.b32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+    return v;
+}
+
+__global__ void __launch_bounds__(kThreads, 1)
+dense_ffn_kernel(const __grid_constant__ CUtensorMap tmA1, const __grid_constant__ CUtensorMap tmB1,
+                 const __grid_constant__ CUtensorMap tmA2, const __grid_constant__ CUtensorMap tmB2,
+                 const DenseFfn f) {
+    using C = DenseCfg::C;
+    constexpr int STAGES = DenseCfg::STAGES;
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t* smem = reinterpret_cast<uint8_t*>(
+        (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    uint64_t* full = reinterpret_cast<uint64_t*>(smem + C::OFF_BARS);
+    uint64_t* empty = full + STAGES;
+    uint64_t* tfull = empty + STAGES;
+    uint64_t* tempty = tfull + 2;
+    uint64_t* drain = tempty + 2;
+    uint32_t* s_tmem = reinterpret_cast<uint32_t*>(smem + C::OFF_MISC);
+    volatile int* s_abort = reinterpret_cast<volatile int*>(smem + C::OFF_MISC + 4);
+    volatile int* ring = reinterpret_cast<volatile int*>(smem + DenseCfg::OFF_RING);
+    uint64_t* rfull = reinterpret_cast<uint64_t*>(smem + DenseCfg::OFF_RBARS);
+    uint64_t* rempty = rfull + kRing;
+    const Params& P = f.g1;  // error record and time limit
+
+    const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
+    const int total = f.n1 + f.n2;
+    const int nb = (f.T + BOX_ROWS - 1) / BOX_ROWS;
+    const uint32_t bytes = A_BYTES + nb * BOX_BYTES;
+    if (warp == 0 && lane == 0) {
+        for (int s = 0; s < STAGES; ++s) {
+            tc::mbar_init(&full[s], 1);
+            tc::mbar_init(&empty[s], 1);
+        }
+        for (int a = 0; a < 2; ++a) {
+            tc::mbar_init(&tfull[a], 1);
+            tc::mbar_init(&tempty[a], kEpiWarps);
+        }
+        for (int r = 0; r < kRing; ++r) {
+            tc::mbar_init(&rfull[r], 1);
+            tc::mbar_init(&rempty[r], 1 + kEpiWarps);
+        }
+        tc::mbar_init(drain, 1);
+        *s_abort = 0;
+        tc::fence_barrier_init();
+        tc::tma_prefetch_desc(&tmA1);
+        tc::tma_prefetch_desc(&tmB1);
+        tc::tma_prefetch_desc(&tmA2);
+        tc::tma_prefetch_desc(&tmB2);
+    }
+    if (warp == 2) {
+        tc::tmem_alloc(s_tmem, C::TMEM_COLS);
+        tc::tmem_relinquish();
+    }
+    pdl_trigger();  // the inputs are the layer's: nothing to wait for before starting
+    tc::fence_before_sync();
+    __syncthreads();
+    tc::fence_after_sync();
+    const uint32_t tmem_base = *s_tmem;
+
+    if (warp == 0) {
+        // ------------------------------------------------ claims + TMA producer
+        if (lane == 0) {
+            int stage = 0, slot = 0;
+            uint32_t phase = 0, rphase = 0;
+            long long fills = 0;
+            bool ok = true;
+            while (ok) {
+                const int item = atomicAdd(f.sched, 1);
+                const int it = item < total ? item : -1;
+                if (!wait_bar(&rempty[slot], rphase ^ 1, s_abort, P, 5)) break;
+                ring[slot] = it;
+                asm volatile("mbarrier.arrive.release.cta.shared::cta.b64 _, [%0];" ::"r"(
+                                 tc::smem_u32(&rfull[slot]))
+                             : "memory");
+                if (++slot == kRing) { slot = 0; rphase ^= 1; }
+                if (it < 0) break;
+                const bool first = it < f.n1;
+                const int e = first ? it / f.mt1 : (it - f.n1) / f.mt2;
+                const int m0 = (first ? it % f.mt1 : (it - f.n1) % f.mt2) * BM;
+                const CUtensorMap* tA = first ? &tmA1 : &tmA2;
+                const CUtensorMap* tB = first ? &tmB1 : &tmB2;
+                const int KB = ((first ? f.g1.K : f.g2.K) + BK - 1) / BK;
+                const int arow = e * (first ? f.g1.n_out : f.g2.n_out) + m0;
+                const int brow = first ? 0 : e * f.T;
+                // a second-GEMM item issues up to STAGES weight boxes before it
+                // waits for its expert's rows of h_all, then their token boxes
+                int deferred = 0;
+                const int target = kEpiWarps * f.mt1;
+                bool ready = first || ld_acquire_gpu(f.sched + 1 + e) >= target;
+                if (!first && ready) asm volatile("fence.proxy.async.global;" ::: "memory");
+                for (int kb = 0; kb < KB && ok; ++kb) {
+                    if (!ready && (deferred == STAGES || ld_acquire_gpu(f.sched + 1 + e) >= target)) {
+                        const uint64_t t0 = tc::globaltimer();
+                        while (ld_acquire_gpu(f.sched + 1 + e) < target) {
+                            if (*s_abort) { ok = false; break; }
+                            if (tc::globaltimer() - t0 > P.timeout_ns) {
+                                *s_abort = 1;
+                                record_error(P.hdr, kErrTimeout, 6);
+                                ok = false;
+                                break;
+                            }
+                        }
+                        if (!ok) break;
+                        asm volatile("fence.proxy.async.global;" ::: "memory");
+                        ready = true;
+                        for (int q = 0; q < deferred; ++q) {
+                            const int kq = kb - deferred + q;
+                            const int sq = (int)((fills - deferred + q) % STAGES);
+                            uint8_t* sb = smem + sq * C::STAGE_BYTES + A_BYTES;
+                            for (int b = 0; b < nb; ++b)
+                                tc::tma_load_2d(sb + b * BOX_BYTES, tB, &full[sq], kq * BK,
+                                                brow + b * BOX_ROWS);
+                        }
+                        deferred = 0;
+                    }
+                    if (!wait_bar(&empty[stage], phase ^ 1, s_abort, P, 1)) { ok = false; break; }
+                    tc::mbar_expect_tx(&full[stage], bytes);
+                    uint8_t* sa = smem + stage * C::STAGE_BYTES;
+                    tc::tma_load_2d(sa, tA, &full[stage], kb * BK, arow);
+                    if (ready) {
+                        for (int b = 0; b < nb; ++b)
+                            tc::tma_load_2d(sa + A_BYTES + b * BOX_BYTES, tB, &full[stage], kb * BK,
+                                            brow + b * BOX_ROWS);
+                    } else {
+                        ++deferred;
+                    }
+                    ++fills;
+                    if (++stage == STAGES) { stage = 0; phase ^= 1; }
+                }
+                if (ok && !ready) {  // a short item: every K step deferred
+                    const uint64_t t0 = tc::globaltimer();
+                    while (ld_acquire_gpu(f.sched + 1 + e) < target) {
+                        if (*s_abort || tc::globaltimer() - t0 > P.timeout_ns) {
+                            if (!*s_abort) record_error(P.hdr, kErrTimeout, 6);
+                            *s_abort = 1;
+                            ok = false;
+                            break;
+                        }
+                    }
+                    if (ok) {
+                        asm volatile("fence.proxy.async.global;" ::: "memory");
+                        for (int q = 0; q < deferred; ++q) {
+                            const int kq = KB - deferred + q;
+                            const int sq = (int)((fills - deferred + q) % STAGES);
+                            uint8_t* sb = smem + sq * C::STAGE_BYTES + A_BYTES;
+                            for (int b = 0; b < nb; ++b)
+                                tc::tma_load_2d(sb + b * BOX_BYTES, tB, &full[sq], kq * BK,
+                                                brow + b * BOX_ROWS);
+                        }
+                    }
+                }
+            }
+            // every issued copy lands before the CTA can exit
+            const long long last = fills < STAGES ? fills : STAGES;
+            for (long long i = fills - last; i < fills; ++i)
+                drain_bar(&full[i % STAGES], (uint32_t)((i / STAGES) & 1));
+        }
+    } else if (warp == 1) {
+        // ------------------------------------------------ MMA issuer
+        if (lane == 0) {
+            int stage = 0, acc = 0, slot = 0;
+            uint32_t phase = 0, acc_phase = 0, rphase = 0;
+            const uint32_t idesc = tc::idesc_bf16_f32(BM, (uint32_t)((f.T + 15) / 16) * 16);
+            bool ok = true;
+            while (ok) {
+                if (!wait_bar(&rfull[slot], rphase, s_abort, P, 7)) break;
+                const int it = ring[slot];
+                tc::mbar_arrive_relaxed(&rempty[slot]);
+                if (++slot == kRing) { slot = 0; rphase ^= 1; }
+                if (it < 0) break;
+                const int KB = ((it < f.n1 ? f.g1.K : f.g2.K) + BK - 1) / BK;
+                if (!wait_bar(&tempty[acc], acc_phase ^ 1, s_abort, P, 2)) break;
+                tc::fence_after_sync();
+                const uint32_t d_tmem = tmem_base + (uint32_t)(acc * 64);
+                for (int kb = 0; kb < KB; ++kb) {
+                    if (!wait_bar(&full[stage], phase, s_abort, P, 3)) { ok = false; break; }
+                    tc::fence_after_sync();
+                    const uint32_t sa = tc::smem_u32(smem + stage * C::STAGE_BYTES);
+                    const uint32_t sb = sa + A_BYTES;
+#pragma unroll
+                    for (int kk = 0; kk < BK / 16; ++kk)
+                        tc::mma_bf16(d_tmem, tc::sdesc_k128_sw128(sa + kk * 32),
+                                     tc::sdesc_k128_sw128(sb + kk * 32), idesc,
+                                     (kb | kk) != 0 ? 1u : 0u);
+                    tc::mma_commit(&empty[stage]);
+                    if (++stage == STAGES) { stage = 0; phase ^= 1; }
+                }
+                if (!ok) break;
+                tc::mma_commit(&tfull[acc]);
+                acc ^= 1;
+                if (acc == 0) acc_phase ^= 1;
+            }
+            tc::mma_commit(drain);
+            drain_bar(drain, 0);
+        }
+    } else if (warp >= 4) {
+        // ------------------------------------------------ epilogue
+        const int ew = warp - 4;
+        const int q = warp & 3;
+        const int half = ew >> 2;
+        uint8_t* stg = smem + C::OFF_STAGING + ew * 32 * 32 * C::OUT_ES;
+        int acc = 0, slot = 0;
+        uint32_t acc_phase = 0, rphase = 0;
+        while (true) {
+            const bool okr = wait_bar(&rfull[slot], rphase, s_abort, P, 8);
+            if (!__all_sync(0xffffffffu, okr)) break;
+            const int it = ring[slot];
+            __syncwarp();
+            if (lane == 0) tc::mbar_arrive_relaxed(&rempty[slot]);
+            if (++slot == kRing) { slot = 0; rphase ^= 1; }
+            if (it < 0) break;
+            const bool ok = wait_bar(&tfull[acc], acc_phase, s_abort, P, 4);
+            if (!__all_sync(0xffffffffu, ok)) break;
+            tc::fence_after_sync();
+            if (it < f.n1) {
+                const int e = it / f.mt1;
+                epilogue_tile<64, true>(f.g1, e, 0, e * f.T, f.T, (it % f.mt1) * BM, tmem_base,
+                                        acc * 64, q, half, 2, lane, stg);
+                // this warp's rows of h_all are stored: count them for expert e
+                __threadfence();
+                __syncwarp();
+                if (lane == 0) atomicAdd(f.sched + 1 + e, 1);
+            } else {
+                const int e = (it - f.n1) / f.mt2;
+                epilogue_tile<64, false>(f.g2, e, e * f.T, e * f.T, f.T, ((it - f.n1) % f.mt2) * BM,
+                                         tmem_base, acc * 64, q, half, 2, lane, stg);
+            }
+            tc::fence_before_sync();
+            __syncwarp();
+            if (lane == 0) tc::mbar_arrive_relaxed(&tempty[acc]);
+            acc ^= 1;
+            if (acc == 0) acc_phase ^= 1;
+        }
+    }
+
+    tc::fence_before_sync();
+    __syncthreads();
+    if (warp == 2) {
+        tc::fence_after_sync();
+        tc::tmem_dealloc(tmem_base, C::TMEM_COLS);
+    }
+    // the grid completes only after the previous kernel of its chain (the
+    // router), which it never waited for
+    if (threadIdx.x == 0) pdl_wait();
 }
 
 // First-GEMM epilogue of the CTA-pair kernel for this CTA's 128 weight rows x
@@ -549,6 +883,7 @@ __device__ __forceinline__ Tile decode_pair_tile(int t, const int* s_tiles, cons
     Tile tl;
     tl.e = lo;
     tl.r0 = s0 + (local % nt) * BN2;
+    tl.o0 = tl.r0;
     tl.n = min(BN2, s1 - tl.r0);
     tl.m0 = (local / nt) * 2 * BM;
     return tl;
@@ -721,8 +1056,8 @@ grouped_gemm_pair(const __grid_constant__ CUtensorMap tmA, const __grid_constant
                 epilogue_gelu<EW / 4>(p, tl.e, tl.r0, tl.n, m0 + rank * BM, tmem_base, acc * BN2,
                                       q, part, lane, stg, &tmO);
             else
-                epilogue_tile<BN2, GEMM1>(p, tl.e, tl.r0, tl.n, m0 + rank * BM, tmem_base, acc * BN2,
-                                      q, part, EW / 4, lane, stg, &tmO,
+                epilogue_tile<BN2, GEMM1>(p, tl.e, tl.r0, tl.r0, tl.n, m0 + rank * BM, tmem_base,
+                                      acc * BN2, q, part, EW / 4, lane, stg, &tmO,
                                       p.koff != nullptr && seg_rows(p, tl.e) == 0);
             tc::fence_before_sync();
             __syncwarp();
@@ -914,6 +1249,62 @@ cudaError_t launch_expert_ffn_tc(const moe_config& c, const void* x_perm, int64_
         return launch_one_pair<3, false, 8, 2>(pm[2], pm[3], pm[5], p2, s);
     }
     return launch_pair<64, 8>(maps, p1, p2, s);
+}
+
+// Dense expert FFN of a decode-sized batch (single-CTA kernel, T <= 64):
+// every expert on all T tokens.  First GEMM: h_all[e*T + t] = GELU(x[t]
+// W1_e^T + b1_e) (bf16); second: y_all[e*T + t] = h_all[e*T + t] W2_e^T +
+// b2_e (fp32, no routing weight).  Each output row is the sparse path's
+// row for that (expert, token) to the bit: the MMA's rows are independent.
+cudaError_t launch_dense_gemm1(const moe_config& c, const void* x, const void* W1, const void* b1,
+                               void* h_all, DeviceHeader* hdr, cudaStream_t s) {
+    CUtensorMap ma, mb;
+    if (!make_map(&ma, W1, c.d, (uint64_t)c.E * c.d_ff, BM) ||
+        !make_map(&mb, x, c.d, (uint64_t)c.T, BOX_ROWS))
+        return cudaErrorInvalidValue;
+    Params p{nullptr, reinterpret_cast<const __nv_bfloat16*>(b1), nullptr, h_all, hdr,
+             g_tc_timeout_ns, c.E, c.d_ff, c.d, c.E * c.T, 1, nullptr, 0, c.T, 1};
+    return launch_one<64, 8, true>(ma, mb, p, s);
+}
+
+cudaError_t launch_dense_gemm2(const moe_config& c, const void* h_all, const void* W2,
+                               const void* b2, float* y_all, DeviceHeader* hdr, cudaStream_t s) {
+    CUtensorMap ma, mb;
+    if (!make_map(&ma, W2, c.d_ff, (uint64_t)c.E * c.d, BM) ||
+        !make_map(&mb, h_all, c.d_ff, (uint64_t)c.E * c.T, BOX_ROWS))
+        return cudaErrorInvalidValue;
+    Params p{nullptr, reinterpret_cast<const __nv_bfloat16*>(b2), nullptr, y_all, hdr,
+             g_tc_timeout_ns, c.E, c.d, c.d_ff, c.E * c.T, 0, nullptr, 0, c.T, 0};
+    return launch_one<64, 8, false>(ma, mb, p, s);
+}
+
+// Both GEMMs of the dense decode FFN in one persistent launch
+// (dense_ffn_kernel).  sched: 1 + E int32 in the workspace, zero at launch.
+cudaError_t launch_dense_ffn(const moe_config& c, const void* x, const void* W1, const void* b1,
+                             const void* W2, const void* b2, void* h_all, float* y_all,
+                             int32_t* sched, DeviceHeader* hdr, cudaStream_t s) {
+    CUtensorMap a1, bx, a2, bh;
+    if (!make_map(&a1, W1, c.d, (uint64_t)c.E * c.d_ff, BM) ||
+        !make_map(&bx, x, c.d, (uint64_t)c.T, BOX_ROWS) ||
+        !make_map(&a2, W2, c.d_ff, (uint64_t)c.E * c.d, BM) ||
+        !make_map(&bh, h_all, c.d_ff, (uint64_t)c.E * c.T, BOX_ROWS))
+        return cudaErrorInvalidValue;
+    DenseFfn f;
+    f.g1 = Params{nullptr, reinterpret_cast<const __nv_bfloat16*>(b1), nullptr, h_all, hdr,
+                  g_tc_timeout_ns, c.E, c.d_ff, c.d, c.E * c.T, 1, nullptr, 0, c.T, 1};
+    f.g2 = Params{nullptr, reinterpret_cast<const __nv_bfloat16*>(b2), nullptr, y_all, hdr,
+                  g_tc_timeout_ns, c.E, c.d, c.d_ff, c.E * c.T, 0, nullptr, 0, c.T, 0};
+    f.sched = sched;
+    f.T = c.T;
+    f.mt1 = (c.d_ff + BM - 1) / BM;
+    f.mt2 = (c.d + BM - 1) / BM;
+    f.n1 = c.E * f.mt1;
+    f.n2 = c.E * f.mt2;
+    constexpr auto kern = dense_ffn_kernel;
+    cudaError_t err = ensure_smem<kern>(DenseCfg::SMEM);
+    if (err != cudaSuccess) return err;
+    return launch_kernel(kern, dim3(num_sms()), dim3(kThreads), DenseCfg::SMEM, s, 1, true, a1, bx,
+                         a2, bh, f);
 }
 
 // One grouped GEMM out[r][n] = sum_k A[r][k] W_e[n][k] (+ bias_e[n]) over the

@@ -17,8 +17,27 @@ void count_launches(int n) { g_launches.fetch_add((uint64_t)n, std::memory_order
 
 // Position of the next launch in the calling thread's current chain.
 static thread_local int t_chain_pos = 0;
+static thread_local bool t_chain_all = false;
 void chain_begin() { t_chain_pos = 0; }
 bool chain_next() { return t_chain_pos++ > 0; }
+bool chain_all_programmatic() { return t_chain_all; }
+ChainProgrammatic::ChainProgrammatic() { t_chain_all = true; }
+ChainProgrammatic::~ChainProgrammatic() { t_chain_all = false; }
+
+// A decode-sized batch streams every expert's weights whichever tokens reach
+// them, so moe_forward evaluates every expert on all T tokens (the extra
+// tensor-core work is hidden under the weight stream) and applies the routing
+// in the combine: the GEMMs then wait for no routing step.  Chosen for bf16
+// token-choice layers that drop on overflow, without shared experts, with
+// T <= 64 (one token tile per expert in the single-CTA GEMM kernel, which the
+// layer uses when T k < 96 E) and T k >= 4 E (each expert is expected to get
+// four or more assignments, so hardly any expert's weights are streamed for
+// nothing).
+bool dense_decode(const moe_config& c) {
+    return c.dtype == MOE_BF16 && c.routing == MOE_TOKEN_CHOICE && c.overflow == MOE_DROP &&
+           c.n_shared == 0 && c.T > 0 && c.T <= 64 && (int64_t)c.T * c.k < 96LL * c.E &&
+           (int64_t)c.T * c.k >= 4LL * c.E;
+}
 
 int num_sms() {
     static int sms[64] = {0};
@@ -168,6 +187,7 @@ WsLayout ws_layout(const moe_config& c) {
     L.header = take(sizeof(DeviceHeader));
     L.counts = take(sizeof(int32_t) * c.E);
     L.top1 = take(sizeof(int32_t) * c.E);
+    L.sched = take(sizeof(int32_t) * (1 + c.E));  // zeroed with the counts (same memset)
     L.blk_p = take(sizeof(float) * (size_t)L.route.blocks * cr.E);
     L.blk_z = take(sizeof(float) * (size_t)L.route.blocks);
     L.blk_hist = take(sizeof(int32_t) * (size_t)L.hist_blocks * c.E);
@@ -184,9 +204,12 @@ WsLayout ws_layout(const moe_config& c) {
     L.slot_of = take(sizeof(int32_t) * (size_t)slots);
     L.perm_token = take(sizeof(int32_t) * (size_t)perm);
     L.perm_w = take(sizeof(float) * (size_t)perm);
+    // the dense decode path keeps every expert's rows for all T tokens in h and y_perm
+    const int64_t frows = dense_decode(c) && (int64_t)c.E * c.T > L.rows ? (int64_t)c.E * c.T
+                                                                        : L.rows;
     L.x_perm = take(es * (size_t)L.rows * c.d);
-    L.h = take(es * (size_t)L.rows * c.d_ff);
-    L.y_perm = take(sizeof(float) * (size_t)L.rows * c.d);
+    L.h = take(es * (size_t)frows * c.d_ff);
+    L.y_perm = take(sizeof(float) * (size_t)frows * c.d);
     L.probs_t = take(ec ? sizeof(float) * (size_t)c.E * c.T : 0);
     const bool rr = rerouting(c);
     L.rr_hist = take(rr ? sizeof(int32_t) * (size_t)L.count_blocks * c.E : 0);
@@ -387,6 +410,30 @@ moe_status moe_forward(const moe_config* cfg, const void* x, const float* W_r,
             e = launch_expert_ffn(c, x_perm, L.rows, offsets, W1, b1, W2, b2, perm_w, y_perm, ws,
                                   L, s);
         if (e == cudaSuccess) e = launch_combine(combine_config(c), y_perm, slot_of, y, L.rows, s);
+        return from_cuda(e);
+    }
+    if (dense_decode(c)) {
+        // every expert on all T tokens: the router, then both expert GEMMs in
+        // one persistent kernel that starts beside it (the GEMMs read only the
+        // layer's inputs), then the combine, which applies the routing
+        // weights and drops and finishes the loss.  The counters (router
+        // counts, the FFN's work-item and ready counters) start at zero.
+        if (cudaMemsetAsync(at<char>(ws, L.counts), 0, L.blk_p - L.counts, s) != cudaSuccess)
+            return MOE_ERR_CUDA;
+        DeviceHeader* hdr = at<DeviceHeader>(ws, L.header);
+        chain_begin();
+        ChainProgrammatic pdl_chain;
+        cudaError_t e = launch_route_inputs_only(c, x, W_r, logit_bias, logit_noise, logits_out,
+                                                 idx, w, ws, L, s);
+        if (e == cudaSuccess)
+            e = launch_dense_ffn(c, x, W1, b1, W2, b2, at<void>(ws, L.h), y_perm,
+                                 at<int32_t>(ws, L.sched), hdr, s);
+        if (e == cudaSuccess)
+            e = launch_dense_combine(c, y_perm, idx, w, y, hdr,
+                                     route_loss_args(c, ws, L, expert_counts, aux_out, z_loss_out),
+                                     expert_counts != nullptr || aux_out != nullptr ||
+                                         z_loss_out != nullptr,
+                                     s);
         return from_cuda(e);
     }
     chain_begin();

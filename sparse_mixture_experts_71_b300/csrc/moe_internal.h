@@ -60,6 +60,7 @@ struct WsLayout {
     size_t header;       // DeviceHeader
     size_t counts;       // int32 [E]   assignments per expert (all slots)
     size_t top1;         // int32 [E]   first-slot choices per expert
+    size_t sched;        // int32 [1+E] work-item counter and per-expert ready counts (dense decode FFN)
     size_t blk_p;        // fp32 [route.blocks][E] per-block sums of p
     size_t blk_z;        // fp32 [route.blocks] per-block sums of the squared log-sum-exp
     size_t blk_hist;     // int32 [hist_blocks][E]
@@ -127,6 +128,13 @@ cudaError_t ensure_smem(int bytes) {
 // next launch may use the attribute and advances the chain.
 void chain_begin();
 bool chain_next();
+// While set (ChainProgrammatic), every launch after the first of the chain
+// uses programmatic stream serialization, the SIMT kernels' included.
+bool chain_all_programmatic();
+struct ChainProgrammatic {
+    ChainProgrammatic();
+    ~ChainProgrammatic();
+};
 
 // Launch `kern` on stream s; cluster > 1 launches clusters of that many
 // blocks along x.  `programmatic` lets the launch use programmatic stream
@@ -151,7 +159,7 @@ cudaError_t launch_kernel(void (*kern)(KArgs...), dim3 grid, dim3 block, size_t 
         attr[n].val.clusterDim.z = 1;
         ++n;
     }
-    if (chain_next() && programmatic) {
+    if (chain_next() && (programmatic || chain_all_programmatic())) {
         attr[n].id = cudaLaunchAttributeProgrammaticStreamSerialization;
         attr[n].val.programmaticStreamSerializationAllowed = 1;
         ++n;
@@ -249,6 +257,28 @@ cudaError_t launch_scan_permute(const moe_config& c, const void* x, const int32_
 // Loss inputs/outputs of the router's per-block statistics in workspace ws.
 LossArgs route_loss_args(const moe_config& c, void* ws, const WsLayout& L,
                          int32_t* expert_counts, float* aux_out, float* z_loss_out);
+
+// Decode-sized layers that stream every expert's weights (dense_decode):
+// moe_forward evaluates every expert on all T tokens, so the expert GEMMs do
+// not depend on the routing (gemm_tc.cu, combine.cu, route.cu).
+bool dense_decode(const moe_config& c);
+cudaError_t launch_dense_ffn(const moe_config& c, const void* x, const void* W1, const void* b1,
+                             const void* W2, const void* b2, void* h_all, float* y_all,
+                             int32_t* sched, DeviceHeader* hdr, cudaStream_t s);
+cudaError_t launch_dense_gemm1(const moe_config& c, const void* x, const void* W1, const void* b1,
+                               void* h_all, DeviceHeader* hdr, cudaStream_t s);
+cudaError_t launch_dense_gemm2(const moe_config& c, const void* h_all, const void* W2,
+                               const void* b2, float* y_all, DeviceHeader* hdr, cudaStream_t s);
+cudaError_t launch_dense_combine(const moe_config& c, const float* y_all, const int32_t* idx,
+                                 const float* w, void* y, DeviceHeader* hdr, const LossArgs& loss,
+                                 bool do_loss, cudaStream_t s);
+// The router on the layer's inputs only, with no memset and no finishing
+// kernel: it starts beside the previous kernel of its chain and waits for it
+// before exiting (SIMT router kernels only).
+cudaError_t launch_route_inputs_only(const moe_config& c, const void* x, const float* W_r,
+                                     const float* logit_bias, const float* logit_noise,
+                                     float* logits_out, int32_t* topk_idx, float* topk_w,
+                                     void* ws, const WsLayout& L, cudaStream_t s);
 
 cudaError_t launch_expert_ffn(const moe_config& c, const void* x_perm, int64_t x_rows,
                               const int32_t* offsets, const void* W1, const void* b1,

@@ -43,8 +43,7 @@ using namespace rt;
 // are added in split order.
 template <typename TX, int EMAX, int TW, int DS>
 __global__ void __launch_bounds__(kThreads) route_warp_kernel(RouteArgs a) {
-    pdl_wait();
-    pdl_trigger();
+    route_begin(a);
     constexpr int G = kWarps / DS;   // token groups per block
     constexpr int TB = G * TW;       // tokens per block
     constexpr int LDS = EMAX + 1;
@@ -149,6 +148,7 @@ __global__ void __launch_bounds__(kThreads) route_warp_kernel(RouteArgs a) {
     if (tid < TB) token_epilogue<EMAX>(a, s_p + tid * LDS, blockIdx.x * TB + tid, tid, s_idx, s_cnt, s_top1);
     __syncthreads();
     finish_block<EMAX>(a, s_p, LDS, TB, s_idx, s_cnt, s_top1, wh, carry);
+    route_end(a);
 }
 
 // ===================================================================== tensor-core kernel
@@ -196,8 +196,7 @@ __device__ __forceinline__ void mma_bf16_16816(float (&d)[4], uint32_t a0, uint3
 
 template <int NT, int MT>
 __global__ void __launch_bounds__(kThreads) route_mma_kernel(RouteArgs a) {
-    pdl_wait();
-    pdl_trigger();
+    route_begin(a);
     constexpr int EMAX = 8 * NT;
     constexpr int DS = kWarps / MT;
     constexpr int TB = 16 * MT;
@@ -310,6 +309,7 @@ __global__ void __launch_bounds__(kThreads) route_mma_kernel(RouteArgs a) {
     if (tid < TB) token_epilogue<EMAX>(a, s_buf + tid * LDS, blockIdx.x * TB + tid, tid, s_idx, s_cnt, s_top1);
     __syncthreads();
     finish_block<EMAX>(a, s_buf, LDS, TB, s_idx, s_cnt, s_top1, wh, carry);
+    route_end(a);
 }
 
 // ===================================================================== tile kernel
@@ -370,8 +370,7 @@ __device__ __forceinline__ void stage_chunk(const RouteArgs& a, int t0, int c0, 
 
 template <typename TX, int EMAX>
 __global__ void __launch_bounds__(kThreads) route_tile_kernel(RouteArgs a) {
-    pdl_wait();
-    pdl_trigger();
+    route_begin(a);
     using Gm = Geo<EMAX>;
     extern __shared__ float4 smem_f4[];
     float* smem = reinterpret_cast<float*>(smem_f4);
@@ -548,6 +547,7 @@ __global__ void __launch_bounds__(kThreads) route_tile_kernel(RouteArgs a) {
     }
     __syncthreads();
     finish_block<EMAX>(a, lg, Gm::LGS, Gm::TB, s_idx, s_cnt, s_top1, wh, carry);
+    route_end(a);
 }
 
 template <typename TX, int EMAX>
@@ -738,12 +738,13 @@ RouteGeom route_geom(const moe_config& c) {
     return g;
 }
 
-cudaError_t launch_route(const moe_config& c, const void* x, const float* W_r,
-                         const float* logit_bias, const float* logit_noise,
-                         const float* logits_in, float* logits_out,
-                         int32_t* topk_idx, float* topk_w, int32_t* expert_counts,
-                         float* aux_out, float* z_loss_out, void* ws, const WsLayout& L,
-                         bool fuse_count, cudaStream_t s, float* probs_t, int knorm) {
+namespace {
+
+RouteArgs route_args(const moe_config& c, const void* x, const float* W_r,
+                     const float* logit_bias, const float* logit_noise, const float* logits_in,
+                     float* logits_out, int32_t* topk_idx, float* topk_w,
+                     int32_t* expert_counts, float* aux_out, void* ws, const WsLayout& L,
+                     bool fuse_count, float* probs_t, int knorm) {
     RouteArgs a;
     a.probs_t = probs_t;
     a.knorm = knorm > 0 ? knorm : c.k;
@@ -759,24 +760,53 @@ cudaError_t launch_route(const moe_config& c, const void* x, const float* W_r,
     a.local_rank = at<int32_t>(ws, L.local_rank);
     a.T = c.T; a.d = c.d; a.E = c.E; a.k = c.k; a.renormalize = c.renormalize;
     a.nblk = L.route.blocks;
+    a.late_wait = 0;
+    return a;
+}
+
+cudaError_t route_kernels(const moe_config& c, const RouteArgs& a, void* ws, const WsLayout& L,
+                          cudaStream_t s) {
+    if (L.route.mma) return launch_mma(a, L.route, s);
+    if (L.route.tc) {
+        __nv_bfloat16* wsp = at<__nv_bfloat16>(ws, L.wsplit);
+        cudaError_t err = launch_split(a, L.route.epad, wsp, s);
+        return err == cudaSuccess ? launch_route_tc(a, wsp, L.route.epad, s) : err;
+    }
+    return c.dtype == MOE_BF16 ? launch_e<__nv_bfloat16>(a, L.route, s)
+                               : launch_e<float>(a, L.route, s);
+}
+
+}  // namespace
+
+cudaError_t launch_route(const moe_config& c, const void* x, const float* W_r,
+                         const float* logit_bias, const float* logit_noise,
+                         const float* logits_in, float* logits_out,
+                         int32_t* topk_idx, float* topk_w, int32_t* expert_counts,
+                         float* aux_out, float* z_loss_out, void* ws, const WsLayout& L,
+                         bool fuse_count, cudaStream_t s, float* probs_t, int knorm) {
+    const RouteArgs a = route_args(c, x, W_r, logit_bias, logit_noise, logits_in, logits_out,
+                                   topk_idx, topk_w, expert_counts, aux_out, ws, L, fuse_count,
+                                   probs_t, knorm);
     // per-call counters: the two count arrays start at zero
     cudaError_t err = cudaMemsetAsync(at<char>(ws, L.counts), 0, L.blk_p - L.counts, s);
     if (err != cudaSuccess) return err;
     chain_begin();  // the next kernel follows the memset
-    if (L.route.mma) {
-        err = launch_mma(a, L.route, s);
-    } else if (L.route.tc) {
-        __nv_bfloat16* wsp = at<__nv_bfloat16>(ws, L.wsplit);
-        err = launch_split(a, L.route.epad, wsp, s);
-        if (err == cudaSuccess) err = launch_route_tc(a, wsp, L.route.epad, s);
-    } else {
-        err = c.dtype == MOE_BF16 ? launch_e<__nv_bfloat16>(a, L.route, s)
-                                  : launch_e<float>(a, L.route, s);
-    }
+    err = route_kernels(c, a, ws, L, s);
     if (err != cudaSuccess || fuse_count) return err;
     if (expert_counts == nullptr && aux_out == nullptr && z_loss_out == nullptr) return err;
     return launch_kernel(route_finish_kernel, dim3(1), dim3(256), 0, s, 1, false,
                          route_loss_args(c, ws, L, expert_counts, aux_out, z_loss_out));
+}
+
+cudaError_t launch_route_inputs_only(const moe_config& c, const void* x, const float* W_r,
+                                     const float* logit_bias, const float* logit_noise,
+                                     float* logits_out, int32_t* topk_idx, float* topk_w,
+                                     void* ws, const WsLayout& L, cudaStream_t s) {
+    if (L.route.mma || L.route.tc) return cudaErrorInvalidValue;  // SIMT router kernels only
+    RouteArgs a = route_args(c, x, W_r, logit_bias, logit_noise, nullptr, logits_out, topk_idx,
+                             topk_w, nullptr, nullptr, ws, L, false, nullptr, 0);
+    a.late_wait = 1;
+    return route_kernels(c, a, ws, L, s);
 }
 
 }  // namespace moe
