@@ -96,20 +96,10 @@ struct Params {
     // zeros.
     const int32_t* koff;
     int tok_rows;
-    // Dense mode (single-CTA kernel, dense_T > 0): every expert e takes
-    // dense_T rows - input rows [0, dense_T) of the token operand when
-    // dense_shared_in (the layer input, shared by all experts), else rows
-    // e*dense_T .. - and writes output rows e*dense_T + j; offsets unused.
-    // With dense_shared_in the kernel reads only the layer's inputs, so it
-    // does not wait for the previous kernel of its chain before starting; the
-    // other dense GEMM loads its first weight stages before that wait.
-    int dense_T;
-    int dense_shared_in;
 };
 
 // Rows of an expert's segment (offsets clamped to the buffers).
 __device__ __forceinline__ int seg_rows(const Params& p, int e) {
-    if (p.dense_T > 0) return p.dense_T;
     const int s0 = min(max(__ldg(p.offsets + e), 0), p.rows_cap);
     const int s1 = min(max(__ldg(p.offsets + e + 1), s0), p.rows_cap);
     return s1 - s0;
@@ -133,20 +123,12 @@ __device__ __forceinline__ Tile decode_tile(int t, const int* s_tiles, const Par
     Tile tl;
     tl.e = lo;
     const int local = t - s_tiles[lo];
-    int s0, s1, ob;
-    if (p.dense_T > 0) {
-        s0 = p.dense_shared_in ? 0 : lo * p.dense_T;
-        s1 = s0 + p.dense_T;
-        ob = lo * p.dense_T;
-    } else {
-        s0 = min(max(__ldg(p.offsets + lo), 0), p.rows_cap);
-        s1 = min(max(__ldg(p.offsets + lo + 1), s0), p.rows_cap);
-        ob = s0;
-    }
+    const int s0 = min(max(__ldg(p.offsets + lo), 0), p.rows_cap);
+    const int s1 = min(max(__ldg(p.offsets + lo + 1), s0), p.rows_cap);
     const int nt = (s1 - s0 + bn_max - 1) / bn_max;
     const int ti = local % nt, gi = local / nt;  // token tile fastest
     tl.r0 = s0 + ti * bn_max;
-    tl.o0 = ob + ti * bn_max;
+    tl.o0 = tl.r0;
     tl.n = min(bn_max, s1 - tl.r0);
     tl.m0 = gi * BM;
     return tl;
@@ -306,8 +288,7 @@ grouped_gemm_tc(const __grid_constant__ CUtensorMap tmA, const __grid_constant__
         tc::tmem_alloc(s_tmem, C::TMEM_COLS);
         tc::tmem_relinquish();
     }
-    const bool dense = p.dense_T > 0;
-    if (!dense) pdl_wait();  // offsets and the operands come from the previous kernel
+    pdl_wait();  // offsets and the operands come from the previous kernel
     pdl_trigger();
     if (warp == 3) {  // exclusive prefix of tiles per expert
         int run = 0;
@@ -341,37 +322,12 @@ grouped_gemm_tc(const __grid_constant__ CUtensorMap tmA, const __grid_constant__
             uint32_t phase = 0;
             long long fills = 0;
             bool ok = true;
-            int pre = 0;  // K steps of the first tile issued in the prologue
-            if (dense && !p.dense_shared_in) {
-                // the token operand comes from the previous kernel, the
-                // weights do not: the first stages' weight boxes are loaded
-                // before the wait, their token boxes after it
-                if (cta < total) {
-                    const Tile tl = decode_tile(cta, s_tiles, p, BN_MAX);
-                    const int nb = (tl.n + BOX_ROWS - 1) / BOX_ROWS;
-                    const uint32_t bytes = A_BYTES + nb * BOX_BYTES;
-                    const int arow = tl.e * p.n_out + tl.m0;
-                    pre = KB < STAGES ? KB : STAGES;
-                    for (int kb = 0; kb < pre; ++kb) {  // fresh stages: nothing to wait for
-                        tc::mbar_expect_tx(&full[kb], bytes);
-                        tc::tma_load_2d(smem + kb * C::STAGE_BYTES, &tmA, &full[kb], kb * BK, arow);
-                    }
-                    pdl_wait();
-                    for (int kb = 0; kb < pre; ++kb)
-                        for (int b = 0; b < nb; ++b)
-                            tc::tma_load_2d(smem + kb * C::STAGE_BYTES + A_BYTES + b * BOX_BYTES,
-                                            &tmB, &full[kb], kb * BK, tl.r0 + b * BOX_ROWS);
-                    fills = pre;
-                    stage = pre % STAGES;
-                    phase = pre == STAGES ? 1u : 0u;
-                }
-            }
             for (int t = cta; t < total && ok; t += nctas) {
                 const Tile tl = decode_tile(t, s_tiles, p, BN_MAX);
                 const int nb = (tl.n + BOX_ROWS - 1) / BOX_ROWS;
                 const uint32_t bytes = A_BYTES + nb * BOX_BYTES;
                 const int arow = tl.e * p.n_out + tl.m0;
-                for (int kb = t == cta ? pre : 0; kb < KB; ++kb) {
+                for (int kb = 0; kb < KB; ++kb) {
                     if (!wait_bar(&empty[stage], phase ^ 1, s_abort, p, 1)) { ok = false; break; }
                     tc::mbar_expect_tx(&full[stage], bytes);
                     uint8_t* sa = smem + stage * C::STAGE_BYTES;
@@ -454,14 +410,13 @@ grouped_gemm_tc(const __grid_constant__ CUtensorMap tmA, const __grid_constant__
         tc::fence_after_sync();
         tc::tmem_dealloc(tmem_base, C::TMEM_COLS);
     }
-    // dense mode: this grid completes only after the previous kernel of the
-    // chain (which the first dense GEMM never waited for)
-    if (dense && threadIdx.x == 0) pdl_wait();
 }
 
 // ===================================================================== dense decode FFN
-// Both expert GEMMs of a decode-sized batch in one persistent kernel (dense
-// mode: every expert on all T <= 64 tokens; see launch_dense_gemm1).  Work
+// Both expert GEMMs of a decode-sized batch in one persistent kernel, each
+// expert evaluated on all T <= 64 tokens (moe_forward's dense decode path;
+// every (expert, token) row equals the sparse path's: the MMA's rows are
+// independent).  Work
 // items 0 .. N1-1 are the first GEMM's 128-row weight tiles (expert
 // e = i / mt1: h_all[e*T + t] = GELU(x[t] W1_e^T + b1_e), bf16), items
 // N1 .. N1+N2-1 the second's (e = (i - N1) / mt2: y_all[e*T + t] =
@@ -476,7 +431,7 @@ grouped_gemm_tc(const __grid_constant__ CUtensorMap tmA, const __grid_constant__
 // A first-GEMM item never waits on anything but its own pipeline, so the
 // waits always end.
 struct DenseFfn {
-    Params g1, g2;    // the two GEMMs (dense mode, as the two-launch form)
+    Params g1, g2;    // the two GEMMs (bias, activation, output, sizes, error record)
     int32_t* sched;   // [0] claim counter, [1 + e] ready arrivals of expert e (zero at launch)
     int T, n1, n2, mt1, mt2;
 };
@@ -1251,33 +1206,6 @@ cudaError_t launch_expert_ffn_tc(const moe_config& c, const void* x_perm, int64_
     return launch_pair<64, 8>(maps, p1, p2, s);
 }
 
-// Dense expert FFN of a decode-sized batch (single-CTA kernel, T <= 64):
-// every expert on all T tokens.  First GEMM: h_all[e*T + t] = GELU(x[t]
-// W1_e^T + b1_e) (bf16); second: y_all[e*T + t] = h_all[e*T + t] W2_e^T +
-// b2_e (fp32, no routing weight).  Each output row is the sparse path's
-// row for that (expert, token) to the bit: the MMA's rows are independent.
-cudaError_t launch_dense_gemm1(const moe_config& c, const void* x, const void* W1, const void* b1,
-                               void* h_all, DeviceHeader* hdr, cudaStream_t s) {
-    CUtensorMap ma, mb;
-    if (!make_map(&ma, W1, c.d, (uint64_t)c.E * c.d_ff, BM) ||
-        !make_map(&mb, x, c.d, (uint64_t)c.T, BOX_ROWS))
-        return cudaErrorInvalidValue;
-    Params p{nullptr, reinterpret_cast<const __nv_bfloat16*>(b1), nullptr, h_all, hdr,
-             g_tc_timeout_ns, c.E, c.d_ff, c.d, c.E * c.T, 1, nullptr, 0, c.T, 1};
-    return launch_one<64, 8, true>(ma, mb, p, s);
-}
-
-cudaError_t launch_dense_gemm2(const moe_config& c, const void* h_all, const void* W2,
-                               const void* b2, float* y_all, DeviceHeader* hdr, cudaStream_t s) {
-    CUtensorMap ma, mb;
-    if (!make_map(&ma, W2, c.d_ff, (uint64_t)c.E * c.d, BM) ||
-        !make_map(&mb, h_all, c.d_ff, (uint64_t)c.E * c.T, BOX_ROWS))
-        return cudaErrorInvalidValue;
-    Params p{nullptr, reinterpret_cast<const __nv_bfloat16*>(b2), nullptr, y_all, hdr,
-             g_tc_timeout_ns, c.E, c.d, c.d_ff, c.E * c.T, 0, nullptr, 0, c.T, 0};
-    return launch_one<64, 8, false>(ma, mb, p, s);
-}
-
 // Both GEMMs of the dense decode FFN in one persistent launch
 // (dense_ffn_kernel).  sched: 1 + E int32 in the workspace, zero at launch.
 cudaError_t launch_dense_ffn(const moe_config& c, const void* x, const void* W1, const void* b1,
@@ -1291,9 +1219,9 @@ cudaError_t launch_dense_ffn(const moe_config& c, const void* x, const void* W1,
         return cudaErrorInvalidValue;
     DenseFfn f;
     f.g1 = Params{nullptr, reinterpret_cast<const __nv_bfloat16*>(b1), nullptr, h_all, hdr,
-                  g_tc_timeout_ns, c.E, c.d_ff, c.d, c.E * c.T, 1, nullptr, 0, c.T, 1};
+                  g_tc_timeout_ns, c.E, c.d_ff, c.d, c.E * c.T, 1, nullptr, 0};
     f.g2 = Params{nullptr, reinterpret_cast<const __nv_bfloat16*>(b2), nullptr, y_all, hdr,
-                  g_tc_timeout_ns, c.E, c.d, c.d_ff, c.E * c.T, 0, nullptr, 0, c.T, 0};
+                  g_tc_timeout_ns, c.E, c.d, c.d_ff, c.E * c.T, 0, nullptr, 0};
     f.sched = sched;
     f.T = c.T;
     f.mt1 = (c.d_ff + BM - 1) / BM;

@@ -423,8 +423,8 @@ moe_status moe_forward(const moe_config* cfg, const void* x, const float* W_r,
         DeviceHeader* hdr = at<DeviceHeader>(ws, L.header);
         chain_begin();
         ChainProgrammatic pdl_chain;
-        cudaError_t e = launch_route_inputs_only(c, x, W_r, logit_bias, logit_noise, logits_out,
-                                                 idx, w, ws, L, s);
+        cudaError_t e = launch_route_no_finish(c, x, W_r, logit_bias, logit_noise, logits_out, idx,
+                                               w, ws, L, s);
         if (e == cudaSuccess)
             e = launch_dense_ffn(c, x, W1, b1, W2, b2, at<void>(ws, L.h), y_perm,
                                  at<int32_t>(ws, L.sched), hdr, s);

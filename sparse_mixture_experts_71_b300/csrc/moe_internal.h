@@ -260,25 +260,21 @@ LossArgs route_loss_args(const moe_config& c, void* ws, const WsLayout& L,
 
 // Decode-sized layers that stream every expert's weights (dense_decode):
 // moe_forward evaluates every expert on all T tokens, so the expert GEMMs do
-// not depend on the routing (gemm_tc.cu, combine.cu, route.cu).
+// not depend on the routing (launch_dense_ffn in gemm_tc.cu, the combine in
+// combine.cu).
 bool dense_decode(const moe_config& c);
 cudaError_t launch_dense_ffn(const moe_config& c, const void* x, const void* W1, const void* b1,
                              const void* W2, const void* b2, void* h_all, float* y_all,
                              int32_t* sched, DeviceHeader* hdr, cudaStream_t s);
-cudaError_t launch_dense_gemm1(const moe_config& c, const void* x, const void* W1, const void* b1,
-                               void* h_all, DeviceHeader* hdr, cudaStream_t s);
-cudaError_t launch_dense_gemm2(const moe_config& c, const void* h_all, const void* W2,
-                               const void* b2, float* y_all, DeviceHeader* hdr, cudaStream_t s);
 cudaError_t launch_dense_combine(const moe_config& c, const float* y_all, const int32_t* idx,
                                  const float* w, void* y, DeviceHeader* hdr, const LossArgs& loss,
                                  bool do_loss, cudaStream_t s);
-// The router on the layer's inputs only, with no memset and no finishing
-// kernel: it starts beside the previous kernel of its chain and waits for it
-// before exiting (SIMT router kernels only).
-cudaError_t launch_route_inputs_only(const moe_config& c, const void* x, const float* W_r,
-                                     const float* logit_bias, const float* logit_noise,
-                                     float* logits_out, int32_t* topk_idx, float* topk_w,
-                                     void* ws, const WsLayout& L, cudaStream_t s);
+// The router kernel alone: no memset of its counters and no finishing
+// kernel (the caller zeroes the counters and finishes the loss).
+cudaError_t launch_route_no_finish(const moe_config& c, const void* x, const float* W_r,
+                                   const float* logit_bias, const float* logit_noise,
+                                   float* logits_out, int32_t* topk_idx, float* topk_w, void* ws,
+                                   const WsLayout& L, cudaStream_t s);
 
 cudaError_t launch_expert_ffn(const moe_config& c, const void* x_perm, int64_t x_rows,
                               const int32_t* offsets, const void* W1, const void* b1,

@@ -43,7 +43,8 @@ using namespace rt;
 // are added in split order.
 template <typename TX, int EMAX, int TW, int DS>
 __global__ void __launch_bounds__(kThreads) route_warp_kernel(RouteArgs a) {
-    route_begin(a);
+    pdl_wait();
+    pdl_trigger();
     constexpr int G = kWarps / DS;   // token groups per block
     constexpr int TB = G * TW;       // tokens per block
     constexpr int LDS = EMAX + 1;
@@ -148,7 +149,6 @@ __global__ void __launch_bounds__(kThreads) route_warp_kernel(RouteArgs a) {
     if (tid < TB) token_epilogue<EMAX>(a, s_p + tid * LDS, blockIdx.x * TB + tid, tid, s_idx, s_cnt, s_top1);
     __syncthreads();
     finish_block<EMAX>(a, s_p, LDS, TB, s_idx, s_cnt, s_top1, wh, carry);
-    route_end(a);
 }
 
 // ===================================================================== tensor-core kernel
@@ -196,7 +196,8 @@ __device__ __forceinline__ void mma_bf16_16816(float (&d)[4], uint32_t a0, uint3
 
 template <int NT, int MT>
 __global__ void __launch_bounds__(kThreads) route_mma_kernel(RouteArgs a) {
-    route_begin(a);
+    pdl_wait();
+    pdl_trigger();
     constexpr int EMAX = 8 * NT;
     constexpr int DS = kWarps / MT;
     constexpr int TB = 16 * MT;
@@ -309,7 +310,6 @@ __global__ void __launch_bounds__(kThreads) route_mma_kernel(RouteArgs a) {
     if (tid < TB) token_epilogue<EMAX>(a, s_buf + tid * LDS, blockIdx.x * TB + tid, tid, s_idx, s_cnt, s_top1);
     __syncthreads();
     finish_block<EMAX>(a, s_buf, LDS, TB, s_idx, s_cnt, s_top1, wh, carry);
-    route_end(a);
 }
 
 // ===================================================================== tile kernel
@@ -370,7 +370,8 @@ __device__ __forceinline__ void stage_chunk(const RouteArgs& a, int t0, int c0, 
 
 template <typename TX, int EMAX>
 __global__ void __launch_bounds__(kThreads) route_tile_kernel(RouteArgs a) {
-    route_begin(a);
+    pdl_wait();
+    pdl_trigger();
     using Gm = Geo<EMAX>;
     extern __shared__ float4 smem_f4[];
     float* smem = reinterpret_cast<float*>(smem_f4);
@@ -547,7 +548,6 @@ __global__ void __launch_bounds__(kThreads) route_tile_kernel(RouteArgs a) {
     }
     __syncthreads();
     finish_block<EMAX>(a, lg, Gm::LGS, Gm::TB, s_idx, s_cnt, s_top1, wh, carry);
-    route_end(a);
 }
 
 template <typename TX, int EMAX>
@@ -760,7 +760,6 @@ RouteArgs route_args(const moe_config& c, const void* x, const float* W_r,
     a.local_rank = at<int32_t>(ws, L.local_rank);
     a.T = c.T; a.d = c.d; a.E = c.E; a.k = c.k; a.renormalize = c.renormalize;
     a.nblk = L.route.blocks;
-    a.late_wait = 0;
     return a;
 }
 
@@ -798,14 +797,12 @@ cudaError_t launch_route(const moe_config& c, const void* x, const float* W_r,
                          route_loss_args(c, ws, L, expert_counts, aux_out, z_loss_out));
 }
 
-cudaError_t launch_route_inputs_only(const moe_config& c, const void* x, const float* W_r,
-                                     const float* logit_bias, const float* logit_noise,
-                                     float* logits_out, int32_t* topk_idx, float* topk_w,
-                                     void* ws, const WsLayout& L, cudaStream_t s) {
-    if (L.route.mma || L.route.tc) return cudaErrorInvalidValue;  // SIMT router kernels only
-    RouteArgs a = route_args(c, x, W_r, logit_bias, logit_noise, nullptr, logits_out, topk_idx,
-                             topk_w, nullptr, nullptr, ws, L, false, nullptr, 0);
-    a.late_wait = 1;
+cudaError_t launch_route_no_finish(const moe_config& c, const void* x, const float* W_r,
+                                   const float* logit_bias, const float* logit_noise,
+                                   float* logits_out, int32_t* topk_idx, float* topk_w, void* ws,
+                                   const WsLayout& L, cudaStream_t s) {
+    const RouteArgs a = route_args(c, x, W_r, logit_bias, logit_noise, nullptr, logits_out,
+                                   topk_idx, topk_w, nullptr, nullptr, ws, L, false, nullptr, 0);
     return route_kernels(c, a, ws, L, s);
 }
 

@@ -36,21 +36,7 @@ struct RouteArgs {
     int32_t* local_rank;  // ws: [T*k]
     int T, d, E, k, renormalize, nblk;
     int knorm;            // slots that are choices (the rest: next-best experts)
-    // 1: the call reads only the layer's inputs, so the kernel starts without
-    // waiting for the previous kernel of its chain (launched programmatically
-    // beside it) and waits for it only before exiting, so that its completion
-    // still implies the previous kernel's
-    int late_wait;
 };
-
-// Start and end of a router kernel (see RouteArgs::late_wait).
-__device__ __forceinline__ void route_begin(const RouteArgs& a) {
-    if (!a.late_wait) pdl_wait();
-    pdl_trigger();
-}
-__device__ __forceinline__ void route_end(const RouteArgs& a) {
-    if (a.late_wait) pdl_wait();
-}
 
 // Histogram of the block's n assignments (expert ids in s_idx, in (token,
 // slot) order) and the rank of each among the earlier ones of its expert.
