@@ -796,6 +796,15 @@ __device__ __forceinline__ void epilogue_gelu(const Params& p, int e, int r0, in
 // on CTA 0's TMEM-empty barrier.
 constexpr int BN2 = 256;  // tokens per pair tile (MMA N, max)
 
+// The token operand of the CTA-pair kernel as four tensor maps whose boxes are
+// 128, 64, 32 and 16 rows high (64 columns): each tile loads, per CTA, the
+// smallest box that holds its half of the tile's rows, so a tile of few
+// tokens (a small expert's segment, the end of a segment) does not move a
+// whole 128-row box per K step.
+struct BMaps {
+    CUtensorMap m[4];
+};
+
 template <int STAGES, bool GEMM1, int EW, int ATOMS>
 struct Cfg2 {
     static constexpr int THREADS = (4 + EW) * 32;       // 4 role warps + EW epilogue warps
@@ -846,7 +855,7 @@ __device__ __forceinline__ Tile decode_pair_tile(int t, const int* s_tiles, cons
 
 template <int STAGES, bool GEMM1, int EW, int ATOMS>
 __global__ void __launch_bounds__(Cfg2<STAGES, GEMM1, EW, ATOMS>::THREADS, 1)
-grouped_gemm_pair(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
+grouped_gemm_pair(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ BMaps tmB,
                   const __grid_constant__ CUtensorMap tmO, const Params p) {
     using C = Cfg2<STAGES, GEMM1, EW, ATOMS>;
     extern __shared__ uint8_t smem_raw[];
@@ -880,7 +889,7 @@ grouped_gemm_pair(const __grid_constant__ CUtensorMap tmA, const __grid_constant
         *s_abort = 0;
         tc::fence_barrier_init();
         tc::tma_prefetch_desc(&tmA);
-        tc::tma_prefetch_desc(&tmB);
+        for (int i = 0; i < 4; ++i) tc::tma_prefetch_desc(&tmB.m[i]);
     }
     if (warp == 2) {
         tc::tmem_alloc_pair(s_tmem, C::TMEM_COLS);
@@ -921,11 +930,14 @@ grouped_gemm_pair(const __grid_constant__ CUtensorMap tmA, const __grid_constant
             uint32_t phase = 0;
             long long fills = 0;
             bool ok = true;
-            const uint32_t bytes = 2 * C::STAGE_BYTES;  // whole boxes of both CTAs
             for (int t = pair; t < total && ok; t += npairs) {
                 const Tile tl = decode_pair_tile(t, s_tiles, p, mt2);
                 const int m0 = tl.m0;  // pair tile base row
                 const int half_rows = ((tl.n + 31) & ~31) / 2;
+                // the smallest token box that holds this CTA's half_rows rows
+                const int bsel = half_rows <= 16 ? 3 : half_rows <= 32 ? 2 : half_rows <= 64 ? 1 : 0;
+                const CUtensorMap* tb = &tmB.m[bsel];
+                const uint32_t bytes = 2 * ATOMS * (A_BYTES + (BN2 / 2 >> bsel) * BK * 2);
                 const bool red = p.koff != nullptr;
                 const int arow = (red ? 0 : tl.e * p.n_out) + m0 + rank * BM;
                 const int brow = (red ? tl.r0 - tl.e * p.tok_rows : tl.r0) + rank * half_rows;
@@ -940,7 +952,7 @@ grouped_gemm_pair(const __grid_constant__ CUtensorMap tmA, const __grid_constant
                         uint8_t* sa = smem + stage * C::STAGE_BYTES + at * C::ATOM_BYTES;
                         const int kc = k0 + (kb * ATOMS + at) * BK;
                         tc::tma_load_2d_pair(sa, &tmA, full_l, kc, arow);
-                        tc::tma_load_2d_pair(sa + A_BYTES, &tmB, full_l, kc, brow);
+                        tc::tma_load_2d_pair(sa + A_BYTES, tb, full_l, kc, brow);
                     }
                     ++fills;
                     if (++stage == STAGES) { stage = 0; phase ^= 1; }
@@ -1075,6 +1087,13 @@ bool make_map(CUtensorMap* m, const void* base, uint64_t inner, uint64_t outer,
               CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+// The four token-operand maps of the CTA-pair kernel (BMaps).
+bool make_b_maps(BMaps* m, const void* base, uint64_t inner, uint64_t outer) {
+    for (int i = 0; i < 4; ++i)
+        if (!make_map(&m->m[i], base, inner, outer, (uint32_t)(BN2 / 2) >> i)) return false;
+    return true;
+}
+
 // Row-major bf16 matrix [outer][inner] as the destination of 16 x 32 tensor
 // stores from staging rows in the 32-byte swizzle.
 bool make_store_map_sw32(CUtensorMap* m, void* base, uint64_t inner, uint64_t outer) {
@@ -1142,7 +1161,7 @@ cudaError_t launch_one(const CUtensorMap& a, const CUtensorMap& b, const Params&
 }
 
 template <int STAGES, bool GEMM1, int EW, int ATOMS>
-cudaError_t launch_one_pair(const CUtensorMap& a, const CUtensorMap& b, const CUtensorMap& o,
+cudaError_t launch_one_pair(const CUtensorMap& a, const BMaps& b, const CUtensorMap& o,
                             const Params& p, cudaStream_t s) {
     using C = Cfg2<STAGES, GEMM1, EW, ATOMS>;
     constexpr auto kern = grouped_gemm_pair<STAGES, GEMM1, EW, ATOMS>;
@@ -1190,18 +1209,17 @@ cudaError_t launch_expert_ffn_tc(const moe_config& c, const void* x_perm, int64_
     Params p2{offsets, reinterpret_cast<const __nv_bfloat16*>(b2), perm_w, y_perm, hdr,
               g_tc_timeout_ns, c.E, c.d, c.d_ff, (int)h_rows, 0, nullptr, 0};
     if (wide) {
-        // 128-row token boxes for the pair kernel; h and y_perm as store targets
-        CUtensorMap pm[6];
-        pm[0] = maps[0];
-        pm[2] = maps[2];
-        if (!make_map(&pm[1], x_perm, c.d, (uint64_t)x_rows, BN2 / 2) ||
-            !make_map(&pm[3], h, c.d_ff, (uint64_t)h_rows, BN2 / 2) ||
-            !make_store_map_sw32(&pm[4], h, c.d_ff, (uint64_t)h_rows) ||
-            !make_store_map_f32(&pm[5], y_perm, c.d, (uint64_t)h_rows))
+        // token boxes for the pair kernel; h and y_perm as store targets
+        BMaps bx, bh;
+        CUtensorMap so[2];
+        if (!make_b_maps(&bx, x_perm, c.d, (uint64_t)x_rows) ||
+            !make_b_maps(&bh, h, c.d_ff, (uint64_t)h_rows) ||
+            !make_store_map_sw32(&so[0], h, c.d_ff, (uint64_t)h_rows) ||
+            !make_store_map_f32(&so[1], y_perm, c.d, (uint64_t)h_rows))
             return cudaErrorInvalidValue;
-        cudaError_t err = launch_one_pair<3, true, 16, 2>(pm[0], pm[1], pm[4], p1, s);
+        cudaError_t err = launch_one_pair<3, true, 16, 2>(maps[0], bx, so[0], p1, s);
         if (err != cudaSuccess) return err;
-        return launch_one_pair<3, false, 8, 2>(pm[2], pm[3], pm[5], p2, s);
+        return launch_one_pair<3, false, 8, 2>(maps[2], bh, so[1], p2, s);
     }
     return launch_pair<64, 8>(maps, p1, p2, s);
 }
@@ -1252,8 +1270,9 @@ cudaError_t launch_grouped_gemm_tc(const moe_config& c, bool bf16_out, bool act,
     CUtensorMap mw;
     if (!make_map(&mw, W, (uint64_t)K, (uint64_t)c.E * n_out, BM)) return cudaErrorInvalidValue;
     if (wide) {
-        CUtensorMap ma, mo;
-        if (!make_map(&ma, A, (uint64_t)K, (uint64_t)a_rows, BN2 / 2)) return cudaErrorInvalidValue;
+        BMaps ma;
+        CUtensorMap mo;
+        if (!make_b_maps(&ma, A, (uint64_t)K, (uint64_t)a_rows)) return cudaErrorInvalidValue;
         if (bf16_out) {
             if (!make_store_map_sw32(&mo, out, (uint64_t)n_out, (uint64_t)out_rows))
                 return cudaErrorInvalidValue;
@@ -1276,9 +1295,10 @@ cudaError_t launch_segment_reduction_tc(int E, const int32_t* offsets, int64_t r
                                         DeviceHeader* hdr, cudaStream_t s) {
     Params p{offsets, nullptr, nullptr, out, hdr, g_tc_timeout_ns, E, n_out, 0, (int)rows_cap, 0,
              koff, tok_rows};
-    CUtensorMap mw, mt, mo;
+    CUtensorMap mw, mo;
+    BMaps mt;
     if (!make_map(&mw, WT, (uint64_t)kcols, (uint64_t)n_out, BM) ||
-        !make_map(&mt, TOK, (uint64_t)kcols, (uint64_t)tok_rows, BN2 / 2) ||
+        !make_b_maps(&mt, TOK, (uint64_t)kcols, (uint64_t)tok_rows) ||
         !make_store_map_f32(&mo, out, (uint64_t)n_out, (uint64_t)E * tok_rows))
         return cudaErrorInvalidValue;
     return launch_one_pair<3, false, 8, 2>(mw, mt, mo, p, s);
