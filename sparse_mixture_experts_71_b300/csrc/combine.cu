@@ -27,15 +27,25 @@ __device__ __forceinline__ void store4(__nv_bfloat16* p, float4 v) {
     *reinterpret_cast<uint2*>(p) = u;
 }
 
+// With do_loss the grid's last block finishes the router's auxiliary loss,
+// z-loss and per-expert counts (off the dispatch's critical path) while the
+// others combine.
 template <typename TY>
 __global__ void __launch_bounds__(256) combine_kernel(const float* __restrict__ y_perm,
                                                       const int32_t* __restrict__ slot_of, int T,
                                                       int k, int d, long long rows,
-                                                      TY* __restrict__ y) {
+                                                      TY* __restrict__ y, LossArgs loss,
+                                                      int do_loss) {
     pdl_wait();
     pdl_trigger();
+    if (do_loss && blockIdx.x == gridDim.x - 1) {
+        __shared__ float s_part[256];
+        __shared__ float s_d[kMaxExperts];
+        loss_and_counts(loss, s_part, s_d);
+        return;
+    }
     const int lane = threadIdx.x % 32;
-    const int nwarps = gridDim.x * (blockDim.x / 32);
+    const int nwarps = (gridDim.x - do_loss) * (blockDim.x / 32);
     const int nv = d / 4;                   // float4 columns per row
     const int nch = (nv + 127) / 128;       // 128-column chunks per row (4 per lane)
     const long long tasks = (long long)T * nch;
@@ -76,8 +86,8 @@ __global__ void __launch_bounds__(256) combine_kernel(const float* __restrict__ 
 // A slot is kept when fewer than `capacity` earlier assignments, in (token,
 // slot) order, went to its expert (capacity < 0: no cap) - the rank the
 // sparse dispatch computes, counted here directly (T <= 64).  An expert index
-// outside [0, E) is skipped and recorded.  Block 0 then finishes the router's
-// auxiliary loss, z-loss and per-expert counts (do_loss).
+// outside [0, E) is skipped and recorded.  With do_loss the grid's last block
+// finishes the router's auxiliary loss, z-loss and per-expert counts.
 template <typename TY>
 __global__ void __launch_bounds__(256) dense_combine_kernel(
     const float* __restrict__ y_all, const int32_t* __restrict__ idx, const float* __restrict__ w,
@@ -85,10 +95,14 @@ __global__ void __launch_bounds__(256) dense_combine_kernel(
     int do_loss) {
     pdl_wait();
     pdl_trigger();
-    __shared__ float s_part[256];
-    __shared__ float s_d[kMaxExperts];
+    if (do_loss && blockIdx.x == gridDim.x - 1) {  // the router's loss, beside the combine
+        __shared__ float s_part[256];
+        __shared__ float s_d[kMaxExperts];
+        loss_and_counts(loss, s_part, s_d);
+        return;
+    }
     const int lane = threadIdx.x % 32;
-    const int nwarps = gridDim.x * (blockDim.x / 32);
+    const int nwarps = (gridDim.x - do_loss) * (blockDim.x / 32);
     const int nv = d / 4;
     const int nch = (nv + 127) / 128;
     const long long tasks = (long long)T * nch;
@@ -130,10 +144,6 @@ __global__ void __launch_bounds__(256) dense_combine_kernel(
         for (int u = 0; u < 4; ++u)
             if (v0 + 32 * u < nv) store4(y + (size_t)t * d + 4 * (v0 + 32 * u), acc[u]);
     }
-    if (do_loss && blockIdx.x == 0) {
-        __syncthreads();
-        loss_and_counts(loss, s_part, s_d);
-    }
 }
 
 }  // namespace
@@ -145,24 +155,27 @@ cudaError_t launch_dense_combine(const moe_config& c, const float* y_all, const 
     const long long tasks = (long long)c.T * ((c.d / 4 + 127) / 128);
     long long blocks = (tasks + 7) / 8;
     if (blocks > num_sms() * 8) blocks = num_sms() * 8;
+    if (do_loss) ++blocks;
     return launch_kernel(dense_combine_kernel<__nv_bfloat16>, dim3((unsigned)blocks), dim3(256), 0,
                          s, 1, false, y_all, idx, w, c.T, c.k, c.d, c.E, c.capacity,
                          reinterpret_cast<__nv_bfloat16*>(y), hdr, loss, do_loss ? 1 : 0);
 }
 
 cudaError_t launch_combine(const moe_config& c, const float* y_perm, const int32_t* slot_of,
-                           void* y, int64_t rows, cudaStream_t s) {
+                           void* y, int64_t rows, cudaStream_t s, const LossArgs* loss) {
     if (c.T == 0) return cudaSuccess;
     const long long tasks = (long long)c.T * ((c.d / 4 + 127) / 128);
     long long blocks = (tasks + 7) / 8;
     if (blocks > num_sms() * 8) blocks = num_sms() * 8;
+    const int do_loss = loss != nullptr ? 1 : 0;
+    const LossArgs l = loss != nullptr ? *loss : LossArgs{};
     if (c.dtype == MOE_BF16)
-        return launch_kernel(combine_kernel<__nv_bfloat16>, dim3((unsigned)blocks), dim3(256), 0,
-                             s, 1, false, y_perm, slot_of, c.T, c.k, c.d, (long long)rows,
-                             reinterpret_cast<__nv_bfloat16*>(y));
-    return launch_kernel(combine_kernel<float>, dim3((unsigned)blocks), dim3(256), 0, s, 1, false,
-                         y_perm, slot_of, c.T, c.k, c.d, (long long)rows,
-                         reinterpret_cast<float*>(y));
+        return launch_kernel(combine_kernel<__nv_bfloat16>, dim3((unsigned)(blocks + do_loss)),
+                             dim3(256), 0, s, 1, false, y_perm, slot_of, c.T, c.k, c.d,
+                             (long long)rows, reinterpret_cast<__nv_bfloat16*>(y), l, do_loss);
+    return launch_kernel(combine_kernel<float>, dim3((unsigned)(blocks + do_loss)), dim3(256), 0, s,
+                         1, false, y_perm, slot_of, c.T, c.k, c.d, (long long)rows,
+                         reinterpret_cast<float*>(y), l, do_loss);
 }
 
 }  // namespace moe

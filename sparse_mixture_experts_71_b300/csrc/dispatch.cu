@@ -15,9 +15,10 @@
 //           that expert in earlier blocks, the per-expert totals, the kept
 //           counts min(total, capacity) (shared experts: total) and their
 //           exclusive prefix sum (offsets).
-//   permute one warp per assignment: rank = base + local rank; kept iff rank <
-//           capacity; row = offsets[e] + rank; writes slot_of / perm_token /
-//           perm_w and copies the token's row with 16-byte vector accesses.
+//   permute one warp per group of four assignments (looked up on four lanes at
+//           once): rank = base + local rank; kept iff rank < capacity; row =
+//           offsets[e] + rank; writes slot_of / perm_token / perm_w, then the
+//           warp copies each kept token row with 16-byte vector accesses.
 
 #include <cuda_runtime.h>
 
@@ -141,6 +142,11 @@ __global__ void __launch_bounds__(1024) scan_kernel(const int32_t* __restrict__ 
     }
 }
 
+// Assignments per permute group: the group's lanes 0 .. kPermG-1 look up
+// their assignments' rows at the same time (four dependent loads each), then
+// the warp copies the kept rows one after another.
+constexpr int kPermG = 4;
+
 template <typename TX>
 __global__ void __launch_bounds__(256) permute_kernel(
     const TX* __restrict__ x, const int32_t* __restrict__ idx, const float* __restrict__ topk_w,
@@ -153,32 +159,40 @@ __global__ void __launch_bounds__(256) permute_kernel(
     const int lane = threadIdx.x % 32;
     const int nwarps = gridDim.x * (blockDim.x / 32);
     const int nvec = d * (int)sizeof(TX) / 16;  // 16-byte vectors per row
-    for (int a = blockIdx.x * (blockDim.x / 32) + threadIdx.x / 32; a < n; a += nwarps) {
-        const int r_local = __ldg(local_rank + a);
+    for (int a0 = (blockIdx.x * (blockDim.x / 32) + threadIdx.x / 32) * kPermG; a0 < n;
+         a0 += nwarps * kPermG) {
+        const int a = a0 + lane;
         int slot = -1;
-        if (r_local >= 0) {
-            const int e = __ldg(idx + a);
-            const int r = __ldg(blk_base + (size_t)(a / asg_per_block) * E + e) + r_local;
-            if (capacity < 0 || r < capacity || e < n_shared) slot = __ldg(offsets + e) + r;
-        }
-        const int t = a / k;
-        if (lane == 0) {
+        if (lane < kPermG && a < n) {
+            const int r_local = __ldg(local_rank + a);
+            if (r_local >= 0) {
+                const int e = __ldg(idx + a);
+                const int r = __ldg(blk_base + (size_t)(a / asg_per_block) * E + e) + r_local;
+                if (capacity < 0 || r < capacity || e < n_shared) slot = __ldg(offsets + e) + r;
+            }
             slot_of[a] = slot;
             if (slot >= 0) {
-                perm_token[slot] = t;
+                perm_token[slot] = a / k;
                 if (perm_w != nullptr) perm_w[slot] = __ldg(topk_w + a);
             }
         }
-        if (slot < 0 || x_perm == nullptr) continue;
-        const uint4* src = reinterpret_cast<const uint4*>(x + (size_t)t * d);
-        uint4* dst = reinterpret_cast<uint4*>(x_perm + (size_t)slot * d);
-        int v = lane;
-        for (; v + 96 < nvec; v += 128) {
-            const uint4 q0 = __ldg(src + v), q1 = __ldg(src + v + 32);
-            const uint4 q2 = __ldg(src + v + 64), q3 = __ldg(src + v + 96);
-            dst[v] = q0; dst[v + 32] = q1; dst[v + 64] = q2; dst[v + 96] = q3;
+        if (x_perm == nullptr) continue;
+        unsigned kept = __ballot_sync(0xffffffffu, slot >= 0);
+        while (kept) {
+            const int src = __ffs(kept) - 1;
+            kept &= kept - 1;
+            const int sl = __shfl_sync(0xffffffffu, slot, src);
+            const int t = (a0 + src) / k;
+            const uint4* srow = reinterpret_cast<const uint4*>(x + (size_t)t * d);
+            uint4* dst = reinterpret_cast<uint4*>(x_perm + (size_t)sl * d);
+            int v = lane;
+            for (; v + 96 < nvec; v += 128) {
+                const uint4 q0 = __ldg(srow + v), q1 = __ldg(srow + v + 32);
+                const uint4 q2 = __ldg(srow + v + 64), q3 = __ldg(srow + v + 96);
+                dst[v] = q0; dst[v + 32] = q1; dst[v + 64] = q2; dst[v + 96] = q3;
+            }
+            for (; v < nvec; v += 32) dst[v] = __ldg(srow + v);
         }
-        for (; v < nvec; v += 32) dst[v] = __ldg(src + v);
     }
 }
 
@@ -223,7 +237,7 @@ cudaError_t launch_scan_permute(const moe_config& c, const void* x, const int32_
                                   (const int32_t*)blk_hist, hist_blocks, c.E, c.capacity,
                                   c.n_shared, blk_base, offsets, loss);
     if (e != cudaSuccess || n == 0) return e;
-    int blocks = (n + 7) / 8;
+    int blocks = (n + 8 * kPermG - 1) / (8 * kPermG);
     blocks = blocks < num_sms() * 8 ? blocks : num_sms() * 8;
     if (c.dtype == MOE_BF16)
         return launch_kernel(permute_kernel<__nv_bfloat16>, dim3(blocks), dim3(256), 0, s, 1, false,

@@ -438,6 +438,7 @@ moe_status moe_forward(const moe_config* cfg, const void* x, const float* W_r,
     }
     chain_begin();
     cudaError_t e;
+    bool loss_in_combine = false;
     if (rerouting(c) && c.capacity >= 0) {
         // K2 ranked experts per token; the drop pass (whose scan also
         // finishes the loss and counts), the offers, the layout
@@ -449,14 +450,13 @@ moe_status moe_forward(const moe_config* cfg, const void* x, const float* W_r,
                 c, reroute_ranked(c), x, idx, w, offsets, slot_of, perm_token, perm_w, x_perm, ws,
                 L, route_loss_args(c, ws, L, expert_counts, aux_out, z_loss_out), s);
     } else if (c.n_shared == 0) {  // (rerouting without a cap drops nothing: this path)
-        // the router also counts (blk_hist, local_rank) and the scan finishes its loss
+        // the router also counts (blk_hist, local_rank); the combine finishes its loss
         e = launch_route(c, x, W_r, logit_bias, logit_noise, nullptr, logits_out, idx, w,
                          expert_counts, aux_out, z_loss_out, ws, L, true, s);
         if (e == cudaSuccess)
             e = launch_scan_permute(c, x, idx, w, L.route.tokens * c.k, L.route.blocks, offsets,
-                                    slot_of, perm_token, perm_w, x_perm, ws, L,
-                                    route_loss_args(c, ws, L, expert_counts, aux_out, z_loss_out),
-                                    s);
+                                    slot_of, perm_token, perm_w, x_perm, ws, L, LossArgs{}, s);
+        loss_in_combine = expert_counts != nullptr || aux_out != nullptr || z_loss_out != nullptr;
     } else {
         // shared experts: route the routed experts, join the shared ones, count all
         int32_t* idx_r = at<int32_t>(ws, L.route_idx);
@@ -474,7 +474,10 @@ moe_status moe_forward(const moe_config* cfg, const void* x, const float* W_r,
     if (e == cudaSuccess)
         e = launch_expert_ffn(cd, x_perm, L.rows, offsets, W1, b1, W2, b2, perm_w, y_perm, ws,
                               L, s);
-    if (e == cudaSuccess) e = launch_combine(cd, y_perm, slot_of, y, L.rows, s);
+    if (e == cudaSuccess) {
+        const LossArgs loss = route_loss_args(c, ws, L, expert_counts, aux_out, z_loss_out);
+        e = launch_combine(cd, y_perm, slot_of, y, L.rows, s, loss_in_combine ? &loss : nullptr);
+    }
     return from_cuda(e);
 }
 

@@ -281,8 +281,11 @@ cudaError_t launch_expert_ffn(const moe_config& c, const void* x_perm, int64_t x
                               const void* W2, const void* b2, const float* perm_w, float* y_perm,
                               void* ws, const WsLayout& L, cudaStream_t s);
 
-// rows: rows of y_perm (slots at or past it are skipped as dropped).
+// rows: rows of y_perm (slots at or past it are skipped as dropped).  With
+// `loss`, one more block finishes the router's loss and counts beside the
+// combine (the forward pass).
 cudaError_t launch_combine(const moe_config& c, const float* y_perm, const int32_t* slot_of,
-                           void* y, int64_t rows, cudaStream_t s);
+                           void* y, int64_t rows, cudaStream_t s,
+                           const LossArgs* loss = nullptr);
 
 }  // namespace moe
