@@ -711,9 +711,7 @@ RouteGeom route_geom(const moe_config& c) {
     if (c.dtype == MOE_BF16 && c.E > 16 && c.E <= 64 && c.T >= 1024) {
         g.tc = true;
         g.epad = c.E <= 32 ? 32 : 64;
-        // 256 tokens per CTA once that still fills ~0.85 of the SMs (one CTA
-        // per SM); 128 (two CTAs per SM) below
-        g.tokens = c.T >= 126 * 256 ? 256 : 128;
+        g.tokens = 128;
     } else if (c.dtype == MOE_BF16 && c.E <= 16 && c.T >= 1024) {
         g.mma = true;
         g.epad = c.E <= 8 ? 8 : 16;
@@ -771,7 +769,7 @@ cudaError_t route_kernels(const moe_config& c, const RouteArgs& a, void* ws, con
     if (L.route.tc) {
         __nv_bfloat16* wsp = at<__nv_bfloat16>(ws, L.wsplit);
         cudaError_t err = launch_split(a, L.route.epad, wsp, s);
-        return err == cudaSuccess ? launch_route_tc(a, wsp, L.route.epad, L.route.tokens, s) : err;
+        return err == cudaSuccess ? launch_route_tc(a, wsp, L.route.epad, s) : err;
     }
     return c.dtype == MOE_BF16 ? launch_e<__nv_bfloat16>(a, L.route, s)
                                : launch_e<float>(a, L.route, s);

@@ -174,9 +174,8 @@ __device__ __forceinline__ void token_epilogue(const RouteArgs& a, float* prow, 
     atomicAdd(&s_top1[sel_e[0]], 1);
 }
 
-// tcgen05 router (route_tc.cu); np = rows per weight part (16, 32 or 64),
-// tt = tokens per CTA (128, or 256 for large batches: RouteGeom::tokens).
-cudaError_t launch_route_tc(const RouteArgs& a, const __nv_bfloat16* wsplit, int np, int tt,
+// tcgen05 router (route_tc.cu); np = rows per weight part (16, 32 or 64).
+cudaError_t launch_route_tc(const RouteArgs& a, const __nv_bfloat16* wsplit, int np,
                             cudaStream_t s);
 
 }  // namespace rt

@@ -5,15 +5,14 @@
 // "Mixture of Experts: Scaling Parameters Without Scaling Compute", section
 // "The MoE layer", step 1: g = W_r x, p = softmax(g).
 //
-// Each CTA owns TT = 128 or 256 tokens (one or two MMAs of M = 128 per
-// weight part and K step, each into its own accumulator).  W_r (fp32) is split beforehand
+// Each CTA owns 128 tokens (the MMA's M).  W_r (fp32) is split beforehand
 // into three bf16 parts hi + mid + lo that add up to W_r exactly; the three
 // MMAs of a K = 16 step accumulate x.hi^T + x.mid^T + x.lo^T into one fp32
 // TMEM accumulator of NP columns (NP = E rounded up), so every product is
 // exact and only the fp32 accumulation rounds.  Warp 0 streams 64-column
-// slices of x (TT x 64) and of the three parts (NP x 64 each) into a ring;
-// warp 1 issues the MMAs; warps 4-7 read the accumulators back (TMEM lane =
-// token) into shared memory.  Then one thread per token does the
+// slices of x (128 x 64) and of the three parts (NP x 64 each) into a
+// 2-deep ring; warp 1 issues the MMAs; warps 4-7 read the accumulator back
+// (TMEM lane = token) into shared memory.  Then one thread per token does the
 // softmax and top-k, and the block finishes like the other router kernels.
 
 #include <cuda.h>
@@ -30,34 +29,30 @@ namespace {
 
 using namespace rt;
 
-constexpr int TM = 128;                  // tokens per MMA (its M)
+constexpr int TM = 128;                  // tokens per CTA
 constexpr int RBK = 64;                  // K per stage
-constexpr int RA_BYTES = TM * RBK * 2;   // 16 KB: one MMA's slice of x
+constexpr int RA_BYTES = TM * RBK * 2;   // 16 KB
+// Two stages, and the logits tile reuses the ring once the MMAs are done, so
+// two CTAs fit on an SM: a batch of T / 128 CTAs then runs in one wave on the
+// 148 SMs (T = 32768: 256 CTAs) instead of 1.7 waves of one CTA per SM, with
+// the same bytes in flight per SM.
+constexpr int RSTAGES = 2;
 constexpr uint64_t kRouteTimeoutNs = 2000000000ull;
 
-// TT = 128: two stages, and the logits tile reuses the ring once the MMAs are
-// done, so two CTAs fit on an SM (a batch of T / 128 CTAs runs in one wave on
-// the 148 SMs up to T = 37888).  TT = 256 (large batches): one CTA per SM
-// with three stages, each holding 256 rows of x and one copy of the weight
-// parts - half the weight-part traffic per token and half as much x again in
-// flight per SM.
-template <int NP, int TT>
+template <int NP>
 struct RCfg {
-    static constexpr int RSTAGES = TT == 256 ? 3 : 2;
-    static constexpr int MINB = TT == 256 ? 1 : 2;  // CTAs per SM
-    static constexpr int X_BYTES = TT * RBK * 2;
     static constexpr int PART_BYTES = NP * RBK * 2;
-    static constexpr int STAGE_BYTES = X_BYTES + 3 * PART_BYTES;
+    static constexpr int STAGE_BYTES = RA_BYTES + 3 * PART_BYTES;
     static constexpr int LDS = NP + 1;
-    static constexpr int OFF_P = 0;  // logits tile [TT][LDS] fp32, over the stage ring
+    static constexpr int OFF_P = 0;  // logits tile [TM][LDS] fp32, over the stage ring
     static constexpr int RING = RSTAGES * STAGE_BYTES;
-    static constexpr int P_BYTES = ((TT * LDS * 4 + 1023) / 1024) * 1024;
+    static constexpr int P_BYTES = ((TM * LDS * 4 + 1023) / 1024) * 1024;
     static constexpr int OFF_BARS = RING > P_BYTES ? RING : P_BYTES;
     static constexpr int NUM_BARS = 2 * RSTAGES + 2;
     static constexpr int SMEM = OFF_BARS + NUM_BARS * 8 + 1023;
-    static constexpr int TMEM_COLS = (TT / TM) * NP < 32 ? 32 : (TT / TM) * NP;
+    static constexpr int TMEM_COLS = NP < 32 ? 32 : NP;
     static_assert(STAGE_BYTES % 1024 == 0, "stage alignment");
-    static_assert(MINB * (SMEM + 12288) <= 233472, "CTAs per SM");
+    static_assert(2 * (SMEM + 8192) <= 233472, "two CTAs per SM");
 };
 
 __device__ __forceinline__ bool wait_or_abort(uint64_t* bar, uint32_t parity, volatile int* abort_flag,
@@ -81,13 +76,11 @@ __device__ __forceinline__ void drain_wait(uint64_t* bar, uint32_t parity) {
         if (tc::globaltimer() - t0 > kRouteTimeoutNs) break;
 }
 
-template <int NP, int TT>
-__global__ void __launch_bounds__(kThreads, RCfg<NP, TT>::MINB)
+template <int NP>
+__global__ void __launch_bounds__(kThreads, 2)
 route_tc_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constant__ CUtensorMap tmW,
                 RouteArgs a) {
-    using C = RCfg<NP, TT>;
-    constexpr int RSTAGES = C::RSTAGES;
-    constexpr int NH = TT / TM;  // MMAs (accumulators) per weight part and K step
+    using C = RCfg<NP>;
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -98,12 +91,12 @@ route_tc_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constant__
     uint64_t* drain = tfull + 1;
     __shared__ uint32_t s_tmem;
     __shared__ int s_abort;
-    __shared__ int s_idx[TT * kMaxTopK];
+    __shared__ int s_idx[TM * kMaxTopK];
     __shared__ int s_cnt[NP], s_top1[NP], carry[NP];
     __shared__ int wh[kWarps][NP];
 
     const int tid = threadIdx.x, warp = tid / 32, lane = tid % 32;
-    const int t0 = blockIdx.x * TT;
+    const int t0 = blockIdx.x * TM;
     const int KB = (a.d + RBK - 1) / RBK;
     const bool gemm = a.logits_in == nullptr;
 
@@ -135,7 +128,7 @@ route_tc_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constant__
     volatile int* abort_flag = &s_abort;
 
     if (!gemm) {
-        for (int i = tid; i < TT * NP; i += kThreads) {
+        for (int i = tid; i < TM * NP; i += kThreads) {
             const int tok = i / NP, e = i % NP;
             const int t = t0 + tok;
             s_p[tok * C::LDS + e] =
@@ -153,7 +146,7 @@ route_tc_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constant__
                 tc::tma_load_2d(sa, &tmX, &full[stage], kb * RBK, t0);
 #pragma unroll
                 for (int part = 0; part < 3; ++part)
-                    tc::tma_load_2d(sa + C::X_BYTES + part * C::PART_BYTES, &tmW, &full[stage],
+                    tc::tma_load_2d(sa + RA_BYTES + part * C::PART_BYTES, &tmW, &full[stage],
                                     kb * RBK, part * NP);
                 ++fills;
                 if (++stage == RSTAGES) { stage = 0; phase ^= 1; }
@@ -176,13 +169,10 @@ route_tc_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constant__
                 for (int kk = 0; kk < RBK / 16; ++kk)
 #pragma unroll
                     for (int part = 0; part < 3; ++part)
-#pragma unroll
-                        for (int h = 0; h < NH; ++h)
-                            tc::mma_bf16(tmem_base + (uint32_t)(h * NP),
-                                         tc::sdesc_k128_sw128(sa + h * RA_BYTES + kk * 32),
-                                         tc::sdesc_k128_sw128(sa + C::X_BYTES +
-                                                              part * C::PART_BYTES + kk * 32),
-                                         idesc, (kb | kk | part) != 0 ? 1u : 0u);
+                        tc::mma_bf16(tmem_base, tc::sdesc_k128_sw128(sa + kk * 32),
+                                     tc::sdesc_k128_sw128(sa + RA_BYTES + part * C::PART_BYTES +
+                                                          kk * 32),
+                                     idesc, (kb | kk | part) != 0 ? 1u : 0u);
                 tc::mma_commit(&empty[stage]);
                 if (++stage == RSTAGES) { stage = 0; phase ^= 1; }
             }
@@ -194,26 +184,21 @@ route_tc_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constant__
         // s_p overlays the stage ring: written only after tfull, when every
         // TMA fill has been consumed by the MMAs
         const int q = warp & 3;
+        const int tok = q * 32 + lane;
         const bool ok = wait_or_abort(tfull, 0, abort_flag, a.hdr, 3);
         if (__all_sync(0xffffffffu, ok)) {
             tc::fence_after_sync();
 #pragma unroll
-            for (int h = 0; h < NH; ++h) {
-                const int tok = h * TM + q * 32 + lane;
+            for (int c0 = 0; c0 < NP; c0 += 32) {
+                float v[32];
+                tc::tmem_ld_32cols(tmem_base + ((uint32_t)(q * 32) << 16) + (uint32_t)c0, v);
 #pragma unroll
-                for (int c0 = 0; c0 < NP; c0 += 32) {
-                    float v[32];
-                    tc::tmem_ld_32cols(tmem_base + ((uint32_t)(q * 32) << 16) +
-                                           (uint32_t)(h * NP + c0),
-                                       v);
-#pragma unroll
-                    for (int j = 0; j < 32; ++j) {
-                        const int e = c0 + j;
-                        if (e < NP) {
-                            float g = v[j];
-                            if (a.bias != nullptr && e < a.E) g += __ldg(a.bias + e);
-                            s_p[tok * C::LDS + e] = g;
-                        }
+                for (int j = 0; j < 32; ++j) {
+                    const int e = c0 + j;
+                    if (e < NP) {
+                        float g = v[j];
+                        if (a.bias != nullptr && e < a.E) g += __ldg(a.bias + e);
+                        s_p[tok * C::LDS + e] = g;
                     }
                 }
             }
@@ -225,10 +210,9 @@ route_tc_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constant__
         tc::fence_after_sync();
         tc::tmem_dealloc(tmem_base, C::TMEM_COLS);
     }
-    for (int tok = tid; tok < TT; tok += kThreads)
-        token_epilogue<NP>(a, s_p + tok * C::LDS, t0 + tok, tok, s_idx, s_cnt, s_top1);
+    if (tid < TM) token_epilogue<NP>(a, s_p + tid * C::LDS, t0 + tid, tid, s_idx, s_cnt, s_top1);
     __syncthreads();
-    finish_block<NP>(a, s_p, C::LDS, TT, s_idx, s_cnt, s_top1, wh, carry);
+    finish_block<NP>(a, s_p, C::LDS, TM, s_idx, s_cnt, s_top1, wh, carry);
 }
 
 PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
@@ -257,19 +241,19 @@ bool make_map(CUtensorMap* m, const void* base, uint64_t inner, uint64_t outer,
               CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-template <int NP, int TT>
+template <int NP>
 cudaError_t launch_np(const RouteArgs& a, const __nv_bfloat16* wsplit, cudaStream_t s) {
-    using C = RCfg<NP, TT>;
+    using C = RCfg<NP>;
     CUtensorMap mx, mw;
     if (a.logits_in == nullptr) {
-        if (!make_map(&mx, a.x, (uint64_t)a.d, (uint64_t)a.T, TT) ||
+        if (!make_map(&mx, a.x, (uint64_t)a.d, (uint64_t)a.T, TM) ||
             !make_map(&mw, wsplit, (uint64_t)a.d, (uint64_t)3 * NP, NP))
             return cudaErrorInvalidValue;
     } else {
         memset(&mx, 0, sizeof(mx));
         memset(&mw, 0, sizeof(mw));
     }
-    constexpr auto kern = route_tc_kernel<NP, TT>;
+    constexpr auto kern = route_tc_kernel<NP>;
     cudaError_t err = ensure_smem<kern>(C::SMEM);
     if (err != cudaSuccess) return err;
     return launch_kernel(kern, dim3(a.nblk), dim3(kThreads), C::SMEM, s, 1, true, mx, mw, a);
@@ -278,12 +262,11 @@ cudaError_t launch_np(const RouteArgs& a, const __nv_bfloat16* wsplit, cudaStrea
 }  // namespace
 
 namespace rt {
-cudaError_t launch_route_tc(const RouteArgs& a, const __nv_bfloat16* wsplit, int np, int tt,
+cudaError_t launch_route_tc(const RouteArgs& a, const __nv_bfloat16* wsplit, int np,
                             cudaStream_t s) {
-    if (tt == 256) return np <= 32 ? launch_np<32, 256>(a, wsplit, s) : launch_np<64, 256>(a, wsplit, s);
-    if (np <= 16) return launch_np<16, 128>(a, wsplit, s);
-    if (np <= 32) return launch_np<32, 128>(a, wsplit, s);
-    return launch_np<64, 128>(a, wsplit, s);
+    if (np <= 16) return launch_np<16>(a, wsplit, s);
+    if (np <= 32) return launch_np<32>(a, wsplit, s);
+    return launch_np<64>(a, wsplit, s);
 }
 }  // namespace rt
 

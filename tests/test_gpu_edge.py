@@ -175,8 +175,8 @@ NOISY = [
     # name, T, d, F, E, k, dtype: one case per router kernel
     ("noise-mma", 2048, 256, 256, 8, 2, "bf16"),    # mma.sync router (E <= 16)
     ("noise-tc", 2048, 256, 256, 40, 2, "bf16"),    # tcgen05 router (16 < E <= 64)
-    # tcgen05 router with 256 tokens per CTA (large batches); the last CTA holds 232
-    ("noise-tc256", 33000, 128, 128, 40, 2, "bf16"),
+    # tcgen05 router on a large batch with a ragged last block (33000 = 257 x 128 + 104)
+    ("noise-tc-large", 33000, 128, 128, 40, 2, "bf16"),
     ("noise-warp", 300, 64, 64, 8, 2, "f32"),       # warp router
     ("noise-tile", 200, 64, 64, 100, 3, "bf16"),    # tile router (E > 64)
 ]
