@@ -96,6 +96,10 @@ struct Params {
     // zeros.
     const int32_t* koff;
     int tok_rows;
+    // CTA-pair kernel: 1 when the operand maps are the 3-D views of
+    // make_map3 (one box covers a stage's ATOMS K atoms), 0 for 2-D maps
+    // (one box per atom)
+    int box3d;
 };
 
 // Rows of an expert's segment (offsets clamped to the buffers).
@@ -805,12 +809,14 @@ struct BMaps {
     CUtensorMap m[4];
 };
 
+// A stage holds the ATOMS weight atoms (A_BYTES each) and then the ATOMS
+// token atoms, each as many 128-byte rows as the tile's token box (at most
+// BN2 / 2), packed one after another.
 template <int STAGES, bool GEMM1, int EW, int ATOMS>
 struct Cfg2 {
     static constexpr int THREADS = (4 + EW) * 32;       // 4 role warps + EW epilogue warps
-    static constexpr int B_BYTES = (BN2 / 2) * BK * 2;  // 16 KB: this CTA's half of B per atom
-    static constexpr int ATOM_BYTES = A_BYTES + B_BYTES;
-    static constexpr int STAGE_BYTES = ATOMS * ATOM_BYTES;  // ATOMS x 64 columns of K
+    static constexpr int B_BYTES = (BN2 / 2) * BK * 2;  // 16 KB: this CTA's half of B per atom (max)
+    static constexpr int STAGE_BYTES = ATOMS * (A_BYTES + B_BYTES);  // ATOMS x 64 columns of K
     static constexpr int OUT_ES = GEMM1 ? 2 : 4;
     static constexpr int STAGING = EW * 32 * 32 * OUT_ES;
     static constexpr int TMEM_COLS = 2 * BN2;
@@ -938,6 +944,7 @@ grouped_gemm_pair(const __grid_constant__ CUtensorMap tmA, const __grid_constant
                 const int bsel = half_rows <= 16 ? 3 : half_rows <= 32 ? 2 : half_rows <= 64 ? 1 : 0;
                 const CUtensorMap* tb = &tmB.m[bsel];
                 const uint32_t bytes = 2 * ATOMS * (A_BYTES + (BN2 / 2 >> bsel) * BK * 2);
+                const int batom = (BN2 / 2 >> bsel) * BK * 2;  // bytes of one token atom
                 const bool red = p.koff != nullptr;
                 const int arow = (red ? 0 : tl.e * p.n_out) + m0 + rank * BM;
                 const int brow = (red ? tl.r0 - tl.e * p.tok_rows : tl.r0) + rank * half_rows;
@@ -947,12 +954,19 @@ grouped_gemm_pair(const __grid_constant__ CUtensorMap tmA, const __grid_constant
                     if (!wait_bar(&empty[stage], phase ^ 1, s_abort, p, 1)) { ok = false; break; }
                     if (leader) tc::mbar_expect_tx(&full[stage], bytes);
                     const uint32_t full_l = tc::cluster_addr(&full[stage], 0);
+                    uint8_t* sa = smem + stage * C::STAGE_BYTES;
+                    uint8_t* sb = sa + ATOMS * A_BYTES;
+                    if (p.box3d) {  // one box per operand: 64 columns x rows x ATOMS atoms
+                        const int kc = k0 / BK + kb * ATOMS;
+                        tc::tma_load_3d_pair(sa, &tmA, full_l, 0, arow, kc);
+                        tc::tma_load_3d_pair(sb, tb, full_l, 0, brow, kc);
+                    } else {
 #pragma unroll
-                    for (int at = 0; at < ATOMS; ++at) {
-                        uint8_t* sa = smem + stage * C::STAGE_BYTES + at * C::ATOM_BYTES;
-                        const int kc = k0 + (kb * ATOMS + at) * BK;
-                        tc::tma_load_2d_pair(sa, &tmA, full_l, kc, arow);
-                        tc::tma_load_2d_pair(sa + A_BYTES, tb, full_l, kc, brow);
+                        for (int at = 0; at < ATOMS; ++at) {
+                            const int kc = k0 + (kb * ATOMS + at) * BK;
+                            tc::tma_load_2d_pair(sa + at * A_BYTES, &tmA, full_l, kc, arow);
+                            tc::tma_load_2d_pair(sb + at * batom, tb, full_l, kc, brow);
+                        }
                     }
                     ++fills;
                     if (++stage == STAGES) { stage = 0; phase ^= 1; }
@@ -973,6 +987,9 @@ grouped_gemm_pair(const __grid_constant__ CUtensorMap tmA, const __grid_constant
                 const Tile tl = decode_pair_tile(t, s_tiles, p, mt2);
                 const uint32_t N = (uint32_t)((tl.n + 31) & ~31);
                 const uint32_t idesc = tc::idesc_bf16_f32(2 * BM, N);
+                const int half_rows = (int)N / 2;  // the producer's token box for this tile
+                const int bsel = half_rows <= 16 ? 3 : half_rows <= 32 ? 2 : half_rows <= 64 ? 1 : 0;
+                const uint32_t batom = (uint32_t)((BN2 / 2 >> bsel) * BK * 2);
                 if (!wait_bar(&tempty[acc], acc_phase ^ 1, s_abort, p, 2)) break;
                 tc::fence_after_sync();
                 const uint32_t d_tmem = tmem_base + (uint32_t)(acc * BN2);
@@ -982,11 +999,11 @@ grouped_gemm_pair(const __grid_constant__ CUtensorMap tmA, const __grid_constant
                 for (int kb = 0; kb < KBt; ++kb) {
                     if (!wait_bar(&full[stage], phase, s_abort, p, 3)) { ok = false; break; }
                     tc::fence_after_sync();
+                    const uint32_t s0 = tc::smem_u32(smem + stage * C::STAGE_BYTES);
 #pragma unroll
                     for (int at = 0; at < ATOMS; ++at) {
-                        const uint32_t sa =
-                            tc::smem_u32(smem + stage * C::STAGE_BYTES + at * C::ATOM_BYTES);
-                        const uint32_t sb = sa + A_BYTES;
+                        const uint32_t sa = s0 + at * A_BYTES;
+                        const uint32_t sb = s0 + ATOMS * A_BYTES + at * batom;
 #pragma unroll
                         for (int kk = 0; kk < BK / 16; ++kk) {
                             tc::mma_bf16_pair(d_tmem, tc::sdesc_k128_sw128(sa + kk * 32),
@@ -1092,6 +1109,45 @@ bool make_b_maps(BMaps* m, const void* base, uint64_t inner, uint64_t outer) {
     for (int i = 0; i < 4; ++i)
         if (!make_map(&m->m[i], base, inner, outer, (uint32_t)(BN2 / 2) >> i)) return false;
     return true;
+}
+
+// Row-major bf16 matrix [outer][inner] (inner a multiple of 64) viewed in 3-D
+// as [inner / 64][outer][64]: the innermost dimension is 64 columns (one
+// 128-byte swizzle row), the next the rows, the outermost the 64-column
+// chunks of K.  A box of 64 x box_outer x atoms then lands in shared memory as
+// `atoms` consecutive 128-byte-swizzled [box_outer][64] tiles - the layout two
+// (or more) 2-D boxes would give - in one TMA operation, which halves the box
+// count per stage (the TMA issue rate per SM, not bytes, bounds a stage of
+// 16 KB boxes).  Chunks past the end read as zero, like columns past K.
+bool make_map3(CUtensorMap* m, const void* base, uint64_t inner, uint64_t outer,
+               uint32_t box_outer, uint32_t atoms) {
+    auto fn = encode_fn();
+    if (fn == nullptr || inner % BK != 0) return false;
+    cuuint64_t dims[3] = {(cuuint64_t)BK, outer, inner / BK};
+    cuuint64_t strides[2] = {inner * 2, (cuuint64_t)BK * 2};
+    cuuint32_t box[3] = {(cuuint32_t)BK, box_outer, atoms};
+    cuuint32_t estr[3] = {1, 1, 1};
+    return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims, strides, box,
+              estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+              CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+constexpr int kPairAtoms = 2;  // K atoms per stage of the CTA-pair kernel
+
+// The CTA-pair kernel's operand maps: 3-D (one box per operand and stage)
+// when K is a multiple of 64 and the driver takes the 3-D view, else 2-D.
+// Returns the Params::box3d value.
+bool make_pair_maps(CUtensorMap* a, const void* W, uint64_t K, uint64_t w_rows, BMaps* b,
+                    const void* T, uint64_t t_rows, int* box3d) {
+    bool ok3 = K % BK == 0 && make_map3(a, W, K, w_rows, BM, kPairAtoms);
+    for (int i = 0; ok3 && i < 4; ++i)
+        ok3 = make_map3(&b->m[i], T, K, t_rows, (uint32_t)(BN2 / 2) >> i, kPairAtoms);
+    if (ok3) {
+        *box3d = 1;
+        return true;
+    }
+    *box3d = 0;
+    return make_map(a, W, K, w_rows, BM) && make_b_maps(b, T, K, t_rows);
 }
 
 // Row-major bf16 matrix [outer][inner] as the destination of 16 x 32 tensor
@@ -1209,17 +1265,19 @@ cudaError_t launch_expert_ffn_tc(const moe_config& c, const void* x_perm, int64_
     Params p2{offsets, reinterpret_cast<const __nv_bfloat16*>(b2), perm_w, y_perm, hdr,
               g_tc_timeout_ns, c.E, c.d, c.d_ff, (int)h_rows, 0, nullptr, 0};
     if (wide) {
-        // token boxes for the pair kernel; h and y_perm as store targets
+        // operand maps for the pair kernel; h and y_perm as store targets
+        CUtensorMap a1, a2, so[2];
         BMaps bx, bh;
-        CUtensorMap so[2];
-        if (!make_b_maps(&bx, x_perm, c.d, (uint64_t)x_rows) ||
-            !make_b_maps(&bh, h, c.d_ff, (uint64_t)h_rows) ||
+        if (!make_pair_maps(&a1, W1, c.d, (uint64_t)c.E * c.d_ff, &bx, x_perm, (uint64_t)x_rows,
+                            &p1.box3d) ||
+            !make_pair_maps(&a2, W2, c.d_ff, (uint64_t)c.E * c.d, &bh, h, (uint64_t)h_rows,
+                            &p2.box3d) ||
             !make_store_map_sw32(&so[0], h, c.d_ff, (uint64_t)h_rows) ||
             !make_store_map_f32(&so[1], y_perm, c.d, (uint64_t)h_rows))
             return cudaErrorInvalidValue;
-        cudaError_t err = launch_one_pair<3, true, 16, 2>(maps[0], bx, so[0], p1, s);
+        cudaError_t err = launch_one_pair<3, true, 16, kPairAtoms>(a1, bx, so[0], p1, s);
         if (err != cudaSuccess) return err;
-        return launch_one_pair<3, false, 8, 2>(maps[2], bh, so[1], p2, s);
+        return launch_one_pair<3, false, 8, kPairAtoms>(a2, bh, so[1], p2, s);
     }
     return launch_pair<64, 8>(maps, p1, p2, s);
 }
@@ -1268,20 +1326,22 @@ cudaError_t launch_grouped_gemm_tc(const moe_config& c, bool bf16_out, bool act,
     Params p{offsets, reinterpret_cast<const __nv_bfloat16*>(bias), bf16_out ? nullptr : row_w,
              out, hdr, g_tc_timeout_ns, c.E, n_out, K, (int)out_rows, act ? 1 : 0, nullptr, 0};
     CUtensorMap mw;
-    if (!make_map(&mw, W, (uint64_t)K, (uint64_t)c.E * n_out, BM)) return cudaErrorInvalidValue;
     if (wide) {
         BMaps ma;
         CUtensorMap mo;
-        if (!make_b_maps(&ma, A, (uint64_t)K, (uint64_t)a_rows)) return cudaErrorInvalidValue;
+        if (!make_pair_maps(&mw, W, (uint64_t)K, (uint64_t)c.E * n_out, &ma, A, (uint64_t)a_rows,
+                            &p.box3d))
+            return cudaErrorInvalidValue;
         if (bf16_out) {
             if (!make_store_map_sw32(&mo, out, (uint64_t)n_out, (uint64_t)out_rows))
                 return cudaErrorInvalidValue;
-            return launch_one_pair<3, true, 16, 2>(mw, ma, mo, p, s);
+            return launch_one_pair<3, true, 16, kPairAtoms>(mw, ma, mo, p, s);
         }
         if (!make_store_map_f32(&mo, out, (uint64_t)n_out, (uint64_t)out_rows))
             return cudaErrorInvalidValue;
-        return launch_one_pair<3, false, 8, 2>(mw, ma, mo, p, s);
+        return launch_one_pair<3, false, 8, kPairAtoms>(mw, ma, mo, p, s);
     }
+    if (!make_map(&mw, W, (uint64_t)K, (uint64_t)c.E * n_out, BM)) return cudaErrorInvalidValue;
     CUtensorMap ma;
     if (!make_map(&ma, A, (uint64_t)K, (uint64_t)a_rows, BOX_ROWS)) return cudaErrorInvalidValue;
     return bf16_out ? launch_one<64, 8, true>(mw, ma, p, s) : launch_one<64, 8, false>(mw, ma, p, s);
@@ -1297,11 +1357,11 @@ cudaError_t launch_segment_reduction_tc(int E, const int32_t* offsets, int64_t r
              koff, tok_rows};
     CUtensorMap mw, mo;
     BMaps mt;
-    if (!make_map(&mw, WT, (uint64_t)kcols, (uint64_t)n_out, BM) ||
-        !make_b_maps(&mt, TOK, (uint64_t)kcols, (uint64_t)tok_rows) ||
+    if (!make_pair_maps(&mw, WT, (uint64_t)kcols, (uint64_t)n_out, &mt, TOK, (uint64_t)tok_rows,
+                        &p.box3d) ||
         !make_store_map_f32(&mo, out, (uint64_t)n_out, (uint64_t)E * tok_rows))
         return cudaErrorInvalidValue;
-    return launch_one_pair<3, false, 8, 2>(mw, mt, mo, p, s);
+    return launch_one_pair<3, false, 8, kPairAtoms>(mw, mt, mo, p, s);
 }
 
 }  // namespace moe
