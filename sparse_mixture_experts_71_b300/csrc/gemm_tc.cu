@@ -830,9 +830,19 @@ struct Cfg2 {
     static_assert(SMEM <= 232448, "shared memory budget");
 };
 
+// Token rows of operand bytes one group of token tiles may hold (see
+// decode_pair_tile): about half the 126 MB L2.
+constexpr long long kGroupBytes = 64ll << 20;
+
 // Pair tile t: expert e (binary search over the per-expert tile prefix),
 // then token tile fastest and 256-row weight tile, so the token tiles that
 // share a weight tile run at about the same time and re-read it from L2.
+// When an expert's token operand (rows x K) is larger than kGroupBytes, its
+// token tiles are taken in groups of GT that fit: within a group, token tile
+// fastest, then weight tile, so a group's token rows stay in L2 while every
+// weight tile passes over them (each weight tile is read once per group,
+// each token row about once) instead of the token rows being read again by
+// every wave of weight tiles.
 __device__ __forceinline__ Tile decode_pair_tile(int t, const int* s_tiles, const Params& p,
                                                  int mt2) {
     int lo = 0, hi = p.E - 1;
@@ -850,12 +860,18 @@ __device__ __forceinline__ Tile decode_pair_tile(int t, const int* s_tiles, cons
     }
     const int nt = (s1 - s0 + BN2 - 1) / BN2;
     const int local = t - s_tiles[lo];
+    int gt = nt;  // token tiles per group
+    if (p.koff == nullptr && (long long)nt * BN2 * p.K * 2 > kGroupBytes)
+        gt = max(1, (int)(kGroupBytes / ((long long)BN2 * p.K * 2)));
+    const int g = local / (gt * mt2);               // group (all but the last are full)
+    const int gsize = min(gt, nt - g * gt);
+    const int lg = local - g * gt * mt2;
     Tile tl;
     tl.e = lo;
-    tl.r0 = s0 + (local % nt) * BN2;
+    tl.r0 = s0 + (g * gt + lg % gsize) * BN2;
     tl.o0 = tl.r0;
     tl.n = min(BN2, s1 - tl.r0);
-    tl.m0 = (local / nt) * 2 * BM;
+    tl.m0 = (lg / gsize) * 2 * BM;
     return tl;
 }
 
