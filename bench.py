@@ -320,32 +320,60 @@ def ffn_roofline(wl, work, ffn_ms, pk, pk_kind):
     return roof
 
 
+def call_roofline(wl, work, step_ms, pk, pk_kind):
+    """Roofline of a decode-sized forward call that moe_forward runs as one
+    fused expert-FFN kernel between the router and the combine: the call's
+    algorithmic bytes (used-expert weights, x, y, W_r) over the timed step,
+    against the measured HBM copy rate."""
+    achieved = work["bytes"] / (step_ms * 1e-3) / 1e9
+    traffic, traffic_src = committed_traffic(wl.name)
+    return {"bound": "hbm", "unit": "GB/s", "peak_source": pk_kind + " HBM copy",
+            "kernel": "whole moe_forward call (router, fused expert-FFN kernel, combine)",
+            "achieved": achieved, "peak": pk["hbm_gbs"], "frac": achieved / pk["hbm_gbs"],
+            "frac_of_8tbs_nominal": achieved / 8000.0,
+            "algorithmic": f"used-expert weights + x + y + W_r = {work['bytes']:.4g} B per call",
+            "traffic": traffic, "traffic_source": traffic_src}
+
+
 TRAFFIC_SUMMARY = os.path.join("profiles", "grouped_gemm_dram_traffic.md")
 
 
 def committed_traffic(workload):
     """DRAM bytes (read + write) of one expert-FFN launch pair of `workload`
-    from the committed ncu summary (its forward GEMM1 and GEMM2 rows), with
-    the summary's path; (None, None) when it has no capture of the workload."""
+    from the committed ncu summary - its forward GEMM1 and GEMM2 rows, or the
+    row of the fused decode kernel when it has one - with the summary's path;
+    (None, None) when it has no capture of the workload."""
     path = os.path.join(ROOT, TRAFFIC_SUMMARY)
     if not os.path.exists(path):
         return None, None
-    total, rows = 0.0, 0
+    pair, fused = [], None
     with open(path) as f:
         for line in f:
             cols = [c.strip() for c in line.strip().strip("|").split("|")]
             if len(cols) < 5 or cols[0].strip("`") != workload:
                 continue
-            if not re.search(r"\bGEMM[12]\b", cols[1]) or "backward" in cols[1]:
-                continue
             try:
-                total += (float(cols[3]) + float(cols[4])) * 1e6
-                rows += 1
+                b = (float(cols[3]) + float(cols[4])) * 1e6
             except ValueError:
                 continue
-    if rows != 2:
+            if "GEMM1 + GEMM2" in cols[1]:
+                fused = b
+            elif re.search(r"\bGEMM[12]\b", cols[1]) and "staged" not in cols[1]:
+                pair.append(b)
+    if fused is not None:
+        return fused, TRAFFIC_SUMMARY
+    if len(pair) != 2:
         return None, None
-    return total, TRAFFIC_SUMMARY
+    return sum(pair), TRAFFIC_SUMMARY
+
+
+def dense_decode(wl) -> bool:
+    """Whether moe_forward takes its dense decode path on this workload (every
+    expert on all T tokens in one fused kernel; the library's condition, see
+    dense_decode in csrc/moe_api.cu)."""
+    return (wl.dtype == "bf16" and wl.routing == "token" and wl.overflow == "drop"
+            and wl.n_shared == 0 and 0 < wl.T <= 64 and wl.T * wl.k < 96 * wl.E
+            and wl.T * wl.k >= 4 * wl.E)
 
 
 def measure_workload(args, wl, dev, stream, flush, world, e2e=True):
@@ -490,8 +518,9 @@ def measure_workload(args, wl, dev, stream, flush, world, e2e=True):
            "stages_ms": {name: statistics.mean(v) for name, v in stage_ms.items()},
            "stages_ms_median": {name: statistics.median(v) for name, v in stage_ms.items()},
            "kept_assignments": work["kept"], "experts_used": work["experts_used"],
-           "roofline": ffn_roofline(wl, work, statistics.mean(stage_ms["expert_ffn"]), pk,
-                                    pk_kind),
+           "roofline": (call_roofline(wl, work, ms_per_step, pk, pk_kind) if dense_decode(wl)
+                        else ffn_roofline(wl, work, statistics.mean(stage_ms["expert_ffn"]), pk,
+                                          pk_kind)),
            "gpu_launches": K * sum(kernels.values()) + (3 if e2e else 2) * K * kernels["forward"],
            "clocks": sampler.summary(),
            "l2": "flushed before every timed step and before every stage-graph step "
