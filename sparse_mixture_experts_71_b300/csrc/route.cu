@@ -723,8 +723,13 @@ RouteGeom route_geom(const moe_config& c) {
     } else if (c.E <= 32) {
         g.warp = true;
         int tw = c.E <= 16 ? 4 : 2, ds = 1;
-        while (tw > 1 && (c.T + kWarps * tw - 1) / (kWarps * tw) < kTargetBlocks) tw /= 2;
-        while (tw == 1 && ds < kWarps && (c.T * ds + kWarps - 1) / kWarps < kTargetBlocks) ds *= 2;
+        // the dense decode path runs the router beside the expert FFN, which
+        // it only has to beat to the combine: few blocks leave the SMs to the FFN
+        if (!dense_decode(c)) {
+            while (tw > 1 && (c.T + kWarps * tw - 1) / (kWarps * tw) < kTargetBlocks) tw /= 2;
+            while (tw == 1 && ds < kWarps && (c.T * ds + kWarps - 1) / kWarps < kTargetBlocks)
+                ds *= 2;
+        }
         g.tw = tw;
         g.ds = ds;
         g.tokens = (kWarps / ds) * tw;
