@@ -421,16 +421,18 @@ moe_status moe_forward(const moe_config* cfg, const void* x, const float* W_r,
         if (cudaMemsetAsync(at<char>(ws, L.counts), 0, L.blk_p - L.counts, s) != cudaSuccess)
             return MOE_ERR_CUDA;
         DeviceHeader* hdr = at<DeviceHeader>(ws, L.header);
+        WsLayout Lr = L;  // the router in few blocks: it runs beside the FFN
+        Lr.route = route_geom_beside(routed_config(c));
         chain_begin();
         ChainProgrammatic pdl_chain;
         cudaError_t e = launch_route_no_finish(c, x, W_r, logit_bias, logit_noise, logits_out, idx,
-                                               w, ws, L, s);
+                                               w, ws, Lr, s);
         if (e == cudaSuccess)
             e = launch_dense_ffn(c, x, W1, b1, W2, b2, at<void>(ws, L.h), y_perm,
                                  at<int32_t>(ws, L.sched), hdr, s);
         if (e == cudaSuccess)
             e = launch_dense_combine(c, y_perm, idx, w, y, hdr,
-                                     route_loss_args(c, ws, L, expert_counts, aux_out, z_loss_out),
+                                     route_loss_args(c, ws, Lr, expert_counts, aux_out, z_loss_out),
                                      expert_counts != nullptr || aux_out != nullptr ||
                                          z_loss_out != nullptr,
                                      s);

@@ -54,6 +54,11 @@ struct RouteGeom {
     int blocks;
 };
 RouteGeom route_geom(const moe_config& c);
+// Geometry of a router that runs beside a long kernel and only has to finish
+// before a later one (the dense decode path): the fewest blocks of the same
+// kernel, never more than route_geom's (so it fits the workspace regions
+// route_geom sized).
+RouteGeom route_geom_beside(const moe_config& c);
 
 // Byte offsets of the workspace regions for one configuration.
 struct WsLayout {

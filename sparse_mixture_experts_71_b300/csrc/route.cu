@@ -567,8 +567,10 @@ cudaError_t launch_warp(const RouteArgs& a, cudaStream_t s) {
 
 template <typename TX, int EMAX>
 cudaError_t launch_warp_tw(const RouteArgs& a, const RouteGeom& g, cudaStream_t s) {
-    if (g.tw >= 4) return launch_warp<TX, EMAX, 4, 1>(a, s);
-    if (g.tw == 2) return launch_warp<TX, EMAX, 2, 1>(a, s);
+    if (g.tw >= 4) return g.ds == kWarps ? launch_warp<TX, EMAX, 4, kWarps>(a, s)
+                                         : launch_warp<TX, EMAX, 4, 1>(a, s);
+    if (g.tw == 2) return g.ds == kWarps ? launch_warp<TX, EMAX, 2, kWarps>(a, s)
+                                         : launch_warp<TX, EMAX, 2, 1>(a, s);
     if (g.ds >= 8) return launch_warp<TX, EMAX, 1, 8>(a, s);
     if (g.ds == 4) return launch_warp<TX, EMAX, 1, 4>(a, s);
     if (g.ds == 2) return launch_warp<TX, EMAX, 1, 2>(a, s);
@@ -723,13 +725,8 @@ RouteGeom route_geom(const moe_config& c) {
     } else if (c.E <= 32) {
         g.warp = true;
         int tw = c.E <= 16 ? 4 : 2, ds = 1;
-        // the dense decode path runs the router beside the expert FFN, which
-        // it only has to beat to the combine: few blocks leave the SMs to the FFN
-        if (!dense_decode(c)) {
-            while (tw > 1 && (c.T + kWarps * tw - 1) / (kWarps * tw) < kTargetBlocks) tw /= 2;
-            while (tw == 1 && ds < kWarps && (c.T * ds + kWarps - 1) / kWarps < kTargetBlocks)
-                ds *= 2;
-        }
+        while (tw > 1 && (c.T + kWarps * tw - 1) / (kWarps * tw) < kTargetBlocks) tw /= 2;
+        while (tw == 1 && ds < kWarps && (c.T * ds + kWarps - 1) / kWarps < kTargetBlocks) ds *= 2;
         g.tw = tw;
         g.ds = ds;
         g.tokens = (kWarps / ds) * tw;
@@ -781,6 +778,20 @@ cudaError_t route_kernels(const moe_config& c, const RouteArgs& a, void* ws, con
 }
 
 }  // namespace
+
+RouteGeom route_geom_beside(const moe_config& c) {
+    RouteGeom g = route_geom(c);
+    // the warp kernel with d split over all eight warps (as route_geom picks
+    // for small batches): more tokens per warp group cut the blocks and leave
+    // each token's sum - split partials added in split order - unchanged, so
+    // the logits are route_geom's to the bit
+    if (g.warp && g.tw == 1 && g.ds == kWarps) {
+        g.tw = c.E <= 16 ? 4 : 2;
+        g.tokens = (kWarps / g.ds) * g.tw;
+        g.blocks = (c.T + g.tokens - 1) / g.tokens;
+    }
+    return g;
+}
 
 cudaError_t launch_route(const moe_config& c, const void* x, const float* W_r,
                          const float* logit_bias, const float* logit_noise,

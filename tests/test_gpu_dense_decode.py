@@ -37,11 +37,15 @@ def test_dense_decode_forward(wl):
     run = LibRun(wl, inp)
     staged = run.staged()
     f = run.forward()
-    # routing outputs and the losses: the same kernels, the same bits
+    # routing outputs: the same router kernel, the same bits
     assert torch.equal(f["logits"], staged["logits"])
     assert torch.equal(f["counts"], staged["counts"])
-    assert torch.equal(f["aux"], staged["aux"])
-    assert torch.equal(f["z"], staged["z"])
+    # the losses: the forward runs the router in fewer, larger blocks, so the
+    # per-block partial sums of p and of the squared log-sum-exp add up in
+    # another order - within two fp32 ulps of the staged calls' values
+    for key in ("aux", "z"):
+        a, b = float(f[key][0]), float(staged[key][0])
+        assert abs(a - b) <= 2.4e-7 * max(abs(b), 1e-30), (key, a, b)
     # the layer output: the sparse path's bits
     assert torch.equal(f["y"], staged["y"]), (
         f"max |dense - sparse| {float((f['y'].float() - staged['y'].float()).abs().max()):.3e}")
