@@ -536,41 +536,56 @@ def gelu_grad(u) -> np.ndarray:
 
 def moe_backward(x, W_r, W1, b1, W2, b2, dy, k: int, renormalize: bool = True,
                  capacity: int | None = None, logit_bias=None, logits=None,
-                 aux_grad: float = 0.0, z_grad: float = 0.0) -> dict:
+                 aux_grad: float = 0.0, z_grad: float = 0.0, n_shared: int = 0,
+                 reroute: bool = False) -> dict:
     """Gradients of L = <dy, y> + aux_grad * aux + z_grad * z_loss.
 
     The training step behind [LECTURE] "The MoE layer" (the layer is trained
     end to end with the load-balancing loss of "The central problem: load
     balancing"; [DAY59] "Load-balancing losses encourage better routing").
-    Routing decisions (top-k, capacity) are constants.  Per kept assignment
-    (token t, expert e, weight w): u = W1_e x + b1_e, h = GELU(u),
+    Routing decisions (top-k, capacity, rerouting) are constants.  Per kept
+    assignment (token t, expert e, weight w): u = W1_e x + b1_e, h = GELU(u),
     o = W2_e h + b2_e, y_t += w o; hence do = w dy_t, dW2_e += do h^T,
     db2_e += do, du = (W2_e^T do) * GELU'(u), dW1_e += du x^T, db1_e += du,
-    dx_t += W1_e^T du, and s = <dy_t, w o> feeds the logits: with the weights
-    a softmax over the token's k choices (renormalised) dg_e = s_e - w_e
-    sum_j s_j on the choices and 0 elsewhere; with w = p (not renormalised)
-    dg_e = s_e - p_e sum_j s_j.  The auxiliary loss adds
-    aux_grad E / T * p_e (f_e - sum_i f_i p_i), the z-loss
+    dx_t += W1_e^T du, and s = <dy_t, w o> feeds the logits through w.
+
+    A routed slot j of token t has final expert f_j (its choice c_j, or with
+    ``reroute`` the expert a dropped slot moved to) and weight w_j = p_{f_j} / S
+    with S the sum of p over the token's k choices (renormalised; S = 1
+    otherwise).  With p the softmax of g:
+        dw_j/dg_m = w_j [m = f_j] - w_j p_m ([m in choices] / S   (renormalised)
+                                             1                    (otherwise)),
+    so dg_m = sum over the kept slots with f_j = m of s_j - (sum_j s_j) *
+    (p_m / S if m is a choice, else 0) when renormalised, and
+    dg_m = sum_{f_j = m} s_j - p_m sum_j s_j otherwise; a dropped slot has
+    s_j = 0 but its choice still counts in S.  Shared experts (``n_shared``,
+    [LECTURE] "Design variations") have weight 1: their slots add to the
+    expert gradients and dx but not to the logits, which cover the routed
+    experts only.  The auxiliary loss adds aux_grad E / T * p_e (f_e -
+    sum_i f_i p_i) (f from the first choice), the z-loss
     z_grad 2 / T * lse_t p_e.  Then dW_r = dg^T x and dx += dg W_r.
     ``logits`` replaces the router GEMM as in moe_forward (W_r still gets
-    its gradient from dg).  Returns dx (T, d), dW_r (E, d), dW1, db1, dW2,
-    db2, all fp64, and dg (T, E).
+    its gradient from dg).  Returns dx (T, d), dW_r (E - n_shared, d), dW1,
+    db1, dW2, db2, all fp64, and dg (T, E - n_shared).
     """
     x = np.asarray(x, f64)
     dy = np.asarray(dy, f64)
     T, d = x.shape
     r = moe_forward(x, W_r, W1, b1, W2, b2, k=k, renormalize=renormalize, capacity=capacity,
-                    logit_bias=logit_bias, logits=logits, layout=False)
-    E = r.logits.shape[1]
+                    logit_bias=logit_bias, logits=logits, layout=False, n_shared=n_shared,
+                    reroute=reroute)
+    E_r = r.logits.shape[1]
     p = r.probs
     g = np.asarray(r.logits, f64)
+    choices = top_k(r.logits, k)  # (T, k) routed expert ids, the weights' normaliser
     W1, b1, W2, b2 = (np.asarray(a, f64) for a in (W1, b1, W2, b2))
+    K = r.idx.shape[1]
     dx = np.zeros((T, d))
     dW1, db1 = np.zeros_like(W1), np.zeros_like(b1)
     dW2, db2 = np.zeros_like(W2), np.zeros_like(b2)
-    s = np.zeros((T, k))  # <dy_t, w o> per slot (0 when dropped)
+    s = np.zeros((T, K))  # <dy_t, w o> per slot (0 when dropped)
     for t in range(T):
-        for j in range(k):
+        for j in range(K):
             if not r.kept[t, j]:
                 continue
             e, w = int(r.idx[t, j]), r.w[t, j]
@@ -585,21 +600,68 @@ def moe_backward(x, W_r, W1, b1, W2, b2, dy, k: int, renormalize: bool = True,
             dW1[e] += np.outer(du, x[t])
             db1[e] += du
             dx[t] += W1[e].T @ du
-    dg = np.zeros((T, E))
+    dg = np.zeros((T, E_r))
     for t in range(T):
-        sel = r.idx[t]
-        tot = s[t].sum()
+        tot = s[t, :k].sum()  # the routed slots
+        for j in range(k):
+            if r.kept[t, j]:
+                dg[t, int(r.idx[t, j]) - n_shared] += s[t, j]
         if renormalize:
-            for j in range(k):
-                dg[t, sel[j]] += s[t, j] - r.w[t, j] * tot
+            S = p[t, choices[t]].sum()
+            for c in choices[t]:
+                dg[t, c] -= tot * p[t, c] / S
         else:
             dg[t] -= p[t] * tot
-            for j in range(k):
-                dg[t, sel[j]] += s[t, j]
     if aux_grad:
-        f = np.bincount(np.asarray(r.idx[:, 0], np.int64), minlength=E) / T
+        f = np.bincount(np.asarray(choices[:, 0], np.int64), minlength=E_r) / T
         fp = (p * f[None, :]).sum(axis=1, keepdims=True)
-        dg += aux_grad * E / T * p * (f[None, :] - fp)
+        dg += aux_grad * E_r / T * p * (f[None, :] - fp)
+    if z_grad:
+        m = g.max(axis=1, keepdims=True)
+        lse = m + np.log(np.exp(g - m).sum(axis=1, keepdims=True))
+        dg += z_grad * 2.0 / T * lse * p
+    dW_r = dg.T @ x
+    dx += dg @ np.asarray(W_r, f64)
+    return dict(dx=dx, dW_r=dW_r, dW1=dW1, db1=db1, dW2=dW2, db2=db2, dg=dg)
+
+
+def expert_choice_backward(x, W_r, W1, b1, W2, b2, dy, k: int, capacity: int | None = None,
+                           logit_bias=None, logits=None, sel=None, z_grad: float = 0.0) -> dict:
+    """Gradients of L = <dy, y> + z_grad * z_loss for the expert-choice layer
+    (expert_choice_forward; [LECTURE] "Design variations"), the selection
+    held constant.  Each chosen (token t, expert e) adds y_t += p_{t,e} o_e(x_t):
+    the expert gradients as in moe_backward with w = p_{t,e}, and with
+    s_{t,e} = <dy_t, p_{t,e} o> the softmax gives dg_{t,m} = s_{t,m} [m chose t]
+    - p_{t,m} sum_e s_{t,e}.  There is no balancing loss.  Returns dx, dW_r,
+    dW1, db1, dW2, db2 (fp64) and dg (T, E)."""
+    x = np.asarray(x, f64)
+    dy = np.asarray(dy, f64)
+    T, d = x.shape
+    r = expert_choice_forward(x, W_r, W1, b1, W2, b2, k=k, capacity=capacity,
+                              logit_bias=logit_bias, logits=logits, sel=sel)
+    E = r.logits.shape[1]
+    p = r.probs
+    g = np.asarray(r.logits, f64)
+    W1, b1, W2, b2 = (np.asarray(a, f64) for a in (W1, b1, W2, b2))
+    dx = np.zeros((T, d))
+    dW1, db1 = np.zeros_like(W1), np.zeros_like(b1)
+    dW2, db2 = np.zeros_like(W2), np.zeros_like(b2)
+    s = np.zeros((T, E))
+    for e in range(E):
+        for j in range(r.C):
+            t, w = int(r.sel[e, j]), r.w[e, j]
+            u = W1[e] @ x[t] + b1[e]
+            h = gelu(u)
+            o = W2[e] @ h + b2[e]
+            s[t, e] = w * float(dy[t] @ o)
+            do = w * dy[t]
+            dW2[e] += np.outer(do, h)
+            db2[e] += do
+            du = (W2[e].T @ do) * gelu_grad(u)
+            dW1[e] += np.outer(du, x[t])
+            db1[e] += du
+            dx[t] += W1[e].T @ du
+    dg = s - p * s.sum(axis=1, keepdims=True)
     if z_grad:
         m = g.max(axis=1, keepdims=True)
         lse = m + np.log(np.exp(g - m).sum(axis=1, keepdims=True))

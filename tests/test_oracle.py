@@ -930,3 +930,185 @@ def test_planted_backward_mistakes_are_caught(monkeypatch):
     with pytest.raises(AssertionError):
         test_backward_matches_torch_autograd(2, True, None, 0.0, 0.0)
     monkeypatch.setattr(O, "gelu_grad", good)
+
+
+# ---- backward of the layer variants: shared experts, rerouting on overflow,
+# expert choice; each against torch autograd of the same layer with its
+# routing decisions held fixed (the oracle's fp32 logit rounding added as a
+# constant, as in _torch_loss)
+
+def _torch_router(t, r_logits, bias=None):
+    g64 = t["x"] @ t["W_r"].T
+    if bias is not None:
+        g64 = g64 + torch.tensor(np.asarray(bias, np.float64))
+    return g64 + (torch.tensor(r_logits.astype(np.float64)) - g64).detach()
+
+
+def _torch_variant_loss(L, dy, k, renorm, cap, aux_grad, z_grad, n_shared=0, reroute=False,
+                        bias=None):
+    """The layer in torch: routed slot j of token t has final expert f_j (the
+    oracle's decision, held fixed) and weight p_{f_j} / sum over the token's
+    k choices of p (renormalised) or p_{f_j}; shared experts weight 1."""
+    r = O.moe_forward(**L, k=k, renormalize=renorm, capacity=cap, n_shared=n_shared,
+                      reroute=reroute, logit_bias=bias)
+    t = {n: torch.tensor(np.asarray(v, np.float64), requires_grad=True) for n, v in L.items()}
+    g = _torch_router(t, r.logits, bias)
+    p = torch.softmax(g, dim=1)
+    choices = torch.tensor(O.top_k(r.logits, k), dtype=torch.int64)
+    S = p.gather(1, choices).sum(1) if renorm else torch.ones(g.shape[0], dtype=torch.float64)
+    T = g.shape[0]
+    ys = []
+    for tok in range(T):
+        yt = torch.zeros(t["x"].shape[1], dtype=torch.float64)
+        for j in range(r.idx.shape[1]):
+            if not r.kept[tok, j]:
+                continue
+            e = int(r.idx[tok, j])
+            w = 1.0 if j >= k else p[tok, e - n_shared] / S[tok]
+            h = TF.gelu(t["W1"][e] @ t["x"][tok] + t["b1"][e])
+            yt = yt + w * (t["W2"][e] @ h + t["b2"][e])
+        ys.append(yt)
+    y = torch.stack(ys)
+    assert np.allclose(y.detach().numpy(), r.y, rtol=1e-12, atol=1e-12)  # the oracle's forward
+    E_r = g.shape[1]
+    f = torch.tensor(np.bincount(O.top_k(r.logits, k)[:, 0], minlength=E_r) / T)
+    aux = E_r * (f * p.mean(0)).sum()
+    z = torch.logsumexp(g, dim=1).pow(2).mean()
+    loss = (torch.tensor(dy) * y).sum() + aux_grad * aux + z_grad * z
+    loss.backward()
+    return {n: t[n].grad.numpy() for n in t}
+
+
+_GRADS = (("x", "dx"), ("W_r", "dW_r"), ("W1", "dW1"), ("b1", "db1"), ("W2", "dW2"), ("b2", "db2"))
+
+
+@pytest.mark.parametrize("k,renorm,cap,aux_grad,z_grad,ns", [
+    (2, True, None, 0.0, 0.0, 1), (1, False, None, 0.2, 0.0, 1), (2, True, 3, 0.3, 0.4, 2),
+    (1, True, 2, 0.0, 1.0, 1)])
+def test_backward_shared_experts_matches_torch_autograd(k, renorm, cap, aux_grad, z_grad, ns):
+    E = 5
+    L = _rand_layer(T=12, d=6, F=7, E=E, seed=60 + ns)
+    L["W_r"] = L["W_r"][: E - ns]  # the router covers the routed experts
+    dy = np.random.default_rng(61).standard_normal((12, 6))
+    want = _torch_variant_loss(L, dy, k, renorm, cap, aux_grad, z_grad, n_shared=ns)
+    got = O.moe_backward(**L, dy=dy, k=k, renormalize=renorm, capacity=cap, aux_grad=aux_grad,
+                         z_grad=z_grad, n_shared=ns)
+    for n, gname in _GRADS:
+        np.testing.assert_allclose(got[gname], want[n], rtol=1e-10, atol=1e-12, err_msg=gname)
+    assert got["dW_r"].shape == (E - ns, 6)
+    # the shared experts see every token
+    assert np.all(np.abs(got["db2"][:ns]).sum(axis=1) > 0)
+
+
+@pytest.mark.parametrize("k,renorm,cap,aux_grad,z_grad", [
+    (1, False, 3, 0.0, 0.0), (2, True, 4, 0.0, 0.0), (2, True, 3, 0.5, 0.3), (1, True, 2, 0.1, 0.0),
+    (2, False, 4, 0.0, 0.2)])
+def test_backward_reroute_matches_torch_autograd(k, renorm, cap, aux_grad, z_grad):
+    L = _rand_layer(T=12, d=5, F=6, E=6, seed=70 + k)
+    bias = np.array([1.5, 1.0, 0.2, -0.5, -1.0, -1.5], np.float32)  # skewed load: overflow
+    dy = np.random.default_rng(71).standard_normal((12, 5))
+    r = O.moe_forward(**L, k=k, renormalize=renorm, capacity=cap, reroute=True, logit_bias=bias)
+    moved = r.kept & (r.idx != O.top_k(r.logits, k))
+    assert moved.any()  # the cap moves some slots to their next-best expert
+    want = _torch_variant_loss(L, dy, k, renorm, cap, aux_grad, z_grad, reroute=True, bias=bias)
+    got = O.moe_backward(**L, dy=dy, k=k, renormalize=renorm, capacity=cap, aux_grad=aux_grad,
+                         z_grad=z_grad, reroute=True, logit_bias=bias)
+    for n, gname in _GRADS:
+        np.testing.assert_allclose(got[gname], want[n], rtol=1e-10, atol=1e-12, err_msg=gname)
+
+
+def test_backward_reroute_without_moves_equals_drop():
+    """No slot moves (a cap no expert reaches): rerouting's gradients are the
+    dropping layer's."""
+    L = _rand_layer(T=8, d=4, F=5, E=4, seed=75)
+    dy = np.random.default_rng(76).standard_normal((8, 4))
+    a = O.moe_backward(**L, dy=dy, k=2, capacity=8, reroute=True, aux_grad=0.2)
+    b = O.moe_backward(**L, dy=dy, k=2, capacity=8, reroute=False, aux_grad=0.2)
+    for _, gname in _GRADS:
+        np.testing.assert_array_equal(a[gname], b[gname])
+
+
+def _torch_ec_loss(L, dy, k, cap, z_grad):
+    r = O.expert_choice_forward(**L, k=k, capacity=cap)
+    t = {n: torch.tensor(np.asarray(v, np.float64), requires_grad=True) for n, v in L.items()}
+    g = _torch_router(t, r.logits)
+    p = torch.softmax(g, dim=1)
+    T, E = g.shape
+    rows = [[] for _ in range(T)]
+    for e in range(E):
+        for j in range(r.C):
+            rows[int(r.sel[e, j])].append(e)
+    ys = []
+    for tok in range(T):
+        yt = torch.zeros(t["x"].shape[1], dtype=torch.float64)
+        for e in rows[tok]:
+            h = TF.gelu(t["W1"][e] @ t["x"][tok] + t["b1"][e])
+            yt = yt + p[tok, e] * (t["W2"][e] @ h + t["b2"][e])
+        ys.append(yt)
+    y = torch.stack(ys)
+    assert np.allclose(y.detach().numpy(), r.y, rtol=1e-12, atol=1e-12)
+    z = torch.logsumexp(g, dim=1).pow(2).mean()
+    ((torch.tensor(dy) * y).sum() + z_grad * z).backward()
+    return {n: t[n].grad.numpy() for n in t}
+
+
+@pytest.mark.parametrize("k,cap,z_grad", [(2, None, 0.0), (1, 3, 0.5), (2, 9, 0.0), (3, None, 1.0)])
+def test_backward_expert_choice_matches_torch_autograd(k, cap, z_grad):
+    L = _rand_layer(T=9, d=5, F=6, E=4, seed=80 + k)
+    dy = np.random.default_rng(81).standard_normal((9, 5))
+    want = _torch_ec_loss(L, dy, k, cap, z_grad)
+    got = O.expert_choice_backward(**L, dy=dy, k=k, capacity=cap, z_grad=z_grad)
+    for n, gname in _GRADS:
+        np.testing.assert_allclose(got[gname], want[n], rtol=1e-10, atol=1e-12, err_msg=gname)
+
+
+def test_backward_expert_choice_every_token_is_the_soft_mixture():
+    """C = T: every expert takes every token, y = sum_e p_e f_e(x), whose
+    router gradient is the softmax's: dg = s - p sum s (finite differences in
+    W_r agree)."""
+    L = _rand_layer(T=5, d=4, F=5, E=3, seed=85)
+    dy = np.random.default_rng(86).standard_normal((5, 4))
+    got = O.expert_choice_backward(**L, dy=dy, k=3, capacity=5)
+    eps = 1e-3
+    for pos in ((0, 1), (2, 3)):
+        a = {n: np.array(v, np.float64) for n, v in L.items()}
+        b = {n: np.array(v, np.float64) for n, v in L.items()}
+        a["W_r"][pos] += eps
+        b["W_r"][pos] -= eps
+        la = float((dy * O.expert_choice_forward(**a, k=3, capacity=5).y).sum())
+        lb = float((dy * O.expert_choice_forward(**b, k=3, capacity=5).y).sum())
+        fd = (la - lb) / (2 * eps)
+        assert abs(fd - got["dW_r"][pos]) <= 5e-5 * max(1.0, abs(fd)), (pos, fd, got["dW_r"][pos])
+
+
+def test_planted_variant_backward_mistakes_are_caught(monkeypatch):
+    """Planted in the oracle's forward (which its backward differentiates): a
+    rerouted slot keeping the weight of the choice it was dropped from, and
+    shared experts weighted by 1/2 instead of 1 - each fails its autograd pin."""
+    good = O.moe_forward
+
+    def wrong_reroute_weight(*a, **kw):
+        r = good(*a, **kw)
+        if kw.get("reroute"):
+            ch = O.top_k(r.logits, kw["k"])
+            p = np.take_along_axis(r.probs, ch, axis=1)
+            S = p.sum(axis=1, keepdims=True) if kw.get("renormalize", True) else 1.0
+            moved = r.kept & (r.idx != ch)
+            r.w = np.where(moved, p / S, r.w)
+        return r
+
+    monkeypatch.setattr(O, "moe_forward", wrong_reroute_weight)
+    with pytest.raises(AssertionError):
+        test_backward_reroute_matches_torch_autograd(2, True, 4, 0.0, 0.0)
+
+    def wrong_shared_weight(*a, **kw):
+        r = good(*a, **kw)
+        if kw.get("n_shared"):
+            r.w = r.w.copy()
+            r.w[:, kw["k"]:] = 0.5
+        return r
+
+    monkeypatch.setattr(O, "moe_forward", wrong_shared_weight)
+    with pytest.raises(AssertionError):
+        test_backward_shared_experts_matches_torch_autograd(2, True, None, 0.0, 0.0, 1)
+    monkeypatch.setattr(O, "moe_forward", good)
