@@ -667,6 +667,35 @@ def bench_ours(args, wl):
     return 0
 
 
+def kept_per_expert(cfg, wl, D, dev):
+    """Rows each expert keeps on this batch (the stage calls' offsets)."""
+    import torch
+    from sparse_mixture_experts_71_b300 import binding as B
+    T, E, d = wl.T, wl.E, wl.d
+    ec = wl.routing == "expert"
+    k = wl.k + wl.n_shared
+    n = max(E * B.expert_choice_capacity(cfg) if ec else T * k, 1)
+    i32, f32 = torch.int32, torch.float32
+    kr = B.ranked_columns(cfg)
+    ws = B.workspace(cfg, device=dev)
+    offsets = torch.empty(E + 1, dtype=i32, device=dev)
+    slot_of = torch.empty((T, E if ec else k), dtype=i32, device=dev)
+    perm_token = torch.empty(n, dtype=i32, device=dev)
+    perm_w = torch.empty(n, dtype=f32, device=dev)
+    x_perm = torch.empty((n, d), dtype=D["x"].dtype, device=dev)
+    if ec:
+        B.route_expert_choice(cfg, D["x"], D["W_r"], offsets, perm_token, perm_w, slot_of, ws,
+                              x_perm=x_perm, logit_bias=D["logit_bias"])
+    else:
+        idx = torch.empty((T, kr), dtype=i32, device=dev)
+        w = torch.empty((T, kr), dtype=f32, device=dev)
+        B.route(cfg, D["x"], D["W_r"], idx, w, ws, logit_bias=D["logit_bias"])
+        B.dispatch(cfg, D["x"], idx, offsets, slot_of, perm_token, x_perm, ws, topk_w=w,
+                   perm_w=perm_w)
+    torch.cuda.synchronize(dev)
+    return [int(v) for v in torch.diff(offsets).cpu().tolist()]
+
+
 def bench_backward(args, wl):
     """One step = one moe_backward call (it recomputes the forward
     intermediates it needs) on the workload's inputs and a seeded dy."""
@@ -680,20 +709,19 @@ def bench_backward(args, wl):
     dev = torch.device("cuda", local)
     if world > 1:
         dist.init_process_group("nccl", device_id=dev)
-    if not (wl.dtype == "bf16" and wl.routing == "token" and wl.overflow == "drop"
-            and wl.n_shared == 0):
-        raise SystemExit(f"{wl.name}: the backward pass covers bf16 token-choice layers that "
-                         "drop on overflow")
+    if wl.dtype != "bf16":
+        raise SystemExit(f"{wl.name}: the backward pass covers bf16 layers")
     inp = I.make_inputs(wl, seed=0)
     D = device_inputs(inp, dev)
     layer = MoELayer(D["W_r"], D["W1"], D["b1"], D["W2"], D["b2"], k=wl.k, capacity=wl.capacity,
-                     renormalize=wl.renormalize, logit_bias=D["logit_bias"])
+                     renormalize=wl.renormalize, logit_bias=D["logit_bias"], routing=wl.routing,
+                     overflow=wl.overflow, n_shared=wl.n_shared)
     cfg = layer.config(wl.T)
     T, d, F, E = wl.T, wl.d, wl.F, wl.E
     ws = B.backward_workspace(cfg, device=dev)
     dy = torch.from_numpy(I.router_noise(T, d, 1.0, seed=1)).to(torch.bfloat16).to(dev)
     f32 = dict(dtype=torch.float32, device=dev)
-    g = dict(dx=torch.empty_like(D["x"]), dW_r=torch.empty((E, d), **f32),
+    g = dict(dx=torch.empty_like(D["x"]), dW_r=torch.empty(tuple(D["W_r"].shape), **f32),
              dW1=torch.empty((E, F, d), **f32), db1=torch.empty((E, F), **f32),
              dW2=torch.empty((E, d, F), **f32), db2=torch.empty((E, d), **f32))
     flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
@@ -713,9 +741,7 @@ def bench_backward(args, wl):
         flush.fill_(1)
         graph.replay()
     torch.cuda.synchronize(dev)
-    # kept assignments of this batch, from the forward layer call
-    counts = torch.empty(E, dtype=torch.int32, device=dev)
-    layer.forward(D["x"], expert_counts=counts)
+    kept = sum(kept_per_expert(cfg, wl, D, dev))  # kept assignments of this batch
     ev = [[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in range(args.steps)]
     sampler = ClockSampler(local)
     if world > 1:
@@ -730,10 +756,9 @@ def bench_backward(args, wl):
         torch.cuda.synchronize(dev)
     total_ms = slowest_rank_ms(sum(e0.elapsed_time(e1) for e0, e1 in ev), world, dev)
     ms = total_ms / args.steps
-    cnt = counts.cpu().numpy()
-    kept = int(np.minimum(cnt, wl.capacity).sum()) if wl.capacity is not None else int(cnt.sum())
-    # 2 forward GEMMs recomputed + dH, dX and the two weight-gradient GEMMs
-    flops = 12.0 * kept * d * F + 3 * 2.0 * T * d * E
+    # 2 forward GEMMs recomputed + dH, dX and the two weight-gradient GEMMs;
+    # the router's logits, dx and dW_r products over the routed experts
+    flops = 12.0 * kept * d * F + 3 * 2.0 * T * d * (E - wl.n_shared)
     pk, pk_kind = peaks()
     clocks = sampler.summary()
     achieved = flops / (ms * 1e-3) / 1e12
@@ -744,7 +769,8 @@ def bench_backward(args, wl):
             "data": "synthetic",
             "config": {"workload": wl.name, "pass": "backward", "T": T, "d": d, "d_ff": F,
                        "E": E, "k": wl.k, "capacity": wl.capacity,
-                       "parallelism": f"replicas{world}",
+                       "routing": wl.routing, "overflow": wl.overflow,
+                       "n_shared": wl.n_shared, "parallelism": f"replicas{world}",
                        "l2": "flushed before every timed step (256 MiB write, untimed)"},
             "kernels_per_step": kernels, "kept_assignments": kept,
             "roofline": {"bound": "tensor", "kernel": f"whole backward call ({kernels} launches)",

@@ -18,25 +18,36 @@
  *     dW2_e += (w dy_t) h^T, db2_e += w dy_t,
  *     du = (W2_e^T (w dy_t)) * GELU'(u), dW1_e += du x_t^T, db1_e += du,
  *     dx_t += W1_e^T du,
- * and with s = <dy_t, w o> per slot the logit gradient dg (renormalised:
+ * and with s = <dy_t, w o> per routed slot the logit gradient dg (renormalised:
  * s_e - w_e sum_j s_j on the choices; raw probabilities: s_e [e chosen] -
  * p_e sum_j s_j) plus the two loss terms gives dW_r = dg^T x and
- * dx += dg W_r.
+ * dx += dg W_r.  The layer variants of moe.h follow the same rule:
+ *   shared experts   the n_shared always-on slots (weight 1) feed the expert
+ *                    gradients and dx but no logit; the router covers the
+ *                    E - n_shared routed experts;
+ *   rerouting        a slot moved to another expert has that expert's
+ *                    probability as its weight (over the same normaliser as
+ *                    the token's k choices), so its s goes to the new
+ *                    expert's logit;
+ *   expert choice    each selected (expert, token) pair has weight p_e(t);
+ *                    dg_e = s_e - p_e sum_j s_j over the token's pairs, and
+ *                    there is no balancing loss (aux_grad is ignored).
  *
  * The call recomputes the forward intermediates it needs (routing, dispatch,
  * the expert pre-activations, the expert outputs) from x and the weights:
  * it does not read a previous moe_forward's workspace.
  *
- * Supported: cfg->dtype = MOE_BF16, token choice, drop on overflow,
- * n_shared = 0 (others return MOE_ERR_UNSUPPORTED).
+ * Supported: cfg->dtype = MOE_BF16, every routing, overflow and n_shared
+ * setting moe_forward accepts (fp32 layers return MOE_ERR_UNSUPPORTED).
  *
  * Arguments (device pointers, caller-owned, layouts as in moe.h):
- *   x [T][d] bf16; W_r [E][d] fp32; logit_bias [E] fp32 or NULL;
+ *   x [T][d] bf16; W_r [E - n_shared][d] fp32;
+ *   logit_bias [E - n_shared] fp32 or NULL;
  *   W1 [E][d_ff][d], b1 [E][d_ff], W2 [E][d][d_ff], b2 [E][d] bf16;
  *   dy [T][d] bf16                       upstream gradient of y
  *   aux_grad, z_grad                     weights of the two losses in L
  *   dx [T][d] bf16                       written (not accumulated)
- *   dW_r [E][d], dW1 [E][d_ff][d], db1 [E][d_ff], dW2 [E][d][d_ff],
+ *   dW_r [E - n_shared][d], dW1 [E][d_ff][d], db1 [E][d_ff], dW2 [E][d][d_ff],
  *   db2 [E][d]                           fp32, written (not accumulated)
  *   ws, ws_bytes                         at least
  *                                        moe_backward_workspace_size(cfg)

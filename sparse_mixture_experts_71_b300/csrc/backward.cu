@@ -90,15 +90,33 @@ __device__ __forceinline__ uint4 pack8(const float* f) {
     return q;
 }
 
-// One warp per token: the slot scores s_j, dY_perm rows and the logit
-// gradient dg[t][:].
+// How the routed slots of a token map to logit columns (router_grad_kernel).
+enum GradMode {
+    kGradChoice = 0,   // slot j < kr: the token's choice j (shared experts: routed ids)
+    kGradReroute = 1,  // slot j: its choice if the drop pass kept it, else the expert it moved to
+    kGradExpert = 2,   // expert choice: slot j is expert j
+};
+
+// One warp per token: the slot scores s_j = <dy_t, w_j o_j> over its K slots
+// (w_j = perm_w of the slot's row), the dY_perm rows w_j dy_t, and the logit
+// gradient dg[t][:] over the El routed experts:
+//   dg_m = sum over the routed slots whose final expert is m of s_j
+//          - S_tot * (sum over the token's choices c_i = m of w_i)   renormalised
+//          - S_tot * p_m                                              otherwise,
+// S_tot = the routed slots' sum of s, w_i the choices' normalised weights (a
+// moved slot's weight is the new expert's p over the same normaliser), plus
+// the auxiliary-loss and z-loss terms.  choice / choice_w: the token's kc
+// choices at stride ld; the first kr of the K slots are routed (shared
+// experts follow).  The row dg[t] first collects the slot scores by final
+// expert (lane 0, slot order), then each lane finishes its columns.
 __global__ void __launch_bounds__(256) router_grad_kernel(
-    const float* __restrict__ logits, const int32_t* __restrict__ idx,
-    const float* __restrict__ topk_w, const int32_t* __restrict__ slot_of,
-    const float* __restrict__ y_perm, const bf16* __restrict__ dy,
-    const int32_t* __restrict__ top1, int T, int E, int k, int d, int64_t rows_cap,
-    int renormalize, float aux_grad, float z_grad, float* __restrict__ dg,
-    bf16* __restrict__ dY_perm) {
+    const float* __restrict__ logits, const int32_t* __restrict__ choice,
+    const float* __restrict__ choice_w, int ld, int kc, const int32_t* __restrict__ slot_of,
+    const float* __restrict__ perm_w, const int32_t* __restrict__ kept_rank,
+    const int32_t* __restrict__ alt, int mode, const float* __restrict__ y_perm,
+    const bf16* __restrict__ dy, const int32_t* __restrict__ top1, int T, int El, int K, int kr,
+    int d, int64_t rows_cap, int renormalize, float aux_grad, float z_grad,
+    float* __restrict__ dg, bf16* __restrict__ dY_perm) {
     pdl_wait();
     pdl_trigger();
     const int lane = threadIdx.x % 32;
@@ -106,42 +124,51 @@ __global__ void __launch_bounds__(256) router_grad_kernel(
     const int nv = d / 8;  // 8-column groups
     for (int t = blockIdx.x * (blockDim.x / 32) + threadIdx.x / 32; t < T; t += nwarps) {
         const uint4* dyr = reinterpret_cast<const uint4*>(dy + (size_t)t * d);
-        float s[kMaxTopK];
+        float* dgt = dg + (size_t)t * El;
+        for (int e = lane; e < El; e += 32) dgt[e] = 0.f;
+        __syncwarp();
         float stot = 0.f;
-        for (int j = 0; j < k; ++j) {
-            const int slot = __ldg(slot_of + (size_t)t * k + j);
+        for (int j = 0; j < K; ++j) {
+            const int slot = __ldg(slot_of + (size_t)t * K + j);
+            if (slot < 0 || slot >= rows_cap) continue;  // dropped: s = 0
+            const float w = __ldg(perm_w + slot);
+            const float4* yr = reinterpret_cast<const float4*>(y_perm + (size_t)slot * d);
+            uint4* dyp = reinterpret_cast<uint4*>(dY_perm + (size_t)slot * d);
             float dot = 0.f;
-            if (slot >= 0 && slot < rows_cap) {
-                const float w = __ldg(topk_w + (size_t)t * k + j);
-                const float4* yr = reinterpret_cast<const float4*>(y_perm + (size_t)slot * d);
-                uint4* dyp = reinterpret_cast<uint4*>(dY_perm + (size_t)slot * d);
-                for (int v = lane; v < nv; v += 32) {
-                    float f[8];
-                    unpack8(__ldg(dyr + v), f);
-                    const float4 a = __ldg(yr + 2 * v), b = __ldg(yr + 2 * v + 1);
-                    dot += f[0] * a.x + f[1] * a.y + f[2] * a.z + f[3] * a.w + f[4] * b.x +
-                           f[5] * b.y + f[6] * b.z + f[7] * b.w;
+            for (int v = lane; v < nv; v += 32) {
+                float f[8];
+                unpack8(__ldg(dyr + v), f);
+                const float4 a = __ldg(yr + 2 * v), b = __ldg(yr + 2 * v + 1);
+                dot += f[0] * a.x + f[1] * a.y + f[2] * a.z + f[3] * a.w + f[4] * b.x +
+                       f[5] * b.y + f[6] * b.z + f[7] * b.w;
 #pragma unroll
-                    for (int q = 0; q < 8; ++q) f[q] *= w;
-                    dyp[v] = pack8(f);
-                }
-#pragma unroll
-                for (int o = 16; o > 0; o >>= 1) dot += __shfl_xor_sync(0xffffffffu, dot, o);
+                for (int q = 0; q < 8; ++q) f[q] *= w;
+                dyp[v] = pack8(f);
             }
-            s[j] = dot;
+#pragma unroll
+            for (int o = 16; o > 0; o >>= 1) dot += __shfl_xor_sync(0xffffffffu, dot, o);
+            if (j >= kr) continue;  // a shared expert: no logit
             stot += dot;
+            int f = j;  // kGradExpert: slot j is expert j
+            if (mode != kGradExpert) {
+                f = __ldg(choice + (size_t)t * ld + j);
+                if (mode == kGradReroute && __ldg(kept_rank + (size_t)t * kr + j) < 0)
+                    f = __ldg(alt + (size_t)t * kr + j);
+            }
+            if (lane == 0 && f >= 0 && f < El) dgt[f] += dot;
         }
+        __syncwarp();
         // softmax statistics of the token's logits
-        const float* g = logits + (size_t)t * E;
+        const float* g = logits + (size_t)t * El;
         float m = -3.402823466e38f;
-        for (int e = lane; e < E; e += 32) m = fmaxf(m, __ldg(g + e));
+        for (int e = lane; e < El; e += 32) m = fmaxf(m, __ldg(g + e));
 #pragma unroll
         for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
         float ssum = 0.f, fp = 0.f;
-        for (int e = lane; e < E; e += 32) {
+        for (int e = lane; e < El; e += 32) {
             const float ex = expf(__ldg(g + e) - m);
             ssum += ex;
-            fp += ex * (float)__ldg(top1 + e);
+            if (top1 != nullptr) fp += ex * (float)__ldg(top1 + e);
         }
 #pragma unroll
         for (int o = 16; o > 0; o >>= 1) {
@@ -151,23 +178,22 @@ __global__ void __launch_bounds__(256) router_grad_kernel(
         const float inv = 1.0f / ssum;
         const float lse = m + logf(ssum);
         fp *= inv / (float)T;  // sum_i f_i p_i
-        for (int e = lane; e < E; e += 32) {
+        for (int e = lane; e < El; e += 32) {
             const float pe = expf(__ldg(g + e) - m) * inv;
-            float v;
+            float v = dgt[e];
             if (renormalize) {
-                v = 0.f;
-                for (int j = 0; j < k; ++j)
-                    if (__ldg(idx + (size_t)t * k + j) == e)
-                        v = s[j] - __ldg(topk_w + (size_t)t * k + j) * stot;
+                for (int i = 0; i < kc; ++i)
+                    if (__ldg(choice + (size_t)t * ld + i) == e)
+                        v -= stot * __ldg(choice_w + (size_t)t * ld + i);
             } else {
-                v = -pe * stot;
-                for (int j = 0; j < k; ++j)
-                    if (__ldg(idx + (size_t)t * k + j) == e) v += s[j];
+                v -= pe * stot;
             }
-            const float fe = (float)__ldg(top1 + e) / (float)T;
-            v += aux_grad * (float)E / (float)T * pe * (fe - fp);
+            if (top1 != nullptr) {
+                const float fe = (float)__ldg(top1 + e) / (float)T;
+                v += aux_grad * (float)El / (float)T * pe * (fe - fp);
+            }
             v += z_grad * 2.0f / (float)T * lse * pe;
-            dg[(size_t)t * E + e] = v;
+            dgt[e] = v;
         }
     }
 }
@@ -263,8 +289,8 @@ __device__ __forceinline__ void store4(bf16* p, float4 v) {
 __global__ void __launch_bounds__(256) dx_kernel(const float* __restrict__ dX_perm,
                                                   const int32_t* __restrict__ slot_of,
                                                   const float* __restrict__ dg,
-                                                  const float* __restrict__ W_r, int T, int k,
-                                                  int E, int d, int64_t rows_cap,
+                                                  const float* __restrict__ W_r, int T, int K,
+                                                  int El, int d, int64_t rows_cap,
                                                   bf16* __restrict__ dx) {
     pdl_wait();
     pdl_trigger();
@@ -280,8 +306,8 @@ __global__ void __launch_bounds__(256) dx_kernel(const float* __restrict__ dX_pe
         float4 acc[4];
 #pragma unroll
         for (int u = 0; u < 4; ++u) acc[u] = make_float4(0.f, 0.f, 0.f, 0.f);
-        for (int j = 0; j < k; ++j) {
-            const int sl = __ldg(slot_of + (size_t)t * k + j);
+        for (int j = 0; j < K; ++j) {
+            const int sl = __ldg(slot_of + (size_t)t * K + j);
             if (sl < 0 || sl >= rows_cap) continue;
             const float4* row = reinterpret_cast<const float4*>(dX_perm + (size_t)sl * d);
 #pragma unroll
@@ -292,8 +318,8 @@ __global__ void __launch_bounds__(256) dx_kernel(const float* __restrict__ dX_pe
                 }
             }
         }
-        for (int e = 0; e < E; ++e) {
-            const float ge = __ldg(dg + (size_t)t * E + e);
+        for (int e = 0; e < El; ++e) {
+            const float ge = __ldg(dg + (size_t)t * El + e);
             const float4* wr = reinterpret_cast<const float4*>(W_r + (size_t)e * d);
 #pragma unroll
             for (int u = 0; u < 4; ++u) {
@@ -550,10 +576,7 @@ BwdLayout bwd_layout(const moe_config& c, const WsLayout& L) {
     return B;
 }
 
-bool backward_supported(const moe_config& c) {
-    return c.dtype == MOE_BF16 && c.routing == MOE_TOKEN_CHOICE && c.overflow == MOE_DROP &&
-           c.n_shared == 0;
-}
+bool backward_supported(const moe_config& c) { return c.dtype == MOE_BF16; }
 
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
@@ -594,9 +617,12 @@ moe_status moe_backward(const moe_config* cfg, const void* x, const float* W_r,
     const BwdLayout Bw = bwd_layout(c, L);
     if (ws == nullptr || (reinterpret_cast<uintptr_t>(ws) & 255u) != 0 || ws_bytes < Bw.total)
         return MOE_ERR_WORKSPACE;
+    const bool ec = c.routing == MOE_EXPERT_CHOICE;
+    const bool rr = c.overflow == MOE_REROUTE && c.capacity >= 0;  // (no cap: nothing moves)
+    const int El = E - c.n_shared;                                 // logit columns
     if (T == 0) {  // no token: every gradient is zero
         const size_t wsz = sizeof(float) * (size_t)E * d * F;
-        if (cudaMemsetAsync(dW_r, 0, sizeof(float) * (size_t)E * d, s) != cudaSuccess ||
+        if (cudaMemsetAsync(dW_r, 0, sizeof(float) * (size_t)El * d, s) != cudaSuccess ||
             cudaMemsetAsync(dW1, 0, wsz, s) != cudaSuccess ||
             cudaMemsetAsync(dW2, 0, wsz, s) != cudaSuccess ||
             cudaMemsetAsync(db1, 0, sizeof(float) * (size_t)E * F, s) != cudaSuccess ||
@@ -623,14 +649,52 @@ moe_status moe_backward(const moe_config* cfg, const void* x, const float* W_r,
     float* dg = at<float>(ws, Bw.dg);
     const int64_t rows = L.rows;
 
+    // slots per token and the token's choices (the routed experts' normaliser)
+    const int K = ec ? E : k + c.n_shared;
+    const int kr = ec ? E : k;  // routed slots
+    const int32_t* choice = idx;
+    const float* choice_w = w;
+    int ld = k;
     chain_begin();
-    // ---- recompute the forward intermediates
-    cudaError_t e = launch_route(c, x, W_r, logit_bias, nullptr, nullptr, logits, idx, w, nullptr,
-                                 nullptr, nullptr, ws, L, true, s);
-    if (e == cudaSuccess)
-        e = launch_scan_permute(c, x, idx, w, L.route.tokens * k, L.route.blocks, offsets, slot_of,
-                                perm_token, perm_w, x_perm, ws, L,
-                                route_loss_args(c, ws, L, nullptr, nullptr, nullptr), s);
+    // ---- recompute the forward intermediates (the forward pass's routing and dispatch)
+    cudaError_t e;
+    if (ec) {
+        float* probs_t = at<float>(ws, L.probs_t);
+        e = launch_route(ec_router_config(c), x, W_r, logit_bias, nullptr, nullptr, logits, idx, w,
+                         nullptr, nullptr, nullptr, ws, L, false, s, probs_t);
+        if (e == cudaSuccess)
+            e = launch_ec_select(c, probs_t, offsets, perm_token, perm_w, slot_of, nullptr, s);
+        if (e == cudaSuccess) e = launch_ec_gather(c, x, perm_token, x_perm, s);
+    } else if (rr) {
+        ld = reroute_ranked(c);
+        e = launch_route(reroute_router_config(c), x, W_r, logit_bias, nullptr, nullptr, logits,
+                         idx, w, nullptr, nullptr, nullptr, ws, L, false, s, nullptr, k);
+        if (e == cudaSuccess)
+            e = launch_reroute_dispatch(c, ld, x, idx, w, offsets, slot_of, perm_token, perm_w,
+                                        x_perm, ws, L, LossArgs{}, s);
+    } else if (c.n_shared > 0) {
+        int32_t* idx_r = at<int32_t>(ws, L.route_idx);
+        float* w_r = at<float>(ws, L.route_w);
+        choice = idx_r;
+        choice_w = w_r;
+        const moe_config cd = dispatch_config(c);
+        e = launch_route(routed_config(c), x, W_r, logit_bias, nullptr, nullptr, logits, idx_r,
+                         w_r, nullptr, nullptr, nullptr, ws, L, false, s);
+        if (e == cudaSuccess)
+            e = launch_join_shared(c, idx_r, w_r, idx, w, at<int32_t>(ws, L.counts), nullptr, s);
+        if (e == cudaSuccess) e = launch_count(cd, idx, ws, L, s);
+        if (e == cudaSuccess)
+            e = launch_scan_permute(cd, x, idx, w, kCountBlock, L.count_blocks, offsets, slot_of,
+                                    perm_token, perm_w, x_perm, ws, L, LossArgs{}, s);
+    } else {
+        e = launch_route(c, x, W_r, logit_bias, nullptr, nullptr, logits, idx, w, nullptr,
+                         nullptr, nullptr, ws, L, true, s);
+        if (e == cudaSuccess)
+            e = launch_scan_permute(c, x, idx, w, L.route.tokens * k, L.route.blocks, offsets,
+                                    slot_of, perm_token, perm_w, x_perm, ws, L,
+                                    route_loss_args(c, ws, L, nullptr, nullptr, nullptr), s);
+    }
+    const moe_config cg = dispatch_config(c);  // the GEMMs as the forward pass runs them
     int32_t* koff = at<int32_t>(ws, Bw.koff);
     bf16* TTd = at<bf16>(ws, Bw.tt_d);  // segment-transposed [d][kcols] operands
     bf16* TTf = at<bf16>(ws, Bw.tt_f);  // segment-transposed [d_ff][kcols] operands
@@ -641,22 +705,26 @@ moe_status moe_backward(const moe_config* cfg, const void* x, const float* W_r,
         e = launch_kernel(seg_koff_kernel, dim3(1), dim3(32), 0, s, 1, false,
                           (const int32_t*)offsets, E, rows, koff);
     if (e == cudaSuccess)
-        e = launch_grouped_gemm_tc(c, true, false, x_perm, rows, offsets, W1, b1, nullptr, U, rows,
+        e = launch_grouped_gemm_tc(cg, true, false, x_perm, rows, offsets, W1, b1, nullptr, U, rows,
                                    F, d, hdr, s);
     if (e == cudaSuccess)  // H = GELU(U) row-major, and H^T for dW2
         e = launch_kernel(seg_transpose_kernel<kSegGelu>, tgrid_f, dim3(256), 0, s, 1, false,
                           (const bf16*)U, H, (const int32_t*)offsets, (const int32_t*)koff, E, F,
                           rows, kc, TTf);
     if (e == cudaSuccess)
-        e = launch_grouped_gemm_tc(c, false, false, H, rows, offsets, W2, b2, perm_w, y_perm, rows,
+        e = launch_grouped_gemm_tc(cg, false, false, H, rows, offsets, W2, b2, perm_w, y_perm, rows,
                                    d, F, hdr, s);
     // ---- router gradient and the scaled upstream rows
     if (e == cudaSuccess)
         e = launch_kernel(router_grad_kernel, dim3(grid_for(T, 8)), dim3(256), 0, s, 1, false,
-                          (const float*)logits, (const int32_t*)idx, (const float*)w,
-                          (const int32_t*)slot_of, (const float*)y_perm,
-                          reinterpret_cast<const bf16*>(dy), (const int32_t*)at<int32_t>(ws, L.top1),
-                          T, E, k, d, rows, c.renormalize, aux_grad, z_grad, dg, dYp);
+                          (const float*)logits, choice, choice_w, ld, ec ? 0 : k,
+                          (const int32_t*)slot_of, (const float*)perm_w,
+                          rr ? (const int32_t*)at<int32_t>(ws, L.rr_kept) : nullptr,
+                          rr ? (const int32_t*)at<int32_t>(ws, L.rr_alt) : nullptr,
+                          ec ? (int)kGradExpert : rr ? (int)kGradReroute : (int)kGradChoice,
+                          (const float*)y_perm, reinterpret_cast<const bf16*>(dy),
+                          ec ? nullptr : (const int32_t*)at<int32_t>(ws, L.top1), T, El, K, kr, d,
+                          rows, ec ? 0 : c.renormalize, aux_grad, z_grad, dg, dYp);
     // ---- dW2_e = dY_perm_e^T H_e, db2
     if (e == cudaSuccess)
         e = launch_kernel(seg_transpose_kernel<kSegCopy>, tgrid_d, dim3(256), 0, s, 1, false,
@@ -677,20 +745,20 @@ moe_status moe_backward(const moe_config* cfg, const void* x, const float* W_r,
                           dim3(256), 0, s, 1, false, reinterpret_cast<const bf16*>(W1), F, d,
                           (const int32_t*)offsets, rows, W1T);
     if (e == cudaSuccess)
-        e = launch_grouped_gemm_tc(c, true, false, dYp, rows, offsets, W2T, nullptr, nullptr, dH,
+        e = launch_grouped_gemm_tc(cg, true, false, dYp, rows, offsets, W2T, nullptr, nullptr, dH,
                                    rows, F, d, hdr, s);
     if (e == cudaSuccess)  // dU = dH * GELU'(U) in place, and dU^T for dW1
         e = launch_kernel(seg_transpose_kernel<kSegGeluGrad>, tgrid_f, dim3(256), 0, s, 1, false,
                           (const bf16*)U, dH, (const int32_t*)offsets, (const int32_t*)koff, E, F,
                           rows, kc, TTf);
     if (e == cudaSuccess)
-        e = launch_grouped_gemm_tc(c, false, false, dH, rows, offsets, W1T, nullptr, nullptr,
+        e = launch_grouped_gemm_tc(cg, false, false, dH, rows, offsets, W1T, nullptr, nullptr,
                                    y_perm, rows, d, F, hdr, s);
     if (e == cudaSuccess) {
         const long long tasks = (long long)T * ((d / 4 + 127) / 128);
         e = launch_kernel(dx_kernel, dim3(grid_for(tasks, 8)), dim3(256), 0, s, 1, false,
                           (const float*)y_perm, (const int32_t*)slot_of, (const float*)dg, W_r, T,
-                          k, E, d, rows, reinterpret_cast<bf16*>(dx));
+                          K, El, d, rows, reinterpret_cast<bf16*>(dx));
     }
     // ---- dW1_e = dU_e^T X_perm_e, db1
     if (e == cudaSuccess)
@@ -704,14 +772,14 @@ moe_status moe_backward(const moe_config* cfg, const void* x, const float* W_r,
                           (const bf16*)dH, (const int32_t*)offsets, rows, F, db1);
     // ---- dW_r = dg^T x: row-slice partials, then their sum
     if (e == cudaSuccess)
-        e = launch_kernel(E <= 8 ? wr_grad_kernel<8> : wr_grad_kernel<32>,
+        e = launch_kernel(El <= 8 ? wr_grad_kernel<8> : wr_grad_kernel<32>,
                           dim3((d + 255) / 256, Bw.wr_slices), dim3(256), 0, s, 1, false,
-                          (const float*)dg, reinterpret_cast<const bf16*>(x), T, E, d,
+                          (const float*)dg, reinterpret_cast<const bf16*>(x), T, El, d,
                           wr_slice_rows(T), at<float>(ws, Bw.parts));
     if (e == cudaSuccess)
-        e = launch_kernel(sum_parts_kernel, dim3(grid_for((int64_t)E * d, 256)), dim3(256), 0, s,
+        e = launch_kernel(sum_parts_kernel, dim3(grid_for((int64_t)El * d, 256)), dim3(256), 0, s,
                           1, false, (const float*)at<float>(ws, Bw.parts), Bw.wr_slices,
-                          (int64_t)E * d, dW_r);
+                          (int64_t)El * d, dW_r);
     return e == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;
 }
 

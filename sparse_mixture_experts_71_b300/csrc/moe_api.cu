@@ -94,26 +94,7 @@ moe_status check_config(const moe_config* c) {
 
 bool rerouting(const moe_config& c) { return c.overflow == MOE_REROUTE; }
 
-// Router view of a rerouting layer: K2 ranked experts per token (the first k
-// are the choices; moe_route / launch_route get knorm = k).
-moe_config reroute_router_config(const moe_config& c) {
-    moe_config r = c;
-    r.k = reroute_ranked(c);
-    r.overflow = MOE_DROP;
-    return r;
-}
-
 bool expert_choice(const moe_config& c) { return c.routing == MOE_EXPERT_CHOICE; }
-
-// Router view of an expert-choice layer: p and the z-loss only (its top-1
-// outputs go to scratch and are not used).
-moe_config ec_router_config(const moe_config& c) {
-    moe_config r = c;
-    r.k = 1;
-    r.capacity = -1;
-    r.routing = MOE_TOKEN_CHOICE;
-    return r;
-}
 
 // The combine's view: K slots per token (expert choice: one per expert).
 moe_config combine_config(const moe_config& c) {

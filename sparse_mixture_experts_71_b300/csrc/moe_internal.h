@@ -224,6 +224,25 @@ cudaError_t launch_reroute_dispatch(const moe_config& c, int ld, const void* x,
                                     const LossArgs& loss, cudaStream_t s);
 inline int reroute_ranked(const moe_config& c) { return 2 * c.k < c.E ? 2 * c.k : c.E; }
 
+// Router view of a rerouting layer: K2 ranked experts per token (the first k
+// are the choices; the router gets knorm = k).
+inline moe_config reroute_router_config(const moe_config& c) {
+    moe_config r = c;
+    r.k = reroute_ranked(c);
+    r.overflow = MOE_DROP;
+    return r;
+}
+
+// Router view of an expert-choice layer: p and the z-loss only (its top-1
+// outputs go to scratch and are not used).
+inline moe_config ec_router_config(const moe_config& c) {
+    moe_config r = c;
+    r.k = 1;
+    r.capacity = -1;
+    r.routing = MOE_TOKEN_CHOICE;
+    return r;
+}
+
 // Expert choice (expert_choice.cu): C; the per-expert top-C selection from
 // the router probabilities probs_t [E][T] (offsets, rows, slot_of [T][E]);
 // the gather of the E*C rows.

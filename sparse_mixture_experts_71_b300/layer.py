@@ -36,8 +36,10 @@ def device_inputs(inp: Inputs, device="cuda") -> dict:
 class MoELayer:
     """Sparsely-gated MoE FFN layer whose forward pass runs in libmoe.
 
-    W_r: (E, d) fp32; W1: (E, d_ff, d); b1: (E, d_ff); W2: (E, d, d_ff);
+    W_r: (E - n_shared, d) fp32; W1: (E, d_ff, d); b1: (E, d_ff); W2: (E, d, d_ff);
     b2: (E, d), all on one CUDA device, W1..b2 of one dtype (fp32 or bf16).
+    n_shared: experts 0 .. n_shared - 1 are always active with weight 1 (the
+    router scores the other E - n_shared).
     routing: "token" (top-k experts per token) or "expert" (each expert takes
     its top-C tokens; k then sets C = ceil(T k / E) unless a capacity is given).
     overflow: "drop" (the capacity cap drops overflow) or "reroute" (a dropped
@@ -46,8 +48,9 @@ class MoELayer:
 
     def __init__(self, W_r, W1, b1, W2, b2, k: int, capacity: int | None = None,
                  renormalize: bool = True, logit_bias=None, routing: str = "token",
-                 overflow: str = "drop"):
+                 overflow: str = "drop", n_shared: int = 0):
         self.E, self.d_ff, self.d = W1.shape
+        self.n_shared = n_shared
         self.k = k
         self.routing = routing
         self.overflow = overflow
@@ -59,7 +62,8 @@ class MoELayer:
 
     def config(self, T: int) -> B.MoeConfig:
         return B.config(T, self.d, self.d_ff, self.E, self.k, self.dtype, self.capacity,
-                        self.renormalize, routing=self.routing, overflow=self.overflow)
+                        self.renormalize, n_shared=self.n_shared, routing=self.routing,
+                        overflow=self.overflow)
 
     def workspace(self, T: int) -> torch.Tensor:
         if T not in self._ws:
@@ -86,7 +90,7 @@ class MoELayer:
 
     def backward(self, x, dy, aux_grad: float = 0.0, z_grad: float = 0.0, stream=None) -> dict:
         """Gradients of <dy, y> + aux_grad * aux + z_grad * z_loss for the batch
-        x (moe_backward; bf16 token-choice layers that drop on overflow):
+        x (moe_backward; bf16 layers, every routing and overflow setting):
         {"dx", "dW_r", "dW1", "db1", "dW2", "db2"}, dx in the layer dtype, the
         weight gradients fp32.  The routing decisions are held fixed."""
         T = x.shape[0]
@@ -95,7 +99,7 @@ class MoELayer:
         if key not in self._ws:
             self._ws[key] = B.backward_workspace(cfg, device=self.W1.device)
         f32 = dict(dtype=torch.float32, device=self.W1.device)
-        g = dict(dx=torch.empty_like(x), dW_r=torch.empty((self.E, self.d), **f32),
+        g = dict(dx=torch.empty_like(x), dW_r=torch.empty(tuple(self.W_r.shape), **f32),
                  dW1=torch.empty((self.E, self.d_ff, self.d), **f32),
                  db1=torch.empty((self.E, self.d_ff), **f32),
                  dW2=torch.empty((self.E, self.d, self.d_ff), **f32),

@@ -175,12 +175,14 @@ def test_backward_host_side():
     c = B.config(64, 64, 128, 4, 2)
     n = lib.moe_backward_workspace_size(ctypes.byref(c))
     assert n >= B.workspace_size(c) and n % 256 == 0
-    for bad in (B.config(64, 64, 128, 4, 2, dtype="f32"), B.config(64, 64, 128, 4, 2, routing="expert"),
-                B.config(64, 64, 128, 4, 1, n_shared=1), B.config(64, 64, 128, 4, 2, capacity=5,
-                                                                   overflow="reroute")):
-        assert lib.moe_backward_workspace_size(ctypes.byref(bad)) == 0
-        assert lib.moe_backward(ctypes.byref(bad), *([FAKE] * 8), ctypes.c_float(0),
-                                ctypes.c_float(0), *([FAKE] * 6), FAKE, 1 << 40, None) == 4
+    # every bf16 variant has a backward pass; fp32 layers have none
+    for ok in (B.config(64, 64, 128, 4, 2, routing="expert"), B.config(64, 64, 128, 4, 1, n_shared=1),
+               B.config(64, 64, 128, 4, 2, capacity=5, overflow="reroute")):
+        assert lib.moe_backward_workspace_size(ctypes.byref(ok)) >= B.workspace_size(ok)
+    bad = B.config(64, 64, 128, 4, 2, dtype="f32")
+    assert lib.moe_backward_workspace_size(ctypes.byref(bad)) == 0
+    assert lib.moe_backward(ctypes.byref(bad), *([FAKE] * 8), ctypes.c_float(0),
+                            ctypes.c_float(0), *([FAKE] * 6), FAKE, 1 << 40, None) == 4
     cr = ctypes.byref(c)
     args = [FAKE] * 8
     outs = [FAKE] * 6  # dx, dW_r, dW1, db1, dW2, db2

@@ -11,7 +11,7 @@ import pytest
 import torch
 
 from oracle import moe_oracle as O
-from parity import LibRun, to_np
+from parity import LibRun, oracle_on, to_np
 from sparse_mixture_experts_71_b300 import binding as B
 from sparse_mixture_experts_71_b300 import inputs as I
 
@@ -30,6 +30,25 @@ CASES = [
     # mid size: ~1024 rows per expert, so the weight-gradient GEMMs' segment
     # reduction walks 8 K tiles of 128 per expert, on both GEMM kernels' wide path
     ("bwd-mid", 4096, 512, 2048, 8, 2, None, True, 0.0, 0.01, 0.001),
+]
+
+
+# The layer variants: shared experts, rerouting on overflow, expert choice.
+VARIANTS = [
+    # workload, aux_grad, z_grad
+    (I.Workload("bwd-shared", 500, 128, 256, 9, 2, n_shared=1), 0.3, 0.1),
+    (I.Workload("bwd-shared2-cap", 700, 128, 256, 10, 2, capacity=80, zipf_bias=1.0,
+                n_shared=2), 0.2, 0.0),
+    (I.Workload("bwd-reroute", 600, 128, 256, 8, 2, capacity=100, zipf_bias=1.0,
+                overflow="reroute"), 0.5, 0.2),
+    (I.Workload("bwd-reroute-top1-raw", 400, 128, 256, 8, 1, renormalize=False, capacity=40,
+                zipf_bias=1.5, overflow="reroute"), 0.0, 0.0),
+    (I.Workload("bwd-reroute-e64", 1100, 128, 128, 64, 2, capacity=30, zipf_bias=1.0,
+                overflow="reroute"), 0.1, 0.1),
+    (I.Workload("bwd-ec", 512, 128, 256, 8, 2, routing="expert"), 0.0, 0.3),
+    (I.Workload("bwd-ec-cap", 300, 128, 256, 8, 2, capacity=40, zipf_bias=1.0,
+                routing="expert"), 0.7, 0.0),   # aux_grad is ignored: no balancing loss
+    (I.Workload("bwd-ec-e64", 1100, 128, 128, 64, 2, routing="expert"), 0.0, 0.1),
 ]
 
 
@@ -76,6 +95,57 @@ def test_backward_matches_oracle(case):
                again["dW_r"], again["dW1"], again["db1"], again["dW2"], again["db2"], ws,
                logit_bias=D["logit_bias"], aux_grad=aux_grad, z_grad=z_grad)
     torch.cuda.synchronize()
+    for n in out:
+        assert torch.equal(out[n], again[n]), n
+
+
+def _lib_backward(run, dy, aux_grad, z_grad):
+    D, wl = run.dev, run.wl
+    ws = B.backward_workspace(run.cfg)
+    f32 = dict(dtype=torch.float32, device="cuda")
+    E, d, F = wl.E, wl.d, wl.F
+    out = dict(dx=torch.empty_like(D["x"]), dW_r=torch.empty(tuple(D["W_r"].shape), **f32),
+               dW1=torch.empty((E, F, d), **f32), db1=torch.empty((E, F), **f32),
+               dW2=torch.empty((E, d, F), **f32), db2=torch.empty((E, d), **f32))
+    B.backward(run.cfg, D["x"], D["W_r"], D["W1"], D["b1"], D["W2"], D["b2"], dy, out["dx"],
+               out["dW_r"], out["dW1"], out["db1"], out["dW2"], out["db2"], ws,
+               logit_bias=D["logit_bias"], aux_grad=aux_grad, z_grad=z_grad)
+    torch.cuda.synchronize()
+    assert B.get_device_error(ws)[0] == 0
+    return out
+
+
+@pytest.mark.parametrize("variant", VARIANTS, ids=[v[0].name for v in VARIANTS])
+def test_variant_backward_matches_oracle(variant):
+    """Shared experts, rerouting and expert choice: moe_backward against the
+    oracle's gradients of the same variant, routing (and, for expert choice,
+    the selection) taken from the kernels' forward pass."""
+    wl, aux_grad, z_grad = variant
+    inp = I.make_inputs(wl, seed=47)
+    run = LibRun(wl, inp)
+    dy = torch.from_numpy(I.router_noise(wl.T, wl.d, 1.0, seed=48)).to(torch.bfloat16).cuda()
+    args = (inp.as_f32("x"), inp.W_r, inp.as_f32("W1"), inp.as_f32("b1"), inp.as_f32("W2"),
+            inp.as_f32("b2"), dy.float().cpu().numpy())
+    if wl.routing == "expert":
+        r = run.staged_ec()
+        C = r["C"]
+        sel = to_np(r["perm_token"])[:wl.E * C].reshape(wl.E, C).astype(np.int64)
+        ref = O.expert_choice_backward(*args, k=wl.k, capacity=wl.capacity,
+                                       logit_bias=inp.logit_bias, logits=to_np(r["logits"]),
+                                       sel=sel, z_grad=z_grad)
+    else:
+        g = run.forward()["logits"]
+        if wl.overflow == "reroute":  # the case moves slots to other experts
+            fwd = oracle_on(inp, wl, logits=to_np(g), layout=False)
+            assert np.any(fwd.idx[:, :wl.k] != O.top_k(to_np(g), wl.k))
+        ref = O.moe_backward(*args, k=wl.k, renormalize=wl.renormalize, capacity=wl.capacity,
+                             logit_bias=inp.logit_bias, logits=to_np(g), aux_grad=aux_grad,
+                             z_grad=z_grad, n_shared=wl.n_shared,
+                             reroute=wl.overflow == "reroute")
+    out = _lib_backward(run, dy, aux_grad, z_grad)
+    errs = {n: _close(n, to_np(out[n]), ref[n]) for n in out}
+    print(wl.name, " ".join(f"{n} {v:.2e}" for n, v in errs.items()))
+    again = _lib_backward(run, dy, aux_grad, z_grad)
     for n in out:
         assert torch.equal(out[n], again[n]), n
 
