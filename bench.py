@@ -696,6 +696,23 @@ def kept_per_expert(cfg, wl, D, dev):
     return [int(v) for v in torch.diff(offsets).cpu().tolist()]
 
 
+def backward_roofline(wl, achieved, kernels, pk, pk_kind, clocks):
+    """bf16 layers: the whole call's GEMM flops against the measured bf16
+    burst peak.  fp32 layers run every product as fp32 FMA on the CUDA cores:
+    against 148 SMs x 128 fp32 lanes x 2 flop x the SM clock (the maximum
+    the clock sampler reports, 2032 MHz if none)."""
+    roof = {"kernel": f"whole backward call ({kernels} launches)", "achieved": achieved,
+            "unit": "TFLOP/s", "traffic": None}
+    if wl.dtype == "bf16":
+        roof.update(bound="tensor", peak=pk["bf16_tflops"], peak_source=pk_kind + " burst")
+    else:
+        mhz = (clocks or {}).get("sm_max_mhz") or 2032.0
+        roof.update(bound="alu", peak=148 * 128 * 2 * mhz * 1e6 / 1e12,
+                    peak_source=f"148 SMs x 128 fp32 FMA lanes x 2 flop x {mhz:.0f} MHz")
+    roof["frac"] = achieved / roof["peak"]
+    return roof
+
+
 def bench_backward(args, wl):
     """One step = one moe_backward call (it recomputes the forward
     intermediates it needs) on the workload's inputs and a seeded dy."""
@@ -709,8 +726,6 @@ def bench_backward(args, wl):
     dev = torch.device("cuda", local)
     if world > 1:
         dist.init_process_group("nccl", device_id=dev)
-    if wl.dtype != "bf16":
-        raise SystemExit(f"{wl.name}: the backward pass covers bf16 layers")
     inp = I.make_inputs(wl, seed=0)
     D = device_inputs(inp, dev)
     layer = MoELayer(D["W_r"], D["W1"], D["b1"], D["W2"], D["b2"], k=wl.k, capacity=wl.capacity,
@@ -719,7 +734,7 @@ def bench_backward(args, wl):
     cfg = layer.config(wl.T)
     T, d, F, E = wl.T, wl.d, wl.F, wl.E
     ws = B.backward_workspace(cfg, device=dev)
-    dy = torch.from_numpy(I.router_noise(T, d, 1.0, seed=1)).to(torch.bfloat16).to(dev)
+    dy = torch.from_numpy(I.router_noise(T, d, 1.0, seed=1)).to(D["x"].dtype).to(dev)
     f32 = dict(dtype=torch.float32, device=dev)
     g = dict(dx=torch.empty_like(D["x"]), dW_r=torch.empty(tuple(D["W_r"].shape), **f32),
              dW1=torch.empty((E, F, d), **f32), db1=torch.empty((E, F), **f32),
@@ -765,7 +780,8 @@ def bench_backward(args, wl):
     line = {"metric": "MoE-layer backward tokens/s (gradients of x, W_r, W1, b1, W2, b2)",
             "value": job_tokens_per_s(world, T, 1, ms), "unit": "tokens/s", "n_gpus": world,
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms,
-            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+            "dtype": "bf16" if wl.dtype == "bf16" else "f32",
             "data": "synthetic",
             "config": {"workload": wl.name, "pass": "backward", "T": T, "d": d, "d_ff": F,
                        "E": E, "k": wl.k, "capacity": wl.capacity,
@@ -773,10 +789,7 @@ def bench_backward(args, wl):
                        "n_shared": wl.n_shared, "parallelism": f"replicas{world}",
                        "l2": "flushed before every timed step (256 MiB write, untimed)"},
             "kernels_per_step": kernels, "kept_assignments": kept,
-            "roofline": {"bound": "tensor", "kernel": f"whole backward call ({kernels} launches)",
-                         "achieved": achieved, "peak": pk["bf16_tflops"],
-                         "peak_source": pk_kind + " burst", "unit": "TFLOP/s",
-                         "frac": achieved / pk["bf16_tflops"], "traffic": None},
+            "roofline": backward_roofline(wl, achieved, kernels, pk, pk_kind, clocks),
             "gpu_launches": kernels * args.steps, "clocks": clocks}
     if rank == 0:
         print(json.dumps(line), flush=True)

@@ -1,5 +1,5 @@
 /*
- * moe_backward.h -- backward pass of the MoE layer of moe.h (bf16 layers).
+ * moe_backward.h -- backward pass of the MoE layer of moe.h.
  *
  * The pages train the layer end to end ("Mixture of Experts: Scaling
  * Parameters Without Scaling Compute", section "The MoE layer"; the
@@ -37,16 +37,18 @@
  * the expert pre-activations, the expert outputs) from x and the weights:
  * it does not read a previous moe_forward's workspace.
  *
- * Supported: cfg->dtype = MOE_BF16, every routing, overflow and n_shared
- * setting moe_forward accepts (fp32 layers return MOE_ERR_UNSUPPORTED).
+ * Supported: every configuration moe_forward accepts.  bf16 layers keep the
+ * pre-activations, activations and scaled upstream rows in bf16 and run the
+ * products on the tcgen05 tensor cores; fp32 layers keep them in fp32 and
+ * run every product with fp32 FMA on the CUDA cores (GELU' from erff).
  *
  * Arguments (device pointers, caller-owned, layouts as in moe.h):
- *   x [T][d] bf16; W_r [E - n_shared][d] fp32;
+ *   x [T][d] (layer dtype); W_r [E - n_shared][d] fp32;
  *   logit_bias [E - n_shared] fp32 or NULL;
- *   W1 [E][d_ff][d], b1 [E][d_ff], W2 [E][d][d_ff], b2 [E][d] bf16;
- *   dy [T][d] bf16                       upstream gradient of y
+ *   W1 [E][d_ff][d], b1 [E][d_ff], W2 [E][d][d_ff], b2 [E][d] (layer dtype);
+ *   dy [T][d] (layer dtype)              upstream gradient of y
  *   aux_grad, z_grad                     weights of the two losses in L
- *   dx [T][d] bf16                       written (not accumulated)
+ *   dx [T][d] (layer dtype)              written (not accumulated)
  *   dW_r [E - n_shared][d], dW1 [E][d_ff][d], db1 [E][d_ff], dW2 [E][d][d_ff],
  *   db2 [E][d]                           fp32, written (not accumulated)
  *   ws, ws_bytes                         at least

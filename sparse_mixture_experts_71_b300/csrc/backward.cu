@@ -90,6 +90,30 @@ __device__ __forceinline__ uint4 pack8(const float* f) {
     return q;
 }
 
+// Eight consecutive elements of a bf16 or fp32 row (16- / 32-byte aligned).
+__device__ __forceinline__ void load8(const bf16* p, float* f) {
+    unpack8(__ldg(reinterpret_cast<const uint4*>(p)), f);
+}
+__device__ __forceinline__ void load8(const float* p, float* f) {
+    const float4 a = __ldg(reinterpret_cast<const float4*>(p));
+    const float4 b = __ldg(reinterpret_cast<const float4*>(p) + 1);
+    f[0] = a.x; f[1] = a.y; f[2] = a.z; f[3] = a.w;
+    f[4] = b.x; f[5] = b.y; f[6] = b.z; f[7] = b.w;
+}
+__device__ __forceinline__ void store8(bf16* p, const float* f) {
+    *reinterpret_cast<uint4*>(p) = pack8(f);
+}
+__device__ __forceinline__ void store8(float* p, const float* f) {
+    reinterpret_cast<float4*>(p)[0] = make_float4(f[0], f[1], f[2], f[3]);
+    reinterpret_cast<float4*>(p)[1] = make_float4(f[4], f[5], f[6], f[7]);
+}
+__device__ __forceinline__ float2 load2(const bf16* p) {
+    return __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(p));
+}
+__device__ __forceinline__ float2 load2(const float* p) {
+    return *reinterpret_cast<const float2*>(p);
+}
+
 // How the routed slots of a token map to logit columns (router_grad_kernel).
 enum GradMode {
     kGradChoice = 0,   // slot j < kr: the token's choice j (shared experts: routed ids)
@@ -109,21 +133,22 @@ enum GradMode {
 // choices at stride ld; the first kr of the K slots are routed (shared
 // experts follow).  The row dg[t] first collects the slot scores by final
 // expert (lane 0, slot order), then each lane finishes its columns.
+template <typename T>
 __global__ void __launch_bounds__(256) router_grad_kernel(
     const float* __restrict__ logits, const int32_t* __restrict__ choice,
     const float* __restrict__ choice_w, int ld, int kc, const int32_t* __restrict__ slot_of,
     const float* __restrict__ perm_w, const int32_t* __restrict__ kept_rank,
     const int32_t* __restrict__ alt, int mode, const float* __restrict__ y_perm,
-    const bf16* __restrict__ dy, const int32_t* __restrict__ top1, int T, int El, int K, int kr,
+    const T* __restrict__ dy, const int32_t* __restrict__ top1, int Tn, int El, int K, int kr,
     int d, int64_t rows_cap, int renormalize, float aux_grad, float z_grad,
-    float* __restrict__ dg, bf16* __restrict__ dY_perm) {
+    float* __restrict__ dg, T* __restrict__ dY_perm) {
     pdl_wait();
     pdl_trigger();
     const int lane = threadIdx.x % 32;
     const int nwarps = gridDim.x * (blockDim.x / 32);
     const int nv = d / 8;  // 8-column groups
-    for (int t = blockIdx.x * (blockDim.x / 32) + threadIdx.x / 32; t < T; t += nwarps) {
-        const uint4* dyr = reinterpret_cast<const uint4*>(dy + (size_t)t * d);
+    for (int t = blockIdx.x * (blockDim.x / 32) + threadIdx.x / 32; t < Tn; t += nwarps) {
+        const T* dyr = dy + (size_t)t * d;
         float* dgt = dg + (size_t)t * El;
         for (int e = lane; e < El; e += 32) dgt[e] = 0.f;
         __syncwarp();
@@ -133,17 +158,17 @@ __global__ void __launch_bounds__(256) router_grad_kernel(
             if (slot < 0 || slot >= rows_cap) continue;  // dropped: s = 0
             const float w = __ldg(perm_w + slot);
             const float4* yr = reinterpret_cast<const float4*>(y_perm + (size_t)slot * d);
-            uint4* dyp = reinterpret_cast<uint4*>(dY_perm + (size_t)slot * d);
+            T* dyp = dY_perm + (size_t)slot * d;
             float dot = 0.f;
             for (int v = lane; v < nv; v += 32) {
                 float f[8];
-                unpack8(__ldg(dyr + v), f);
+                load8(dyr + 8 * v, f);
                 const float4 a = __ldg(yr + 2 * v), b = __ldg(yr + 2 * v + 1);
                 dot += f[0] * a.x + f[1] * a.y + f[2] * a.z + f[3] * a.w + f[4] * b.x +
                        f[5] * b.y + f[6] * b.z + f[7] * b.w;
 #pragma unroll
                 for (int q = 0; q < 8; ++q) f[q] *= w;
-                dyp[v] = pack8(f);
+                store8(dyp + 8 * v, f);
             }
 #pragma unroll
             for (int o = 16; o > 0; o >>= 1) dot += __shfl_xor_sync(0xffffffffu, dot, o);
@@ -177,7 +202,7 @@ __global__ void __launch_bounds__(256) router_grad_kernel(
         }
         const float inv = 1.0f / ssum;
         const float lse = m + logf(ssum);
-        fp *= inv / (float)T;  // sum_i f_i p_i
+        fp *= inv / (float)Tn;  // sum_i f_i p_i
         for (int e = lane; e < El; e += 32) {
             const float pe = expf(__ldg(g + e) - m) * inv;
             float v = dgt[e];
@@ -189,10 +214,10 @@ __global__ void __launch_bounds__(256) router_grad_kernel(
                 v -= pe * stot;
             }
             if (top1 != nullptr) {
-                const float fe = (float)__ldg(top1 + e) / (float)T;
-                v += aux_grad * (float)El / (float)T * pe * (fe - fp);
+                const float fe = (float)__ldg(top1 + e) / (float)Tn;
+                v += aux_grad * (float)El / (float)Tn * pe * (fe - fp);
             }
-            v += z_grad * 2.0f / (float)T * lse * pe;
+            v += z_grad * 2.0f / (float)Tn * lse * pe;
             dgt[e] = v;
         }
     }
@@ -276,6 +301,7 @@ __global__ void __launch_bounds__(256) transpose_kernel(const bf16* __restrict__
     }
 }
 
+__device__ __forceinline__ void store4(float* p, float4 v) { *reinterpret_cast<float4*>(p) = v; }
 __device__ __forceinline__ void store4(bf16* p, float4 v) {
     __nv_bfloat162 lo = __floats2bfloat162_rn(v.x, v.y), hi = __floats2bfloat162_rn(v.z, v.w);
     uint2 u;
@@ -286,12 +312,13 @@ __device__ __forceinline__ void store4(bf16* p, float4 v) {
 
 // dx[t] = sum over the token's slots of dX_perm rows + sum_e dg[t][e] W_r[e];
 // one warp per (token, 512-column chunk).
+template <typename TX>
 __global__ void __launch_bounds__(256) dx_kernel(const float* __restrict__ dX_perm,
                                                   const int32_t* __restrict__ slot_of,
                                                   const float* __restrict__ dg,
                                                   const float* __restrict__ W_r, int T, int K,
                                                   int El, int d, int64_t rows_cap,
-                                                  bf16* __restrict__ dx) {
+                                                  TX* __restrict__ dx) {
     pdl_wait();
     pdl_trigger();
     const int lane = threadIdx.x % 32;
@@ -342,9 +369,9 @@ __global__ void __launch_bounds__(256) dx_kernel(const float* __restrict__ dX_pe
 // of dg staged in shared memory.
 constexpr int WR_CHUNK = 64;
 
-template <int WR_EG>
+template <int WR_EG, typename TX>
 __global__ void __launch_bounds__(256) wr_grad_kernel(const float* __restrict__ dg,
-                                                       const bf16* __restrict__ x, int T, int E,
+                                                       const TX* __restrict__ x, int T, int E,
                                                        int d, int slice, float* __restrict__ part) {
     __shared__ float sg[WR_CHUNK][WR_EG];
     pdl_wait();
@@ -367,7 +394,7 @@ __global__ void __launch_bounds__(256) wr_grad_kernel(const float* __restrict__ 
             if (j < d) {
                 const int rows = min(WR_CHUNK, t1 - tb);
                 for (int r = 0; r < rows; ++r) {
-                    const float xv = __bfloat162float(x[(size_t)(tb + r) * d + j]);
+                    const float xv = to_f32(x[(size_t)(tb + r) * d + j]);
 #pragma unroll
                     for (int c = 0; c < WR_EG; ++c) acc[c] = fmaf(sg[r][c], xv, acc[c]);
                 }
@@ -382,7 +409,8 @@ __global__ void __launch_bounds__(256) wr_grad_kernel(const float* __restrict__ 
 // out[e][m] = sum over the rows of segment e of A[r][m]: a block per (64
 // columns, expert); warp w sums rows w, w + 8, ... (two columns a lane),
 // then the eight partial sums are added in warp order.
-__global__ void __launch_bounds__(256) colsum_kernel(const bf16* __restrict__ A,
+template <typename T>
+__global__ void __launch_bounds__(256) colsum_kernel(const T* __restrict__ A,
                                                       const int32_t* __restrict__ offsets,
                                                       int64_t rows_cap, int M,
                                                       float* __restrict__ out) {
@@ -396,8 +424,7 @@ __global__ void __launch_bounds__(256) colsum_kernel(const bf16* __restrict__ A,
     float a = 0.f, b = 0.f;
     if (m < M)  // M is even (a multiple of 8)
         for (int r = r0 + warp; r < r1; r += 8) {
-            const float2 v = __bfloat1622float2(
-                *reinterpret_cast<const __nv_bfloat162*>(A + (size_t)r * M + m));
+            const float2 v = load2(A + (size_t)r * M + m);
             a += v.x;
             b += v.y;
         }
@@ -558,17 +585,19 @@ BwdLayout bwd_layout(const moe_config& c, const WsLayout& L) {
         return at;
     };
     const size_t rows = (size_t)L.rows;
+    const bool f32 = c.dtype == MOE_F32;  // fp32: no weight or segment transposes
+    const size_t es = f32 ? 4 : 2;         // bytes of a token-row element
     B.logits = take(sizeof(float) * (size_t)c.T * c.E);
-    B.u = take(2 * rows * c.d_ff);
-    B.dyp = take(2 * rows * c.d);
-    B.dh = take(2 * rows * c.d_ff);
-    B.w1t = take(2 * (size_t)c.E * c.d * c.d_ff);
-    B.w2t = take(2 * (size_t)c.E * c.d * c.d_ff);
+    B.u = take(es * rows * c.d_ff);
+    B.dyp = take(es * rows * c.d);
+    B.dh = take(es * rows * c.d_ff);
+    B.w1t = take(f32 ? 0 : 2 * (size_t)c.E * c.d * c.d_ff);
+    B.w2t = take(f32 ? 0 : 2 * (size_t)c.E * c.d * c.d_ff);
     B.dg = take(sizeof(float) * (size_t)c.T * c.E);
     B.koff = take(sizeof(int32_t) * (size_t)(c.E + 1));
     B.kcols = (L.rows + (int64_t)kSegPad * c.E + kSegPad - 1) / kSegPad * kSegPad;
-    B.tt_d = take(2 * (size_t)c.d * B.kcols);
-    B.tt_f = take(2 * (size_t)c.d_ff * B.kcols);
+    B.tt_d = take(f32 ? 0 : 2 * (size_t)c.d * B.kcols);
+    B.tt_f = take(f32 ? 0 : 2 * (size_t)c.d_ff * B.kcols);
     const int chunk = wr_slice_rows(c.T);
     B.wr_slices = (c.T + chunk - 1) / chunk;
     B.parts = take(sizeof(float) * (size_t)B.wr_slices * c.E * c.d);
@@ -576,7 +605,9 @@ BwdLayout bwd_layout(const moe_config& c, const WsLayout& L) {
     return B;
 }
 
-bool backward_supported(const moe_config& c) { return c.dtype == MOE_BF16; }
+bool backward_supported(const moe_config& c) {
+    return c.dtype == MOE_BF16 || c.dtype == MOE_F32;
+}
 
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
@@ -694,6 +725,67 @@ moe_status moe_backward(const moe_config* cfg, const void* x, const float* W_r,
                                     slot_of, perm_token, perm_w, x_perm, ws, L,
                                     route_loss_args(c, ws, L, nullptr, nullptr, nullptr), s);
     }
+    const int grad_mode = ec ? (int)kGradExpert : rr ? (int)kGradReroute : (int)kGradChoice;
+    const int32_t* kept_rank = rr ? at<int32_t>(ws, L.rr_kept) : nullptr;
+    const int32_t* alt = rr ? at<int32_t>(ws, L.rr_alt) : nullptr;
+    const int32_t* top1 = ec ? nullptr : at<int32_t>(ws, L.top1);
+    if (c.dtype == MOE_F32) {
+        // fp32 layers: every product on CUDA cores in fp32 (backward_f32.cu)
+        float* Uf = at<float>(ws, Bw.u);     // pre-activations, then (in dH) dU
+        float* Hf = at<float>(ws, L.h);      // GELU(U)
+        float* dYf = at<float>(ws, Bw.dyp);  // w dy per row
+        float* dHf = at<float>(ws, Bw.dh);
+        const float* xp = at<float>(ws, L.x_perm);
+        const int64_t max_seg = ec ? rows / E : (rows < T ? rows : (int64_t)T);
+        const float* W1f = reinterpret_cast<const float*>(W1);
+        const float* W2f = reinterpret_cast<const float*>(W2);
+        if (e == cudaSuccess)
+            e = launch_seg_gemm_f32(false, 1, xp, offsets, E, W1f,
+                                    reinterpret_cast<const float*>(b1), nullptr, Uf, Hf, F, d,
+                                    max_seg, rows, s);
+        if (e == cudaSuccess)
+            e = launch_seg_gemm_f32(false, 2, Hf, offsets, E, W2f,
+                                    reinterpret_cast<const float*>(b2), perm_w, y_perm, nullptr,
+                                    d, F, max_seg, rows, s);
+        if (e == cudaSuccess)
+            e = launch_kernel(router_grad_kernel<float>, dim3(grid_for(T, 8)), dim3(256), 0, s, 1,
+                              false, (const float*)logits, choice, choice_w, ld, ec ? 0 : k,
+                              (const int32_t*)slot_of, (const float*)perm_w, kept_rank, alt,
+                              grad_mode, (const float*)y_perm, reinterpret_cast<const float*>(dy),
+                              top1, T, El, K, kr, d, rows, ec ? 0 : c.renormalize, aux_grad,
+                              z_grad, dg, dYf);
+        if (e == cudaSuccess) e = launch_seg_atb_f32(dYf, Hf, offsets, E, d, F, rows, dW2, s);
+        if (e == cudaSuccess)
+            e = launch_kernel(colsum_kernel<float>, dim3((d + 63) / 64, E), dim3(256), 0, s, 1,
+                              false, (const float*)dYf, (const int32_t*)offsets, rows, d, db2);
+        if (e == cudaSuccess)  // dH = dY W2_e (W2_e: [d][d_ff] = [K][N])
+            e = launch_seg_gemm_f32(true, 0, dYf, offsets, E, W2f, nullptr, nullptr, dHf, nullptr,
+                                    F, d, max_seg, rows, s);
+        if (e == cudaSuccess) e = launch_gelu_grad_f32(Uf, dHf, offsets, E, F, rows, s);
+        if (e == cudaSuccess) e = launch_seg_atb_f32(dHf, xp, offsets, E, F, d, rows, dW1, s);
+        if (e == cudaSuccess)
+            e = launch_kernel(colsum_kernel<float>, dim3((F + 63) / 64, E), dim3(256), 0, s, 1,
+                              false, (const float*)dHf, (const int32_t*)offsets, rows, F, db1);
+        if (e == cudaSuccess)  // dX_perm = dU W1_e (W1_e: [d_ff][d] = [K][N]), over y_perm
+            e = launch_seg_gemm_f32(true, 0, dHf, offsets, E, W1f, nullptr, nullptr, y_perm,
+                                    nullptr, d, F, max_seg, rows, s);
+        if (e == cudaSuccess) {
+            const long long tasks = (long long)T * ((d / 4 + 127) / 128);
+            e = launch_kernel(dx_kernel<float>, dim3(grid_for(tasks, 8)), dim3(256), 0, s, 1,
+                              false, (const float*)y_perm, (const int32_t*)slot_of,
+                              (const float*)dg, W_r, T, K, El, d, rows, reinterpret_cast<float*>(dx));
+        }
+        if (e == cudaSuccess)
+            e = launch_kernel(El <= 8 ? wr_grad_kernel<8, float> : wr_grad_kernel<32, float>,
+                              dim3((d + 255) / 256, Bw.wr_slices), dim3(256), 0, s, 1, false,
+                              (const float*)dg, reinterpret_cast<const float*>(x), T, El, d,
+                              wr_slice_rows(T), at<float>(ws, Bw.parts));
+        if (e == cudaSuccess)
+            e = launch_kernel(sum_parts_kernel, dim3(grid_for((int64_t)El * d, 256)), dim3(256), 0,
+                              s, 1, false, (const float*)at<float>(ws, Bw.parts), Bw.wr_slices,
+                              (int64_t)El * d, dW_r);
+        return e == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;
+    }
     const moe_config cg = dispatch_config(c);  // the GEMMs as the forward pass runs them
     int32_t* koff = at<int32_t>(ws, Bw.koff);
     bf16* TTd = at<bf16>(ws, Bw.tt_d);  // segment-transposed [d][kcols] operands
@@ -716,15 +808,12 @@ moe_status moe_backward(const moe_config* cfg, const void* x, const float* W_r,
                                    d, F, hdr, s);
     // ---- router gradient and the scaled upstream rows
     if (e == cudaSuccess)
-        e = launch_kernel(router_grad_kernel, dim3(grid_for(T, 8)), dim3(256), 0, s, 1, false,
+        e = launch_kernel(router_grad_kernel<bf16>, dim3(grid_for(T, 8)), dim3(256), 0, s, 1, false,
                           (const float*)logits, choice, choice_w, ld, ec ? 0 : k,
-                          (const int32_t*)slot_of, (const float*)perm_w,
-                          rr ? (const int32_t*)at<int32_t>(ws, L.rr_kept) : nullptr,
-                          rr ? (const int32_t*)at<int32_t>(ws, L.rr_alt) : nullptr,
-                          ec ? (int)kGradExpert : rr ? (int)kGradReroute : (int)kGradChoice,
-                          (const float*)y_perm, reinterpret_cast<const bf16*>(dy),
-                          ec ? nullptr : (const int32_t*)at<int32_t>(ws, L.top1), T, El, K, kr, d,
-                          rows, ec ? 0 : c.renormalize, aux_grad, z_grad, dg, dYp);
+                          (const int32_t*)slot_of, (const float*)perm_w, kept_rank, alt,
+                          grad_mode, (const float*)y_perm, reinterpret_cast<const bf16*>(dy), top1,
+                          T, El, K, kr, d, rows, ec ? 0 : c.renormalize, aux_grad, z_grad, dg,
+                          dYp);
     // ---- dW2_e = dY_perm_e^T H_e, db2
     if (e == cudaSuccess)
         e = launch_kernel(seg_transpose_kernel<kSegCopy>, tgrid_d, dim3(256), 0, s, 1, false,
@@ -733,7 +822,7 @@ moe_status moe_backward(const moe_config* cfg, const void* x, const float* W_r,
     if (e == cudaSuccess)
         e = launch_segment_reduction_tc(E, offsets, rows, koff, TTd, d, TTf, F, kc, dW2, hdr, s);
     if (e == cudaSuccess)
-        e = launch_kernel(colsum_kernel, dim3((d + 63) / 64, E), dim3(256), 0, s, 1, false,
+        e = launch_kernel(colsum_kernel<bf16>, dim3((d + 63) / 64, E), dim3(256), 0, s, 1, false,
                           (const bf16*)dYp, (const int32_t*)offsets, rows, d, db2);
     // ---- dx path: transposed weights, dH, GELU', dX_perm, dx
     if (e == cudaSuccess)
@@ -756,7 +845,7 @@ moe_status moe_backward(const moe_config* cfg, const void* x, const float* W_r,
                                    y_perm, rows, d, F, hdr, s);
     if (e == cudaSuccess) {
         const long long tasks = (long long)T * ((d / 4 + 127) / 128);
-        e = launch_kernel(dx_kernel, dim3(grid_for(tasks, 8)), dim3(256), 0, s, 1, false,
+        e = launch_kernel(dx_kernel<bf16>, dim3(grid_for(tasks, 8)), dim3(256), 0, s, 1, false,
                           (const float*)y_perm, (const int32_t*)slot_of, (const float*)dg, W_r, T,
                           K, El, d, rows, reinterpret_cast<bf16*>(dx));
     }
@@ -768,11 +857,11 @@ moe_status moe_backward(const moe_config* cfg, const void* x, const float* W_r,
     if (e == cudaSuccess)
         e = launch_segment_reduction_tc(E, offsets, rows, koff, TTf, F, TTd, d, kc, dW1, hdr, s);
     if (e == cudaSuccess)
-        e = launch_kernel(colsum_kernel, dim3((F + 63) / 64, E), dim3(256), 0, s, 1, false,
+        e = launch_kernel(colsum_kernel<bf16>, dim3((F + 63) / 64, E), dim3(256), 0, s, 1, false,
                           (const bf16*)dH, (const int32_t*)offsets, rows, F, db1);
     // ---- dW_r = dg^T x: row-slice partials, then their sum
     if (e == cudaSuccess)
-        e = launch_kernel(El <= 8 ? wr_grad_kernel<8> : wr_grad_kernel<32>,
+        e = launch_kernel(El <= 8 ? wr_grad_kernel<8, bf16> : wr_grad_kernel<32, bf16>,
                           dim3((d + 255) / 256, Bw.wr_slices), dim3(256), 0, s, 1, false,
                           (const float*)dg, reinterpret_cast<const bf16*>(x), T, El, d,
                           wr_slice_rows(T), at<float>(ws, Bw.parts));

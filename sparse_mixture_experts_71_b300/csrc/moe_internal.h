@@ -243,6 +243,20 @@ inline moe_config ec_router_config(const moe_config& c) {
     return r;
 }
 
+// Backward pass of fp32 layers (backward_f32.cu): C = A B_e^T per expert
+// segment with B_e = W[e] ([N][K]; epi 1: C = acc + bias and C2 = GELU(C);
+// epi 2: C = (acc + bias) * row_w) or, with bkn, C = A W[e] (W[e] [K][N],
+// no epilogue); C[e] = A_e^T B_e over each segment's rows ([E][M][N]); and
+// dH *= GELU'(U) over the kept rows.
+cudaError_t launch_seg_gemm_f32(bool bkn, int epi, const float* A, const int32_t* offsets, int E,
+                                const float* W, const float* bias, const float* row_w, float* C,
+                                float* C2, int N, int K, int64_t max_seg, int64_t rows_cap,
+                                cudaStream_t s);
+cudaError_t launch_seg_atb_f32(const float* A, const float* B, const int32_t* offsets, int E,
+                               int M, int N, int64_t rows_cap, float* C, cudaStream_t s);
+cudaError_t launch_gelu_grad_f32(const float* U, float* dH, const int32_t* offsets, int E, int F,
+                                 int64_t rows_cap, cudaStream_t s);
+
 // Expert choice (expert_choice.cu): C; the per-expert top-C selection from
 // the router probabilities probs_t [E][T] (offsets, rows, slot_of [T][E]);
 // the gather of the E*C rows.

@@ -90,7 +90,7 @@ class MoELayer:
 
     def backward(self, x, dy, aux_grad: float = 0.0, z_grad: float = 0.0, stream=None) -> dict:
         """Gradients of <dy, y> + aux_grad * aux + z_grad * z_loss for the batch
-        x (moe_backward; bf16 layers, every routing and overflow setting):
+        x (moe_backward; every layer this object can run):
         {"dx", "dW_r", "dW1", "db1", "dW2", "db2"}, dx in the layer dtype, the
         weight gradients fp32.  The routing decisions are held fixed."""
         T = x.shape[0]

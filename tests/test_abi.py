@@ -175,11 +175,17 @@ def test_backward_host_side():
     c = B.config(64, 64, 128, 4, 2)
     n = lib.moe_backward_workspace_size(ctypes.byref(c))
     assert n >= B.workspace_size(c) and n % 256 == 0
-    # every bf16 variant has a backward pass; fp32 layers have none
+    # every variant of both dtypes has a backward pass
     for ok in (B.config(64, 64, 128, 4, 2, routing="expert"), B.config(64, 64, 128, 4, 1, n_shared=1),
-               B.config(64, 64, 128, 4, 2, capacity=5, overflow="reroute")):
+               B.config(64, 64, 128, 4, 2, capacity=5, overflow="reroute"),
+               B.config(64, 64, 128, 4, 2, dtype="f32"),
+               B.config(64, 64, 128, 4, 2, dtype="f32", routing="expert")):
         assert lib.moe_backward_workspace_size(ctypes.byref(ok)) >= B.workspace_size(ok)
-    bad = B.config(64, 64, 128, 4, 2, dtype="f32")
+    # fp32 token rows take twice the bytes of bf16 ones; no weight transposes
+    f32 = B.config(64, 64, 128, 4, 2, dtype="f32")
+    assert lib.moe_backward_workspace_size(ctypes.byref(f32)) - B.workspace_size(f32) < \
+        n - B.workspace_size(c) + 3 * 128 * 128 * 2
+    bad = B.config(64, 64, 128, 300, 2)  # E > 256: unsupported configuration
     assert lib.moe_backward_workspace_size(ctypes.byref(bad)) == 0
     assert lib.moe_backward(ctypes.byref(bad), *([FAKE] * 8), ctypes.c_float(0),
                             ctypes.c_float(0), *([FAKE] * 6), FAKE, 1 << 40, None) == 4
