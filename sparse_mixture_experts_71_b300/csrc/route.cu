@@ -146,6 +146,8 @@ __global__ void __launch_bounds__(kThreads) route_warp_kernel(RouteArgs a) {
             for (int e = 0; e < EMAX; ++e) s_p[(grp * TW + i) * LDS + e] = acc[i][e];
     }
     __syncthreads();
+    stage_logits<EMAX>(a, s_p, LDS, TB, blockIdx.x * TB);
+    __syncthreads();
     if (tid < TB) token_epilogue<EMAX>(a, s_p + tid * LDS, blockIdx.x * TB + tid, tid, s_idx, s_cnt, s_top1);
     __syncthreads();
     finish_block<EMAX>(a, s_p, LDS, TB, s_idx, s_cnt, s_top1, wh, carry);
@@ -306,6 +308,8 @@ __global__ void __launch_bounds__(kThreads) route_mma_kernel(RouteArgs a) {
             s_buf[tok * LDS + e] = (t < a.T && e < a.E) ? __ldg(a.logits_in + (size_t)t * a.E + e) : 0.f;
         }
     }
+    __syncthreads();
+    stage_logits<EMAX>(a, s_buf, LDS, TB, blockIdx.x * TB);
     __syncthreads();
     if (tid < TB) token_epilogue<EMAX>(a, s_buf + tid * LDS, blockIdx.x * TB + tid, tid, s_idx, s_cnt, s_top1);
     __syncthreads();

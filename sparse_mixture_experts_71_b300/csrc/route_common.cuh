@@ -108,9 +108,31 @@ __device__ void finish_block(const RouteArgs& a, const float* s_p, int lds, int 
     }
 }
 
+// The block's staged logits (rows of s_rows, lds apart; TB tokens from t0)
+// finished by the whole block before the per-token pass: the caller's
+// noise [T][E] added (noisy gating) and the logits written to logits_out.
+// The block's rows of both arrays are one contiguous range of TB * E
+// floats, so consecutive threads take consecutive floats (coalesced), where
+// a thread per token would stride E floats between neighbouring lanes.
+template <int EMAX>
+__device__ void stage_logits(const RouteArgs& a, float* s_rows, int lds, int TB, int t0) {
+    if (a.noise == nullptr && a.logits_out == nullptr) return;
+    const int n = min(TB, a.T - t0) * a.E;
+    for (int i = threadIdx.x; i < n; i += kThreads) {
+        const int tok = i / a.E, e = i - tok * a.E;
+        float g = s_rows[tok * lds + e];
+        if (a.noise != nullptr) {
+            g += __ldg(a.noise + (size_t)t0 * a.E + i);
+            s_rows[tok * lds + e] = g;  // the logits used for routing
+        }
+        if (a.logits_out != nullptr) a.logits_out[(size_t)t0 * a.E + i] = g;
+    }
+}
+
 // Softmax, top-k and gate weights of token t from its logits in prow
-// (EMAX slots, E used); the probabilities replace the logits in prow (zeros
-// for a token past the end of the batch).  One thread per token.
+// (EMAX slots, E used; noise already added by stage_logits); the
+// probabilities replace the logits in prow (zeros for a token past the end
+// of the batch).  One thread per token.
 template <int EMAX>
 __device__ __forceinline__ void token_epilogue(const RouteArgs& a, float* prow, int t, int slot,
                                                int* s_idx, int* s_cnt, int* s_top1) {
@@ -124,10 +146,6 @@ __device__ __forceinline__ void token_epilogue(const RouteArgs& a, float* prow, 
 #pragma unroll
     for (int e = 0; e < EMAX; ++e) {
         g[e] = e < a.E ? prow[e] : -FLT_MAX;
-        if (a.noise != nullptr && e < a.E) {
-            g[e] += __ldg(a.noise + (size_t)t * a.E + e);
-            prow[e] = g[e];  // the logits used for routing (logits_out)
-        }
         m = fmaxf(m, g[e]);
     }
     // exp(g - m) is evaluated where it is needed rather than kept (one more
@@ -139,8 +157,6 @@ __device__ __forceinline__ void token_epilogue(const RouteArgs& a, float* prow, 
     const float inv = 1.0f / ssum;
     const float lse = m + logf(ssum);
     prow[EMAX] = lse * lse;  // squared log-sum-exp (router z-loss), the row's pad slot
-    if (a.logits_out != nullptr)
-        for (int e = 0; e < a.E; ++e) a.logits_out[(size_t)t * a.E + e] = prow[e];
 #pragma unroll
     for (int e = 0; e < EMAX; ++e) prow[e] = (e < a.E ? expf(g[e] - m) : 0.f) * inv;  // p replaces g
     // top-k on the logits, larger first, ties to the lower expert index
@@ -163,6 +179,88 @@ __device__ __forceinline__ void token_epilogue(const RouteArgs& a, float* prow, 
         sel_e[j] = be;
         sel_x[j] = bx;
         sel_sum += j < a.knorm ? bx : 0.f;
+    }
+    const float wden = a.renormalize ? 1.0f / sel_sum : inv;
+    for (int j = 0; j < a.k; ++j) {
+        a.topk_idx[(size_t)t * a.k + j] = sel_e[j];
+        a.topk_w[(size_t)t * a.k + j] = sel_x[j] * wden;
+        s_idx[slot * a.k + j] = sel_e[j];
+        if (j < a.knorm) atomicAdd(&s_cnt[sel_e[j]], 1);
+    }
+    atomicAdd(&s_top1[sel_e[0]], 1);
+}
+
+// token_epilogue with two threads per token (lanes 2j and 2j + 1 of a warp,
+// half = the lane's low bit), for EMAX = 64: each thread holds the
+// exponentials of its 32 logits (experts half * 32 + i), so every exp is
+// taken once, and the pair combines its maximum, sum and top-k candidates
+// with one shuffle each; both threads end with the same values.  The sum of
+// exponentials is each half's sum in expert order, then the two added
+// (a different rounding order from token_epilogue's single sweep).  Half 0
+// writes the token's outputs.
+template <int EMAX>
+__device__ __forceinline__ void token_epilogue_pair(const RouteArgs& a, float* prow, int t,
+                                                    int slot, int half, int* s_idx, int* s_cnt,
+                                                    int* s_top1) {
+    static_assert(EMAX == 64, "two halves of 32 experts");
+    constexpr int H = EMAX / 2;
+    float* ph = prow + half * H;
+    // a token past the end of the batch still runs the pair's shuffles (every
+    // lane of the warp takes part) on zero logits, then writes zeros
+    const bool valid = t < a.T;
+    const int e0 = half * H;
+    float x[H];
+    float m = -FLT_MAX;
+#pragma unroll
+    for (int i = 0; i < H; ++i) {
+        x[i] = e0 + i < a.E ? (valid ? ph[i] : 0.f) : -FLT_MAX;
+        m = fmaxf(m, x[i]);
+    }
+    m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, 1));
+    // top-k on the logits (x still holds them), larger first, ties to the
+    // lower expert index; each round takes the pair's better candidate
+    uint32_t taken = 0;
+    int sel_e[kMaxTopK];
+    float sel_g[kMaxTopK];
+    for (int j = 0; j < a.k; ++j) {
+        float bv = -FLT_MAX;
+        int be = 0x7fffffff;
+#pragma unroll
+        for (int i = 0; i < H; ++i)
+            if (e0 + i < a.E && !((taken >> i) & 1u) && (be == 0x7fffffff || x[i] > bv)) {
+                bv = x[i];
+                be = e0 + i;
+            }
+        const float ov = __shfl_xor_sync(0xffffffffu, bv, 1);
+        const int oe = __shfl_xor_sync(0xffffffffu, be, 1);
+        if (oe != 0x7fffffff && (be == 0x7fffffff || ov > bv || (ov == bv && oe < be))) {
+            bv = ov;
+            be = oe;
+        }
+        if (be >= e0 && be < e0 + H) taken |= 1u << (be - e0);
+        sel_e[j] = be;
+        sel_g[j] = bv;
+    }
+    float ssum = 0.f;
+#pragma unroll
+    for (int i = 0; i < H; ++i) {
+        x[i] = e0 + i < a.E ? expf(x[i] - m) : 0.f;
+        ssum += x[i];
+    }
+    ssum += __shfl_xor_sync(0xffffffffu, ssum, 1);  // a + b == b + a: the same on both
+    const float inv = 1.0f / ssum;
+    if (half == 0) {
+        const float lse = m + logf(ssum);
+        prow[EMAX] = valid ? lse * lse : 0.f;  // squared log-sum-exp (router z-loss), pad slot
+    }
+#pragma unroll
+    for (int i = 0; i < H; ++i) ph[i] = valid ? x[i] * inv : 0.f;  // p replaces g
+    if (half != 0 || !valid) return;
+    float sel_x[kMaxTopK];
+    float sel_sum = 0.f;
+    for (int j = 0; j < a.k; ++j) {
+        sel_x[j] = expf(sel_g[j] - m);
+        sel_sum += j < a.knorm ? sel_x[j] : 0.f;
     }
     const float wden = a.renormalize ? 1.0f / sel_sum : inv;
     for (int j = 0; j < a.k; ++j) {

@@ -82,6 +82,14 @@ __device__ __forceinline__ void tma_load_3d_pair(void* dst, const CUtensorMap* t
         : "memory");
 }
 
+// L2 prefetch of a 2-D tensor box (no shared memory, no completion).
+__device__ __forceinline__ void tma_prefetch_l2_2d(const CUtensorMap* tm, int32_t c0, int32_t c1) {
+    asm volatile("cp.async.bulk.prefetch.tensor.2d.L2.global.tile [%0, {%1, %2}];" ::"l"(
+                     reinterpret_cast<uint64_t>(tm)),
+                 "r"(c0), "r"(c1)
+                 : "memory");
+}
+
 // Tensor store of a 2-D box from shared memory (bulk-group completion).  The
 // shared-memory writes it reads must be fenced into the async proxy first.
 __device__ __forceinline__ void tma_store_2d(const CUtensorMap* tm, const void* src, int32_t c0,
