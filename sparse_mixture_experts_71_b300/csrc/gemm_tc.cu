@@ -100,6 +100,15 @@ struct Params {
     // make_map3 (one box covers a stage's ATOMS K atoms), 0 for 2-D maps
     // (one box per atom)
     int box3d;
+    // CTA-pair kernel, second GEMM: may split each tile's K in two halves
+    // (split_ok) when that evens out the waves; the second half adds its
+    // product to the first half's output once ksync[tile] (zero at launch)
+    // counts the first half's epilogue warps.  zero_ksync: this launch (the
+    // first GEMM) zeroes ksync[0 .. ksync_cap).
+    int32_t* ksync;
+    int ksync_cap;
+    int split_ok;
+    int zero_ksync;
 };
 
 // Rows of an expert's segment (offsets clamped to the buffers).
@@ -181,10 +190,12 @@ __device__ __forceinline__ void epilogue_tile(const Params& p, int e, int r0, in
                                               uint32_t tmem_base, int acc_col, int q, int part,
                                               int nparts, int lane, uint8_t* stg,
                                               const CUtensorMap* tm_out = nullptr,
-                                              bool zero = false) {
+                                              bool zero = false, bool accumulate = false) {
     const int f0 = fbase + q * 32;  // first weight row (output feature) of this warp
     const int f = f0 + lane;
-    const float bias = f < p.n_out && p.bias != nullptr
+    // accumulate (second GEMM, second K half): out += acc * w, the bias
+    // having come with the first half
+    const float bias = f < p.n_out && p.bias != nullptr && !accumulate
                            ? __bfloat162float(p.bias[(size_t)e * p.n_out + f])
                            : 0.f;
     const int c_begin = part * (COLS / nparts), c_end = min(c_begin + COLS / nparts, n);
@@ -231,7 +242,10 @@ __device__ __forceinline__ void epilogue_tile(const Params& p, int e, int r0, in
                 tc::fence_proxy_async_smem();
                 __syncwarp();
                 if (lane == 0) {
-                    tc::tma_store_2d(tm_out, stg, f0, o0 + c);
+                    if (accumulate)
+                        tc::tma_reduce_add_2d(tm_out, stg, f0, o0 + c);
+                    else
+                        tc::tma_store_2d(tm_out, stg, f0, o0 + c);
                     tc::bulk_commit();
                 }
                 continue;
@@ -244,7 +258,15 @@ __device__ __forceinline__ void epilogue_tile(const Params& p, int e, int r0, in
                 const int fc = f0 + part * 4;
                 if (j < rows_here && fc < p.n_out) {
                     const float4 val = *reinterpret_cast<const float4*>(stg + j * 128 + part * 16);
-                    *reinterpret_cast<float4*>(out + (size_t)(o0 + c + j) * p.n_out + fc) = val;
+                    float* dst = out + (size_t)(o0 + c + j) * p.n_out + fc;
+                    if (accumulate) {
+                        atomicAdd(dst, val.x);
+                        atomicAdd(dst + 1, val.y);
+                        atomicAdd(dst + 2, val.z);
+                        atomicAdd(dst + 3, val.w);
+                    } else {
+                        *reinterpret_cast<float4*>(dst) = val;
+                    }
                 }
             }
         }
@@ -456,6 +478,23 @@ __device__ __forceinline__ int ld_acquire_gpu(const int32_t* p) {
     int v;
     asm volatile("ld.acquire.gpu.global.b32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
     return v;
+}
+
+// Spin (bounded by the pipeline time-out) until *cnt >= target; a time-out
+// records the error (where) and raises the CTA's abort flag.
+__device__ __forceinline__ bool wait_count(const int32_t* cnt, int target, volatile int* abort_flag,
+                                           const Params& p, int where) {
+    if (ld_acquire_gpu(cnt) >= target) return true;
+    const uint64_t t0 = tc::globaltimer();
+    while (ld_acquire_gpu(cnt) < target) {
+        if (*abort_flag) return false;
+        if (tc::globaltimer() - t0 > p.timeout_ns) {
+            *abort_flag = 1;
+            record_error(p.hdr, kErrTimeout, where);
+            return false;
+        }
+    }
+    return true;
 }
 
 __global__ void __launch_bounds__(kThreads, 1)
@@ -919,7 +958,10 @@ grouped_gemm_pair(const __grid_constant__ CUtensorMap tmA, const __grid_constant
     }
     pdl_wait();  // offsets and the operands come from the previous kernel
     pdl_trigger();
+    int* s_split = reinterpret_cast<int*>(smem + C::OFF_MISC + 8);
     if (warp == 3) {  // exclusive prefix of pair tiles per expert
+        if (p.zero_ksync && blockIdx.x == 0)  // the second GEMM's half-tile counters
+            for (int i = lane; i < p.ksync_cap; i += 32) p.ksync[i] = 0;
         int run = 0;
         for (int e0 = 0; e0 < p.E; e0 += 32) {
             const int e = e0 + lane;
@@ -937,13 +979,27 @@ grouped_gemm_pair(const __grid_constant__ CUtensorMap tmA, const __grid_constant
             if (e < p.E) s_tiles[e] = run + v - nt;
             run += __shfl_sync(0xffffffffu, v, 31);
         }
-        if (lane == 0) s_tiles[p.E] = run;
+        if (lane == 0) {
+            s_tiles[p.E] = run;
+            // split K in two when the half tiles fill the last wave of pairs
+            // clearly better than the whole ones (K a multiple of two stages)
+            int split = 0;
+            if (!GEMM1 && p.split_ok && p.koff == nullptr && run > 0 && run <= p.ksync_cap &&
+                p.K % (2 * ATOMS * BK) == 0) {
+                const float w = (float)run / (float)npairs;
+                split = 2.0f * w / ceilf(2.0f * w) > w / ceilf(w) + 0.05f;
+            }
+            *s_split = split;
+        }
     }
     tc::fence_before_sync();
     tc::cluster_sync();  // both CTAs' barriers and TMEM exist before any cross-CTA traffic
     tc::fence_after_sync();
     const uint32_t tmem_base = *s_tmem;
-    const int total = s_tiles[p.E];
+    const int base_total = s_tiles[p.E];  // whole tiles
+    const int split = *s_split;           // 1: tile t + base_total is tile t's second K half
+    const int total = base_total << split;
+    const int KBh = KB >> split;          // stages per (half) tile
 
     if (warp == 0) {
         // ------------------------------------------------ TMA producer (both CTAs)
@@ -953,7 +1009,8 @@ grouped_gemm_pair(const __grid_constant__ CUtensorMap tmA, const __grid_constant
             long long fills = 0;
             bool ok = true;
             for (int t = pair; t < total && ok; t += npairs) {
-                const Tile tl = decode_pair_tile(t, s_tiles, p, mt2);
+                const int kh = t >= base_total ? 1 : 0;
+                const Tile tl = decode_pair_tile(t - kh * base_total, s_tiles, p, mt2);
                 const int m0 = tl.m0;  // pair tile base row
                 const int half_rows = ((tl.n + 31) & ~31) / 2;
                 // the smallest token box that holds this CTA's half_rows rows
@@ -964,8 +1021,8 @@ grouped_gemm_pair(const __grid_constant__ CUtensorMap tmA, const __grid_constant
                 const bool red = p.koff != nullptr;
                 const int arow = (red ? 0 : tl.e * p.n_out) + m0 + rank * BM;
                 const int brow = (red ? tl.r0 - tl.e * p.tok_rows : tl.r0) + rank * half_rows;
-                const int k0 = red ? __ldg(p.koff + tl.e) : 0;
-                const int KBt = red ? (seg_rows(p, tl.e) + ATOMS * BK - 1) / (ATOMS * BK) : KB;
+                const int k0 = red ? __ldg(p.koff + tl.e) : kh * KBh * ATOMS * BK;
+                const int KBt = red ? (seg_rows(p, tl.e) + ATOMS * BK - 1) / (ATOMS * BK) : KBh;
                 for (int kb = 0; kb < KBt; ++kb) {
                     if (!wait_bar(&empty[stage], phase ^ 1, s_abort, p, 1)) { ok = false; break; }
                     if (leader) tc::mbar_expect_tx(&full[stage], bytes);
@@ -1000,7 +1057,8 @@ grouped_gemm_pair(const __grid_constant__ CUtensorMap tmA, const __grid_constant
             uint32_t phase = 0, acc_phase = 0;
             bool ok = true;
             for (int t = pair; t < total && ok; t += npairs) {
-                const Tile tl = decode_pair_tile(t, s_tiles, p, mt2);
+                const Tile tl = decode_pair_tile(t >= base_total ? t - base_total : t, s_tiles, p,
+                                                 mt2);
                 const uint32_t N = (uint32_t)((tl.n + 31) & ~31);
                 const uint32_t idesc = tc::idesc_bf16_f32(2 * BM, N);
                 const int half_rows = (int)N / 2;  // the producer's token box for this tile
@@ -1011,7 +1069,7 @@ grouped_gemm_pair(const __grid_constant__ CUtensorMap tmA, const __grid_constant
                 const uint32_t d_tmem = tmem_base + (uint32_t)(acc * BN2);
                 const int KBt = p.koff != nullptr
                                     ? (seg_rows(p, tl.e) + ATOMS * BK - 1) / (ATOMS * BK)
-                                    : KB;
+                                    : KBh;
                 for (int kb = 0; kb < KBt; ++kb) {
                     if (!wait_bar(&full[stage], phase, s_abort, p, 3)) { ok = false; break; }
                     tc::fence_after_sync();
@@ -1047,18 +1105,43 @@ grouped_gemm_pair(const __grid_constant__ CUtensorMap tmA, const __grid_constant
         int acc = 0;
         uint32_t acc_phase = 0;
         for (int t = pair; t < total; t += npairs) {
-            const Tile tl = decode_pair_tile(t, s_tiles, p, mt2);
+            const int kh = t >= base_total ? 1 : 0;
+            const int tb = t - kh * base_total;  // the whole tile
+            const Tile tl = decode_pair_tile(tb, s_tiles, p, mt2);
             const int m0 = tl.m0;
             const bool ok = wait_bar(&tfull[acc], acc_phase, s_abort, p, 4);
             if (!__all_sync(0xffffffffu, ok)) break;
             tc::fence_after_sync();
+            if (kh == 1) {
+                // the first K half of this tile is in the output: its 2 x EW
+                // epilogue warps have counted themselves in ksync[tb]
+                bool okw = true;
+                if (lane == 0) okw = wait_count(p.ksync + tb, 2 * EW, s_abort, p, 5);
+                if (!__all_sync(0xffffffffu, __shfl_sync(0xffffffffu, okw, 0))) break;
+                (void)ld_acquire_gpu(p.ksync + tb);  // every lane acquires
+                asm volatile("fence.proxy.async.global;" ::: "memory");
+            }
             if constexpr (GEMM1)
                 epilogue_gelu<EW / 4>(p, tl.e, tl.r0, tl.n, m0 + rank * BM, tmem_base, acc * BN2,
                                       q, part, lane, stg, &tmO);
             else
                 epilogue_tile<BN2, GEMM1>(p, tl.e, tl.r0, tl.r0, tl.n, m0 + rank * BM, tmem_base,
                                       acc * BN2, q, part, EW / 4, lane, stg, &tmO,
-                                      p.koff != nullptr && seg_rows(p, tl.e) == 0);
+                                      p.koff != nullptr && seg_rows(p, tl.e) == 0, kh == 1);
+            if (split && kh == 0) {
+                // publish this warp's part of the first half: its tensor
+                // stores complete, its plain stores fenced, then one count
+                if (lane == 0) {
+                    tc::bulk_wait_all();
+                    asm volatile("fence.proxy.async.global;" ::: "memory");
+                }
+                __threadfence();
+                __syncwarp();
+                if (lane == 0) {
+                    __threadfence();
+                    atomicAdd(p.ksync + tb, 1);
+                }
+            }
             tc::fence_before_sync();
             __syncwarp();
             if (lane == 0) tc::mbar_arrive_cluster_relaxed(tc::cluster_addr(&tempty[acc], 0));
@@ -1265,7 +1348,7 @@ cudaError_t launch_expert_ffn_tc(const moe_config& c, const void* x_perm, int64_
                                  const int32_t* offsets, const void* W1, const void* b1,
                                  const void* W2, const void* b2, const float* perm_w,
                                  float* y_perm, void* h, int64_t h_rows, DeviceHeader* hdr,
-                                 cudaStream_t s) {
+                                 int32_t* ksync, cudaStream_t s) {
     if (h_rows == 0) return cudaSuccess;
     // tokens per expert on average decides the widest token tile
     const bool wide = (int64_t)c.T * c.k >= 96LL * c.E;
@@ -1291,6 +1374,11 @@ cudaError_t launch_expert_ffn_tc(const moe_config& c, const void* x_perm, int64_
             !make_store_map_sw32(&so[0], h, c.d_ff, (uint64_t)h_rows) ||
             !make_store_map_f32(&so[1], y_perm, c.d, (uint64_t)h_rows))
             return cudaErrorInvalidValue;
+        // the first GEMM zeroes the counters the second may use to split K
+        p1.ksync = p2.ksync = ksync;
+        p1.ksync_cap = p2.ksync_cap = ksync != nullptr ? kKsyncCap : 0;
+        p1.zero_ksync = ksync != nullptr;
+        p2.split_ok = ksync != nullptr;
         cudaError_t err = launch_one_pair<3, true, 16, kPairAtoms>(a1, bx, so[0], p1, s);
         if (err != cudaSuccess) return err;
         return launch_one_pair<3, false, 8, kPairAtoms>(a2, bh, so[1], p2, s);

@@ -61,7 +61,7 @@ cudaError_t launch_expert_ffn_tc(const moe_config& c, const void* x_perm, int64_
                                  const int32_t* offsets, const void* W1, const void* b1,
                                  const void* W2, const void* b2, const float* perm_w,
                                  float* y_perm, void* h, int64_t h_rows, DeviceHeader* hdr,
-                                 cudaStream_t s);
+                                 int32_t* ksync, cudaStream_t s);
 
 namespace {
 
@@ -169,6 +169,7 @@ WsLayout ws_layout(const moe_config& c) {
     L.counts = take(sizeof(int32_t) * c.E);
     L.top1 = take(sizeof(int32_t) * c.E);
     L.sched = take(sizeof(int32_t) * (1 + c.E));  // zeroed with the counts (same memset)
+    L.ksync = take(sizeof(int32_t) * kKsyncCap);  // zeroed by the first expert GEMM
     L.blk_p = take(sizeof(float) * (size_t)L.route.blocks * cr.E);
     L.blk_z = take(sizeof(float) * (size_t)L.route.blocks);
     L.blk_hist = take(sizeof(int32_t) * (size_t)L.hist_blocks * c.E);
@@ -210,7 +211,8 @@ cudaError_t launch_expert_ffn(const moe_config& c, const void* x_perm, int64_t x
                               void* ws, const WsLayout& L, cudaStream_t s) {
     if (c.dtype == MOE_BF16)
         return launch_expert_ffn_tc(c, x_perm, x_rows, offsets, W1, b1, W2, b2, perm_w, y_perm,
-                                    at<void>(ws, L.h), L.rows, at<DeviceHeader>(ws, L.header), s);
+                                    at<void>(ws, L.h), L.rows, at<DeviceHeader>(ws, L.header),
+                                    at<int32_t>(ws, L.ksync), s);
     return launch_expert_ffn_simt(c, x_perm, offsets, W1, b1, W2, b2, perm_w, y_perm,
                                   at<void>(ws, L.h), max_segment(c), L.rows, s);
 }

@@ -60,12 +60,17 @@ RouteGeom route_geom(const moe_config& c);
 // route_geom sized).
 RouteGeom route_geom_beside(const moe_config& c);
 
+// Tiles of the second expert GEMM whose K may be split in two (CTA-pair
+// kernel): one first-half counter each in the workspace.
+constexpr int kKsyncCap = 512;
+
 // Byte offsets of the workspace regions for one configuration.
 struct WsLayout {
     size_t header;       // DeviceHeader
     size_t counts;       // int32 [E]   assignments per expert (all slots)
     size_t top1;         // int32 [E]   first-slot choices per expert
     size_t sched;        // int32 [1+E] work-item counter and per-expert ready counts (dense decode FFN)
+    size_t ksync;        // int32 [kKsyncCap] second expert GEMM: first-K-half counts per tile
     size_t blk_p;        // fp32 [route.blocks][E] per-block sums of p
     size_t blk_z;        // fp32 [route.blocks] per-block sums of the squared log-sum-exp
     size_t blk_hist;     // int32 [hist_blocks][E]

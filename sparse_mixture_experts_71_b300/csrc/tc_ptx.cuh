@@ -99,6 +99,16 @@ __device__ __forceinline__ void tma_store_2d(const CUtensorMap* tm, const void* 
                  "r"(smem_u32(src)), "r"(c0), "r"(c1)
                  : "memory");
 }
+// Element-wise add of a 2-D box from shared memory into global memory (the
+// add happens at L2; bulk-group completion like a store).
+__device__ __forceinline__ void tma_reduce_add_2d(const CUtensorMap* tm, const void* src,
+                                                  int32_t c0, int32_t c1) {
+    asm volatile(
+        "cp.reduce.async.bulk.tensor.2d.global.shared::cta.add.tile.bulk_group [%0, {%2, %3}], [%1];"
+        ::"l"(reinterpret_cast<uint64_t>(tm)),
+        "r"(smem_u32(src)), "r"(c0), "r"(c1)
+        : "memory");
+}
 __device__ __forceinline__ void bulk_commit() {
     asm volatile("cp.async.bulk.commit_group;" ::: "memory");
 }
