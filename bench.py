@@ -306,6 +306,7 @@ def ffn_roofline(wl, work, ffn_ms, pk, pk_kind):
         peak = pk["bf16_tflops"]
         roof = {"bound": "tensor", "unit": "TFLOP/s", "peak_source": pk_kind + " bf16 burst",
                 "frac_of_sustained": achieved / pk["bf16_tflops_sustained"],
+                "frac_of_2250_nominal": achieved / 2250.0,
                 "algorithmic": f"4*d*d_ff*kept = {work['flops_ffn']:.4g} flop per launch pair"}
     else:
         achieved = work["ffn_bytes"] / ffn_s / 1e9

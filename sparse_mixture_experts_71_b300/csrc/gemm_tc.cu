@@ -32,6 +32,11 @@
 //               computes 256 weight rows x 256 tokens with cta_group::2
 //               MMAs (M = 256); three stages of two K atoms; 16 (first GEMM)
 //               or 8 (second) epilogue warps; output by TMA tensor stores.
+//               The second GEMM may split each tile's K in two halves (when
+//               the half tiles fill the last wave of pairs better): the
+//               first half stores its product, the second adds its own by
+//               TMA reduce-add after a per-tile count of the first half's
+//               epilogue warps.
 //   grouped_gemm_tc (decode-sized batches, token tiles of up to 64 rows):
 //               one CTA per SM, M = 128, eight stages; 8 epilogue warps;
 //               output by 16-byte lane stores.
