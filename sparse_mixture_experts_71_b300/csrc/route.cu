@@ -150,7 +150,7 @@ __global__ void __launch_bounds__(kThreads) route_warp_kernel(RouteArgs a) {
     __syncthreads();
     if (tid < TB) token_epilogue<EMAX>(a, s_p + tid * LDS, blockIdx.x * TB + tid, tid, s_idx, s_cnt, s_top1);
     __syncthreads();
-    finish_block<EMAX>(a, s_p, LDS, TB, s_idx, s_cnt, s_top1, wh, carry);
+    finish_block<EMAX>(a, s_p, LDS, TB, s_idx, s_cnt, s_top1, wh, carry, blockIdx.x);
 }
 
 // ===================================================================== tensor-core kernel
@@ -313,7 +313,7 @@ __global__ void __launch_bounds__(kThreads) route_mma_kernel(RouteArgs a) {
     __syncthreads();
     if (tid < TB) token_epilogue<EMAX>(a, s_buf + tid * LDS, blockIdx.x * TB + tid, tid, s_idx, s_cnt, s_top1);
     __syncthreads();
-    finish_block<EMAX>(a, s_buf, LDS, TB, s_idx, s_cnt, s_top1, wh, carry);
+    finish_block<EMAX>(a, s_buf, LDS, TB, s_idx, s_cnt, s_top1, wh, carry, blockIdx.x);
 }
 
 // ===================================================================== tile kernel
@@ -551,7 +551,7 @@ __global__ void __launch_bounds__(kThreads) route_tile_kernel(RouteArgs a) {
         }
     }
     __syncthreads();
-    finish_block<EMAX>(a, lg, Gm::LGS, Gm::TB, s_idx, s_cnt, s_top1, wh, carry);
+    finish_block<EMAX>(a, lg, Gm::LGS, Gm::TB, s_idx, s_cnt, s_top1, wh, carry, blockIdx.x);
 }
 
 template <typename TX, int EMAX>

@@ -74,18 +74,20 @@ __device__ void block_rank(const int* s_idx, int n, int E, int (*wh)[EMAX], int*
 // Per-block sums of p (rows of s_p, fixed order) and of the squared
 // log-sum-exp (column EMAX of s_p, the rows' pad slot), counts, and the fused
 // dispatch histogram.
+// blk: the block's index among the router blocks (its tokens start at
+// blk * TB).
 template <int EMAX>
 __device__ void finish_block(const RouteArgs& a, const float* s_p, int lds, int TB,
                              const int* s_idx, const int* s_cnt, const int* s_top1,
-                             int (*wh)[EMAX], int* carry) {
+                             int (*wh)[EMAX], int* carry, int blk) {
     const int tid = threadIdx.x;
-    const int t0 = blockIdx.x * TB;
+    const int t0 = blk * TB;
     if (tid < 32) {  // warp 0: tokens tid, tid + 32, ... then a fixed shuffle tree
         float z = 0.f;
         for (int tok = tid; tok < TB; tok += 32) z += s_p[tok * lds + EMAX];
 #pragma unroll
         for (int o = 16; o > 0; o >>= 1) z += __shfl_xor_sync(0xffffffffu, z, o);
-        if (tid == 0) a.blk_z[blockIdx.x] = z;
+        if (tid == 0) a.blk_z[blk] = z;
     }
     if (a.probs_t != nullptr) {  // transposed, token-contiguous per expert
         const int n = min(TB, a.T - t0);
@@ -97,13 +99,13 @@ __device__ void finish_block(const RouteArgs& a, const float* s_p, int lds, int 
     for (int e = tid; e < a.E; e += kThreads) {
         float v = 0.f;
         for (int tok = 0; tok < TB; ++tok) v += s_p[tok * lds + e];
-        a.blk_p[(size_t)blockIdx.x * a.E + e] = v;
+        a.blk_p[(size_t)blk * a.E + e] = v;
         if (s_cnt[e]) atomicAdd(&a.counts[e], s_cnt[e]);
         if (s_top1[e]) atomicAdd(&a.top1[e], s_top1[e]);
     }
     if (a.blk_hist != nullptr) {
         const int n = min(TB, a.T - t0) * a.k;
-        block_rank<EMAX>(s_idx, n, a.E, wh, carry, a.blk_hist + (size_t)blockIdx.x * a.E,
+        block_rank<EMAX>(s_idx, n, a.E, wh, carry, a.blk_hist + (size_t)blk * a.E,
                          a.local_rank + (size_t)t0 * a.k);
     }
 }

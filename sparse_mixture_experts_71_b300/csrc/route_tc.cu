@@ -15,6 +15,11 @@
 // x slices prefetched into L2 a few stages ahead; warp 1 issues the MMAs; warps 4-7 read the accumulator back
 // (TMEM lane = token) into shared memory.  Then one thread per token does the
 // softmax and top-k, and the block finishes like the other router kernels.
+// A small batch (too few 128-token tiles to fill the SMs) splits each tile's
+// K over a cluster of 2 or 4 CTAs: each accumulates its share of the
+// 64-column slices, rank 0 adds the other ranks' partial logits from their
+// shared memory (in rank order, so the sum repeats bit for bit) and
+// finishes the tile.
 
 #include <cuda.h>
 #include <cudaTypedefs.h>
@@ -83,7 +88,7 @@ __device__ __forceinline__ void drain_wait(uint64_t* bar, uint32_t parity) {
 template <int NP>
 __global__ void __launch_bounds__(kThreads, 2)
 route_tc_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constant__ CUtensorMap tmW,
-                RouteArgs a) {
+                RouteArgs a, int ks) {
     using C = RCfg<NP>;
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>(
@@ -100,8 +105,13 @@ route_tc_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constant__
     __shared__ int wh[kWarps][NP];
 
     const int tid = threadIdx.x, warp = tid / 32, lane = tid % 32;
-    const int t0 = blockIdx.x * TM;
+    // ks > 1: a cluster of ks CTAs shares the tile, each summing its share of
+    // K; rank 0 adds the others' partial logits and finishes the tile
+    const int rank = ks > 1 ? (int)tc::cluster_ctarank() : 0;
+    const int tile = blockIdx.x / ks;
+    const int t0 = tile * TM;
     const int KB = (a.d + RBK - 1) / RBK;
+    const int kb0 = rank * KB / ks, kb1 = (rank + 1) * KB / ks;  // this CTA's K steps
     const bool gemm = a.logits_in == nullptr;
 
     if (tid < NP) { s_cnt[tid] = 0; s_top1[tid] = 0; }
@@ -145,9 +155,10 @@ route_tc_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constant__
             int fills = 0;
             // x is read once: its boxes go to L2 kXPrefetch stages ahead of
             // their loads, so more of the batch is in flight than the ring holds
-            for (int j = 0; j < kXPrefetch && j < KB; ++j) tc::tma_prefetch_l2_2d(&tmX, j * RBK, t0);
-            for (int kb = 0; kb < KB; ++kb) {
-                if (kb + kXPrefetch < KB) tc::tma_prefetch_l2_2d(&tmX, (kb + kXPrefetch) * RBK, t0);
+            for (int j = kb0; j < kb0 + kXPrefetch && j < kb1; ++j)
+                tc::tma_prefetch_l2_2d(&tmX, j * RBK, t0);
+            for (int kb = kb0; kb < kb1; ++kb) {
+                if (kb + kXPrefetch < kb1) tc::tma_prefetch_l2_2d(&tmX, (kb + kXPrefetch) * RBK, t0);
                 if (!wait_or_abort(&empty[stage], phase ^ 1, abort_flag, a.hdr, 1)) break;
                 tc::mbar_expect_tx(&full[stage], C::STAGE_BYTES);
                 uint8_t* sa = smem + stage * C::STAGE_BYTES;
@@ -167,7 +178,7 @@ route_tc_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constant__
             int stage = 0;
             uint32_t phase = 0;
             bool ok = true;
-            for (int kb = 0; kb < KB && ok; ++kb) {
+            for (int kb = kb0; kb < kb1 && ok; ++kb) {
                 if (!wait_or_abort(&full[stage], phase, abort_flag, a.hdr, 2)) { ok = false; break; }
                 tc::fence_after_sync();
                 const uint32_t sa = tc::smem_u32(smem + stage * C::STAGE_BYTES);
@@ -178,7 +189,7 @@ route_tc_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constant__
                         tc::mma_bf16(tmem_base, tc::sdesc_k128_sw128(sa + kk * 32),
                                      tc::sdesc_k128_sw128(sa + RA_BYTES + part * C::PART_BYTES +
                                                           kk * 32),
-                                     idesc, (kb | kk | part) != 0 ? 1u : 0u);
+                                     idesc, (kb != kb0 || kk != 0 || part != 0) ? 1u : 0u);
                 tc::mma_commit(&empty[stage]);
                 if (++stage == RSTAGES) { stage = 0; phase ^= 1; }
             }
@@ -203,7 +214,7 @@ route_tc_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constant__
                     const int e = c0 + j;
                     if (e < NP) {
                         float g = v[j];
-                        if (a.bias != nullptr && e < a.E) g += __ldg(a.bias + e);
+                        if (a.bias != nullptr && e < a.E && rank == 0) g += __ldg(a.bias + e);
                         s_p[tok * C::LDS + e] = g;
                     }
                 }
@@ -216,6 +227,44 @@ route_tc_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constant__
         tc::fence_after_sync();
         tc::tmem_dealloc(tmem_base, C::TMEM_COLS);
     }
+    if (ks > 1) {
+        tc::cluster_sync();  // every rank's partial logits are in its shared memory
+        if (rank == 0) {
+            // 8 elements a round: their remote loads are all issued before the
+            // adds wait on any of them
+            uint32_t rbase[3];
+#pragma unroll
+            for (int r = 1; r < 4; ++r) rbase[r - 1] = r < ks ? tc::cluster_addr(s_p, (uint32_t)r) : 0u;
+            constexpr int PER = TM * NP / kThreads;
+            static_assert(PER % 8 == 0, "8-element rounds");
+#pragma unroll 1
+            for (int j0 = 0; j0 < PER; j0 += 8) {
+                int off[8];
+                float part[3][8];
+#pragma unroll
+                for (int q = 0; q < 8; ++q) {
+                    const int i = tid + (j0 + q) * kThreads;
+                    off[q] = (i / NP) * C::LDS + i % NP;
+                }
+#pragma unroll
+                for (int r = 1; r < 4; ++r)
+#pragma unroll
+                    for (int q = 0; q < 8; ++q)
+                        part[r - 1][q] = r < ks ? tc::ld_shared_cluster_f32(rbase[r - 1] + 4u * off[q])
+                                                : 0.f;
+#pragma unroll
+                for (int q = 0; q < 8; ++q) {
+                    float acc = s_p[off[q]];
+#pragma unroll
+                    for (int r = 1; r < 4; ++r)  // fixed order: rank 0 + 1 + 2 + 3
+                        if (r < ks) acc += part[r - 1][q];
+                    s_p[off[q]] = acc;
+                }
+            }
+        }
+        tc::cluster_sync();  // rank 0 has read the partials: the others leave
+        if (rank != 0) return;
+    }
     stage_logits<NP>(a, s_p, C::LDS, TM, t0);
     __syncthreads();
     if constexpr (NP == 64) {  // two threads per token (all 256)
@@ -226,7 +275,7 @@ route_tc_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constant__
         token_epilogue<NP>(a, s_p + tid * C::LDS, t0 + tid, tid, s_idx, s_cnt, s_top1);
     }
     __syncthreads();
-    finish_block<NP>(a, s_p, C::LDS, TM, s_idx, s_cnt, s_top1, wh, carry);
+    finish_block<NP>(a, s_p, C::LDS, TM, s_idx, s_cnt, s_top1, wh, carry, tile);
 }
 
 PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
@@ -267,10 +316,18 @@ cudaError_t launch_np(const RouteArgs& a, const __nv_bfloat16* wsplit, cudaStrea
         memset(&mx, 0, sizeof(mx));
         memset(&mw, 0, sizeof(mw));
     }
+    // few tiles (a small batch): split K over a cluster of 2 or 4 CTAs per
+    // tile while all the CTAs still fit one per SM, at least 4 K steps each
+    int ks = 1;
+    const int KB = (a.d + RBK - 1) / RBK;
+    while (a.logits_in == nullptr && ks < 4 && (int64_t)a.nblk * (2 * ks) <= num_sms() &&
+           KB >= 4 * (2 * ks))
+        ks *= 2;
     constexpr auto kern = route_tc_kernel<NP>;
     cudaError_t err = ensure_smem<kern>(C::SMEM);
     if (err != cudaSuccess) return err;
-    return launch_kernel(kern, dim3(a.nblk), dim3(kThreads), C::SMEM, s, 1, true, mx, mw, a);
+    return launch_kernel(kern, dim3(a.nblk * ks), dim3(kThreads), C::SMEM, s, ks, true, mx, mw, a,
+                         ks);
 }
 
 }  // namespace
