@@ -32,11 +32,13 @@
 //               computes 256 weight rows x 256 tokens with cta_group::2
 //               MMAs (M = 256); three stages of two K atoms; 16 (first GEMM)
 //               or 8 (second) epilogue warps; output by TMA tensor stores.
-//               The second GEMM may split each tile's K in two halves (when
-//               the half tiles fill the last wave of pairs better): the
-//               first half stores its product, the second adds its own by
-//               TMA reduce-add after a per-tile count of the first half's
-//               epilogue warps.
+//               Used one GEMM at a time by the backward pass (and its
+//               segment-reduction mode for the weight gradients).
+//   ffn_pair_kernel: the same CTA pairs running both GEMMs of the forward
+//               expert FFN in one persistent launch (first-GEMM tiles, then
+//               second-GEMM tiles gated by per-token-tile ready counts; the
+//               second GEMM may split each tile's K in two halves when the
+//               half tiles fill the last wave of pairs better).
 //   grouped_gemm_tc (decode-sized batches, token tiles of up to 64 rows):
 //               one CTA per SM, M = 128, eight stages; 8 epilogue warps;
 //               output by 16-byte lane stores.
@@ -105,15 +107,10 @@ struct Params {
     // make_map3 (one box covers a stage's ATOMS K atoms), 0 for 2-D maps
     // (one box per atom)
     int box3d;
-    // CTA-pair kernel, second GEMM: may split each tile's K in two halves
-    // (split_ok) when that evens out the waves; the second half adds its
-    // product to the first half's output once ksync[tile] (zero at launch)
-    // counts the first half's epilogue warps.  zero_ksync: this launch (the
-    // first GEMM) zeroes ksync[0 .. ksync_cap).
+    // fused expert FFN, second GEMM: per-tile counts of the first K half's
+    // epilogue warps when it splits K (zero at launch), ksync_cap of them
     int32_t* ksync;
     int ksync_cap;
-    int split_ok;
-    int zero_ksync;
 };
 
 // Rows of an expert's segment (offsets clamped to the buffers).
@@ -198,8 +195,9 @@ __device__ __forceinline__ void epilogue_tile(const Params& p, int e, int r0, in
                                               bool zero = false, bool accumulate = false) {
     const int f0 = fbase + q * 32;  // first weight row (output feature) of this warp
     const int f = f0 + lane;
-    // accumulate (second GEMM, second K half): out += acc * w, the bias
-    // having come with the first half
+    // accumulate (second GEMM, second K half): out += acc * w, the bias having
+    // come with the first half; full chunks by TMA reduce-add, the others by a
+    // plain load, add and store (a float atomic would flush subnormals)
     const float bias = f < p.n_out && p.bias != nullptr && !accumulate
                            ? __bfloat162float(p.bias[(size_t)e * p.n_out + f])
                            : 0.f;
@@ -263,14 +261,12 @@ __device__ __forceinline__ void epilogue_tile(const Params& p, int e, int r0, in
                 const int fc = f0 + part * 4;
                 if (j < rows_here && fc < p.n_out) {
                     const float4 val = *reinterpret_cast<const float4*>(stg + j * 128 + part * 16);
-                    float* dst = out + (size_t)(o0 + c + j) * p.n_out + fc;
+                    float4* dst = reinterpret_cast<float4*>(out + (size_t)(o0 + c + j) * p.n_out + fc);
                     if (accumulate) {
-                        atomicAdd(dst, val.x);
-                        atomicAdd(dst + 1, val.y);
-                        atomicAdd(dst + 2, val.z);
-                        atomicAdd(dst + 3, val.w);
+                        const float4 o = __ldcg(dst);
+                        *dst = make_float4(o.x + val.x, o.y + val.y, o.z + val.z, o.w + val.w);
                     } else {
-                        *reinterpret_cast<float4*>(dst) = val;
+                        *dst = val;
                     }
                 }
             }
@@ -483,6 +479,27 @@ __device__ __forceinline__ int ld_acquire_gpu(const int32_t* p) {
     int v;
     asm volatile("ld.acquire.gpu.global.b32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
     return v;
+}
+
+// wait_bar for warps with nothing else to do until the barrier completes (the
+// epilogue warps of the fused FFN, which outnumber the issuing threads): a
+// short sleep between polls leaves the issue slots to the producer and MMA
+// threads of the same SM sub-partitions.
+__device__ __forceinline__ bool wait_bar_idle(uint64_t* bar, uint32_t parity,
+                                              volatile int* abort_flag, const Params& p,
+                                              int where) {
+    if (tc::mbar_try_wait(bar, parity)) return true;
+    const uint64_t t0 = tc::globaltimer();
+    while (!tc::mbar_try_wait(bar, parity)) {
+        if (*abort_flag) return false;
+        if (tc::globaltimer() - t0 > p.timeout_ns) {
+            *abort_flag = 1;
+            record_error(p.hdr, kErrTimeout, where);
+            return false;
+        }
+        __nanosleep(256);
+    }
+    return true;
 }
 
 // Spin (bounded by the pipeline time-out) until *cnt >= target; a time-out
@@ -874,6 +891,12 @@ struct Cfg2 {
     static_assert(SMEM <= 232448, "shared memory budget");
 };
 
+// The CTA-pair token box for half_rows rows a CTA: the smallest of the 128-,
+// 64-, 32- and 16-row boxes that holds them (index into BMaps).
+__device__ __forceinline__ int pair_bsel_rows(int half_rows) {
+    return half_rows <= 16 ? 3 : half_rows <= 32 ? 2 : half_rows <= 64 ? 1 : 0;
+}
+
 // Token rows of operand bytes one group of token tiles may hold (see
 // decode_pair_tile): about half the 126 MB L2.
 constexpr long long kGroupBytes = 64ll << 20;
@@ -887,12 +910,14 @@ constexpr long long kGroupBytes = 64ll << 20;
 // weight tile passes over them (each weight tile is read once per group,
 // each token row about once) instead of the token rows being read again by
 // every wave of weight tiles.
+// s_tiles[e] * mul is expert e's first tile (mul = 1: a table of tiles;
+// mul = mt2: a table of token tiles, which both GEMMs of one layer share).
 __device__ __forceinline__ Tile decode_pair_tile(int t, const int* s_tiles, const Params& p,
-                                                 int mt2) {
+                                                 int mt2, int mul = 1) {
     int lo = 0, hi = p.E - 1;
     while (lo < hi) {  // last expert whose first tile is <= t
         const int mid = (lo + hi + 1) >> 1;
-        if (s_tiles[mid] <= t) lo = mid; else hi = mid - 1;
+        if (s_tiles[mid] * mul <= t) lo = mid; else hi = mid - 1;
     }
     int s0, s1;
     if (p.koff != nullptr) {  // segment reduction: tok_rows output rows per expert
@@ -903,7 +928,7 @@ __device__ __forceinline__ Tile decode_pair_tile(int t, const int* s_tiles, cons
         s1 = min(max(__ldg(p.offsets + lo + 1), s0), p.rows_cap);
     }
     const int nt = (s1 - s0 + BN2 - 1) / BN2;
-    const int local = t - s_tiles[lo];
+    const int local = t - s_tiles[lo] * mul;
     int gt = nt;  // token tiles per group
     if (p.koff == nullptr && (long long)nt * BN2 * p.K * 2 > kGroupBytes)
         gt = max(1, (int)(kGroupBytes / ((long long)BN2 * p.K * 2)));
@@ -963,10 +988,7 @@ grouped_gemm_pair(const __grid_constant__ CUtensorMap tmA, const __grid_constant
     }
     pdl_wait();  // offsets and the operands come from the previous kernel
     pdl_trigger();
-    int* s_split = reinterpret_cast<int*>(smem + C::OFF_MISC + 8);
     if (warp == 3) {  // exclusive prefix of pair tiles per expert
-        if (p.zero_ksync && blockIdx.x == 0)  // the second GEMM's half-tile counters
-            for (int i = lane; i < p.ksync_cap; i += 32) p.ksync[i] = 0;
         int run = 0;
         for (int e0 = 0; e0 < p.E; e0 += 32) {
             const int e = e0 + lane;
@@ -984,27 +1006,13 @@ grouped_gemm_pair(const __grid_constant__ CUtensorMap tmA, const __grid_constant
             if (e < p.E) s_tiles[e] = run + v - nt;
             run += __shfl_sync(0xffffffffu, v, 31);
         }
-        if (lane == 0) {
-            s_tiles[p.E] = run;
-            // split K in two when the half tiles fill the last wave of pairs
-            // clearly better than the whole ones (K a multiple of two stages)
-            int split = 0;
-            if (!GEMM1 && p.split_ok && p.koff == nullptr && run > 0 && run <= p.ksync_cap &&
-                p.K % (2 * ATOMS * BK) == 0) {
-                const float w = (float)run / (float)npairs;
-                split = 2.0f * w / ceilf(2.0f * w) > w / ceilf(w) + 0.05f;
-            }
-            *s_split = split;
-        }
+        if (lane == 0) s_tiles[p.E] = run;
     }
     tc::fence_before_sync();
     tc::cluster_sync();  // both CTAs' barriers and TMEM exist before any cross-CTA traffic
     tc::fence_after_sync();
     const uint32_t tmem_base = *s_tmem;
-    const int base_total = s_tiles[p.E];  // whole tiles
-    const int split = *s_split;           // 1: tile t + base_total is tile t's second K half
-    const int total = base_total << split;
-    const int KBh = KB >> split;          // stages per (half) tile
+    const int total = s_tiles[p.E];
 
     if (warp == 0) {
         // ------------------------------------------------ TMA producer (both CTAs)
@@ -1014,8 +1022,7 @@ grouped_gemm_pair(const __grid_constant__ CUtensorMap tmA, const __grid_constant
             long long fills = 0;
             bool ok = true;
             for (int t = pair; t < total && ok; t += npairs) {
-                const int kh = t >= base_total ? 1 : 0;
-                const Tile tl = decode_pair_tile(t - kh * base_total, s_tiles, p, mt2);
+                const Tile tl = decode_pair_tile(t, s_tiles, p, mt2);
                 const int m0 = tl.m0;  // pair tile base row
                 const int half_rows = ((tl.n + 31) & ~31) / 2;
                 // the smallest token box that holds this CTA's half_rows rows
@@ -1026,8 +1033,8 @@ grouped_gemm_pair(const __grid_constant__ CUtensorMap tmA, const __grid_constant
                 const bool red = p.koff != nullptr;
                 const int arow = (red ? 0 : tl.e * p.n_out) + m0 + rank * BM;
                 const int brow = (red ? tl.r0 - tl.e * p.tok_rows : tl.r0) + rank * half_rows;
-                const int k0 = red ? __ldg(p.koff + tl.e) : kh * KBh * ATOMS * BK;
-                const int KBt = red ? (seg_rows(p, tl.e) + ATOMS * BK - 1) / (ATOMS * BK) : KBh;
+                const int k0 = red ? __ldg(p.koff + tl.e) : 0;
+                const int KBt = red ? (seg_rows(p, tl.e) + ATOMS * BK - 1) / (ATOMS * BK) : KB;
                 for (int kb = 0; kb < KBt; ++kb) {
                     if (!wait_bar(&empty[stage], phase ^ 1, s_abort, p, 1)) { ok = false; break; }
                     if (leader) tc::mbar_expect_tx(&full[stage], bytes);
@@ -1062,8 +1069,7 @@ grouped_gemm_pair(const __grid_constant__ CUtensorMap tmA, const __grid_constant
             uint32_t phase = 0, acc_phase = 0;
             bool ok = true;
             for (int t = pair; t < total && ok; t += npairs) {
-                const Tile tl = decode_pair_tile(t >= base_total ? t - base_total : t, s_tiles, p,
-                                                 mt2);
+                const Tile tl = decode_pair_tile(t, s_tiles, p, mt2);
                 const uint32_t N = (uint32_t)((tl.n + 31) & ~31);
                 const uint32_t idesc = tc::idesc_bf16_f32(2 * BM, N);
                 const int half_rows = (int)N / 2;  // the producer's token box for this tile
@@ -1074,7 +1080,7 @@ grouped_gemm_pair(const __grid_constant__ CUtensorMap tmA, const __grid_constant
                 const uint32_t d_tmem = tmem_base + (uint32_t)(acc * BN2);
                 const int KBt = p.koff != nullptr
                                     ? (seg_rows(p, tl.e) + ATOMS * BK - 1) / (ATOMS * BK)
-                                    : KBh;
+                                    : KB;
                 for (int kb = 0; kb < KBt; ++kb) {
                     if (!wait_bar(&full[stage], phase, s_abort, p, 3)) { ok = false; break; }
                     tc::fence_after_sync();
@@ -1110,48 +1116,350 @@ grouped_gemm_pair(const __grid_constant__ CUtensorMap tmA, const __grid_constant
         int acc = 0;
         uint32_t acc_phase = 0;
         for (int t = pair; t < total; t += npairs) {
-            const int kh = t >= base_total ? 1 : 0;
-            const int tb = t - kh * base_total;  // the whole tile
-            const Tile tl = decode_pair_tile(tb, s_tiles, p, mt2);
+            const Tile tl = decode_pair_tile(t, s_tiles, p, mt2);
             const int m0 = tl.m0;
             const bool ok = wait_bar(&tfull[acc], acc_phase, s_abort, p, 4);
             if (!__all_sync(0xffffffffu, ok)) break;
             tc::fence_after_sync();
-            if (kh == 1) {
-                // the first K half of this tile is in the output: its 2 x EW
-                // epilogue warps have counted themselves in ksync[tb]
-                bool okw = true;
-                if (lane == 0) okw = wait_count(p.ksync + tb, 2 * EW, s_abort, p, 5);
-                if (!__all_sync(0xffffffffu, __shfl_sync(0xffffffffu, okw, 0))) break;
-                (void)ld_acquire_gpu(p.ksync + tb);  // every lane acquires
-                asm volatile("fence.proxy.async.global;" ::: "memory");
-            }
             if constexpr (GEMM1)
                 epilogue_gelu<EW / 4>(p, tl.e, tl.r0, tl.n, m0 + rank * BM, tmem_base, acc * BN2,
                                       q, part, lane, stg, &tmO);
             else
                 epilogue_tile<BN2, GEMM1>(p, tl.e, tl.r0, tl.r0, tl.n, m0 + rank * BM, tmem_base,
                                       acc * BN2, q, part, EW / 4, lane, stg, &tmO,
-                                      p.koff != nullptr && seg_rows(p, tl.e) == 0, kh == 1);
-            if (split && kh == 0) {
-                // publish this warp's part of the first half: its tensor
-                // stores complete, its plain stores fenced, then one count
-                if (lane == 0) {
-                    tc::bulk_wait_all();
-                    asm volatile("fence.proxy.async.global;" ::: "memory");
-                }
-                __threadfence();
-                __syncwarp();
-                if (lane == 0) {
-                    __threadfence();
-                    atomicAdd(p.ksync + tb, 1);
-                }
-            }
+                                      p.koff != nullptr && seg_rows(p, tl.e) == 0);
             tc::fence_before_sync();
             __syncwarp();
             if (lane == 0) tc::mbar_arrive_cluster_relaxed(tc::cluster_addr(&tempty[acc], 0));
             acc ^= 1;
             if (acc == 0) acc_phase ^= 1;
+        }
+    }
+
+    if (warp >= 4 && lane == 0) tc::bulk_wait_all();  // the output is written before exit
+    if (warp == 1 && lane == 0) drain_bar(drain, 0);
+    tc::fence_before_sync();
+    tc::cluster_sync();  // no cross-CTA arrive or MMA write is still pending
+    if (warp == 2) {
+        tc::fence_after_sync();
+        tc::tmem_dealloc_pair(tmem_base, C::TMEM_COLS);
+    }
+}
+
+// ------------------------------------------------------------------------
+// The expert FFN's two GEMMs in one persistent launch of CTA pairs.
+//
+// Work items: every first-GEMM tile (h = GELU(x_perm W1^T + b1)), then every
+// second-GEMM tile (y_perm = (h W2^T + b2) w, split in K halves by the same
+// rule as the second-GEMM kernel, first halves before second halves), dealt
+// round robin to the CTA pairs.  A pair that runs out of first-GEMM tiles
+// goes on to second-GEMM tiles while the others finish theirs, where two
+// launches make the whole second GEMM wait for the slowest pair's last
+// first-GEMM tile and for the launch boundary.  A second-GEMM tile reads the
+// h rows of one 256-token tile: its producer waits until every first-GEMM
+// tile of those rows has counted its 32 epilogue warps (2 CTAs x 16) in
+// ready[token tile], each after its h stores completed.  Every pair takes its
+// items in increasing order and all first-GEMM items come before all
+// second-GEMM items, so a wait is only ever on items that wait on nothing.
+//
+// 16 epilogue warps: all of them run a first-GEMM tile's GELU epilogue (2 KB
+// of staging each), the first 8 a second-GEMM tile's epilogue (4 KB each, TMA
+// stores of fp32 y_perm, as in the second-GEMM kernel).  The two layouts
+// overlap, so before its first second-GEMM tile each warp waits until all 16
+// have finished staging first-GEMM output (a bounded barrier; items come in
+// the same order to every warp, and all first-GEMM items come first).
+struct FfnPair {
+    Params g1, g2;   // g1: n_out = d_ff, K = d, GELU, bf16 h; g2: n_out = d, K = d_ff
+    int32_t* ready;  // [ready_cap] first-GEMM arrivals per token tile, zero at launch
+    int ready_cap;
+};
+
+// One work item of the fused kernel.
+struct FfnItem {
+    Tile tl;
+    int g;   // 0: first GEMM, 1: second
+    int kh;  // second GEMM split in K: 0 first half (or whole), 1 second half
+    int tb;  // the whole tile's index within its GEMM
+    int tt;  // token tile (index of its ready counter)
+};
+
+__device__ __forceinline__ FfnItem decode_ffn_item(int t, int n1, int n2, const int* s_tt,
+                                                   const FfnPair& f, int mt1, int mt2) {
+    FfnItem it;
+    if (t < n1) {
+        it.g = 0;
+        it.kh = 0;
+        it.tb = t;
+        it.tl = decode_pair_tile(t, s_tt, f.g1, mt1, mt1);
+    } else {
+        const int u = t - n1;
+        it.g = 1;
+        it.kh = u >= n2 ? 1 : 0;
+        it.tb = u - it.kh * n2;
+        it.tl = decode_pair_tile(it.tb, s_tt, f.g2, mt2, mt2);
+    }
+    const int s0 = min(max(__ldg(f.g1.offsets + it.tl.e), 0), f.g1.rows_cap);
+    it.tt = s_tt[it.tl.e] + (it.tl.r0 - s0) / BN2;
+    return it;
+}
+
+// Publish this warp's output of a finished item: its tensor stores complete,
+// its plain stores fenced, then one count.
+__device__ __forceinline__ void publish_count(int32_t* cnt, int lane) {
+    if (lane == 0) {
+        tc::bulk_wait_all();
+        asm volatile("fence.proxy.async.global;" ::: "memory");
+    }
+    __threadfence();
+    __syncwarp();
+    if (lane == 0) {
+        __threadfence();
+        atomicAdd(cnt, 1);
+    }
+}
+
+template <int STAGES, int ATOMS>
+__global__ void __launch_bounds__(Cfg2<STAGES, true, 16, ATOMS>::THREADS, 1)
+ffn_pair_kernel(const __grid_constant__ CUtensorMap tmA1, const __grid_constant__ BMaps tmB1,
+                const __grid_constant__ CUtensorMap tmO1, const __grid_constant__ CUtensorMap tmA2,
+                const __grid_constant__ BMaps tmB2, const __grid_constant__ CUtensorMap tmO2,
+                const FfnPair f) {
+    constexpr int EW = 16, EW2 = 8;  // epilogue warps of a first / second-GEMM tile
+    using C = Cfg2<STAGES, true, EW, ATOMS>;
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t* smem = reinterpret_cast<uint8_t*>(
+        (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    uint64_t* full = reinterpret_cast<uint64_t*>(smem + C::OFF_BARS);
+    uint64_t* empty = full + STAGES;
+    uint64_t* tfull = empty + STAGES;
+    uint64_t* tempty = tfull + 2;
+    uint64_t* drain = tempty + 2;
+    uint32_t* s_tmem = reinterpret_cast<uint32_t*>(smem + C::OFF_MISC);
+    volatile int* s_abort = reinterpret_cast<volatile int*>(smem + C::OFF_MISC + 4);
+    int* s_split = reinterpret_cast<int*>(smem + C::OFF_MISC + 8);
+    int* s_tt = reinterpret_cast<int*>(smem + C::OFF_TILES);  // token-tile prefix per expert
+    __shared__ uint64_t s_xfer;  // the epilogue warps' hand-over of the staging memory
+    const Params& P = f.g1;      // time-out and error record
+
+    const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
+    const int rank = (int)tc::cluster_ctarank();
+    const bool leader = rank == 0;
+    const int pair = blockIdx.x / 2, npairs = gridDim.x / 2;
+    const int mt1 = (f.g1.n_out + 2 * BM - 1) / (2 * BM), mt2 = (f.g2.n_out + 2 * BM - 1) / (2 * BM);
+    const int KB1 = (f.g1.K + ATOMS * BK - 1) / (ATOMS * BK);
+    const int KB2 = (f.g2.K + ATOMS * BK - 1) / (ATOMS * BK);
+    if (warp == 0 && lane == 0) {
+        for (int s = 0; s < STAGES; ++s) {
+            tc::mbar_init(&full[s], 1);
+            tc::mbar_init(&empty[s], 1);
+        }
+        for (int a = 0; a < 2; ++a) {
+            tc::mbar_init(&tfull[a], 1);
+            tc::mbar_init(&tempty[a], 2 * EW);
+        }
+        tc::mbar_init(drain, 1);
+        tc::mbar_init(&s_xfer, EW);
+        *s_abort = 0;
+        tc::fence_barrier_init();
+        tc::tma_prefetch_desc(&tmA1);
+        tc::tma_prefetch_desc(&tmA2);
+        for (int i = 0; i < 4; ++i) {
+            tc::tma_prefetch_desc(&tmB1.m[i]);
+            tc::tma_prefetch_desc(&tmB2.m[i]);
+        }
+    }
+    if (warp == 2) {
+        tc::tmem_alloc_pair(s_tmem, C::TMEM_COLS);
+        tc::tmem_relinquish_pair();
+    }
+    pdl_wait();  // offsets and x_perm come from the previous kernel
+    pdl_trigger();
+    if (warp == 3) {  // exclusive prefix of token tiles per expert
+        int run = 0;
+        for (int e0 = 0; e0 < f.g1.E; e0 += 32) {
+            const int e = e0 + lane;
+            const int nt = e < f.g1.E ? (seg_rows(f.g1, e) + BN2 - 1) / BN2 : 0;
+            int v = nt;
+#pragma unroll
+            for (int o = 1; o < 32; o <<= 1) {
+                const int u = __shfl_up_sync(0xffffffffu, v, o);
+                if (lane >= o) v += u;
+            }
+            if (e < f.g1.E) s_tt[e] = run + v - nt;
+            run += __shfl_sync(0xffffffffu, v, 31);
+        }
+        if (lane == 0) {
+            s_tt[f.g1.E] = run;
+            // the second GEMM's split in K, as in grouped_gemm_pair
+            const int n2 = run * mt2;
+            int split = 0;
+            if (n2 > 0 && n2 <= f.g2.ksync_cap && f.g2.K % (2 * ATOMS * BK) == 0) {
+                const float w = (float)n2 / (float)npairs;
+                split = 2.0f * w / ceilf(2.0f * w) > w / ceilf(w) + 0.05f;
+            }
+            *s_split = split;
+        }
+    }
+    tc::fence_before_sync();
+    tc::cluster_sync();  // both CTAs' barriers and TMEM exist before any cross-CTA traffic
+    tc::fence_after_sync();
+    const uint32_t tmem_base = *s_tmem;
+    const int TT = s_tt[f.g1.E];
+    const int n1 = TT * mt1, n2 = TT * mt2;
+    const int split = *s_split;
+    const int total = n1 + (n2 << split);
+    const int KB2h = KB2 >> split;
+    const int ready_target = mt1 * 2 * EW;  // arrivals of a token tile's first-GEMM items
+
+    if (warp == 0) {
+        // ------------------------------------------------ TMA producer (both CTAs)
+        if (lane == 0) {
+            int stage = 0;
+            uint32_t phase = 0;
+            long long fills = 0;
+            bool ok = true;
+            for (int t = pair; t < total && ok; t += npairs) {
+                const FfnItem it = decode_ffn_item(t, n1, n2, s_tt, f, mt1, mt2);
+                const Params& p = it.g ? f.g2 : f.g1;
+                const CUtensorMap* tA = it.g ? &tmA2 : &tmA1;
+                if (it.g == 1) {  // the h rows of this token tile are complete
+                    if (it.tt >= f.ready_cap ||
+                        !wait_count(f.ready + it.tt, ready_target, s_abort, P, 7)) {
+                        ok = false;
+                        break;
+                    }
+                    asm volatile("fence.proxy.async.global;" ::: "memory");
+                }
+                const int m0 = it.tl.m0;
+                const int half_rows = ((it.tl.n + 31) & ~31) / 2;
+                const int bsel = pair_bsel_rows(half_rows);
+                const CUtensorMap* tb = it.g ? &tmB2.m[bsel] : &tmB1.m[bsel];
+                const uint32_t bytes = 2 * ATOMS * (A_BYTES + (BN2 / 2 >> bsel) * BK * 2);
+                const int batom = (BN2 / 2 >> bsel) * BK * 2;
+                const int arow = it.tl.e * p.n_out + m0 + rank * BM;
+                const int brow = it.tl.r0 + rank * half_rows;
+                const int KBt = it.g ? KB2h : KB1;
+                const int k0 = it.kh * KB2h * ATOMS * BK;
+                for (int kb = 0; kb < KBt; ++kb) {
+                    if (!wait_bar(&empty[stage], phase ^ 1, s_abort, P, 1)) { ok = false; break; }
+                    if (leader) tc::mbar_expect_tx(&full[stage], bytes);
+                    const uint32_t full_l = tc::cluster_addr(&full[stage], 0);
+                    uint8_t* sa = smem + stage * C::STAGE_BYTES;
+                    uint8_t* sb = sa + ATOMS * A_BYTES;
+                    if (p.box3d) {
+                        const int kc = k0 / BK + kb * ATOMS;
+                        tc::tma_load_3d_pair(sa, tA, full_l, 0, arow, kc);
+                        tc::tma_load_3d_pair(sb, tb, full_l, 0, brow, kc);
+                    } else {
+#pragma unroll
+                        for (int at = 0; at < ATOMS; ++at) {
+                            const int kc = k0 + (kb * ATOMS + at) * BK;
+                            tc::tma_load_2d_pair(sa + at * A_BYTES, tA, full_l, kc, arow);
+                            tc::tma_load_2d_pair(sb + at * batom, tb, full_l, kc, brow);
+                        }
+                    }
+                    ++fills;
+                    if (++stage == STAGES) { stage = 0; phase ^= 1; }
+                }
+            }
+            const long long last = fills < STAGES ? fills : STAGES;
+            for (long long i = fills - last; i < fills; ++i)
+                drain_bar(&empty[i % STAGES], (uint32_t)((i / STAGES) & 1));
+        }
+    } else if (warp == 1) {
+        // ------------------------------------------------ MMA issuer (CTA 0)
+        if (lane == 0 && leader) {
+            int stage = 0, acc = 0;
+            uint32_t phase = 0, acc_phase = 0;
+            bool ok = true;
+            for (int t = pair; t < total && ok; t += npairs) {
+                const FfnItem it = decode_ffn_item(t, n1, n2, s_tt, f, mt1, mt2);
+                const uint32_t N = (uint32_t)((it.tl.n + 31) & ~31);
+                const uint32_t idesc = tc::idesc_bf16_f32(2 * BM, N);
+                const int bsel = pair_bsel_rows((int)N / 2);
+                const uint32_t batom = (uint32_t)((BN2 / 2 >> bsel) * BK * 2);
+                if (!wait_bar(&tempty[acc], acc_phase ^ 1, s_abort, P, 2)) break;
+                tc::fence_after_sync();
+                const uint32_t d_tmem = tmem_base + (uint32_t)(acc * BN2);
+                const int KBt = it.g ? KB2h : KB1;
+                for (int kb = 0; kb < KBt; ++kb) {
+                    if (!wait_bar(&full[stage], phase, s_abort, P, 3)) { ok = false; break; }
+                    tc::fence_after_sync();
+                    const uint32_t s0 = tc::smem_u32(smem + stage * C::STAGE_BYTES);
+#pragma unroll
+                    for (int at = 0; at < ATOMS; ++at) {
+                        const uint32_t sa = s0 + at * A_BYTES;
+                        const uint32_t sb = s0 + ATOMS * A_BYTES + at * batom;
+#pragma unroll
+                        for (int kk = 0; kk < BK / 16; ++kk)
+                            tc::mma_bf16_pair(d_tmem, tc::sdesc_k128_sw128(sa + kk * 32),
+                                              tc::sdesc_k128_sw128(sb + kk * 32), idesc,
+                                              (kb | at | kk) != 0 ? 1u : 0u);
+                    }
+                    tc::mma_commit_pair_mc(&empty[stage], 0x3);
+                    if (++stage == STAGES) { stage = 0; phase ^= 1; }
+                }
+                if (!ok) break;
+                tc::mma_commit_pair_mc(&tfull[acc], 0x3);
+                acc ^= 1;
+                if (acc == 0) acc_phase ^= 1;
+            }
+            tc::mma_commit_pair_mc(drain, 0x3);
+        }
+    } else if (warp >= 4) {
+        // ------------------------------------------------ epilogue (both CTAs)
+        const int ew = warp - 4;
+        const int q = warp & 3;
+        const int part = ew >> 2;  // which of the column parts of the tile
+        uint8_t* stg1 = smem + C::OFF_STAGING + ew * 32 * 32 * 2;
+        uint8_t* stg2 = smem + C::OFF_STAGING + ew * 32 * 32 * 4;
+        static_assert(EW2 * 32 * 32 * 4 <= C::STAGING, "second-GEMM staging");
+        int acc = 0;
+        uint32_t acc_phase = 0;
+        bool staged2 = false;  // this warp has handed over to second-GEMM staging
+        for (int t = pair; t < total; t += npairs) {
+            const FfnItem it = decode_ffn_item(t, n1, n2, s_tt, f, mt1, mt2);
+            const int fb = it.tl.m0 + rank * BM;
+            if (it.g == 1 && !staged2) {
+                // this warp's first-GEMM tensor stores have read its staging rows;
+                // once all 16 warps say so the second-GEMM layout may be written
+                if (lane == 0) {
+                    tc::bulk_wait_read_all();
+                    tc::mbar_arrive(&s_xfer);
+                }
+                __syncwarp();
+                const bool okx = wait_bar_idle(&s_xfer, 0, s_abort, P, 8);
+                if (!__all_sync(0xffffffffu, okx)) break;
+                staged2 = true;
+            }
+            const bool ok = wait_bar_idle(&tfull[acc], acc_phase, s_abort, P, 4);
+            if (!__all_sync(0xffffffffu, ok)) break;
+            tc::fence_after_sync();
+            if (it.kh == 1 && ew < EW2) {  // the first K half of this tile is in y_perm
+                bool okw = true;
+                if (lane == 0) okw = wait_count(f.g2.ksync + it.tb, 2 * EW2, s_abort, P, 5);
+                if (!__all_sync(0xffffffffu, __shfl_sync(0xffffffffu, okw, 0))) break;
+                (void)ld_acquire_gpu(f.g2.ksync + it.tb);  // every lane acquires
+                asm volatile("fence.proxy.async.global;" ::: "memory");
+            }
+            if (it.g == 0)
+                epilogue_gelu<EW / 4>(f.g1, it.tl.e, it.tl.r0, it.tl.n, fb, tmem_base, acc * BN2,
+                                      q, part, lane, stg1, &tmO1);
+            else if (ew < EW2)
+                epilogue_tile<BN2, false>(f.g2, it.tl.e, it.tl.r0, it.tl.r0, it.tl.n, fb,
+                                          tmem_base, acc * BN2, q, part, EW2 / 4, lane, stg2,
+                                          &tmO2, false, it.kh == 1);
+            // the accumulator is read: hand it back before waiting on the stores
+            tc::fence_before_sync();
+            __syncwarp();
+            if (lane == 0) tc::mbar_arrive_cluster_relaxed(tc::cluster_addr(&tempty[acc], 0));
+            acc ^= 1;
+            if (acc == 0) acc_phase ^= 1;
+            if (it.g == 0) {
+                if (it.tt < f.ready_cap) publish_count(f.ready + it.tt, lane);
+            } else if (split && it.kh == 0 && ew < EW2) {
+                publish_count(f.g2.ksync + it.tb, lane);
+            }
         }
     }
 
@@ -1237,6 +1545,14 @@ bool make_map3(CUtensorMap* m, const void* base, uint64_t inner, uint64_t outer,
 }
 
 constexpr int kPairAtoms = 2;  // K atoms per stage of the CTA-pair kernel
+
+// The fused expert FFN (ffn_pair_kernel) for layers whose GEMMs are at most
+// this many multiply-adds (T k d d_ff; upper bound on the kept rows).  In A/B
+// runs on one B300 it took the T = 4096 layer's expert FFN from 122.8 to
+// 117.5 us, the Switch layer's from 334 to 327 us and the expert-choice
+// layer's from 119.3 to 115.7 us, but the large-FFN layer's (T k d d_ff =
+// 1.9e12) from 5.16 to 5.49 ms, so that one keeps two launches.
+constexpr double kFusedFfnMaxWork = 1099511627776.0;  // 2^40
 
 // The CTA-pair kernel's operand maps: 3-D (one box per operand and stage)
 // when K is a multiple of 64 and the driver takes the 3-D view, else 2-D.
@@ -1331,6 +1647,18 @@ cudaError_t launch_one_pair(const CUtensorMap& a, const BMaps& b, const CUtensor
                          dim3(C::THREADS), C::SMEM, s, 2, true, a, b, o, p);
 }
 
+template <int STAGES, int ATOMS>
+cudaError_t launch_ffn_pair(const CUtensorMap& a1, const BMaps& b1, const CUtensorMap& o1,
+                            const CUtensorMap& a2, const BMaps& b2, const CUtensorMap& o2,
+                            const FfnPair& f, cudaStream_t s) {
+    using C = Cfg2<STAGES, true, 16, ATOMS>;
+    constexpr auto kern = ffn_pair_kernel<STAGES, ATOMS>;
+    cudaError_t err = ensure_smem<kern>(C::SMEM);
+    if (err != cudaSuccess) return err;
+    return launch_kernel(kern, dim3(2 * resident_clusters<kern>(2, C::SMEM, C::THREADS)),
+                         dim3(C::THREADS), C::SMEM, s, 2, true, a1, b1, o1, a2, b2, o2, f);
+}
+
 template <int BN_MAX, int STAGES>
 cudaError_t launch_pair(const CUtensorMap* maps, const Params& p1, const Params& p2,
                         cudaStream_t s) {
@@ -1353,7 +1681,7 @@ cudaError_t launch_expert_ffn_tc(const moe_config& c, const void* x_perm, int64_
                                  const int32_t* offsets, const void* W1, const void* b1,
                                  const void* W2, const void* b2, const float* perm_w,
                                  float* y_perm, void* h, int64_t h_rows, DeviceHeader* hdr,
-                                 int32_t* ksync, cudaStream_t s) {
+                                 int32_t* ksync, int32_t* ready, cudaStream_t s) {
     if (h_rows == 0) return cudaSuccess;
     // tokens per expert on average decides the widest token tile
     const bool wide = (int64_t)c.T * c.k >= 96LL * c.E;
@@ -1379,11 +1707,15 @@ cudaError_t launch_expert_ffn_tc(const moe_config& c, const void* x_perm, int64_
             !make_store_map_sw32(&so[0], h, c.d_ff, (uint64_t)h_rows) ||
             !make_store_map_f32(&so[1], y_perm, c.d, (uint64_t)h_rows))
             return cudaErrorInvalidValue;
-        // the first GEMM zeroes the counters the second may use to split K
-        p1.ksync = p2.ksync = ksync;
-        p1.ksync_cap = p2.ksync_cap = ksync != nullptr ? kKsyncCap : 0;
-        p1.zero_ksync = ksync != nullptr;
-        p2.split_ok = ksync != nullptr;
+        // Layers up to kFusedFfnMaxWork multiply-adds a GEMM run both GEMMs in
+        // one launch (its counters, ready and ksync, are zero); larger ones as
+        // two launches, where the boundary is a small share of the time.
+        if ((double)c.T * c.k * c.d * c.d_ff <= kFusedFfnMaxWork) {
+            p2.ksync = ksync;
+            p2.ksync_cap = kKsyncCap;
+            const FfnPair f{p1, p2, ready, ready_tiles(h_rows, c.E)};
+            return launch_ffn_pair<3, kPairAtoms>(a1, bx, so[0], a2, bh, so[1], f, s);
+        }
         cudaError_t err = launch_one_pair<3, true, 16, kPairAtoms>(a1, bx, so[0], p1, s);
         if (err != cudaSuccess) return err;
         return launch_one_pair<3, false, 8, kPairAtoms>(a2, bh, so[1], p2, s);

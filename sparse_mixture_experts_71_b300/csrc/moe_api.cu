@@ -61,7 +61,7 @@ cudaError_t launch_expert_ffn_tc(const moe_config& c, const void* x_perm, int64_
                                  const int32_t* offsets, const void* W1, const void* b1,
                                  const void* W2, const void* b2, const float* perm_w,
                                  float* y_perm, void* h, int64_t h_rows, DeviceHeader* hdr,
-                                 int32_t* ksync, cudaStream_t s);
+                                 int32_t* ksync, int32_t* ready, cudaStream_t s);
 
 namespace {
 
@@ -169,7 +169,10 @@ WsLayout ws_layout(const moe_config& c) {
     L.counts = take(sizeof(int32_t) * c.E);
     L.top1 = take(sizeof(int32_t) * c.E);
     L.sched = take(sizeof(int32_t) * (1 + c.E));  // zeroed with the counts (same memset)
-    L.ksync = take(sizeof(int32_t) * kKsyncCap);  // zeroed by the first expert GEMM
+    // the fused expert FFN's counters: zeroed with the counts by the router's
+    // memset (moe_expert_ffn zeroes them itself)
+    L.ksync = take(sizeof(int32_t) * kKsyncCap);
+    L.ready = take(sizeof(int32_t) * (size_t)ready_tiles(L.rows, c.E));
     L.blk_p = take(sizeof(float) * (size_t)L.route.blocks * cr.E);
     L.blk_z = take(sizeof(float) * (size_t)L.route.blocks);
     L.blk_hist = take(sizeof(int32_t) * (size_t)L.hist_blocks * c.E);
@@ -212,7 +215,7 @@ cudaError_t launch_expert_ffn(const moe_config& c, const void* x_perm, int64_t x
     if (c.dtype == MOE_BF16)
         return launch_expert_ffn_tc(c, x_perm, x_rows, offsets, W1, b1, W2, b2, perm_w, y_perm,
                                     at<void>(ws, L.h), L.rows, at<DeviceHeader>(ws, L.header),
-                                    at<int32_t>(ws, L.ksync), s);
+                                    at<int32_t>(ws, L.ksync), at<int32_t>(ws, L.ready), s);
     return launch_expert_ffn_simt(c, x_perm, offsets, W1, b1, W2, b2, perm_w, y_perm,
                                   at<void>(ws, L.h), max_segment(c), L.rows, s);
 }
@@ -331,6 +334,12 @@ moe_status moe_expert_ffn(const moe_config* cfg, const void* x_perm, const int32
     WsLayout L;
     if ((st = check_ws(c, ws, ws_bytes, &L)) != MOE_OK) return st;
     const moe_config cd = dispatch_config(c);
+    // the fused expert FFN's counters start at zero (moe_forward zeroes them
+    // with the router's counts)
+    const size_t cnt_end = L.ready + sizeof(int32_t) * (size_t)ready_tiles(L.rows, c.E);
+    if (cudaMemsetAsync(at<char>(ws, L.ksync), 0, cnt_end - L.ksync,
+                        reinterpret_cast<cudaStream_t>(stream)) != cudaSuccess)
+        return MOE_ERR_CUDA;
     chain_begin();
     return from_cuda(launch_expert_ffn(cd, x_perm, call_rows(c), offsets, W1, b1, W2, b2,
                                        perm_w, y_perm, ws, L,

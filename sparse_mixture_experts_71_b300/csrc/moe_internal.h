@@ -63,6 +63,9 @@ RouteGeom route_geom_beside(const moe_config& c);
 // Tiles of the second expert GEMM whose K may be split in two (CTA-pair
 // kernel): one first-half counter each in the workspace.
 constexpr int kKsyncCap = 512;
+// 256-token tiles the expert segments of `rows` permuted rows can form (one
+// ready counter each for the fused expert FFN).
+inline int ready_tiles(int64_t rows, int E) { return (int)((rows + 255) / 256) + E + 1; }
 
 // Byte offsets of the workspace regions for one configuration.
 struct WsLayout {
@@ -71,6 +74,7 @@ struct WsLayout {
     size_t top1;         // int32 [E]   first-slot choices per expert
     size_t sched;        // int32 [1+E] work-item counter and per-expert ready counts (dense decode FFN)
     size_t ksync;        // int32 [kKsyncCap] second expert GEMM: first-K-half counts per tile
+    size_t ready;        // int32 [ready_tiles] fused expert FFN: first-GEMM counts per token tile
     size_t blk_p;        // fp32 [route.blocks][E] per-block sums of p
     size_t blk_z;        // fp32 [route.blocks] per-block sums of the squared log-sum-exp
     size_t blk_hist;     // int32 [hist_blocks][E]

@@ -127,6 +127,11 @@ route_tc_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constant__
         if (gemm) {
             tc::tma_prefetch_desc(&tmX);
             tc::tma_prefetch_desc(&tmW);
+            // x is the caller's input, written before this call's first
+            // kernel started: its first slices can head for L2 while the
+            // previous kernel (the router-weight split) finishes
+            for (int j = kb0; j < kb0 + kXPrefetch && j < kb1; ++j)
+                tc::tma_prefetch_l2_2d(&tmX, j * RBK, t0);
         }
     }
     if (warp == 2) {
@@ -154,9 +159,8 @@ route_tc_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constant__
             uint32_t phase = 0;
             int fills = 0;
             // x is read once: its boxes go to L2 kXPrefetch stages ahead of
-            // their loads, so more of the batch is in flight than the ring holds
-            for (int j = kb0; j < kb0 + kXPrefetch && j < kb1; ++j)
-                tc::tma_prefetch_l2_2d(&tmX, j * RBK, t0);
+            // their loads, so more of the batch is in flight than the ring
+            // holds (the first ones before the programmatic wait, above)
             for (int kb = kb0; kb < kb1; ++kb) {
                 if (kb + kXPrefetch < kb1) tc::tma_prefetch_l2_2d(&tmX, (kb + kXPrefetch) * RBK, t0);
                 if (!wait_or_abort(&empty[stage], phase ^ 1, abort_flag, a.hdr, 1)) break;

@@ -131,6 +131,11 @@ __device__ __forceinline__ uint32_t cluster_addr(const void* p, uint32_t rank) {
     asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(smem_u32(p)), "r"(rank));
     return r;
 }
+// Arrive with release semantics (the arriving thread's earlier memory
+// operations are visible to a thread that then sees the phase complete).
+__device__ __forceinline__ void mbar_arrive(uint64_t* bar) {
+    asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_u32(bar)) : "memory");
+}
 // Relaxed arrives, for barriers that only hand back a resource whose use is
 // already complete and fenced (an accumulator after tcgen05.wait::ld and
 // tcgen05.fence::before_thread_sync): they do not wait for the arriving

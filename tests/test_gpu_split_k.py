@@ -1,9 +1,11 @@
-"""The second expert GEMM with each tile's K split in two halves: the CTA-pair
-kernel does this when the half tiles fill the last wave of the 74 CTA pairs
-clearly better than whole tiles (the first half stores (acc + b2) w, the
-second adds acc w once the first half's epilogue warps have counted
-themselves), so the layer output must still match the oracle and repeat bit
-for bit.
+"""The second expert GEMM with each tile's K split in two halves: the fused
+expert-FFN kernel (both GEMMs in one launch of CTA pairs) does this when the
+half tiles fill the last wave of the 74 CTA pairs clearly better than whole
+tiles (the first half stores (acc + b2) w, the second adds acc w once the
+first half's epilogue warps have counted themselves), so the layer output
+must still match the oracle and repeat bit for bit.  The second-GEMM tiles
+also wait on the first GEMM's per-token-tile ready counts, which every
+forward test exercises.
 
 "Mixture of Experts: Scaling Parameters Without Scaling Compute", section
 "The MoE layer": y_t = sum over the chosen experts of w_e (W2_e GELU(W1_e x_t
