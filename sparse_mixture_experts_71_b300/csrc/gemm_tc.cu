@@ -1150,9 +1150,12 @@ grouped_gemm_pair(const __grid_constant__ CUtensorMap tmA, const __grid_constant
 // The expert FFN's two GEMMs in one persistent launch of CTA pairs.
 //
 // Work items: every first-GEMM tile (h = GELU(x_perm W1^T + b1)), then every
-// second-GEMM tile (y_perm = (h W2^T + b2) w, split in K halves by the same
-// rule as the second-GEMM kernel, first halves before second halves), dealt
-// round robin to the CTA pairs.  A pair that runs out of first-GEMM tiles
+// second-GEMM tile (y_perm = (h W2^T + b2) w), dealt round robin to the CTA
+// pairs.  When the second GEMM's w = tiles / pairs waves end better in half
+// tiles (2w / ceil(2w) > w / ceil(w) + 0.05) its K is split in two: the first
+// halves come before all second halves, a first half stores (acc + b2) w and
+// the second adds acc w once ksync[tile] counts the first half's 16 epilogue
+// warps (a fixed order, so the result repeats bit for bit).  A pair that runs out of first-GEMM tiles
 // goes on to second-GEMM tiles while the others finish theirs, where two
 // launches make the whole second GEMM wait for the slowest pair's last
 // first-GEMM tile and for the launch boundary.  A second-GEMM tile reads the
@@ -1290,7 +1293,7 @@ ffn_pair_kernel(const __grid_constant__ CUtensorMap tmA1, const __grid_constant_
         }
         if (lane == 0) {
             s_tt[f.g1.E] = run;
-            // the second GEMM's split in K, as in grouped_gemm_pair
+            // the second GEMM's split in K (see above)
             const int n2 = run * mt2;
             int split = 0;
             if (n2 > 0 && n2 <= f.g2.ksync_cap && f.g2.K % (2 * ATOMS * BK) == 0) {
