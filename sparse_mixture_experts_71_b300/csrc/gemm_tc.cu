@@ -1550,12 +1550,13 @@ bool make_map3(CUtensorMap* m, const void* base, uint64_t inner, uint64_t outer,
 constexpr int kPairAtoms = 2;  // K atoms per stage of the CTA-pair kernel
 
 // The fused expert FFN (ffn_pair_kernel) for layers whose GEMMs are at most
-// this many multiply-adds (T k d d_ff; upper bound on the kept rows).  In A/B
-// runs on one B300 it took the T = 4096 layer's expert FFN from 122.8 to
-// 117.5 us, the Switch layer's from 334 to 327 us and the expert-choice
-// layer's from 119.3 to 115.7 us, but the large-FFN layer's (T k d d_ff =
-// 1.9e12) from 5.16 to 5.49 ms, so that one keeps two launches.
-constexpr double kFusedFfnMaxWork = 1099511627776.0;  // 2^40
+// this many multiply-adds (T k d d_ff; upper bound on the kept rows).  A/B
+// on one B300, expert FFN alone (uniform segments, L2 flushed), fused vs two
+// launches: (T k, d, d_ff) = (8192, 1024, 4096) 114.7 vs 118.8 us; (16384,
+// 2048, 8192) 682 vs 682 us; (16384, 4096, 14336) 2.30 vs 2.26 ms; (32768,
+// 4096, 14336) 5.46-5.71 vs 5.46-5.57 ms.  In the full layer the Switch
+// layer (32768 x 2048 x 8192 = 2^39) went from 334 to 327 us.
+constexpr double kFusedFfnMaxWork = 549755813888.0;  // 2^39
 
 // The CTA-pair kernel's operand maps: 3-D (one box per operand and stage)
 // when K is a multiple of 64 and the driver takes the 3-D view, else 2-D.
