@@ -315,7 +315,11 @@ def ffn_roofline(wl, work, ffn_ms, pk, pk_kind):
                 "frac_of_8tbs_nominal": achieved / 8000.0,
                 "algorithmic": f"used-expert weights + kept rows in and out = "
                                f"{work['ffn_bytes']:.4g} B per launch pair"}
-    roof.update({"kernel": "expert FFN (grouped GEMM1 + GEMM2)", "achieved": achieved,
+    fused = (wl.dtype == "bf16" and wl.T * wl.k >= 96 * wl.E and
+             wl.T * wl.k * wl.d * wl.F <= 2 ** 39)  # the library's rule (csrc/gemm_tc.cu)
+    kern = ("expert FFN (ffn_pair_kernel: both grouped GEMMs in one launch)" if fused
+            else "expert FFN (grouped GEMM1 + GEMM2)")
+    roof.update({"kernel": kern, "achieved": achieved,
                  "peak": peak, "frac": achieved / peak, "traffic": traffic,
                  "traffic_source": traffic_src})
     return roof
