@@ -82,6 +82,22 @@ moe_status moe_backward(const moe_config* cfg, const void* x, const float* W_r,
                         float* dW_r, float* dW1, float* db1, float* dW2, float* db2, void* ws,
                         size_t ws_bytes, void* stream);
 
+/*
+ * Diagnostics: the weight-gradient products of moe_backward read each expert
+ * segment through its own TMA tensor map, made on the device by editing a
+ * copy of a whole-buffer map (base address and row extent, PTX
+ * tensormap.replace).  This call makes such maps for three test segments (a
+ * ragged, an empty and a long one) in both views the products use (3-D and
+ * 2-D boxes), copies them back and compares them byte for byte with the
+ * driver's own encoding of the same segments (cuTensorMapEncodeTiled).  No
+ * tensor copy runs.  ws: at least 3 MiB of device memory, 256-byte aligned
+ * (MOE_ERR_WORKSPACE otherwise); its first 2 KB are overwritten.  Returns
+ * MOE_OK when every map matches, MOE_ERR_UNSUPPORTED on a mismatch,
+ * MOE_ERR_CUDA when a CUDA call fails.  Synchronises `stream`.  No
+ * counterpart on the pages.
+ */
+moe_status moe_check_segment_maps(void* ws, size_t ws_bytes, void* stream);
+
 #ifdef __cplusplus
 }
 #endif

@@ -30,7 +30,7 @@ EXPORTED = ("moe_workspace_size", "moe_status_string", "moe_route", "moe_dispatc
             "moe_update_balance_bias", "moe_pipeline_workspace_size", "moe_pipeline_create",
             "moe_pipeline_submit", "moe_pipeline_join", "moe_pipeline_destroy",
             "moe_route_expert_choice", "moe_expert_choice_capacity",
-            "moe_backward_workspace_size", "moe_backward")
+            "moe_backward_workspace_size", "moe_backward", "moe_check_segment_maps")
 
 
 class MoeConfig(ctypes.Structure):
@@ -88,6 +88,8 @@ def load() -> ctypes.CDLL:
         lib.moe_expert_choice_capacity.argtypes = [cfgp]
         lib.moe_backward_workspace_size.restype = ctypes.c_size_t
         lib.moe_backward_workspace_size.argtypes = [cfgp]
+        lib.moe_check_segment_maps.restype = ctypes.c_int
+        lib.moe_check_segment_maps.argtypes = [_P, sz, _P]
         lib.moe_backward.restype = ctypes.c_int
         lib.moe_backward.argtypes = ([cfgp] + [_P] * 8 + [ctypes.c_float, ctypes.c_float]
                                      + [_P] * 7 + [sz, _P])
@@ -259,6 +261,14 @@ def check_wait_timeout(ws, timeout_ns: int, stream=None) -> None:
     is recorded in ws's error record (read it with get_device_error)."""
     _check("moe_check_wait_timeout",
            load().moe_check_wait_timeout(_ptr(ws), ctypes.c_uint64(timeout_ns), _stream(stream)))
+
+
+def check_segment_maps(ws, stream=None) -> None:
+    """Check the device-side edits of the per-segment tensor maps the backward
+    pass's weight-gradient products use against the driver's encoding
+    (diagnostics; ws: a device buffer of at least 3 MiB; synchronises)."""
+    _check("moe_check_segment_maps", load().moe_check_segment_maps(
+        _ptr(ws), ctypes.c_size_t(ws.numel() * ws.element_size()), _stream(stream)))
 
 
 def get_device_error(ws, stream=None):

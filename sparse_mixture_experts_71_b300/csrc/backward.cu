@@ -7,23 +7,22 @@
 //
 // Steps (one stream):
 //   recompute   router (logits kept) + dispatch, GEMM1 without GELU -> U,
-//               H = GELU(U) (with H transposed per segment for dW2), GEMM2 ->
-//               y_perm = w * o
+//               H = GELU(U), GEMM2 -> y_perm = w * o
 //   router      one warp per token: s_j = <dy_t, y_perm[slot_j]>, the logit
 //               gradient dg (softmax / renormalisation, auxiliary loss,
 //               z-loss) and dY_perm[slot_j] = w_j dy_t
-//   dx path     W2, W1 transposed per expert; dH = dY_perm W2_e (the
-//               forward's tcgen05 GEMM with W2^T as its weight), dU = dH *
-//               GELU'(U) (with dU transposed per segment for dW1),
-//               dX_perm = dU W1_e (W1^T); dx = sum over the
-//               token's slots of dX_perm + dg W_r
+//   dx path     dH = dY_perm W2_e and dX_perm = dU W1_e on the CTA-pair
+//               tcgen05 kernel with the weights read MN-major as they are
+//               stored (W2_e [d][d_ff] is dH's [K][N]), dU = dH * GELU'(U);
+//               dx = sum over the token's slots of dX_perm + dg W_r
 //   weights     dW2_e = dY_perm_e^T H_e and dW1_e = dU_e^T X_perm_e on the
-//               CTA-pair tcgen05 kernel in its segment-reduction mode (both
-//               operands transposed per expert segment, K = the segment's
-//               rows), dW_r = dg^T x on CUDA cores (row-slice partials summed
-//               in a fixed order), db2, db1 = column sums over each expert's
-//               rows.  GELU and GELU' use the forward epilogue's
-//               Abramowitz & Stegun 7.1.26 erf.
+//               same kernel in its segment-reduction mode (K = the segment's
+//               rows; both operands read MN-major from the row-major
+//               permuted rows through per-segment tensor maps, so a segment's
+//               last K stage reads zeros past its end), dW_r = dg^T x on CUDA
+//               cores (row-slice partials summed in a fixed order), db2, db1
+//               = column sums over each expert's rows.  GELU and GELU' use
+//               the forward epilogue's Abramowitz & Stegun 7.1.26 erf.
 
 #include <cuda_runtime.h>
 #include <cuda_bf16.h>
@@ -34,19 +33,8 @@
 
 namespace moe {
 
-cudaError_t launch_grouped_gemm_tc(const moe_config& c, bool bf16_out, bool act, const void* A,
-                                   int64_t a_rows, const int32_t* offsets, const void* W,
-                                   const void* bias, const float* row_w, void* out,
-                                   int64_t out_rows, int n_out, int K, DeviceHeader* hdr,
-                                   cudaStream_t s);
-cudaError_t launch_segment_reduction_tc(int E, const int32_t* offsets, int64_t rows_cap,
-                                        const int32_t* koff, const void* TOK, int tok_rows,
-                                        const void* WT, int n_out, int64_t kcols, float* out,
-                                        DeviceHeader* hdr, cudaStream_t s);
-
 namespace {
 
-constexpr int kSegPad = 128;  // K columns per stage of the CTA-pair kernel
 
 using bf16 = __nv_bfloat16;
 
@@ -223,84 +211,6 @@ __global__ void __launch_bounds__(256) router_grad_kernel(
     }
 }
 
-// 64 x 64 bf16 tile transposes: 16-byte global loads and stores, the tile
-// in shared memory with an odd word stride (33 words a row) so that the
-// column reads spread over the banks.
-constexpr int TP = 64, TP_LD = 66;  // tile side, shared row length (bf16)
-
-// Stage rows src(i) (i < 64; null: zeros), columns c0 .. c0 + 63 of a
-// row-major matrix with `ld` columns, into tile[i][.].
-template <typename RowPtr>
-__device__ __forceinline__ void tile_load(bf16 (*tile)[TP_LD], RowPtr src, int c0, int C) {
-    const int t = threadIdx.x;
-#pragma unroll
-    for (int h = 0; h < 2; ++h) {
-        const int i = t / 8 + 32 * h, cg = (t % 8) * 8;
-        const bf16* row = src(i);
-        uint4 q = make_uint4(0, 0, 0, 0);
-        if (row != nullptr && c0 + cg < C) q = __ldg(reinterpret_cast<const uint4*>(row + c0 + cg));
-        const uint32_t* w = reinterpret_cast<const uint32_t*>(&q);
-        uint32_t* dst = reinterpret_cast<uint32_t*>(&tile[i][cg]);
-#pragma unroll
-        for (int k = 0; k < 4; ++k) dst[k] = w[k];
-    }
-}
-
-// Write the transposed tile: out row (c0 + j) gets tile[0..63][j] at
-// columns r_out .. r_out + 63 (dst(j): the row's start, null: skip).
-template <typename RowPtr>
-__device__ __forceinline__ void tile_store(bf16 (*tile)[TP_LD], RowPtr dst) {
-    const int t = threadIdx.x;
-#pragma unroll
-    for (int h = 0; h < 2; ++h) {
-        const int j = t / 8 + 32 * h, rg = (t % 8) * 8;
-        bf16* row = dst(j);
-        if (row == nullptr) continue;
-        uint4 q;
-        bf16* v = reinterpret_cast<bf16*>(&q);
-#pragma unroll
-        for (int k = 0; k < 8; ++k) v[k] = tile[rg + k][j];
-        *reinterpret_cast<uint4*>(row + rg) = q;
-    }
-}
-
-// out[e][c][r] = in[e][r][c] for R x C bf16 matrices (R, C multiples of 8);
-// an expert whose segment is empty is skipped (no GEMM reads its copy).
-__global__ void __launch_bounds__(256) transpose_kernel(const bf16* __restrict__ in, int R, int C,
-                                                        const int32_t* __restrict__ offsets,
-                                                        int64_t rows_cap,
-                                                        bf16* __restrict__ out) {
-    __shared__ __align__(16) bf16 tile[TP][TP_LD];
-    pdl_wait();
-    pdl_trigger();
-    {
-        const int e = blockIdx.z;
-        const int64_t r1 = min((int64_t)max(__ldg(offsets + e + 1), 0), rows_cap);
-        const int64_t r0 = min((int64_t)max(__ldg(offsets + e), 0), r1);
-        if (r1 == r0) return;
-    }
-    const size_t base = (size_t)blockIdx.z * R * C;
-    const int c0 = blockIdx.x * TP, r0 = blockIdx.y * TP;
-    tile_load(tile, [&](int i) -> const bf16* {
-        return r0 + i < R ? in + base + (size_t)(r0 + i) * C : nullptr;
-    }, c0, C);
-    __syncthreads();
-    // rows of the output are columns of the input; a partial last group of
-    // 8 output columns (R not a multiple of 64) is written element by element
-    const int t = threadIdx.x;
-#pragma unroll
-    for (int h = 0; h < 2; ++h) {
-        const int j = t / 8 + 32 * h, rg = (t % 8) * 8;
-        if (c0 + j >= C || r0 + rg >= R) continue;
-        bf16* row = out + base + (size_t)(c0 + j) * R + r0;
-        uint4 q;
-        bf16* v = reinterpret_cast<bf16*>(&q);
-#pragma unroll
-        for (int k = 0; k < 8; ++k) v[k] = tile[rg + k][j];
-        *reinterpret_cast<uint4*>(row + rg) = q;  // R % 8 == 0: the group is whole
-    }
-}
-
 __device__ __forceinline__ void store4(float* p, float4 v) { *reinterpret_cast<float4*>(p) = v; }
 __device__ __forceinline__ void store4(bf16* p, float4 v) {
     __nv_bfloat162 lo = __floats2bfloat162_rn(v.x, v.y), hi = __floats2bfloat162_rn(v.z, v.w);
@@ -440,104 +350,43 @@ __global__ void __launch_bounds__(256) colsum_kernel(const T* __restrict__ A,
     }
 }
 
-// koff[e] = sum over e' < e of the segment lengths rounded up to kSegPad
-// (koff[E]: the total), one warp.
-__global__ void __launch_bounds__(32) seg_koff_kernel(const int32_t* __restrict__ offsets, int E,
-                                                      int64_t rows_cap,
-                                                      int32_t* __restrict__ koff) {
-    pdl_wait();
-    pdl_trigger();
-    const int lane = threadIdx.x;
-    int carry = 0;
-    for (int e0 = 0; e0 < E; e0 += 32) {
-        const int e = e0 + lane;
-        int v = 0;
-        if (e < E) {
-            const int r1 = (int)min((int64_t)max(__ldg(offsets + e + 1), 0), rows_cap);
-            const int r0 = min(max(__ldg(offsets + e), 0), r1);
-            v = (r1 - r0 + kSegPad - 1) / kSegPad * kSegPad;
-        }
-        int incl = v;
-#pragma unroll
-        for (int o = 1; o < 32; o <<= 1) {
-            const int u = __shfl_up_sync(0xffffffffu, incl, o);
-            if (lane >= o) incl += u;
-        }
-        if (e < E) koff[e] = carry + incl - v;
-        carry += __shfl_sync(0xffffffffu, incl, 31);
-    }
-    if (lane == 0) koff[E] = carry;
-}
-
-// Every expert segment of a [rows][M] matrix transposed into out [M][kcols]:
-// out[m][koff[e] + j] = V[offsets[e] + j][m] for j < the segment's length,
-// 0 for the rest of its padded window, where V is
-//   kSegCopy      A itself;
-//   kSegGelu      GELU(A) (A = U), also written row-major to rowout (H);
-//   kSegGeluGrad  rowout * GELU'(A) (A = U, rowout = dH, overwritten in
-//                 place with dU).
-// 64 x 64 tiles (a tile never spans two windows: they start at multiples of
-// kSegPad); every kept row is covered by exactly one window position.
-enum SegOp { kSegCopy = 0, kSegGelu = 1, kSegGeluGrad = 2 };
+// Over the rows of the expert segments (offsets[0] .. offsets[E]) of [rows][F]
+// bf16 matrices, eight columns a thread (F a multiple of 8):
+//   kRowGelu      out = GELU(U), the forward epilogue's GELU (H);
+//   kRowGeluGrad  out *= GELU'(U) (out = dH, overwritten with dU).
+enum RowOp { kRowGelu = 0, kRowGeluGrad = 1 };
 
 template <int OP>
-__global__ void __launch_bounds__(256) seg_transpose_kernel(const bf16* __restrict__ A,
-                                                             bf16* __restrict__ rowout,
-                                                             const int32_t* __restrict__ offsets,
-                                                             const int32_t* __restrict__ koff,
-                                                             int E, int M, int64_t rows_cap,
-                                                             int64_t kcols, bf16* __restrict__ out) {
-    __shared__ __align__(16) bf16 tile[TP][TP_LD];
+__global__ void __launch_bounds__(256) gelu_rows_kernel(const bf16* __restrict__ U,
+                                                         bf16* out,
+                                                         const int32_t* __restrict__ offsets,
+                                                         int E, int F, int64_t rows_cap) {
     pdl_wait();
     pdl_trigger();
-    const int c0 = blockIdx.x * TP, m0 = blockIdx.y * TP;
-    if (c0 >= __ldg(koff + E)) return;  // past the last window: never read
-    int lo = 0, hi = E - 1;
-    while (lo < hi) {  // last expert whose window starts at or before c0
-        const int mid = (lo + hi + 1) >> 1;
-        if (__ldg(koff + mid) <= c0) lo = mid; else hi = mid - 1;
-    }
-    const int r1 = (int)min((int64_t)max(__ldg(offsets + lo + 1), 0), rows_cap);
-    const int r0 = min(max(__ldg(offsets + lo), 0), r1);
-    const int j0 = c0 - __ldg(koff + lo);
-    const int t = threadIdx.x;
+    const int64_t r1 = min((int64_t)max(__ldg(offsets + E), 0), rows_cap);
+    const int64_t r0 = min((int64_t)max(__ldg(offsets), 0), r1);
+    const int64_t n8 = (r1 - r0) * (F / 8);
+    const size_t base = (size_t)r0 * F;
+    for (int64_t i = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; i < n8;
+         i += (int64_t)gridDim.x * blockDim.x) {
+        const size_t at_ = base + (size_t)i * 8;
+        float f[8];
+        load8(U + at_, f);
+        if (OP == kRowGelu) {
 #pragma unroll
-    for (int h = 0; h < 2; ++h) {  // tile[i][.] = V row r0 + j0 + i (zeros past the segment)
-        const int i = t / 8 + 32 * h, cg = (t % 8) * 8;
-        const int r = r0 + j0 + i;
-        uint4 q = make_uint4(0, 0, 0, 0);
-        if (r < r1 && m0 + cg < M) {
-            const size_t at_ = (size_t)r * M + m0 + cg;
-            q = __ldg(reinterpret_cast<const uint4*>(A + at_));
-            if (OP != kSegCopy) {
-                float f[8];
-                unpack8(q, f);
-                if (OP == kSegGelu) {
-#pragma unroll
-                    for (int j = 0; j < 8; j += 2) {  // the forward epilogue's GELU
-                        const float2 g = gelu2_as7126(make_float2(f[j], f[j + 1]));
-                        f[j] = g.x;
-                        f[j + 1] = g.y;
-                    }
-                } else {
-                    float g[8];
-                    unpack8(*reinterpret_cast<const uint4*>(rowout + at_), g);
-#pragma unroll
-                    for (int j = 0; j < 8; ++j) f[j] = g[j] * gelu_grad(f[j]);
-                }
-                q = pack8(f);
-                *reinterpret_cast<uint4*>(rowout + at_) = q;
+            for (int j = 0; j < 8; j += 2) {
+                const float2 g = gelu2_as7126(make_float2(f[j], f[j + 1]));
+                f[j] = g.x;
+                f[j + 1] = g.y;
             }
-        }
-        const uint32_t* w = reinterpret_cast<const uint32_t*>(&q);
-        uint32_t* dst = reinterpret_cast<uint32_t*>(&tile[i][cg]);
+        } else {
+            float g[8];
+            unpack8(*reinterpret_cast<const uint4*>(out + at_), g);
 #pragma unroll
-        for (int kq = 0; kq < 4; ++kq) dst[kq] = w[kq];
+            for (int j = 0; j < 8; ++j) f[j] = g[j] * gelu_grad(f[j]);
+        }
+        store8(out + at_, f);
     }
-    __syncthreads();
-    tile_store(tile, [&](int j) -> bf16* {
-        return m0 + j < M ? out + (size_t)(m0 + j) * kcols + c0 : nullptr;
-    });
 }
 
 // out[i] = sum over z < S of part[z][i], in z order.
@@ -562,8 +411,7 @@ int grid_for(int64_t work, int per_block) {
 
 // Backward workspace: the forward layout, then these regions.
 struct BwdLayout {
-    size_t logits, u, dyp, dh, w1t, w2t, dg, koff, tt_d, tt_f, parts, total;
-    int64_t kcols;     // columns of the segment-transposed operands
+    size_t logits, u, dyp, dh, dg, maps, parts, total;
     int wr_slices;     // row slices of the router-weight gradient
 };
 
@@ -591,13 +439,9 @@ BwdLayout bwd_layout(const moe_config& c, const WsLayout& L) {
     B.u = take(es * rows * c.d_ff);
     B.dyp = take(es * rows * c.d);
     B.dh = take(es * rows * c.d_ff);
-    B.w1t = take(f32 ? 0 : 2 * (size_t)c.E * c.d * c.d_ff);
-    B.w2t = take(f32 ? 0 : 2 * (size_t)c.E * c.d * c.d_ff);
     B.dg = take(sizeof(float) * (size_t)c.T * c.E);
-    B.koff = take(sizeof(int32_t) * (size_t)(c.E + 1));
-    B.kcols = (L.rows + (int64_t)kSegPad * c.E + kSegPad - 1) / kSegPad * kSegPad;
-    B.tt_d = take(f32 ? 0 : 2 * (size_t)c.d * B.kcols);
-    B.tt_f = take(f32 ? 0 : 2 * (size_t)c.d_ff * B.kcols);
+    // per-segment tensor maps of the two weight-gradient reductions (2E each)
+    B.maps = take(f32 ? 0 : 4 * kSegMapBytes * (size_t)c.E);
     const int chunk = wr_slice_rows(c.T);
     B.wr_slices = (c.T + chunk - 1) / chunk;
     B.parts = take(sizeof(float) * (size_t)B.wr_slices * c.E * c.d);
@@ -617,6 +461,10 @@ bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) ==
 using namespace moe;
 
 extern "C" {
+
+moe_status moe_check_segment_maps(void* ws, size_t ws_bytes, void* stream) {
+    return check_segment_maps(ws, ws_bytes, reinterpret_cast<cudaStream_t>(stream));
+}
 
 size_t moe_backward_workspace_size(const moe_config* cfg) {
     if (config_status(cfg) != MOE_OK || !backward_supported(*cfg)) return 0;
@@ -675,8 +523,6 @@ moe_status moe_backward(const moe_config* cfg, const void* x, const float* W_r,
     bf16* U = at<bf16>(ws, Bw.u);
     bf16* dYp = at<bf16>(ws, Bw.dyp);
     bf16* dH = at<bf16>(ws, Bw.dh);
-    bf16* W1T = at<bf16>(ws, Bw.w1t);
-    bf16* W2T = at<bf16>(ws, Bw.w2t);
     float* dg = at<float>(ws, Bw.dg);
     const int64_t rows = L.rows;
 
@@ -787,22 +633,14 @@ moe_status moe_backward(const moe_config* cfg, const void* x, const float* W_r,
         return e == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;
     }
     const moe_config cg = dispatch_config(c);  // the GEMMs as the forward pass runs them
-    int32_t* koff = at<int32_t>(ws, Bw.koff);
-    bf16* TTd = at<bf16>(ws, Bw.tt_d);  // segment-transposed [d][kcols] operands
-    bf16* TTf = at<bf16>(ws, Bw.tt_f);  // segment-transposed [d_ff][kcols] operands
-    const int64_t kc = Bw.kcols;
-    const dim3 tgrid_d((unsigned)(kc / TP), (unsigned)((d + TP - 1) / TP));
-    const dim3 tgrid_f((unsigned)(kc / TP), (unsigned)((F + TP - 1) / TP));
-    if (e == cudaSuccess)
-        e = launch_kernel(seg_koff_kernel, dim3(1), dim3(32), 0, s, 1, false,
-                          (const int32_t*)offsets, E, rows, koff);
+    CUtensorMap* maps = at<CUtensorMap>(ws, Bw.maps);
+    const int gF = grid_for(rows * (F / 8), 256);
     if (e == cudaSuccess)
         e = launch_grouped_gemm_tc(cg, true, false, x_perm, rows, offsets, W1, b1, nullptr, U, rows,
                                    F, d, hdr, s);
-    if (e == cudaSuccess)  // H = GELU(U) row-major, and H^T for dW2
-        e = launch_kernel(seg_transpose_kernel<kSegGelu>, tgrid_f, dim3(256), 0, s, 1, false,
-                          (const bf16*)U, H, (const int32_t*)offsets, (const int32_t*)koff, E, F,
-                          rows, kc, TTf);
+    if (e == cudaSuccess)  // H = GELU(U)
+        e = launch_kernel(gelu_rows_kernel<kRowGelu>, dim3(gF), dim3(256), 0, s, 1, false,
+                          (const bf16*)U, H, (const int32_t*)offsets, E, F, rows);
     if (e == cudaSuccess)
         e = launch_grouped_gemm_tc(cg, false, false, H, rows, offsets, W2, b2, perm_w, y_perm, rows,
                                    d, F, hdr, s);
@@ -816,33 +654,18 @@ moe_status moe_backward(const moe_config* cfg, const void* x, const float* W_r,
                           dYp);
     // ---- dW2_e = dY_perm_e^T H_e, db2
     if (e == cudaSuccess)
-        e = launch_kernel(seg_transpose_kernel<kSegCopy>, tgrid_d, dim3(256), 0, s, 1, false,
-                          (const bf16*)dYp, (bf16*)nullptr, (const int32_t*)offsets,
-                          (const int32_t*)koff, E, d, rows, kc, TTd);
-    if (e == cudaSuccess)
-        e = launch_segment_reduction_tc(E, offsets, rows, koff, TTd, d, TTf, F, kc, dW2, hdr, s);
+        e = launch_segment_reduction_tc(E, offsets, rows, dYp, d, H, F, dW2, maps, hdr, s);
     if (e == cudaSuccess)
         e = launch_kernel(colsum_kernel<bf16>, dim3((d + 63) / 64, E), dim3(256), 0, s, 1, false,
                           (const bf16*)dYp, (const int32_t*)offsets, rows, d, db2);
-    // ---- dx path: transposed weights, dH, GELU', dX_perm, dx
+    // ---- dx path: dH = dY_perm W2_e, dU = dH GELU'(U), dX_perm = dU W1_e, dx
     if (e == cudaSuccess)
-        e = launch_kernel(transpose_kernel, dim3((F + TP - 1) / TP, (d + TP - 1) / TP, E),
-                          dim3(256), 0, s, 1, false, reinterpret_cast<const bf16*>(W2), d, F,
-                          (const int32_t*)offsets, rows, W2T);
+        e = launch_grouped_gemm_mn(cg, true, dYp, rows, offsets, W2, dH, rows, F, d, hdr, s);
+    if (e == cudaSuccess)  // dU = dH * GELU'(U) in place
+        e = launch_kernel(gelu_rows_kernel<kRowGeluGrad>, dim3(gF), dim3(256), 0, s, 1, false,
+                          (const bf16*)U, dH, (const int32_t*)offsets, E, F, rows);
     if (e == cudaSuccess)
-        e = launch_kernel(transpose_kernel, dim3((d + TP - 1) / TP, (F + TP - 1) / TP, E),
-                          dim3(256), 0, s, 1, false, reinterpret_cast<const bf16*>(W1), F, d,
-                          (const int32_t*)offsets, rows, W1T);
-    if (e == cudaSuccess)
-        e = launch_grouped_gemm_tc(cg, true, false, dYp, rows, offsets, W2T, nullptr, nullptr, dH,
-                                   rows, F, d, hdr, s);
-    if (e == cudaSuccess)  // dU = dH * GELU'(U) in place, and dU^T for dW1
-        e = launch_kernel(seg_transpose_kernel<kSegGeluGrad>, tgrid_f, dim3(256), 0, s, 1, false,
-                          (const bf16*)U, dH, (const int32_t*)offsets, (const int32_t*)koff, E, F,
-                          rows, kc, TTf);
-    if (e == cudaSuccess)
-        e = launch_grouped_gemm_tc(cg, false, false, dH, rows, offsets, W1T, nullptr, nullptr,
-                                   y_perm, rows, d, F, hdr, s);
+        e = launch_grouped_gemm_mn(cg, false, dH, rows, offsets, W1, y_perm, rows, d, F, hdr, s);
     if (e == cudaSuccess) {
         const long long tasks = (long long)T * ((d / 4 + 127) / 128);
         e = launch_kernel(dx_kernel<bf16>, dim3(grid_for(tasks, 8)), dim3(256), 0, s, 1, false,
@@ -851,11 +674,8 @@ moe_status moe_backward(const moe_config* cfg, const void* x, const float* W_r,
     }
     // ---- dW1_e = dU_e^T X_perm_e, db1
     if (e == cudaSuccess)
-        e = launch_kernel(seg_transpose_kernel<kSegCopy>, tgrid_d, dim3(256), 0, s, 1, false,
-                          (const bf16*)x_perm, (bf16*)nullptr, (const int32_t*)offsets,
-                          (const int32_t*)koff, E, d, rows, kc, TTd);
-    if (e == cudaSuccess)
-        e = launch_segment_reduction_tc(E, offsets, rows, koff, TTf, F, TTd, d, kc, dW1, hdr, s);
+        e = launch_segment_reduction_tc(E, offsets, rows, dH, F, x_perm, d, dW1, maps + 2 * E, hdr,
+                                        s);
     if (e == cudaSuccess)
         e = launch_kernel(colsum_kernel<bf16>, dim3((F + 63) / 64, E), dim3(256), 0, s, 1, false,
                           (const bf16*)dH, (const int32_t*)offsets, rows, F, db1);

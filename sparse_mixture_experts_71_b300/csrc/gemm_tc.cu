@@ -50,6 +50,8 @@
 #include <cuda.h>
 #include <cudaTypedefs.h>
 #include <cuda_runtime.h>
+#include <stdio.h>
+#include <string.h>
 
 #include "moe_device.cuh"
 #include "moe_internal.h"
@@ -94,14 +96,15 @@ struct Params {
     uint64_t timeout_ns;
     int E, n_out, K, rows_cap;
     int act;                    // first GEMM: 1 = GELU, 0 = none (the pre-activation)
-    // Segment-reduction mode (CTA-pair kernel, second-GEMM epilogue; koff not
-    // null): out[e*tok_rows + i][n] = sum over the rows r of expert e's
-    // segment (offsets) of TOK[i][koff[e] + r] * WT[n][koff[e] + r], where
-    // the token operand TOK [tok_rows][*] and the weight operand WT
-    // [n_out][*] hold every segment transposed, starting at column koff[e]
-    // and zero-padded to a multiple of 128 columns.  An empty segment gives
-    // zeros.
-    const int32_t* koff;
+    // Segment-reduction mode (CTA-pair kernel, second-GEMM epilogue;
+    // seg_maps not null): out[e*tok_rows + i][n] = sum over the rows r of
+    // expert e's segment (offsets) of TOK[r][i] * WT[r][n], both operands
+    // row-major over the permuted rows ([rows][tok_rows], [rows][n_out]) and
+    // read MN-major: the K dimension of the MMAs is the segment's rows.
+    // seg_maps[2e] (WT) and seg_maps[2e + 1] (TOK) are tensor maps of that
+    // segment alone (rows past its end read as zero), written on the device
+    // by seg_maps_kernel.  An empty segment gives zeros.
+    const CUtensorMap* seg_maps;
     int tok_rows;
     // CTA-pair kernel: 1 when the operand maps are the 3-D views of
     // make_map3 (one box covers a stage's ATOMS K atoms), 0 for 2-D maps
@@ -111,6 +114,10 @@ struct Params {
     // epilogue warps when it splits K (zero at launch), ksync_cap of them
     int32_t* ksync;
     int ksync_cap;
+    // CTA-pair kernel, not segment reduction: 1 when the weight operand is
+    // W [E][K][n_out] (the transpose of the usual [E][n_out][K]), read
+    // MN-major through a map of 64-column x 128-row boxes over its E*K rows
+    int a_mn;
 };
 
 // Rows of an expert's segment (offsets clamped to the buffers).
@@ -920,7 +927,7 @@ __device__ __forceinline__ Tile decode_pair_tile(int t, const int* s_tiles, cons
         if (s_tiles[mid] * mul <= t) lo = mid; else hi = mid - 1;
     }
     int s0, s1;
-    if (p.koff != nullptr) {  // segment reduction: tok_rows output rows per expert
+    if (p.seg_maps != nullptr) {  // segment reduction: tok_rows output rows per expert
         s0 = lo * p.tok_rows;
         s1 = s0 + p.tok_rows;
     } else {
@@ -930,7 +937,7 @@ __device__ __forceinline__ Tile decode_pair_tile(int t, const int* s_tiles, cons
     const int nt = (s1 - s0 + BN2 - 1) / BN2;
     const int local = t - s_tiles[lo] * mul;
     int gt = nt;  // token tiles per group
-    if (p.koff == nullptr && (long long)nt * BN2 * p.K * 2 > kGroupBytes)
+    if (p.seg_maps == nullptr && (long long)nt * BN2 * p.K * 2 > kGroupBytes)
         gt = max(1, (int)(kGroupBytes / ((long long)BN2 * p.K * 2)));
     const int g = local / (gt * mt2);               // group (all but the last are full)
     const int gsize = min(gt, nt - g * gt);
@@ -994,7 +1001,7 @@ grouped_gemm_pair(const __grid_constant__ CUtensorMap tmA, const __grid_constant
             const int e = e0 + lane;
             int nt = 0;
             if (e < p.E) {
-                const int rows_e = p.koff != nullptr ? p.tok_rows : seg_rows(p, e);
+                const int rows_e = p.seg_maps != nullptr ? p.tok_rows : seg_rows(p, e);
                 nt = ((rows_e + BN2 - 1) / BN2) * mt2;
             }
             int v = nt;
@@ -1021,19 +1028,30 @@ grouped_gemm_pair(const __grid_constant__ CUtensorMap tmA, const __grid_constant
             uint32_t phase = 0;
             long long fills = 0;
             bool ok = true;
+            int last_e = -1;
             for (int t = pair; t < total && ok; t += npairs) {
                 const Tile tl = decode_pair_tile(t, s_tiles, p, mt2);
                 const int m0 = tl.m0;  // pair tile base row
-                const int half_rows = ((tl.n + 31) & ~31) / 2;
+                // segment reduction: both operands MN-major through the
+                // segment's own maps, the whole 256-token MMA N (128 a CTA)
+                const bool red = p.seg_maps != nullptr;
+                const bool amn = red || p.a_mn != 0;
+                const int half_rows = red ? BN2 / 2 : ((tl.n + 31) & ~31) / 2;
                 // the smallest token box that holds this CTA's half_rows rows
                 const int bsel = half_rows <= 16 ? 3 : half_rows <= 32 ? 2 : half_rows <= 64 ? 1 : 0;
-                const CUtensorMap* tb = &tmB.m[bsel];
+                const CUtensorMap* ta = red ? p.seg_maps + 2 * tl.e : &tmA;
+                const CUtensorMap* tb = red ? p.seg_maps + 2 * tl.e + 1 : &tmB.m[bsel];
+                if (red && tl.e != last_e) {  // the maps were written by the previous kernel
+                    tc::tensormap_acquire(ta);
+                    tc::tensormap_acquire(tb);
+                    last_e = tl.e;
+                }
                 const uint32_t bytes = 2 * ATOMS * (A_BYTES + (BN2 / 2 >> bsel) * BK * 2);
                 const int batom = (BN2 / 2 >> bsel) * BK * 2;  // bytes of one token atom
-                const bool red = p.koff != nullptr;
-                const int arow = (red ? 0 : tl.e * p.n_out) + m0 + rank * BM;
+                // K-major weight rows / MN-major weight columns of this CTA
+                const int arow = (amn ? 0 : tl.e * p.n_out) + m0 + rank * BM;
                 const int brow = (red ? tl.r0 - tl.e * p.tok_rows : tl.r0) + rank * half_rows;
-                const int k0 = red ? __ldg(p.koff + tl.e) : 0;
+                const int krow0 = red ? 0 : tl.e * p.K;  // MN-major: the expert's first K row
                 const int KBt = red ? (seg_rows(p, tl.e) + ATOMS * BK - 1) / (ATOMS * BK) : KB;
                 for (int kb = 0; kb < KBt; ++kb) {
                     if (!wait_bar(&empty[stage], phase ^ 1, s_abort, p, 1)) { ok = false; break; }
@@ -1041,16 +1059,29 @@ grouped_gemm_pair(const __grid_constant__ CUtensorMap tmA, const __grid_constant
                     const uint32_t full_l = tc::cluster_addr(&full[stage], 0);
                     uint8_t* sa = smem + stage * C::STAGE_BYTES;
                     uint8_t* sb = sa + ATOMS * A_BYTES;
+                    const int kr = krow0 + kb * ATOMS * BK;  // MN-major: first K row of the stage
                     if (p.box3d) {  // one box per operand: 64 columns x rows x ATOMS atoms
-                        const int kc = k0 / BK + kb * ATOMS;
-                        tc::tma_load_3d_pair(sa, &tmA, full_l, 0, arow, kc);
-                        tc::tma_load_3d_pair(sb, tb, full_l, 0, brow, kc);
+                        const int kc = kb * ATOMS;
+                        if (amn)  // 64 MN columns x 128 K rows x 2 column chunks
+                            tc::tma_load_3d_pair(sa, ta, full_l, 0, kr, arow / BK);
+                        else
+                            tc::tma_load_3d_pair(sa, ta, full_l, 0, arow, kc);
+                        if (red)
+                            tc::tma_load_3d_pair(sb, tb, full_l, 0, kr, brow / BK);
+                        else
+                            tc::tma_load_3d_pair(sb, tb, full_l, 0, brow, kc);
                     } else {
 #pragma unroll
                         for (int at = 0; at < ATOMS; ++at) {
-                            const int kc = k0 + (kb * ATOMS + at) * BK;
-                            tc::tma_load_2d_pair(sa + at * A_BYTES, &tmA, full_l, kc, arow);
-                            tc::tma_load_2d_pair(sb + at * batom, tb, full_l, kc, brow);
+                            const int kc = (kb * ATOMS + at) * BK;
+                            if (amn)
+                                tc::tma_load_2d_pair(sa + at * A_BYTES, ta, full_l, arow + at * BK, kr);
+                            else
+                                tc::tma_load_2d_pair(sa + at * A_BYTES, ta, full_l, kc, arow);
+                            if (red)
+                                tc::tma_load_2d_pair(sb + at * batom, tb, full_l, brow + at * BK, kr);
+                            else
+                                tc::tma_load_2d_pair(sb + at * batom, tb, full_l, kc, brow);
                         }
                     }
                     ++fills;
@@ -1070,17 +1101,18 @@ grouped_gemm_pair(const __grid_constant__ CUtensorMap tmA, const __grid_constant
             bool ok = true;
             for (int t = pair; t < total && ok; t += npairs) {
                 const Tile tl = decode_pair_tile(t, s_tiles, p, mt2);
-                const uint32_t N = (uint32_t)((tl.n + 31) & ~31);
-                const uint32_t idesc = tc::idesc_bf16_f32(2 * BM, N);
+                const bool red = p.seg_maps != nullptr;  // both operands MN-major
+                const bool amn = red || p.a_mn != 0;
+                const uint32_t N = red ? (uint32_t)BN2 : (uint32_t)((tl.n + 31) & ~31);
+                const uint32_t idesc = tc::idesc_bf16_f32(2 * BM, N) | (amn ? tc::kIdescAMn : 0u) |
+                                       (red ? tc::kIdescBMn : 0u);
                 const int half_rows = (int)N / 2;  // the producer's token box for this tile
                 const int bsel = half_rows <= 16 ? 3 : half_rows <= 32 ? 2 : half_rows <= 64 ? 1 : 0;
                 const uint32_t batom = (uint32_t)((BN2 / 2 >> bsel) * BK * 2);
                 if (!wait_bar(&tempty[acc], acc_phase ^ 1, s_abort, p, 2)) break;
                 tc::fence_after_sync();
                 const uint32_t d_tmem = tmem_base + (uint32_t)(acc * BN2);
-                const int KBt = p.koff != nullptr
-                                    ? (seg_rows(p, tl.e) + ATOMS * BK - 1) / (ATOMS * BK)
-                                    : KB;
+                const int KBt = red ? (seg_rows(p, tl.e) + ATOMS * BK - 1) / (ATOMS * BK) : KB;
                 for (int kb = 0; kb < KBt; ++kb) {
                     if (!wait_bar(&full[stage], phase, s_abort, p, 3)) { ok = false; break; }
                     tc::fence_after_sync();
@@ -1091,9 +1123,16 @@ grouped_gemm_pair(const __grid_constant__ CUtensorMap tmA, const __grid_constant
                         const uint32_t sb = s0 + ATOMS * A_BYTES + at * batom;
 #pragma unroll
                         for (int kk = 0; kk < BK / 16; ++kk) {
-                            tc::mma_bf16_pair(d_tmem, tc::sdesc_k128_sw128(sa + kk * 32),
-                                              tc::sdesc_k128_sw128(sb + kk * 32), idesc,
-                                              (kb | at | kk) != 0 ? 1u : 0u);
+                            // MN-major: K step at * 4 + kk is 16 rows of 128 bytes
+                            // into the first box; the second box (the next 64
+                            // MN columns) lies A_BYTES / batom further on
+                            const uint32_t kmn = (uint32_t)(at * (BK / 16) + kk) * 2048u;
+                            const uint64_t ad = amn ? tc::sdesc_mn_sw128(s0 + kmn, A_BYTES)
+                                                    : tc::sdesc_k128_sw128(sa + kk * 32);
+                            const uint64_t bd =
+                                red ? tc::sdesc_mn_sw128(s0 + ATOMS * A_BYTES + kmn, batom)
+                                    : tc::sdesc_k128_sw128(sb + kk * 32);
+                            tc::mma_bf16_pair(d_tmem, ad, bd, idesc, (kb | at | kk) != 0 ? 1u : 0u);
                         }
                     }
                     tc::mma_commit_pair_mc(&empty[stage], 0x3);
@@ -1127,7 +1166,7 @@ grouped_gemm_pair(const __grid_constant__ CUtensorMap tmA, const __grid_constant
             else
                 epilogue_tile<BN2, GEMM1>(p, tl.e, tl.r0, tl.r0, tl.n, m0 + rank * BM, tmem_base,
                                       acc * BN2, q, part, EW / 4, lane, stg, &tmO,
-                                      p.koff != nullptr && seg_rows(p, tl.e) == 0);
+                                      p.seg_maps != nullptr && seg_rows(p, tl.e) == 0);
             tc::fence_before_sync();
             __syncwarp();
             if (lane == 0) tc::mbar_arrive_cluster_relaxed(tc::cluster_addr(&tempty[acc], 0));
@@ -1792,21 +1831,177 @@ cudaError_t launch_grouped_gemm_tc(const moe_config& c, bool bf16_out, bool act,
     return bf16_out ? launch_one<64, 8, true>(mw, ma, p, s) : launch_one<64, 8, false>(mw, ma, p, s);
 }
 
-// Segment reduction on the CTA-pair kernel (see Params::koff): out fp32
-// [E*tok_rows][n_out], TOK [tok_rows][kcols] and WT [n_out][kcols] bf16.
-cudaError_t launch_segment_reduction_tc(int E, const int32_t* offsets, int64_t rows_cap,
-                                        const int32_t* koff, const void* TOK, int tok_rows,
-                                        const void* WT, int n_out, int64_t kcols, float* out,
-                                        DeviceHeader* hdr, cudaStream_t s) {
-    Params p{offsets, nullptr, nullptr, out, hdr, g_tc_timeout_ns, E, n_out, 0, (int)rows_cap, 0,
-             koff, tok_rows};
+// One grouped GEMM out[r][n] = sum_k A[r][k] W[e][k][n] over the expert
+// segments of A with the weight stored K-major-transposed, W [E][K][n_out]
+// (the backward pass's dH = dY_perm W2 and dX_perm = dU W1 read W2 [E][d][d_ff]
+// and W1 [E][d_ff][d] as they are): the CTA-pair kernel with its weight
+// operand read MN-major.  bf16_out: bf16 out (no bias, no GELU); else fp32.
+cudaError_t launch_grouped_gemm_mn(const moe_config& c, bool bf16_out, const void* A,
+                                   int64_t a_rows, const int32_t* offsets, const void* W,
+                                   void* out, int64_t out_rows, int n_out, int K,
+                                   DeviceHeader* hdr, cudaStream_t s) {
+    if (out_rows == 0) return cudaSuccess;
+    Params p{offsets, nullptr, nullptr, out, hdr, g_tc_timeout_ns, c.E, n_out, K, (int)out_rows,
+             0, nullptr, 0};
+    p.a_mn = 1;
     CUtensorMap mw, mo;
-    BMaps mt;
-    if (!make_pair_maps(&mw, WT, (uint64_t)kcols, (uint64_t)n_out, &mt, TOK, (uint64_t)tok_rows,
-                        &p.box3d) ||
+    BMaps ma;
+    const uint64_t w_rows = (uint64_t)c.E * K;
+    // 3-D boxes when both the weight's n_out and the tokens' K allow them
+    bool ok = n_out % BK == 0 && K % BK == 0 &&
+              make_map3(&mw, W, (uint64_t)n_out, w_rows, kPairAtoms * BK, kPairAtoms);
+    for (int i = 0; ok && i < 4; ++i)
+        ok = make_map3(&ma.m[i], A, (uint64_t)K, (uint64_t)a_rows, (uint32_t)(BN2 / 2) >> i,
+                       kPairAtoms);
+    p.box3d = ok ? 1 : 0;
+    if (!ok && !(make_map(&mw, W, (uint64_t)n_out, w_rows, kPairAtoms * BK) &&
+                 make_b_maps(&ma, A, (uint64_t)K, (uint64_t)a_rows)))
+        return cudaErrorInvalidValue;
+    if (bf16_out) {
+        if (!make_store_map_sw32(&mo, out, (uint64_t)n_out, (uint64_t)out_rows))
+            return cudaErrorInvalidValue;
+        return launch_one_pair<3, true, 16, kPairAtoms>(mw, ma, mo, p, s);
+    }
+    if (!make_store_map_f32(&mo, out, (uint64_t)n_out, (uint64_t)out_rows))
+        return cudaErrorInvalidValue;
+    return launch_one_pair<3, false, 8, kPairAtoms>(mw, ma, mo, p, s);
+}
+
+namespace {
+
+// Tensor maps of a row-major bf16 [rows][inner] buffer read MN-major by the
+// segment reduction: boxes of 64 columns x 128 rows (a stage's K), in the
+// 3-D view (two column chunks a box) when inner is a multiple of 64.
+bool make_seg_template(CUtensorMap* m, const void* base, uint64_t inner, uint64_t rows,
+                       bool box3d) {
+    return box3d ? make_map3(m, base, inner, rows, kPairAtoms * BK, kPairAtoms)
+                 : make_map(m, base, inner, rows, kPairAtoms * BK);
+}
+
+// For each expert e, out[2e] (WT) and out[2e + 1] (TOK): copies of the
+// whole-buffer maps whose base is the segment's first row and whose row
+// extent is the segment's length, so that a box reaching past the segment's
+// end reads zeros there instead of the next segment's rows.
+__global__ void __launch_bounds__(128) seg_maps_kernel(
+    const __grid_constant__ CUtensorMap wt, const __grid_constant__ CUtensorMap tok,
+    const int32_t* __restrict__ offsets, int E, int rows_cap, const uint8_t* wt_base,
+    int64_t wt_row_bytes, const uint8_t* tok_base, int64_t tok_row_bytes, CUtensorMap* out) {
+    pdl_wait();
+    const int e = blockIdx.x * blockDim.x + threadIdx.x;
+    if (e < E) {
+        const int s0 = min(max(__ldg(offsets + e), 0), rows_cap);
+        const int s1 = min(max(__ldg(offsets + e + 1), s0), rows_cap);
+        const int n = max(s1 - s0, 1);  // (an empty segment's maps are never read)
+        const CUtensorMap* src[2] = {&wt, &tok};
+        const uint8_t* base[2] = {wt_base + s0 * wt_row_bytes, tok_base + s0 * tok_row_bytes};
+#pragma unroll
+        for (int o = 0; o < 2; ++o) {
+            CUtensorMap* m = out + 2 * e + o;
+            const uint4* from = reinterpret_cast<const uint4*>(src[o]);
+            uint4* to = reinterpret_cast<uint4*>(m);
+#pragma unroll
+            for (int i = 0; i < (int)(sizeof(CUtensorMap) / sizeof(uint4)); ++i) to[i] = from[i];
+            tc::tensormap_set_address(m, base[o]);
+            tc::tensormap_set_dim1(m, n);
+        }
+        tc::tensormap_release();
+    }
+    pdl_trigger();
+}
+
+cudaError_t launch_seg_maps(const CUtensorMap& wt, const CUtensorMap& tok, const int32_t* offsets,
+                            int E, int64_t rows_cap, const void* WT, int n_out, const void* TOK,
+                            int tok_rows, CUtensorMap* maps, cudaStream_t s) {
+    return launch_kernel(seg_maps_kernel, dim3((E + 127) / 128), dim3(128), 0, s, 1, true, wt, tok,
+                         offsets, E, (int)rows_cap, static_cast<const uint8_t*>(WT),
+                         (int64_t)n_out * 2, static_cast<const uint8_t*>(TOK),
+                         (int64_t)tok_rows * 2, maps);
+}
+
+}  // namespace
+
+// Segment reduction on the CTA-pair kernel (see Params::seg_maps): out fp32
+// [E*tok_rows][n_out] = per expert TOK_e^T WT_e over the segment's rows, TOK
+// [rows_cap][tok_rows] and WT [rows_cap][n_out] bf16 row-major over the
+// permuted rows.  maps: 2E tensor maps of workspace (128-byte aligned),
+// written here by seg_maps_kernel and read by the GEMM.
+cudaError_t launch_segment_reduction_tc(int E, const int32_t* offsets, int64_t rows_cap,
+                                        const void* TOK, int tok_rows, const void* WT, int n_out,
+                                        float* out, CUtensorMap* maps, DeviceHeader* hdr,
+                                        cudaStream_t s) {
+    Params p{offsets, nullptr, nullptr, out, hdr, g_tc_timeout_ns, E, n_out, 0, (int)rows_cap, 0,
+             maps, tok_rows};
+    const bool box3d = n_out % BK == 0 && tok_rows % BK == 0;
+    CUtensorMap mw, mt, mo;
+    if (!make_seg_template(&mw, WT, (uint64_t)n_out, (uint64_t)rows_cap, box3d) ||
+        !make_seg_template(&mt, TOK, (uint64_t)tok_rows, (uint64_t)rows_cap, box3d) ||
         !make_store_map_f32(&mo, out, (uint64_t)n_out, (uint64_t)E * tok_rows))
         return cudaErrorInvalidValue;
-    return launch_one_pair<3, false, 8, kPairAtoms>(mw, mt, mo, p, s);
+    p.box3d = box3d ? 1 : 0;
+    cudaError_t err = launch_seg_maps(mw, mt, offsets, E, rows_cap, WT, n_out, TOK, tok_rows,
+                                      maps, s);
+    if (err != cudaSuccess) return err;
+    BMaps mb;  // (the kernel loads through the segment maps in this mode)
+    for (int i = 0; i < 4; ++i) mb.m[i] = mt;
+    return launch_one_pair<3, false, 8, kPairAtoms>(mw, mb, mo, p, s);
+}
+
+// The device-side map edits of launch_segment_reduction_tc checked against
+// the driver's own encoding (moe_check_segment_maps).
+moe_status check_segment_maps(void* ws, size_t ws_bytes, cudaStream_t s) {
+    constexpr int E = 3;
+    constexpr size_t kMaps = 256;
+    if (ws == nullptr || (reinterpret_cast<uintptr_t>(ws) & 255u) != 0) return MOE_ERR_WORKSPACE;
+    if (ws_bytes < kSegMapCheckBytes) return MOE_ERR_WORKSPACE;
+    const int32_t offs[E + 1] = {0, 37, 37, 301};  // a ragged, an empty and a long segment
+    const int64_t rows_cap = 320;
+    uint8_t* base = static_cast<uint8_t*>(ws);
+    int32_t* d_offs = reinterpret_cast<int32_t*>(base);
+    CUtensorMap* d_maps = reinterpret_cast<CUtensorMap*>(base + kMaps);
+    // buffers that are never read (no copy runs): WT [rows][192], TOK [rows][136]
+    const void* WT = base + (1 << 20);
+    const void* TOK = base + (2 << 20);
+    const int n_out = 192, tok_rows = 136;
+    for (int v = 0; v < 2; ++v) {  // the 3-D and the 2-D views
+        const bool box3d = v == 0;
+        const int tr = box3d ? 128 : tok_rows;  // the 3-D view wants multiples of 64
+        CUtensorMap mw, mt;
+        if (!make_seg_template(&mw, WT, n_out, rows_cap, box3d) ||
+            !make_seg_template(&mt, TOK, tr, rows_cap, box3d))
+            return MOE_ERR_CUDA;
+        if (cudaMemcpyAsync(d_offs, offs, sizeof(offs), cudaMemcpyHostToDevice, s) != cudaSuccess ||
+            cudaMemsetAsync(d_maps, 0, 2 * E * sizeof(CUtensorMap), s) != cudaSuccess)
+            return MOE_ERR_CUDA;
+        chain_begin();  // the launch follows a memset: no programmatic overlap
+        if (launch_seg_maps(mw, mt, d_offs, E, rows_cap, WT, n_out, TOK, tr, d_maps, s) !=
+                cudaSuccess)
+            return MOE_ERR_CUDA;
+        CUtensorMap got[2 * E];
+        if (cudaMemcpyAsync(got, d_maps, sizeof(got), cudaMemcpyDeviceToHost, s) != cudaSuccess ||
+            cudaStreamSynchronize(s) != cudaSuccess)
+            return MOE_ERR_CUDA;
+        for (int e = 0; e < E; ++e) {
+            const int n = offs[e + 1] - offs[e] > 0 ? offs[e + 1] - offs[e] : 1;
+            CUtensorMap want[2];
+            if (!make_seg_template(&want[0], static_cast<const uint8_t*>(WT) + offs[e] * n_out * 2,
+                                   n_out, n, box3d) ||
+                !make_seg_template(&want[1], static_cast<const uint8_t*>(TOK) + offs[e] * tr * 2,
+                                   tr, n, box3d))
+                return MOE_ERR_CUDA;
+            for (int o = 0; o < 2; ++o) {
+                if (memcmp(&want[o], &got[2 * e + o], sizeof(CUtensorMap)) == 0) continue;
+                const uint8_t* w = reinterpret_cast<const uint8_t*>(&want[o]);
+                const uint8_t* g = reinterpret_cast<const uint8_t*>(&got[2 * e + o]);
+                fprintf(stderr, "segment map %d.%d (%s view) differs at bytes:", e, o,
+                        box3d ? "3-D" : "2-D");
+                for (int b = 0; b < (int)sizeof(CUtensorMap); ++b)
+                    if (w[b] != g[b]) fprintf(stderr, " %d (%02x, edited %02x)", b, w[b], g[b]);
+                fprintf(stderr, "\n");
+                return MOE_ERR_UNSUPPORTED;
+            }
+        }
+    }
+    return MOE_OK;
 }
 
 }  // namespace moe

@@ -1,6 +1,7 @@
 // Internal declarations shared by the kernels and the C-ABI layer of libmoe.
 #pragma once
 
+#include <cuda.h>
 #include <cuda_runtime.h>
 #include <cuda_bf16.h>
 #include <stdint.h>
@@ -265,6 +266,34 @@ cudaError_t launch_seg_atb_f32(const float* A, const float* B, const int32_t* of
                                int M, int N, int64_t rows_cap, float* C, cudaStream_t s);
 cudaError_t launch_gelu_grad_f32(const float* U, float* dH, const int32_t* offsets, int E, int F,
                                  int64_t rows_cap, cudaStream_t s);
+
+// Backward pass of bf16 layers on the CTA-pair tcgen05 kernel (gemm_tc.cu):
+//   launch_grouped_gemm_tc   out = A W_e^T (+ bias) per segment, W [E][n_out][K]
+//                            (the forward pass's GEMMs);
+//   launch_grouped_gemm_mn   out = A W_e per segment, W [E][K][n_out] read
+//                            MN-major;
+//   launch_segment_reduction_tc  out[e] = TOK_e^T WT_e over each segment's
+//                            rows, both row-major [rows][*] and read MN-major
+//                            through 2E per-segment tensor maps it writes
+//                            into `maps` (workspace, 128-byte aligned).
+// check_segment_maps: those maps' device-side edits against the driver's
+// encoding (moe_check_segment_maps; ws of at least kSegMapCheckBytes).
+cudaError_t launch_grouped_gemm_tc(const moe_config& c, bool bf16_out, bool act, const void* A,
+                                   int64_t a_rows, const int32_t* offsets, const void* W,
+                                   const void* bias, const float* row_w, void* out,
+                                   int64_t out_rows, int n_out, int K, DeviceHeader* hdr,
+                                   cudaStream_t s);
+cudaError_t launch_grouped_gemm_mn(const moe_config& c, bool bf16_out, const void* A,
+                                   int64_t a_rows, const int32_t* offsets, const void* W,
+                                   void* out, int64_t out_rows, int n_out, int K,
+                                   DeviceHeader* hdr, cudaStream_t s);
+constexpr size_t kSegMapBytes = 128;  // one tensor map
+cudaError_t launch_segment_reduction_tc(int E, const int32_t* offsets, int64_t rows_cap,
+                                        const void* TOK, int tok_rows, const void* WT, int n_out,
+                                        float* out, CUtensorMap* maps, DeviceHeader* hdr,
+                                        cudaStream_t s);
+constexpr size_t kSegMapCheckBytes = 3u << 20;
+moe_status check_segment_maps(void* ws, size_t ws_bytes, cudaStream_t s);
 
 // Expert choice (expert_choice.cu): C; the per-expert top-C selection from
 // the router probabilities probs_t [E][T] (offsets, rows, slot_of [T][E]);

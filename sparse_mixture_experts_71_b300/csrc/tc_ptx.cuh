@@ -205,12 +205,57 @@ __device__ __forceinline__ uint64_t sdesc_k128_sw128(uint32_t smem_addr) {
     return d;
 }
 
+// Shared-memory matrix descriptor: MN-major operand tile in the 128-byte
+// swizzle, as a TMA box of 64 MN columns x R K rows lands it: each K row is
+// one 128-byte line of 64 consecutive M (or N) elements, 8-row K groups 1024
+// bytes apart (stride byte offset), and the next 64 MN elements `lbo` bytes
+// further on (leading byte offset: the next box).  A K = 16 step starts 16
+// rows (2048 bytes) further on.  Other fields as sdesc_k128_sw128.
+__device__ __forceinline__ uint64_t sdesc_mn_sw128(uint32_t smem_addr, uint32_t lbo) {
+    uint64_t d = 0;
+    d |= (uint64_t)((smem_addr & 0x3FFFFu) >> 4);
+    d |= (uint64_t)((lbo >> 4) & 0x3FFFu) << 16;
+    d |= (uint64_t)(1024u >> 4) << 32;
+    d |= (uint64_t)1 << 46;
+    d |= (uint64_t)2 << 61;
+    return d;
+}
+
 // Instruction descriptor of tcgen05.mma kind::f16: bf16 A and B (both
 // K-major), fp32 accumulator, shape M x N.  Fields: D format [4,6) = 1 (f32),
 // A format [7,10) = 1 (bf16), B format [10,13) = 1 (bf16), N >> 3 [17,23),
 // M >> 4 [24,29).
 __host__ __device__ __forceinline__ uint32_t idesc_bf16_f32(uint32_t M, uint32_t N) {
     return (1u << 4) | (1u << 7) | (1u << 10) | ((N >> 3) << 17) | ((M >> 4) << 24);
+}
+// Operand-major bits of the instruction descriptor: A MN-major [15], B
+// MN-major [16].
+constexpr uint32_t kIdescAMn = 1u << 15;
+constexpr uint32_t kIdescBMn = 1u << 16;
+
+// Device-side edits of a tensor map held in global memory (128-byte aligned):
+// its base address and the extent of dimension 1 (the rows).  The writer
+// releases the edits to the tensor-map proxy; a thread that then loads
+// through the map acquires them first.
+__device__ __forceinline__ void tensormap_set_address(void* gmap, const void* base) {
+    asm volatile("tensormap.replace.tile.global_address.global.b1024.b64 [%0], %1;" ::"l"(
+                     reinterpret_cast<uint64_t>(gmap)),
+                 "l"(reinterpret_cast<uint64_t>(base))
+                 : "memory");
+}
+__device__ __forceinline__ void tensormap_set_dim1(void* gmap, int32_t extent) {
+    asm volatile("tensormap.replace.tile.global_dim.global.b1024.b32 [%0], 1, %1;" ::"l"(
+                     reinterpret_cast<uint64_t>(gmap)),
+                 "r"(extent)
+                 : "memory");
+}
+__device__ __forceinline__ void tensormap_release() {
+    asm volatile("fence.proxy.tensormap::generic.release.gpu;" ::: "memory");
+}
+__device__ __forceinline__ void tensormap_acquire(const void* gmap) {
+    asm volatile("fence.proxy.tensormap::generic.acquire.gpu [%0], 128;" ::"l"(
+                     reinterpret_cast<uint64_t>(gmap))
+                 : "memory");
 }
 
 // D[tmem] (+)= A[smem] * B[smem]^T, issued by one thread.

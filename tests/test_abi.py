@@ -103,6 +103,10 @@ def test_calls_reject_null_misaligned_and_small_workspace():
     assert lib.moe_check_wait_timeout(None, ctypes.c_uint64(1000), None) == 1
     assert lib.moe_update_balance_bias(cr, None, FAKE, ctypes.c_float(0.1), None) == 1
     assert lib.moe_check_wait_timeout(FAKE + 16, ctypes.c_uint64(1000), None) == 3
+    # the segment-map check: no workspace, a misaligned one, one below 3 MiB
+    assert lib.moe_check_segment_maps(None, 3 << 20, None) == 3
+    assert lib.moe_check_segment_maps(FAKE + 16, 3 << 20, None) == 3
+    assert lib.moe_check_segment_maps(FAKE, (3 << 20) - 1, None) == 3
 
 
 def test_pipeline_workspace_and_host_rejections():

@@ -31,6 +31,10 @@ CASES = [
     ("bwd-decode", 64, 256, 512, 8, 2, None, True, 0.0, 0.0, 0.0),     # single-CTA GEMMs
     ("bwd-e64-tc-router", 1100, 128, 128, 64, 2, 30, True, 1.0, 0.1, 0.1),
     ("bwd-ragged", 1500, 64, 192, 5, 2, 500, True, 1.0, 0.0, 0.0),
+    # d and d_ff not multiples of 64: the 2-D box forms of the MN-major reads
+    ("bwd-2d-boxes", 700, 136, 200, 6, 2, None, True, 0.5, 0.1, 0.0),
+    # rows narrower than one 64-column box
+    ("bwd-tiny-dims", 65, 24, 40, 5, 2, None, True, 0.0, 0.0, 0.0),
     # mid size: ~1024 rows per expert, so the weight-gradient GEMMs' segment
     # reduction walks 8 K tiles of 128 per expert, on both GEMM kernels' wide path
     ("bwd-mid", 4096, 512, 2048, 8, 2, None, True, 0.0, 0.01, 0.001),
@@ -64,6 +68,15 @@ VARIANTS = [
                 overflow="reroute"), 0.1, 0.1),
     (I.Workload("bwd-f32-ec", 256, 128, 192, 8, 2, dtype="f32", routing="expert"), 0.0, 0.2),
 ]
+
+
+def test_segment_maps_match_driver_encoding():
+    """The weight-gradient products read each expert segment through its own
+    tensor map, edited on the device from a whole-buffer map; every edited map
+    must equal the driver's encoding of the same segment (runs before any
+    product loads through one)."""
+    ws = torch.empty(3 << 20, dtype=torch.uint8, device="cuda")
+    B.check_segment_maps(ws)
 
 
 def _close(name, got, want, f32=False):
