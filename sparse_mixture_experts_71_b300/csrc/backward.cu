@@ -13,8 +13,9 @@
 //               z-loss) and dY_perm[slot_j] = w_j dy_t
 //   dx path     dH = dY_perm W2_e and dX_perm = dU W1_e on the CTA-pair
 //               tcgen05 kernel with the weights read MN-major as they are
-//               stored (W2_e [d][d_ff] is dH's [K][N]), dU = dH * GELU'(U);
-//               dx = sum over the token's slots of dX_perm + dg W_r
+//               stored (W2_e [d][d_ff] is dH's [K][N]); dU = dH * GELU'(U)
+//               in the dH product's epilogue; dx = sum over the token's
+//               slots of dX_perm + dg W_r
 //   weights     dW2_e = dY_perm_e^T H_e and dW1_e = dU_e^T X_perm_e on the
 //               same kernel in its segment-reduction mode (K = the segment's
 //               rows; both operands read MN-major from the row-major
@@ -37,28 +38,6 @@ namespace {
 
 
 using bf16 = __nv_bfloat16;
-
-// d/du of the GELU u Phi(u): Phi(u) + u phi(u).  Phi from the erf
-// approximation of Abramowitz & Stegun, formula 7.1.26 (|erf error| <=
-// 1.5e-7, the form the forward GEMM's epilogue uses): with z = |u| / sqrt 2,
-// erf(z) = 1 - q(t) e^{-z^2}, t = 1 / (1 + p z), so Phi(u) = 1 - h for
-// u >= 0 and h for u < 0, h = 0.5 q(t) e^{-u^2/2}; phi(u) = e^{-u^2/2} /
-// sqrt(2 pi) shares the exponential.  e^{-u^2/2} = 2^{-y^2} with
-// y = |u| sqrt(log2(e) / 2), and p z = (p / sqrt(log2 e)) y.
-__device__ __forceinline__ float gelu_grad(float u) {
-    constexpr float c = 0.84932180028801904f;  // sqrt(log2(e) / 2)
-    constexpr float pz = 0.27273748f;          // 0.3275911 / sqrt(log2 e)
-    const float y = fabsf(u) * c;
-    const float t = __fdividef(1.0f, fmaf(y, pz, 1.0f));
-    float q = fmaf(t, 1.061405429f, -1.453152027f);
-    q = fmaf(t, q, 1.421413741f);
-    q = fmaf(t, q, -0.284496736f);
-    q = fmaf(t, q, 0.254829592f);
-    q *= t;
-    const float e = ex2_approx(-y * y);
-    const float h = 0.5f * q * e;
-    return (u >= 0.f ? 1.0f - h : h) + u * e * 0.39894228040143268f;
-}
 
 __device__ __forceinline__ void unpack8(uint4 q, float* f) {
     const __nv_bfloat162* h = reinterpret_cast<const __nv_bfloat162*>(&q);
@@ -350,15 +329,11 @@ __global__ void __launch_bounds__(256) colsum_kernel(const T* __restrict__ A,
     }
 }
 
-// Over the rows of the expert segments (offsets[0] .. offsets[E]) of [rows][F]
-// bf16 matrices, eight columns a thread (F a multiple of 8):
-//   kRowGelu      out = GELU(U), the forward epilogue's GELU (H);
-//   kRowGeluGrad  out *= GELU'(U) (out = dH, overwritten with dU).
-enum RowOp { kRowGelu = 0, kRowGeluGrad = 1 };
-
-template <int OP>
+// H = GELU(U) (the forward epilogue's GELU) over the rows of the expert
+// segments (offsets[0] .. offsets[E]) of [rows][F] bf16 matrices, eight
+// columns a thread (F a multiple of 8).
 __global__ void __launch_bounds__(256) gelu_rows_kernel(const bf16* __restrict__ U,
-                                                         bf16* out,
+                                                         bf16* __restrict__ H,
                                                          const int32_t* __restrict__ offsets,
                                                          int E, int F, int64_t rows_cap) {
     pdl_wait();
@@ -372,20 +347,13 @@ __global__ void __launch_bounds__(256) gelu_rows_kernel(const bf16* __restrict__
         const size_t at_ = base + (size_t)i * 8;
         float f[8];
         load8(U + at_, f);
-        if (OP == kRowGelu) {
 #pragma unroll
-            for (int j = 0; j < 8; j += 2) {
-                const float2 g = gelu2_as7126(make_float2(f[j], f[j + 1]));
-                f[j] = g.x;
-                f[j + 1] = g.y;
-            }
-        } else {
-            float g[8];
-            unpack8(*reinterpret_cast<const uint4*>(out + at_), g);
-#pragma unroll
-            for (int j = 0; j < 8; ++j) f[j] = g[j] * gelu_grad(f[j]);
+        for (int j = 0; j < 8; j += 2) {
+            const float2 g = gelu2_as7126(make_float2(f[j], f[j + 1]));
+            f[j] = g.x;
+            f[j + 1] = g.y;
         }
-        store8(out + at_, f);
+        store8(H + at_, f);
     }
 }
 
@@ -639,7 +607,7 @@ moe_status moe_backward(const moe_config* cfg, const void* x, const float* W_r,
         e = launch_grouped_gemm_tc(cg, true, false, x_perm, rows, offsets, W1, b1, nullptr, U, rows,
                                    F, d, hdr, s);
     if (e == cudaSuccess)  // H = GELU(U)
-        e = launch_kernel(gelu_rows_kernel<kRowGelu>, dim3(gF), dim3(256), 0, s, 1, false,
+        e = launch_kernel(gelu_rows_kernel, dim3(gF), dim3(256), 0, s, 1, false,
                           (const bf16*)U, H, (const int32_t*)offsets, E, F, rows);
     if (e == cudaSuccess)
         e = launch_grouped_gemm_tc(cg, false, false, H, rows, offsets, W2, b2, perm_w, y_perm, rows,
@@ -658,14 +626,12 @@ moe_status moe_backward(const moe_config* cfg, const void* x, const float* W_r,
     if (e == cudaSuccess)
         e = launch_kernel(colsum_kernel<bf16>, dim3((d + 63) / 64, E), dim3(256), 0, s, 1, false,
                           (const bf16*)dYp, (const int32_t*)offsets, rows, d, db2);
-    // ---- dx path: dH = dY_perm W2_e, dU = dH GELU'(U), dX_perm = dU W1_e, dx
+    // ---- dx path: dU = (dY_perm W2_e) GELU'(U) (in dH's buffer), dX_perm = dU W1_e, dx
     if (e == cudaSuccess)
-        e = launch_grouped_gemm_mn(cg, true, dYp, rows, offsets, W2, dH, rows, F, d, hdr, s);
-    if (e == cudaSuccess)  // dU = dH * GELU'(U) in place
-        e = launch_kernel(gelu_rows_kernel<kRowGeluGrad>, dim3(gF), dim3(256), 0, s, 1, false,
-                          (const bf16*)U, dH, (const int32_t*)offsets, E, F, rows);
+        e = launch_grouped_gemm_mn(cg, true, dYp, rows, offsets, W2, U, dH, rows, F, d, hdr, s);
     if (e == cudaSuccess)
-        e = launch_grouped_gemm_mn(cg, false, dH, rows, offsets, W1, y_perm, rows, d, F, hdr, s);
+        e = launch_grouped_gemm_mn(cg, false, dH, rows, offsets, W1, nullptr, y_perm, rows, d, F,
+                                   hdr, s);
     if (e == cudaSuccess) {
         const long long tasks = (long long)T * ((d / 4 + 127) / 128);
         e = launch_kernel(dx_kernel<bf16>, dim3(grid_for(tasks, 8)), dim3(256), 0, s, 1, false,

@@ -118,6 +118,11 @@ struct Params {
     // W [E][K][n_out] (the transpose of the usual [E][n_out][K]), read
     // MN-major through a map of 64-column x 128-row boxes over its E*K rows
     int a_mn;
+    // first-GEMM epilogue (bf16 out, no bias, no GELU): when not null, each
+    // output element o[r][n], once rounded to bf16, is multiplied by
+    // GELU'(gelu_u[r][n]) (the backward pass's dU = dH GELU'(U); gelu_u
+    // [rows][n_out] bf16) and rounded again
+    const __nv_bfloat16* gelu_u;
 };
 
 // Rows of an expert's segment (offsets clamped to the buffers).
@@ -806,6 +811,18 @@ __device__ __forceinline__ void epilogue_gelu(const Params& p, int e, int r0, in
         const float ba = bias != nullptr && fr + g < p.n_out ? __bfloat162float(bias[fr + g]) : 0.f;
         const float bb =
             bias != nullptr && fr + 8 + g < p.n_out ? __bfloat162float(bias[fr + 8 + g]) : 0.f;
+        // GELU' operand (Params::gelu_u): this lane's two 8-column chunks of
+        // the item's U, loaded before the accumulator so the load overlaps it
+        uint4 uq[2] = {make_uint4(0, 0, 0, 0), make_uint4(0, 0, 0, 0)};
+        if (p.gelu_u != nullptr) {
+#pragma unroll
+            for (int j = 0; j < 2; ++j) {
+                const int ci = lane + 32 * j, tok = ci >> 1, fc = fr + 8 * (ci & 1);
+                if (c + tok < n && fc < p.n_out)
+                    uq[j] = __ldg(reinterpret_cast<const uint4*>(
+                        p.gelu_u + (size_t)(r0 + c + tok) * p.n_out + fc));
+            }
+        }
         uint32_t r[16];
         tc::tmem_ld_16x32(tmem_base + ((uint32_t)(q * 32 + h * 16) << 16) + (uint32_t)(acc_col + c), r);
         uint32_t pk[8];  // pk[2b]: rows g, pk[2b+1]: rows g + 8; tokens 8b + 2(lane%4), +1
@@ -828,6 +845,28 @@ __device__ __forceinline__ void epilogue_gelu(const Params& p, int e, int r0, in
         __syncwarp();
         tc::stmatrix_x4_trans(st_addr[0], pk[0], pk[1], pk[2], pk[3]);
         tc::stmatrix_x4_trans(st_addr[1], pk[4], pk[5], pk[6], pk[7]);
+        if (p.gelu_u != nullptr) {
+            // staging holds the item's [32 tokens][16 columns] in bf16; each
+            // lane scales two 8-column chunks by GELU' of the same U chunk
+            __syncwarp();
+#pragma unroll
+            for (int j = 0; j < 2; ++j) {
+                const int ci = lane + 32 * j, tok = ci >> 1, sh = ci & 1;
+                const int fc = fr + 8 * sh;
+                if (c + tok < n && fc < p.n_out) {
+                    uint4* chunk = reinterpret_cast<uint4*>(
+                        stg + tok * 32 + ((sh ^ ((tok >> 2) & 1)) << 4));
+                    uint4 dq = *chunk;
+                    const __nv_bfloat162* uh = reinterpret_cast<const __nv_bfloat162*>(&uq[j]);
+                    __nv_bfloat162* dh = reinterpret_cast<__nv_bfloat162*>(&dq);
+#pragma unroll
+                    for (int i = 0; i < 4; ++i)
+                        dh[i] = __float22bfloat162_rn(__fmul2_rn(
+                            __bfloat1622float2(dh[i]), gelu_grad2(__bfloat1622float2(uh[i]))));
+                    *chunk = dq;
+                }
+            }
+        }
         const int rows_here = min(32, n - c);
         if (rows_here == 32 && fr < p.n_out) {
             tc::fence_proxy_async_smem();
@@ -850,6 +889,21 @@ __device__ __forceinline__ void epilogue_gelu(const Params& p, int e, int r0, in
             }
         }
         __syncwarp();
+    }
+}
+
+// The GELU' operand of a first-GEMM-epilogue tile (Params::gelu_u) fetched
+// into L2 by one epilogue warp ahead of its use: for each of the warp's
+// items (as epilogue_gelu deals them), lane l takes token row l's 32 bytes.
+template <int NPQ>
+__device__ __forceinline__ void prefetch_gelu_u(const Params& p, int r0, int n, int fbase, int q,
+                                                int wq, int lane) {
+    const int items = 2 * ((n + 31) / 32);
+    for (int it = wq; it < items; it += NPQ) {
+        const int c = (it >> 1) * 32, fr = fbase + q * 32 + (it & 1) * 16;
+        if (c + lane < n && fr < p.n_out)
+            asm volatile("prefetch.global.L2 [%0];" ::"l"(
+                p.gelu_u + (size_t)(r0 + c + lane) * p.n_out + fr));
     }
 }
 
@@ -1154,9 +1208,17 @@ grouped_gemm_pair(const __grid_constant__ CUtensorMap tmA, const __grid_constant
         uint8_t* stg = smem + C::OFF_STAGING + ew * 32 * 32 * C::OUT_ES;
         int acc = 0;
         uint32_t acc_phase = 0;
+        if (GEMM1 && p.gelu_u != nullptr && pair < total) {
+            const Tile t0 = decode_pair_tile(pair, s_tiles, p, mt2);
+            prefetch_gelu_u<EW / 4>(p, t0.r0, t0.n, t0.m0 + rank * BM, q, part, lane);
+        }
         for (int t = pair; t < total; t += npairs) {
             const Tile tl = decode_pair_tile(t, s_tiles, p, mt2);
             const int m0 = tl.m0;
+            if (GEMM1 && p.gelu_u != nullptr && t + npairs < total) {  // the next tile's U
+                const Tile tn = decode_pair_tile(t + npairs, s_tiles, p, mt2);
+                prefetch_gelu_u<EW / 4>(p, tn.r0, tn.n, tn.m0 + rank * BM, q, part, lane);
+            }
             const bool ok = wait_bar(&tfull[acc], acc_phase, s_abort, p, 4);
             if (!__all_sync(0xffffffffu, ok)) break;
             tc::fence_after_sync();
@@ -1835,15 +1897,18 @@ cudaError_t launch_grouped_gemm_tc(const moe_config& c, bool bf16_out, bool act,
 // segments of A with the weight stored K-major-transposed, W [E][K][n_out]
 // (the backward pass's dH = dY_perm W2 and dX_perm = dU W1 read W2 [E][d][d_ff]
 // and W1 [E][d_ff][d] as they are): the CTA-pair kernel with its weight
-// operand read MN-major.  bf16_out: bf16 out (no bias, no GELU); else fp32.
+// operand read MN-major.  bf16_out: bf16 out (no bias), times GELU'(gelu_u)
+// when gelu_u is not null (Params::gelu_u); else fp32.
 cudaError_t launch_grouped_gemm_mn(const moe_config& c, bool bf16_out, const void* A,
                                    int64_t a_rows, const int32_t* offsets, const void* W,
-                                   void* out, int64_t out_rows, int n_out, int K,
-                                   DeviceHeader* hdr, cudaStream_t s) {
+                                   const void* gelu_u, void* out, int64_t out_rows, int n_out,
+                                   int K, DeviceHeader* hdr, cudaStream_t s) {
     if (out_rows == 0) return cudaSuccess;
+    if (gelu_u != nullptr && !bf16_out) return cudaErrorInvalidValue;
     Params p{offsets, nullptr, nullptr, out, hdr, g_tc_timeout_ns, c.E, n_out, K, (int)out_rows,
              0, nullptr, 0};
     p.a_mn = 1;
+    p.gelu_u = static_cast<const __nv_bfloat16*>(gelu_u);
     CUtensorMap mw, mo;
     BMaps ma;
     const uint64_t w_rows = (uint64_t)c.E * K;

@@ -89,6 +89,50 @@ __device__ __forceinline__ float2 gelu2_as7126(float2 u) {
     return __ffma2_rn(y, __fmul2_rn(q, e), make_float2(fmaxf(u.x, 0.f), fmaxf(u.y, 0.f)));
 }
 
+// d/du of the GELU u Phi(u): Phi(u) + u phi(u).  Phi from the erf
+// approximation of Abramowitz & Stegun, formula 7.1.26 (|erf error| <=
+// 1.5e-7, the form the forward GEMM's epilogue uses): with z = |u| / sqrt 2,
+// erf(z) = 1 - q(t) e^{-z^2}, t = 1 / (1 + p z), so Phi(u) = 1 - h for
+// u >= 0 and h for u < 0, h = 0.5 q(t) e^{-u^2/2}; phi(u) = e^{-u^2/2} /
+// sqrt(2 pi) shares the exponential.  e^{-u^2/2} = 2^{-y^2} with
+// y = |u| sqrt(log2(e) / 2), and p z = (p / sqrt(log2 e)) y.
+__device__ __forceinline__ float gelu_grad(float u) {
+    constexpr float c = 0.84932180028801904f;  // sqrt(log2(e) / 2)
+    constexpr float pz = 0.27273748f;          // 0.3275911 / sqrt(log2 e)
+    const float y = fabsf(u) * c;
+    const float t = __fdividef(1.0f, fmaf(y, pz, 1.0f));
+    float q = fmaf(t, 1.061405429f, -1.453152027f);
+    q = fmaf(t, q, 1.421413741f);
+    q = fmaf(t, q, -0.284496736f);
+    q = fmaf(t, q, 0.254829592f);
+    q *= t;
+    const float e = ex2_approx(-y * y);
+    const float h = 0.5f * q * e;
+    return (u >= 0.f ? 1.0f - h : h) + u * e * 0.39894228040143268f;
+}
+
+// gelu_grad for two values at once with packed fp32 arithmetic (the same
+// formula; for epilogues where the scalar form's instruction count shows).
+__device__ __forceinline__ float2 gelu_grad2(float2 u) {
+    constexpr float c = 0.84932180028801904f;  // sqrt(log2(e) / 2)
+    constexpr float pz = 0.27273748f;          // 0.3275911 / sqrt(log2 e)
+    const float2 y = make_float2(fabsf(u.x) * c, fabsf(u.y) * c);
+    const float2 den = __ffma2_rn(y, make_float2(pz, pz), make_float2(1.f, 1.f));
+    const float2 t = make_float2(__fdividef(1.0f, den.x), __fdividef(1.0f, den.y));
+    float2 q = __ffma2_rn(t, make_float2(1.061405429f, 1.061405429f),
+                          make_float2(-1.453152027f, -1.453152027f));
+    q = __ffma2_rn(t, q, make_float2(1.421413741f, 1.421413741f));
+    q = __ffma2_rn(t, q, make_float2(-0.284496736f, -0.284496736f));
+    q = __ffma2_rn(t, q, make_float2(0.254829592f, 0.254829592f));
+    q = __fmul2_rn(q, t);
+    const float2 s = __fmul2_rn(y, y);
+    const float2 e = make_float2(ex2_approx(-s.x), ex2_approx(-s.y));
+    const float2 h = __fmul2_rn(__fmul2_rn(make_float2(0.5f, 0.5f), q), e);
+    const float2 phi0 = make_float2(u.x >= 0.f ? 1.0f - h.x : h.x, u.y >= 0.f ? 1.0f - h.y : h.y);
+    return __ffma2_rn(__fmul2_rn(u, e), make_float2(0.39894228040143268f, 0.39894228040143268f),
+                      phi0);
+}
+
 // Inputs of the auxiliary-loss reduction: per-block sums of p written by the
 // router (blk_p, nblk rows of E) and the first-slot / all-slot counts.
 struct LossArgs {
