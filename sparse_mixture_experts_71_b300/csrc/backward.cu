@@ -6,8 +6,9 @@
 // balancing" (the auxiliary loss and the router z-loss it is trained with).
 //
 // Steps (one stream):
-//   recompute   router (logits kept) + dispatch, GEMM1 without GELU -> U,
-//               H = GELU(U), GEMM2 -> y_perm = w * o
+//   recompute   router (logits kept) + dispatch, GEMM1 -> H = GELU(u) and the
+//               pre-activation U (both bf16, from the fp32 accumulator, as the
+//               forward's H), GEMM2 -> y_perm = w * o
 //   router      one warp per token: s_j = <dy_t, y_perm[slot_j]>, the logit
 //               gradient dg (softmax / renormalisation, auxiliary loss,
 //               z-loss) and dY_perm[slot_j] = w_j dy_t
@@ -329,34 +330,6 @@ __global__ void __launch_bounds__(256) colsum_kernel(const T* __restrict__ A,
     }
 }
 
-// H = GELU(U) (the forward epilogue's GELU) over the rows of the expert
-// segments (offsets[0] .. offsets[E]) of [rows][F] bf16 matrices, eight
-// columns a thread (F a multiple of 8).
-__global__ void __launch_bounds__(256) gelu_rows_kernel(const bf16* __restrict__ U,
-                                                         bf16* __restrict__ H,
-                                                         const int32_t* __restrict__ offsets,
-                                                         int E, int F, int64_t rows_cap) {
-    pdl_wait();
-    pdl_trigger();
-    const int64_t r1 = min((int64_t)max(__ldg(offsets + E), 0), rows_cap);
-    const int64_t r0 = min((int64_t)max(__ldg(offsets), 0), r1);
-    const int64_t n8 = (r1 - r0) * (F / 8);
-    const size_t base = (size_t)r0 * F;
-    for (int64_t i = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; i < n8;
-         i += (int64_t)gridDim.x * blockDim.x) {
-        const size_t at_ = base + (size_t)i * 8;
-        float f[8];
-        load8(U + at_, f);
-#pragma unroll
-        for (int j = 0; j < 8; j += 2) {
-            const float2 g = gelu2_as7126(make_float2(f[j], f[j + 1]));
-            f[j] = g.x;
-            f[j + 1] = g.y;
-        }
-        store8(H + at_, f);
-    }
-}
-
 // out[i] = sum over z < S of part[z][i], in z order.
 __global__ void __launch_bounds__(256) sum_parts_kernel(const float* __restrict__ part, int S,
                                                          int64_t n, float* __restrict__ out) {
@@ -602,13 +575,9 @@ moe_status moe_backward(const moe_config* cfg, const void* x, const float* W_r,
     }
     const moe_config cg = dispatch_config(c);  // the GEMMs as the forward pass runs them
     CUtensorMap* maps = at<CUtensorMap>(ws, Bw.maps);
-    const int gF = grid_for(rows * (F / 8), 256);
-    if (e == cudaSuccess)
-        e = launch_grouped_gemm_tc(cg, true, false, x_perm, rows, offsets, W1, b1, nullptr, U, rows,
-                                   F, d, hdr, s);
-    if (e == cudaSuccess)  // H = GELU(U)
-        e = launch_kernel(gelu_rows_kernel, dim3(gF), dim3(256), 0, s, 1, false,
-                          (const bf16*)U, H, (const int32_t*)offsets, E, F, rows);
+    if (e == cudaSuccess)  // H = GELU(x_perm W1^T + b1), and the pre-activation U
+        e = launch_grouped_gemm_tc(cg, true, true, x_perm, rows, offsets, W1, b1, nullptr, H, rows,
+                                   F, d, hdr, s, U);
     if (e == cudaSuccess)
         e = launch_grouped_gemm_tc(cg, false, false, H, rows, offsets, W2, b2, perm_w, y_perm, rows,
                                    d, F, hdr, s);

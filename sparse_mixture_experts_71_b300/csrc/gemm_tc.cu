@@ -118,6 +118,10 @@ struct Params {
     // W [E][K][n_out] (the transpose of the usual [E][n_out][K]), read
     // MN-major through a map of 64-column x 128-row boxes over its E*K rows
     int a_mn;
+    // first-GEMM epilogue: when not null, the pre-activation (acc + bias,
+    // before the GELU) is also written, rounded to bf16, to pre_out
+    // [rows][n_out] (the backward pass's U beside H = GELU)
+    __nv_bfloat16* pre_out;
     // first-GEMM epilogue (bf16 out, no bias, no GELU): when not null, each
     // output element o[r][n], once rounded to bf16, is multiplied by
     // GELU'(gelu_u[r][n]) (the backward pass's dU = dH GELU'(U); gelu_u
@@ -825,24 +829,43 @@ __device__ __forceinline__ void epilogue_gelu(const Params& p, int e, int r0, in
         }
         uint32_t r[16];
         tc::tmem_ld_16x32(tmem_base + ((uint32_t)(q * 32 + h * 16) << 16) + (uint32_t)(acc_col + c), r);
-        uint32_t pk[8];  // pk[2b]: rows g, pk[2b+1]: rows g + 8; tokens 8b + 2(lane%4), +1
+        float2 v[8];  // v[2b]: rows g, v[2b+1]: rows g + 8; tokens 8b + 2(lane%4), +1
 #pragma unroll
         for (int b = 0; b < 4; ++b) {
-            float2 ga = __fadd2_rn(
+            v[2 * b] = __fadd2_rn(
                 make_float2(__uint_as_float(r[4 * b]), __uint_as_float(r[4 * b + 1])), make_float2(ba, ba));
-            float2 gb = __fadd2_rn(
+            v[2 * b + 1] = __fadd2_rn(
                 make_float2(__uint_as_float(r[4 * b + 2]), __uint_as_float(r[4 * b + 3])), make_float2(bb, bb));
-            if (p.act) {
-                ga = gelu2_as7126(ga);
-                gb = gelu2_as7126(gb);
-            }
-            const __nv_bfloat162 pa = __floats2bfloat162_rn(ga.x, ga.y);
-            const __nv_bfloat162 pb = __floats2bfloat162_rn(gb.x, gb.y);
-            pk[2 * b] = *reinterpret_cast<const uint32_t*>(&pa);
-            pk[2 * b + 1] = *reinterpret_cast<const uint32_t*>(&pb);
         }
+        uint32_t pk[8];
         if (lane == 0) tc::bulk_wait_read_all();  // the previous store has read the rows
         __syncwarp();
+        if (p.pre_out != nullptr) {  // the pre-activation through staging to pre_out
+#pragma unroll
+            for (int i = 0; i < 8; ++i) {
+                const __nv_bfloat162 pv = __float22bfloat162_rn(v[i]);
+                pk[i] = *reinterpret_cast<const uint32_t*>(&pv);
+            }
+            tc::stmatrix_x4_trans(st_addr[0], pk[0], pk[1], pk[2], pk[3]);
+            tc::stmatrix_x4_trans(st_addr[1], pk[4], pk[5], pk[6], pk[7]);
+            __syncwarp();
+#pragma unroll
+            for (int j = 0; j < 2; ++j) {
+                const int ci = lane + 32 * j, tok = ci >> 1, sh = ci & 1;
+                const int fc = fr + 8 * sh;
+                if (c + tok < n && fc < p.n_out)
+                    *reinterpret_cast<uint4*>(p.pre_out + (size_t)(r0 + c + tok) * p.n_out + fc) =
+                        *reinterpret_cast<const uint4*>(
+                            stg + tok * 32 + ((sh ^ ((tok >> 2) & 1)) << 4));
+            }
+            __syncwarp();
+        }
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+            const float2 o = p.act ? gelu2_as7126(v[i]) : v[i];
+            const __nv_bfloat162 pv = __float22bfloat162_rn(o);
+            pk[i] = *reinterpret_cast<const uint32_t*>(&pv);
+        }
         tc::stmatrix_x4_trans(st_addr[0], pk[0], pk[1], pk[2], pk[3]);
         tc::stmatrix_x4_trans(st_addr[1], pk[4], pk[5], pk[6], pk[7]);
         if (p.gelu_u != nullptr) {
@@ -1859,18 +1882,22 @@ cudaError_t launch_dense_ffn(const moe_config& c, const void* x, const void* W1,
 
 // One grouped GEMM out[r][n] = sum_k A[r][k] W_e[n][k] (+ bias_e[n]) over the
 // expert segments of A (the forward pass's kernels, for the backward pass):
-// bf16_out: bf16 out, optional GELU (act); else fp32 out times row_w[r]
-// (row_w null: 1).  A: [a_rows][K] bf16, W: [E][n_out][K] bf16, out:
+// bf16_out: bf16 out, optional GELU (act), and with pre_out also the
+// pre-activation (Params::pre_out; CTA-pair kernel); else fp32 out times
+// row_w[r] (row_w null: 1).  A: [a_rows][K] bf16, W: [E][n_out][K] bf16, out:
 // [out_rows][n_out].  `wide` picks the CTA-pair kernel (as the forward does).
 cudaError_t launch_grouped_gemm_tc(const moe_config& c, bool bf16_out, bool act, const void* A,
                                    int64_t a_rows, const int32_t* offsets, const void* W,
                                    const void* bias, const float* row_w, void* out,
                                    int64_t out_rows, int n_out, int K, DeviceHeader* hdr,
-                                   cudaStream_t s) {
+                                   cudaStream_t s, void* pre_out) {
     if (out_rows == 0) return cudaSuccess;
-    const bool wide = (int64_t)c.T * c.k >= 96LL * c.E;
+    if (pre_out != nullptr && !bf16_out) return cudaErrorInvalidValue;
+    // (the pre-activation output is a CTA-pair kernel epilogue mode)
+    const bool wide = (int64_t)c.T * c.k >= 96LL * c.E || pre_out != nullptr;
     Params p{offsets, reinterpret_cast<const __nv_bfloat16*>(bias), bf16_out ? nullptr : row_w,
              out, hdr, g_tc_timeout_ns, c.E, n_out, K, (int)out_rows, act ? 1 : 0, nullptr, 0};
+    p.pre_out = static_cast<__nv_bfloat16*>(pre_out);
     CUtensorMap mw;
     if (wide) {
         BMaps ma;

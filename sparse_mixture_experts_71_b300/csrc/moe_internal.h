@@ -269,7 +269,8 @@ cudaError_t launch_gelu_grad_f32(const float* U, float* dH, const int32_t* offse
 
 // Backward pass of bf16 layers on the CTA-pair tcgen05 kernel (gemm_tc.cu):
 //   launch_grouped_gemm_tc   out = A W_e^T (+ bias) per segment, W [E][n_out][K]
-//                            (the forward pass's GEMMs);
+//                            (the forward pass's GEMMs; optionally the
+//                            pre-activation beside the GELU output too);
 //   launch_grouped_gemm_mn   out = A W_e per segment, W [E][K][n_out] read
 //                            MN-major (bf16 out optionally times GELU'(U));
 //   launch_segment_reduction_tc  out[e] = TOK_e^T WT_e over each segment's
@@ -282,7 +283,7 @@ cudaError_t launch_grouped_gemm_tc(const moe_config& c, bool bf16_out, bool act,
                                    int64_t a_rows, const int32_t* offsets, const void* W,
                                    const void* bias, const float* row_w, void* out,
                                    int64_t out_rows, int n_out, int K, DeviceHeader* hdr,
-                                   cudaStream_t s);
+                                   cudaStream_t s, void* pre_out = nullptr);
 cudaError_t launch_grouped_gemm_mn(const moe_config& c, bool bf16_out, const void* A,
                                    int64_t a_rows, const int32_t* offsets, const void* W,
                                    const void* gelu_u, void* out, int64_t out_rows, int n_out,
