@@ -32,6 +32,7 @@
 #include "../../include/moe_backward.h"
 #include "moe_device.cuh"
 #include "moe_internal.h"
+#include "tc_ptx.cuh"
 
 namespace moe {
 
@@ -296,38 +297,77 @@ __global__ void __launch_bounds__(256) wr_grad_kernel(const float* __restrict__ 
     }
 }
 
-// out[e][m] = sum over the rows of segment e of A[r][m]: a block per (64
-// columns, expert); warp w sums rows w, w + 8, ... (two columns a lane),
-// then the eight partial sums are added in warp order.
+// out[e][m] = sum over the rows of segment e of A[r][m].  A cluster of
+// kColSlices CTAs per (256 columns, expert): CTA z, warp w sums the rows
+// i = 8z + w (mod 64) of the segment, eight columns a lane (16- or 32-byte
+// loads, four rows in flight); each CTA adds its warps' sums in warp order,
+// then CTA 0 adds the CTAs' sums in rank order from their shared memory, so
+// the result does not depend on timing.
+constexpr int kColSlices = 8;
+
 template <typename T>
 __global__ void __launch_bounds__(256) colsum_kernel(const T* __restrict__ A,
                                                       const int32_t* __restrict__ offsets,
                                                       int64_t rows_cap, int M,
                                                       float* __restrict__ out) {
-    __shared__ float part[8][64];
+    __shared__ float part[8][256];
+    __shared__ float blk[256];
     pdl_wait();
     pdl_trigger();
-    const int e = blockIdx.y, warp = threadIdx.x / 32, lane = threadIdx.x % 32;
-    const int m = blockIdx.x * 64 + 2 * lane;
+    const int z = (int)tc::cluster_ctarank(), e = blockIdx.z;
+    const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
+    const int m = blockIdx.y * 256 + 8 * lane;
     const int r1 = (int)min((int64_t)max(__ldg(offsets + e + 1), 0), rows_cap);
     const int r0 = min(max(__ldg(offsets + e), 0), r1);
-    float a = 0.f, b = 0.f;
-    if (m < M)  // M is even (a multiple of 8)
-        for (int r = r0 + warp; r < r1; r += 8) {
-            const float2 v = load2(A + (size_t)r * M + m);
-            a += v.x;
-            b += v.y;
+    const int n = r1 - r0;
+    float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+    if (m < M) {  // M is a multiple of 8: a lane's eight columns are all in or all out
+        const T* col = A + (size_t)r0 * M + m;
+        int i = z * 8 + warp;
+        for (; i + 192 < n; i += 256) {  // four rows 64 apart in flight
+            float v[4][8];
+#pragma unroll
+            for (int u = 0; u < 4; ++u) load8(col + (size_t)(i + 64 * u) * M, v[u]);
+#pragma unroll
+            for (int u = 0; u < 4; ++u)
+#pragma unroll
+                for (int j = 0; j < 8; ++j) acc[j] += v[u][j];
         }
-    part[warp][2 * lane] = a;
-    part[warp][2 * lane + 1] = b;
+        for (; i < n; i += 64) {
+            float v[8];
+            load8(col + (size_t)i * M, v);
+#pragma unroll
+            for (int j = 0; j < 8; ++j) acc[j] += v[j];
+        }
+    }
+#pragma unroll
+    for (int j = 0; j < 8; ++j) part[warp][8 * lane + j] = acc[j];
     __syncthreads();
-    const int c = threadIdx.x;
-    if (c < 64 && blockIdx.x * 64 + c < M) {
+    {
+        const int t = threadIdx.x;
         float v = 0.f;
 #pragma unroll
-        for (int w = 0; w < 8; ++w) v += part[w][c];
-        out[(size_t)e * M + blockIdx.x * 64 + c] = v;
+        for (int w = 0; w < 8; ++w) v += part[w][t];
+        blk[t] = v;
     }
+    tc::cluster_sync();  // every CTA's sums are in its shared memory
+    if (z == 0) {
+        const int t = threadIdx.x, mc = blockIdx.y * 256 + t;
+        float v = 0.f;
+#pragma unroll
+        for (int r = 0; r < kColSlices; ++r) v += tc::ld_shared_cluster_f32(tc::cluster_addr(&blk[t], r));
+        if (mc < M) out[(size_t)e * M + mc] = v;
+    }
+    tc::cluster_sync();  // no CTA leaves while CTA 0 reads its shared memory
+}
+
+// colsum_kernel's launch: grid (kColSlices, 256-column chunks, E), clusters
+// of kColSlices along x.
+template <typename T>
+cudaError_t launch_colsum(const T* A, const int32_t* offsets, int64_t rows_cap, int E, int M,
+                          float* out, cudaStream_t s) {
+    return launch_kernel(colsum_kernel<T>, dim3(kColSlices, (M + 255) / 256, E), dim3(256), 0, s,
+                         kColSlices, false, A, offsets, rows_cap, M, out);
 }
 
 // out[i] = sum over z < S of part[z][i], in z order.
@@ -543,16 +583,14 @@ moe_status moe_backward(const moe_config* cfg, const void* x, const float* W_r,
                               z_grad, dg, dYf);
         if (e == cudaSuccess) e = launch_seg_atb_f32(dYf, Hf, offsets, E, d, F, rows, dW2, s);
         if (e == cudaSuccess)
-            e = launch_kernel(colsum_kernel<float>, dim3((d + 63) / 64, E), dim3(256), 0, s, 1,
-                              false, (const float*)dYf, (const int32_t*)offsets, rows, d, db2);
+            e = launch_colsum((const float*)dYf, (const int32_t*)offsets, rows, E, d, db2, s);
         if (e == cudaSuccess)  // dH = dY W2_e (W2_e: [d][d_ff] = [K][N])
             e = launch_seg_gemm_f32(true, 0, dYf, offsets, E, W2f, nullptr, nullptr, dHf, nullptr,
                                     F, d, max_seg, rows, s);
         if (e == cudaSuccess) e = launch_gelu_grad_f32(Uf, dHf, offsets, E, F, rows, s);
         if (e == cudaSuccess) e = launch_seg_atb_f32(dHf, xp, offsets, E, F, d, rows, dW1, s);
         if (e == cudaSuccess)
-            e = launch_kernel(colsum_kernel<float>, dim3((F + 63) / 64, E), dim3(256), 0, s, 1,
-                              false, (const float*)dHf, (const int32_t*)offsets, rows, F, db1);
+            e = launch_colsum((const float*)dHf, (const int32_t*)offsets, rows, E, F, db1, s);
         if (e == cudaSuccess)  // dX_perm = dU W1_e (W1_e: [d_ff][d] = [K][N]), over y_perm
             e = launch_seg_gemm_f32(true, 0, dHf, offsets, E, W1f, nullptr, nullptr, y_perm,
                                     nullptr, d, F, max_seg, rows, s);
@@ -593,8 +631,7 @@ moe_status moe_backward(const moe_config* cfg, const void* x, const float* W_r,
     if (e == cudaSuccess)
         e = launch_segment_reduction_tc(E, offsets, rows, dYp, d, H, F, dW2, maps, hdr, s);
     if (e == cudaSuccess)
-        e = launch_kernel(colsum_kernel<bf16>, dim3((d + 63) / 64, E), dim3(256), 0, s, 1, false,
-                          (const bf16*)dYp, (const int32_t*)offsets, rows, d, db2);
+        e = launch_colsum((const bf16*)dYp, (const int32_t*)offsets, rows, E, d, db2, s);
     // ---- dx path: dU = (dY_perm W2_e) GELU'(U) (in dH's buffer), dX_perm = dU W1_e, dx
     if (e == cudaSuccess)
         e = launch_grouped_gemm_mn(cg, true, dYp, rows, offsets, W2, U, dH, rows, F, d, hdr, s);
@@ -612,8 +649,7 @@ moe_status moe_backward(const moe_config* cfg, const void* x, const float* W_r,
         e = launch_segment_reduction_tc(E, offsets, rows, dH, F, x_perm, d, dW1, maps + 2 * E, hdr,
                                         s);
     if (e == cudaSuccess)
-        e = launch_kernel(colsum_kernel<bf16>, dim3((F + 63) / 64, E), dim3(256), 0, s, 1, false,
-                          (const bf16*)dH, (const int32_t*)offsets, rows, F, db1);
+        e = launch_colsum((const bf16*)dH, (const int32_t*)offsets, rows, E, F, db1, s);
     // ---- dW_r = dg^T x: row-slice partials, then their sum
     if (e == cudaSuccess)
         e = launch_kernel(El <= 8 ? wr_grad_kernel<8, bf16> : wr_grad_kernel<32, bf16>,
