@@ -795,12 +795,12 @@ dense_ffn_kernel(const __grid_constant__ CUtensorMap tmA1, const __grid_constant
 template <int NPQ>
 __device__ __forceinline__ void epilogue_gelu(const Params& p, int e, int r0, int n, int fbase,
                                               uint32_t tmem_base, int acc_col, int q, int wq,
-                                              int lane, uint8_t* stg, const CUtensorMap* tm_out) {
+                                              int lane, uint8_t* stg_w, const CUtensorMap* tm_out) {
     const int g = lane >> 2;
     const int items = 2 * ((n + 31) / 32);
     const __nv_bfloat16* bias = p.bias != nullptr ? p.bias + (size_t)e * p.n_out : nullptr;
     __nv_bfloat16* out = reinterpret_cast<__nv_bfloat16*>(p.out);
-    const uint32_t stg_s = tc::smem_u32(stg);
+    const uint32_t stg_s = tc::smem_u32(stg_w);
     // this lane's stmatrix row address (matrix lane/8, row lane%8) for the two stores
     const int mi = lane >> 3, rr = lane & 7;
     uint32_t st_addr[2];
@@ -809,9 +809,16 @@ __device__ __forceinline__ void epilogue_gelu(const Params& p, int e, int r0, in
         const int b = 2 * k + (mi >> 1), sh = mi & 1, tok = 8 * b + rr;
         st_addr[k] = stg_s + tok * 32 + ((sh ^ ((tok >> 2) & 1)) << 4);
     }
-    for (int it = wq; it < items; it += NPQ) {
+    // the warp's 2 KB of staging holds two items: item i stages in half i % 2
+    // while the store of item i - 1 may still be reading the other half (the
+    // previous tile's stores, in either half, have read theirs first)
+    if (lane == 0) tc::bulk_wait_read_all();
+    __syncwarp();
+    for (int it = wq, nth = 0; it < items; it += NPQ, ++nth) {
         const int h = it & 1, c = (it >> 1) * 32;
         const int fr = fbase + q * 32 + h * 16;  // first weight row of the item
+        const uint32_t half = (uint32_t)(nth & 1) * 1024u;
+        uint8_t* stg = stg_w + half;
         const float ba = bias != nullptr && fr + g < p.n_out ? __bfloat162float(bias[fr + g]) : 0.f;
         const float bb =
             bias != nullptr && fr + 8 + g < p.n_out ? __bfloat162float(bias[fr + 8 + g]) : 0.f;
@@ -838,7 +845,7 @@ __device__ __forceinline__ void epilogue_gelu(const Params& p, int e, int r0, in
                 make_float2(__uint_as_float(r[4 * b + 2]), __uint_as_float(r[4 * b + 3])), make_float2(bb, bb));
         }
         uint32_t pk[8];
-        if (lane == 0) tc::bulk_wait_read_all();  // the previous store has read the rows
+        if (lane == 0) tc::bulk_wait_read_1();  // the store before last has read this half
         __syncwarp();
         if (p.pre_out != nullptr) {  // the pre-activation through staging to pre_out
 #pragma unroll
@@ -846,8 +853,8 @@ __device__ __forceinline__ void epilogue_gelu(const Params& p, int e, int r0, in
                 const __nv_bfloat162 pv = __float22bfloat162_rn(v[i]);
                 pk[i] = *reinterpret_cast<const uint32_t*>(&pv);
             }
-            tc::stmatrix_x4_trans(st_addr[0], pk[0], pk[1], pk[2], pk[3]);
-            tc::stmatrix_x4_trans(st_addr[1], pk[4], pk[5], pk[6], pk[7]);
+            tc::stmatrix_x4_trans(st_addr[0] + half, pk[0], pk[1], pk[2], pk[3]);
+            tc::stmatrix_x4_trans(st_addr[1] + half, pk[4], pk[5], pk[6], pk[7]);
             __syncwarp();
 #pragma unroll
             for (int j = 0; j < 2; ++j) {
@@ -866,8 +873,8 @@ __device__ __forceinline__ void epilogue_gelu(const Params& p, int e, int r0, in
             const __nv_bfloat162 pv = __float22bfloat162_rn(o);
             pk[i] = *reinterpret_cast<const uint32_t*>(&pv);
         }
-        tc::stmatrix_x4_trans(st_addr[0], pk[0], pk[1], pk[2], pk[3]);
-        tc::stmatrix_x4_trans(st_addr[1], pk[4], pk[5], pk[6], pk[7]);
+        tc::stmatrix_x4_trans(st_addr[0] + half, pk[0], pk[1], pk[2], pk[3]);
+        tc::stmatrix_x4_trans(st_addr[1] + half, pk[4], pk[5], pk[6], pk[7]);
         if (p.gelu_u != nullptr) {
             // staging holds the item's [32 tokens][16 columns] in bf16; each
             // lane scales two 8-column chunks by GELU' of the same U chunk
