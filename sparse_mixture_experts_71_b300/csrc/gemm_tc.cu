@@ -809,15 +809,20 @@ __device__ __forceinline__ void epilogue_gelu(const Params& p, int e, int r0, in
         const int b = 2 * k + (mi >> 1), sh = mi & 1, tok = 8 * b + rr;
         st_addr[k] = stg_s + tok * 32 + ((sh ^ ((tok >> 2) & 1)) << 4);
     }
-    // the warp's 2 KB of staging holds two items: item i stages in half i % 2
+    // With the backward pass's extra epilogue work (gelu_u, pre_out) the
+    // warp's 2 KB of staging holds two items: item i stages in half i % 2
     // while the store of item i - 1 may still be reading the other half (the
-    // previous tile's stores, in either half, have read theirs first)
-    if (lane == 0) tc::bulk_wait_read_all();
-    __syncwarp();
+    // previous tile's stores, in either half, have read theirs first).  The
+    // forward pass's plain GELU epilogue keeps one half (measured faster).
+    const bool dbl = p.gelu_u != nullptr || p.pre_out != nullptr;
+    if (dbl) {
+        if (lane == 0) tc::bulk_wait_read_all();
+        __syncwarp();
+    }
     for (int it = wq, nth = 0; it < items; it += NPQ, ++nth) {
         const int h = it & 1, c = (it >> 1) * 32;
         const int fr = fbase + q * 32 + h * 16;  // first weight row of the item
-        const uint32_t half = (uint32_t)(nth & 1) * 1024u;
+        const uint32_t half = dbl ? (uint32_t)(nth & 1) * 1024u : 0u;
         uint8_t* stg = stg_w + half;
         const float ba = bias != nullptr && fr + g < p.n_out ? __bfloat162float(bias[fr + g]) : 0.f;
         const float bb =
@@ -845,7 +850,10 @@ __device__ __forceinline__ void epilogue_gelu(const Params& p, int e, int r0, in
                 make_float2(__uint_as_float(r[4 * b + 2]), __uint_as_float(r[4 * b + 3])), make_float2(bb, bb));
         }
         uint32_t pk[8];
-        if (lane == 0) tc::bulk_wait_read_1();  // the store before last has read this half
+        if (lane == 0) {  // the store that last used this half has read it
+            if (dbl) tc::bulk_wait_read_1();
+            else tc::bulk_wait_read_all();
+        }
         __syncwarp();
         if (p.pre_out != nullptr) {  // the pre-activation through staging to pre_out
 #pragma unroll
