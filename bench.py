@@ -776,9 +776,12 @@ def bench_backward(args, wl):
         torch.cuda.synchronize(dev)
     total_ms = slowest_rank_ms(sum(e0.elapsed_time(e1) for e0, e1 in ev), world, dev)
     ms = total_ms / args.steps
-    # 2 forward GEMMs recomputed + dH, dX and the two weight-gradient GEMMs;
-    # the router's logits, dx and dW_r products over the routed experts
-    flops = 12.0 * kept * d * F + 3 * 2.0 * T * d * (E - wl.n_shared)
+    # the GEMMs the call runs: the first forward GEMM recomputed (bf16 layers
+    # take the slot scores from the dH product's epilogue; fp32 layers also
+    # recompute the second), dH, dX and the two weight-gradient GEMMs; the
+    # router's logits, dx and dW_r products over the routed experts
+    gemms = 5 if wl.dtype == "bf16" else 6
+    flops = gemms * 2.0 * kept * d * F + 3 * 2.0 * T * d * (E - wl.n_shared)
     pk, pk_kind = peaks()
     clocks = sampler.summary()
     achieved = flops / (ms * 1e-3) / 1e12

@@ -5,17 +5,20 @@
 // "The MoE layer" (the layer being trained) and "The central problem: load
 // balancing" (the auxiliary loss and the router z-loss it is trained with).
 //
-// Steps (one stream):
+// Steps (one stream), bf16 layers:
 //   recompute   router (logits kept) + dispatch, GEMM1 -> H = GELU(u) and the
 //               pre-activation U (both bf16, from the fp32 accumulator, as the
-//               forward's H), GEMM2 -> y_perm = w * o
-//   router      one warp per token: s_j = <dy_t, y_perm[slot_j]>, the logit
-//               gradient dg (softmax / renormalisation, auxiliary loss,
-//               z-loss) and dY_perm[slot_j] = w_j dy_t
-//   dx path     dH = dY_perm W2_e and dX_perm = dU W1_e on the CTA-pair
-//               tcgen05 kernel with the weights read MN-major as they are
-//               stored (W2_e [d][d_ff] is dH's [K][N]); dU = dH * GELU'(U)
-//               in the dH product's epilogue; dx = sum over the token's
+//               forward's H)
+//   dY_perm     the scaled upstream rows w_j dy_t of every kept slot
+//   dH          dH = dY_perm W2_e on the CTA-pair tcgen05 kernel with W2 read
+//               MN-major as stored (W2_e [d][d_ff] is dH's [K][N]); its
+//               epilogue writes dU = dH * GELU'(U) and, per 16 columns, the
+//               row's dot with GELU(U): the slot score s_j = <dy_t, w_j o_j> =
+//               <dH_j, h_j> + w_j <dy_t, b2_e> then needs no second-GEMM
+//               recompute
+//   router      one warp per token: the slot scores, the logit gradient dg
+//               (softmax / renormalisation, auxiliary loss, z-loss)
+//   dx path     dX_perm = dU W1_e (W1 MN-major); dx = sum over the token's
 //               slots of dX_perm + dg W_r
 //   weights     dW2_e = dY_perm_e^T H_e and dW1_e = dU_e^T X_perm_e on the
 //               same kernel in its segment-reduction mode (K = the segment's
@@ -25,6 +28,8 @@
 //               cores (row-slice partials summed in a fixed order), db2, db1
 //               = column sums over each expert's rows.  GELU and GELU' use
 //               the forward epilogue's Abramowitz & Stegun 7.1.26 erf.
+// fp32 layers run the same steps on CUDA-core kernels (backward_f32.cu),
+// with the second GEMM recomputed for the slot scores.
 
 #include <cuda_runtime.h>
 #include <cuda_bf16.h>
@@ -102,12 +107,29 @@ enum GradMode {
 // choices at stride ld; the first kr of the K slots are routed (shared
 // experts follow).  The row dg[t] first collects the slot scores by final
 // expert (lane 0, slot order), then each lane finishes its columns.
+// Where the slot scores come from: y_perm rows (w o in fp32; the kernel also
+// writes the dY_perm rows), or, when spart is set, the dH product's partial
+// dots (Params::spart of the GEMM kernels): with dH = W2_e^T (w_j dy_t),
+//   s_j = <dy_t, w_j (W2_e h + b2_e)> = <dH_j, h_j> + w_j <dy_t, b2_e>,
+// the first term the sum of the nparts partials of the slot's row (lane
+// by lane, then across the warp in a fixed order), e the slot's expert (its
+// segment in offsets); dY_perm is then already written.
+template <typename T>
+struct ScoreSrc {
+    const float* y_perm;     // [rows][d] or null
+    const float* spart;      // [rows_cap][nparts] or null
+    int nparts;
+    const T* b2;             // [E][d]
+    const int32_t* offsets;  // [E + 1]
+    int E;
+};
+
 template <typename T>
 __global__ void __launch_bounds__(256) router_grad_kernel(
     const float* __restrict__ logits, const int32_t* __restrict__ choice,
     const float* __restrict__ choice_w, int ld, int kc, const int32_t* __restrict__ slot_of,
     const float* __restrict__ perm_w, const int32_t* __restrict__ kept_rank,
-    const int32_t* __restrict__ alt, int mode, const float* __restrict__ y_perm,
+    const int32_t* __restrict__ alt, int mode, const ScoreSrc<T> src,
     const T* __restrict__ dy, const int32_t* __restrict__ top1, int Tn, int El, int K, int kr,
     int d, int64_t rows_cap, int renormalize, float aux_grad, float z_grad,
     float* __restrict__ dg, T* __restrict__ dY_perm) {
@@ -126,18 +148,38 @@ __global__ void __launch_bounds__(256) router_grad_kernel(
             const int slot = __ldg(slot_of + (size_t)t * K + j);
             if (slot < 0 || slot >= rows_cap) continue;  // dropped: s = 0
             const float w = __ldg(perm_w + slot);
-            const float4* yr = reinterpret_cast<const float4*>(y_perm + (size_t)slot * d);
-            T* dyp = dY_perm + (size_t)slot * d;
             float dot = 0.f;
-            for (int v = lane; v < nv; v += 32) {
-                float f[8];
-                load8(dyr + 8 * v, f);
-                const float4 a = __ldg(yr + 2 * v), b = __ldg(yr + 2 * v + 1);
-                dot += f[0] * a.x + f[1] * a.y + f[2] * a.z + f[3] * a.w + f[4] * b.x +
-                       f[5] * b.y + f[6] * b.z + f[7] * b.w;
+            if (src.spart == nullptr) {
+                const float4* yr = reinterpret_cast<const float4*>(src.y_perm + (size_t)slot * d);
+                T* dyp = dY_perm + (size_t)slot * d;
+                for (int v = lane; v < nv; v += 32) {
+                    float f[8];
+                    load8(dyr + 8 * v, f);
+                    const float4 a = __ldg(yr + 2 * v), b = __ldg(yr + 2 * v + 1);
+                    dot += f[0] * a.x + f[1] * a.y + f[2] * a.z + f[3] * a.w + f[4] * b.x +
+                           f[5] * b.y + f[6] * b.z + f[7] * b.w;
 #pragma unroll
-                for (int q = 0; q < 8; ++q) f[q] *= w;
-                store8(dyp + 8 * v, f);
+                    for (int q = 0; q < 8; ++q) f[q] *= w;
+                    store8(dyp + 8 * v, f);
+                }
+            } else {
+                if (j >= kr) continue;  // a shared expert: no logit, nothing to score
+                int lo = 0, hi = src.E - 1;
+                while (lo < hi) {  // the slot's expert: last segment starting at or before it
+                    const int mid = (lo + hi + 1) >> 1;
+                    if (__ldg(src.offsets + mid) <= slot) lo = mid; else hi = mid - 1;
+                }
+                const T* b2e = src.b2 + (size_t)lo * d;
+                for (int v = lane; v < nv; v += 32) {
+                    float f[8], b[8];
+                    load8(dyr + 8 * v, f);
+                    load8(b2e + 8 * v, b);
+#pragma unroll
+                    for (int q = 0; q < 8; ++q) dot = fmaf(f[q], b[q], dot);
+                }
+                dot *= w;
+                const float* sp = src.spart + (size_t)slot * src.nparts;
+                for (int g = lane; g < src.nparts; g += 32) dot += __ldg(sp + g);
             }
 #pragma unroll
             for (int o = 16; o > 0; o >>= 1) dot += __shfl_xor_sync(0xffffffffu, dot, o);
@@ -188,6 +230,37 @@ __global__ void __launch_bounds__(256) router_grad_kernel(
             }
             v += z_grad * 2.0f / (float)Tn * lse * pe;
             dgt[e] = v;
+        }
+    }
+}
+
+// dY_perm[slot] = w_slot dy_t for every kept slot of every token; a warp per
+// token (the rows the dH product reads before the slot scores exist).
+template <typename T>
+__global__ void __launch_bounds__(256) scaled_rows_kernel(const int32_t* __restrict__ slot_of,
+                                                           const float* __restrict__ perm_w,
+                                                           const T* __restrict__ dy, int Tn,
+                                                           int K, int d, int64_t rows_cap,
+                                                           T* __restrict__ dY_perm) {
+    pdl_wait();
+    pdl_trigger();
+    const int lane = threadIdx.x % 32;
+    const int nwarps = gridDim.x * (blockDim.x / 32);
+    const int nv = d / 8;
+    for (int t = blockIdx.x * (blockDim.x / 32) + threadIdx.x / 32; t < Tn; t += nwarps) {
+        const T* dyr = dy + (size_t)t * d;
+        for (int j = 0; j < K; ++j) {
+            const int slot = __ldg(slot_of + (size_t)t * K + j);
+            if (slot < 0 || slot >= rows_cap) continue;
+            const float w = __ldg(perm_w + slot);
+            T* dyp = dY_perm + (size_t)slot * d;
+            for (int v = lane; v < nv; v += 32) {
+                float f[8];
+                load8(dyr + 8 * v, f);
+#pragma unroll
+                for (int q = 0; q < 8; ++q) f[q] *= w;
+                store8(dyp + 8 * v, f);
+            }
         }
     }
 }
@@ -392,7 +465,8 @@ int grid_for(int64_t work, int per_block) {
 
 // Backward workspace: the forward layout, then these regions.
 struct BwdLayout {
-    size_t logits, u, dyp, dh, dg, maps, parts, total;
+    size_t logits, u, dyp, dh, dg, maps, spart, parts, total;
+    int nparts;        // 16-column partial dots per row (bf16 layers)
     int wr_slices;     // row slices of the router-weight gradient
 };
 
@@ -423,6 +497,9 @@ BwdLayout bwd_layout(const moe_config& c, const WsLayout& L) {
     B.dg = take(sizeof(float) * (size_t)c.T * c.E);
     // per-segment tensor maps of the two weight-gradient reductions (2E each)
     B.maps = take(f32 ? 0 : 4 * kSegMapBytes * (size_t)c.E);
+    // the dH product's partial dots per 16 columns (the slot scores)
+    B.nparts = (c.d_ff + 15) / 16;
+    B.spart = take(f32 ? 0 : sizeof(float) * (size_t)B.nparts * rows);
     const int chunk = wr_slice_rows(c.T);
     B.wr_slices = (c.T + chunk - 1) / chunk;
     B.parts = take(sizeof(float) * (size_t)B.wr_slices * c.E * c.d);
@@ -578,9 +655,10 @@ moe_status moe_backward(const moe_config* cfg, const void* x, const float* W_r,
             e = launch_kernel(router_grad_kernel<float>, dim3(grid_for(T, 8)), dim3(256), 0, s, 1,
                               false, (const float*)logits, choice, choice_w, ld, ec ? 0 : k,
                               (const int32_t*)slot_of, (const float*)perm_w, kept_rank, alt,
-                              grad_mode, (const float*)y_perm, reinterpret_cast<const float*>(dy),
-                              top1, T, El, K, kr, d, rows, ec ? 0 : c.renormalize, aux_grad,
-                              z_grad, dg, dYf);
+                              grad_mode,
+                              ScoreSrc<float>{(const float*)y_perm, nullptr, 0, nullptr, nullptr, E},
+                              reinterpret_cast<const float*>(dy), top1, T, El, K, kr, d, rows,
+                              ec ? 0 : c.renormalize, aux_grad, z_grad, dg, dYf);
         if (e == cudaSuccess) e = launch_seg_atb_f32(dYf, Hf, offsets, E, d, F, rows, dW2, s);
         if (e == cudaSuccess)
             e = launch_colsum((const float*)dYf, (const int32_t*)offsets, rows, E, d, db2, s);
@@ -613,31 +691,39 @@ moe_status moe_backward(const moe_config* cfg, const void* x, const float* W_r,
     }
     const moe_config cg = dispatch_config(c);  // the GEMMs as the forward pass runs them
     CUtensorMap* maps = at<CUtensorMap>(ws, Bw.maps);
+    float* spart = at<float>(ws, Bw.spart);
     if (e == cudaSuccess)  // H = GELU(x_perm W1^T + b1), and the pre-activation U
         e = launch_grouped_gemm_tc(cg, true, true, x_perm, rows, offsets, W1, b1, nullptr, H, rows,
                                    F, d, hdr, s, U);
+    // ---- the scaled upstream rows dY_perm = w dy_t
     if (e == cudaSuccess)
-        e = launch_grouped_gemm_tc(cg, false, false, H, rows, offsets, W2, b2, perm_w, y_perm, rows,
-                                   d, F, hdr, s);
-    // ---- router gradient and the scaled upstream rows
+        e = launch_kernel(scaled_rows_kernel<bf16>, dim3(grid_for(T, 8)), dim3(256), 0, s, 1,
+                          false, (const int32_t*)slot_of, (const float*)perm_w,
+                          reinterpret_cast<const bf16*>(dy), T, K, d, rows, dYp);
+    // ---- dU = (dY_perm W2_e) GELU'(U) (in dH's buffer), with the rows' partial
+    // dots <dH, GELU(U)> that make the slot scores (no second-GEMM recompute)
+    if (e == cudaSuccess)
+        e = launch_grouped_gemm_mn(cg, true, dYp, rows, offsets, W2, U, spart, dH, rows, F, d, hdr,
+                                   s);
+    // ---- router gradient
     if (e == cudaSuccess)
         e = launch_kernel(router_grad_kernel<bf16>, dim3(grid_for(T, 8)), dim3(256), 0, s, 1, false,
                           (const float*)logits, choice, choice_w, ld, ec ? 0 : k,
                           (const int32_t*)slot_of, (const float*)perm_w, kept_rank, alt,
-                          grad_mode, (const float*)y_perm, reinterpret_cast<const bf16*>(dy), top1,
-                          T, El, K, kr, d, rows, ec ? 0 : c.renormalize, aux_grad, z_grad, dg,
-                          dYp);
+                          grad_mode,
+                          ScoreSrc<bf16>{nullptr, spart, Bw.nparts,
+                                         reinterpret_cast<const bf16*>(b2), offsets, E},
+                          reinterpret_cast<const bf16*>(dy), top1, T, El, K, kr, d, rows,
+                          ec ? 0 : c.renormalize, aux_grad, z_grad, dg, (bf16*)nullptr);
     // ---- dW2_e = dY_perm_e^T H_e, db2
     if (e == cudaSuccess)
         e = launch_segment_reduction_tc(E, offsets, rows, dYp, d, H, F, dW2, maps, hdr, s);
     if (e == cudaSuccess)
         e = launch_colsum((const bf16*)dYp, (const int32_t*)offsets, rows, E, d, db2, s);
-    // ---- dx path: dU = (dY_perm W2_e) GELU'(U) (in dH's buffer), dX_perm = dU W1_e, dx
+    // ---- dX_perm = dU W1_e (over y_perm), dx
     if (e == cudaSuccess)
-        e = launch_grouped_gemm_mn(cg, true, dYp, rows, offsets, W2, U, dH, rows, F, d, hdr, s);
-    if (e == cudaSuccess)
-        e = launch_grouped_gemm_mn(cg, false, dH, rows, offsets, W1, nullptr, y_perm, rows, d, F,
-                                   hdr, s);
+        e = launch_grouped_gemm_mn(cg, false, dH, rows, offsets, W1, nullptr, nullptr, y_perm, rows,
+                                   d, F, hdr, s);
     if (e == cudaSuccess) {
         const long long tasks = (long long)T * ((d / 4 + 127) / 128);
         e = launch_kernel(dx_kernel<bf16>, dim3(grid_for(tasks, 8)), dim3(256), 0, s, 1, false,

@@ -127,6 +127,12 @@ struct Params {
     // GELU'(gelu_u[r][n]) (the backward pass's dU = dH GELU'(U); gelu_u
     // [rows][n_out] bf16) and rounded again
     const __nv_bfloat16* gelu_u;
+    // with gelu_u: when not null, also the dots of each output row with
+    // GELU(gelu_u) over every 16 columns, before the GELU' scaling:
+    // spart[r][n / 16] = sum over the 16 columns n of o[r][n] GELU(u[r][n])
+    // (o rounded to bf16; ceil(n_out / 16) a row; the backward pass's slot
+    // scores)
+    float* spart;
 };
 
 // Rows of an expert's segment (offsets clamped to the buffers).
@@ -891,6 +897,7 @@ __device__ __forceinline__ void epilogue_gelu(const Params& p, int e, int r0, in
             for (int j = 0; j < 2; ++j) {
                 const int ci = lane + 32 * j, tok = ci >> 1, sh = ci & 1;
                 const int fc = fr + 8 * sh;
+                float part = 0.f;  // this chunk's dot with GELU(u) (Params::spart)
                 if (c + tok < n && fc < p.n_out) {
                     uint4* chunk = reinterpret_cast<uint4*>(
                         stg + tok * 32 + ((sh ^ ((tok >> 2) & 1)) << 4));
@@ -898,10 +905,25 @@ __device__ __forceinline__ void epilogue_gelu(const Params& p, int e, int r0, in
                     const __nv_bfloat162* uh = reinterpret_cast<const __nv_bfloat162*>(&uq[j]);
                     __nv_bfloat162* dh = reinterpret_cast<__nv_bfloat162*>(&dq);
 #pragma unroll
-                    for (int i = 0; i < 4; ++i)
-                        dh[i] = __float22bfloat162_rn(__fmul2_rn(
-                            __bfloat1622float2(dh[i]), gelu_grad2(__bfloat1622float2(uh[i]))));
+                    for (int i = 0; i < 4; ++i) {
+                        const float2 uf = __bfloat1622float2(uh[i]);
+                        const float2 df = __bfloat1622float2(dh[i]);
+                        float2 gr;
+                        if (p.spart != nullptr) {
+                            float2 hg;
+                            gr = gelu_and_grad2(uf, &hg);
+                            part = fmaf(df.x, hg.x, fmaf(df.y, hg.y, part));
+                        } else {
+                            gr = gelu_grad2(uf);
+                        }
+                        dh[i] = __float22bfloat162_rn(__fmul2_rn(df, gr));
+                    }
                     *chunk = dq;
+                }
+                if (p.spart != nullptr) {  // the token's two chunks: lanes 2t, 2t + 1
+                    part += __shfl_xor_sync(0xffffffffu, part, 1);
+                    if (sh == 0 && c + tok < n && fr < p.n_out)
+                        p.spart[(size_t)(r0 + c + tok) * ((p.n_out + 15) >> 4) + (fr >> 4)] = part;
                 }
             }
         }
@@ -1940,17 +1962,20 @@ cudaError_t launch_grouped_gemm_tc(const moe_config& c, bool bf16_out, bool act,
 // (the backward pass's dH = dY_perm W2 and dX_perm = dU W1 read W2 [E][d][d_ff]
 // and W1 [E][d_ff][d] as they are): the CTA-pair kernel with its weight
 // operand read MN-major.  bf16_out: bf16 out (no bias), times GELU'(gelu_u)
-// when gelu_u is not null (Params::gelu_u); else fp32.
+// when gelu_u is not null (Params::gelu_u), with the partial dots spart
+// ([out_rows][ceil(n_out / 16)]) when that is not null; else fp32.
 cudaError_t launch_grouped_gemm_mn(const moe_config& c, bool bf16_out, const void* A,
                                    int64_t a_rows, const int32_t* offsets, const void* W,
-                                   const void* gelu_u, void* out, int64_t out_rows, int n_out,
-                                   int K, DeviceHeader* hdr, cudaStream_t s) {
+                                   const void* gelu_u, float* spart, void* out, int64_t out_rows,
+                                   int n_out, int K, DeviceHeader* hdr, cudaStream_t s) {
     if (out_rows == 0) return cudaSuccess;
-    if (gelu_u != nullptr && !bf16_out) return cudaErrorInvalidValue;
+    if ((gelu_u != nullptr && !bf16_out) || (spart != nullptr && gelu_u == nullptr))
+        return cudaErrorInvalidValue;
     Params p{offsets, nullptr, nullptr, out, hdr, g_tc_timeout_ns, c.E, n_out, K, (int)out_rows,
              0, nullptr, 0};
     p.a_mn = 1;
     p.gelu_u = static_cast<const __nv_bfloat16*>(gelu_u);
+    p.spart = spart;
     CUtensorMap mw, mo;
     BMaps ma;
     const uint64_t w_rows = (uint64_t)c.E * K;

@@ -133,6 +133,32 @@ __device__ __forceinline__ float2 gelu_grad2(float2 u) {
                       phi0);
 }
 
+// gelu_grad2 and the GELU itself from the same intermediate terms: with
+// h = 0.5 q(t) e^{-u^2/2} as in gelu_grad, GELU(u) = u Phi(u) = max(u, 0) -
+// |u| h.  Returns GELU'(u); *g receives GELU(u).
+__device__ __forceinline__ float2 gelu_and_grad2(float2 u, float2* g) {
+    constexpr float c = 0.84932180028801904f;  // sqrt(log2(e) / 2)
+    constexpr float pz = 0.27273748f;          // 0.3275911 / sqrt(log2 e)
+    const float2 au = make_float2(fabsf(u.x), fabsf(u.y));
+    const float2 y = make_float2(au.x * c, au.y * c);
+    const float2 den = __ffma2_rn(y, make_float2(pz, pz), make_float2(1.f, 1.f));
+    const float2 t = make_float2(__fdividef(1.0f, den.x), __fdividef(1.0f, den.y));
+    float2 q = __ffma2_rn(t, make_float2(1.061405429f, 1.061405429f),
+                          make_float2(-1.453152027f, -1.453152027f));
+    q = __ffma2_rn(t, q, make_float2(1.421413741f, 1.421413741f));
+    q = __ffma2_rn(t, q, make_float2(-0.284496736f, -0.284496736f));
+    q = __ffma2_rn(t, q, make_float2(0.254829592f, 0.254829592f));
+    q = __fmul2_rn(q, t);
+    const float2 s = __fmul2_rn(y, y);
+    const float2 e = make_float2(ex2_approx(-s.x), ex2_approx(-s.y));
+    const float2 h = __fmul2_rn(__fmul2_rn(make_float2(0.5f, 0.5f), q), e);
+    *g = __ffma2_rn(make_float2(-au.x, -au.y), h,
+                    make_float2(fmaxf(u.x, 0.f), fmaxf(u.y, 0.f)));
+    const float2 phi0 = make_float2(u.x >= 0.f ? 1.0f - h.x : h.x, u.y >= 0.f ? 1.0f - h.y : h.y);
+    return __ffma2_rn(__fmul2_rn(u, e), make_float2(0.39894228040143268f, 0.39894228040143268f),
+                      phi0);
+}
+
 // Inputs of the auxiliary-loss reduction: per-block sums of p written by the
 // router (blk_p, nblk rows of E) and the first-slot / all-slot counts.
 struct LossArgs {

@@ -272,7 +272,8 @@ cudaError_t launch_gelu_grad_f32(const float* U, float* dH, const int32_t* offse
 //                            (the forward pass's GEMMs; optionally the
 //                            pre-activation beside the GELU output too);
 //   launch_grouped_gemm_mn   out = A W_e per segment, W [E][K][n_out] read
-//                            MN-major (bf16 out optionally times GELU'(U));
+//                            MN-major (bf16 out optionally times GELU'(U),
+//                            with the rows' partial dots with GELU(U));
 //   launch_segment_reduction_tc  out[e] = TOK_e^T WT_e over each segment's
 //                            rows, both row-major [rows][*] and read MN-major
 //                            through 2E per-segment tensor maps it writes
@@ -286,8 +287,8 @@ cudaError_t launch_grouped_gemm_tc(const moe_config& c, bool bf16_out, bool act,
                                    cudaStream_t s, void* pre_out = nullptr);
 cudaError_t launch_grouped_gemm_mn(const moe_config& c, bool bf16_out, const void* A,
                                    int64_t a_rows, const int32_t* offsets, const void* W,
-                                   const void* gelu_u, void* out, int64_t out_rows, int n_out,
-                                   int K, DeviceHeader* hdr, cudaStream_t s);
+                                   const void* gelu_u, float* spart, void* out, int64_t out_rows,
+                                   int n_out, int K, DeviceHeader* hdr, cudaStream_t s);
 constexpr size_t kSegMapBytes = 128;  // one tensor map
 cudaError_t launch_segment_reduction_tc(int E, const int32_t* offsets, int64_t rows_cap,
                                         const void* TOK, int tok_rows, const void* WT, int n_out,
