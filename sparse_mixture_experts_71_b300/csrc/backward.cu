@@ -357,6 +357,7 @@ __global__ void __launch_bounds__(256) wr_grad_kernel(const float* __restrict__ 
             __syncthreads();
             if (j < d) {
                 const int rows = min(WR_CHUNK, t1 - tb);
+#pragma unroll 4
                 for (int r = 0; r < rows; ++r) {
                     const float xv = to_f32(x[(size_t)(tb + r) * d + j]);
 #pragma unroll
@@ -451,7 +452,8 @@ __global__ void __launch_bounds__(256) sum_parts_kernel(const float* __restrict_
     for (int64_t i = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; i < n;
          i += (int64_t)gridDim.x * blockDim.x) {
         float v = 0.f;
-        for (int z = 0; z < S; ++z) v += __ldg(part + (size_t)z * n + i);
+#pragma unroll 8
+        for (int z = 0; z < S; ++z) v += __ldg(part + (size_t)z * n + i);  // loads ahead, adds in z order
         out[i] = v;
     }
 }

@@ -798,8 +798,84 @@ dense_ffn_kernel(const __grid_constant__ CUtensorMap tmA1, const __grid_constant
 // Compared with 32 scalar shared stores and a read-back per 32 x 32 chunk this
 // halves the epilogue's shared-memory traffic, which competes with the MMA
 // operand reads and the TMA fills.
+// The first-GEMM epilogue of the forward pass: bias (+ GELU), bf16, each
+// item (16 weight rows x 32 tokens) through the warp's staging and out by a
+// TMA tensor store (lane stores for a partial item).
 template <int NPQ>
 __device__ __forceinline__ void epilogue_gelu(const Params& p, int e, int r0, int n, int fbase,
+                                              uint32_t tmem_base, int acc_col, int q, int wq,
+                                              int lane, uint8_t* stg, const CUtensorMap* tm_out) {
+    const int g = lane >> 2;
+    const int items = 2 * ((n + 31) / 32);
+    const __nv_bfloat16* bias = p.bias != nullptr ? p.bias + (size_t)e * p.n_out : nullptr;
+    __nv_bfloat16* out = reinterpret_cast<__nv_bfloat16*>(p.out);
+    const uint32_t stg_s = tc::smem_u32(stg);
+    // this lane's stmatrix row address (matrix lane/8, row lane%8) for the two stores
+    const int mi = lane >> 3, rr = lane & 7;
+    uint32_t st_addr[2];
+#pragma unroll
+    for (int k = 0; k < 2; ++k) {
+        const int b = 2 * k + (mi >> 1), sh = mi & 1, tok = 8 * b + rr;
+        st_addr[k] = stg_s + tok * 32 + ((sh ^ ((tok >> 2) & 1)) << 4);
+    }
+    for (int it = wq; it < items; it += NPQ) {
+        const int h = it & 1, c = (it >> 1) * 32;
+        const int fr = fbase + q * 32 + h * 16;  // first weight row of the item
+        const float ba = bias != nullptr && fr + g < p.n_out ? __bfloat162float(bias[fr + g]) : 0.f;
+        const float bb =
+            bias != nullptr && fr + 8 + g < p.n_out ? __bfloat162float(bias[fr + 8 + g]) : 0.f;
+        uint32_t r[16];
+        tc::tmem_ld_16x32(tmem_base + ((uint32_t)(q * 32 + h * 16) << 16) + (uint32_t)(acc_col + c), r);
+        uint32_t pk[8];  // pk[2b]: rows g, pk[2b+1]: rows g + 8; tokens 8b + 2(lane%4), +1
+#pragma unroll
+        for (int b = 0; b < 4; ++b) {
+            float2 ga = __fadd2_rn(
+                make_float2(__uint_as_float(r[4 * b]), __uint_as_float(r[4 * b + 1])), make_float2(ba, ba));
+            float2 gb = __fadd2_rn(
+                make_float2(__uint_as_float(r[4 * b + 2]), __uint_as_float(r[4 * b + 3])), make_float2(bb, bb));
+            if (p.act) {
+                ga = gelu2_as7126(ga);
+                gb = gelu2_as7126(gb);
+            }
+            const __nv_bfloat162 pa = __floats2bfloat162_rn(ga.x, ga.y);
+            const __nv_bfloat162 pb = __floats2bfloat162_rn(gb.x, gb.y);
+            pk[2 * b] = *reinterpret_cast<const uint32_t*>(&pa);
+            pk[2 * b + 1] = *reinterpret_cast<const uint32_t*>(&pb);
+        }
+        if (lane == 0) tc::bulk_wait_read_all();  // the previous store has read the rows
+        __syncwarp();
+        tc::stmatrix_x4_trans(st_addr[0], pk[0], pk[1], pk[2], pk[3]);
+        tc::stmatrix_x4_trans(st_addr[1], pk[4], pk[5], pk[6], pk[7]);
+        const int rows_here = min(32, n - c);
+        if (rows_here == 32 && fr < p.n_out) {
+            tc::fence_proxy_async_smem();
+            __syncwarp();
+            if (lane == 0) {
+                tc::tma_store_2d(tm_out, stg, fr, r0 + c);
+                tc::bulk_commit();
+            }
+            continue;
+        }
+        __syncwarp();
+#pragma unroll
+        for (int j = 0; j < 2; ++j) {
+            const int ci = lane + 32 * j, tok = ci >> 1, sh = ci & 1;
+            const int fc = fr + 8 * sh;
+            if (c + tok < n && fc < p.n_out) {
+                const uint4 val = *reinterpret_cast<const uint4*>(
+                    stg + tok * 32 + ((sh ^ ((tok >> 2) & 1)) << 4));
+                *reinterpret_cast<uint4*>(out + (size_t)(r0 + c + tok) * p.n_out + fc) = val;
+            }
+        }
+        __syncwarp();
+    }
+}
+
+// The first-GEMM epilogue with the backward pass's extra work (Params
+// gelu_u, spart, pre_out): the forward epilogue's steps plus the
+// pre-activation output, the GELU' scaling and the partial dots.
+template <int NPQ>
+__device__ __forceinline__ void epilogue_gelu_bwd(const Params& p, int e, int r0, int n, int fbase,
                                               uint32_t tmem_base, int acc_col, int q, int wq,
                                               int lane, uint8_t* stg_w, const CUtensorMap* tm_out) {
     const int g = lane >> 2;
@@ -1065,11 +1141,19 @@ __device__ __forceinline__ Tile decode_pair_tile(int t, const int* s_tiles, cons
     return tl;
 }
 
-template <int STAGES, bool GEMM1, int EW, int ATOMS>
+// OPS, the operand forms and epilogue work (fixed at compile time, so the
+// forward pass's kernels carry none of the backward pass's cases):
+//   0  both operands K-major, the forward epilogues;
+//   1  both K-major, the backward first-GEMM epilogue (Params::pre_out);
+//   2  the weight operand MN-major (Params::a_mn), the backward first-GEMM
+//      epilogue (Params::gelu_u, spart) or the second-GEMM one;
+//   3  segment reduction, both operands MN-major (Params::seg_maps).
+template <int STAGES, bool GEMM1, int EW, int ATOMS, int OPS>
 __global__ void __launch_bounds__(Cfg2<STAGES, GEMM1, EW, ATOMS>::THREADS, 1)
 grouped_gemm_pair(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ BMaps tmB,
                   const __grid_constant__ CUtensorMap tmO, const Params p) {
     using C = Cfg2<STAGES, GEMM1, EW, ATOMS>;
+    constexpr bool kRed = OPS == 3, kAmn = OPS >= 2, kBwdEpi = OPS == 1 || OPS == 2;
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -1148,8 +1232,7 @@ grouped_gemm_pair(const __grid_constant__ CUtensorMap tmA, const __grid_constant
                 const int m0 = tl.m0;  // pair tile base row
                 // segment reduction: both operands MN-major through the
                 // segment's own maps, the whole 256-token MMA N (128 a CTA)
-                const bool red = p.seg_maps != nullptr;
-                const bool amn = red || p.a_mn != 0;
+                constexpr bool red = kRed, amn = kAmn;
                 const int half_rows = red ? BN2 / 2 : ((tl.n + 31) & ~31) / 2;
                 // the smallest token box that holds this CTA's half_rows rows
                 const int bsel = half_rows <= 16 ? 3 : half_rows <= 32 ? 2 : half_rows <= 64 ? 1 : 0;
@@ -1215,8 +1298,7 @@ grouped_gemm_pair(const __grid_constant__ CUtensorMap tmA, const __grid_constant
             bool ok = true;
             for (int t = pair; t < total && ok; t += npairs) {
                 const Tile tl = decode_pair_tile(t, s_tiles, p, mt2);
-                const bool red = p.seg_maps != nullptr;  // both operands MN-major
-                const bool amn = red || p.a_mn != 0;
+                constexpr bool red = kRed, amn = kAmn;  // red: both operands MN-major
                 const uint32_t N = red ? (uint32_t)BN2 : (uint32_t)((tl.n + 31) & ~31);
                 const uint32_t idesc = tc::idesc_bf16_f32(2 * BM, N) | (amn ? tc::kIdescAMn : 0u) |
                                        (red ? tc::kIdescBMn : 0u);
@@ -1268,21 +1350,24 @@ grouped_gemm_pair(const __grid_constant__ CUtensorMap tmA, const __grid_constant
         uint8_t* stg = smem + C::OFF_STAGING + ew * 32 * 32 * C::OUT_ES;
         int acc = 0;
         uint32_t acc_phase = 0;
-        if (GEMM1 && p.gelu_u != nullptr && pair < total) {
+        if (GEMM1 && kBwdEpi && p.gelu_u != nullptr && pair < total) {
             const Tile t0 = decode_pair_tile(pair, s_tiles, p, mt2);
             prefetch_gelu_u<EW / 4>(p, t0.r0, t0.n, t0.m0 + rank * BM, q, part, lane);
         }
         for (int t = pair; t < total; t += npairs) {
             const Tile tl = decode_pair_tile(t, s_tiles, p, mt2);
             const int m0 = tl.m0;
-            if (GEMM1 && p.gelu_u != nullptr && t + npairs < total) {  // the next tile's U
+            if (GEMM1 && kBwdEpi && p.gelu_u != nullptr && t + npairs < total) {  // next tile's U
                 const Tile tn = decode_pair_tile(t + npairs, s_tiles, p, mt2);
                 prefetch_gelu_u<EW / 4>(p, tn.r0, tn.n, tn.m0 + rank * BM, q, part, lane);
             }
             const bool ok = wait_bar(&tfull[acc], acc_phase, s_abort, p, 4);
             if (!__all_sync(0xffffffffu, ok)) break;
             tc::fence_after_sync();
-            if constexpr (GEMM1)
+            if constexpr (GEMM1 && kBwdEpi)
+                epilogue_gelu_bwd<EW / 4>(p, tl.e, tl.r0, tl.n, m0 + rank * BM, tmem_base,
+                                          acc * BN2, q, part, lane, stg, &tmO);
+            else if constexpr (GEMM1)
                 epilogue_gelu<EW / 4>(p, tl.e, tl.r0, tl.n, m0 + rank * BM, tmem_base, acc * BN2,
                                       q, part, lane, stg, &tmO);
             else
@@ -1801,11 +1886,11 @@ cudaError_t launch_one(const CUtensorMap& a, const CUtensorMap& b, const Params&
     return launch_kernel(kern, dim3(num_sms()), dim3(kThreads), C::SMEM, s, 1, true, a, b, p);
 }
 
-template <int STAGES, bool GEMM1, int EW, int ATOMS>
+template <int STAGES, bool GEMM1, int EW, int ATOMS, int OPS = 0>
 cudaError_t launch_one_pair(const CUtensorMap& a, const BMaps& b, const CUtensorMap& o,
                             const Params& p, cudaStream_t s) {
     using C = Cfg2<STAGES, GEMM1, EW, ATOMS>;
-    constexpr auto kern = grouped_gemm_pair<STAGES, GEMM1, EW, ATOMS>;
+    constexpr auto kern = grouped_gemm_pair<STAGES, GEMM1, EW, ATOMS, OPS>;
     cudaError_t err = ensure_smem<kern>(C::SMEM);
     if (err != cudaSuccess) return err;
     return launch_kernel(kern, dim3(2 * resident_clusters<kern>(2, C::SMEM, C::THREADS)),
@@ -1945,7 +2030,9 @@ cudaError_t launch_grouped_gemm_tc(const moe_config& c, bool bf16_out, bool act,
         if (bf16_out) {
             if (!make_store_map_sw32(&mo, out, (uint64_t)n_out, (uint64_t)out_rows))
                 return cudaErrorInvalidValue;
-            return launch_one_pair<3, true, 16, kPairAtoms>(mw, ma, mo, p, s);
+            return pre_out != nullptr
+                       ? launch_one_pair<3, true, 16, kPairAtoms, 1>(mw, ma, mo, p, s)
+                       : launch_one_pair<3, true, 16, kPairAtoms>(mw, ma, mo, p, s);
         }
         if (!make_store_map_f32(&mo, out, (uint64_t)n_out, (uint64_t)out_rows))
             return cudaErrorInvalidValue;
@@ -1992,11 +2079,11 @@ cudaError_t launch_grouped_gemm_mn(const moe_config& c, bool bf16_out, const voi
     if (bf16_out) {
         if (!make_store_map_sw32(&mo, out, (uint64_t)n_out, (uint64_t)out_rows))
             return cudaErrorInvalidValue;
-        return launch_one_pair<3, true, 16, kPairAtoms>(mw, ma, mo, p, s);
+        return launch_one_pair<3, true, 16, kPairAtoms, 2>(mw, ma, mo, p, s);
     }
     if (!make_store_map_f32(&mo, out, (uint64_t)n_out, (uint64_t)out_rows))
         return cudaErrorInvalidValue;
-    return launch_one_pair<3, false, 8, kPairAtoms>(mw, ma, mo, p, s);
+    return launch_one_pair<3, false, 8, kPairAtoms, 2>(mw, ma, mo, p, s);
 }
 
 namespace {
@@ -2075,7 +2162,7 @@ cudaError_t launch_segment_reduction_tc(int E, const int32_t* offsets, int64_t r
     if (err != cudaSuccess) return err;
     BMaps mb;  // (the kernel loads through the segment maps in this mode)
     for (int i = 0; i < 4; ++i) mb.m[i] = mt;
-    return launch_one_pair<3, false, 8, kPairAtoms>(mw, mb, mo, p, s);
+    return launch_one_pair<3, false, 8, kPairAtoms, 3>(mw, mb, mo, p, s);
 }
 
 // The device-side map edits of launch_segment_reduction_tc checked against
