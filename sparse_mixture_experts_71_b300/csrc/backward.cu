@@ -490,7 +490,7 @@ BwdLayout bwd_layout(const moe_config& c, const WsLayout& L) {
         return at;
     };
     const size_t rows = (size_t)L.rows;
-    const bool f32 = c.dtype == MOE_F32;  // fp32: no weight or segment transposes
+    const bool f32 = c.dtype == MOE_F32;  // fp32: no tensor maps, no slot-score partials
     const size_t es = f32 ? 4 : 2;         // bytes of a token-row element
     B.logits = take(sizeof(float) * (size_t)c.T * c.E);
     B.u = take(es * rows * c.d_ff);

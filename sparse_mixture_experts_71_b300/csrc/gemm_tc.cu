@@ -2045,7 +2045,7 @@ cudaError_t launch_grouped_gemm_tc(const moe_config& c, bool bf16_out, bool act,
 }
 
 // One grouped GEMM out[r][n] = sum_k A[r][k] W[e][k][n] over the expert
-// segments of A with the weight stored K-major-transposed, W [E][K][n_out]
+// segments of A with the weight stored K rows by n_out columns, W [E][K][n_out]
 // (the backward pass's dH = dY_perm W2 and dX_perm = dU W1 read W2 [E][d][d_ff]
 // and W1 [E][d_ff][d] as they are): the CTA-pair kernel with its weight
 // operand read MN-major.  bf16_out: bf16 out (no bias), times GELU'(gelu_u)

@@ -185,7 +185,8 @@ def test_backward_host_side():
                B.config(64, 64, 128, 4, 2, dtype="f32"),
                B.config(64, 64, 128, 4, 2, dtype="f32", routing="expert")):
         assert lib.moe_backward_workspace_size(ctypes.byref(ok)) >= B.workspace_size(ok)
-    # fp32 token rows take twice the bytes of bf16 ones; no weight transposes
+    # fp32 token rows take twice the bytes of bf16 ones (the bf16 layout adds
+    # only the tensor maps and the slot-score partials)
     f32 = B.config(64, 64, 128, 4, 2, dtype="f32")
     assert lib.moe_backward_workspace_size(ctypes.byref(f32)) - B.workspace_size(f32) < \
         n - B.workspace_size(c) + 3 * 128 * 128 * 2
