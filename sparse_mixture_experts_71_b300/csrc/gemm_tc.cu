@@ -208,7 +208,7 @@ __device__ __forceinline__ void drain_bar(uint64_t* bar, uint32_t parity) {
 // nor issues the global stores; a partial chunk (the end of an expert's
 // segment: the rows after it belong to the next segment) is stored by the
 // lanes.
-template <int COLS, bool GEMM1>
+template <int COLS, bool GEMM1, bool ZERO_TILES = false>
 __device__ __forceinline__ void epilogue_tile(const Params& p, int e, int r0, int o0, int n,
                                               int fbase,
                                               uint32_t tmem_base, int acc_col, int q, int part,
@@ -226,9 +226,20 @@ __device__ __forceinline__ void epilogue_tile(const Params& p, int e, int r0, in
     const int c_begin = part * (COLS / nparts), c_end = min(c_begin + COLS / nparts, n);
     for (int c = c_begin; c < c_end; c += 32) {
         float v[32];
-        tc::tmem_ld_32cols(tmem_base + ((uint32_t)(q * 32) << 16) +
-                               (uint32_t)(acc_col + c),
-                           v);
+        if constexpr (ZERO_TILES) {
+            if (zero) {  // no MMA wrote this accumulator: its contents are undefined
+#pragma unroll
+                for (int j = 0; j < 32; ++j) v[j] = 0.f;
+            } else {
+                tc::tmem_ld_32cols(tmem_base + ((uint32_t)(q * 32) << 16) +
+                                       (uint32_t)(acc_col + c),
+                                   v);
+            }
+        } else {
+            tc::tmem_ld_32cols(tmem_base + ((uint32_t)(q * 32) << 16) +
+                                   (uint32_t)(acc_col + c),
+                               v);
+        }
         const int rows_here = min(32, n - c);
         if (GEMM1) {
             __nv_bfloat16* s16 = reinterpret_cast<__nv_bfloat16*>(stg);
@@ -253,7 +264,7 @@ __device__ __forceinline__ void epilogue_tile(const Params& p, int e, int r0, in
         } else {
             float wl = 1.f;
             if (p.row_w != nullptr && lane < rows_here) wl = __ldg(p.row_w + r0 + c + lane);
-            if (zero) wl = 0.f;  // no MMA wrote this accumulator
+            if (zero) wl = 0.f;  // an empty segment's tile is zero whatever the bias
 #pragma unroll
             for (int j = 0; j < 32; ++j) v[j] = (v[j] + bias) * __shfl_sync(0xffffffffu, wl, j);
             if (tm_out != nullptr) {  // the previous chunk's store has read the staging rows
@@ -1371,9 +1382,10 @@ grouped_gemm_pair(const __grid_constant__ CUtensorMap tmA, const __grid_constant
                 epilogue_gelu<EW / 4>(p, tl.e, tl.r0, tl.n, m0 + rank * BM, tmem_base, acc * BN2,
                                       q, part, lane, stg, &tmO);
             else
-                epilogue_tile<BN2, GEMM1>(p, tl.e, tl.r0, tl.r0, tl.n, m0 + rank * BM, tmem_base,
-                                      acc * BN2, q, part, EW / 4, lane, stg, &tmO,
-                                      p.seg_maps != nullptr && seg_rows(p, tl.e) == 0);
+                epilogue_tile<BN2, GEMM1, kRed>(p, tl.e, tl.r0, tl.r0, tl.n, m0 + rank * BM,
+                                                tmem_base, acc * BN2, q, part, EW / 4, lane, stg,
+                                                &tmO,
+                                                p.seg_maps != nullptr && seg_rows(p, tl.e) == 0);
             tc::fence_before_sync();
             __syncwarp();
             if (lane == 0) tc::mbar_arrive_cluster_relaxed(tc::cluster_addr(&tempty[acc], 0));
