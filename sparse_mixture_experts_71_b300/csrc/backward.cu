@@ -327,6 +327,100 @@ __global__ void __launch_bounds__(256) dx_kernel(const float* __restrict__ dX_pe
     }
 }
 
+// dx for bf16 layers with many routed experts, where the dg W_r term (T x El
+// by El x d) dominates: that product on the tensor cores as tf32 mma.sync
+// m16n8k8 (dg and W_r rounded to tf32, fp32 accumulation; dx is rounded to
+// bf16 after), a block per 64 tokens x 128 columns, each of its 4 warps 16
+// tokens; W_r's 128 columns of every expert and the tokens' dg rows staged
+// in shared memory (rows padded so the fragment reads hit distinct banks);
+// then each lane adds its tokens' slots' dX_perm values and stores dx.
+// Fragments (PTX m16n8k8 .tf32): A a0 (g, q), a1 (g + 8, q), a2 (g, q + 4),
+// a3 (g + 8, q + 4); B b0 (k = q, n = g), b1 (q + 4, g); D (g, 2q), (g, 2q + 1),
+// (g + 8, 2q), (g + 8, 2q + 1), with g = lane / 4, q = lane % 4.
+constexpr int kDxTok = 64, kDxCols = 128, kDxMaxE = 64;
+constexpr int kDxWld = kDxCols + 8, kDxGld = kDxMaxE + 4;  // shared row lengths (floats)
+constexpr int kDxSmem = (kDxMaxE * kDxWld + kDxTok * kDxGld) * 4;
+
+__device__ __forceinline__ uint32_t to_tf32(float x) {
+    uint32_t r;
+    asm("cvt.rna.tf32.f32 %0, %1;" : "=r"(r) : "f"(x));
+    return r;
+}
+
+__global__ void __launch_bounds__(128) dx_tc_kernel(const float* __restrict__ dX_perm,
+                                                     const int32_t* __restrict__ slot_of,
+                                                     const float* __restrict__ dg,
+                                                     const float* __restrict__ W_r, int T, int K,
+                                                     int El, int d, int64_t rows_cap,
+                                                     bf16* __restrict__ dx) {
+    extern __shared__ __align__(16) float dx_smem[];
+    float* sW = dx_smem;                    // [kDxMaxE][kDxWld]
+    float* sG = dx_smem + kDxMaxE * kDxWld;  // [kDxTok][kDxGld]
+    pdl_wait();
+    pdl_trigger();
+    const int t0 = blockIdx.x * kDxTok, c0 = blockIdx.y * kDxCols;
+    const int Ep = (El + 7) & ~7;  // K rounded up to the MMA's 8 (zeros past El)
+    for (int i = threadIdx.x; i < Ep * (kDxCols / 4); i += blockDim.x) {
+        const int e = i / (kDxCols / 4), c4 = (i % (kDxCols / 4)) * 4;
+        float4 v = make_float4(0.f, 0.f, 0.f, 0.f);
+        if (e < El && c0 + c4 < d) v = __ldg(reinterpret_cast<const float4*>(W_r + (size_t)e * d + c0 + c4));
+        *reinterpret_cast<float4*>(sW + e * kDxWld + c4) = v;
+    }
+    for (int i = threadIdx.x; i < kDxTok * Ep; i += blockDim.x) {
+        const int r = i / Ep, e = i % Ep;
+        sG[r * kDxGld + e] = t0 + r < T && e < El ? __ldg(dg + (size_t)(t0 + r) * El + e) : 0.f;
+    }
+    __syncthreads();
+    const int warp = threadIdx.x / 32, lane = threadIdx.x % 32, g = lane >> 2, q = lane & 3;
+    const int m0 = warp * 16;
+    float acc[16][4];
+#pragma unroll
+    for (int nt = 0; nt < 16; ++nt)
+#pragma unroll
+        for (int i = 0; i < 4; ++i) acc[nt][i] = 0.f;
+    for (int k0 = 0; k0 < Ep; k0 += 8) {
+        const uint32_t a0 = to_tf32(sG[(m0 + g) * kDxGld + k0 + q]);
+        const uint32_t a1 = to_tf32(sG[(m0 + g + 8) * kDxGld + k0 + q]);
+        const uint32_t a2 = to_tf32(sG[(m0 + g) * kDxGld + k0 + q + 4]);
+        const uint32_t a3 = to_tf32(sG[(m0 + g + 8) * kDxGld + k0 + q + 4]);
+#pragma unroll
+        for (int nt = 0; nt < 16; ++nt) {
+            const uint32_t b0 = to_tf32(sW[(k0 + q) * kDxWld + nt * 8 + g]);
+            const uint32_t b1 = to_tf32(sW[(k0 + q + 4) * kDxWld + nt * 8 + g]);
+            asm volatile(
+                "mma.sync.aligned.m16n8k8.row.col.f32.tf32.tf32.f32 {%0, %1, %2, %3}, "
+                "{%4, %5, %6, %7}, {%8, %9}, {%0, %1, %2, %3};"
+                : "+f"(acc[nt][0]), "+f"(acc[nt][1]), "+f"(acc[nt][2]), "+f"(acc[nt][3])
+                : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+        }
+    }
+#pragma unroll
+    for (int h = 0; h < 2; ++h) {  // token rows g and g + 8 of the warp's 16
+        const int t = t0 + m0 + g + 8 * h;
+        if (t >= T) continue;
+        float2 v[16];
+#pragma unroll
+        for (int nt = 0; nt < 16; ++nt) v[nt] = make_float2(acc[nt][2 * h], acc[nt][2 * h + 1]);
+        for (int j = 0; j < K; ++j) {
+            const int sl = __ldg(slot_of + (size_t)t * K + j);
+            if (sl < 0 || sl >= rows_cap) continue;
+            const float* row = dX_perm + (size_t)sl * d + c0 + 2 * q;
+#pragma unroll
+            for (int nt = 0; nt < 16; ++nt)
+                if (c0 + nt * 8 + 2 * q < d) {
+                    const float2 r2 = __ldg(reinterpret_cast<const float2*>(row + nt * 8));
+                    v[nt].x += r2.x;
+                    v[nt].y += r2.y;
+                }
+        }
+        bf16* out = dx + (size_t)t * d + c0 + 2 * q;
+#pragma unroll
+        for (int nt = 0; nt < 16; ++nt)
+            if (c0 + nt * 8 + 2 * q < d)
+                *reinterpret_cast<__nv_bfloat162*>(out + nt * 8) = __floats2bfloat162_rn(v[nt].x, v[nt].y);
+    }
+}
+
 // Partial router-weight gradients: part[z][e][j] = sum over the tokens t of
 // row slice z of dg[t][e] x[t][j].  A thread per column j (256 a block),
 // EG experts per pass with their accumulators in registers, 64-token chunks
@@ -726,7 +820,14 @@ moe_status moe_backward(const moe_config* cfg, const void* x, const float* W_r,
     if (e == cudaSuccess)
         e = launch_grouped_gemm_mn(cg, false, dH, rows, offsets, W1, nullptr, nullptr, y_perm, rows,
                                    d, F, hdr, s);
-    if (e == cudaSuccess) {
+    if (e == cudaSuccess && El >= 16 && El <= kDxMaxE) {  // the dg W_r term dominates
+        e = ensure_smem<dx_tc_kernel>(kDxSmem);
+        if (e == cudaSuccess)
+            e = launch_kernel(dx_tc_kernel, dim3((T + kDxTok - 1) / kDxTok, (d + kDxCols - 1) / kDxCols),
+                              dim3(128), kDxSmem, s, 1, false, (const float*)y_perm,
+                              (const int32_t*)slot_of, (const float*)dg, W_r, T, K, El, d, rows,
+                              reinterpret_cast<bf16*>(dx));
+    } else if (e == cudaSuccess) {
         const long long tasks = (long long)T * ((d / 4 + 127) / 128);
         e = launch_kernel(dx_kernel<bf16>, dim3(grid_for(tasks, 8)), dim3(256), 0, s, 1, false,
                           (const float*)y_perm, (const int32_t*)slot_of, (const float*)dg, W_r, T,

@@ -35,6 +35,9 @@ CASES = [
     ("bwd-2d-boxes", 700, 136, 200, 6, 2, None, True, 0.5, 0.1, 0.0),
     # rows narrower than one 64-column box
     ("bwd-tiny-dims", 65, 24, 40, 5, 2, None, True, 0.0, 0.0, 0.0),
+    # 20 routed experts (the dx product's tensor-core form, its K padded to
+    # 24) and d not a multiple of its 128-column tiles
+    ("bwd-e20", 700, 200, 256, 20, 2, None, True, 0.5, 0.1, 0.1),
     # mid size: ~1024 rows per expert, so the weight-gradient GEMMs' segment
     # reduction walks 8 K tiles of 128 per expert, on both GEMM kernels' wide path
     ("bwd-mid", 4096, 512, 2048, 8, 2, None, True, 0.0, 0.01, 0.001),
