@@ -465,6 +465,79 @@ __global__ void __launch_bounds__(256) wr_grad_kernel(const float* __restrict__ 
     }
 }
 
+// Partial router-weight gradients for bf16 layers with 16-64 routed experts
+// on the tensor cores: part[z][e][j] = sum over the tokens t of slice z
+// (kWrSlice tokens) of dg[t][e] x[t][j] as tf32 mma.sync m16n8k8 (M = the
+// experts, 16 a warp; N = 128 columns a block; K = the slice's tokens in
+// chunks of 32 staged in shared memory; dg rounded to tf32, x exact, fp32
+// accumulation).  sum_parts_kernel then adds the slices in order.
+constexpr int kWrCols = 128, kWrChunk = 32, kWrSlice = 1024;
+constexpr int kWrGld = kDxMaxE + 8, kWrXld = kWrCols + 8;  // shared row lengths (floats)
+
+__global__ void __launch_bounds__(128) wr_tc_kernel(const float* __restrict__ dg,
+                                                     const bf16* __restrict__ x, int T, int El,
+                                                     int d, float* __restrict__ part) {
+    __shared__ __align__(16) float sG[kWrChunk][kWrGld];
+    __shared__ __align__(16) float sX[kWrChunk][kWrXld];
+    pdl_wait();
+    pdl_trigger();
+    const int z = blockIdx.x, c0 = blockIdx.y * kWrCols;
+    const int tb = z * kWrSlice, te = min(T, tb + kWrSlice);
+    const int warp = threadIdx.x / 32, lane = threadIdx.x % 32, g = lane >> 2, q = lane & 3;
+    const int m0 = warp * 16;  // this warp's 16 experts
+    float acc[16][4];
+#pragma unroll
+    for (int nt = 0; nt < 16; ++nt)
+#pragma unroll
+        for (int i = 0; i < 4; ++i) acc[nt][i] = 0.f;
+    for (int tc = tb; tc < te; tc += kWrChunk) {
+        __syncthreads();  // the previous chunk's fragments are read
+        for (int i = threadIdx.x; i < kWrChunk * kDxMaxE; i += blockDim.x) {
+            const int r = i / kDxMaxE, e = i % kDxMaxE;
+            sG[r][e] = tc + r < te && e < El ? __ldg(dg + (size_t)(tc + r) * El + e) : 0.f;
+        }
+        for (int i = threadIdx.x; i < kWrChunk * (kWrCols / 8); i += blockDim.x) {
+            const int r = i / (kWrCols / 8), c8 = (i % (kWrCols / 8)) * 8;
+            float f[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+            if (tc + r < te && c0 + c8 < d) load8(x + (size_t)(tc + r) * d + c0 + c8, f);
+#pragma unroll
+            for (int u = 0; u < 8; ++u) sX[r][c8 + u] = f[u];
+        }
+        __syncthreads();
+        if (m0 < El) {
+#pragma unroll
+            for (int k0 = 0; k0 < kWrChunk; k0 += 8) {
+                const uint32_t a0 = to_tf32(sG[k0 + q][m0 + g]);
+                const uint32_t a1 = to_tf32(sG[k0 + q][m0 + g + 8]);
+                const uint32_t a2 = to_tf32(sG[k0 + q + 4][m0 + g]);
+                const uint32_t a3 = to_tf32(sG[k0 + q + 4][m0 + g + 8]);
+#pragma unroll
+                for (int nt = 0; nt < 16; ++nt) {
+                    const uint32_t b0 = __float_as_uint(sX[k0 + q][nt * 8 + g]);  // bf16: exact in tf32
+                    const uint32_t b1 = __float_as_uint(sX[k0 + q + 4][nt * 8 + g]);
+                    asm volatile(
+                        "mma.sync.aligned.m16n8k8.row.col.f32.tf32.tf32.f32 {%0, %1, %2, %3}, "
+                        "{%4, %5, %6, %7}, {%8, %9}, {%0, %1, %2, %3};"
+                        : "+f"(acc[nt][0]), "+f"(acc[nt][1]), "+f"(acc[nt][2]), "+f"(acc[nt][3])
+                        : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+                }
+            }
+        }
+    }
+    if (m0 >= El) return;
+#pragma unroll
+    for (int h = 0; h < 2; ++h) {
+        const int e = m0 + g + 8 * h;
+        if (e >= El) continue;
+        float* out = part + ((size_t)z * El + e) * d + c0 + 2 * q;
+#pragma unroll
+        for (int nt = 0; nt < 16; ++nt)
+            if (c0 + nt * 8 + 2 * q < d)
+                *reinterpret_cast<float2*>(out + nt * 8) =
+                    make_float2(acc[nt][2 * h], acc[nt][2 * h + 1]);
+    }
+}
+
 // out[e][m] = sum over the rows of segment e of A[r][m].  A cluster of
 // kColSlices CTAs per (256 columns, expert): CTA z, warp w sums the rows
 // i = 8z + w (mod 64) of the segment, eight columns a lane (16- or 32-byte
@@ -840,14 +913,20 @@ moe_status moe_backward(const moe_config* cfg, const void* x, const float* W_r,
     if (e == cudaSuccess)
         e = launch_colsum((const bf16*)dH, (const int32_t*)offsets, rows, E, F, db1, s);
     // ---- dW_r = dg^T x: row-slice partials, then their sum
-    if (e == cudaSuccess)
+    const bool wr_tc = El >= 16 && El <= kDxMaxE;
+    const int wr_slices = wr_tc ? (T + kWrSlice - 1) / kWrSlice : Bw.wr_slices;
+    if (e == cudaSuccess && wr_tc)
+        e = launch_kernel(wr_tc_kernel, dim3(wr_slices, (d + kWrCols - 1) / kWrCols), dim3(128), 0,
+                          s, 1, false, (const float*)dg, reinterpret_cast<const bf16*>(x), T, El,
+                          d, at<float>(ws, Bw.parts));
+    else if (e == cudaSuccess)
         e = launch_kernel(El <= 8 ? wr_grad_kernel<8, bf16> : wr_grad_kernel<32, bf16>,
                           dim3((d + 255) / 256, Bw.wr_slices), dim3(256), 0, s, 1, false,
                           (const float*)dg, reinterpret_cast<const bf16*>(x), T, El, d,
                           wr_slice_rows(T), at<float>(ws, Bw.parts));
     if (e == cudaSuccess)
         e = launch_kernel(sum_parts_kernel, dim3(grid_for((int64_t)El * d, 256)), dim3(256), 0, s,
-                          1, false, (const float*)at<float>(ws, Bw.parts), Bw.wr_slices,
+                          1, false, (const float*)at<float>(ws, Bw.parts), wr_slices,
                           (int64_t)El * d, dW_r);
     return e == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;
 }
