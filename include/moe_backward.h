@@ -39,7 +39,8 @@
  *
  * Supported: every configuration moe_forward accepts.  bf16 layers keep the
  * pre-activations, activations and scaled upstream rows in bf16 and run the
- * products on the tcgen05 tensor cores; fp32 layers keep them in fp32 and
+ * products on the tcgen05 tensor cores (the router terms dg W_r and dg^T x,
+ * with 16-64 routed experts, as tf32 mma.sync); fp32 layers keep them in fp32 and
  * run every product with fp32 FMA on the CUDA cores (GELU' from erff).
  *
  * Arguments (device pointers, caller-owned, layouts as in moe.h):

@@ -19,13 +19,15 @@
 //   router      one warp per token: the slot scores, the logit gradient dg
 //               (softmax / renormalisation, auxiliary loss, z-loss)
 //   dx path     dX_perm = dU W1_e (W1 MN-major); dx = sum over the token's
-//               slots of dX_perm + dg W_r
+//               slots of dX_perm + dg W_r (with 16-64 routed experts that
+//               product as tf32 mma.sync tiles)
 //   weights     dW2_e = dY_perm_e^T H_e and dW1_e = dU_e^T X_perm_e on the
 //               same kernel in its segment-reduction mode (K = the segment's
 //               rows; both operands read MN-major from the row-major
 //               permuted rows through per-segment tensor maps, so a segment's
-//               last K stage reads zeros past its end), dW_r = dg^T x on CUDA
-//               cores (row-slice partials summed in a fixed order), db2, db1
+//               last K stage reads zeros past its end), dW_r = dg^T x
+//               (row-slice partials summed in a fixed order; CUDA cores, or
+//               tf32 mma.sync tiles with 16-64 routed experts), db2, db1
 //               = column sums over each expert's rows.  GELU and GELU' use
 //               the forward epilogue's Abramowitz & Stegun 7.1.26 erf.
 // fp32 layers run the same steps on CUDA-core kernels (backward_f32.cu),
